@@ -1,0 +1,311 @@
+/*
+ * lapl_oracle.c -- plain fp64 CPU oracle for Laplacian-kernel Nystrom attention.
+ *
+ * TEST INFRASTRUCTURE ONLY (see lapl_oracle.h).  Slow on purpose: plain loops in the order of
+ * the method's steps, no blocking, fusion or reordering, so that each step can be checked
+ * against its description by eye.  Build with -ffp-contract=off so that x86 and Arm hosts
+ * round identically.
+ *
+ * Source of each step: "LaplacianFormer: Rethinking Linear Attention with Laplacian Kernel",
+ * the explainer pages (English, German, Chinese, Korean and Japanese editions).  Where the
+ * pages leave a detail open, the reading used is stated beside the code.
+ */
+#include "lapl_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---- step 1: landmarks ---------------------------------------------------------------
+ * English page, 2.C.1 (Nystrom Approximation): landmark keys are selected by average pooling.
+ * Reading: 2-D average pooling over the grid_h x grid_w token grid with non-overlapping
+ * windows of (grid_h/s) x (grid_w/s) tokens, s = sqrt(m); landmark j = jr*s + jc covers token
+ * rows jr*ph .. jr*ph+ph-1 and columns jc*pw .. jc*pw+pw-1; token n = r*grid_w + c.
+ * The window is summed in index order (rows, then columns) and divided by ph*pw.
+ */
+static void landmarks_avgpool(const double* K, int grid_w, int d, int s, int ph, int pw,
+                              double* L) {
+  for (int jr = 0; jr < s; ++jr) {
+    for (int jc = 0; jc < s; ++jc) {
+      const int j = jr * s + jc;
+      for (int c = 0; c < d; ++c) {
+        double sum = 0.0;
+        for (int r = jr * ph; r < (jr + 1) * ph; ++r)
+          for (int cc = jc * pw; cc < (jc + 1) * pw; ++cc)
+            sum += K[(size_t)(r * grid_w + cc) * d + c];
+        L[(size_t)j * d + c] = sum / (double)(ph * pw);
+      }
+    }
+  }
+}
+
+/* ---- step 2: Laplacian kernel ---------------------------------------------------------
+ * English page, 2.A; German page, 2 (Laplacian-Kernel als Ahnlichkeitsmass):
+ * k(x,y) = exp(-||x - y||_1 / lambda), with the L1 (Manhattan) distance summed over the
+ * d channels in ascending order.
+ */
+static double l1_distance(const double* x, const double* y, int d) {
+  double sum = 0.0;
+  for (int c = 0; c < d; ++c) sum += fabs(x[c] - y[c]);
+  return sum;
+}
+
+static double laplacian_of_distance(double dist, double lambda) { return exp(-dist / lambda); }
+
+/* ---- step 3: Newton-Schulz inverse of W ---------------------------------------------
+ * English page, 2.C.2; German page, 2 (Newton-Schulz Iteration fur Inversion); Korean page,
+ * 2.3: the landmark kernel matrix is inverted with the multiply-only Newton-Schulz iteration
+ * X <- X (2I - W X); a small eps*I keeps W strictly positive definite.
+ * Reading: X0 = W^T / (|W|_1 |W|_inf) with |W|_1 the largest absolute column sum and
+ * |W|_inf the largest absolute row sum, both of W after eps*I is added; exactly T steps,
+ * no early exit; T = 0 returns X0.  Each step forms P = W X, then Z = 2I - P, then X Z.
+ */
+static double frob_residual(const double* W, const double* X, int m) {
+  double acc = 0.0;
+  for (int i = 0; i < m; ++i)
+    for (int j = 0; j < m; ++j) {
+      double wx = 0.0;
+      for (int k = 0; k < m; ++k) wx += W[(size_t)i * m + k] * X[(size_t)k * m + j];
+      const double r = (i == j ? 1.0 : 0.0) - wx;
+      acc += r * r;
+    }
+  return sqrt(acc);
+}
+
+static int newton_schulz(const double* W, int m, int T, double* X, double* resid) {
+  double n1 = 0.0, ninf = 0.0;
+  for (int j = 0; j < m; ++j) { /* |W|_1: largest absolute column sum */
+    double s = 0.0;
+    for (int i = 0; i < m; ++i) s += fabs(W[(size_t)i * m + j]);
+    if (s > n1) n1 = s;
+  }
+  for (int i = 0; i < m; ++i) { /* |W|_inf: largest absolute row sum */
+    double s = 0.0;
+    for (int j = 0; j < m; ++j) s += fabs(W[(size_t)i * m + j]);
+    if (s > ninf) ninf = s;
+  }
+  const double scale = n1 * ninf;
+  for (int i = 0; i < m; ++i)
+    for (int j = 0; j < m; ++j) X[(size_t)i * m + j] = W[(size_t)j * m + i] / scale;
+  if (resid) resid[0] = frob_residual(W, X, m);
+
+  double* P = (double*)malloc(sizeof(double) * (size_t)m * m);
+  double* Z = (double*)malloc(sizeof(double) * (size_t)m * m);
+  double* Xn = (double*)malloc(sizeof(double) * (size_t)m * m);
+  if (!P || !Z || !Xn) {
+    free(P); free(Z); free(Xn);
+    return ORC_ERR_NOMEM;
+  }
+  for (int t = 1; t <= T; ++t) {
+    for (int i = 0; i < m; ++i) /* P = W X */
+      for (int j = 0; j < m; ++j) {
+        double s = 0.0;
+        for (int k = 0; k < m; ++k) s += W[(size_t)i * m + k] * X[(size_t)k * m + j];
+        P[(size_t)i * m + j] = s;
+      }
+    for (int i = 0; i < m; ++i) /* Z = 2I - P */
+      for (int j = 0; j < m; ++j)
+        Z[(size_t)i * m + j] = (i == j ? 2.0 : 0.0) - P[(size_t)i * m + j];
+    for (int i = 0; i < m; ++i) /* X <- X Z */
+      for (int j = 0; j < m; ++j) {
+        double s = 0.0;
+        for (int k = 0; k < m; ++k) s += X[(size_t)i * m + k] * Z[(size_t)k * m + j];
+        Xn[(size_t)i * m + j] = s;
+      }
+    memcpy(X, Xn, sizeof(double) * (size_t)m * m);
+    if (resid) resid[t] = frob_residual(W, X, m);
+  }
+  free(P); free(Z); free(Xn);
+  return ORC_OK;
+}
+
+/* ---- step 4: whitening (injective feature map) ----------------------------------------
+ * Korean page, 2.2: z_i = Sigma^{-1/2} (k(q_i, .) - mean) + bias, with Sigma replaced by a
+ * diagonal estimator of the empirical variance (English page, 2.B; Japanese page, 2.2).
+ * Reading: the similarity vector of query i is row i of A (over the m landmarks); mean and
+ * variance are taken per landmark column over the N tokens of the (b,h) slice; the variance
+ * divides by N; delta sits inside the square root; bias has shape [H,m] (zeros when absent).
+ * Mean and variance are computed in two passes.
+ */
+static void whiten_columns(const double* A, int N, int m, double delta, const double* beta,
+                           double* mu, double* var, double* Ahat) {
+  for (int j = 0; j < m; ++j) {
+    double s = 0.0;
+    for (int i = 0; i < N; ++i) s += A[(size_t)i * m + j];
+    const double mean = s / (double)N;
+    double ss = 0.0;
+    for (int i = 0; i < N; ++i) {
+      const double dv = A[(size_t)i * m + j] - mean;
+      ss += dv * dv;
+    }
+    const double variance = ss / (double)N;
+    const double scale = 1.0 / sqrt(variance + delta);
+    const double b = beta ? beta[j] : 0.0;
+    for (int i = 0; i < N; ++i) Ahat[(size_t)i * m + j] = (A[(size_t)i * m + j] - mean) * scale + b;
+    mu[j] = mean;
+    var[j] = variance;
+  }
+}
+
+/* ---- step 5: output chain --------------------------------------------------------------
+ * Chinese page, 2.2: the N x N kernel matrix is approximated in low-rank form from the
+ * landmark blocks without forming it explicitly.  Reading: O = A_hat (X (B V)), evaluated
+ * right to left: BV = B V (m x d), M = X BV (m x d), O = A_hat M (N x d).
+ */
+static void matmul(const double* Aop, const double* Bop, int rows, int inner, int cols,
+                   double* C) {
+  for (int i = 0; i < rows; ++i)
+    for (int j = 0; j < cols; ++j) {
+      double s = 0.0;
+      for (int k = 0; k < inner; ++k) s += Aop[(size_t)i * inner + k] * Bop[(size_t)k * cols + j];
+      C[(size_t)i * cols + j] = s;
+    }
+}
+
+static int isqrt_exact(int m) {
+  for (int s = 1; s * s <= m; ++s)
+    if (s * s == m) return s;
+  return -1;
+}
+
+static int check_config(const orc_config* c) {
+  if (!c) return ORC_ERR_ARG;
+  if (c->batch < 0 || c->heads < 1 || c->grid_h < 1 || c->grid_w < 1 || c->head_dim < 1 ||
+      c->num_landmarks < 1 || c->ns_steps < 0)
+    return ORC_ERR_ARG;
+  if (!(c->lambda > 0.0) || !(c->eps >= 0.0)) return ORC_ERR_ARG;
+  if (c->whiten && !(c->delta > 0.0)) return ORC_ERR_ARG;
+  const int s = isqrt_exact(c->num_landmarks);
+  if (s < 0 || c->grid_h % s != 0 || c->grid_w % s != 0) return ORC_ERR_UNSUPPORTED;
+  return ORC_OK;
+}
+
+/* One (b,h) slice.  Offsets into the intermediates are taken by the caller. */
+static int forward_slice(const orc_config* cfg, int h, const double* Q, const double* K,
+                         const double* V, const double* bias, double* O,
+                         const orc_intermediates* im, long slice) {
+  const int N = cfg->grid_h * cfg->grid_w, d = cfg->head_dim, m = cfg->num_landmarks;
+  const int s = isqrt_exact(m), ph = cfg->grid_h / s, pw = cfg->grid_w / s;
+  const int T = cfg->ns_steps;
+  const size_t nm = (size_t)N * m, mm = (size_t)m * m, md = (size_t)m * d;
+
+  double* L = (double*)malloc(sizeof(double) * md);
+  double* Dql = (double*)malloc(sizeof(double) * nm);
+  double* Dll = (double*)malloc(sizeof(double) * mm);
+  double* Dlk = (double*)malloc(sizeof(double) * nm);
+  double* A = (double*)malloc(sizeof(double) * nm);
+  double* Bm = (double*)malloc(sizeof(double) * nm);
+  double* W = (double*)malloc(sizeof(double) * mm);
+  double* X = (double*)malloc(sizeof(double) * mm);
+  double* mu = (double*)malloc(sizeof(double) * m);
+  double* var = (double*)malloc(sizeof(double) * m);
+  double* Ahat = (double*)malloc(sizeof(double) * nm);
+  double* BV = (double*)malloc(sizeof(double) * md);
+  double* M = (double*)malloc(sizeof(double) * md);
+  double* resid = (double*)malloc(sizeof(double) * (size_t)(T + 1));
+  int rc = ORC_OK;
+  if (!L || !Dql || !Dll || !Dlk || !A || !Bm || !W || !X || !mu || !var || !Ahat || !BV || !M ||
+      !resid) {
+    rc = ORC_ERR_NOMEM;
+    goto done;
+  }
+
+  /* 1. landmarks */
+  landmarks_avgpool(K, cfg->grid_w, d, s, ph, pw, L);
+
+  /* 2. kernel blocks: A = k(Q,L) [N,m], B = k(L,K) [m,N], W = k(L,L) + eps I [m,m] */
+  for (int i = 0; i < N; ++i)
+    for (int j = 0; j < m; ++j) {
+      Dql[(size_t)i * m + j] = l1_distance(Q + (size_t)i * d, L + (size_t)j * d, d);
+      A[(size_t)i * m + j] = laplacian_of_distance(Dql[(size_t)i * m + j], cfg->lambda);
+    }
+  for (int j = 0; j < m; ++j)
+    for (int n = 0; n < N; ++n) {
+      Dlk[(size_t)j * N + n] = l1_distance(L + (size_t)j * d, K + (size_t)n * d, d);
+      Bm[(size_t)j * N + n] = laplacian_of_distance(Dlk[(size_t)j * N + n], cfg->lambda);
+    }
+  for (int j = 0; j < m; ++j)
+    for (int k = 0; k < m; ++k) {
+      Dll[(size_t)j * m + k] = l1_distance(L + (size_t)j * d, L + (size_t)k * d, d);
+      W[(size_t)j * m + k] = laplacian_of_distance(Dll[(size_t)j * m + k], cfg->lambda) +
+                             (j == k ? cfg->eps : 0.0);
+    }
+
+  /* 3. Newton-Schulz */
+  rc = newton_schulz(W, m, T, X, resid);
+  if (rc != ORC_OK) goto done;
+
+  /* 4. whitening */
+  if (cfg->whiten) {
+    whiten_columns(A, N, m, cfg->delta, bias ? bias + (size_t)h * m : NULL, mu, var, Ahat);
+  } else {
+    memcpy(Ahat, A, sizeof(double) * nm);
+    for (int j = 0; j < m; ++j) { /* statistics are still reported when whitening is off */
+      double sacc = 0.0;
+      for (int i = 0; i < N; ++i) sacc += A[(size_t)i * m + j];
+      mu[j] = sacc / (double)N;
+      double ss = 0.0;
+      for (int i = 0; i < N; ++i) {
+        const double dv = A[(size_t)i * m + j] - mu[j];
+        ss += dv * dv;
+      }
+      var[j] = ss / (double)N;
+    }
+  }
+
+  /* 5. output chain, right to left */
+  matmul(Bm, V, m, N, d, BV);
+  matmul(X, BV, m, m, d, M);
+  matmul(Ahat, M, N, m, d, O);
+
+  if (im) {
+#define COPY_OUT(field, src, count) \
+  if (im->field) memcpy(im->field + (size_t)slice * (count), src, sizeof(double) * (count))
+    COPY_OUT(landmarks, L, md);
+    COPY_OUT(d_ql, Dql, nm);
+    COPY_OUT(d_ll, Dll, mm);
+    COPY_OUT(d_lk, Dlk, nm);
+    COPY_OUT(a, A, nm);
+    COPY_OUT(b, Bm, nm);
+    COPY_OUT(w, W, mm);
+    COPY_OUT(x, X, mm);
+    COPY_OUT(mu, mu, (size_t)m);
+    COPY_OUT(var, var, (size_t)m);
+    COPY_OUT(a_hat, Ahat, nm);
+    COPY_OUT(bv, BV, md);
+    COPY_OUT(m_mat, M, md);
+    COPY_OUT(ns_resid, resid, (size_t)(T + 1));
+#undef COPY_OUT
+  }
+
+done:
+  free(L); free(Dql); free(Dll); free(Dlk); free(A); free(Bm); free(W); free(X);
+  free(mu); free(var); free(Ahat); free(BV); free(M); free(resid);
+  return rc;
+}
+
+int orc_forward_slices(const orc_config* cfg, const double* q, const double* k, const double* v,
+                       const double* bias, double* out, const orc_intermediates* im,
+                       long slice_begin, long slice_count) {
+  const int rc = check_config(cfg);
+  if (rc != ORC_OK) return rc;
+  const long slices = (long)cfg->batch * cfg->heads;
+  if (slice_begin < 0 || slice_count < 0 || slice_begin + slice_count > slices) return ORC_ERR_ARG;
+  if (slice_count == 0) return ORC_OK;
+  if (!q || !k || !v || !out) return ORC_ERR_ARG;
+  const size_t nd = (size_t)cfg->grid_h * cfg->grid_w * cfg->head_dim;
+  for (long sl = slice_begin; sl < slice_begin + slice_count; ++sl) {
+    const int h = (int)(sl % cfg->heads);
+    const int r = forward_slice(cfg, h, q + (size_t)sl * nd, k + (size_t)sl * nd,
+                                v + (size_t)sl * nd, bias, out + (size_t)sl * nd, im, sl);
+    if (r != ORC_OK) return r;
+  }
+  return ORC_OK;
+}
+
+int orc_forward(const orc_config* cfg, const double* q, const double* k, const double* v,
+                const double* bias, double* out, const orc_intermediates* im) {
+  const int rc = check_config(cfg);
+  if (rc != ORC_OK) return rc;
+  return orc_forward_slices(cfg, q, k, v, bias, out, im, 0, (long)cfg->batch * cfg->heads);
+}

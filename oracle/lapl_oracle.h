@@ -1,0 +1,82 @@
+/*
+ * lapl_oracle.h -- plain fp64 CPU oracle for Laplacian-kernel Nystrom attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is the independent CPU reference that the CUDA library is
+ * checked against.  Only the test suite, the smoke check and the benchmark's CPU-baseline leg
+ * load it.  It shares no code, header, table or constant with the CUDA library: nothing under
+ * laplacian_nystr_attention_gb300/ includes this file and nothing here includes theirs.
+ *
+ * What it computes (per batch b and head h, all in double precision), following
+ * "LaplacianFormer: Rethinking Linear Attention with Laplacian Kernel" (explainer pages):
+ *   1. landmarks L = 2-D average pooling of K over the token grid        (English page, 2.C.1)
+ *   2. A = k(Q,L), B = k(L,K), W = k(L,L) + eps*I with
+ *      k(x,y) = exp(-||x-y||_1 / lambda)                                  (English page, 2.A;
+ *                                                                          small eps*I: 2.C.2)
+ *   3. X = T Newton-Schulz steps X <- X(2I - W X) from X0 = W^T/(|W|_1 |W|_inf)
+ *                                                                         (English page, 2.C.2)
+ *   4. whitening of A column by column with a diagonal estimator:
+ *      A_hat = (A - mean) / sqrt(var + delta) + bias                      (Korean page, 2.2)
+ *   5. O = A_hat * (X * (B * V)): the N x N matrix is never formed        (Chinese page, 2.2)
+ */
+#ifndef LAPL_ORACLE_H
+#define LAPL_ORACLE_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+  int batch, heads;        /* B, H: independent (b,h) slices */
+  int grid_h, grid_w;      /* token grid; N = grid_h * grid_w, token n = r * grid_w + c */
+  int head_dim;            /* d */
+  int num_landmarks;       /* m = s*s; grid_h % s == 0 and grid_w % s == 0 */
+  double lambda;           /* kernel scale, > 0 */
+  double eps;              /* diagonal perturbation of W, >= 0 */
+  double delta;            /* whitening variance floor, > 0 when whiten != 0 */
+  int ns_steps;            /* T >= 0 Newton-Schulz steps, no early exit */
+  int whiten;              /* 1: whiten A; 0: A_hat = A (bias ignored) */
+} orc_config;
+
+/* Every pointer may be NULL.  Shapes are for the whole [B,H] batch, C order. */
+typedef struct {
+  double* landmarks; /* [B,H,m,d]   L                              */
+  double* d_ql;      /* [B,H,N,m]   sum_c |Q_ic - L_jc|             */
+  double* d_ll;      /* [B,H,m,m]   sum_c |L_jc - L_kc|             */
+  double* d_lk;      /* [B,H,m,N]   sum_c |L_jc - K_nc|             */
+  double* a;         /* [B,H,N,m]   exp(-D_QL / lambda)             */
+  double* b;         /* [B,H,m,N]   exp(-D_LK / lambda)             */
+  double* w;         /* [B,H,m,m]   exp(-D_LL / lambda) + eps I     */
+  double* x;         /* [B,H,m,m]   X_T                             */
+  double* mu;        /* [B,H,m]     column means of A               */
+  double* var;       /* [B,H,m]     column variances of A (divide by N) */
+  double* a_hat;     /* [B,H,N,m]   whitened A                      */
+  double* bv;        /* [B,H,m,d]   B V                             */
+  double* m_mat;     /* [B,H,m,d]   X (B V)                         */
+  double* ns_resid;  /* [B,H,T+1]   Frobenius norm of I - W X_t, t = 0..T */
+} orc_intermediates;
+
+/* Status codes. */
+enum { ORC_OK = 0, ORC_ERR_ARG = 1, ORC_ERR_UNSUPPORTED = 2, ORC_ERR_NOMEM = 3 };
+
+/*
+ * Full forward over every (b,h) slice.
+ * q, k, v, out: [B,H,N,d]; bias: [H,m] or NULL (zeros).
+ */
+int orc_forward(const orc_config* cfg, const double* q, const double* k, const double* v,
+                const double* bias, double* out, const orc_intermediates* im);
+
+/*
+ * Same, restricted to the slices s = b*H + h with slice_begin <= s < slice_begin + slice_count.
+ * Arrays are still the full [B,H,...] arrays; only those slices are read or written.
+ */
+int orc_forward_slices(const orc_config* cfg, const double* q, const double* k, const double* v,
+                       const double* bias, double* out, const orc_intermediates* im,
+                       long slice_begin, long slice_count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAPL_ORACLE_H */
