@@ -1,0 +1,364 @@
+#!/usr/bin/env python
+"""Benchmark of the Laplacian-Nystrom attention forward on GB300.
+
+One step = one full forward (pooling, Newton-Schulz, fused L1-distance + exp for the query and
+key blocks, whitening statistics, B V, X (B V), output) over one batch of the synthetic
+workload, inputs resident in HBM.  Default workload: the stage-1 vision shape (B=8, H=2,
+56x56 tokens, d=32, m=49, T=20, fp32, heavy-tailed Q/K), the shape the L1-distance roofline is
+quoted on.
+
+Prints one JSON line (rank 0).  Multi-GPU (torchrun): every rank runs its own copy of the
+workload (independent (batch, head) slices, no data-path collective): weak scaling.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from lapl_workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "Laplacian-Nyström attn fwd tokens/s on 1 GB300; L1-cdist % of FP32 ALU peak"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+FLUSH_BYTES = 512 * 1024 * 1024
+
+# DRAM traffic (read + write bytes) of one launch of the distance kernel, from an ncu capture
+# (summary: profiles/cdist_exp_kernel_stage1_f32.md).  Valid only for the source it was taken
+# on: the sha256 of csrc/cdist.cu is compared and the figure reported as null on mismatch.
+CDIST_TRAFFIC = {"stage1_f32": None}
+CDIST_TRAFFIC_SHA = None
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="stage1_f32", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="budget of the oracle CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_desc(w) -> dict:
+    return {
+        "workload": (f"{w.name}: B={w.batch} H={w.heads} grid {w.grid_h}x{w.grid_w} "
+                     f"(N={w.n}) d={w.head_dim} m={w.num_landmarks} T={w.ns_steps} "
+                     f"lambda={w.lam:g} eps={w.eps:g} delta={w.delta:g} {w.dtype} {w.dist}"),
+        "batch": w.batch, "heads": w.heads, "seq_len": w.n, "head_dim": w.head_dim,
+        "landmarks": w.num_landmarks, "ns_steps": w.ns_steps,
+    }
+
+
+def cdist_ops_per_launch(w) -> float:
+    """Algorithmic FP32 operations of the distance kernel: 3 (subtract, absolute value, add)
+    per (token, landmark, channel) element, for the query block and the key block."""
+    return 3.0 * 2.0 * w.batch * w.heads * w.n * w.num_landmarks * w.head_dim
+
+
+def fp32_peak_tflops(num_sms: int, sm_mhz: float) -> float:
+    """FP32 CUDA-core peak: SMs x 128 FP32 lanes x 2 (an FMA counts 2) x SM clock."""
+    return num_sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling in the background during a timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.2)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "samples": len(rows),
+                "reasons": reasons}
+
+
+def cpu_baseline(w, q, k, v, budget_s: float) -> dict:
+    """The fp64 oracle on a bounded sample: whole (b,h) slices until the budget is spent."""
+    import oracle
+    oracle.build()
+    cfg = w.config()
+    slices = w.batch * w.heads
+    done, t0 = 0, time.perf_counter()
+    while done < slices:
+        oracle.forward(cfg, q, k, v, slices=(done, 1))
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    tokens = done * w.n / w.heads          # tokens are counted once across heads
+    return {"value": tokens / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {slices} (batch, head) slices of {w.name} in {dt:.2f} s, "
+                      "single-threaded fp64 C oracle; tokens/s = slices * N / H / seconds"}
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    q, k, v = make_inputs(w)
+    import oracle
+    oracle.build()
+    cfg = w.config()
+    slices = w.batch * w.heads
+    per_step = max(1, min(slices, 2))
+    times = []
+    for step in range(args.warmup + args.steps):
+        s0 = (step * per_step) % slices
+        cnt = min(per_step, slices - s0)
+        t0 = time.perf_counter()
+        oracle.forward(cfg, q, k, v, slices=(s0, cnt))
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append((dt, cnt))
+    tot_t = sum(t for t, _ in times)
+    tot_tok = sum(c for _, c in times) * w.n / w.heads
+    value = tot_tok / tot_t
+    sample = (f"{per_step} (batch, head) slice(s) of {w.name} per step, single-threaded fp64 C "
+              "oracle; tokens/s = slices * N / H / seconds")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_desc(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as tdist
+
+    world, rank, local = dist_env()
+    if world > 1:
+        tdist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    if not os.path.exists(os.path.join(ROOT, "laplacian_nystr_attention_gb300",
+                                       "liblapl_attn.so")):
+        import __graft_entry__
+        __graft_entry__.build()
+    import laplacian_nystr_attention_gb300 as lna
+    from laplacian_nystr_attention_gb300 import _lib
+
+    q, k, v = make_inputs(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    hq, hk, hv = (torch.from_numpy(x).to(tdt).pin_memory() for x in (q, k, v))
+    dq, dk, dv = (x.to(dev) for x in (hq, hk, hv))
+    cfg = lna.make_config(**{**w.config(), "in_dtype": w.dtype})
+    att = lna.LaplacianNystromAttention(cfg)
+    out = torch.empty((w.batch, w.heads, w.n, w.head_dim), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        att.forward(dq, dk, dv, out=out)
+
+    def barrier():
+        if world > 1:
+            tdist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    barrier()
+
+    # ---- timed region: K forwards, L2 flushed before each (flush not timed) ----
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        barrier()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        ms = float(t.item())
+    kernels = lna.lapl_attn_kernels_per_forward(att.handle)
+    gpu_launches = kernels * args.steps
+
+    # ---- stage times of the same forward, recorded with CUDA events on its streams ----
+    lna.lapl_attn_set_timing(att.handle, True)
+    stage = {s: [] for s in _lib.STAGES}
+    for i in range(args.steps):
+        flush.zero_()
+        step()
+        for key, val in lna.lapl_attn_stage_times(att.handle).items():
+            stage[key].append(val)
+    lna.lapl_attn_set_timing(att.handle, False)
+    stage_ms = {key: sum(vals) / len(vals) for key, vals in stage.items()}
+
+    # ---- end to end through the C ABI with host buffers (pinned) ----
+    e2e = None
+    if not args.no_e2e:
+        h = lna.lapl_attn_create(cfg)
+        nbytes = lna.lapl_attn_host_staging_size(h)
+        staging = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        args_h = (h, hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), None, hout.data_ptr(),
+                  staging.data_ptr(), nbytes, stream.cuda_stream)
+        for _ in range(args.warmup):
+            lna.lapl_attn_forward_host(*args_h)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            lna.lapl_attn_forward_host(*args_h)
+        e1.record(stream)
+        barrier()
+        e2e_ms = e0.elapsed_time(e1) / args.steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        in_b = hq.numel() * hq.element_size()
+        e2e = {"value": world * w.tokens / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": 3 * in_b,
+               "d2h_bytes_per_step": hout.numel() * hout.element_size(),
+               "ms_per_step": e2e_ms}
+        lna.lapl_attn_destroy(h)
+
+    if rank != 0:
+        if world > 1:
+            tdist.destroy_process_group()
+        return
+
+    peaks, peaks_src = measured_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+    peak = fp32_peak_tflops(props.multi_processor_count, sm_max)
+    achieved = cdist_ops_per_launch(w) / (stage_ms["cdist"] / 1e3) / 1e12
+    src_sha = hashlib.sha256(open(os.path.join(ROOT, "laplacian_nystr_attention_gb300", "csrc",
+                                               "cdist.cu"), "rb").read()).hexdigest()
+    traffic = CDIST_TRAFFIC.get(w.name) if CDIST_TRAFFIC_SHA == src_sha else None
+    clk = clocks.summary()
+    line = {
+        "metric": METRIC, "value": world * w.tokens / (ms / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {**workload_desc(w),
+                   "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write, "
+                         "not timed)",
+                   "parallelism": f"replicas x{world} (independent (batch, head) slices)"},
+        "roofline": {
+            "kernel": "cdist_exp_kernel (fused L1 distance + exp, query and key blocks)",
+            "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": traffic,
+            "peak_source": (f"derived: {props.multi_processor_count} SMs x 128 FP32 lanes x 2 x "
+                            f"{sm_max:g} MHz (max SM clock, MEASURED_PEAKS {peaks_src})"),
+            "ops_per_launch": cdist_ops_per_launch(w),
+            "ops_convention": "3 per (token, landmark, channel): subtract, abs, add",
+            "kernel_ms": stage_ms["cdist"],
+        },
+        "stage_ms": stage_ms,
+        "cpu_baseline": None,
+        "e2e": e2e,
+        "gpu_launches": gpu_launches,
+        "clocks": clk,
+        "impl": "ours",
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, q, k, v, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    att.close()
+    if world > 1:
+        tdist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

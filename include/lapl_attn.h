@@ -1,0 +1,160 @@
+/*
+ * lapl_attn.h -- C ABI of the GB300 (sm_103a) Laplacian-kernel Nystrom attention forward.
+ *
+ * The operation ("LaplacianFormer: Rethinking Linear Attention with Laplacian Kernel",
+ * explainer pages): for every batch b and head h independently,
+ *   L  = 2-D average pooling of K over the grid_h x grid_w token grid into m = s*s rows
+ *        (English page, 2.C.1: landmarks selected via average pooling)
+ *   A  = exp(-cdist_L1(Q, L) / lambda)        [N, m]   (English page, 2.A: Laplacian kernel)
+ *   B  = exp(-cdist_L1(L, K) / lambda)        [m, N]
+ *   W  = exp(-cdist_L1(L, L) / lambda) + eps I  [m, m] (English page, 2.C.2: eps I keeps W PD)
+ *   X  = T Newton-Schulz steps X <- X (2I - W X), X0 = W^T / (|W|_1 |W|_inf)
+ *        (English page, 2.C.2; German page, 2: multiply-only inverse)
+ *   A^ = (A - mean_col) / sqrt(var_col + delta) + bias   (Korean page, 2.2: whitening with a
+ *        diagonal estimator; mean/var per landmark column over the N tokens, var divides by N)
+ *   O  = A^ (X (B V))                         [N, d]   (Chinese page, 2.2: the N x N matrix
+ *        is never formed)
+ *
+ * Layouts: Q, K, V, O are [B, H, N, d] contiguous (C order), token n = r * grid_w + c.
+ * Every buffer is owned by the caller.  The handle holds host state only (the configuration
+ * and two CUDA events plus one auxiliary stream used to overlap the Newton-Schulz solve with
+ * the distance kernel).  No entry point allocates device memory; forward() never
+ * synchronises the host.
+ *
+ * Errors: every entry point returns a lapl_status.  Argument errors are detected on the host
+ * before any launch.  CUDA errors from launches map to LAPL_ERR_CUDA (the CUDA error string is
+ * available from lapl_attn_last_error()).  Nothing aborts the process.
+ *
+ * Threading: a handle may be used by one host thread at a time, on one stream at a time.
+ */
+#ifndef LAPL_ATTN_H
+#define LAPL_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LAPL_OK = 0,
+  LAPL_ERR_INVALID_ARG = 1,     /* null pointer, bad size or parameter                    */
+  LAPL_ERR_UNSUPPORTED = 2,     /* valid but outside what the kernels handle (see create) */
+  LAPL_ERR_WORKSPACE = 3,       /* workspace smaller than lapl_attn_workspace_size()       */
+  LAPL_ERR_ALIGNMENT = 4,       /* a device pointer is not 16-byte aligned                 */
+  LAPL_ERR_CUDA = 5,            /* a CUDA runtime call or launch failed                    */
+  LAPL_ERR_DEVICE_TIMEOUT = 6,  /* reserved: a bounded device-side wait gave up            */
+  LAPL_ERR_NOT_IMPLEMENTED = 7
+} lapl_status;
+
+typedef enum { LAPL_F32 = 0, LAPL_BF16 = 1 } lapl_dtype;
+
+typedef struct {
+  int batch;          /* B >= 0 (B == 0: forward is a no-op)                                */
+  int heads;          /* H >= 1                                                             */
+  int grid_h, grid_w; /* token grid, N = grid_h * grid_w                                    */
+  int head_dim;       /* d: multiple of 8, 8 <= d <= 128                                    */
+  int num_landmarks;  /* m = s*s with 1 <= s <= 8; grid_h % s == 0 and grid_w % s == 0      */
+  float lambda;       /* kernel scale, > 0 (the pages' best value is 4)                    */
+  float eps;          /* >= 0, added to the diagonal of W                                    */
+  float delta;        /* > 0 when whiten != 0: variance floor inside the square root         */
+  int ns_steps;       /* T, 0 <= T <= 1000, exactly T Newton-Schulz steps                    */
+  int whiten;         /* 1: whiten A (default); 0: A^ = A and bias is ignored                */
+  int in_dtype;       /* lapl_dtype of Q, K, V                                               */
+  int out_dtype;      /* lapl_dtype of O (LAPL_F32 recommended; LAPL_BF16 rounds at the end) */
+} lapl_attn_config;
+
+typedef struct lapl_attn_plan* lapl_attn_handle;
+
+/* Nullable device pointers for intermediate results (all fp32, C order). */
+typedef struct {
+  float* d_ql;       /* [B,H,N,m] raw L1 distances sum_c |Q_ic - L_jc|  */
+  float* d_ll;       /* [B,H,m,m] raw L1 distances between landmarks    */
+  float* d_lk;       /* [B,H,m,N] raw L1 distances sum_c |L_jc - K_nc|  */
+  float* landmarks;  /* [B,H,m,d] L                                      */
+  float* w;          /* [B,H,m,m] W = k(L,L) + eps I                     */
+  float* x;          /* [B,H,m,m] X after T Newton-Schulz steps          */
+  float* a;          /* [B,H,N,m] A = k(Q,L), before whitening           */
+  float* mu;         /* [B,H,m]   column means of A                      */
+  float* rstd;       /* [B,H,m]   1/sqrt(var + delta) (var divides by N) */
+  float* bv;         /* [B,H,m,d] B V                                    */
+  float* m;          /* [B,H,m,d] X (B V)                                */
+} lapl_attn_debug;
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int lapl_attn_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* lapl_attn_status_string(lapl_status s);
+
+/* Text of the last CUDA error seen by this handle ("" if none; owned by the handle). */
+const char* lapl_attn_last_error(lapl_attn_handle h);
+
+/*
+ * Validate cfg and create a plan on the current CUDA device.  *out receives the handle.
+ * Returns LAPL_ERR_INVALID_ARG / LAPL_ERR_UNSUPPORTED for bad configurations (nothing is
+ * created), LAPL_ERR_CUDA if the event/stream creation fails.
+ */
+lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out);
+
+/* Bytes of device workspace forward() needs (a multiple of 256, linear in B*H*N). */
+lapl_status lapl_attn_workspace_size(lapl_attn_handle h, size_t* bytes);
+
+/*
+ * Forward pass, stream-ordered and asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ * default stream).  q, k, v: device [B,H,N,d] in in_dtype; bias: device [H,m] fp32 or NULL
+ * (zeros); out: device [B,H,N,d] in out_dtype; workspace: device, >= workspace_size bytes,
+ * contents need not be initialised and are overwritten.  q, k, v, out and workspace must be
+ * 16-byte aligned and must not overlap.  No allocation, no host synchronisation.
+ */
+lapl_status lapl_attn_forward(lapl_attn_handle h, const void* q, const void* k, const void* v,
+                              const float* bias, void* out, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* forward() that also writes the non-NULL fields of *dbg (device buffers, fp32). */
+lapl_status lapl_attn_forward_debug(lapl_attn_handle h, const void* q, const void* k,
+                                    const void* v, const float* bias, void* out,
+                                    void* workspace, size_t workspace_bytes, void* stream,
+                                    const lapl_attn_debug* dbg);
+
+/*
+ * Bytes of device staging memory forward_host() needs: device copies of Q, K, V, O and the
+ * workspace, each 256-byte aligned.
+ */
+lapl_status lapl_attn_host_staging_size(lapl_attn_handle h, size_t* bytes);
+
+/*
+ * End-to-end forward from host memory: copies q, k, v (host, in_dtype) and bias (host [H,m]
+ * fp32 or NULL) into `staging` (device, >= host_staging_size bytes), runs forward(), and copies
+ * O back into out (host, out_dtype), all on `stream`.  Page-locked host buffers make the copies
+ * asynchronous; with pageable memory the CUDA runtime stages them synchronously.  Returns
+ * after enqueueing: synchronise the stream before reading out.
+ */
+lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void* k,
+                                   const void* v, const float* bias, void* out, void* staging,
+                                   size_t staging_bytes, void* stream);
+
+/*
+ * Stage timing, a profiling aid.  After lapl_attn_set_timing(h, 1) every forward records CUDA
+ * events (created here, host-owned) around its five stages: on the launching stream for
+ * pooling, distances, finish and output, on the side stream for Newton-Schulz.
+ * lapl_attn_stage_times() waits for the events of the last forward (it synchronises the host
+ * with them) and writes the elapsed milliseconds of
+ *   ms[0] pooling, ms[1] Newton-Schulz, ms[2] distance kernel, ms[3] finish, ms[4] output.
+ * LAPL_ERR_INVALID_ARG if timing is off or no forward ran since it was switched on.
+ */
+lapl_status lapl_attn_set_timing(lapl_attn_handle h, int enable);
+lapl_status lapl_attn_stage_times(lapl_attn_handle h, float* ms);
+
+/* Number of kernels one forward launches (for launch accounting). */
+int lapl_attn_kernels_per_forward(lapl_attn_handle h);
+
+/* Release the plan (host state only).  NULL is accepted. */
+lapl_status lapl_attn_destroy(lapl_attn_handle h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAPL_ATTN_H */

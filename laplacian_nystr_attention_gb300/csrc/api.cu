@@ -1,0 +1,377 @@
+// api.cu -- the C ABI (include/lapl_attn.h): validation, plan, workspace layout, and the
+// stream-ordered launch sequence of one forward pass.
+//
+//   K1 pool      L = avg-pool(K)                          stream
+//   fork ------------------------------------------------ side stream: K3 Newton-Schulz (W, X)
+//   K2 cdist     A^T + tile stats (queries), B V partials (keys)        stream
+//   join <----------------------------------------------- (needs X)
+//   K4 finish    mean/rstd, B V, M = X (B V)              stream
+//   K5 output    O = whiten(A) M                          stream
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+
+#include "common.cuh"
+
+namespace lapl {
+
+size_t finish_smem_bytes(int m, int d);
+int output_tile_tokens(int d);
+
+namespace {
+
+int isqrt_exact(int m) {
+  for (int s = 1; s * s <= m; ++s)
+    if (s * s == m) return s;
+  return -1;
+}
+
+lapl_status validate(const lapl_attn_config* c) {
+  if (!c) return LAPL_ERR_INVALID_ARG;
+  if (c->batch < 0 || c->heads < 1 || c->grid_h < 1 || c->grid_w < 1) return LAPL_ERR_INVALID_ARG;
+  if (c->head_dim < 1 || c->num_landmarks < 1) return LAPL_ERR_INVALID_ARG;
+  if (!(c->lambda > 0.f) || !isfinite(c->lambda)) return LAPL_ERR_INVALID_ARG;
+  if (!(c->eps >= 0.f) || !isfinite(c->eps)) return LAPL_ERR_INVALID_ARG;
+  if (c->whiten != 0 && c->whiten != 1) return LAPL_ERR_INVALID_ARG;
+  if (c->whiten && (!(c->delta > 0.f) || !isfinite(c->delta))) return LAPL_ERR_INVALID_ARG;
+  if (c->ns_steps < 0 || c->ns_steps > 1000) return LAPL_ERR_INVALID_ARG;
+  if ((c->in_dtype != LAPL_F32 && c->in_dtype != LAPL_BF16) ||
+      (c->out_dtype != LAPL_F32 && c->out_dtype != LAPL_BF16))
+    return LAPL_ERR_INVALID_ARG;
+  const int s = isqrt_exact(c->num_landmarks);
+  if (s < 0 || s > kMaxS) return LAPL_ERR_UNSUPPORTED;
+  if (c->grid_h % s != 0 || c->grid_w % s != 0) return LAPL_ERR_UNSUPPORTED;
+  if (c->head_dim % 8 != 0 || c->head_dim > kMaxD) return LAPL_ERR_UNSUPPORTED;
+  const long long n = (long long)c->grid_h * c->grid_w;
+  if (n > (1LL << 24)) return LAPL_ERR_UNSUPPORTED;
+  if ((long long)c->batch * c->heads > (1LL << 24)) return LAPL_ERR_UNSUPPORTED;
+  return LAPL_OK;
+}
+
+void set_error(lapl_attn_plan* p, cudaError_t e, const char* where) {
+  snprintf(p->last_error, sizeof(p->last_error), "%s: %s (%s)", where, cudaGetErrorName(e),
+           cudaGetErrorString(e));
+}
+
+bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
+
+size_t elem_bytes(int dtype) { return dtype == LAPL_BF16 ? 2 : 4; }
+
+}  // namespace
+}  // namespace lapl
+
+using namespace lapl;
+
+extern "C" {
+
+int lapl_attn_version(void) { return 100; }
+
+const char* lapl_attn_status_string(lapl_status s) {
+  switch (s) {
+    case LAPL_OK: return "LAPL_OK";
+    case LAPL_ERR_INVALID_ARG: return "LAPL_ERR_INVALID_ARG";
+    case LAPL_ERR_UNSUPPORTED: return "LAPL_ERR_UNSUPPORTED";
+    case LAPL_ERR_WORKSPACE: return "LAPL_ERR_WORKSPACE";
+    case LAPL_ERR_ALIGNMENT: return "LAPL_ERR_ALIGNMENT";
+    case LAPL_ERR_CUDA: return "LAPL_ERR_CUDA";
+    case LAPL_ERR_DEVICE_TIMEOUT: return "LAPL_ERR_DEVICE_TIMEOUT";
+    case LAPL_ERR_NOT_IMPLEMENTED: return "LAPL_ERR_NOT_IMPLEMENTED";
+  }
+  return "LAPL_ERR_UNKNOWN";
+}
+
+const char* lapl_attn_last_error(lapl_attn_handle h) { return h ? h->last_error : ""; }
+
+lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out) {
+  if (!out) return LAPL_ERR_INVALID_ARG;
+  *out = nullptr;
+  lapl_status st = validate(cfg);
+  if (st != LAPL_OK) return st;
+
+  lapl_attn_plan* p = new (std::nothrow) lapl_attn_plan();
+  if (!p) return LAPL_ERR_INVALID_ARG;
+  p->cfg = *cfg;
+  p->last_error[0] = '\0';
+  p->neg_log2e_over_lambda = (float)(-1.4426950408889634 / (double)cfg->lambda);
+
+  Geometry& g = p->geo;
+  g.s = isqrt_exact(cfg->num_landmarks);
+  g.m = cfg->num_landmarks;
+  g.d = cfg->head_dim;
+  g.n = cfg->grid_h * cfg->grid_w;
+  g.bh = (long)cfg->batch * cfg->heads;
+
+  cudaError_t e = cudaGetDevice(&p->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+  if (e != cudaSuccess) {
+    set_error(p, e, "create/device");
+    delete p;
+    return LAPL_ERR_CUDA;
+  }
+
+  // Distance kernel: 128-token tiles; CTAs of one head walk consecutive tiles so that the
+  // grid is about one wave of resident CTAs.
+  g.cd_tile = cdist_tile_tokens();
+  g.cd_rows = g.cd_tile / 32;
+  g.cd_tiles = (g.n + g.cd_tile - 1) / g.cd_tile;
+  g.cd_smem = cdist_smem_bytes(g.s, g.d, g.cd_tile);
+  int per_sm = 1;
+  e = cdist_configure(g.s, g.d, cfg->in_dtype == LAPL_BF16, g.cd_smem, &per_sm);
+  if (e == cudaSuccess) {
+    g.ns_smem = ns_smem_bytes(g.m, g.d);
+    e = ns_configure(g.ns_smem);
+  }
+  if (e == cudaSuccess) {
+    g.out_tile = output_tile_tokens(g.d);
+    g.out_threads = 256;
+    g.out_smem = output_smem_bytes(g.m, g.d, g.out_tile);
+    e = output_configure(g.out_smem);
+  }
+  if (e != cudaSuccess) {
+    set_error(p, e, "create/configure");
+    delete p;
+    return LAPL_ERR_CUDA;
+  }
+  if (per_sm < 1) per_sm = 1;
+  const long long target = (long long)p->num_sms * per_sm;
+  const long long total_tiles = 2LL * (g.bh > 0 ? g.bh : 1) * g.cd_tiles;
+  long long tps = (total_tiles + target - 1) / target;
+  if (tps < 1) tps = 1;
+  if (tps > g.cd_tiles) tps = g.cd_tiles;
+  g.cd_tiles_per_split = (int)tps;
+  g.cd_splits = (int)((g.cd_tiles + tps - 1) / tps);
+
+  // Workspace regions.
+  WorkspaceLayout& w = p->ws;
+  const size_t bh = (size_t)g.bh, m = g.m, d = g.d, n = g.n;
+  size_t off = 0;
+  auto take = [&](size_t floats) {
+    const size_t at = off;
+    off = align_up(off + floats * sizeof(float), kAlign);
+    return at;
+  };
+  w.landmarks = take(bh * m * d);
+  w.x = take(bh * m * m);
+  w.at = take(bh * m * n);
+  w.stats = take(bh * g.cd_tiles * 2 * m);
+  w.bvp = take(bh * g.cd_splits * m * d);
+  w.mmat = take(bh * m * d);
+  w.mu = take(bh * m);
+  w.rstd = take(bh * m);
+  w.total = off;
+
+  e = cudaStreamCreateWithFlags(&p->side_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    set_error(p, e, "create/stream");
+    if (p->side_stream) cudaStreamDestroy(p->side_stream);
+    if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+    delete p;
+    return LAPL_ERR_CUDA;
+  }
+  *out = p;
+  return LAPL_OK;
+}
+
+lapl_status lapl_attn_workspace_size(lapl_attn_handle h, size_t* bytes) {
+  if (!h || !bytes) return LAPL_ERR_INVALID_ARG;
+  *bytes = h->ws.total;
+  return LAPL_OK;
+}
+
+static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k, const void* v,
+                               const float* bias, void* out, void* workspace,
+                               size_t workspace_bytes, cudaStream_t st,
+                               const lapl_attn_debug* dbg) {
+  if (!p) return LAPL_ERR_INVALID_ARG;
+  if (p->geo.bh == 0) return LAPL_OK;   // empty batch
+  if (!q || !k || !v || !out || !workspace) return LAPL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      !aligned16(workspace) || (bias && ((uintptr_t)bias & 3u)))
+    return LAPL_ERR_ALIGNMENT;
+  if (workspace_bytes < p->ws.total) return LAPL_ERR_WORKSPACE;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error(p, e, "forward/device");
+    return LAPL_ERR_CUDA;
+  }
+  if (dev != p->device) return LAPL_ERR_INVALID_ARG;
+
+  char* ws = static_cast<char*>(workspace);
+  float* L = reinterpret_cast<float*>(ws + p->ws.landmarks);
+  float* X = reinterpret_cast<float*>(ws + p->ws.x);
+  float* At = reinterpret_cast<float*>(ws + p->ws.at);
+  float* stats = reinterpret_cast<float*>(ws + p->ws.stats);
+  float* bvp = reinterpret_cast<float*>(ws + p->ws.bvp);
+  float* M = reinterpret_cast<float*>(ws + p->ws.mmat);
+  float* mu = reinterpret_cast<float*>(ws + p->ws.mu);
+  float* rstd = reinterpret_cast<float*>(ws + p->ws.rstd);
+  const lapl_attn_debug none = {};
+  const lapl_attn_debug& D = dbg ? *dbg : none;
+
+#define LAPL_TRY(call, where)        \
+  do {                               \
+    cudaError_t err_ = (call);       \
+    if (err_ != cudaSuccess) {       \
+      set_error(p, err_, where);     \
+      return LAPL_ERR_CUDA;          \
+    }                                \
+  } while (0)
+
+  const bool tm = p->timing;
+#define LAPL_MARK(i, s)                                              \
+  if (tm) LAPL_TRY(cudaEventRecord(p->ev_stage[i], s), "forward/timing")
+
+  LAPL_MARK(0, st);
+  LAPL_TRY(launch_pool(*p, k, L, D.landmarks, st), "forward/pool");
+  LAPL_MARK(1, st);
+  LAPL_TRY(cudaEventRecord(p->ev_fork, st), "forward/fork");
+  LAPL_TRY(cudaStreamWaitEvent(p->side_stream, p->ev_fork, 0), "forward/fork-wait");
+  LAPL_MARK(5, p->side_stream);
+  LAPL_TRY(launch_ns(*p, L, X, D.d_ll, D.w, D.x, p->side_stream), "forward/newton-schulz");
+  LAPL_MARK(6, p->side_stream);
+  LAPL_TRY(cudaEventRecord(p->ev_join, p->side_stream), "forward/join");
+  LAPL_TRY(launch_cdist(*p, q, k, v, L, At, stats, bvp, D.d_ql, D.d_lk, D.a, st), "forward/cdist");
+  LAPL_MARK(2, st);
+  LAPL_TRY(cudaStreamWaitEvent(st, p->ev_join, 0), "forward/join-wait");
+  LAPL_TRY(launch_finish(*p, stats, bvp, X, M, mu, rstd, D.mu, D.rstd, D.bv, D.m, st),
+           "forward/finish");
+  LAPL_MARK(3, st);
+  LAPL_TRY(launch_output(*p, At, M, mu, rstd, bias, out, st), "forward/output");
+  LAPL_MARK(4, st);
+  if (tm) p->timed_once = true;
+#undef LAPL_MARK
+#undef LAPL_TRY
+  return LAPL_OK;
+}
+
+lapl_status lapl_attn_forward(lapl_attn_handle h, const void* q, const void* k, const void* v,
+                              const float* bias, void* out, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return run_forward(h, q, k, v, bias, out, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream), nullptr);
+}
+
+lapl_status lapl_attn_forward_debug(lapl_attn_handle h, const void* q, const void* k,
+                                    const void* v, const float* bias, void* out,
+                                    void* workspace, size_t workspace_bytes, void* stream,
+                                    const lapl_attn_debug* dbg) {
+  if (!dbg) return LAPL_ERR_INVALID_ARG;
+  return run_forward(h, q, k, v, bias, out, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream), dbg);
+}
+
+namespace {
+struct StagingLayout {
+  size_t q, k, v, out, bias, ws, total;
+};
+
+StagingLayout staging_layout(const lapl_attn_plan* p) {
+  StagingLayout s;
+  const size_t elems = (size_t)p->geo.bh * p->geo.n * p->geo.d;
+  const size_t in_b = elems * elem_bytes(p->cfg.in_dtype);
+  const size_t out_b = elems * elem_bytes(p->cfg.out_dtype);
+  size_t off = 0;
+  s.q = off; off = align_up(off + in_b, kAlign);
+  s.k = off; off = align_up(off + in_b, kAlign);
+  s.v = off; off = align_up(off + in_b, kAlign);
+  s.out = off; off = align_up(off + out_b, kAlign);
+  s.bias = off; off = align_up(off + (size_t)p->cfg.heads * p->geo.m * sizeof(float), kAlign);
+  s.ws = off; off = align_up(off + p->ws.total, kAlign);
+  s.total = off;
+  return s;
+}
+}  // namespace
+
+lapl_status lapl_attn_host_staging_size(lapl_attn_handle h, size_t* bytes) {
+  if (!h || !bytes) return LAPL_ERR_INVALID_ARG;
+  *bytes = staging_layout(h).total;
+  return LAPL_OK;
+}
+
+lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void* k,
+                                   const void* v, const float* bias, void* out, void* staging,
+                                   size_t staging_bytes, void* stream) {
+  if (!h) return LAPL_ERR_INVALID_ARG;
+  if (h->geo.bh == 0) return LAPL_OK;
+  if (!q || !k || !v || !out || !staging) return LAPL_ERR_INVALID_ARG;
+  if (!aligned16(staging)) return LAPL_ERR_ALIGNMENT;
+  const StagingLayout s = staging_layout(h);
+  if (staging_bytes < s.total) return LAPL_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(staging);
+  const size_t elems = (size_t)h->geo.bh * h->geo.n * h->geo.d;
+  const size_t in_b = elems * elem_bytes(h->cfg.in_dtype);
+  const size_t out_b = elems * elem_bytes(h->cfg.out_dtype);
+  cudaError_t e = cudaMemcpyAsync(base + s.q, q, in_b, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.k, k, in_b, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.v, v, in_b, cudaMemcpyHostToDevice, st);
+  float* dbias = nullptr;
+  if (e == cudaSuccess && bias) {
+    dbias = reinterpret_cast<float*>(base + s.bias);
+    e = cudaMemcpyAsync(dbias, bias, (size_t)h->cfg.heads * h->geo.m * sizeof(float),
+                        cudaMemcpyHostToDevice, st);
+  }
+  if (e != cudaSuccess) {
+    set_error(h, e, "forward_host/h2d");
+    return LAPL_ERR_CUDA;
+  }
+  lapl_status r = run_forward(h, base + s.q, base + s.k, base + s.v, dbias, base + s.out,
+                              base + s.ws, h->ws.total, st, nullptr);
+  if (r != LAPL_OK) return r;
+  e = cudaMemcpyAsync(out, base + s.out, out_b, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) {
+    set_error(h, e, "forward_host/d2h");
+    return LAPL_ERR_CUDA;
+  }
+  return LAPL_OK;
+}
+
+lapl_status lapl_attn_set_timing(lapl_attn_handle h, int enable) {
+  if (!h) return LAPL_ERR_INVALID_ARG;
+  if (enable && !h->ev_stage[0]) {
+    for (int i = 0; i < 7; ++i) {
+      cudaError_t e = cudaEventCreate(&h->ev_stage[i]);
+      if (e != cudaSuccess) {
+        set_error(h, e, "set_timing");
+        return LAPL_ERR_CUDA;
+      }
+    }
+  }
+  h->timing = enable != 0;
+  h->timed_once = false;
+  return LAPL_OK;
+}
+
+lapl_status lapl_attn_stage_times(lapl_attn_handle h, float* ms) {
+  if (!h || !ms || !h->timing || !h->timed_once) return LAPL_ERR_INVALID_ARG;
+  cudaError_t e = cudaEventSynchronize(h->ev_stage[4]);
+  if (e == cudaSuccess) e = cudaEventSynchronize(h->ev_stage[6]);
+  const int pairs[5][2] = {{0, 1}, {5, 6}, {1, 2}, {2, 3}, {3, 4}};
+  for (int i = 0; i < 5 && e == cudaSuccess; ++i)
+    e = cudaEventElapsedTime(&ms[i], h->ev_stage[pairs[i][0]], h->ev_stage[pairs[i][1]]);
+  if (e != cudaSuccess) {
+    set_error(h, e, "stage_times");
+    return LAPL_ERR_CUDA;
+  }
+  return LAPL_OK;
+}
+
+int lapl_attn_kernels_per_forward(lapl_attn_handle h) { return (h && h->geo.bh > 0) ? 5 : 0; }
+
+lapl_status lapl_attn_destroy(lapl_attn_handle h) {
+  if (!h) return LAPL_OK;
+  for (int i = 0; i < 7; ++i)
+    if (h->ev_stage[i]) cudaEventDestroy(h->ev_stage[i]);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->side_stream) cudaStreamDestroy(h->side_stream);
+  delete h;
+  return LAPL_OK;
+}
+
+}  // extern "C"

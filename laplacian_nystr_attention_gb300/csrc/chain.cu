@@ -1,0 +1,208 @@
+// chain.cu -- whitening statistics and the output chain O = A^ (X (B V)).
+//
+// "LaplacianFormer: Rethinking Linear Attention with Laplacian Kernel":
+//  * whitening (Korean explainer page, 2.2; English page, 2.B): A^ = (A - mean) / sqrt(var +
+//    delta) + bias with a diagonal estimator, i.e. one mean and one variance per landmark
+//    column, taken over the N tokens of the (batch, head) slice (variance divides by N);
+//  * low-rank product without the N x N matrix (Chinese page, 2.2), evaluated right to left.
+//
+// finish_kernel (one CTA per (batch, head)):
+//   merges the per-tile (mean, M2) of the distance kernel in tile order (Chan's pairwise
+//   update), reduces the per-split partials of B V in split order, and forms M = X (B V).
+//   Fixed reduction orders: the result is bit-reproducible run to run.
+// output_kernel (one CTA per (batch, head, token tile)):
+//   loads the A^T tile, whitens it on the way into shared memory, and writes O = A^ M with a
+//   4 tokens x 4 channels register tile per thread.
+#include "common.cuh"
+
+namespace lapl {
+namespace {
+
+constexpr int kFinishThreads = 256;
+
+__global__ void __launch_bounds__(kFinishThreads)
+finish_kernel(const float* __restrict__ stats, const float* __restrict__ bvp,
+              const float* __restrict__ xg, float* __restrict__ mmat, float* __restrict__ mu,
+              float* __restrict__ rstd, float* __restrict__ dbg_mu, float* __restrict__ dbg_rstd,
+              float* __restrict__ dbg_bv, float* __restrict__ dbg_m, int m, int d, int n,
+              int tiles, int tile_tokens, int splits, float delta) {
+  extern __shared__ float4 smem_fin4[];
+  float* smem = reinterpret_cast<float*>(smem_fin4);
+  const long bh = blockIdx.x;
+  float* sX = smem;             // [m][m]
+  float* sBV = sX + m * m;      // [m][d]
+
+  for (int i = threadIdx.x; i < m * m; i += kFinishThreads) sX[i] = xg[(size_t)bh * m * m + i];
+
+  // Column statistics: Chan's merge of (count, mean, M2) over the tiles, in tile order.
+  for (int j = threadIdx.x; j < m; j += kFinishThreads) {
+    const float* st = stats + (size_t)bh * tiles * 2 * m;
+    float cnt = 0.f, mean = 0.f, m2 = 0.f;
+    for (int t = 0; t < tiles; ++t) {
+      const float nb = (float)min(tile_tokens, n - t * tile_tokens);
+      const float mb = st[(size_t)t * 2 * m + j];
+      const float m2b = st[(size_t)t * 2 * m + m + j];
+      const float tot = cnt + nb;
+      const float dlt = mb - mean;
+      mean += dlt * (nb / tot);
+      m2 += m2b + dlt * dlt * (cnt * nb / tot);
+      cnt = tot;
+    }
+    const float var = m2 / (float)n;
+    const float rs = 1.f / sqrtf(var + delta);
+    mu[(size_t)bh * m + j] = mean;
+    rstd[(size_t)bh * m + j] = rs;
+    if (dbg_mu) dbg_mu[(size_t)bh * m + j] = mean;
+    if (dbg_rstd) dbg_rstd[(size_t)bh * m + j] = rs;
+  }
+
+  // B V = sum over splits, in split order.
+  for (int i = threadIdx.x; i < m * d; i += kFinishThreads) {
+    const float* src = bvp + (size_t)bh * splits * m * d + i;
+    float acc = 0.f;
+    for (int sp = 0; sp < splits; ++sp) acc += src[(size_t)sp * m * d];
+    sBV[i] = acc;
+    if (dbg_bv) dbg_bv[(size_t)bh * m * d + i] = acc;
+  }
+  __syncthreads();
+
+  // M = X (B V).
+  for (int i = threadIdx.x; i < m * d; i += kFinishThreads) {
+    const int j = i / d, c = i % d;
+    float acc = 0.f;
+    for (int k = 0; k < m; ++k) acc = fmaf(sX[j * m + k], sBV[k * d + c], acc);
+    mmat[(size_t)bh * m * d + i] = acc;
+    if (dbg_m) dbg_m[(size_t)bh * m * d + i] = acc;
+  }
+}
+
+constexpr int kOutThreads = 256;
+
+template <bool kOutBf16>
+__global__ void __launch_bounds__(kOutThreads)
+output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
+              const float* __restrict__ mu, const float* __restrict__ rstd,
+              const float* __restrict__ bias, void* __restrict__ out, int m, int d, int n,
+              int heads, int tile, int tiles, int whiten) {
+  extern __shared__ float4 smem_out4[];
+  float* smem = reinterpret_cast<float*>(smem_out4);
+  const long bh = blockIdx.x / tiles;
+  const int tix = blockIdx.x % tiles;
+  const int h = (int)(bh % heads);
+  const int n0 = tix * tile;
+  float* sM = smem;                 // [m][d]
+  float* sA = sM + m * d;           // [m][tile] whitened A, landmark-major
+  float* sCoef = sA + m * tile;     // mean [m], scale [m], bias [m]
+
+  for (int i = threadIdx.x; i < m * d; i += kOutThreads) sM[i] = mmat[(size_t)bh * m * d + i];
+  for (int j = threadIdx.x; j < m; j += kOutThreads) {
+    float mean = 0.f, scale = 1.f, b = 0.f;
+    if (whiten) {
+      mean = mu[(size_t)bh * m + j];
+      scale = rstd[(size_t)bh * m + j];
+      b = bias ? bias[(size_t)h * m + j] : 0.f;
+    }
+    sCoef[j] = mean;
+    sCoef[m + j] = scale;
+    sCoef[2 * m + j] = b;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < m * tile; i += kOutThreads) {
+    const int j = i / tile, t = i % tile;
+    const int tok = n0 + t;
+    float val = 0.f;
+    if (tok < n) {
+      const float a = at[((size_t)bh * m + j) * n + tok];
+      val = (a - sCoef[j]) * sCoef[m + j] + sCoef[2 * m + j];
+    }
+    sA[i] = val;
+  }
+  __syncthreads();
+
+  const int cg = d >> 2;                     // channel quads
+  const int q = threadIdx.x % cg;
+  const int tg = threadIdx.x / cg;           // token quad
+  if (4 * tg >= tile) return;
+  float acc[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+  for (int j = 0; j < m; ++j) {
+    const float4 a4 = *reinterpret_cast<const float4*>(&sA[j * tile + 4 * tg]);
+    const float4 m4 = *reinterpret_cast<const float4*>(&sM[j * d + 4 * q]);
+    const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+    const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], mv[c], acc[r][c]);
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int tok = n0 + 4 * tg + r;
+    if (tok >= n) break;
+    const size_t o = ((size_t)bh * n + tok) * d + 4 * q;
+    if constexpr (kOutBf16) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc[r][0], acc[r][1]);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc[r][2], acc[r][3]);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + o) = pk;
+    } else {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + o) =
+          make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+    }
+  }
+}
+
+}  // namespace
+
+size_t finish_smem_bytes(int m, int d) { return sizeof(float) * ((size_t)m * m + (size_t)m * d); }
+
+int output_tile_tokens(int d) {
+  const int cg = d / 4;
+  return 4 * (kOutThreads / cg);
+}
+
+size_t output_smem_bytes(int m, int d, int tile) {
+  return sizeof(float) * ((size_t)m * d + (size_t)m * tile + 3 * (size_t)m);
+}
+
+cudaError_t output_configure(size_t smem) {
+  cudaError_t e = cudaFuncSetAttribute(output_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(output_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem);
+}
+
+cudaError_t launch_finish(const lapl_attn_plan& p, const float* stats, const float* bvp,
+                          const float* x, float* mmat, float* mu, float* rstd, float* dbg_mu,
+                          float* dbg_rstd, float* dbg_bv, float* dbg_m, cudaStream_t st) {
+  const Geometry& g = p.geo;
+  finish_kernel<<<(unsigned)g.bh, kFinishThreads, finish_smem_bytes(g.m, g.d), st>>>(
+      stats, bvp, x, mmat, mu, rstd, dbg_mu, dbg_rstd, dbg_bv, dbg_m, g.m, g.d, g.n,
+      g.cd_tiles, g.cd_tile, g.cd_splits, p.cfg.delta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float* mmat,
+                          const float* mu, const float* rstd, const float* bias, void* out,
+                          cudaStream_t st) {
+  const Geometry& g = p.geo;
+  const int tiles = (g.n + g.out_tile - 1) / g.out_tile;
+  const unsigned grid = (unsigned)(g.bh * tiles);
+  if (p.cfg.out_dtype == LAPL_BF16)
+    output_kernel<true><<<grid, kOutThreads, g.out_smem, st>>>(
+        at, mmat, mu, rstd, bias, out, g.m, g.d, g.n, p.cfg.heads, g.out_tile, tiles,
+        p.cfg.whiten);
+  else
+    output_kernel<false><<<grid, kOutThreads, g.out_smem, st>>>(
+        at, mmat, mu, rstd, bias, out, g.m, g.d, g.n, p.cfg.heads, g.out_tile, tiles,
+        p.cfg.whiten);
+  return cudaGetLastError();
+}
+
+}  // namespace lapl

@@ -1,0 +1,105 @@
+// common.cuh -- internal declarations shared by the CUDA translation units of liblapl_attn.
+//
+// Nothing here is part of the public ABI (include/lapl_attn.h is).  The plan holds host
+// state only; every device buffer belongs to the caller.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "lapl_attn.h"
+
+namespace lapl {
+
+constexpr int kMaxS = 8;            // landmark grid side: m = s*s <= 64
+constexpr int kMaxM = kMaxS * kMaxS;
+constexpr int kMaxD = 128;
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Offsets (bytes) of the workspace regions for one configuration.  All fp32.
+struct WorkspaceLayout {
+  size_t landmarks;    // [BH, m, d]         pooled keys L
+  size_t x;            // [BH, m, m]         Newton-Schulz result X
+  size_t at;           // [BH, m, N]         A = k(Q, L), landmark-major (A transposed)
+  size_t stats;        // [BH, tiles, 2, m]  per-tile (mean, M2) of the columns of A
+  size_t bvp;          // [BH, splits, m, d] per-split partial sums of B V
+  size_t mmat;         // [BH, m, d]         M = X (B V)
+  size_t mu;           // [BH, m]            column means
+  size_t rstd;         // [BH, m]            1 / sqrt(var + delta)
+  size_t total;
+};
+
+// Launch geometry decided once per plan.
+struct Geometry {
+  int s, m, d, n;          // landmark grid side, landmarks, head dim, tokens per head
+  long bh;                 // batch * heads
+  int cd_rows;             // tokens per thread in the distance kernel
+  int cd_tile;             // tokens per distance tile = 32 * cd_rows
+  int cd_tiles;            // tiles per head and side
+  int cd_tiles_per_split;  // consecutive tiles one CTA walks through
+  int cd_splits;           // CTAs per head and side
+  size_t cd_smem;          // dynamic shared memory of the distance kernel
+  int out_tile;            // tokens per output-kernel CTA
+  int out_threads;
+  size_t out_smem;
+  size_t ns_smem;
+  size_t pool_threads;
+};
+
+}  // namespace lapl
+
+struct lapl_attn_plan {
+  lapl_attn_config cfg;
+  lapl::Geometry geo;
+  lapl::WorkspaceLayout ws;
+  int device;
+  int num_sms;
+  float neg_log2e_over_lambda;  // exp(-D/lambda) == exp2(D * this)
+  cudaStream_t side_stream;     // runs the Newton-Schulz solve next to the distance kernel
+  cudaEvent_t ev_fork, ev_join;
+  bool timing;                  // record stage events in forward
+  bool timed_once;              // a forward ran with timing on
+  cudaEvent_t ev_stage[7];      // start, pool, cdist, finish, output ends; ns start, ns end
+  char last_error[256];
+};
+
+namespace lapl {
+
+// Kernel launchers, one per translation unit.  Each returns the launch's cudaError_t.
+cudaError_t launch_pool(const lapl_attn_plan& p, const void* k, float* landmarks,
+                        float* dbg_landmarks, cudaStream_t st);
+cudaError_t launch_ns(const lapl_attn_plan& p, const float* landmarks, float* x, float* dbg_dll,
+                      float* dbg_w, float* dbg_x, cudaStream_t st);
+cudaError_t launch_cdist(const lapl_attn_plan& p, const void* q, const void* k, const void* v,
+                         const float* landmarks, float* at, float* stats, float* bvp,
+                         float* dbg_dql, float* dbg_dlk, float* dbg_a, cudaStream_t st);
+cudaError_t launch_finish(const lapl_attn_plan& p, const float* stats, const float* bvp,
+                          const float* x, float* mmat, float* mu, float* rstd, float* dbg_mu,
+                          float* dbg_rstd, float* dbg_bv, float* dbg_m, cudaStream_t st);
+cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float* mmat,
+                          const float* mu, const float* rstd, const float* bias, void* out,
+                          cudaStream_t st);
+
+// Shared-memory sizes, needed at plan time to size grids and opt in to > 48 KB.
+size_t cdist_smem_bytes(int s, int d, int tile);
+cudaError_t cdist_configure(int s, int d, bool bf16, size_t smem, int* ctas_per_sm);
+int cdist_tile_tokens();
+size_t ns_smem_bytes(int m, int d);
+cudaError_t ns_configure(size_t smem);
+size_t output_smem_bytes(int m, int d, int tile);
+cudaError_t output_configure(size_t smem);
+
+// ---- device helpers ---------------------------------------------------------------------
+__device__ __forceinline__ float laplacian_from_distance(float dist, float neg_log2e_over_lambda) {
+  // exp(-dist/lambda) as exp2(dist * (-log2(e)/lambda)); exp2f(0) == 1 exactly.
+  return exp2f(dist * neg_log2e_over_lambda);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t two) { return __uint_as_float(two << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t two) { return __uint_as_float(two & 0xffff0000u); }
+
+}  // namespace lapl

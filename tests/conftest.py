@@ -13,6 +13,16 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: long-running CPU test")
 
 
+def build_library():
+    """Compile liblapl_attn.so (loading build.py by path, before the package is imported)."""
+    import importlib.util
+    path = os.path.join(ROOT, "laplacian_nystr_attention_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("lapl_attn_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()
+
+
 @pytest.fixture(scope="session")
 def oracle_mod():
     import oracle

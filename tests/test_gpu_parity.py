@@ -1,0 +1,246 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the fp64 CPU oracle on the
+same seeded inputs.
+
+Bars: distance matrices and landmarks bit-exact on small-integer inputs; O within a normwise
+relative error of 1e-4 per (b,h) slice for fp32 inputs and 2e-2 for bf16 inputs (the oracle
+receives the bf16-rounded values, so both sides compute the same function).
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+from lapl_workloads import WORKLOADS, make_bias, make_inputs
+from parity_utils import (TOL_BF16, TOL_F32, elem_rel, rel_to_max, run_gpu, slice_rel_err,
+                          to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from conftest import build_library
+    build_library()
+    import oracle
+    oracle.build()
+
+
+def oracle_run(w, q, k, v, bias=None, slices=None, inter=False, **over):
+    import oracle
+    cfg = w.config()
+    cfg.update(over)
+    return oracle.forward(cfg, q, k, v, bias=bias, intermediates=inter, slices=slices)
+
+
+def tol_of(w):
+    return TOL_BF16 if w.dtype == "bf16" else TOL_F32
+
+
+# ---- every intermediate on the tiny workload ------------------------------------------------
+def test_tiny_intermediates():
+    w = WORKLOADS["tiny_f32"]
+    q, k, v = make_inputs(w)
+    out, g = run_gpu(w, q, k, v, debug=True)
+    ref, o = oracle_run(w, q, k, v, inter=True)
+    assert rel_to_max(g["landmarks"], o["landmarks"]) < 1e-6
+    assert elem_rel(g["d_ql"], o["d_ql"]) < 1e-5
+    assert elem_rel(g["d_lk"], o["d_lk"]) < 1e-5
+    assert rel_to_max(g["d_ll"], o["d_ll"]) < 1e-5
+    assert elem_rel(g["a"], o["a"]) < 1e-5
+    assert rel_to_max(g["w"], o["w"]) < 1e-6
+    assert np.array_equal(np.diag(g["w"][0, 0]), np.full(16, np.float32(1) + np.float32(1e-3)))
+    assert rel_to_max(g["x"], o["x"]) < 1e-4
+    assert elem_rel(g["mu"], o["mu"]) < 1e-5
+    assert elem_rel(g["rstd"], o["rstd"]) < 1e-4
+    assert rel_to_max(g["bv"], o["bv"]) < 1e-5
+    assert rel_to_max(g["m"], o["m_mat"]) < 1e-4
+    assert slice_rel_err(out, ref) < TOL_F32
+
+
+def test_integer_inputs_distances_bit_exact():
+    w = WORKLOADS["tiny_int"]
+    q, k, v = make_inputs(w)
+    out, g = run_gpu(w, q, k, v, debug=True)
+    ref, o = oracle_run(w, q, k, v, inter=True)
+    for name in ("landmarks", "d_ql", "d_ll", "d_lk"):
+        assert np.array_equal(g[name], o[name]), name
+    assert slice_rel_err(out, ref) < TOL_F32
+
+
+@pytest.mark.parametrize("name", ["stage1_f32", "stage23_bf16", "hires_bf16"])
+def test_integer_variant_of_each_shape_bit_exact(name):
+    """Same shapes and launch configuration as the workload, integer-valued Q and K."""
+    w = WORKLOADS[name].replace(dist="integer", batch=1)
+    q, k, v = make_inputs(w)
+    _, g = run_gpu(w, q, k, v, debug=True)
+    _, o = oracle_run(w, q, k, v, inter=True, slices=(0, 1))
+    for nm in ("landmarks", "d_ql", "d_ll", "d_lk"):
+        assert np.array_equal(g[nm][0, 0], o[nm][0, 0]), nm
+
+
+# ---- the five workloads, end to end --------------------------------------------------------
+FULL = ["tiny_f32", "stage1_f32", "stage23_bf16"]
+SAMPLED = ["hires_bf16", "sweep_f32_1024", "sweep_f32_4096", "sweep_f32_16384",
+           "sweep_f32_65536", "sweep_bf16_1024", "sweep_bf16_65536"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_workload_full(name):
+    w = WORKLOADS[name]
+    q, k, v = make_inputs(w)
+    out, _ = run_gpu(w, q, k, v)
+    ref, _ = oracle_run(w, q, k, v)
+    err = slice_rel_err(out, ref)
+    assert err < tol_of(w), err
+
+
+@pytest.mark.parametrize("name", SAMPLED)
+def test_workload_sampled_slices(name):
+    """Full-size launch; the oracle computes the first and the last (b,h) slice."""
+    w = WORKLOADS[name]
+    q, k, v = make_inputs(w)
+    out, _ = run_gpu(w, q, k, v)
+    nslices = w.batch * w.heads
+    for s0 in sorted({0, nslices - 1}):
+        ref, _ = oracle_run(w, q, k, v, slices=(s0, 1))
+        b, h = divmod(s0, w.heads)
+        err = slice_rel_err(out[b, h][None, None], ref[b, h][None, None])
+        assert err < tol_of(w), (s0, err)
+    assert np.isfinite(out).all()
+
+
+# ---- edge cases ----------------------------------------------------------------------------
+TINY = WORKLOADS["tiny_f32"]
+
+EDGE = {
+    "ragged_14x14_m49": dict(grid_h=14, grid_w=14, num_landmarks=49),
+    "nonsquare_20x12_m16": dict(grid_h=20, grid_w=12, num_landmarks=16),
+    "m1": dict(num_landmarks=1),
+    "m4": dict(num_landmarks=4),
+    "m64_pool2": dict(num_landmarks=64),
+    "single_token": dict(grid_h=1, grid_w=1, num_landmarks=1),
+    "d8": dict(head_dim=8),
+    "d16": dict(head_dim=16),
+    "d24": dict(head_dim=24),
+    "d128": dict(head_dim=128),
+    "T0": dict(ns_steps=0),
+    "T1": dict(ns_steps=1),
+    "T3": dict(ns_steps=3),
+    "whiten_off": dict(whiten=0),
+    "lambda_large": dict(lam=1e6, eps=1.0, whiten=0),
+    "batch_heads": dict(batch=3, heads=5),
+    "n_equals_tile": dict(grid_h=8, grid_w=16, num_landmarks=4),
+    "n_tile_plus_1": dict(grid_h=3, grid_w=43, num_landmarks=1),
+}
+
+
+@pytest.mark.parametrize("case", sorted(EDGE))
+def test_edge_case(case):
+    w = TINY.replace(**EDGE[case])
+    q, k, v = make_inputs(w)
+    out, _ = run_gpu(w, q, k, v)
+    ref, _ = oracle_run(w, q, k, v)
+    err = slice_rel_err(out, ref)
+    assert err < TOL_F32, err
+
+
+def test_unconverged_iteration_heavy_tailed():
+    """T = 4 on a kappa ~ 65 landmark matrix: X is far from W^-1, the iterate itself is compared."""
+    w = WORKLOADS["stage1_f32"].replace(batch=1, heads=2, ns_steps=4)
+    q, k, v = make_inputs(w)
+    out, g = run_gpu(w, q, k, v, debug=True)
+    ref, o = oracle_run(w, q, k, v, inter=True)
+    assert o["ns_resid"][0, 0, -1] > 0.5
+    assert rel_to_max(g["x"], o["x"]) < 1e-5
+    assert slice_rel_err(out, ref) < TOL_F32
+
+
+def test_bias_and_bf16_output():
+    w = TINY.replace(heads=3, batch=2)
+    q, k, v = make_inputs(w)
+    bias = make_bias(w)
+    ref, _ = oracle_run(w, q, k, v, bias=bias)
+    out, _ = run_gpu(w, q, k, v, bias=bias)
+    assert slice_rel_err(out, ref) < TOL_F32
+    out16, _ = run_gpu(w, q, k, v, bias=bias, out_dtype="bf16")
+    assert slice_rel_err(out16, ref) < 2 ** -8
+
+
+def test_constant_keys_closed_form_regime():
+    w = TINY.replace(eps=1.0, ns_steps=30)
+    q, k, v = make_inputs(w)
+    k = np.broadcast_to(k[:, :, :1, :], k.shape).copy()
+    out, _ = run_gpu(w, q, k, v)
+    ref, _ = oracle_run(w, q, k, v)
+    assert slice_rel_err(out, ref) < TOL_F32
+
+
+def test_empty_batch():
+    import torch
+    import laplacian_nystr_attention_gb300 as lna
+    w = TINY.replace(batch=0)
+    att = lna.LaplacianNystromAttention(lna.make_config(**w.config()))
+    z = torch.zeros((0, 1, 256, 32), device="cuda")
+    out = att.forward(z, z, z)
+    assert out.shape == (0, 1, 256, 32)
+    att.close()
+
+
+# ---- determinism, errors, host entry point ------------------------------------------------
+def test_deterministic():
+    w = WORKLOADS["stage1_f32"]
+    q, k, v = make_inputs(w)
+    a, _ = run_gpu(w, q, k, v)
+    b, _ = run_gpu(w, q, k, v)
+    assert np.array_equal(a, b)
+
+
+def test_error_paths():
+    import torch
+    import laplacian_nystr_attention_gb300 as lna
+    from laplacian_nystr_attention_gb300 import _lib
+    w = TINY
+    att = lna.LaplacianNystromAttention(lna.make_config(**w.config()))
+    q = torch.randn(1, 1, 256, 32, device="cuda")
+    out = torch.empty_like(q)
+    h = att.handle
+    st = torch.cuda.current_stream().cuda_stream
+    ws = att.workspace
+    L = _lib.LIB
+    assert L.lapl_attn_forward(h, q.data_ptr(), q.data_ptr(), q.data_ptr(), None, out.data_ptr(),
+                               ws.data_ptr(), att.workspace_bytes - 1, st) == _lib.LAPL_ERR_WORKSPACE
+    assert L.lapl_attn_forward(h, q.data_ptr() + 4, q.data_ptr(), q.data_ptr(), None,
+                               out.data_ptr(), ws.data_ptr(), att.workspace_bytes,
+                               st) == _lib.LAPL_ERR_ALIGNMENT
+    assert L.lapl_attn_forward(h, None, q.data_ptr(), q.data_ptr(), None, out.data_ptr(),
+                               ws.data_ptr(), att.workspace_bytes, st) == _lib.LAPL_ERR_INVALID_ARG
+    # the handle still works after rejected calls
+    assert L.lapl_attn_forward(h, q.data_ptr(), q.data_ptr(), q.data_ptr(), None, out.data_ptr(),
+                               ws.data_ptr(), att.workspace_bytes, st) == _lib.LAPL_OK
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    att.close()
+
+
+def test_forward_host_matches_device_path():
+    import torch
+    import laplacian_nystr_attention_gb300 as lna
+    from laplacian_nystr_attention_gb300 import _lib
+    w = WORKLOADS["stage1_f32"].replace(batch=2)
+    q, k, v = make_inputs(w)
+    dev, _ = run_gpu(w, q, k, v)
+    cfg = lna.make_config(**{**w.config(), "in_dtype": "f32"})
+    h = lna.lapl_attn_create(cfg)
+    nbytes = lna.lapl_attn_host_staging_size(h)
+    staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    hq, hk, hv = (torch.from_numpy(x).pin_memory() for x in (q, k, v))
+    hout = torch.empty(q.shape, dtype=torch.float32).pin_memory()
+    st = torch.cuda.current_stream()
+    lna.lapl_attn_forward_host(h, hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), None,
+                               hout.data_ptr(), staging.data_ptr(), nbytes, st.cuda_stream)
+    st.synchronize()
+    assert np.array_equal(hout.numpy().astype(np.float64), dev)
+    lna.lapl_attn_destroy(h)
