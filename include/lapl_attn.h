@@ -150,6 +150,26 @@ lapl_status lapl_attn_stage_times(lapl_attn_handle h, float* ms);
 /* Number of kernels one forward launches (for launch accounting). */
 int lapl_attn_kernels_per_forward(lapl_attn_handle h);
 
+/*
+ * Forward pass for callers that cannot allocate device memory (for example code embedded in a
+ * host application that owns every allocation, or a plugin that must not call cudaMalloc).
+ * The paper has no counterpart: this is a deployment convenience of this library.
+ *
+ * Same inputs, outputs and results as lapl_attn_forward, but no workspace argument: the
+ * workspace lives in a 32 MiB array in the library's own device memory, which every GPU that
+ * loads the library holds until the process exits.  Configurations whose workspace
+ * (lapl_attn_workspace_size) exceeds 32 MiB are rejected with LAPL_ERR_WORKSPACE and a message
+ * in lapl_attn_last_error().  Allocates nothing.
+ *
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  All calls share the
+ * one array: calls that may overlap on the GPU (other streams, other handles, other threads)
+ * race on it and must be serialised by the caller.  Every region of the workspace is written
+ * before it is read, so nothing needs clearing between calls.
+ */
+lapl_status lapl_attn_forward_noalloc(lapl_attn_handle h, const void* q, const void* k,
+                                      const void* v, const float* bias, void* out, void* stream);
+
 /* Release the plan (host state only).  NULL is accepted. */
 lapl_status lapl_attn_destroy(lapl_attn_handle h);
 

@@ -72,6 +72,7 @@ def _load():
         "lapl_attn_set_timing": ([H, ctypes.c_int], st),
         "lapl_attn_stage_times": ([H, ctypes.POINTER(ctypes.c_float)], st),
         "lapl_attn_kernels_per_forward": ([H], ctypes.c_int),
+        "lapl_attn_forward_noalloc": ([H, vp, vp, vp, vp, vp, vp], st),
         "lapl_attn_destroy": ([H], st),
     }
     for name, (args, res) in sigs.items():
@@ -86,7 +87,7 @@ EXPORTED = ["lapl_attn_version", "lapl_attn_status_string", "lapl_attn_last_erro
             "lapl_attn_create", "lapl_attn_workspace_size", "lapl_attn_forward",
             "lapl_attn_forward_debug", "lapl_attn_host_staging_size", "lapl_attn_forward_host",
             "lapl_attn_set_timing", "lapl_attn_stage_times", "lapl_attn_kernels_per_forward",
-            "lapl_attn_destroy"]
+            "lapl_attn_forward_noalloc", "lapl_attn_destroy"]
 
 
 def status_string(status: int) -> str:
@@ -148,6 +149,12 @@ def lapl_attn_forward_debug(handle, q, k, v, bias, out, workspace, workspace_byt
 def lapl_attn_forward_host(handle, q, k, v, bias, out, staging, staging_bytes, stream) -> None:
     _check(LIB.lapl_attn_forward_host(handle, q, k, v, bias, out, staging, staging_bytes, stream),
            "lapl_attn_forward_host", handle)
+
+
+def lapl_attn_forward_noalloc(handle, q, k, v, bias, out, stream) -> None:
+    """Forward without a workspace argument (the library's static device scratch is used)."""
+    _check(LIB.lapl_attn_forward_noalloc(handle, q, k, v, bias, out, stream),
+           "lapl_attn_forward_noalloc", handle)
 
 
 STAGES = ("pool", "newton_schulz", "cdist", "finish", "output")

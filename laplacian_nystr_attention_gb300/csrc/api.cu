@@ -375,3 +375,16 @@ lapl_status lapl_attn_destroy(lapl_attn_handle h) {
 }
 
 }  // extern "C"
+
+namespace lapl {
+// Internal: the plain forward on a caller-chosen workspace (used by noalloc.cu).
+lapl_status forward_on_workspace(lapl_attn_handle p, const void* q, const void* k, const void* v,
+                                 const float* bias, void* out, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t st) {
+  return run_forward(p, q, k, v, bias, out, workspace, workspace_bytes, st, nullptr);
+}
+
+void record_error(lapl_attn_handle p, const char* text) {
+  snprintf(p->last_error, sizeof(p->last_error), "%s", text);
+}
+}  // namespace lapl
