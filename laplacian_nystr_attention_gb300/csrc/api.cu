@@ -121,7 +121,7 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   e = cdist_configure(g.s, g.d, cfg->in_dtype == LAPL_BF16, g.cd_smem, &per_sm);
   if (e == cudaSuccess) {
     g.ns_smem = ns_smem_bytes(g.m, g.d);
-    e = ns_configure(g.ns_smem);
+    e = ns_configure(g.s, g.ns_smem);
   }
   if (e == cudaSuccess) {
     g.out_tile = output_tile_tokens(g.d);

@@ -19,7 +19,10 @@ namespace lapl {
 namespace {
 
 constexpr int kFinishThreads = 256;
+constexpr int kFinishCols = 8;     // value columns per finish CTA
 
+// grid (BH * column chunks): CTA (bh, cc) reduces the B V partials of columns
+// [cc*8, cc*8+8) and forms those columns of M = X (B V); chunk 0 also merges the statistics.
 __global__ void __launch_bounds__(kFinishThreads)
 finish_kernel(const float* __restrict__ stats, const float* __restrict__ bvp,
               const float* __restrict__ xg, float* __restrict__ mmat, float* __restrict__ mu,
@@ -28,51 +31,80 @@ finish_kernel(const float* __restrict__ stats, const float* __restrict__ bvp,
               int tiles, int tile_tokens, int splits, float delta) {
   extern __shared__ float4 smem_fin4[];
   float* smem = reinterpret_cast<float*>(smem_fin4);
-  const long bh = blockIdx.x;
+  const int chunks = (d + kFinishCols - 1) / kFinishCols;
+  const long bh = blockIdx.x / chunks;
+  const int cc = blockIdx.x % chunks;
+  const int c0 = cc * kFinishCols;
+  const int cw = min(kFinishCols, d - c0);
   float* sX = smem;             // [m][m]
-  float* sBV = sX + m * m;      // [m][d]
+  float* sBV = sX + m * m;      // [m][kFinishCols]
 
   for (int i = threadIdx.x; i < m * m; i += kFinishThreads) sX[i] = xg[(size_t)bh * m * m + i];
 
-  // Column statistics: Chan's merge of (count, mean, M2) over the tiles, in tile order.
-  for (int j = threadIdx.x; j < m; j += kFinishThreads) {
-    const float* st = stats + (size_t)bh * tiles * 2 * m;
-    float cnt = 0.f, mean = 0.f, m2 = 0.f;
-    for (int t = 0; t < tiles; ++t) {
-      const float nb = (float)min(tile_tokens, n - t * tile_tokens);
-      const float mb = st[(size_t)t * 2 * m + j];
-      const float m2b = st[(size_t)t * 2 * m + m + j];
-      const float tot = cnt + nb;
-      const float dlt = mb - mean;
-      mean += dlt * (nb / tot);
-      m2 += m2b + dlt * dlt * (cnt * nb / tot);
-      cnt = tot;
+  // B V columns of this chunk: sum over splits in split order (loads issued 4 at a time).
+  for (int i = threadIdx.x; i < m * cw; i += kFinishThreads) {
+    const int j = i / cw, c = c0 + i % cw;
+    const float* src = bvp + (size_t)bh * splits * m * d + (size_t)j * d + c;
+    const size_t stride = (size_t)m * d;
+    float acc = 0.f;
+    int sp = 0;
+    for (; sp + 4 <= splits; sp += 4) {
+      const float a0 = src[(sp + 0) * stride], a1 = src[(sp + 1) * stride];
+      const float a2 = src[(sp + 2) * stride], a3 = src[(sp + 3) * stride];
+      acc += a0; acc += a1; acc += a2; acc += a3;
     }
-    const float var = m2 / (float)n;
-    const float rs = 1.f / sqrtf(var + delta);
-    mu[(size_t)bh * m + j] = mean;
-    rstd[(size_t)bh * m + j] = rs;
-    if (dbg_mu) dbg_mu[(size_t)bh * m + j] = mean;
-    if (dbg_rstd) dbg_rstd[(size_t)bh * m + j] = rs;
+    for (; sp < splits; ++sp) acc += src[sp * stride];
+    sBV[j * kFinishCols + (c - c0)] = acc;
+    if (dbg_bv) dbg_bv[((size_t)bh * m + j) * d + c] = acc;
   }
 
-  // B V = sum over splits, in split order.
-  for (int i = threadIdx.x; i < m * d; i += kFinishThreads) {
-    const float* src = bvp + (size_t)bh * splits * m * d + i;
-    float acc = 0.f;
-    for (int sp = 0; sp < splits; ++sp) acc += src[(size_t)sp * m * d];
-    sBV[i] = acc;
-    if (dbg_bv) dbg_bv[(size_t)bh * m * d + i] = acc;
+  // Column statistics (chunk 0): Chan's merge of (count, mean, M2) over the tiles in tile
+  // order; the loads of 8 tiles are issued before their merges.
+  if (cc == 0) {
+    for (int j = threadIdx.x; j < m; j += kFinishThreads) {
+      const float* st = stats + (size_t)bh * tiles * 2 * m;
+      float cnt = 0.f, mean = 0.f, m2 = 0.f;
+      for (int t0 = 0; t0 < tiles; t0 += 8) {
+        float mb[8], m2b[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          mb[u] = 0.f;
+          m2b[u] = 0.f;
+          if (t0 + u < tiles) {
+            mb[u] = st[(size_t)(t0 + u) * 2 * m + j];
+            m2b[u] = st[(size_t)(t0 + u) * 2 * m + m + j];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (t0 + u < tiles) {
+            const float nb = (float)min(tile_tokens, n - (t0 + u) * tile_tokens);
+            const float tot = cnt + nb;
+            const float dlt = mb[u] - mean;
+            mean += dlt * (nb / tot);
+            m2 += m2b[u] + dlt * dlt * (cnt * nb / tot);
+            cnt = tot;
+          }
+        }
+      }
+      const float var = m2 / (float)n;
+      const float rs = 1.f / sqrtf(var + delta);
+      mu[(size_t)bh * m + j] = mean;
+      rstd[(size_t)bh * m + j] = rs;
+      if (dbg_mu) dbg_mu[(size_t)bh * m + j] = mean;
+      if (dbg_rstd) dbg_rstd[(size_t)bh * m + j] = rs;
+    }
   }
   __syncthreads();
 
-  // M = X (B V).
-  for (int i = threadIdx.x; i < m * d; i += kFinishThreads) {
-    const int j = i / d, c = i % d;
+  // M[:, chunk] = X (B V)[:, chunk].
+  for (int i = threadIdx.x; i < m * cw; i += kFinishThreads) {
+    const int j = i / cw, c = i % cw;
     float acc = 0.f;
-    for (int k = 0; k < m; ++k) acc = fmaf(sX[j * m + k], sBV[k * d + c], acc);
-    mmat[(size_t)bh * m * d + i] = acc;
-    if (dbg_m) dbg_m[(size_t)bh * m * d + i] = acc;
+    for (int k = 0; k < m; ++k) acc = fmaf(sX[j * m + k], sBV[k * kFinishCols + c], acc);
+    const size_t o = ((size_t)bh * m + j) * d + c0 + c;
+    mmat[o] = acc;
+    if (dbg_m) dbg_m[o] = acc;
   }
 }
 
@@ -107,15 +139,29 @@ output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
     sCoef[2 * m + j] = b;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < m * tile; i += kOutThreads) {
-    const int j = i / tile, t = i % tile;
-    const int tok = n0 + t;
-    float val = 0.f;
-    if (tok < n) {
-      const float a = at[((size_t)bh * m + j) * n + tok];
-      val = (a - sCoef[j]) * sCoef[m + j] + sCoef[2 * m + j];
+  // A^T tile -> whitened, landmark-major shared tile.  Loads are issued 16 per thread before
+  // any of them is consumed, so enough requests are in flight to cover DRAM latency.
+  constexpr int kBatch = 16;
+  const int total = m * tile;
+  for (int base = 0; base < total; base += kBatch * kOutThreads) {
+    float a[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * kOutThreads + threadIdx.x;
+      a[u] = 0.f;
+      if (i < total) {
+        const int j = i / tile, tok = n0 + i % tile;
+        if (tok < n) a[u] = at[((size_t)bh * m + j) * n + tok];
+      }
     }
-    sA[i] = val;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * kOutThreads + threadIdx.x;
+      if (i < total) {
+        const int j = i / tile;
+        sA[i] = (a[u] - sCoef[j]) * sCoef[m + j] + sCoef[2 * m + j];
+      }
+    }
   }
   __syncthreads();
 
@@ -159,7 +205,10 @@ output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
 
 }  // namespace
 
-size_t finish_smem_bytes(int m, int d) { return sizeof(float) * ((size_t)m * m + (size_t)m * d); }
+size_t finish_smem_bytes(int m, int d) {
+  (void)d;
+  return sizeof(float) * ((size_t)m * m + (size_t)m * kFinishCols);
+}
 
 int output_tile_tokens(int d) {
   const int cg = d / 4;
@@ -182,7 +231,8 @@ cudaError_t launch_finish(const lapl_attn_plan& p, const float* stats, const flo
                           const float* x, float* mmat, float* mu, float* rstd, float* dbg_mu,
                           float* dbg_rstd, float* dbg_bv, float* dbg_m, cudaStream_t st) {
   const Geometry& g = p.geo;
-  finish_kernel<<<(unsigned)g.bh, kFinishThreads, finish_smem_bytes(g.m, g.d), st>>>(
+  const int chunks = (g.d + kFinishCols - 1) / kFinishCols;
+  finish_kernel<<<(unsigned)(g.bh * chunks), kFinishThreads, finish_smem_bytes(g.m, g.d), st>>>(
       stats, bvp, x, mmat, mu, rstd, dbg_mu, dbg_rstd, dbg_bv, dbg_m, g.m, g.d, g.n,
       g.cd_tiles, g.cd_tile, g.cd_splits, p.cfg.delta);
   return cudaGetLastError();

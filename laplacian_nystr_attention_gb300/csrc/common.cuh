@@ -89,7 +89,7 @@ size_t cdist_smem_bytes(int s, int d, int tile);
 cudaError_t cdist_configure(int s, int d, bool bf16, size_t smem, int* ctas_per_sm);
 int cdist_tile_tokens();
 size_t ns_smem_bytes(int m, int d);
-cudaError_t ns_configure(size_t smem);
+cudaError_t ns_configure(int s, size_t smem);
 size_t output_smem_bytes(int m, int d, int tile);
 cudaError_t output_configure(size_t smem);
 

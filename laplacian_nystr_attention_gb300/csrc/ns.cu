@@ -6,88 +6,133 @@
 // definite.  X0 = W^T / (|W|_1 |W|_inf) (largest absolute column sum times largest absolute
 // row sum), exactly T steps.
 //
-// One CTA per (batch, head): the m x m matrices (m <= 64) live in shared memory, zero-padded
-// to a multiple of 4 so that every thread owns a 4 x 4 register tile of each product; the
-// padding rows and columns stay exactly zero through the iteration.  Each step is
-// P = W X followed by X <- 2X - X P, in fp32.
+// One CTA per (batch, head); the m x m matrices (m <= 64) live in shared memory, zero-padded
+// to MP = a multiple of 4 (the padding stays exactly zero through the iteration).
+//
+// Symmetry.  W is symmetric, X0 = W^T / c is symmetric, and X_{t+1} = X_t (2I - W X_t) is
+// symmetric whenever X_t is a polynomial in W.  The update X <- 2X - X P is therefore evaluated
+// on the upper-triangle 4 x 4 blocks only and mirrored, so every iterate is exactly symmetric.
+// P = W X is computed in full: mirroring it as well drops its commutator part [W, X]/2, and in
+// fp32 that error grows through the slow first phase of the iteration until it diverges
+// (kappa(W) ~ 65 already does), whereas mirroring one of the two products stays within
+// rounding of the plain iteration.  With A symmetric both factors are row reads,
+// (A B)[i][j] = sum_k A[k][i] B[k][j]: one 128-bit load of A and one of B per 16 FMAs.
+// The k range of a block is split over KP adjacent lanes, combined with shuffles, so that
+// enough warps are in flight.
 #include "common.cuh"
 
 namespace lapl {
 namespace {
 
-constexpr int kNsThreads = 256;
+constexpr int kNsThreads = 1024;
 
-// C = A B (mp x mp, row-major, shared memory).  If kTwoXMinus, C = 2*Xs - A B instead.
-template <bool kTwoXMinus>
-__device__ __forceinline__ void small_matmul(const float* __restrict__ A,
-                                             const float* __restrict__ Bm,
-                                             const float* __restrict__ Xs, float* __restrict__ C,
-                                             int mp) {
-  const int nt = mp >> 2;
-  for (int tile = threadIdx.x; tile < nt * nt; tile += kNsThreads) {
-    const int ti = tile / nt, tj = tile % nt;
-    float acc[4][4];
+// Lanes per block: largest power of two <= 8 that divides MP and keeps blocks*KP <= threads.
+constexpr int lanes_per_block(int mp, int blocks) {
+  return (mp % 8 == 0 && blocks * 8 <= kNsThreads) ? 8
+       : (mp % 4 == 0 && blocks * 4 <= kNsThreads) ? 4
+       : (mp % 2 == 0 && blocks * 2 <= kNsThreads) ? 2 : 1;
+}
+
+template <int S>
+struct NsShape {
+  static constexpr int M = S * S;
+  static constexpr int MP = (M + 3) & ~3;
+  static constexpr int NT = MP / 4;                  // 4x4 blocks per side
+  static constexpr int NFULL = NT * NT;              // all blocks (P = W X)
+  static constexpr int NB = NT * (NT + 1) / 2;       // upper-triangle blocks (X update)
+  static constexpr int KP1 = lanes_per_block(MP, NFULL);
+  static constexpr int KP2 = lanes_per_block(MP, NB);
+};
+
+// C = A B for symmetric A (MP x MP, row-major): (A B)[i][j] = sum_k A[k][i] B[k][j].
+// kMirror: C = 2 Xs - A B on an upper-triangle block, written to (i, j) and (j, i).
+// Otherwise: C = A B on any block.
+template <int MP, int KP, bool kMirror>
+__device__ __forceinline__ void sym_product(const float* __restrict__ A,
+                                            const float* __restrict__ B,
+                                            const float* __restrict__ Xs, float* __restrict__ C,
+                                            int bi, int bj, int kp, bool active) {
+  constexpr int KLEN = MP / KP;
+  float acc[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+  if (active) {
+    const float* a = A + (kp * KLEN) * MP + 4 * bi;
+    const float* b = B + (kp * KLEN) * MP + 4 * bj;
+#pragma unroll
+    for (int kk = 0; kk < KLEN; ++kk) {
+      const float4 av = *reinterpret_cast<const float4*>(a + kk * MP);
+      const float4 bv = *reinterpret_cast<const float4*>(b + kk * MP);
+      const float ar[4] = {av.x, av.y, av.z, av.w};
+      const float br[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(ar[r], br[c], acc[r][c]);
+    }
+  }
+#pragma unroll
+  for (int o = 1; o < KP; o <<= 1)
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
-    for (int k = 0; k < mp; ++k) {
-      float a[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) a[r] = A[(4 * ti + r) * mp + k];
-      const float4 b = *reinterpret_cast<const float4*>(&Bm[k * mp + 4 * tj]);
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        acc[r][0] = fmaf(a[r], b.x, acc[r][0]);
-        acc[r][1] = fmaf(a[r], b.y, acc[r][1]);
-        acc[r][2] = fmaf(a[r], b.z, acc[r][2]);
-        acc[r][3] = fmaf(a[r], b.w, acc[r][3]);
-      }
-    }
+      for (int c = 0; c < 4; ++c) acc[r][c] += __shfl_xor_sync(0xffffffffu, acc[r][c], o);
+  if (active && kp == 0) {
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      float4 o;
-      float* op = reinterpret_cast<float*>(&o);
+      if constexpr (kMirror) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int idx = (4 * ti + r) * mp + 4 * tj + c;
-        op[c] = kTwoXMinus ? 2.f * Xs[idx] - acc[r][c] : acc[r][c];
+        for (int c = 0; c < 4; ++c) {
+          const int i = 4 * bi + r, j = 4 * bj + c;
+          if (bi < bj || r <= c) {
+            const float v = 2.f * Xs[i * MP + j] - acc[r][c];
+            C[i * MP + j] = v;
+            C[j * MP + i] = v;
+          }
+        }
+      } else {
+        *reinterpret_cast<float4*>(&C[(4 * bi + r) * MP + 4 * bj]) =
+            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
       }
-      *reinterpret_cast<float4*>(&C[(4 * ti + r) * mp + 4 * tj]) = o;
     }
   }
 }
 
+template <int S>
 __global__ void __launch_bounds__(kNsThreads)
 ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
                   float* __restrict__ dbg_dll, float* __restrict__ dbg_w,
-                  float* __restrict__ dbg_x, int m, int d, int T, float eps, float c_exp) {
+                  float* __restrict__ dbg_x, int d, int T, float eps, float c_exp) {
+  using Sh = NsShape<S>;
+  constexpr int M = Sh::M, MP = Sh::MP, NT = Sh::NT;
+  constexpr int KP1 = Sh::KP1, KP2 = Sh::KP2;
   extern __shared__ float4 smem_ns4[];
   float* smem = reinterpret_cast<float*>(smem_ns4);
-  const int mp = (m + 3) & ~3;
   const long bh = blockIdx.x;
-  float* sL = smem;              // [m][d]
-  float* W = sL + m * d;         // [mp][mp]  (m*d is a multiple of 8: 16-byte aligned)
-  float* X = W + mp * mp;
-  float* P = X + mp * mp;
-  float* Y = P + mp * mp;
-  float* red = Y + mp * mp;      // column sums [64], row sums [64], scale
+  float* W = smem;               // [MP][MP]
+  float* X = W + MP * MP;
+  float* P = X + MP * MP;
+  float* Y = P + MP * MP;
+  float* red = Y + MP * MP;      // column sums [64], row sums [64], scale
+  float* sL = red + 132;         // [M][d]
 
-  const float4* Lg = reinterpret_cast<const float4*>(landmarks + (size_t)bh * m * d);
-  for (int i = threadIdx.x; i < (m * d) >> 2; i += kNsThreads)
+  const float4* Lg = reinterpret_cast<const float4*>(landmarks + (size_t)bh * M * d);
+  for (int i = threadIdx.x; i < (M * d) >> 2; i += kNsThreads)
     reinterpret_cast<float4*>(sL)[i] = Lg[i];
   __syncthreads();
 
-  // W = exp(-D_LL / lambda) + eps I, zero padding outside m x m.
-  for (int idx = threadIdx.x; idx < mp * mp; idx += kNsThreads) {
-    const int i = idx / mp, k = idx % mp;
+  // W = exp(-D_LL / lambda) + eps I (exactly symmetric: |a-b| == |b-a| and the same order).
+  for (int idx = threadIdx.x; idx < MP * MP; idx += kNsThreads) {
+    const int i = idx / MP, k = idx % MP;
     float w = 0.f;
-    if (i < m && k < m) {
+    if (i < M && k < M) {
       float dist = 0.f;
       for (int c = 0; c < d; ++c) dist += fabsf(sL[i * d + c] - sL[k * d + c]);
       w = laplacian_from_distance(dist, c_exp);
       if (i == k) w += eps;
-      const size_t o = ((size_t)bh * m + i) * m + k;
+      const size_t o = ((size_t)bh * M + i) * M + k;
       if (dbg_dll) dbg_dll[o] = dist;
       if (dbg_w) dbg_w[o] = w;
     }
@@ -96,12 +141,12 @@ ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
   __syncthreads();
 
   // |W|_1 (largest absolute column sum) and |W|_inf (largest absolute row sum).
-  if (threadIdx.x < m) {
+  if (threadIdx.x < M) {
     const int j = threadIdx.x;
     float cs = 0.f, rs = 0.f;
-    for (int i = 0; i < m; ++i) {
-      cs += fabsf(W[i * mp + j]);
-      rs += fabsf(W[j * mp + i]);
+    for (int i = 0; i < M; ++i) {
+      cs += fabsf(W[i * MP + j]);
+      rs += fabsf(W[j * MP + i]);
     }
     red[j] = cs;
     red[64 + j] = rs;
@@ -109,7 +154,7 @@ ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
   __syncthreads();
   if (threadIdx.x == 0) {
     float n1 = 0.f, ninf = 0.f;
-    for (int j = 0; j < m; ++j) {
+    for (int j = 0; j < M; ++j) {
       n1 = fmaxf(n1, red[j]);
       ninf = fmaxf(ninf, red[64 + j]);
     }
@@ -117,25 +162,58 @@ ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
   }
   __syncthreads();
   const float scale = red[128];
-  for (int idx = threadIdx.x; idx < mp * mp; idx += kNsThreads) {
-    const int i = idx / mp, k = idx % mp;
-    X[idx] = W[k * mp + i] / scale;     // X0 = W^T / (|W|_1 |W|_inf)
+  for (int idx = threadIdx.x; idx < MP * MP; idx += kNsThreads) {
+    const int i = idx / MP, k = idx % MP;
+    X[idx] = W[k * MP + i] / scale;     // X0 = W^T / (|W|_1 |W|_inf)
+  }
+
+  // Blocks of this lane group: any block for P = W X, an upper-triangle block for the update.
+  const int item1 = threadIdx.x / KP1, kp1 = threadIdx.x % KP1;
+  const bool act1 = item1 < Sh::NFULL;
+  const int bi1 = act1 ? item1 / NT : 0, bj1 = act1 ? item1 % NT : 0;
+  const int item2 = threadIdx.x / KP2, kp2 = threadIdx.x % KP2;
+  const bool act2 = item2 < Sh::NB;
+  int bi2 = 0, bj2 = 0;
+  if (act2) {
+    int rem = item2;
+    while (rem >= NT - bi2) {
+      rem -= NT - bi2;
+      ++bi2;
+    }
+    bj2 = bi2 + rem;
   }
   __syncthreads();
 
   for (int t = 0; t < T; ++t) {
-    small_matmul<false>(W, X, nullptr, P, mp);   // P = W X
+    sym_product<MP, KP1, false>(W, X, nullptr, P, bi1, bj1, kp1, act1);  // P = W X
     __syncthreads();
-    small_matmul<true>(X, P, X, Y, mp);          // Y = 2X - X P = X (2I - W X)
+    sym_product<MP, KP2, true>(X, P, X, Y, bi2, bj2, kp2, act2);         // Y = 2X - X P
     __syncthreads();
     float* tmp = X; X = Y; Y = tmp;
   }
 
-  for (int idx = threadIdx.x; idx < m * m; idx += kNsThreads) {
-    const int i = idx / m, k = idx % m;
-    const float x = X[i * mp + k];
-    xout[(size_t)bh * m * m + idx] = x;
-    if (dbg_x) dbg_x[(size_t)bh * m * m + idx] = x;
+  for (int idx = threadIdx.x; idx < M * M; idx += kNsThreads) {
+    const int i = idx / M, k = idx % M;
+    const float x = X[i * MP + k];
+    xout[(size_t)bh * M * M + idx] = x;
+    if (dbg_x) dbg_x[(size_t)bh * M * M + idx] = x;
+  }
+}
+
+template <int S>
+const void* ns_ptr() { return reinterpret_cast<const void*>(&ns_inverse_kernel<S>); }
+
+const void* pick_ns(int s) {
+  switch (s) {
+    case 1: return ns_ptr<1>();
+    case 2: return ns_ptr<2>();
+    case 3: return ns_ptr<3>();
+    case 4: return ns_ptr<4>();
+    case 5: return ns_ptr<5>();
+    case 6: return ns_ptr<6>();
+    case 7: return ns_ptr<7>();
+    case 8: return ns_ptr<8>();
+    default: return nullptr;
   }
 }
 
@@ -143,21 +221,24 @@ ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
 
 size_t ns_smem_bytes(int m, int d) {
   const int mp = (m + 3) & ~3;
-  return sizeof(float) * ((size_t)m * d + 4 * (size_t)mp * mp + 132);
+  return sizeof(float) * (4 * (size_t)mp * mp + 132 + (size_t)m * d);
 }
 
-cudaError_t ns_configure(size_t smem) {
-  return cudaFuncSetAttribute(ns_inverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem);
+cudaError_t ns_configure(int s, size_t smem) {
+  const void* f = pick_ns(s);
+  if (!f) return cudaErrorInvalidValue;
+  return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
 cudaError_t launch_ns(const lapl_attn_plan& p, const float* landmarks, float* x, float* dbg_dll,
                       float* dbg_w, float* dbg_x, cudaStream_t st) {
   const Geometry& g = p.geo;
-  ns_inverse_kernel<<<(unsigned)g.bh, kNsThreads, g.ns_smem, st>>>(
-      landmarks, x, dbg_dll, dbg_w, dbg_x, g.m, g.d, p.cfg.ns_steps, p.cfg.eps,
-      p.neg_log2e_over_lambda);
-  return cudaGetLastError();
+  const void* f = pick_ns(g.s);
+  if (!f) return cudaErrorInvalidValue;
+  int d = g.d, T = p.cfg.ns_steps;
+  float eps = p.cfg.eps, c_exp = p.neg_log2e_over_lambda;
+  void* args[] = {&landmarks, &x, &dbg_dll, &dbg_w, &dbg_x, &d, &T, &eps, &c_exp};
+  return cudaLaunchKernel(f, dim3((unsigned)g.bh), dim3(kNsThreads), args, g.ns_smem, st);
 }
 
 }  // namespace lapl
