@@ -47,21 +47,25 @@ __device__ __forceinline__ int swizzle_mask(int d) {
 }
 
 // Stage rows [n0, n0+tile) of a [N, d] matrix into shared memory as fp32, zero beyond N.
-// kSwizzle: 16-byte chunk c of row t is stored at chunk c ^ (t & mask).
+// kSwizzle: 16-byte chunk c of row t is stored at chunk c ^ (t & mask).  Each thread keeps one
+// chunk column and walks the rows, so no index needs a division inside the loop.
 template <bool kBf16, bool kSwizzle>
 __device__ __forceinline__ void stage_rows(const void* __restrict__ src, float* __restrict__ dst,
                                            size_t row0, int valid, int tile, int d, int mask,
                                            int nthreads) {
   if constexpr (kBf16) {
     const int d8 = d >> 3;
-    const uint4* s8 = reinterpret_cast<const uint4*>(src);
-    for (int idx = threadIdx.x; idx < tile * d8; idx += nthreads) {
-      const int t = idx / d8, c8 = idx % d8;
+    const int rstep = nthreads / d8;
+    const int c8 = threadIdx.x % d8;
+    const int t0 = threadIdx.x / d8;
+    if (t0 >= rstep) return;
+    const uint4* s8 = reinterpret_cast<const uint4*>(src) + ((row0 * d) >> 3) + c8;
+    const int c0 = 2 * c8, c1 = 2 * c8 + 1;
+    for (int t = t0; t < tile; t += rstep) {
       uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-      if (t < valid) raw = s8[((row0 + t) * d >> 3) + c8];
+      if (t < valid) raw = s8[(size_t)t * d8];
       const float4 lo = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
       const float4 hi = make_float4(bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w));
-      const int c0 = 2 * c8, c1 = 2 * c8 + 1;
       const int p0 = kSwizzle ? (c0 ^ (t & mask)) : c0;
       const int p1 = kSwizzle ? (c1 ^ (t & mask)) : c1;
       *reinterpret_cast<float4*>(&dst[t * d + 4 * p0]) = lo;
@@ -69,11 +73,14 @@ __device__ __forceinline__ void stage_rows(const void* __restrict__ src, float* 
     }
   } else {
     const int d4 = d >> 2;
-    const float4* s4 = reinterpret_cast<const float4*>(src);
-    for (int idx = threadIdx.x; idx < tile * d4; idx += nthreads) {
-      const int t = idx / d4, c4 = idx % d4;
+    const int rstep = nthreads / d4;
+    const int c4 = threadIdx.x % d4;
+    const int t0 = threadIdx.x / d4;
+    if (t0 >= rstep) return;
+    const float4* s4 = reinterpret_cast<const float4*>(src) + ((row0 * d) >> 2) + c4;
+    for (int t = t0; t < tile; t += rstep) {
       float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (t < valid) x = s4[((row0 + t) * d >> 2) + c4];
+      if (t < valid) x = s4[(size_t)t * d4];
       const int p = kSwizzle ? (c4 ^ (t & mask)) : c4;
       *reinterpret_cast<float4*>(&dst[t * d + 4 * p]) = x;
     }
@@ -91,14 +98,15 @@ __global__ void __launch_bounds__(32 * S)
 cdist_exp_kernel(const CdistArgs a) {
   constexpr int kThreads = 32 * S;
   constexpr int kTile = 32 * R;
+  constexpr int kTileP = kTile + 4;    // padded row of the kernel-value tile
   constexpr int M = S * S;
   extern __shared__ float4 smem_cd4[];
   float* smem = reinterpret_cast<float*>(smem_cd4);
   const int d = a.d, n = a.n;
   float* sL = smem;                    // [M][d]
   float* sX = sL + M * d;              // [kTile][d] swizzled token rows
-  float* sOut = sX + kTile * d;        // [M][kTile] kernel values, landmark-major
-  float* sV = sOut + M * kTile;        // [kTile][d] values (key side)
+  float* sOut = sX + kTile * d;        // [M][kTileP] kernel values, landmark-major
+  float* sV = sOut + M * kTileP;       // [kTile][d] values (key side)
 
   const int side = blockIdx.y;
   const long bh = blockIdx.x / a.splits;
@@ -107,6 +115,7 @@ cdist_exp_kernel(const CdistArgs a) {
   const int mask = swizzle_mask(d);
   const int tile_begin = split * a.tiles_per_split;
   const int tile_end = min(a.tiles, tile_begin + a.tiles_per_split);
+  const bool debug = a.dbg_dql || a.dbg_dlk || a.dbg_a;
 
   {
     const float4* Lg = reinterpret_cast<const float4*>(a.landmarks + (size_t)bh * M * d);
@@ -114,13 +123,20 @@ cdist_exp_kernel(const CdistArgs a) {
       reinterpret_cast<float4*>(sL)[i] = Lg[i];
   }
 
-  // value columns per lane: c = lane + 32*cc, cc < DC = ceil(d/32)
-  const bool debug = a.dbg_dql || a.dbg_dlk || a.dbg_a;
-  float bv[S][DC];
+  // Key side, B V: thread (ks, lg, cq) accumulates landmarks lg*S .. lg*S+S-1 times channels
+  // 4cq .. 4cq+3 over the token quads q == ks (mod KS) of every tile, in registers.
+  const int cqn = d >> 2;
+  const int set = S * cqn;
+  const int KS = kThreads / set;       // token classes (>= 1 since d <= 128)
+  const int bv_ks = threadIdx.x / set;
+  const int bv_lg = (threadIdx.x % set) / cqn;
+  const int bv_cq = threadIdx.x % cqn;
+  const bool bv_on = bv_ks < KS;
+  float bv[S][4];
 #pragma unroll
   for (int jj = 0; jj < S; ++jj)
 #pragma unroll
-    for (int cc = 0; cc < DC; ++cc) bv[jj][cc] = 0.f;
+    for (int c = 0; c < 4; ++c) bv[jj][c] = 0.f;
 
   const void* src = side == 0 ? a.q : a.k;
   for (int tile = tile_begin; tile < tile_end; ++tile) {
@@ -167,16 +183,14 @@ cdist_exp_kernel(const CdistArgs a) {
       for (int jj = 0; jj < S; ++jj) {
         const int j = warp * S + jj;
         const float val = t < valid ? laplacian_from_distance(acc[r][jj], a.c_exp) : 0.f;
-        sOut[j * kTile + t] = val;
-        if (debug) {
-          if (t < valid) {
-            const size_t tok = row0 + t;
-            if (side == 0) {
-              if (a.dbg_dql) a.dbg_dql[tok * M + j] = acc[r][jj];
-              if (a.dbg_a) a.dbg_a[tok * M + j] = val;
-            } else if (a.dbg_dlk) {
-              a.dbg_dlk[((size_t)bh * M + j) * n + n0 + t] = acc[r][jj];
-            }
+        sOut[j * kTileP + t] = val;
+        if (debug && t < valid) {
+          const size_t tok = row0 + t;
+          if (side == 0) {
+            if (a.dbg_dql) a.dbg_dql[tok * M + j] = acc[r][jj];
+            if (a.dbg_a) a.dbg_a[tok * M + j] = val;
+          } else if (a.dbg_dlk) {
+            a.dbg_dlk[((size_t)bh * M + j) * n + n0 + t] = acc[r][jj];
           }
         }
       }
@@ -187,7 +201,7 @@ cdist_exp_kernel(const CdistArgs a) {
       // A^T rows of this tile (coalesced along the tokens).
       for (int idx = threadIdx.x; idx < M * kTile; idx += kThreads) {
         const int j = idx / kTile, t = idx % kTile;
-        if (t < valid) a.at[((size_t)bh * M + j) * n + n0 + t] = sOut[idx];
+        if (t < valid) a.at[((size_t)bh * M + j) * n + n0 + t] = sOut[j * kTileP + t];
       }
       // Per-landmark mean and M2 over the tile's valid tokens: warp w reduces rows
       // w, w+S, ..., one row per pass, with shuffles (fixed order: deterministic).
@@ -197,7 +211,7 @@ cdist_exp_kernel(const CdistArgs a) {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           const int t = lane + 32 * r;
-          if (t < valid) sum += sOut[j * kTile + t];
+          if (t < valid) sum += sOut[j * kTileP + t];
         }
         const float mean = warp_sum(sum) * inv_valid;
         float ss = 0.f;
@@ -205,7 +219,7 @@ cdist_exp_kernel(const CdistArgs a) {
         for (int r = 0; r < R; ++r) {
           const int t = lane + 32 * r;
           if (t < valid) {
-            const float dv = sOut[j * kTile + t] - mean;
+            const float dv = sOut[j * kTileP + t] - mean;
             ss = fmaf(dv, dv, ss);
           }
         }
@@ -216,29 +230,25 @@ cdist_exp_kernel(const CdistArgs a) {
           st[M + j] = ss;
         }
       }
-    } else {
-      // bv[jj][cc] += sum_t B[warp*S+jj][t] * V[t][lane+32cc]; padded tokens are zero.
-      const float* brow = sOut + warp * S * kTile;
-      for (int t4 = 0; t4 < kTile; t4 += 4) {
-        float vv[4][DC];
+    } else if (bv_on) {
+      // bv[jj][c] += sum_t B[lg*S+jj][t] * V[t][4cq+c]; padded tokens have B = 0 and V = 0.
+      const float* brow = sOut + bv_lg * S * kTileP;
+      for (int q = bv_ks; q < kTile / 4; q += KS) {
+        const int t = 4 * q;
+        float4 v4[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int cc = 0; cc < DC; ++cc) {
-            const int c = lane + 32 * cc;
-            vv[u][cc] = c < d ? sV[(t4 + u) * d + c] : 0.f;
-          }
+          v4[u] = *reinterpret_cast<const float4*>(&sV[(t + u) * d + 4 * bv_cq]);
 #pragma unroll
         for (int jj = 0; jj < S; ++jj) {
-          const float4 b4 = *reinterpret_cast<const float4*>(&brow[jj * kTile + t4]);
+          const float4 b4 = *reinterpret_cast<const float4*>(&brow[jj * kTileP + t]);
+          const float bu[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-          for (int cc = 0; cc < DC; ++cc) {
-            float t = bv[jj][cc];
-            t = fmaf(b4.x, vv[0][cc], t);
-            t = fmaf(b4.y, vv[1][cc], t);
-            t = fmaf(b4.z, vv[2][cc], t);
-            t = fmaf(b4.w, vv[3][cc], t);
-            bv[jj][cc] = t;
+          for (int u = 0; u < 4; ++u) {
+            bv[jj][0] = fmaf(bu[u], v4[u].x, bv[jj][0]);
+            bv[jj][1] = fmaf(bu[u], v4[u].y, bv[jj][1]);
+            bv[jj][2] = fmaf(bu[u], v4[u].z, bv[jj][2]);
+            bv[jj][3] = fmaf(bu[u], v4[u].w, bv[jj][3]);
           }
         }
       }
@@ -247,14 +257,22 @@ cdist_exp_kernel(const CdistArgs a) {
   }
 
   if (side == 1) {
+    // Combine the KS token classes (fixed order) through shared memory, then store the
+    // CTA's partial B V.  sX and sOut are free now: KS * M * d <= 128 * M floats fit there.
+    float* red = sX;
+    if (bv_on) {
+#pragma unroll
+      for (int jj = 0; jj < S; ++jj)
+        *reinterpret_cast<float4*>(&red[((size_t)bv_ks * M + bv_lg * S + jj) * d + 4 * bv_cq]) =
+            make_float4(bv[jj][0], bv[jj][1], bv[jj][2], bv[jj][3]);
+    }
+    __syncthreads();
     float* dst = a.bvp + ((size_t)bh * a.splits + split) * M * d;
-#pragma unroll
-    for (int jj = 0; jj < S; ++jj)
-#pragma unroll
-      for (int cc = 0; cc < DC; ++cc) {
-        const int c = lane + 32 * cc;
-        if (c < d) dst[(warp * S + jj) * d + c] = bv[jj][cc];
-      }
+    for (int i = threadIdx.x; i < M * d; i += kThreads) {
+      float sum = red[i];
+      for (int q = 1; q < KS; ++q) sum += red[(size_t)q * M * d + i];
+      dst[i] = sum;
+    }
   }
 }
 
@@ -296,7 +314,7 @@ const void* pick(int s, int d, bool bf16) {
 
 size_t cdist_smem_bytes(int s, int d, int tile) {
   const size_t m = (size_t)s * s;
-  return sizeof(float) * (m * d + (size_t)tile * d + m * tile + (size_t)tile * d);
+  return sizeof(float) * (m * d + (size_t)tile * d + m * (tile + 4) + (size_t)tile * d);
 }
 
 int cdist_tile_tokens() { return 32 * kRows; }

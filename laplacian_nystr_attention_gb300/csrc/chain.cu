@@ -139,27 +139,58 @@ output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
     sCoef[2 * m + j] = b;
   }
   __syncthreads();
-  // A^T tile -> whitened, landmark-major shared tile.  Loads are issued 16 per thread before
-  // any of them is consumed, so enough requests are in flight to cover DRAM latency.
-  constexpr int kBatch = 16;
-  const int total = m * tile;
-  for (int base = 0; base < total; base += kBatch * kOutThreads) {
-    float a[kBatch];
+  // A^T tile -> whitened, landmark-major shared tile.  With N % 4 == 0 every row piece is
+  // 16-byte aligned: tile/4 threads per row read float4s, several rows per thread in flight.
+  // Otherwise scalar loads, 16 issued per thread before any is consumed.
+  if ((n & 3) == 0) {
+    const int tq = tile >> 2;                 // float4 per row
+    const int rpp = kOutThreads / tq;         // rows per pass
+    const int r0 = threadIdx.x / tq, q4 = threadIdx.x % tq;
+    const int tok = n0 + 4 * q4;
+    if (r0 < rpp) {
+      constexpr int kRows = 4;
+      for (int jb = r0; jb < m; jb += kRows * rpp) {
+        float4 a[kRows];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = base + u * kOutThreads + threadIdx.x;
-      a[u] = 0.f;
-      if (i < total) {
-        const int j = i / tile, tok = n0 + i % tile;
-        if (tok < n) a[u] = at[((size_t)bh * m + j) * n + tok];
+        for (int u = 0; u < kRows; ++u) {
+          const int j = jb + u * rpp;
+          a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (j < m && tok < n)
+            a[u] = *reinterpret_cast<const float4*>(&at[((size_t)bh * m + j) * n + tok]);
+        }
+#pragma unroll
+        for (int u = 0; u < kRows; ++u) {
+          const int j = jb + u * rpp;
+          if (j < m) {
+            const float mean = sCoef[j], sc = sCoef[m + j], b = sCoef[2 * m + j];
+            *reinterpret_cast<float4*>(&sA[j * tile + 4 * q4]) =
+                make_float4((a[u].x - mean) * sc + b, (a[u].y - mean) * sc + b,
+                            (a[u].z - mean) * sc + b, (a[u].w - mean) * sc + b);
+          }
+        }
       }
     }
+  } else {
+    constexpr int kBatch = 16;
+    const int total = m * tile;
+    for (int base = 0; base < total; base += kBatch * kOutThreads) {
+      float a[kBatch];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = base + u * kOutThreads + threadIdx.x;
-      if (i < total) {
-        const int j = i / tile;
-        sA[i] = (a[u] - sCoef[j]) * sCoef[m + j] + sCoef[2 * m + j];
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = base + u * kOutThreads + threadIdx.x;
+        a[u] = 0.f;
+        if (i < total) {
+          const int j = i / tile, tok = n0 + i % tile;
+          if (tok < n) a[u] = at[((size_t)bh * m + j) * n + tok];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = base + u * kOutThreads + threadIdx.x;
+        if (i < total) {
+          const int j = i / tile;
+          sA[i] = (a[u] - sCoef[j]) * sCoef[m + j] + sCoef[2 * m + j];
+        }
       }
     }
   }

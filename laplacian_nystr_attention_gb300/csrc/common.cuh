@@ -95,8 +95,11 @@ cudaError_t output_configure(size_t smem);
 
 // ---- device helpers ---------------------------------------------------------------------
 __device__ __forceinline__ float laplacian_from_distance(float dist, float neg_log2e_over_lambda) {
-  // exp(-dist/lambda) as exp2(dist * (-log2(e)/lambda)); exp2f(0) == 1 exactly.
-  return exp2f(dist * neg_log2e_over_lambda);
+  // exp(-dist/lambda) = 2^(dist * (-log2(e)/lambda)), with the hardware base-2 exponential
+  // (relative error of a few ulp; results below 2^-126 flush to zero).
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(dist * neg_log2e_over_lambda));
+  return y;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t two) { return __uint_as_float(two << 16); }

@@ -17,8 +17,8 @@
 // (kappa(W) ~ 65 already does), whereas mirroring one of the two products stays within
 // rounding of the plain iteration.  With A symmetric both factors are row reads,
 // (A B)[i][j] = sum_k A[k][i] B[k][j]: one 128-bit load of A and one of B per 16 FMAs.
-// The k range of a block is split over KP adjacent lanes, combined with shuffles, so that
-// enough warps are in flight.
+// The k range of each product is cut into slices over groups of warps (see sym_product), so
+// that enough warps are in flight.
 #include "common.cuh"
 
 namespace lapl {
@@ -26,11 +26,14 @@ namespace {
 
 constexpr int kNsThreads = 1024;
 
-// Lanes per block: largest power of two <= 8 that divides MP and keeps blocks*KP <= threads.
-constexpr int lanes_per_block(int mp, int blocks) {
-  return (mp % 8 == 0 && blocks * 8 <= kNsThreads) ? 8
-       : (mp % 4 == 0 && blocks * 4 <= kNsThreads) ? 4
-       : (mp % 2 == 0 && blocks * 2 <= kNsThreads) ? 2 : 1;
+// Work split of one product over the CTA: the blocks of the product are laid out 32 per warp
+// in row-major (bi, bj) order, so a warp's 128-bit reads of A hit at most a few distinct
+// addresses (broadcast) and its reads of B are contiguous rows; the k range is cut into KS
+// slices, one per group of warps, whose partial 4x4 tiles are summed through shared memory in
+// slice order.
+constexpr int slices_for(int mp, int blocks) {
+  return (mp % 4 == 0 && ((blocks + 31) / 32) * 4 <= kNsThreads / 32) ? 4
+       : (mp % 2 == 0 && ((blocks + 31) / 32) * 2 <= kNsThreads / 32) ? 2 : 1;
 }
 
 template <int S>
@@ -40,29 +43,54 @@ struct NsShape {
   static constexpr int NT = MP / 4;                  // 4x4 blocks per side
   static constexpr int NFULL = NT * NT;              // all blocks (P = W X)
   static constexpr int NB = NT * (NT + 1) / 2;       // upper-triangle blocks (X update)
-  static constexpr int KP1 = lanes_per_block(MP, NFULL);
-  static constexpr int KP2 = lanes_per_block(MP, NB);
+  static constexpr int KS1 = slices_for(MP, NFULL);
+  static constexpr int KS2 = slices_for(MP, NB);
+  static constexpr int PART_FLOATS = (KS1 * NFULL > KS2 * NB ? KS1 * NFULL : KS2 * NB) * 16;
 };
 
+// Block index -> (bi, bj): row-major over all blocks, or over the upper triangle.
+template <int NT, bool kUpper>
+__device__ __forceinline__ void block_of(int item, int& bi, int& bj) {
+  if constexpr (kUpper) {
+    int b = 0, rem = item;
+    while (rem >= NT - b) {
+      rem -= NT - b;
+      ++b;
+    }
+    bi = b;
+    bj = b + rem;
+  } else {
+    bi = item / NT;
+    bj = item % NT;
+  }
+}
+
 // C = A B for symmetric A (MP x MP, row-major): (A B)[i][j] = sum_k A[k][i] B[k][j].
-// kMirror: C = 2 Xs - A B on an upper-triangle block, written to (i, j) and (j, i).
-// Otherwise: C = A B on any block.
-template <int MP, int KP, bool kMirror>
+// kMirror: the blocks are the upper triangle and C = 2 Xs - A B is written to (i, j) and
+// (j, i).  Otherwise every block is computed and C = A B.  Ends with a __syncthreads().
+template <int MP, int NBLK, int KS, bool kMirror>
 __device__ __forceinline__ void sym_product(const float* __restrict__ A,
                                             const float* __restrict__ B,
                                             const float* __restrict__ Xs, float* __restrict__ C,
-                                            int bi, int bj, int kp, bool active) {
-  constexpr int KLEN = MP / KP;
-  float acc[4][4];
+                                            float* __restrict__ part) {
+  constexpr int NT = MP / 4;
+  constexpr int WPS = (NBLK + 31) / 32;          // warps per k slice
+  constexpr int KL = MP / KS;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ks = warp / WPS;
+  const int item = (warp % WPS) * 32 + lane;
+  if (ks < KS && item < NBLK) {
+    int bi, bj;
+    block_of<NT, kMirror>(item, bi, bj);
+    float acc[4][4];
 #pragma unroll
-  for (int r = 0; r < 4; ++r)
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
-  if (active) {
-    const float* a = A + (kp * KLEN) * MP + 4 * bi;
-    const float* b = B + (kp * KLEN) * MP + 4 * bj;
+      for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+    const float* a = A + (ks * KL) * MP + 4 * bi;
+    const float* b = B + (ks * KL) * MP + 4 * bj;
 #pragma unroll
-    for (int kk = 0; kk < KLEN; ++kk) {
+    for (int kk = 0; kk < KL; ++kk) {
       const float4 av = *reinterpret_cast<const float4*>(a + kk * MP);
       const float4 bv = *reinterpret_cast<const float4*>(b + kk * MP);
       const float ar[4] = {av.x, av.y, av.z, av.w};
@@ -72,32 +100,31 @@ __device__ __forceinline__ void sym_product(const float* __restrict__ A,
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(ar[r], br[c], acc[r][c]);
     }
+    float4* dst = reinterpret_cast<float4*>(part) + ((size_t)ks * NBLK + item) * 4;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) dst[r] = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
   }
+  __syncthreads();
+  // Sum the KS slices of every output element, in slice order.
+  for (int e = threadIdx.x; e < NBLK * 16; e += kNsThreads) {
+    const int item2 = e >> 4, rc = e & 15;
+    float v = part[e];
 #pragma unroll
-  for (int o = 1; o < KP; o <<= 1)
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[r][c] += __shfl_xor_sync(0xffffffffu, acc[r][c], o);
-  if (active && kp == 0) {
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      if constexpr (kMirror) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int i = 4 * bi + r, j = 4 * bj + c;
-          if (bi < bj || r <= c) {
-            const float v = 2.f * Xs[i * MP + j] - acc[r][c];
-            C[i * MP + j] = v;
-            C[j * MP + i] = v;
-          }
-        }
-      } else {
-        *reinterpret_cast<float4*>(&C[(4 * bi + r) * MP + 4 * bj]) =
-            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+    for (int q = 1; q < KS; ++q) v += part[(size_t)q * NBLK * 16 + e];
+    int bi, bj;
+    block_of<NT, kMirror>(item2, bi, bj);
+    const int i = 4 * bi + (rc >> 2), j = 4 * bj + (rc & 3);
+    if constexpr (kMirror) {
+      if (bi < bj || (rc >> 2) <= (rc & 3)) {
+        const float y = 2.f * Xs[i * MP + j] - v;
+        C[i * MP + j] = y;
+        C[j * MP + i] = y;
       }
+    } else {
+      C[i * MP + j] = v;
     }
   }
+  __syncthreads();
 }
 
 template <int S>
@@ -106,8 +133,7 @@ ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
                   float* __restrict__ dbg_dll, float* __restrict__ dbg_w,
                   float* __restrict__ dbg_x, int d, int T, float eps, float c_exp) {
   using Sh = NsShape<S>;
-  constexpr int M = Sh::M, MP = Sh::MP, NT = Sh::NT;
-  constexpr int KP1 = Sh::KP1, KP2 = Sh::KP2;
+  constexpr int M = Sh::M, MP = Sh::MP;
   extern __shared__ float4 smem_ns4[];
   float* smem = reinterpret_cast<float*>(smem_ns4);
   const long bh = blockIdx.x;
@@ -116,7 +142,8 @@ ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
   float* P = X + MP * MP;
   float* Y = P + MP * MP;
   float* red = Y + MP * MP;      // column sums [64], row sums [64], scale
-  float* sL = red + 132;         // [M][d]
+  float* part = red + 132;       // partial 4x4 tiles of the k slices
+  float* sL = part + Sh::PART_FLOATS;   // [M][d]
 
   const float4* Lg = reinterpret_cast<const float4*>(landmarks + (size_t)bh * M * d);
   for (int i = threadIdx.x; i < (M * d) >> 2; i += kNsThreads)
@@ -130,8 +157,8 @@ ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
     if (i < M && k < M) {
       float dist = 0.f;
       for (int c = 0; c < d; ++c) dist += fabsf(sL[i * d + c] - sL[k * d + c]);
-      w = laplacian_from_distance(dist, c_exp);
-      if (i == k) w += eps;
+      // k(x, x) = 1 exactly: D_LL[i][i] = 0 and exp(0) = 1.
+      w = (i == k) ? 1.f + eps : laplacian_from_distance(dist, c_exp);
       const size_t o = ((size_t)bh * M + i) * M + k;
       if (dbg_dll) dbg_dll[o] = dist;
       if (dbg_w) dbg_w[o] = w;
@@ -167,28 +194,11 @@ ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
     X[idx] = W[k * MP + i] / scale;     // X0 = W^T / (|W|_1 |W|_inf)
   }
 
-  // Blocks of this lane group: any block for P = W X, an upper-triangle block for the update.
-  const int item1 = threadIdx.x / KP1, kp1 = threadIdx.x % KP1;
-  const bool act1 = item1 < Sh::NFULL;
-  const int bi1 = act1 ? item1 / NT : 0, bj1 = act1 ? item1 % NT : 0;
-  const int item2 = threadIdx.x / KP2, kp2 = threadIdx.x % KP2;
-  const bool act2 = item2 < Sh::NB;
-  int bi2 = 0, bj2 = 0;
-  if (act2) {
-    int rem = item2;
-    while (rem >= NT - bi2) {
-      rem -= NT - bi2;
-      ++bi2;
-    }
-    bj2 = bi2 + rem;
-  }
   __syncthreads();
 
   for (int t = 0; t < T; ++t) {
-    sym_product<MP, KP1, false>(W, X, nullptr, P, bi1, bj1, kp1, act1);  // P = W X
-    __syncthreads();
-    sym_product<MP, KP2, true>(X, P, X, Y, bi2, bj2, kp2, act2);         // Y = 2X - X P
-    __syncthreads();
+    sym_product<MP, Sh::NFULL, Sh::KS1, false>(W, X, nullptr, P, part);   // P = W X
+    sym_product<MP, Sh::NB, Sh::KS2, true>(X, P, X, Y, part);             // Y = 2X - X P
     float* tmp = X; X = Y; Y = tmp;
   }
 
@@ -219,9 +229,24 @@ const void* pick_ns(int s) {
 
 }  // namespace
 
+template <int S>
+size_t ns_smem_of(int d) {
+  using Sh = NsShape<S>;
+  return sizeof(float) * (4 * (size_t)Sh::MP * Sh::MP + 132 + Sh::PART_FLOATS + (size_t)Sh::M * d);
+}
+
 size_t ns_smem_bytes(int m, int d) {
-  const int mp = (m + 3) & ~3;
-  return sizeof(float) * (4 * (size_t)mp * mp + 132 + (size_t)m * d);
+  switch (m) {
+    case 1: return ns_smem_of<1>(d);
+    case 4: return ns_smem_of<2>(d);
+    case 9: return ns_smem_of<3>(d);
+    case 16: return ns_smem_of<4>(d);
+    case 25: return ns_smem_of<5>(d);
+    case 36: return ns_smem_of<6>(d);
+    case 49: return ns_smem_of<7>(d);
+    case 64: return ns_smem_of<8>(d);
+    default: return 0;
+  }
 }
 
 cudaError_t ns_configure(int s, size_t smem) {

@@ -32,18 +32,29 @@ pool_landmarks_kernel(const void* __restrict__ kin, float* __restrict__ landmark
 
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (slice < slices) {
-    for (int w = slice; w < win; w += slices) {
-      const int r = jr * ph + w / pw;
-      const int c = jc * pw + w % pw;
-      const size_t tok = (size_t)bh * n + (size_t)r * grid_w + c;
-      float4 x;
-      if constexpr (kBf16) {
-        const uint2 raw = reinterpret_cast<const uint2*>(kin)[(tok * d >> 2) + quad];
-        x = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
-      } else {
-        x = reinterpret_cast<const float4*>(kin)[(tok * d >> 2) + quad];
+    // Four window positions per pass: their loads are issued before any is summed.
+    for (int w0 = slice; w0 < win; w0 += 4 * slices) {
+      float4 x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int w = w0 + u * slices;
+        x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (w < win) {
+          const int r = jr * ph + w / pw;
+          const int c = jc * pw + w % pw;
+          const size_t tok = (size_t)bh * n + (size_t)r * grid_w + c;
+          if constexpr (kBf16) {
+            const uint2 raw = reinterpret_cast<const uint2*>(kin)[(tok * d >> 2) + quad];
+            x[u] = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
+          } else {
+            x[u] = reinterpret_cast<const float4*>(kin)[(tok * d >> 2) + quad];
+          }
+        }
       }
-      acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc.x += x[u].x; acc.y += x[u].y; acc.z += x[u].z; acc.w += x[u].w;
+      }
     }
     smem_pool[slice * d4 + quad] = acc;
   }
