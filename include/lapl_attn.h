@@ -137,11 +137,12 @@ lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void
 
 /*
  * Stage timing, a profiling aid.  After lapl_attn_set_timing(h, 1) every forward records CUDA
- * events (created here, host-owned) around its five stages: on the launching stream for
- * pooling, distances, finish and output, on the side stream for Newton-Schulz.
+ * events (created here, host-owned) around its six stages: on the launching stream for
+ * pooling, distances, B V, finish and output, on the side stream for Newton-Schulz.
  * lapl_attn_stage_times() waits for the events of the last forward (it synchronises the host
  * with them) and writes the elapsed milliseconds of
- *   ms[0] pooling, ms[1] Newton-Schulz, ms[2] distance kernel, ms[3] finish, ms[4] output.
+ *   ms[0] pooling, ms[1] Newton-Schulz, ms[2] distance kernel, ms[3] B V, ms[4] finish,
+ *   ms[5] output.
  * LAPL_ERR_INVALID_ARG if timing is off or no forward ran since it was switched on.
  */
 lapl_status lapl_attn_set_timing(lapl_attn_handle h, int enable);

@@ -157,7 +157,7 @@ def lapl_attn_forward_noalloc(handle, q, k, v, bias, out, stream) -> None:
            "lapl_attn_forward_noalloc", handle)
 
 
-STAGES = ("pool", "newton_schulz", "cdist", "finish", "output")
+STAGES = ("pool", "newton_schulz", "cdist", "bv", "finish", "output")
 
 
 def lapl_attn_set_timing(handle, enable: bool) -> None:
@@ -165,7 +165,7 @@ def lapl_attn_set_timing(handle, enable: bool) -> None:
 
 
 def lapl_attn_stage_times(handle) -> dict:
-    ms = (ctypes.c_float * 5)()
+    ms = (ctypes.c_float * len(STAGES))()
     _check(LIB.lapl_attn_stage_times(handle, ms), "lapl_attn_stage_times", handle)
     return dict(zip(STAGES, [float(x) for x in ms]))
 

@@ -3,7 +3,8 @@
 //
 //   K1 pool      L = avg-pool(K)                          stream
 //   fork ------------------------------------------------ side stream: K3 Newton-Schulz (W, X)
-//   K2 cdist     A^T + tile stats (queries), B V partials (keys)        stream
+//   K2 cdist     A^T + run statistics (queries), B^T (keys)            stream
+//   K2b bv       B V partials per token split                           stream
 //   join <----------------------------------------------- (needs X)
 //   K4 finish    mean/rstd, B V, M = X (B V)              stream
 //   K5 output    O = whiten(A) M                          stream
@@ -11,6 +12,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <new>
 
 #include "common.cuh"
@@ -47,6 +49,7 @@ lapl_status validate(const lapl_attn_config* c) {
   const long long n = (long long)c->grid_h * c->grid_w;
   if (n > (1LL << 24)) return LAPL_ERR_UNSUPPORTED;
   if ((long long)c->batch * c->heads > (1LL << 24)) return LAPL_ERR_UNSUPPORTED;
+  if ((long long)c->batch * c->heads * n > (1LL << 40)) return LAPL_ERR_UNSUPPORTED;
   return LAPL_OK;
 }
 
@@ -59,6 +62,18 @@ bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 
 size_t elem_bytes(int dtype) { return dtype == LAPL_BF16 ? 2 : 4; }
 
+// Split of the distance kernel over `ctas` persistent CTAs (see Partition).  runs_q bounds
+// how many CTA ranges can meet one head's query tokens (slots of the per-run statistics).
+void setup_cdist_partition(Geometry& g, int ctas) {
+  Partition& pt = g.cd_part;
+  pt.uq = (long long)g.bh * g.n;
+  pt.total = 2 * pt.uq;
+  if (ctas > pt.total) ctas = (int)std::max<long long>(pt.total, 1);
+  pt.ctas = ctas;
+  pt.q = pt.total / ctas;
+  pt.rem = (int)(pt.total % ctas);
+  g.cd_runs_q = pt.q > 0 ? (int)std::min<long long>((g.n + pt.q - 1) / pt.q + 1, ctas) : ctas;
+}
 }  // namespace
 }  // namespace lapl
 
@@ -111,12 +126,10 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
     return LAPL_ERR_CUDA;
   }
 
-  // Distance kernel: 128-token tiles; CTAs of one head walk consecutive tiles so that the
-  // grid is about one wave of resident CTAs.
+  // Distance kernel: persistent CTAs, one wave of resident CTAs, balanced ranges.
   g.cd_tile = cdist_tile_tokens();
   g.cd_rows = g.cd_tile / 32;
-  g.cd_tiles = (g.n + g.cd_tile - 1) / g.cd_tile;
-  g.cd_smem = cdist_smem_bytes(g.s, g.d, g.cd_tile);
+  g.cd_smem = cdist_smem_bytes(g.s, g.d, g.cd_tile, cfg->in_dtype == LAPL_BF16);
   int per_sm = 1;
   e = cdist_configure(g.s, g.d, cfg->in_dtype == LAPL_BF16, g.cd_smem, &per_sm);
   if (e == cudaSuccess) {
@@ -134,14 +147,32 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
     delete p;
     return LAPL_ERR_CUDA;
   }
+  if (e == cudaSuccess) {
+    g.bv_threads = bv_threads(g.m, g.d);
+    g.bv_smem = bv_smem_bytes(g.m, g.d, g.bv_threads);
+    e = bv_configure(g.bv_smem);
+  }
+  if (e != cudaSuccess) {
+    set_error(p, e, "create/configure");
+    delete p;
+    return LAPL_ERR_CUDA;
+  }
   if (per_sm < 1) per_sm = 1;
-  const long long target = (long long)p->num_sms * per_sm;
-  const long long total_tiles = 2LL * (g.bh > 0 ? g.bh : 1) * g.cd_tiles;
-  long long tps = (total_tiles + target - 1) / target;
-  if (tps < 1) tps = 1;
-  if (tps > g.cd_tiles) tps = g.cd_tiles;
-  g.cd_tiles_per_split = (int)tps;
-  g.cd_splits = (int)((g.cd_tiles + tps - 1) / tps);
+  {
+    // B V: about two CTAs per SM in total, whole 128-token chunks per CTA.
+    const long long bh1 = g.bh > 0 ? g.bh : 1;
+    const int tiles = (g.n + bv_tile_tokens() - 1) / bv_tile_tokens();
+    long long want = (2LL * p->num_sms + bh1 - 1) / bh1;
+    want = std::max<long long>(1, std::min<long long>(want, tiles));
+    g.bv_tiles_per_split = (int)((tiles + want - 1) / want);
+    g.bv_splits = (tiles + g.bv_tiles_per_split - 1) / g.bv_tiles_per_split;
+  }
+  {
+    // No more CTAs than chunks of work.
+    const long long chunks = 2LL * (g.bh > 0 ? g.bh : 1) * ((g.n + g.cd_tile - 1) / g.cd_tile);
+    const long long ctas = std::min<long long>((long long)p->num_sms * per_sm, chunks);
+    setup_cdist_partition(g, (int)std::max<long long>(ctas, 1));
+  }
 
   // Workspace regions.
   WorkspaceLayout& w = p->ws;
@@ -155,8 +186,9 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   w.landmarks = take(bh * m * d);
   w.x = take(bh * m * m);
   w.at = take(bh * m * n);
-  w.stats = take(bh * g.cd_tiles * 2 * m);
-  w.bvp = take(bh * g.cd_splits * m * d);
+  w.bt = take(bh * m * n);
+  w.stats = take(bh * g.cd_runs_q * 3 * m);
+  w.bvp = take(bh * g.bv_splits * m * d);
   w.mmat = take(bh * m * d);
   w.mu = take(bh * m);
   w.rstd = take(bh * m);
@@ -205,6 +237,7 @@ static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k,
   float* L = reinterpret_cast<float*>(ws + p->ws.landmarks);
   float* X = reinterpret_cast<float*>(ws + p->ws.x);
   float* At = reinterpret_cast<float*>(ws + p->ws.at);
+  float* Bt = reinterpret_cast<float*>(ws + p->ws.bt);
   float* stats = reinterpret_cast<float*>(ws + p->ws.stats);
   float* bvp = reinterpret_cast<float*>(ws + p->ws.bvp);
   float* M = reinterpret_cast<float*>(ws + p->ws.mmat);
@@ -235,8 +268,10 @@ static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k,
   LAPL_TRY(launch_ns(*p, L, X, D.d_ll, D.w, D.x, p->side_stream), "forward/newton-schulz");
   LAPL_MARK(6, p->side_stream);
   LAPL_TRY(cudaEventRecord(p->ev_join, p->side_stream), "forward/join");
-  LAPL_TRY(launch_cdist(*p, q, k, v, L, At, stats, bvp, D.d_ql, D.d_lk, D.a, st), "forward/cdist");
+  LAPL_TRY(launch_cdist(*p, q, k, v, L, At, Bt, stats, D.d_ql, D.d_lk, D.a, st), "forward/cdist");
   LAPL_MARK(2, st);
+  LAPL_TRY(launch_bv(*p, Bt, v, bvp, st), "forward/bv");
+  LAPL_MARK(7, st);
   LAPL_TRY(cudaStreamWaitEvent(st, p->ev_join, 0), "forward/join-wait");
   LAPL_TRY(launch_finish(*p, stats, bvp, X, M, mu, rstd, D.mu, D.rstd, D.bv, D.m, st),
            "forward/finish");
@@ -334,7 +369,7 @@ lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void
 lapl_status lapl_attn_set_timing(lapl_attn_handle h, int enable) {
   if (!h) return LAPL_ERR_INVALID_ARG;
   if (enable && !h->ev_stage[0]) {
-    for (int i = 0; i < 7; ++i) {
+    for (int i = 0; i < 8; ++i) {
       cudaError_t e = cudaEventCreate(&h->ev_stage[i]);
       if (e != cudaSuccess) {
         set_error(h, e, "set_timing");
@@ -351,8 +386,8 @@ lapl_status lapl_attn_stage_times(lapl_attn_handle h, float* ms) {
   if (!h || !ms || !h->timing || !h->timed_once) return LAPL_ERR_INVALID_ARG;
   cudaError_t e = cudaEventSynchronize(h->ev_stage[4]);
   if (e == cudaSuccess) e = cudaEventSynchronize(h->ev_stage[6]);
-  const int pairs[5][2] = {{0, 1}, {5, 6}, {1, 2}, {2, 3}, {3, 4}};
-  for (int i = 0; i < 5 && e == cudaSuccess; ++i)
+  const int pairs[6][2] = {{0, 1}, {5, 6}, {1, 2}, {2, 7}, {7, 3}, {3, 4}};
+  for (int i = 0; i < 6 && e == cudaSuccess; ++i)
     e = cudaEventElapsedTime(&ms[i], h->ev_stage[pairs[i][0]], h->ev_stage[pairs[i][1]]);
   if (e != cudaSuccess) {
     set_error(h, e, "stage_times");
@@ -361,11 +396,11 @@ lapl_status lapl_attn_stage_times(lapl_attn_handle h, float* ms) {
   return LAPL_OK;
 }
 
-int lapl_attn_kernels_per_forward(lapl_attn_handle h) { return (h && h->geo.bh > 0) ? 5 : 0; }
+int lapl_attn_kernels_per_forward(lapl_attn_handle h) { return (h && h->geo.bh > 0) ? 6 : 0; }
 
 lapl_status lapl_attn_destroy(lapl_attn_handle h) {
   if (!h) return LAPL_OK;
-  for (int i = 0; i < 7; ++i)
+  for (int i = 0; i < 8; ++i)
     if (h->ev_stage[i]) cudaEventDestroy(h->ev_stage[i]);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);

@@ -1,0 +1,25 @@
+// cdist_d32.cu -- instantiations of the distance kernel for head dim 32.
+#include "cdist_kernel.cuh"
+
+namespace lapl {
+namespace cdist_impl {
+
+template <bool kBf16>
+static const void* pick_s(int s) {
+  switch (s) {
+    case 1: return reinterpret_cast<const void*>(&cdist_exp_kernel<1, 4, 32, kBf16>);
+    case 2: return reinterpret_cast<const void*>(&cdist_exp_kernel<2, 4, 32, kBf16>);
+    case 3: return reinterpret_cast<const void*>(&cdist_exp_kernel<3, 4, 32, kBf16>);
+    case 4: return reinterpret_cast<const void*>(&cdist_exp_kernel<4, 4, 32, kBf16>);
+    case 5: return reinterpret_cast<const void*>(&cdist_exp_kernel<5, 4, 32, kBf16>);
+    case 6: return reinterpret_cast<const void*>(&cdist_exp_kernel<6, 4, 32, kBf16>);
+    case 7: return reinterpret_cast<const void*>(&cdist_exp_kernel<7, 4, 32, kBf16>);
+    case 8: return reinterpret_cast<const void*>(&cdist_exp_kernel<8, 4, 32, kBf16>);
+    default: return nullptr;
+  }
+}
+
+const void* kernel_d32(int s, bool bf16) { return bf16 ? pick_s<true>(s) : pick_s<false>(s); }
+
+}  // namespace cdist_impl
+}  // namespace lapl

@@ -6,6 +6,9 @@
 //    column, taken over the N tokens of the (batch, head) slice (variance divides by N);
 //  * low-rank product without the N x N matrix (Chinese page, 2.2), evaluated right to left.
 //
+// bv_kernel (one CTA per (batch, head, token split)):
+//   partial B V of the split's tokens from B^T [BH, m, N] and V, register-tiled on the CUDA
+//   cores (4 landmarks x 4 channels per thread, 8 shared loads per 64 FMAs).
 // finish_kernel (one CTA per (batch, head)):
 //   merges the per-tile (mean, M2) of the distance kernel in tile order (Chan's pairwise
 //   update), reduces the per-split partials of B V in split order, and forms M = X (B V).
@@ -18,6 +21,115 @@
 namespace lapl {
 namespace {
 
+constexpr int kBvTile = 128;          // tokens per staged chunk
+constexpr int kBvTileP = kBvTile + 4;  // padded row of the B^T chunk
+
+template <bool kBf16>
+__global__ void __launch_bounds__(512)
+bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __restrict__ bvp,
+          int m, int d, int n, int tiles_per_split, int splits) {
+  extern __shared__ float4 smem_bv4[];
+  float* smem = reinterpret_cast<float*>(smem_bv4);
+  const int nthreads = blockDim.x;
+  const int mp4 = (m + 3) & ~3;
+  float* sB = smem;                       // [mp4][kBvTileP] kernel values, landmark-major
+  float* sV = sB + mp4 * kBvTileP;        // [kBvTile][d]
+  float* red = sV + kBvTile * d;          // [16][nthreads]
+  const long bh = blockIdx.x / splits;
+  const int sp = blockIdx.x % splits;
+  const int tiles = (n + kBvTile - 1) / kBvTile;
+  const int t_begin = sp * tiles_per_split;
+  const int t_end = min(tiles, t_begin + tiles_per_split);
+
+  // Thread (ks, lg, cq): landmarks 4lg..4lg+3, channels 4cq..4cq+3, token quads == ks mod KS.
+  const int cqn = d >> 2, lgn = mp4 >> 2;
+  const int set = lgn * cqn;
+  const int KS = max(1, nthreads / set);
+  const int ks = threadIdx.x / set, lg = (threadIdx.x % set) / cqn, cq = threadIdx.x % cqn;
+  const bool on = ks < KS;
+  float acc[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+
+  // Padding rows of the landmark dimension stay zero.
+  for (int i = threadIdx.x; i < (mp4 - m) * kBvTileP; i += nthreads) sB[m * kBvTileP + i] = 0.f;
+
+  const bool vec = (n & 3) == 0;
+  for (int tile = t_begin; tile < t_end; ++tile) {
+    const int n0 = tile * kBvTile;
+    const int valid = min(kBvTile, n - n0);
+    // B^T rows j, tokens n0 .. n0+127 (zero beyond N).
+    if (vec) {
+      for (int i = threadIdx.x; i < m * (kBvTile / 4); i += nthreads) {
+        const int j = i / (kBvTile / 4), q4 = i % (kBvTile / 4);
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (4 * q4 < valid)
+          x = *reinterpret_cast<const float4*>(&bt[((size_t)bh * m + j) * n + n0 + 4 * q4]);
+        *reinterpret_cast<float4*>(&sB[j * kBvTileP + 4 * q4]) = x;
+      }
+    } else {
+      for (int i = threadIdx.x; i < m * kBvTile; i += nthreads) {
+        const int j = i / kBvTile, t = i % kBvTile;
+        sB[j * kBvTileP + t] = t < valid ? bt[((size_t)bh * m + j) * n + n0 + t] : 0.f;
+      }
+    }
+    // V rows n0 .. n0+127 as fp32 (zero beyond N).
+    for (int i = threadIdx.x; i < kBvTile * cqn; i += nthreads) {
+      const int t = i / cqn, c4 = i % cqn;
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < valid) {
+        const size_t e = ((size_t)bh * n + n0 + t) * d + 4 * c4;
+        if constexpr (kBf16) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(vin) + e);
+          x = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
+        } else {
+          x = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(vin) + e);
+        }
+      }
+      *reinterpret_cast<float4*>(&sV[t * d + 4 * c4]) = x;
+    }
+    __syncthreads();
+    if (on) {
+      for (int q = ks; q < kBvTile / 4; q += KS) {
+        const int t = 4 * q;
+        float4 b4[4], v4[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          b4[r] = *reinterpret_cast<const float4*>(&sB[(4 * lg + r) * kBvTileP + t]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          v4[u] = *reinterpret_cast<const float4*>(&sV[(t + u) * d + 4 * cq]);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float bu[4] = {b4[r].x, b4[r].y, b4[r].z, b4[r].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            acc[r][0] = fmaf(bu[u], v4[u].x, acc[r][0]);
+            acc[r][1] = fmaf(bu[u], v4[u].y, acc[r][1]);
+            acc[r][2] = fmaf(bu[u], v4[u].z, acc[r][2]);
+            acc[r][3] = fmaf(bu[u], v4[u].w, acc[r][3]);
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // Combine the KS token classes in order, store the split's partial B V.
+#pragma unroll
+  for (int e = 0; e < 16; ++e) red[e * nthreads + threadIdx.x] = on ? acc[e >> 2][e & 3] : 0.f;
+  __syncthreads();
+  float* dst = bvp + ((size_t)bh * splits + sp) * m * d;
+  for (int i = threadIdx.x; i < m * d; i += nthreads) {
+    const int j = i / d, c = i % d;
+    const int lgi = j >> 2, r = j & 3, cqi = c >> 2, cc = c & 3;
+    float sum = 0.f;
+    for (int q = 0; q < KS; ++q) sum += red[(r * 4 + cc) * nthreads + q * set + lgi * cqn + cqi];
+    dst[i] = sum;
+  }
+}
+
 constexpr int kFinishThreads = 256;
 constexpr int kFinishCols = 8;     // value columns per finish CTA
 
@@ -28,7 +140,7 @@ finish_kernel(const float* __restrict__ stats, const float* __restrict__ bvp,
               const float* __restrict__ xg, float* __restrict__ mmat, float* __restrict__ mu,
               float* __restrict__ rstd, float* __restrict__ dbg_mu, float* __restrict__ dbg_rstd,
               float* __restrict__ dbg_bv, float* __restrict__ dbg_m, int m, int d, int n,
-              int tiles, int tile_tokens, int splits, float delta) {
+              const Partition pt, int runs_q, int bv_splits, float delta) {
   extern __shared__ float4 smem_fin4[];
   float* smem = reinterpret_cast<float*>(smem_fin4);
   const int chunks = (d + kFinishCols - 1) / kFinishCols;
@@ -41,51 +153,42 @@ finish_kernel(const float* __restrict__ stats, const float* __restrict__ bvp,
 
   for (int i = threadIdx.x; i < m * m; i += kFinishThreads) sX[i] = xg[(size_t)bh * m * m + i];
 
-  // B V columns of this chunk: sum over splits in split order (loads issued 4 at a time).
+  // Statistics slots of this head: one per distance-kernel CTA range that met its query
+  // tokens, in CTA order.
+  const long long fq = (long long)bh * n;
+  const int nq = part_owner(pt, fq + n - 1) - part_owner(pt, fq) + 1;
+
+  // B V columns of this chunk: sum over the token splits in order (loads batched by 4).
   for (int i = threadIdx.x; i < m * cw; i += kFinishThreads) {
     const int j = i / cw, c = c0 + i % cw;
-    const float* src = bvp + (size_t)bh * splits * m * d + (size_t)j * d + c;
+    const float* src = bvp + (size_t)bh * bv_splits * m * d + (size_t)j * d + c;
     const size_t stride = (size_t)m * d;
     float acc = 0.f;
     int sp = 0;
-    for (; sp + 4 <= splits; sp += 4) {
+    for (; sp + 4 <= bv_splits; sp += 4) {
       const float a0 = src[(sp + 0) * stride], a1 = src[(sp + 1) * stride];
       const float a2 = src[(sp + 2) * stride], a3 = src[(sp + 3) * stride];
       acc += a0; acc += a1; acc += a2; acc += a3;
     }
-    for (; sp < splits; ++sp) acc += src[sp * stride];
+    for (; sp < bv_splits; ++sp) acc += src[sp * stride];
     sBV[j * kFinishCols + (c - c0)] = acc;
     if (dbg_bv) dbg_bv[((size_t)bh * m + j) * d + c] = acc;
   }
 
-  // Column statistics (chunk 0): Chan's merge of (count, mean, M2) over the tiles in tile
-  // order; the loads of 8 tiles are issued before their merges.
+  // Column statistics (chunk 0): Chan's merge of the slots' (count, mean, M2), in order.
   if (cc == 0) {
     for (int j = threadIdx.x; j < m; j += kFinishThreads) {
-      const float* st = stats + (size_t)bh * tiles * 2 * m;
+      const float* st = stats + (size_t)bh * runs_q * 3 * m;
       float cnt = 0.f, mean = 0.f, m2 = 0.f;
-      for (int t0 = 0; t0 < tiles; t0 += 8) {
-        float mb[8], m2b[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          mb[u] = 0.f;
-          m2b[u] = 0.f;
-          if (t0 + u < tiles) {
-            mb[u] = st[(size_t)(t0 + u) * 2 * m + j];
-            m2b[u] = st[(size_t)(t0 + u) * 2 * m + m + j];
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          if (t0 + u < tiles) {
-            const float nb = (float)min(tile_tokens, n - (t0 + u) * tile_tokens);
-            const float tot = cnt + nb;
-            const float dlt = mb[u] - mean;
-            mean += dlt * (nb / tot);
-            m2 += m2b[u] + dlt * dlt * (cnt * nb / tot);
-            cnt = tot;
-          }
-        }
+      for (int sp = 0; sp < nq; ++sp) {
+        const float nb = st[(size_t)sp * 3 * m + j];
+        const float mb = st[(size_t)sp * 3 * m + m + j];
+        const float m2b = st[(size_t)sp * 3 * m + 2 * m + j];
+        const float tot = cnt + nb;
+        const float dlt = mb - mean;
+        mean += dlt * (nb / tot);
+        m2 += m2b + dlt * dlt * (cnt * nb / tot);
+        cnt = tot;
       }
       const float var = m2 / (float)n;
       const float rs = 1.f / sqrtf(var + delta);
@@ -258,6 +361,38 @@ cudaError_t output_configure(size_t smem) {
                               (int)smem);
 }
 
+size_t bv_smem_bytes(int m, int d, int threads) {
+  const int mp4 = (m + 3) & ~3;
+  return sizeof(float) * ((size_t)mp4 * kBvTileP + (size_t)kBvTile * d + 16 * (size_t)threads);
+}
+
+int bv_threads(int m, int d) {
+  const int set = ((m + 3) / 4) * (d / 4);
+  return set > 256 ? 512 : 256;
+}
+
+int bv_tile_tokens() { return kBvTile; }
+
+cudaError_t bv_configure(size_t smem) {
+  cudaError_t e = cudaFuncSetAttribute(bv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(bv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+cudaError_t launch_bv(const lapl_attn_plan& p, const float* bt, const void* v, float* bvp,
+                      cudaStream_t st) {
+  const Geometry& g = p.geo;
+  const unsigned grid = (unsigned)(g.bh * g.bv_splits);
+  if (p.cfg.in_dtype == LAPL_BF16)
+    bv_kernel<true><<<grid, g.bv_threads, g.bv_smem, st>>>(bt, v, bvp, g.m, g.d, g.n,
+                                                           g.bv_tiles_per_split, g.bv_splits);
+  else
+    bv_kernel<false><<<grid, g.bv_threads, g.bv_smem, st>>>(bt, v, bvp, g.m, g.d, g.n,
+                                                            g.bv_tiles_per_split, g.bv_splits);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_finish(const lapl_attn_plan& p, const float* stats, const float* bvp,
                           const float* x, float* mmat, float* mu, float* rstd, float* dbg_mu,
                           float* dbg_rstd, float* dbg_bv, float* dbg_m, cudaStream_t st) {
@@ -265,7 +400,7 @@ cudaError_t launch_finish(const lapl_attn_plan& p, const float* stats, const flo
   const int chunks = (g.d + kFinishCols - 1) / kFinishCols;
   finish_kernel<<<(unsigned)(g.bh * chunks), kFinishThreads, finish_smem_bytes(g.m, g.d), st>>>(
       stats, bvp, x, mmat, mu, rstd, dbg_mu, dbg_rstd, dbg_bv, dbg_m, g.m, g.d, g.n,
-      g.cd_tiles, g.cd_tile, g.cd_splits, p.cfg.delta);
+      g.cd_part, g.cd_runs_q, g.bv_splits, p.cfg.delta);
   return cudaGetLastError();
 }
 

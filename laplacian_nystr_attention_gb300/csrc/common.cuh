@@ -20,13 +20,38 @@ constexpr size_t kAlign = 256;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Balanced split of the distance kernel's work.  Positions 0 .. 2*BH*N-1 list every (side,
+// head, token): query tokens first (position bh*N + n), then key tokens (BH*N + bh*N + n).  The
+// `ctas` CTAs take consecutive ranges of q or q+1 positions (q = total / ctas; the first
+// total % ctas CTAs take one more), so every CTA gets the same work up to one token.
+struct Partition {
+  long long uq;      // query positions, BH * N (key positions follow)
+  long long total;   // 2 * uq
+  long long q;       // total / ctas
+  int rem;           // total % ctas
+  int ctas;
+};
+
+// First position of CTA c (c == ctas gives the end of the list).
+__host__ __device__ inline long long part_start(const Partition& pt, int c) {
+  return (long long)c * pt.q + (c < pt.rem ? c : pt.rem);
+}
+
+// The CTA whose range holds position x (for q > 0).
+__host__ __device__ inline int part_owner(const Partition& pt, long long x) {
+  const long long big = (long long)pt.rem * (pt.q + 1);
+  if (x < big) return (int)(x / (pt.q + 1));
+  return pt.rem + (int)((x - big) / pt.q);
+}
+
 // Offsets (bytes) of the workspace regions for one configuration.  All fp32.
 struct WorkspaceLayout {
   size_t landmarks;    // [BH, m, d]         pooled keys L
   size_t x;            // [BH, m, m]         Newton-Schulz result X
   size_t at;           // [BH, m, N]         A = k(Q, L), landmark-major (A transposed)
-  size_t stats;        // [BH, tiles, 2, m]  per-tile (mean, M2) of the columns of A
-  size_t bvp;          // [BH, splits, m, d] per-split partial sums of B V
+  size_t bt;           // [BH, m, N]         B = k(L, K)
+  size_t stats;        // [BH, runs_q, 3, m]  per-CTA-run (count, mean, M2) of the columns of A
+  size_t bvp;          // [BH, bv_splits, m, d]  per-split partial sums of B V
   size_t mmat;         // [BH, m, d]         M = X (B V)
   size_t mu;           // [BH, m]            column means
   size_t rstd;         // [BH, m]            1 / sqrt(var + delta)
@@ -38,10 +63,13 @@ struct Geometry {
   int s, m, d, n;          // landmark grid side, landmarks, head dim, tokens per head
   long bh;                 // batch * heads
   int cd_rows;             // tokens per thread in the distance kernel
-  int cd_tile;             // tokens per distance tile = 32 * cd_rows
-  int cd_tiles;            // tiles per head and side
-  int cd_tiles_per_split;  // consecutive tiles one CTA walks through
-  int cd_splits;           // CTAs per head and side
+  int cd_tile;             // tokens per distance chunk = 32 * cd_rows
+  Partition cd_part;       // balanced split over cd_part.ctas persistent CTAs
+  int cd_runs_q;           // most CTAs whose range meets one head's query tokens
+  int bv_splits;           // B V: CTAs per head
+  int bv_tiles_per_split;  // B V: 128-token chunks per CTA
+  int bv_threads;
+  size_t bv_smem;
   size_t cd_smem;          // dynamic shared memory of the distance kernel
   int out_tile;            // tokens per output-kernel CTA
   int out_threads;
@@ -63,7 +91,8 @@ struct lapl_attn_plan {
   cudaEvent_t ev_fork, ev_join;
   bool timing;                  // record stage events in forward
   bool timed_once;              // a forward ran with timing on
-  cudaEvent_t ev_stage[7];      // start, pool, cdist, finish, output ends; ns start, ns end
+  cudaEvent_t ev_stage[8];      // start, pool, cdist, finish, output ends; ns start, ns end;
+                                // bv end
   char last_error[256];
 };
 
@@ -75,8 +104,10 @@ cudaError_t launch_pool(const lapl_attn_plan& p, const void* k, float* landmarks
 cudaError_t launch_ns(const lapl_attn_plan& p, const float* landmarks, float* x, float* dbg_dll,
                       float* dbg_w, float* dbg_x, cudaStream_t st);
 cudaError_t launch_cdist(const lapl_attn_plan& p, const void* q, const void* k, const void* v,
-                         const float* landmarks, float* at, float* stats, float* bvp,
+                         const float* landmarks, float* at, float* bt, float* stats,
                          float* dbg_dql, float* dbg_dlk, float* dbg_a, cudaStream_t st);
+cudaError_t launch_bv(const lapl_attn_plan& p, const float* bt, const void* v, float* bvp,
+                      cudaStream_t st);
 cudaError_t launch_finish(const lapl_attn_plan& p, const float* stats, const float* bvp,
                           const float* x, float* mmat, float* mu, float* rstd, float* dbg_mu,
                           float* dbg_rstd, float* dbg_bv, float* dbg_m, cudaStream_t st);
@@ -85,13 +116,17 @@ cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float*
                           cudaStream_t st);
 
 // Shared-memory sizes, needed at plan time to size grids and opt in to > 48 KB.
-size_t cdist_smem_bytes(int s, int d, int tile);
+size_t cdist_smem_bytes(int s, int d, int tile, bool bf16);
 cudaError_t cdist_configure(int s, int d, bool bf16, size_t smem, int* ctas_per_sm);
 int cdist_tile_tokens();
 size_t ns_smem_bytes(int m, int d);
 cudaError_t ns_configure(int s, size_t smem);
 size_t output_smem_bytes(int m, int d, int tile);
 cudaError_t output_configure(size_t smem);
+size_t bv_smem_bytes(int m, int d, int threads);
+int bv_threads(int m, int d);
+int bv_tile_tokens();
+cudaError_t bv_configure(size_t smem);
 
 // ---- device helpers ---------------------------------------------------------------------
 __device__ __forceinline__ float laplacian_from_distance(float dist, float neg_log2e_over_lambda) {

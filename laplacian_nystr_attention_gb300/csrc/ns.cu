@@ -7,121 +7,147 @@
 // row sum), exactly T steps.
 //
 // One CTA per (batch, head); the m x m matrices (m <= 64) live in shared memory, zero-padded
-// to MP = a multiple of 4 (the padding stays exactly zero through the iteration).
+// to 64 x 64 (the padding stays exactly zero through the iteration).
 //
 // Symmetry.  W is symmetric, X0 = W^T / c is symmetric, and X_{t+1} = X_t (2I - W X_t) is
 // symmetric whenever X_t is a polynomial in W.  The update X <- 2X - X P is therefore evaluated
-// on the upper-triangle 4 x 4 blocks only and mirrored, so every iterate is exactly symmetric.
+// on the upper-triangle tiles only and mirrored, so every iterate is exactly symmetric.
 // P = W X is computed in full: mirroring it as well drops its commutator part [W, X]/2, and in
 // fp32 that error grows through the slow first phase of the iteration until it diverges
 // (kappa(W) ~ 65 already does), whereas mirroring one of the two products stays within
 // rounding of the plain iteration.  With A symmetric both factors are row reads,
-// (A B)[i][j] = sum_k A[k][i] B[k][j]: one 128-bit load of A and one of B per 16 FMAs.
-// The k range of each product is cut into slices over groups of warps (see sym_product), so
-// that enough warps are in flight.
+// (A B)[i][j] = sum_k A[k][i] B[k][j].
+//
+// Products.  Matrices are stored 64 x 64 (zero padding, row stride kMS).  A warp owns a 32 x 32
+// output tile and a quarter of the k range; lane (rq, cq) = (lane / 8, lane % 8) owns rows
+// 8rq..8rq+7 and columns 4cq..4cq+3 of it.  Per k a warp issues two 128-bit reads of A (all 8
+// lanes of a quarter-warp read the same address) and one of B (a quarter reads 128 contiguous
+// bytes): 8 shared-memory wavefronts per 32 FMAs per lane.  The k quarters meet through shared
+// memory in a lane-major (conflict-free) layout.
 #include "common.cuh"
 
 namespace lapl {
 namespace {
 
-constexpr int kNsThreads = 1024;
+constexpr int kNsThreads = 512;
 
-// Work split of one product over the CTA: the blocks of the product are laid out 32 per warp
-// in row-major (bi, bj) order, so a warp's 128-bit reads of A hit at most a few distinct
-// addresses (broadcast) and its reads of B are contiguous rows; the k range is cut into KS
-// slices, one per group of warps, whose partial 4x4 tiles are summed through shared memory in
-// slice order.
-constexpr int slices_for(int mp, int blocks) {
-  return (mp % 4 == 0 && ((blocks + 31) / 32) * 4 <= kNsThreads / 32) ? 4
-       : (mp % 2 == 0 && ((blocks + 31) / 32) * 2 <= kNsThreads / 32) ? 2 : 1;
-}
+constexpr int kMS = 68;   // stored row stride: 64 columns (padded) + 4, 16-byte aligned, and
+                          // column-direction stores spread over more banks than with 64
 
 template <int S>
 struct NsShape {
   static constexpr int M = S * S;
-  static constexpr int MP = (M + 3) & ~3;
-  static constexpr int NT = MP / 4;                  // 4x4 blocks per side
-  static constexpr int NFULL = NT * NT;              // all blocks (P = W X)
-  static constexpr int NB = NT * (NT + 1) / 2;       // upper-triangle blocks (X update)
-  static constexpr int KS1 = slices_for(MP, NFULL);
-  static constexpr int KS2 = slices_for(MP, NB);
-  static constexpr int PART_FLOATS = (KS1 * NFULL > KS2 * NB ? KS1 * NFULL : KS2 * NB) * 16;
+  static constexpr int MK = (M + 3) & ~3;            // k range actually summed
+  static constexpr int NWT = (M + 31) / 32;          // 32x32 warp tiles per side (1 or 2)
+  static constexpr int PART_FLOATS = 4 * 3 * 32 * 32;  // 4 tiles x 3 upper slices x 32 x 32
 };
 
-// Block index -> (bi, bj): row-major over all blocks, or over the upper triangle.
-template <int NT, bool kUpper>
-__device__ __forceinline__ void block_of(int item, int& bi, int& bj) {
-  if constexpr (kUpper) {
-    int b = 0, rem = item;
-    while (rem >= NT - b) {
-      rem -= NT - b;
-      ++b;
-    }
-    bi = b;
-    bj = b + rem;
-  } else {
-    bi = item / NT;
-    bj = item % NT;
-  }
-}
-
-// C = A B for symmetric A (MP x MP, row-major): (A B)[i][j] = sum_k A[k][i] B[k][j].
-// kMirror: the blocks are the upper triangle and C = 2 Xs - A B is written to (i, j) and
-// (j, i).  Otherwise every block is computed and C = A B.  Ends with a __syncthreads().
-template <int MP, int NBLK, int KS, bool kMirror>
+// C = A B for symmetric A (row stride kMS): (A B)[i][j] = sum_k A[k][i] B[k][j].
+// kMirror: only warp tiles tr <= tc, C = 2 Xs - A B written to (i, j) and (j, i) (on a diagonal
+// tile only the entries with i <= j, so C is exactly symmetric).  Otherwise every tile, C = A B.
+// Warp w: tile w % NTILES, k quarter w / NTILES (the four slice-0 warps land on four different
+// sub-partitions).  Ends with a __syncthreads().
+template <int MK, int NWT, bool kMirror>
 __device__ __forceinline__ void sym_product(const float* __restrict__ A,
                                             const float* __restrict__ B,
                                             const float* __restrict__ Xs, float* __restrict__ C,
                                             float* __restrict__ part) {
-  constexpr int NT = MP / 4;
-  constexpr int WPS = (NBLK + 31) / 32;          // warps per k slice
-  constexpr int KL = MP / KS;
+  constexpr int NTILES = kMirror ? NWT * (NWT + 1) / 2 : NWT * NWT;
+  constexpr int KS = 4;
+  constexpr int KQ = MK / KS;                        // MK is a multiple of 4
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ks = warp / WPS;
-  const int item = (warp % WPS) * 32 + lane;
-  if (ks < KS && item < NBLK) {
-    int bi, bj;
-    block_of<NT, kMirror>(item, bi, bj);
-    float acc[4][4];
+  const int tile = warp % NTILES, ks = warp / NTILES;
+  const bool active = ks < KS;
+  int tr = 0, tc = 0;
+  if (kMirror) {
+    tr = (tile == 2) ? 1 : 0;                        // tiles (0,0), (0,1), (1,1)
+    tc = (tile >= 1) ? 1 : 0;
+  } else {
+    tr = tile / NWT;
+    tc = tile % NWT;
+  }
+  const int rq = lane >> 3, cq = lane & 7;
+  const int r0 = 32 * tr + 8 * rq, c0 = 32 * tc + 4 * cq;
+  float acc[8][4];
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+  for (int r = 0; r < 8; ++r)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
-    const float* a = A + (ks * KL) * MP + 4 * bi;
-    const float* b = B + (ks * KL) * MP + 4 * bj;
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+  if (active) {
+    const float* a = A + (ks * KQ) * kMS + r0;
+    const float* b = B + (ks * KQ) * kMS + c0;
+    // Operands of step kk+1 are loaded while the 32 FMAs of step kk issue.
+    float4 a0 = *reinterpret_cast<const float4*>(a);
+    float4 a1 = *reinterpret_cast<const float4*>(a + 4);
+    float4 bv = *reinterpret_cast<const float4*>(b);
 #pragma unroll
-    for (int kk = 0; kk < KL; ++kk) {
-      const float4 av = *reinterpret_cast<const float4*>(a + kk * MP);
-      const float4 bv = *reinterpret_cast<const float4*>(b + kk * MP);
-      const float ar[4] = {av.x, av.y, av.z, av.w};
+    for (int kk = 0; kk < KQ; ++kk) {
+      const int kn = kk + 1 < KQ ? kk + 1 : kk;
+      const float4 na0 = *reinterpret_cast<const float4*>(a + kn * kMS);
+      const float4 na1 = *reinterpret_cast<const float4*>(a + kn * kMS + 4);
+      const float4 nbv = *reinterpret_cast<const float4*>(b + kn * kMS);
+      const float ar[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
       const float br[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+      for (int r = 0; r < 8; ++r)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(ar[r], br[c], acc[r][c]);
+      a0 = na0;
+      a1 = na1;
+      bv = nbv;
     }
-    float4* dst = reinterpret_cast<float4*>(part) + ((size_t)ks * NBLK + item) * 4;
+    if (ks > 0) {
 #pragma unroll
-    for (int r = 0; r < 4; ++r) dst[r] = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      for (int e = 0; e < 32; ++e)
+        part[(((ks - 1) * NTILES + tile) * 32 + e) * 32 + lane] = acc[e >> 2][e & 3];
+    }
   }
   __syncthreads();
-  // Sum the KS slices of every output element, in slice order.
-  for (int e = threadIdx.x; e < NBLK * 16; e += kNsThreads) {
-    const int item2 = e >> 4, rc = e & 15;
-    float v = part[e];
+  if (active && ks == 0) {
 #pragma unroll
-    for (int q = 1; q < KS; ++q) v += part[(size_t)q * NBLK * 16 + e];
-    int bi, bj;
-    block_of<NT, kMirror>(item2, bi, bj);
-    const int i = 4 * bi + (rc >> 2), j = 4 * bj + (rc & 3);
+    for (int q = 1; q < KS; ++q)
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        acc[e >> 2][e & 3] += part[(((q - 1) * NTILES + tile) * 32 + e) * 32 + lane];
     if constexpr (kMirror) {
-      if (bi < bj || (rc >> 2) <= (rc & 3)) {
-        const float y = 2.f * Xs[i * MP + j] - v;
-        C[i * MP + j] = y;
-        C[j * MP + i] = y;
+      float v[8][4];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float4 x4 = *reinterpret_cast<const float4*>(&Xs[(r0 + r) * kMS + c0]);
+        v[r][0] = 2.f * x4.x - acc[r][0];
+        v[r][1] = 2.f * x4.y - acc[r][1];
+        v[r][2] = 2.f * x4.z - acc[r][2];
+        v[r][3] = 2.f * x4.w - acc[r][3];
+      }
+      if (tr == tc) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int i = r0 + r, j = c0 + c;
+            if (i <= j) {
+              C[i * kMS + j] = v[r][c];
+              C[j * kMS + i] = v[r][c];
+            }
+          }
+      } else {
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          *reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]) =
+              make_float4(v[r][0], v[r][1], v[r][2], v[r][3]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          *reinterpret_cast<float4*>(&C[(c0 + c) * kMS + r0]) =
+              make_float4(v[0][c], v[1][c], v[2][c], v[3][c]);
+          *reinterpret_cast<float4*>(&C[(c0 + c) * kMS + r0 + 4]) =
+              make_float4(v[4][c], v[5][c], v[6][c], v[7][c]);
+        }
       }
     } else {
-      C[i * MP + j] = v;
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        *reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]) =
+            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
     }
   }
   __syncthreads();
@@ -133,72 +159,71 @@ ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
                   float* __restrict__ dbg_dll, float* __restrict__ dbg_w,
                   float* __restrict__ dbg_x, int d, int T, float eps, float c_exp) {
   using Sh = NsShape<S>;
-  constexpr int M = Sh::M, MP = Sh::MP;
+  constexpr int M = Sh::M, MP = kMS;
   extern __shared__ float4 smem_ns4[];
   float* smem = reinterpret_cast<float*>(smem_ns4);
   const long bh = blockIdx.x;
-  float* W = smem;               // [MP][MP]
-  float* X = W + MP * MP;
-  float* P = X + MP * MP;
-  float* Y = P + MP * MP;
-  float* red = Y + MP * MP;      // column sums [64], row sums [64], scale
+  float* W = smem;               // [64][MP]
+  float* X = W + 64 * MP;
+  float* P = X + 64 * MP;
+  float* Y = P + 64 * MP;
+  float* red = Y + 64 * MP;      // column sums [64], scale at [128]
   float* part = red + 132;       // partial 4x4 tiles of the k slices
-  float* sL = part + Sh::PART_FLOATS;   // [M][d]
+  float* sL = part + Sh::PART_FLOATS;   // [d][64], channel-major
 
-  const float4* Lg = reinterpret_cast<const float4*>(landmarks + (size_t)bh * M * d);
-  for (int i = threadIdx.x; i < (M * d) >> 2; i += kNsThreads)
-    reinterpret_cast<float4*>(sL)[i] = Lg[i];
+  // Landmarks, stored channel-major (sL[c * 64 + j]): in the distance loop below a warp reads
+  // one broadcast value and 32 consecutive values per channel, free of bank conflicts.
+  const float* Lg = landmarks + (size_t)bh * M * d;
+  for (int i = threadIdx.x; i < M * d; i += kNsThreads) {
+    const int j = i / d, c = i % d;
+    sL[c * 64 + j] = Lg[i];
+  }
   __syncthreads();
 
-  // W = exp(-D_LL / lambda) + eps I (exactly symmetric: |a-b| == |b-a| and the same order).
-  for (int idx = threadIdx.x; idx < MP * MP; idx += kNsThreads) {
-    const int i = idx / MP, k = idx % MP;
+  // W = exp(-D_LL / lambda) + eps I, zero outside m x m.  Exactly symmetric: |a-b| == |b-a|
+  // and both orders sum the channels in the same order.
+  for (int idx = threadIdx.x; idx < 64 * 64; idx += kNsThreads) {
+    const int i = idx >> 6, k = idx & 63;
     float w = 0.f;
     if (i < M && k < M) {
       float dist = 0.f;
-      for (int c = 0; c < d; ++c) dist += fabsf(sL[i * d + c] - sL[k * d + c]);
+      for (int c = 0; c < d; ++c) dist += fabsf(sL[c * 64 + i] - sL[c * 64 + k]);
       // k(x, x) = 1 exactly: D_LL[i][i] = 0 and exp(0) = 1.
       w = (i == k) ? 1.f + eps : laplacian_from_distance(dist, c_exp);
       const size_t o = ((size_t)bh * M + i) * M + k;
       if (dbg_dll) dbg_dll[o] = dist;
       if (dbg_w) dbg_w[o] = w;
     }
-    W[idx] = w;
+    W[i * MP + k] = w;
   }
   __syncthreads();
 
-  // |W|_1 (largest absolute column sum) and |W|_inf (largest absolute row sum).
+  // |W|_1 = largest absolute column sum.  W is exactly symmetric, so row j holds the same
+  // values in the same order as column j and |W|_inf (largest absolute row sum) equals |W|_1
+  // bit for bit.
   if (threadIdx.x < M) {
     const int j = threadIdx.x;
-    float cs = 0.f, rs = 0.f;
-    for (int i = 0; i < M; ++i) {
-      cs += fabsf(W[i * MP + j]);
-      rs += fabsf(W[j * MP + i]);
-    }
+    float cs = 0.f;
+    for (int i = 0; i < M; ++i) cs += fabsf(W[i * MP + j]);
     red[j] = cs;
-    red[64 + j] = rs;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    float n1 = 0.f, ninf = 0.f;
-    for (int j = 0; j < M; ++j) {
-      n1 = fmaxf(n1, red[j]);
-      ninf = fmaxf(ninf, red[64 + j]);
-    }
-    red[128] = n1 * ninf;
+    float n1 = 0.f;
+    for (int j = 0; j < M; ++j) n1 = fmaxf(n1, red[j]);
+    red[128] = n1 * n1;            // |W|_1 |W|_inf
   }
   __syncthreads();
   const float scale = red[128];
-  for (int idx = threadIdx.x; idx < MP * MP; idx += kNsThreads) {
-    const int i = idx / MP, k = idx % MP;
-    X[idx] = W[k * MP + i] / scale;     // X0 = W^T / (|W|_1 |W|_inf)
+  for (int idx = threadIdx.x; idx < 64 * 64; idx += kNsThreads) {
+    const int i = idx >> 6, k = idx & 63;
+    X[i * MP + k] = W[i * MP + k] / scale;     // X0 = W^T / (|W|_1 |W|_inf); W^T == W exactly
   }
-
   __syncthreads();
 
   for (int t = 0; t < T; ++t) {
-    sym_product<MP, Sh::NFULL, Sh::KS1, false>(W, X, nullptr, P, part);   // P = W X
-    sym_product<MP, Sh::NB, Sh::KS2, true>(X, P, X, Y, part);             // Y = 2X - X P
+    sym_product<Sh::MK, Sh::NWT, false>(W, X, nullptr, P, part);   // P = W X
+    sym_product<Sh::MK, Sh::NWT, true>(X, P, X, Y, part);          // Y = 2X - X P
     float* tmp = X; X = Y; Y = tmp;
   }
 
@@ -232,7 +257,7 @@ const void* pick_ns(int s) {
 template <int S>
 size_t ns_smem_of(int d) {
   using Sh = NsShape<S>;
-  return sizeof(float) * (4 * (size_t)Sh::MP * Sh::MP + 132 + Sh::PART_FLOATS + (size_t)Sh::M * d);
+  return sizeof(float) * (4 * 64 * (size_t)kMS + 132 + Sh::PART_FLOATS + 64 * (size_t)d);
 }
 
 size_t ns_smem_bytes(int m, int d) {
