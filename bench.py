@@ -38,9 +38,11 @@ FLUSH_BYTES = 512 * 1024 * 1024
 
 # DRAM traffic (read + write bytes) of one launch of the distance kernel, from an ncu capture
 # (summary: profiles/cdist_exp_kernel_stage1_f32.md).  Valid only for the source it was taken
-# on: the sha256 of csrc/cdist.cu is compared and the figure reported as null on mismatch.
-CDIST_TRAFFIC = {"stage1_f32": None}
-CDIST_TRAFFIC_SHA = None
+# on: the sha256 of the kernel's source files is compared and the figure reported as null on
+# mismatch.
+CDIST_TRAFFIC = {"stage1_f32": 13034752 + 8704}
+CDIST_TRAFFIC_SHA = "c5aa25c668fb493e035297ecc32688a163ce16ec9f30af75a2704c230de11f96"
+CDIST_SOURCES = ["cdist_kernel.cuh", "cdist.cu", "cdist_d32.cu"]
 
 
 def parse():
@@ -313,8 +315,10 @@ def run_ours(args, w):
     sm_max = float(peaks.get("sm_max_mhz", 2070.0))
     peak = fp32_peak_tflops(props.multi_processor_count, sm_max)
     achieved = cdist_ops_per_launch(w) / (stage_ms["cdist"] / 1e3) / 1e12
-    src_sha = hashlib.sha256(open(os.path.join(ROOT, "laplacian_nystr_attention_gb300", "csrc",
-                                               "cdist.cu"), "rb").read()).hexdigest()
+    hs = hashlib.sha256()
+    for f in CDIST_SOURCES:
+        hs.update(open(os.path.join(ROOT, "laplacian_nystr_attention_gb300", "csrc", f), "rb").read())
+    src_sha = hs.hexdigest()
     traffic = CDIST_TRAFFIC.get(w.name) if CDIST_TRAFFIC_SHA == src_sha else None
     clk = clocks.summary()
     line = {

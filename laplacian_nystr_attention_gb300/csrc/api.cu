@@ -19,7 +19,6 @@
 
 namespace lapl {
 
-size_t finish_smem_bytes(int m, int d);
 int output_tile_tokens(int d);
 
 namespace {
@@ -133,8 +132,14 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   int per_sm = 1;
   e = cdist_configure(g.s, g.d, cfg->in_dtype == LAPL_BF16, g.cd_smem, &per_sm);
   if (e == cudaSuccess) {
+    // Newton-Schulz is the longest dependency chain of the forward.  With few heads its CTAs
+    // ask for (almost) a whole SM's shared memory, so no other kernel's CTA shares their SM.
+    g.ns_exclusive = g.bh <= p->num_sms / 4;
+    int smem_max = 0;
+    e = cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
     g.ns_smem = ns_smem_bytes(g.m, g.d);
-    e = ns_configure(g.s, g.ns_smem);
+    if (e == cudaSuccess && g.ns_exclusive && (size_t)smem_max > g.ns_smem) g.ns_smem = smem_max;
+    if (e == cudaSuccess) e = ns_configure(g.s, g.ns_smem);
   }
   if (e == cudaSuccess) {
     g.out_tile = output_tile_tokens(g.d);
@@ -170,8 +175,20 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   {
     // No more CTAs than chunks of work.
     const long long chunks = 2LL * (g.bh > 0 ? g.bh : 1) * ((g.n + g.cd_tile - 1) / g.cd_tile);
-    const long long ctas = std::min<long long>((long long)p->num_sms * per_sm, chunks);
+    // When the Newton-Schulz solve needs few SMs (one CTA per head, at most a quarter of the
+    // SMs), it gets those SMs to itself: the distance kernel's persistent grid covers the
+    // others (see ns_exclusive).
+    long long slots = (long long)p->num_sms * per_sm;
+    if (g.ns_exclusive) slots -= g.bh * per_sm;
+    const long long ctas = std::min<long long>(slots, chunks);
     setup_cdist_partition(g, (int)std::max<long long>(ctas, 1));
+    g.fin_smem = finish_smem_bytes(g.m, g.cd_runs_q, g.bv_splits);
+    e = finish_configure(g.fin_smem);
+    if (e != cudaSuccess) {
+      set_error(p, e, "create/configure-finish");
+      delete p;
+      return LAPL_ERR_CUDA;
+    }
   }
 
   // Workspace regions.
@@ -194,7 +211,11 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   w.rstd = take(bh * m);
   w.total = off;
 
-  e = cudaStreamCreateWithFlags(&p->side_stream, cudaStreamNonBlocking);
+  // The side stream (Newton-Schulz, the longest dependency chain) gets the highest priority.
+  int prio_least = 0, prio_greatest = 0;
+  e = cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest);
+  if (e == cudaSuccess)
+    e = cudaStreamCreateWithPriority(&p->side_stream, cudaStreamNonBlocking, prio_greatest);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming);
   if (e != cudaSuccess) {

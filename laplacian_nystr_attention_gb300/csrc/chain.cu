@@ -133,8 +133,15 @@ bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __r
 constexpr int kFinishThreads = 256;
 constexpr int kFinishCols = 8;     // value columns per finish CTA
 
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+  const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(src) : "memory");
+}
+
 // grid (BH * column chunks): CTA (bh, cc) reduces the B V partials of columns
 // [cc*8, cc*8+8) and forms those columns of M = X (B V); chunk 0 also merges the statistics.
+// Every global read is issued up front as an asynchronous copy, so the kernel waits for one
+// round trip to memory instead of one per dependent load.
 __global__ void __launch_bounds__(kFinishThreads)
 finish_kernel(const float* __restrict__ stats, const float* __restrict__ bvp,
               const float* __restrict__ xg, float* __restrict__ mmat, float* __restrict__ mu,
@@ -148,42 +155,49 @@ finish_kernel(const float* __restrict__ stats, const float* __restrict__ bvp,
   const int cc = blockIdx.x % chunks;
   const int c0 = cc * kFinishCols;
   const int cw = min(kFinishCols, d - c0);
-  float* sX = smem;             // [m][m]
-  float* sBV = sX + m * m;      // [m][kFinishCols]
-
-  for (int i = threadIdx.x; i < m * m; i += kFinishThreads) sX[i] = xg[(size_t)bh * m * m + i];
 
   // Statistics slots of this head: one per distance-kernel CTA range that met its query
   // tokens, in CTA order.
   const long long fq = (long long)bh * n;
-  const int nq = part_owner(pt, fq + n - 1) - part_owner(pt, fq) + 1;
+  const int slot0 = part_owner(pt, fq);
+  const int nq = part_owner(pt, fq + n - 1) - slot0 + 1;
 
-  // B V columns of this chunk: sum over the token splits in order (loads batched by 4).
+  float* sX = smem;                                 // [m][m]
+  float* sP = sX + m * m;                           // [bv_splits][m][kFinishCols] partials
+  float* sS = sP + (size_t)bv_splits * m * kFinishCols;   // [nq][3][m] statistics slots
+  float* sBV = sS + (size_t)runs_q * 3 * m;         // [m][kFinishCols]
+
+  for (int i = threadIdx.x; i < m * m; i += kFinishThreads) cp_async4(&sX[i], &xg[(size_t)bh * m * m + i]);
+  const float* pbase = bvp + (size_t)bh * bv_splits * m * d + c0;
+  for (int i = threadIdx.x; i < bv_splits * m * cw; i += kFinishThreads) {
+    const int sp = i / (m * cw), rest = i % (m * cw);
+    const int j = rest / cw, c = rest % cw;
+    cp_async4(&sP[(sp * m + j) * kFinishCols + c], &pbase[((size_t)sp * m + j) * d + c]);
+  }
+  if (cc == 0) {
+    const float* sbase = stats + (size_t)bh * runs_q * 3 * m;
+    for (int i = threadIdx.x; i < nq * 3 * m; i += kFinishThreads) cp_async4(&sS[i], &sbase[i]);
+  }
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+  __syncthreads();
+
+  // B V columns of this chunk: sum over the token splits in order.
   for (int i = threadIdx.x; i < m * cw; i += kFinishThreads) {
-    const int j = i / cw, c = c0 + i % cw;
-    const float* src = bvp + (size_t)bh * bv_splits * m * d + (size_t)j * d + c;
-    const size_t stride = (size_t)m * d;
+    const int j = i / cw, c = i % cw;
     float acc = 0.f;
-    int sp = 0;
-    for (; sp + 4 <= bv_splits; sp += 4) {
-      const float a0 = src[(sp + 0) * stride], a1 = src[(sp + 1) * stride];
-      const float a2 = src[(sp + 2) * stride], a3 = src[(sp + 3) * stride];
-      acc += a0; acc += a1; acc += a2; acc += a3;
-    }
-    for (; sp < bv_splits; ++sp) acc += src[sp * stride];
-    sBV[j * kFinishCols + (c - c0)] = acc;
-    if (dbg_bv) dbg_bv[((size_t)bh * m + j) * d + c] = acc;
+    for (int sp = 0; sp < bv_splits; ++sp) acc += sP[(sp * m + j) * kFinishCols + c];
+    sBV[j * kFinishCols + c] = acc;
+    if (dbg_bv) dbg_bv[((size_t)bh * m + j) * d + c0 + c] = acc;
   }
 
   // Column statistics (chunk 0): Chan's merge of the slots' (count, mean, M2), in order.
   if (cc == 0) {
     for (int j = threadIdx.x; j < m; j += kFinishThreads) {
-      const float* st = stats + (size_t)bh * runs_q * 3 * m;
       float cnt = 0.f, mean = 0.f, m2 = 0.f;
       for (int sp = 0; sp < nq; ++sp) {
-        const float nb = st[(size_t)sp * 3 * m + j];
-        const float mb = st[(size_t)sp * 3 * m + m + j];
-        const float m2b = st[(size_t)sp * 3 * m + 2 * m + j];
+        const float nb = sS[sp * 3 * m + j];
+        const float mb = sS[sp * 3 * m + m + j];
+        const float m2b = sS[sp * 3 * m + 2 * m + j];
         const float tot = cnt + nb;
         const float dlt = mb - mean;
         mean += dlt * (nb / tot);
@@ -339,9 +353,13 @@ output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
 
 }  // namespace
 
-size_t finish_smem_bytes(int m, int d) {
-  (void)d;
-  return sizeof(float) * ((size_t)m * m + (size_t)m * kFinishCols);
+size_t finish_smem_bytes(int m, int runs_q, int bv_splits) {
+  return sizeof(float) * ((size_t)m * m + (size_t)bv_splits * m * kFinishCols +
+                          (size_t)runs_q * 3 * m + (size_t)m * kFinishCols);
+}
+
+cudaError_t finish_configure(size_t smem) {
+  return cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
 int output_tile_tokens(int d) {
@@ -398,7 +416,7 @@ cudaError_t launch_finish(const lapl_attn_plan& p, const float* stats, const flo
                           float* dbg_rstd, float* dbg_bv, float* dbg_m, cudaStream_t st) {
   const Geometry& g = p.geo;
   const int chunks = (g.d + kFinishCols - 1) / kFinishCols;
-  finish_kernel<<<(unsigned)(g.bh * chunks), kFinishThreads, finish_smem_bytes(g.m, g.d), st>>>(
+  finish_kernel<<<(unsigned)(g.bh * chunks), kFinishThreads, g.fin_smem, st>>>(
       stats, bvp, x, mmat, mu, rstd, dbg_mu, dbg_rstd, dbg_bv, dbg_m, g.m, g.d, g.n,
       g.cd_part, g.cd_runs_q, g.bv_splits, p.cfg.delta);
   return cudaGetLastError();

@@ -70,11 +70,13 @@ struct Geometry {
   int bv_tiles_per_split;  // B V: 128-token chunks per CTA
   int bv_threads;
   size_t bv_smem;
+  size_t fin_smem;
   size_t cd_smem;          // dynamic shared memory of the distance kernel
   int out_tile;            // tokens per output-kernel CTA
   int out_threads;
   size_t out_smem;
   size_t ns_smem;
+  bool ns_exclusive;       // Newton-Schulz CTAs own their SMs (few heads)
   size_t pool_threads;
 };
 
@@ -127,6 +129,8 @@ size_t bv_smem_bytes(int m, int d, int threads);
 int bv_threads(int m, int d);
 int bv_tile_tokens();
 cudaError_t bv_configure(size_t smem);
+size_t finish_smem_bytes(int m, int runs_q, int bv_splits);
+cudaError_t finish_configure(size_t smem);
 
 // ---- device helpers ---------------------------------------------------------------------
 __device__ __forceinline__ float laplacian_from_distance(float dist, float neg_log2e_over_lambda) {
