@@ -154,7 +154,7 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   }
   if (e == cudaSuccess) {
     g.bv_threads = bv_threads(g.m, g.d);
-    g.bv_smem = bv_smem_bytes(g.m, g.d, g.bv_threads);
+    g.bv_smem = bv_smem_bytes(g.m, g.d, g.bv_threads, cfg->in_dtype == LAPL_BF16);
     e = bv_configure(g.bv_smem);
   }
   if (e != cudaSuccess) {

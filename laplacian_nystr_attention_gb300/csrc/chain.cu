@@ -24,6 +24,19 @@ namespace {
 constexpr int kBvTile = 128;          // tokens per staged chunk
 constexpr int kBvTileP = kBvTile + 4;  // padded row of the B^T chunk
 
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, int src_bytes) {
+  const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4_zfill(void* dst, const void* src, int src_bytes) {
+  const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(d), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+// Partial B V of the split's tokens.  Chunks of 128 tokens (B^T rows and V rows) are copied
+// asynchronously into one of two shared buffers while the other is contracted.
 template <bool kBf16>
 __global__ void __launch_bounds__(512)
 bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __restrict__ bvp,
@@ -32,9 +45,10 @@ bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __r
   float* smem = reinterpret_cast<float*>(smem_bv4);
   const int nthreads = blockDim.x;
   const int mp4 = (m + 3) & ~3;
-  float* sB = smem;                       // [mp4][kBvTileP] kernel values, landmark-major
-  float* sV = sB + mp4 * kBvTileP;        // [kBvTile][d]
-  float* red = sV + kBvTile * d;          // [16][nthreads]
+  const int vrow = d * (kBf16 ? 2 : 4);                    // bytes per staged V row
+  float* sB0 = smem;                                       // 2 x [mp4][kBvTileP]
+  char* sV0 = reinterpret_cast<char*>(sB0 + 2 * mp4 * kBvTileP);   // 2 x [kBvTile][d]
+  float* red = smem;   // [16][nthreads], reuses the staging buffers after the last chunk
   const long bh = blockIdx.x / splits;
   const int sp = blockIdx.x % splits;
   const int tiles = (n + kBvTile - 1) / kBvTile;
@@ -53,45 +67,50 @@ bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __r
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
 
-  // Padding rows of the landmark dimension stay zero.
-  for (int i = threadIdx.x; i < (mp4 - m) * kBvTileP; i += nthreads) sB[m * kBvTileP + i] = 0.f;
+  // Padding rows of the landmark dimension stay zero in both buffers.
+  for (int i = threadIdx.x; i < (mp4 - m) * kBvTileP; i += nthreads) {
+    sB0[m * kBvTileP + i] = 0.f;
+    sB0[(mp4 + m) * kBvTileP + i] = 0.f;
+  }
 
   const bool vec = (n & 3) == 0;
-  for (int tile = t_begin; tile < t_end; ++tile) {
+  auto issue = [&](int tile, int buf) {
     const int n0 = tile * kBvTile;
     const int valid = min(kBvTile, n - n0);
-    // B^T rows j, tokens n0 .. n0+127 (zero beyond N).
+    float* sB = sB0 + buf * mp4 * kBvTileP;
     if (vec) {
       for (int i = threadIdx.x; i < m * (kBvTile / 4); i += nthreads) {
-        const int j = i / (kBvTile / 4), q4 = i % (kBvTile / 4);
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (4 * q4 < valid)
-          x = *reinterpret_cast<const float4*>(&bt[((size_t)bh * m + j) * n + n0 + 4 * q4]);
-        *reinterpret_cast<float4*>(&sB[j * kBvTileP + 4 * q4]) = x;
+        const int j = i >> 5, q4 = i & 31;
+        const float* src = &bt[((size_t)bh * m + j) * n + n0 + (4 * q4 < valid ? 4 * q4 : 0)];
+        cp_async16_zfill(&sB[j * kBvTileP + 4 * q4], src, 4 * q4 < valid ? 16 : 0);
       }
     } else {
       for (int i = threadIdx.x; i < m * kBvTile; i += nthreads) {
-        const int j = i / kBvTile, t = i % kBvTile;
-        sB[j * kBvTileP + t] = t < valid ? bt[((size_t)bh * m + j) * n + n0 + t] : 0.f;
+        const int j = i >> 7, t = i & 127;
+        const float* src = &bt[((size_t)bh * m + j) * n + n0 + (t < valid ? t : 0)];
+        cp_async4_zfill(&sB[j * kBvTileP + t], src, t < valid ? 4 : 0);
       }
     }
-    // V rows n0 .. n0+127 as fp32 (zero beyond N).
-    for (int i = threadIdx.x; i < kBvTile * cqn; i += nthreads) {
-      const int t = i / cqn, c4 = i % cqn;
-      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (t < valid) {
-        const size_t e = ((size_t)bh * n + n0 + t) * d + 4 * c4;
-        if constexpr (kBf16) {
-          const uint2 raw = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(vin) + e);
-          x = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
-        } else {
-          x = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(vin) + e);
-        }
-      }
-      *reinterpret_cast<float4*>(&sV[t * d + 4 * c4]) = x;
+    char* sV = sV0 + buf * kBvTile * vrow;
+    const int pieces = vrow >> 4;
+    const char* vbase = reinterpret_cast<const char*>(vin) + ((size_t)bh * n + n0) * vrow;
+    for (int i = threadIdx.x; i < kBvTile * pieces; i += nthreads) {
+      const int t = i / pieces, pc = i % pieces;
+      cp_async16_zfill(sV + t * vrow + pc * 16, vbase + (size_t)(t < valid ? t : 0) * vrow + pc * 16,
+                       t < valid ? 16 : 0);
     }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  };
+
+  if (t_begin < t_end) issue(t_begin, 0);
+  int buf = 0;
+  for (int tile = t_begin; tile < t_end; ++tile) {
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
     __syncthreads();
+    if (tile + 1 < t_end) issue(tile + 1, buf ^ 1);
     if (on) {
+      const float* sB = sB0 + buf * mp4 * kBvTileP;
+      const char* sV = sV0 + buf * kBvTile * vrow;
       for (int q = ks; q < kBvTile / 4; q += KS) {
         const int t = 4 * q;
         float4 b4[4], v4[4];
@@ -99,8 +118,14 @@ bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __r
         for (int r = 0; r < 4; ++r)
           b4[r] = *reinterpret_cast<const float4*>(&sB[(4 * lg + r) * kBvTileP + t]);
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          v4[u] = *reinterpret_cast<const float4*>(&sV[(t + u) * d + 4 * cq]);
+        for (int u = 0; u < 4; ++u) {
+          if constexpr (kBf16) {
+            const uint2 raw = *reinterpret_cast<const uint2*>(sV + (t + u) * vrow + 8 * cq);
+            v4[u] = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
+          } else {
+            v4[u] = *reinterpret_cast<const float4*>(sV + (t + u) * vrow + 16 * cq);
+          }
+        }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const float bu[4] = {b4[r].x, b4[r].y, b4[r].z, b4[r].w};
@@ -114,9 +139,10 @@ bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __r
         }
       }
     }
-    __syncthreads();
+    buf ^= 1;
   }
   // Combine the KS token classes in order, store the split's partial B V.
+  __syncthreads();
 #pragma unroll
   for (int e = 0; e < 16; ++e) red[e * nthreads + threadIdx.x] = on ? acc[e >> 2][e & 3] : 0.f;
   __syncthreads();
@@ -379,9 +405,12 @@ cudaError_t output_configure(size_t smem) {
                               (int)smem);
 }
 
-size_t bv_smem_bytes(int m, int d, int threads) {
+size_t bv_smem_bytes(int m, int d, int threads, bool bf16) {
   const int mp4 = (m + 3) & ~3;
-  return sizeof(float) * ((size_t)mp4 * kBvTileP + (size_t)kBvTile * d + 16 * (size_t)threads);
+  const size_t staging = sizeof(float) * 2 * (size_t)mp4 * kBvTileP +
+                         2 * (size_t)kBvTile * d * (bf16 ? 2 : 4);
+  const size_t red = sizeof(float) * 16 * (size_t)threads;
+  return staging > red ? staging : red;
 }
 
 int bv_threads(int m, int d) {

@@ -125,7 +125,7 @@ size_t ns_smem_bytes(int m, int d);
 cudaError_t ns_configure(int s, size_t smem);
 size_t output_smem_bytes(int m, int d, int tile);
 cudaError_t output_configure(size_t smem);
-size_t bv_smem_bytes(int m, int d, int threads);
+size_t bv_smem_bytes(int m, int d, int threads, bool bf16);
 int bv_threads(int m, int d);
 int bv_tile_tokens();
 cudaError_t bv_configure(size_t smem);
