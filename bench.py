@@ -37,12 +37,22 @@ L2_BYTES = 129 * 1024 * 1024
 FLUSH_BYTES = 512 * 1024 * 1024
 
 # DRAM traffic (read + write bytes) of one launch of the distance kernel, from an ncu capture
-# (summary: profiles/cdist_exp_kernel_stage1_f32.md).  Valid only for the source it was taken
-# on: the sha256 of the kernel's source files is compared and the figure reported as null on
-# mismatch.
-CDIST_TRAFFIC = {"stage1_f32": 13034752 + 8704}
-CDIST_TRAFFIC_SHA = "c5aa25c668fb493e035297ecc32688a163ce16ec9f30af75a2704c230de11f96"
-CDIST_SOURCES = ["cdist_kernel.cuh", "cdist.cu", "cdist_d32.cu"]
+# (summaries under profiles/), per (feed, workload) with the sha256 of the distance kernel's
+# source files it was taken on; reported as null when the sources have changed since.
+CDIST_TRAFFIC = {}
+CDIST_SOURCES = ["cdist_kernel.cuh", "cdist_tma.cuh", "cdist.cu", "cdist_d32.cu", "cdist_d64.cu",
+                 "cdist_d0.cu", "cdist_tma_f32.cu", "cdist_tma_bf16.cu"]
+CDIST_KERNEL = {
+    "tma": "cdist_tma_kernel (fused L1 distance + exp, query and key blocks; TMA-fed)",
+    "cp.async": "cdist_exp_kernel (fused L1 distance + exp, query and key blocks; cp.async-fed)",
+}
+
+
+def cdist_sources_sha() -> str:
+    hs = hashlib.sha256()
+    for f in CDIST_SOURCES:
+        hs.update(open(os.path.join(ROOT, "laplacian_nystr_attention_gb300", "csrc", f), "rb").read())
+    return hs.hexdigest()
 
 
 def parse():
@@ -305,6 +315,10 @@ def run_ours(args, w):
                "ms_per_step": e2e_ms}
         lna.lapl_attn_destroy(h)
 
+    # No bounded device-side wait may have given up during any of the forwards above.
+    flags = lna.lapl_attn_device_errors(att.handle, stream.cuda_stream)
+    assert flags == 0, flags
+
     if rank != 0:
         if world > 1:
             tdist.destroy_process_group()
@@ -315,11 +329,9 @@ def run_ours(args, w):
     sm_max = float(peaks.get("sm_max_mhz", 2070.0))
     peak = fp32_peak_tflops(props.multi_processor_count, sm_max)
     achieved = cdist_ops_per_launch(w) / (stage_ms["cdist"] / 1e3) / 1e12
-    hs = hashlib.sha256()
-    for f in CDIST_SOURCES:
-        hs.update(open(os.path.join(ROOT, "laplacian_nystr_attention_gb300", "csrc", f), "rb").read())
-    src_sha = hs.hexdigest()
-    traffic = CDIST_TRAFFIC.get(w.name) if CDIST_TRAFFIC_SHA == src_sha else None
+    feed = "tma" if lna.lapl_attn_uses_tma(att.handle) else "cp.async"
+    rec = CDIST_TRAFFIC.get((feed, w.name))
+    traffic = rec[0] if rec and rec[1] == cdist_sources_sha() else None
     clk = clocks.summary()
     line = {
         "metric": METRIC, "value": world * w.tokens / (ms / 1e3), "unit": UNIT, "n_gpus": world,
@@ -329,9 +341,10 @@ def run_ours(args, w):
         "config": {**workload_desc(w),
                    "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write, "
                          "not timed)",
-                   "parallelism": f"replicas x{world} (independent (batch, head) slices)"},
+                   "parallelism": f"replicas x{world} (independent (batch, head) slices)",
+                   "cdist_feed": feed},
         "roofline": {
-            "kernel": "cdist_exp_kernel (fused L1 distance + exp, query and key blocks)",
+            "kernel": CDIST_KERNEL[feed],
             "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": traffic,
             "peak_source": (f"derived: {props.multi_processor_count} SMs x 128 FP32 lanes x 2 x "

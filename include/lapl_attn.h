@@ -44,7 +44,7 @@ typedef enum {
   LAPL_ERR_WORKSPACE = 3,       /* workspace smaller than lapl_attn_workspace_size()       */
   LAPL_ERR_ALIGNMENT = 4,       /* a device pointer is not 16-byte aligned                 */
   LAPL_ERR_CUDA = 5,            /* a CUDA runtime call or launch failed                    */
-  LAPL_ERR_DEVICE_TIMEOUT = 6,  /* reserved: a bounded device-side wait gave up            */
+  LAPL_ERR_DEVICE_TIMEOUT = 6,  /* a bounded device-side wait gave up (device_errors)      */
   LAPL_ERR_NOT_IMPLEMENTED = 7
 } lapl_status;
 
@@ -150,6 +150,26 @@ lapl_status lapl_attn_stage_times(lapl_attn_handle h, float* ms);
 
 /* Number of kernels one forward launches (for launch accounting). */
 int lapl_attn_kernels_per_forward(lapl_attn_handle h);
+
+/*
+ * Device-side failure report.  The distance kernel's TMA pipeline waits on shared-memory
+ * barriers; every such wait gives up after one second, sets bit 1 of a device error word (one
+ * per device, shared by all handles), and the waiting warp leaves the kernel, so a failed
+ * forward ends instead of hanging and its outputs are undefined.  This call copies the word to
+ * *flags, clears it, and synchronises `stream` (a cudaStream_t; enqueue it after the forwards
+ * to be checked).  Returns LAPL_ERR_DEVICE_TIMEOUT (with a message in lapl_attn_last_error)
+ * when a flag was set, LAPL_OK when none was, LAPL_ERR_CUDA if the copy fails.
+ */
+lapl_status lapl_attn_device_errors(lapl_attn_handle h, void* stream, unsigned* flags);
+
+/*
+ * 1 if this plan's distance kernel is fed by the Tensor Memory Accelerator, 0 if by cp.async;
+ * both give the same distances bit for bit.  Chosen at create: TMA for fp32 inputs with d = 32
+ * and m <= 49, cp.async otherwise.  The environment variable LAPL_ATTN_CDIST_FEED, read at
+ * create, overrides the choice: "cp.async" always, "tma" wherever the TMA kernel exists (fp32
+ * with d = 32 or 64, bf16 with d = 64) and B*H*N >= 128.
+ */
+int lapl_attn_uses_tma(lapl_attn_handle h);
 
 /*
  * Forward pass for callers that cannot allocate device memory (for example code embedded in a

@@ -73,6 +73,8 @@ def _load():
         "lapl_attn_stage_times": ([H, ctypes.POINTER(ctypes.c_float)], st),
         "lapl_attn_kernels_per_forward": ([H], ctypes.c_int),
         "lapl_attn_forward_noalloc": ([H, vp, vp, vp, vp, vp, vp], st),
+        "lapl_attn_device_errors": ([H, vp, ctypes.POINTER(ctypes.c_uint)], st),
+        "lapl_attn_uses_tma": ([H], ctypes.c_int),
         "lapl_attn_destroy": ([H], st),
     }
     for name, (args, res) in sigs.items():
@@ -87,7 +89,8 @@ EXPORTED = ["lapl_attn_version", "lapl_attn_status_string", "lapl_attn_last_erro
             "lapl_attn_create", "lapl_attn_workspace_size", "lapl_attn_forward",
             "lapl_attn_forward_debug", "lapl_attn_host_staging_size", "lapl_attn_forward_host",
             "lapl_attn_set_timing", "lapl_attn_stage_times", "lapl_attn_kernels_per_forward",
-            "lapl_attn_forward_noalloc", "lapl_attn_destroy"]
+            "lapl_attn_forward_noalloc", "lapl_attn_device_errors", "lapl_attn_uses_tma",
+            "lapl_attn_destroy"]
 
 
 def status_string(status: int) -> str:
@@ -172,6 +175,18 @@ def lapl_attn_stage_times(handle) -> dict:
 
 def lapl_attn_kernels_per_forward(handle) -> int:
     return LIB.lapl_attn_kernels_per_forward(handle)
+
+
+def lapl_attn_device_errors(handle, stream) -> int:
+    """Read and clear the device error word (synchronises `stream`); raises on a set flag."""
+    flags = ctypes.c_uint(0)
+    _check(LIB.lapl_attn_device_errors(handle, stream, ctypes.byref(flags)),
+           "lapl_attn_device_errors", handle)
+    return flags.value
+
+
+def lapl_attn_uses_tma(handle) -> bool:
+    return bool(LIB.lapl_attn_uses_tma(handle))
 
 
 def lapl_attn_destroy(handle) -> None:

@@ -126,11 +126,9 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   }
 
   // Distance kernel: persistent CTAs, one wave of resident CTAs, balanced ranges.
-  g.cd_tile = cdist_tile_tokens();
-  g.cd_rows = g.cd_tile / 32;
-  g.cd_smem = cdist_smem_bytes(g.s, g.d, g.cd_tile, cfg->in_dtype == LAPL_BF16);
   int per_sm = 1;
-  e = cdist_configure(g.s, g.d, cfg->in_dtype == LAPL_BF16, g.cd_smem, &per_sm);
+  e = device_error_word(&p->dev_err);
+  if (e == cudaSuccess) e = cdist_plan(*p, &per_sm);
   if (e == cudaSuccess) {
     // Newton-Schulz is the longest dependency chain of the forward.  With few heads its CTAs
     // ask for (almost) a whole SM's shared memory, so no other kernel's CTA shares their SM.
@@ -418,6 +416,28 @@ lapl_status lapl_attn_stage_times(lapl_attn_handle h, float* ms) {
 }
 
 int lapl_attn_kernels_per_forward(lapl_attn_handle h) { return (h && h->geo.bh > 0) ? 6 : 0; }
+
+lapl_status lapl_attn_device_errors(lapl_attn_handle h, void* stream, unsigned* flags) {
+  if (!h || !flags) return LAPL_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, h->dev_err, sizeof(word), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->dev_err, 0, sizeof(word), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    set_error(h, e, "device_errors");
+    return LAPL_ERR_CUDA;
+  }
+  *flags = word;
+  if (word) {
+    snprintf(h->last_error, sizeof(h->last_error),
+             "device error flags 0x%x: a pipeline wait in the distance kernel gave up", word);
+    return LAPL_ERR_DEVICE_TIMEOUT;
+  }
+  return LAPL_OK;
+}
+
+int lapl_attn_uses_tma(lapl_attn_handle h) { return (h && h->geo.cd_tma) ? 1 : 0; }
 
 lapl_status lapl_attn_destroy(lapl_attn_handle h) {
   if (!h) return LAPL_OK;

@@ -1,6 +1,22 @@
-// cdist.cu -- host side of the fused L1 distance + exp kernel (cdist_kernel.cuh): shared
-// memory size, occupancy, kernel choice and launch.
-#include "cdist_kernel.cuh"
+// cdist.cu -- host side of the fused L1 distance + exp kernels: kernel choice, tensor maps,
+// shared memory, occupancy and launch.
+//
+// Two kernels compute the same outputs (A^T, B^T and the per-run statistics of A):
+//   cdist_tma_kernel (cdist_tma.cuh)   token chunks loaded by the Tensor Memory Accelerator into
+//                                      a ring of 128B-swizzled stages, producer warp + consumer
+//                                      warps on mbarriers; instantiated for fp32 with d in
+//                                      {32, 64} and bf16 with d = 64;
+//   cdist_exp_kernel (cdist_kernel.cuh) chunks loaded with cp.async by the whole CTA, every
+//                                      shape.
+// Automatic choice: the TMA feed for fp32, d = 32, s <= 7 (as fast as cp.async there); cp.async
+// elsewhere (faster where the TMA kernel's extra producer warp costs registers, s = 8, or its
+// consumer warps each widen the same bf16 chunk).  The environment variable
+// LAPL_ATTN_CDIST_FEED=tma or =cp.async, read at plan creation, overrides the choice (tma only
+// where it is instantiated and the tensor holds at least one chunk of rows).
+#include <stdlib.h>
+#include <string.h>
+
+#include "cdist_tma.cuh"
 
 namespace lapl {
 namespace cdist_impl {
@@ -18,43 +34,143 @@ const void* pick(int s, int d, bool bf16) {
   return kernel_d0(s, bf16);
 }
 
-}  // namespace cdist_impl
-
-using cdist_impl::pick;
-using cdist_impl::CdistArgs;
-using cdist_impl::kRows;
-
-size_t cdist_smem_bytes(int s, int d, int tile, bool bf16) {
+size_t smem_bytes(int s, int d, int tile, bool bf16) {
   const size_t m = (size_t)s * s;
   const size_t staged = 2 * (size_t)tile * d * (bf16 ? 2 : 4);
   return sizeof(float) * m * d + staged + (bf16 ? sizeof(float) * (size_t)tile * d : 0);
 }
+}  // namespace cdist_impl
 
-int cdist_tile_tokens() { return 32 * kRows; }
+namespace cdist_tma {
+const void* kernel_f32(int s, int d);
+const void* kernel_bf16(int s, int d);
 
-cudaError_t cdist_configure(int s, int d, bool bf16, size_t smem, int* ctas_per_sm) {
-  const void* f = pick(s, d, bf16);
+const void* pick(int s, int d, bool bf16) { return bf16 ? kernel_bf16(s, d) : kernel_f32(s, d); }
+
+// Dynamic shared memory: 1024 bytes of alignment slack, the stage ring, the landmark ring and
+// the 2 * kStages mbarriers.
+size_t smem_bytes(int s, int d, bool bf16) {
+  const size_t m = (size_t)s * s;
+  const size_t stage = (size_t)kTile * 128 * (bf16 ? 1 : d / 32);
+  return 1024 + kStages * stage + (size_t)kLmSlots * m * d * sizeof(float) + 2 * kStages * 8;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, found once through the runtime (no link against libcuda).
+EncodeTiledFn encoder() {
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    const cudaError_t e =
+        cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// 2-D view [rows, d] of Q or K; a box is 128 rows of 128 bytes (32 fp32 or 64 bf16 channels),
+// swizzled 128B; rows past the end read as zero.
+bool encode(CUtensorMap* map, const void* base, long long rows, int d, bool bf16) {
+  const EncodeTiledFn fn = encoder();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * (bf16 ? 2 : 4)};
+  const cuuint32_t box[2] = {bf16 ? 64u : 32u, (cuuint32_t)kTile};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r =
+      fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+         const_cast<void*>(base), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+}  // namespace cdist_tma
+
+// Error bits raised by device-side bounded waits; read and cleared by lapl_attn_device_errors.
+__device__ unsigned g_device_errors;
+
+cudaError_t device_error_word(unsigned** word) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_device_errors);
+  *word = static_cast<unsigned*>(p);
+  return e;
+}
+
+cudaError_t cdist_plan(lapl_attn_plan& p, int* ctas_per_sm) {
+  Geometry& g = p.geo;
+  const bool bf16 = p.cfg.in_dtype == LAPL_BF16;
+  g.cd_rows = cdist_impl::kRows;
+  g.cd_tile = 32 * g.cd_rows;
+  const char* feed = getenv("LAPL_ATTN_CDIST_FEED");
+  const bool want_tma = feed && strcmp(feed, "tma") == 0;
+  const bool want_cpasync = feed && strcmp(feed, "cp.async") == 0;
+  const bool auto_tma = !bf16 && g.d == 32 && g.s <= 7;
+  const long long rows = (long long)g.bh * g.n;
+  const void* f = cdist_tma::pick(g.s, g.d, bf16);
+  // Tensor-map coordinates are 32-bit; a box must not be taller than the tensor.
+  g.cd_tma = f && (want_tma || (auto_tma && !want_cpasync)) && rows >= cdist_tma::kTile &&
+             rows < (1LL << 31) && cdist_tma::encoder() != nullptr;
+  if (g.cd_tma) {
+    g.cd_threads = 32 * (g.s + 1);
+    g.cd_smem = cdist_tma::smem_bytes(g.s, g.d, bf16);
+  } else {
+    f = cdist_impl::pick(g.s, g.d, bf16);
+    g.cd_threads = 32 * g.s;
+    g.cd_smem = cdist_impl::smem_bytes(g.s, g.d, g.cd_tile, bf16);
+  }
   if (!f) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.cd_smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, f, 32 * s, smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, f, g.cd_threads, g.cd_smem);
 }
 
 cudaError_t launch_cdist(const lapl_attn_plan& p, const void* q, const void* k, const void* v,
                          const float* landmarks, float* at, float* bt, float* stats,
                          float* dbg_dql, float* dbg_dlk, float* dbg_a, cudaStream_t st) {
   const Geometry& g = p.geo;
-  CdistArgs a;
+  const bool bf16 = p.cfg.in_dtype == LAPL_BF16;
+  if (g.cd_tma) {
+    const long long rows = (long long)g.bh * g.n;
+    if (p.tmap_q_ptr != q) {
+      if (!cdist_tma::encode(&p.tmap_q, q, rows, g.d, bf16)) return cudaErrorInvalidValue;
+      p.tmap_q_ptr = q;
+    }
+    if (p.tmap_k_ptr != k) {
+      if (!cdist_tma::encode(&p.tmap_k, k, rows, g.d, bf16)) return cudaErrorInvalidValue;
+      p.tmap_k_ptr = k;
+    }
+    cdist_tma::TmaArgs a;
+    a.landmarks = landmarks; a.at = at; a.bt = bt; a.stats = stats; a.err = p.dev_err;
+    a.dbg_dql = dbg_dql; a.dbg_dlk = dbg_dlk; a.dbg_a = dbg_a;
+    a.part = g.cd_part;
+    a.bh_count = g.bh;
+    a.n = g.n; a.runs_q = g.cd_runs_q;
+    a.c_exp = p.neg_log2e_over_lambda;
+    const void* f = cdist_tma::pick(g.s, g.d, bf16);
+    if (!f) return cudaErrorInvalidValue;
+    void* args[] = {&a, &p.tmap_q, &p.tmap_k};
+    return cudaLaunchKernel(f, dim3((unsigned)g.cd_part.ctas), dim3(g.cd_threads), args, g.cd_smem,
+                            st);
+  }
+  cdist_impl::CdistArgs a;
   a.q = q; a.k = k; a.v = v; a.landmarks = landmarks; a.at = at; a.bt = bt; a.stats = stats;
   a.dbg_dql = dbg_dql; a.dbg_dlk = dbg_dlk; a.dbg_a = dbg_a;
   a.part = g.cd_part;
   a.bh_count = g.bh;
   a.n = g.n; a.d = g.d; a.runs_q = g.cd_runs_q;
   a.c_exp = p.neg_log2e_over_lambda;
-  const void* f = pick(g.s, g.d, p.cfg.in_dtype == LAPL_BF16);
+  const void* f = cdist_impl::pick(g.s, g.d, bf16);
   if (!f) return cudaErrorInvalidValue;
   void* args[] = {&a};
-  return cudaLaunchKernel(f, dim3((unsigned)g.cd_part.ctas), dim3(32 * g.s), args, g.cd_smem, st);
+  return cudaLaunchKernel(f, dim3((unsigned)g.cd_part.ctas), dim3(g.cd_threads), args, g.cd_smem, st);
 }
 
 }  // namespace lapl

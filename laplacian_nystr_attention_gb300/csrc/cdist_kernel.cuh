@@ -1,7 +1,8 @@
-// cdist_kernel.cuh -- the fused L1 distance + exp kernel template (see cdist.cu).
-// Included by the translation units that instantiate it for given head dims.
+// cdist_kernel.cuh -- the fused L1 distance + Laplacian kernel for the query and key blocks,
+// fed by cp.async (cdist.cu chooses between it and the TMA-fed kernel of cdist_tma.cuh, which
+// shares its helpers from this file).  Included by the translation units that instantiate it
+// for given head dims.
 #pragma once
-// cdist.cu -- fused L1 distance + Laplacian kernel for the query and key blocks.
 //
 // "LaplacianFormer: Rethinking Linear Attention with Laplacian Kernel": the similarity is
 // k(x, y) = exp(-||x - y||_1 / lambda) (English explainer page, 2.A), and the distance and the

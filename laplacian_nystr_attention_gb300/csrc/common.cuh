@@ -4,6 +4,7 @@
 // state only; every device buffer belongs to the caller.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stddef.h>
@@ -64,6 +65,8 @@ struct Geometry {
   long bh;                 // batch * heads
   int cd_rows;             // tokens per thread in the distance kernel
   int cd_tile;             // tokens per distance chunk = 32 * cd_rows
+  bool cd_tma;             // distance kernel fed by TMA (cdist_tma.cuh), else by cp.async
+  int cd_threads;          // threads of a distance-kernel CTA
   Partition cd_part;       // balanced split over cd_part.ctas persistent CTAs
   int cd_runs_q;           // most CTAs whose range meets one head's query tokens
   int bv_splits;           // B V: CTAs per head
@@ -95,6 +98,11 @@ struct lapl_attn_plan {
   bool timed_once;              // a forward ran with timing on
   cudaEvent_t ev_stage[8];      // start, pool, cdist, finish, output ends; ns start, ns end;
                                 // bv end
+  unsigned* dev_err;            // the library's device error word on this device
+  // Tensor maps of Q and K for the TMA-fed distance kernel, re-encoded when the pointers change.
+  mutable CUtensorMap tmap_q, tmap_k;
+  mutable const void* tmap_q_ptr;
+  mutable const void* tmap_k_ptr;
   char last_error[256];
 };
 
@@ -117,10 +125,12 @@ cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float*
                           const float* mu, const float* rstd, const float* bias, void* out,
                           cudaStream_t st);
 
+// Distance kernel choice for a plan: sets geo.cd_tma, cd_tile, cd_rows, cd_threads and cd_smem,
+// opts in to the shared memory and returns the resident CTAs per SM.
+cudaError_t cdist_plan(lapl_attn_plan& p, int* ctas_per_sm);
+// Address of the library's device error word (bit kErrTimeout: a bounded wait gave up).
+cudaError_t device_error_word(unsigned** word);
 // Shared-memory sizes, needed at plan time to size grids and opt in to > 48 KB.
-size_t cdist_smem_bytes(int s, int d, int tile, bool bf16);
-cudaError_t cdist_configure(int s, int d, bool bf16, size_t smem, int* ctas_per_sm);
-int cdist_tile_tokens();
 size_t ns_smem_bytes(int m, int d);
 cudaError_t ns_configure(int s, size_t smem);
 size_t output_smem_bytes(int m, int d, int tile);

@@ -7,6 +7,8 @@ near zero and an elementwise relative error would be ill-posed.
 """
 from __future__ import annotations
 
+import ctypes
+
 import numpy as np
 
 # Tolerances on O (normwise per slice, see module docstring).
@@ -47,8 +49,11 @@ def to_device(arr: np.ndarray, dtype: str):
     return t.cuda()
 
 
-def run_gpu(w, q, k, v, bias=None, debug=False, out_dtype="f32", **cfg_over):
-    """Run the CUDA path via the C ABI.  Returns (out float64 ndarray, dict of intermediates)."""
+def run_gpu(w, q, k, v, bias=None, debug=False, out_dtype="f32", info=None, **cfg_over):
+    """Run the CUDA path via the C ABI.  Returns (out float64 ndarray, dict of intermediates).
+
+    info: optional dict that receives "uses_tma" (distance kernel fed by TMA) and
+    "device_errors" (the device error word after the forward, then cleared)."""
     import torch
     import laplacian_nystr_attention_gb300 as lna
     cfg = w.config()
@@ -68,6 +73,12 @@ def run_gpu(w, q, k, v, bias=None, debug=False, out_dtype="f32", **cfg_over):
                for kname, s in shapes.items()}
     out = att.forward(dq, dk, dv, bias=db, debug=dbg)
     torch.cuda.synchronize()
+    if info is not None:
+        info["uses_tma"] = lna.lapl_attn_uses_tma(att.handle)
+        flags = ctypes.c_uint(0)
+        lna._lib.LIB.lapl_attn_device_errors(att.handle, torch.cuda.current_stream().cuda_stream,
+                                            ctypes.byref(flags))
+        info["device_errors"] = flags.value
     res = out.float().cpu().numpy().astype(np.float64)
     inter = {kname: t.cpu().numpy().astype(np.float64) for kname, t in (dbg or {}).items()}
     att.close()

@@ -1,0 +1,131 @@
+"""The two feeds of the fused distance + exp kernel against the oracle and each other.
+
+The kernel exists twice: token chunks brought into shared memory by the Tensor Memory
+Accelerator (a producer warp and mbarriers; fp32 with d = 32 or 64, bf16 with d = 64) and by
+cp.async (every shape); LAPL_ATTN_CDIST_FEED=tma / =cp.async at plan creation forces either.  Both add
+|x_c - l_c| over the channels in the same order, so their distances agree bit for bit.  On
+small-integer inputs pooled over a power-of-two window the landmarks are dyadic and every
+distance is exact in fp32, so both feeds equal the oracle exactly; other windows round the
+landmark and are compared within 1e-5.  The partitions may differ (the two
+kernels have different occupancy), so the whitening statistics, and O, agree to rounding.
+Every case ends with the device error word clear (no bounded wait gave up).
+"""
+import numpy as np
+import pytest
+
+from lapl_workloads import WORKLOADS, make_inputs
+from parity_utils import TOL_BF16, TOL_F32, elem_rel, run_gpu, slice_rel_err
+
+pytestmark = pytest.mark.gpu
+
+TINY = WORKLOADS["tiny_f32"]
+
+# name -> (workload overrides, expect TMA when allowed)
+CASES = {
+    # ragged: N = 196 is not a multiple of the 128-token chunk; 4 heads
+    "f32_d32_m49_ragged": (dict(batch=2, heads=2, grid_h=14, grid_w=14, num_landmarks=49), True),
+    # d = 64 (two TMA boxes per row), 15 heads, N = 240
+    "f32_d64_m16_15heads": (dict(batch=3, heads=5, grid_h=20, grid_w=12, head_dim=64,
+                                  num_landmarks=16), True),
+    "bf16_d64_m49": (dict(batch=2, heads=2, grid_h=28, grid_w=28, head_dim=64,
+                          num_landmarks=49, dtype="bf16"), True),
+    # one head: the switch from query to key tokens keeps the same landmarks
+    "f32_d32_m1_one_head_129": (dict(grid_h=3, grid_w=43, num_landmarks=1), True),
+    # exactly one chunk of rows in the whole tensor
+    "f32_d32_m4_128_rows": (dict(grid_h=8, grid_w=16, num_landmarks=4), True),
+    "f32_d32_m64": (dict(grid_h=16, grid_w=16, num_landmarks=64), True),
+    "bf16_d64_m64": (dict(batch=2, grid_h=16, grid_w=16, head_dim=64, num_landmarks=64,
+                          dtype="bf16"), True),
+    "f32_d64_m36": (dict(batch=2, heads=3, grid_h=12, grid_w=24, head_dim=64,
+                         num_landmarks=36), True),
+    # fewer rows than one chunk: always cp.async
+    "f32_d32_m4_below_chunk": (dict(grid_h=8, grid_w=8, num_landmarks=4), False),
+    # head dims without a TMA instantiation
+    "f32_d16_m16": (dict(head_dim=16), False),
+    "bf16_d32_m16": (dict(dtype="bf16"), False),
+}
+
+
+def _dyadic_window(w) -> bool:
+    s = int(round(w.num_landmarks ** 0.5))
+    win = (w.grid_h // s) * (w.grid_w // s)
+    return win & (win - 1) == 0
+
+
+def _oracle(w, q, k, v):
+    import oracle
+    return oracle.forward(w.config(), q, k, v, intermediates=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from conftest import build_library
+    build_library()
+    import oracle
+    oracle.build()
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_both_feeds_match_oracle_and_each_other(case, monkeypatch):
+    over, expect_tma = CASES[case]
+    w = TINY.replace(dist="integer", **over)
+    q, k, v = make_inputs(w, seed=3)
+    ref, o = _oracle(w, q, k, v)
+    runs = {}
+    for feed in ("tma", "cp.async"):
+        monkeypatch.setenv("LAPL_ATTN_CDIST_FEED", feed)
+        info = {}
+        out, g = run_gpu(w, q, k, v, debug=True, info=info)
+        assert info["device_errors"] == 0, feed
+        assert info["uses_tma"] == (expect_tma and feed == "tma"), feed
+        for name in ("d_ql", "d_lk", "d_ll", "landmarks"):
+            if _dyadic_window(w):
+                assert np.array_equal(g[name], o[name]), (feed, name)
+            else:
+                assert elem_rel(g[name], o[name]) < 1e-5, (feed, name)
+        tol = TOL_BF16 if w.dtype == "bf16" else TOL_F32
+        assert slice_rel_err(out, ref) < tol, feed
+        runs[feed] = (out, g)
+    (o1, g1), (o2, g2) = runs["tma"], runs["cp.async"]
+    for name in ("d_ql", "d_lk", "a"):
+        assert np.array_equal(g1[name], g2[name]), name
+    assert slice_rel_err(o1, o2) < 1e-5
+
+
+@pytest.mark.parametrize("name", ["stage1_f32", "stage23_bf16", "hires_bf16"])
+def test_workload_shape_feeds_agree(name, monkeypatch):
+    """Full launch configuration of the workload, Gaussian-valued inputs: A from both feeds is
+    identical bit for bit, O agrees to rounding."""
+    w = WORKLOADS[name]
+    q, k, v = make_inputs(w, seed=11)
+    outs = {}
+    for feed in ("tma", "cp.async"):
+        monkeypatch.setenv("LAPL_ATTN_CDIST_FEED", feed)
+        info = {}
+        outs[feed] = run_gpu(w, q, k, v, debug=True, info=info)
+        assert info["uses_tma"] == (feed == "tma")
+        assert info["device_errors"] == 0
+    (o1, g1), (o2, g2) = outs["tma"], outs["cp.async"]
+    assert np.array_equal(g1["d_ql"], g2["d_ql"])
+    assert np.array_equal(g1["d_lk"], g2["d_lk"])
+    assert slice_rel_err(o1, o2) < 1e-5
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(grid_h=56, grid_w=56, num_landmarks=49), True),                    # fp32, d = 32
+    (dict(grid_h=56, grid_w=56, num_landmarks=64), False),                   # s = 8
+    (dict(grid_h=28, grid_w=28, head_dim=64, num_landmarks=49), False),      # d = 64
+    (dict(grid_h=28, grid_w=28, head_dim=64, num_landmarks=49, dtype="bf16"), False),
+])
+def test_automatic_feed_choice(over, expect, monkeypatch):
+    import laplacian_nystr_attention_gb300 as lna
+    monkeypatch.delenv("LAPL_ATTN_CDIST_FEED", raising=False)
+    w = TINY.replace(**over)
+    h = lna.lapl_attn_create(lna.make_config(**{**w.config(), "in_dtype": w.dtype}))
+    try:
+        assert lna.lapl_attn_uses_tma(h) == expect
+    finally:
+        lna.lapl_attn_destroy(h)
