@@ -329,7 +329,8 @@ def run_ours(args, w):
     sm_max = float(peaks.get("sm_max_mhz", 2070.0))
     peak = fp32_peak_tflops(props.multi_processor_count, sm_max)
     achieved = cdist_ops_per_launch(w) / (stage_ms["cdist"] / 1e3) / 1e12
-    feed = "tma" if lna.lapl_attn_uses_tma(att.handle) else "cp.async"
+    plan = lna.lapl_attn_plan_info_get(att.handle)
+    feed = "tma" if plan["cdist_tma"] else "cp.async"
     rec = CDIST_TRAFFIC.get((feed, w.name))
     traffic = rec[0] if rec and rec[1] == cdist_sources_sha() else None
     clk = clocks.summary()
@@ -342,7 +343,7 @@ def run_ours(args, w):
                    "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write, "
                          "not timed)",
                    "parallelism": f"replicas x{world} (independent (batch, head) slices)",
-                   "cdist_feed": feed},
+                   "plan": plan},
         "roofline": {
             "kernel": CDIST_KERNEL[feed],
             "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

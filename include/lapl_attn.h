@@ -16,10 +16,11 @@
  *        is never formed)
  *
  * Layouts: Q, K, V, O are [B, H, N, d] contiguous (C order), token n = r * grid_w + c.
- * Every buffer is owned by the caller.  The handle holds host state only (the configuration
- * and two CUDA events plus one auxiliary stream used to overlap the Newton-Schulz solve with
- * the distance kernel).  No entry point allocates device memory; forward() never
- * synchronises the host.
+ * Every buffer is owned by the caller.  The handle holds host state only: the configuration,
+ * three CUDA events and one auxiliary stream (highest priority) that runs pooling and the
+ * Newton-Schulz solve while the launching stream runs the distance kernel.  The library's
+ * device globals are a 4-byte error word and the scratch of lapl_attn_forward_noalloc.  No
+ * entry point allocates device memory; forward() never synchronises the host.
  *
  * Errors: every entry point returns a lapl_status.  Argument errors are detected on the host
  * before any launch.  CUDA errors from launches map to LAPL_ERR_CUDA (the CUDA error string is
@@ -137,8 +138,9 @@ lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void
 
 /*
  * Stage timing, a profiling aid.  After lapl_attn_set_timing(h, 1) every forward records CUDA
- * events (created here, host-owned) around its six stages: on the launching stream for
- * pooling, distances, B V, finish and output, on the side stream for Newton-Schulz.
+ * events (created here, host-owned) around its six stages: on the side stream for pooling
+ * (from the start of the forward on the launching stream) and Newton-Schulz, on the launching
+ * stream for distances (from the end of pooling), B V, finish and output.
  * lapl_attn_stage_times() waits for the events of the last forward (it synchronises the host
  * with them) and writes the elapsed milliseconds of
  *   ms[0] pooling, ms[1] Newton-Schulz, ms[2] distance kernel, ms[3] B V, ms[4] finish,
@@ -147,6 +149,15 @@ lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void
  */
 lapl_status lapl_attn_set_timing(lapl_attn_handle h, int enable);
 lapl_status lapl_attn_stage_times(lapl_attn_handle h, float* ms);
+
+/*
+ * Timeline of the last timed forward (same events as lapl_attn_stage_times, same waiting and
+ * errors): milliseconds since the start of the forward on the launching stream of
+ *   ms[0] start (0), ms[1] pooling done, ms[2] Newton-Schulz start, ms[3] Newton-Schulz done,
+ *   ms[4] distance kernel start (the launching stream has seen pooling done), ms[5] distance
+ *   kernel done, ms[6] B V done, ms[7] finish done, ms[8] output done.
+ */
+lapl_status lapl_attn_stage_marks(lapl_attn_handle h, float* ms);
 
 /* Number of kernels one forward launches (for launch accounting). */
 int lapl_attn_kernels_per_forward(lapl_attn_handle h);
@@ -162,14 +173,30 @@ int lapl_attn_kernels_per_forward(lapl_attn_handle h);
  */
 lapl_status lapl_attn_device_errors(lapl_attn_handle h, void* stream, unsigned* flags);
 
+/* Launch choices of a plan (fixed at create). */
+typedef struct {
+  int cdist_tma;      /* 1: the distance kernel's token chunks are loaded by the Tensor Memory
+                         Accelerator; 0: by cp.async.  Same distances bit for bit.          */
+  int cdist_ctas;     /* persistent CTAs of the distance kernel                              */
+  int cdist_threads;  /* threads per distance-kernel CTA                                     */
+  int ns_cluster;     /* CTAs per head in the Newton-Schulz solve: 1, or 2 (a cluster pair,
+                         m > 32, on request); same X bit for bit                            */
+  int ns_tensor_core; /* 1: the solve's products run on the tensor cores (TF32 high/low
+                         split, fp32 accumulation); X agrees to rounding                     */
+  int ns_exclusive;   /* 1: the solve's CTAs have their SMs to themselves                    */
+  int bv_splits;      /* CTAs per head of the B V kernel                                     */
+} lapl_attn_plan_info;
+
 /*
- * 1 if this plan's distance kernel is fed by the Tensor Memory Accelerator, 0 if by cp.async;
- * both give the same distances bit for bit.  Chosen at create: TMA for fp32 inputs with d = 32
- * and m <= 49, cp.async otherwise.  The environment variable LAPL_ATTN_CDIST_FEED, read at
- * create, overrides the choice: "cp.async" always, "tma" wherever the TMA kernel exists (fp32
- * with d = 32 or 64, bf16 with d = 64) and B*H*N >= 128.
+ * Fill *info.  Choices made at create: the TMA feed for fp32 inputs with d = 32 and m <= 49,
+ * cp.async otherwise; for the solve one CTA per head, with tensor-core products for m >= 25
+ * and CUDA-core products for m <= 16.  Environment
+ * variables read at create override them: LAPL_ATTN_CDIST_FEED = "cp.async" (always) or "tma"
+ * (wherever the TMA kernel exists: fp32 with d = 32 or 64, bf16 with d = 64, and
+ * B*H*N >= 128); LAPL_ATTN_NS_KERNEL = "ffma", "pair" (a CTA pair per head, m > 32) or "tc"
+ * (tensor-core products).
  */
-int lapl_attn_uses_tma(lapl_attn_handle h);
+lapl_status lapl_attn_plan_info_get(lapl_attn_handle h, lapl_attn_plan_info* info);
 
 /*
  * Forward pass for callers that cannot allocate device memory (for example code embedded in a

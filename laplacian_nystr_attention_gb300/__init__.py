@@ -20,16 +20,17 @@ from ._lib import (LAPL_BF16, LAPL_F32, LaplAttnError, lapl_attn_config, lapl_at
                    lapl_attn_forward,
                    lapl_attn_forward_debug, lapl_attn_forward_host, lapl_attn_host_staging_size,
                    lapl_attn_kernels_per_forward, lapl_attn_last_error,
-                   lapl_attn_set_timing, lapl_attn_stage_times, lapl_attn_status_string,
-                   lapl_attn_uses_tma, lapl_attn_version, lapl_attn_workspace_size)
+                   lapl_attn_set_timing, lapl_attn_stage_marks, lapl_attn_stage_times,
+                   lapl_attn_status_string,
+                   lapl_attn_plan_info_get, lapl_attn_version, lapl_attn_workspace_size)
 
 __all__ = [
     "LaplacianNystromAttention", "LaplAttnError", "lapl_attn_config", "lapl_attn_debug",
     "lapl_attn_create", "lapl_attn_destroy", "lapl_attn_forward", "lapl_attn_forward_debug",
     "lapl_attn_forward_host", "lapl_attn_host_staging_size", "lapl_attn_last_error",
     "lapl_attn_status_string", "lapl_attn_version", "lapl_attn_workspace_size", "LAPL_F32",
-    "LAPL_BF16", "lapl_attn_set_timing", "lapl_attn_stage_times",
-    "lapl_attn_kernels_per_forward", "lapl_attn_device_errors", "lapl_attn_uses_tma",
+    "LAPL_BF16", "lapl_attn_set_timing", "lapl_attn_stage_times", "lapl_attn_stage_marks",
+    "lapl_attn_kernels_per_forward", "lapl_attn_device_errors", "lapl_attn_plan_info_get",
     "make_config",
 ]
 

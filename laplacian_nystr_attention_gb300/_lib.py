@@ -44,6 +44,12 @@ class lapl_attn_debug(ctypes.Structure):
                 ("d_ql", "d_ll", "d_lk", "landmarks", "w", "x", "a", "mu", "rstd", "bv", "m")]
 
 
+class lapl_attn_plan_info(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int) for name in
+                ("cdist_tma", "cdist_ctas", "cdist_threads", "ns_cluster", "ns_tensor_core",
+                 "ns_exclusive", "bv_splits")]
+
+
 class LaplAttnError(RuntimeError):
     def __init__(self, status: int, where: str, detail: str = ""):
         self.status = status
@@ -71,10 +77,11 @@ def _load():
         "lapl_attn_forward_host": ([H, vp, vp, vp, vp, vp, vp, sz, vp], st),
         "lapl_attn_set_timing": ([H, ctypes.c_int], st),
         "lapl_attn_stage_times": ([H, ctypes.POINTER(ctypes.c_float)], st),
+        "lapl_attn_stage_marks": ([H, ctypes.POINTER(ctypes.c_float)], st),
         "lapl_attn_kernels_per_forward": ([H], ctypes.c_int),
         "lapl_attn_forward_noalloc": ([H, vp, vp, vp, vp, vp, vp], st),
         "lapl_attn_device_errors": ([H, vp, ctypes.POINTER(ctypes.c_uint)], st),
-        "lapl_attn_uses_tma": ([H], ctypes.c_int),
+        "lapl_attn_plan_info_get": ([H, ctypes.POINTER(lapl_attn_plan_info)], st),
         "lapl_attn_destroy": ([H], st),
     }
     for name, (args, res) in sigs.items():
@@ -88,8 +95,9 @@ LIB = _load()
 EXPORTED = ["lapl_attn_version", "lapl_attn_status_string", "lapl_attn_last_error",
             "lapl_attn_create", "lapl_attn_workspace_size", "lapl_attn_forward",
             "lapl_attn_forward_debug", "lapl_attn_host_staging_size", "lapl_attn_forward_host",
-            "lapl_attn_set_timing", "lapl_attn_stage_times", "lapl_attn_kernels_per_forward",
-            "lapl_attn_forward_noalloc", "lapl_attn_device_errors", "lapl_attn_uses_tma",
+            "lapl_attn_set_timing", "lapl_attn_stage_times", "lapl_attn_stage_marks",
+            "lapl_attn_kernels_per_forward",
+            "lapl_attn_forward_noalloc", "lapl_attn_device_errors", "lapl_attn_plan_info_get",
             "lapl_attn_destroy"]
 
 
@@ -173,6 +181,16 @@ def lapl_attn_stage_times(handle) -> dict:
     return dict(zip(STAGES, [float(x) for x in ms]))
 
 
+MARKS = ("start", "pool_done", "ns_start", "ns_done", "cdist_start", "cdist_done", "bv_done",
+         "finish_done", "output_done")
+
+
+def lapl_attn_stage_marks(handle) -> dict:
+    ms = (ctypes.c_float * len(MARKS))()
+    _check(LIB.lapl_attn_stage_marks(handle, ms), "lapl_attn_stage_marks", handle)
+    return dict(zip(MARKS, [float(x) for x in ms]))
+
+
 def lapl_attn_kernels_per_forward(handle) -> int:
     return LIB.lapl_attn_kernels_per_forward(handle)
 
@@ -185,8 +203,11 @@ def lapl_attn_device_errors(handle, stream) -> int:
     return flags.value
 
 
-def lapl_attn_uses_tma(handle) -> bool:
-    return bool(LIB.lapl_attn_uses_tma(handle))
+def lapl_attn_plan_info_get(handle) -> dict:
+    info = lapl_attn_plan_info()
+    _check(LIB.lapl_attn_plan_info_get(handle, ctypes.byref(info)), "lapl_attn_plan_info_get",
+           handle)
+    return {name: int(getattr(info, name)) for name, _ in lapl_attn_plan_info._fields_}
 
 
 def lapl_attn_destroy(handle) -> None:

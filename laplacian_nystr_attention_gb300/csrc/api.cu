@@ -1,15 +1,21 @@
 // api.cu -- the C ABI (include/lapl_attn.h): validation, plan, workspace layout, and the
 // stream-ordered launch sequence of one forward pass.
 //
-//   K1 pool      L = avg-pool(K)                          stream
-//   fork ------------------------------------------------ side stream: K3 Newton-Schulz (W, X)
-//   K2 cdist     A^T + run statistics (queries), B^T (keys)            stream
-//   K2b bv       B V partials per token split                           stream
-//   join <----------------------------------------------- (needs X)
+//   fork ---------------------------------------------> side stream (highest priority):
+//                                                          K1 pool     L = avg-pool(K)
+//   wait (L) <-------------------------------------------- pooled
+//   K2 cdist     A^T + run statistics (queries), B^T (keys) K3 Newton-Schulz (W, X)
+//   K2b bv       B V partials per token split
+//   join (X) <-------------------------------------------- solved
 //   K4 finish    mean/rstd, B V, M = X (B V)              stream
 //   K5 output    O = whiten(A) M                          stream
+//
+// The solve is the longest dependency chain.  It follows pooling on the same stream, so its
+// CTAs are dispatched the moment pooling ends; the distance kernel waits for pooling across
+// streams and takes the SMs that are left.
 #include <math.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -130,14 +136,40 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   e = device_error_word(&p->dev_err);
   if (e == cudaSuccess) e = cdist_plan(*p, &per_sm);
   if (e == cudaSuccess) {
-    // Newton-Schulz is the longest dependency chain of the forward.  With few heads its CTAs
-    // ask for (almost) a whole SM's shared memory, so no other kernel's CTA shares their SM.
-    g.ns_exclusive = g.bh <= p->num_sms / 4;
+    // Newton-Schulz is the longest dependency chain of the forward.  Kernels: "tc" (one CTA per
+    // head, products on the tensor cores; the default for m >= 25), "ffma" (one CTA per head,
+    // CUDA-core products; the default for m <= 16) and "pair" (a cluster of two CTAs per head
+    // that split every CUDA-core product; m > 32).  LAPL_ATTN_NS_KERNEL, read here, picks one.
+    const char* nk = getenv("LAPL_ATTN_NS_KERNEL");
+    g.ns_cluster = 1;
+    g.ns_tc = g.s >= 5;
+    if (nk && strcmp(nk, "ffma") == 0) g.ns_tc = false;
+    if (nk && strcmp(nk, "pair") == 0 && ns_cluster_supported(g.s, 2)) {
+      g.ns_cluster = 2;
+      g.ns_tc = false;
+    }
+    if (nk && strcmp(nk, "tc") == 0) g.ns_tc = true;
+    // With few heads the solve's CTAs ask for (almost) a whole SM's shared memory, so no other
+    // kernel's CTA shares their SM.
+    g.ns_exclusive = g.bh * g.ns_cluster <= p->num_sms / 4;
     int smem_max = 0;
     e = cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
-    g.ns_smem = ns_smem_bytes(g.m, g.d);
+    g.ns_smem = g.ns_tc ? ns_tc_smem_bytes(g.d) : ns_smem_bytes(g.m, g.d);
     if (e == cudaSuccess && g.ns_exclusive && (size_t)smem_max > g.ns_smem) g.ns_smem = smem_max;
-    if (e == cudaSuccess) e = ns_configure(g.s, g.ns_smem);
+    if (e == cudaSuccess && g.ns_tc) {
+      e = ns_tc_configure(g.s, g.ns_smem);
+    } else if (e == cudaSuccess && g.ns_cluster == 2) {
+      int clusters = 0;
+      e = ns_configure(g.s, 2, g.ns_smem, &clusters);
+      if (e != cudaSuccess || clusters < 1) {   // no room for a pair: one CTA per head
+        cudaGetLastError();
+        g.ns_cluster = 1;
+        g.ns_exclusive = g.bh <= p->num_sms / 4;
+        e = cudaSuccess;
+      }
+    }
+    if (e == cudaSuccess && !g.ns_tc && g.ns_cluster == 1)
+      e = ns_configure(g.s, 1, g.ns_smem, nullptr);
   }
   if (e == cudaSuccess) {
     g.out_tile = output_tile_tokens(g.d);
@@ -177,7 +209,7 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
     // SMs), it gets those SMs to itself: the distance kernel's persistent grid covers the
     // others (see ns_exclusive).
     long long slots = (long long)p->num_sms * per_sm;
-    if (g.ns_exclusive) slots -= g.bh * per_sm;
+    if (g.ns_exclusive) slots -= g.bh * g.ns_cluster * per_sm;
     const long long ctas = std::min<long long>(slots, chunks);
     setup_cdist_partition(g, (int)std::max<long long>(ctas, 1));
     g.fin_smem = finish_smem_bytes(g.m, g.cd_runs_q, g.bv_splits);
@@ -216,10 +248,12 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
     e = cudaStreamCreateWithPriority(&p->side_stream, cudaStreamNonBlocking, prio_greatest);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_pool, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     set_error(p, e, "create/stream");
     if (p->side_stream) cudaStreamDestroy(p->side_stream);
     if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+    if (p->ev_join) cudaEventDestroy(p->ev_join);
     delete p;
     return LAPL_ERR_CUDA;
   }
@@ -279,14 +313,19 @@ static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k,
   if (tm) LAPL_TRY(cudaEventRecord(p->ev_stage[i], s), "forward/timing")
 
   LAPL_MARK(0, st);
-  LAPL_TRY(launch_pool(*p, k, L, D.landmarks, st), "forward/pool");
-  LAPL_MARK(1, st);
   LAPL_TRY(cudaEventRecord(p->ev_fork, st), "forward/fork");
   LAPL_TRY(cudaStreamWaitEvent(p->side_stream, p->ev_fork, 0), "forward/fork-wait");
+  LAPL_TRY(launch_pool(*p, k, L, D.landmarks, p->side_stream), "forward/pool");
+  LAPL_MARK(1, p->side_stream);
+  LAPL_TRY(cudaEventRecord(p->ev_pool, p->side_stream), "forward/pooled");
   LAPL_MARK(5, p->side_stream);
-  LAPL_TRY(launch_ns(*p, L, X, D.d_ll, D.w, D.x, p->side_stream), "forward/newton-schulz");
+  LAPL_TRY(p->geo.ns_tc ? launch_ns_tc(*p, L, X, D.d_ll, D.w, D.x, p->side_stream)
+                        : launch_ns(*p, L, X, D.d_ll, D.w, D.x, p->side_stream),
+           "forward/newton-schulz");
   LAPL_MARK(6, p->side_stream);
   LAPL_TRY(cudaEventRecord(p->ev_join, p->side_stream), "forward/join");
+  LAPL_TRY(cudaStreamWaitEvent(st, p->ev_pool, 0), "forward/pooled-wait");
+  LAPL_MARK(8, st);
   LAPL_TRY(launch_cdist(*p, q, k, v, L, At, Bt, stats, D.d_ql, D.d_lk, D.a, st), "forward/cdist");
   LAPL_MARK(2, st);
   LAPL_TRY(launch_bv(*p, Bt, v, bvp, st), "forward/bv");
@@ -388,7 +427,7 @@ lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void
 lapl_status lapl_attn_set_timing(lapl_attn_handle h, int enable) {
   if (!h) return LAPL_ERR_INVALID_ARG;
   if (enable && !h->ev_stage[0]) {
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 9; ++i) {
       cudaError_t e = cudaEventCreate(&h->ev_stage[i]);
       if (e != cudaSuccess) {
         set_error(h, e, "set_timing");
@@ -410,6 +449,21 @@ lapl_status lapl_attn_stage_times(lapl_attn_handle h, float* ms) {
     e = cudaEventElapsedTime(&ms[i], h->ev_stage[pairs[i][0]], h->ev_stage[pairs[i][1]]);
   if (e != cudaSuccess) {
     set_error(h, e, "stage_times");
+    return LAPL_ERR_CUDA;
+  }
+  return LAPL_OK;
+}
+
+lapl_status lapl_attn_stage_marks(lapl_attn_handle h, float* ms) {
+  if (!h || !ms || !h->timing || !h->timed_once) return LAPL_ERR_INVALID_ARG;
+  cudaError_t e = cudaEventSynchronize(h->ev_stage[4]);
+  if (e == cudaSuccess) e = cudaEventSynchronize(h->ev_stage[6]);
+  // start, pool end, NS start, NS end, cdist start, cdist end, bv end, finish end, output end
+  const int order[9] = {0, 1, 5, 6, 8, 2, 7, 3, 4};
+  for (int i = 0; i < 9 && e == cudaSuccess; ++i)
+    e = cudaEventElapsedTime(&ms[i], h->ev_stage[0], h->ev_stage[order[i]]);
+  if (e != cudaSuccess) {
+    set_error(h, e, "stage_marks");
     return LAPL_ERR_CUDA;
   }
   return LAPL_OK;
@@ -437,13 +491,25 @@ lapl_status lapl_attn_device_errors(lapl_attn_handle h, void* stream, unsigned* 
   return LAPL_OK;
 }
 
-int lapl_attn_uses_tma(lapl_attn_handle h) { return (h && h->geo.cd_tma) ? 1 : 0; }
+lapl_status lapl_attn_plan_info_get(lapl_attn_handle h, lapl_attn_plan_info* info) {
+  if (!h || !info) return LAPL_ERR_INVALID_ARG;
+  const Geometry& g = h->geo;
+  info->cdist_tma = g.cd_tma ? 1 : 0;
+  info->cdist_ctas = g.cd_part.ctas;
+  info->cdist_threads = g.cd_threads;
+  info->ns_cluster = g.ns_cluster;
+  info->ns_tensor_core = g.ns_tc ? 1 : 0;
+  info->ns_exclusive = g.ns_exclusive ? 1 : 0;
+  info->bv_splits = g.bv_splits;
+  return LAPL_OK;
+}
 
 lapl_status lapl_attn_destroy(lapl_attn_handle h) {
   if (!h) return LAPL_OK;
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < 9; ++i)
     if (h->ev_stage[i]) cudaEventDestroy(h->ev_stage[i]);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->ev_pool) cudaEventDestroy(h->ev_pool);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
   if (h->side_stream) cudaStreamDestroy(h->side_stream);
   delete h;

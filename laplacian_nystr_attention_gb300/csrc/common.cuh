@@ -79,6 +79,8 @@ struct Geometry {
   int out_threads;
   size_t out_smem;
   size_t ns_smem;
+  int ns_cluster;          // Newton-Schulz CTAs per head (a cluster of 1 or 2)
+  bool ns_tc;              // Newton-Schulz products on the tensor cores (ns_tc.cu)
   bool ns_exclusive;       // Newton-Schulz CTAs own their SMs (few heads)
   size_t pool_threads;
 };
@@ -92,12 +94,14 @@ struct lapl_attn_plan {
   int device;
   int num_sms;
   float neg_log2e_over_lambda;  // exp(-D/lambda) == exp2(D * this)
-  cudaStream_t side_stream;     // runs the Newton-Schulz solve next to the distance kernel
-  cudaEvent_t ev_fork, ev_join;
+  cudaStream_t side_stream;     // runs pooling and the Newton-Schulz solve next to the
+                                // distance kernel
+  cudaEvent_t ev_fork, ev_pool, ev_join;
   bool timing;                  // record stage events in forward
   bool timed_once;              // a forward ran with timing on
-  cudaEvent_t ev_stage[8];      // start, pool, cdist, finish, output ends; ns start, ns end;
-                                // bv end
+  cudaEvent_t ev_stage[9];      // start, pool end (side), cdist, finish, output ends; ns
+                                // start, ns end (side); bv end; cdist start (after the wait
+                                // for pooling)
   unsigned* dev_err;            // the library's device error word on this device
   // Tensor maps of Q and K for the TMA-fed distance kernel, re-encoded when the pointers change.
   mutable CUtensorMap tmap_q, tmap_k;
@@ -132,7 +136,14 @@ cudaError_t cdist_plan(lapl_attn_plan& p, int* ctas_per_sm);
 cudaError_t device_error_word(unsigned** word);
 // Shared-memory sizes, needed at plan time to size grids and opt in to > 48 KB.
 size_t ns_smem_bytes(int m, int d);
-cudaError_t ns_configure(int s, size_t smem);
+bool ns_cluster_supported(int s, int cluster);
+// Sets the shared-memory attribute; with clusters_per_gpu, also how many clusters of the
+// kernel can be resident at once.
+cudaError_t ns_configure(int s, int cluster, size_t smem, int* clusters_per_gpu);
+size_t ns_tc_smem_bytes(int d);
+cudaError_t ns_tc_configure(int s, size_t smem);
+cudaError_t launch_ns_tc(const lapl_attn_plan& p, const float* landmarks, float* x,
+                         float* dbg_dll, float* dbg_w, float* dbg_x, cudaStream_t st);
 size_t output_smem_bytes(int m, int d, int tile);
 cudaError_t output_configure(size_t smem);
 size_t bv_smem_bytes(int m, int d, int threads, bool bf16);

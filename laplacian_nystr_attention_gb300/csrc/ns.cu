@@ -24,23 +24,21 @@
 // lanes of a quarter-warp read the same address) and one of B (a quarter reads 128 contiguous
 // bytes): 8 shared-memory wavefronts per 32 FMAs per lane.  The k quarters meet through shared
 // memory in a lane-major (conflict-free) layout.
-#include "common.cuh"
+//
+// Pairs.  For m > 32 (2 x 2 warp tiles) a head can run on a cluster of two CTAs
+// (ns_pair_kernel): both build W and X0, each computes half of every product's output rows and
+// stores them into its own and its peer's shared memory (distributed shared memory), and one
+// cluster barrier per product makes the halves visible.  Every CTA executes the same sequence
+// of barriers and none leaves early, so every barrier completes.
+#include <cooperative_groups.h>
+
+#include "ns_common.cuh"
 
 namespace lapl {
+using namespace ns_detail;
 namespace {
 
 constexpr int kNsThreads = 512;
-
-constexpr int kMS = 68;   // stored row stride: 64 columns (padded) + 4, 16-byte aligned, and
-                          // column-direction stores spread over more banks than with 64
-
-template <int S>
-struct NsShape {
-  static constexpr int M = S * S;
-  static constexpr int MK = (M + 3) & ~3;            // k range actually summed
-  static constexpr int NWT = (M + 31) / 32;          // 32x32 warp tiles per side (1 or 2)
-  static constexpr int PART_FLOATS = 4 * 3 * 32 * 32;  // 4 tiles x 3 upper slices x 32 x 32
-};
 
 // C = A B for symmetric A (row stride kMS): (A B)[i][j] = sum_k A[k][i] B[k][j].
 // kMirror: only warp tiles tr <= tc, C = 2 Xs - A B written to (i, j) and (j, i) (on a diagonal
@@ -161,65 +159,15 @@ ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
   using Sh = NsShape<S>;
   constexpr int M = Sh::M, MP = kMS;
   extern __shared__ float4 smem_ns4[];
-  float* smem = reinterpret_cast<float*>(smem_ns4);
+  const NsSmem sm = ns_smem_layout<S>(reinterpret_cast<float*>(smem_ns4));
   const long bh = blockIdx.x;
-  float* W = smem;               // [64][MP]
-  float* X = W + 64 * MP;
-  float* P = X + 64 * MP;
-  float* Y = P + 64 * MP;
-  float* red = Y + 64 * MP;      // column sums [64], scale at [128]
-  float* part = red + 132;       // partial 4x4 tiles of the k slices
-  float* sL = part + Sh::PART_FLOATS;   // [d][64], channel-major
-
-  // Landmarks, stored channel-major (sL[c * 64 + j]): in the distance loop below a warp reads
-  // one broadcast value and 32 consecutive values per channel, free of bank conflicts.
-  const float* Lg = landmarks + (size_t)bh * M * d;
-  for (int i = threadIdx.x; i < M * d; i += kNsThreads) {
-    const int j = i / d, c = i % d;
-    sL[c * 64 + j] = Lg[i];
-  }
-  __syncthreads();
-
-  // W = exp(-D_LL / lambda) + eps I, zero outside m x m.  Exactly symmetric: |a-b| == |b-a|
-  // and both orders sum the channels in the same order.
-  for (int idx = threadIdx.x; idx < 64 * 64; idx += kNsThreads) {
-    const int i = idx >> 6, k = idx & 63;
-    float w = 0.f;
-    if (i < M && k < M) {
-      float dist = 0.f;
-      for (int c = 0; c < d; ++c) dist += fabsf(sL[c * 64 + i] - sL[c * 64 + k]);
-      // k(x, x) = 1 exactly: D_LL[i][i] = 0 and exp(0) = 1.
-      w = (i == k) ? 1.f + eps : laplacian_from_distance(dist, c_exp);
-      const size_t o = ((size_t)bh * M + i) * M + k;
-      if (dbg_dll) dbg_dll[o] = dist;
-      if (dbg_w) dbg_w[o] = w;
-    }
-    W[i * MP + k] = w;
-  }
-  __syncthreads();
-
-  // |W|_1 = largest absolute column sum.  W is exactly symmetric, so row j holds the same
-  // values in the same order as column j and |W|_inf (largest absolute row sum) equals |W|_1
-  // bit for bit.
-  if (threadIdx.x < M) {
-    const int j = threadIdx.x;
-    float cs = 0.f;
-    for (int i = 0; i < M; ++i) cs += fabsf(W[i * MP + j]);
-    red[j] = cs;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float n1 = 0.f;
-    for (int j = 0; j < M; ++j) n1 = fmaxf(n1, red[j]);
-    red[128] = n1 * n1;            // |W|_1 |W|_inf
-  }
-  __syncthreads();
-  const float scale = red[128];
-  for (int idx = threadIdx.x; idx < 64 * 64; idx += kNsThreads) {
-    const int i = idx >> 6, k = idx & 63;
-    X[i * MP + k] = W[i * MP + k] / scale;     // X0 = W^T / (|W|_1 |W|_inf); W^T == W exactly
-  }
-  __syncthreads();
+  ns_prologue<S, kNsThreads>(sm, landmarks + (size_t)bh * M * d, d, eps, c_exp, true, dbg_dll,
+                             dbg_w, bh);
+  float* W = sm.W;
+  float* X = sm.X;
+  float* P = sm.P;
+  float* Y = sm.Y;
+  float* part = sm.part;
 
   for (int t = 0; t < T; ++t) {
     sym_product<Sh::MK, Sh::NWT, false>(W, X, nullptr, P, part);   // P = W X
@@ -235,10 +183,220 @@ ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
   }
 }
 
+// One product on a CTA pair (m > 32, 2 x 2 warp tiles).  The product's output strips (8 rows x
+// 32 columns, four per 32 x 32 tile, tile-major) are cut in two: CTA rank `crank` computes
+// strips [crank * n / 2, (crank + 1) * n / 2), n = 16 (plain) or 12 (mirrored: the upper
+// tiles).  A warp job is two adjacent strips, 16 rows of one tile; lane (rq, cq) = (lane / 8,
+// lane % 8) holds rows 4rq..4rq+3 and columns 4cq..4cq+3 of it, and warp w takes job w % 4
+// over k quarter w / 4.  Results (with their mirror images) are stored into C; pair_publish
+// then copies this CTA's region into the peer.
+template <int MK, bool kMirror>
+__device__ __forceinline__ void pair_product(const float* __restrict__ A,
+                                             const float* __restrict__ B,
+                                             const float* __restrict__ Xs, float* C,
+                                             float* __restrict__ part, int crank) {
+  constexpr int KS = 4;
+  constexpr int KQ = MK / KS;
+  constexpr int NJOBS = kMirror ? 3 : 4;             // two-strip jobs per CTA
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int job = warp & 3, ks = warp >> 2;
+  const bool active = job < NJOBS;
+  const int pair = crank * NJOBS + job;
+  const int tile = pair >> 1, half = pair & 1;
+  int tr, tc;
+  if (kMirror) {
+    tr = (tile == 2) ? 1 : 0;                        // tiles (0,0), (0,1), (1,1)
+    tc = (tile >= 1) ? 1 : 0;
+  } else {
+    tr = tile >> 1;
+    tc = tile & 1;
+  }
+  const int rq = lane >> 3, cq = lane & 7;
+  const int r0 = 32 * tr + 16 * half + 4 * rq, c0 = 32 * tc + 4 * cq;
+  float acc[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+  if (active) {
+    const float* a = A + (ks * KQ) * kMS + r0;
+    const float* b = B + (ks * KQ) * kMS + c0;
+    float4 av = *reinterpret_cast<const float4*>(a);
+    float4 bv = *reinterpret_cast<const float4*>(b);
+#pragma unroll
+    for (int kk = 0; kk < KQ; ++kk) {
+      const int kn = kk + 1 < KQ ? kk + 1 : kk;
+      const float4 nav = *reinterpret_cast<const float4*>(a + kn * kMS);
+      const float4 nbv = *reinterpret_cast<const float4*>(b + kn * kMS);
+      const float ar[4] = {av.x, av.y, av.z, av.w};
+      const float br[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(ar[r], br[c], acc[r][c]);
+      av = nav;
+      bv = nbv;
+    }
+    if (ks > 0) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        part[(((ks - 1) * 4 + job) * 16 + e) * 32 + lane] = acc[e >> 2][e & 3];
+    }
+  }
+  __syncthreads();
+  if (active && ks == 0) {
+#pragma unroll
+    for (int q = 1; q < KS; ++q)
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        acc[e >> 2][e & 3] += part[(((q - 1) * 4 + job) * 16 + e) * 32 + lane];
+    if constexpr (kMirror) {
+      float v[4][4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float4 x4 = *reinterpret_cast<const float4*>(&Xs[(r0 + r) * kMS + c0]);
+        v[r][0] = 2.f * x4.x - acc[r][0];
+        v[r][1] = 2.f * x4.y - acc[r][1];
+        v[r][2] = 2.f * x4.z - acc[r][2];
+        v[r][3] = 2.f * x4.w - acc[r][3];
+      }
+      if (tr == tc) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int i = r0 + r, j = c0 + c;
+            if (i <= j) {
+              C[i * kMS + j] = v[r][c];
+              C[j * kMS + i] = v[r][c];
+            }
+          }
+      } else {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          *reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]) =
+              make_float4(v[r][0], v[r][1], v[r][2], v[r][3]);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          *reinterpret_cast<float4*>(&C[(c0 + c) * kMS + r0]) =
+              make_float4(v[0][c], v[1][c], v[2][c], v[3][c]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        *reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]) =
+            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Copy this CTA's part of a pair product from C into the peer's copy Cpeer: one 16-byte
+// store per thread (512 threads x 4 floats = 2048 floats, a half of the 64 x 64 matrix).
+// Plain product: rank r owns rows 32r..32r+31.  Mirrored product (strips 0-5 / 6-11 of the
+// upper tiles, with their mirror images): rank 0 owns rows 0-31 x columns 0-31, rows 0-15 x
+// columns 32-63 and rows 32-63 x columns 0-15; rank 1 owns the rest.
+template <bool kMirror>
+__device__ __forceinline__ void pair_publish(const float* __restrict__ C, float* Cpeer,
+                                             int crank) {
+  const int t = threadIdx.x;             // 0 .. 511
+  int row, col;
+  if (!kMirror) {
+    row = 32 * crank + (t >> 4);
+    col = 4 * (t & 15);
+  } else if (crank == 0) {
+    if (t < 256) {                       // rows 0-31, columns 0-31
+      row = t >> 3;
+      col = 4 * (t & 7);
+    } else if (t < 384) {                // rows 0-15, columns 32-63
+      row = (t - 256) >> 3;
+      col = 32 + 4 * (t & 7);
+    } else {                             // rows 32-63, columns 0-15
+      row = 32 + ((t - 384) >> 2);
+      col = 4 * (t & 3);
+    }
+  } else {
+    if (t < 128) {                       // rows 16-31, columns 32-63
+      row = 16 + (t >> 3);
+      col = 32 + 4 * (t & 7);
+    } else if (t < 256) {                // rows 32-63, columns 16-31
+      row = 32 + ((t - 128) >> 2);
+      col = 16 + 4 * (t & 3);
+    } else {                             // rows 32-63, columns 32-63
+      row = 32 + ((t - 256) >> 3);
+      col = 32 + 4 * (t & 7);
+    }
+  }
+  *reinterpret_cast<float4*>(&Cpeer[row * kMS + col]) =
+      *reinterpret_cast<const float4*>(&C[row * kMS + col]);
+}
+
+// One head per cluster of two CTAs (m > 32).  Both CTAs build W and X0; each product is split
+// between them (pair_product) and published by a cluster barrier.
+template <int S>
+__global__ void __launch_bounds__(kNsThreads)
+ns_pair_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
+               float* __restrict__ dbg_dll, float* __restrict__ dbg_w,
+               float* __restrict__ dbg_x, int d, int T, float eps, float c_exp) {
+  using Sh = NsShape<S>;
+  static_assert(Sh::NWT == 2, "the pair split assumes 2 x 2 warp tiles");
+  constexpr int M = Sh::M, MP = kMS;
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int crank = (int)cluster.block_rank();
+  extern __shared__ float4 smem_ns4[];
+  const NsSmem sm = ns_smem_layout<S>(reinterpret_cast<float*>(smem_ns4));
+  const long bh = blockIdx.x >> 1;
+  ns_prologue<S, kNsThreads>(sm, landmarks + (size_t)bh * M * d, d, eps, c_exp, crank == 0,
+                             dbg_dll, dbg_w, bh);
+  float* X = sm.X;
+  float* Y = sm.Y;
+  float* Yp = cluster.map_shared_rank(sm.Y, crank ^ 1);
+  float* Xp = cluster.map_shared_rank(sm.X, crank ^ 1);
+  float* Pp = cluster.map_shared_rank(sm.P, crank ^ 1);
+  cluster.sync();                  // the peer is running before anything is stored into it
+
+  for (int t = 0; t < T; ++t) {
+    pair_product<Sh::MK, false>(sm.W, X, nullptr, sm.P, sm.part, crank);   // P = W X
+    pair_publish<false>(sm.P, Pp, crank);
+    cluster.sync();
+    pair_product<Sh::MK, true>(X, sm.P, X, Y, sm.part, crank);            // Y = 2X - X P
+    pair_publish<true>(Y, Yp, crank);
+    cluster.sync();
+    float* tmp = X; X = Y; Y = tmp;
+    tmp = Xp; Xp = Yp; Yp = tmp;
+  }
+
+  // Both CTAs hold the final X; each writes half of it.
+  const int total = M * M, half = (total + 1) / 2;
+  const int lo = crank == 0 ? 0 : half, hi = crank == 0 ? half : total;
+  for (int idx = lo + threadIdx.x; idx < hi; idx += kNsThreads) {
+    const int i = idx / M, k = idx % M;
+    const float x = X[i * MP + k];
+    xout[(size_t)bh * M * M + idx] = x;
+    if (dbg_x) dbg_x[(size_t)bh * M * M + idx] = x;
+  }
+}
+
 template <int S>
 const void* ns_ptr() { return reinterpret_cast<const void*>(&ns_inverse_kernel<S>); }
 
-const void* pick_ns(int s) {
+template <int S>
+const void* ns_pair_ptr() { return reinterpret_cast<const void*>(&ns_pair_kernel<S>); }
+
+// Kernel for landmark grid side s on clusters of `cluster` CTAs (1, or 2 for s >= 6).
+const void* pick_ns(int s, int cluster) {
+  if (cluster == 2) {
+    switch (s) {
+      case 6: return ns_pair_ptr<6>();
+      case 7: return ns_pair_ptr<7>();
+      case 8: return ns_pair_ptr<8>();
+      default: return nullptr;
+    }
+  }
   switch (s) {
     case 1: return ns_ptr<1>();
     case 2: return ns_ptr<2>();
@@ -257,7 +415,7 @@ const void* pick_ns(int s) {
 template <int S>
 size_t ns_smem_of(int d) {
   using Sh = NsShape<S>;
-  return sizeof(float) * (4 * 64 * (size_t)kMS + 132 + Sh::PART_FLOATS + 64 * (size_t)d);
+  return sizeof(float) * (4 * 64 * (size_t)kMS + kRedFloats + Sh::PART_FLOATS + 64 * (size_t)d);
 }
 
 size_t ns_smem_bytes(int m, int d) {
@@ -274,21 +432,50 @@ size_t ns_smem_bytes(int m, int d) {
   }
 }
 
-cudaError_t ns_configure(int s, size_t smem) {
-  const void* f = pick_ns(s);
+bool ns_cluster_supported(int s, int cluster) { return pick_ns(s, cluster) != nullptr; }
+
+cudaError_t ns_configure(int s, int cluster, size_t smem, int* clusters_per_gpu) {
+  const void* f = pick_ns(s, cluster);
   if (!f) return cudaErrorInvalidValue;
-  return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess || !clusters_per_gpu) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(cluster);
+  cfg.blockDim = dim3(kNsThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(clusters_per_gpu, f, &cfg);
 }
 
 cudaError_t launch_ns(const lapl_attn_plan& p, const float* landmarks, float* x, float* dbg_dll,
                       float* dbg_w, float* dbg_x, cudaStream_t st) {
   const Geometry& g = p.geo;
-  const void* f = pick_ns(g.s);
+  const void* f = pick_ns(g.s, g.ns_cluster);
   if (!f) return cudaErrorInvalidValue;
   int d = g.d, T = p.cfg.ns_steps;
   float eps = p.cfg.eps, c_exp = p.neg_log2e_over_lambda;
   void* args[] = {&landmarks, &x, &dbg_dll, &dbg_w, &dbg_x, &d, &T, &eps, &c_exp};
-  return cudaLaunchKernel(f, dim3((unsigned)g.bh), dim3(kNsThreads), args, g.ns_smem, st);
+  if (g.ns_cluster == 1)
+    return cudaLaunchKernel(f, dim3((unsigned)g.bh), dim3(kNsThreads), args, g.ns_smem, st);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = g.ns_cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(g.bh * g.ns_cluster));
+  cfg.blockDim = dim3(kNsThreads);
+  cfg.dynamicSmemBytes = g.ns_smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, f, args);
 }
 
 }  // namespace lapl

@@ -1,0 +1,134 @@
+// ns_common.cuh -- pieces shared by the Newton-Schulz kernels (ns.cu: CUDA-core products on one
+// CTA or a CTA pair; ns_tc.cu: tensor-core products): the padded matrix shape, the
+// shared-memory layout and the prologue that builds W = k(L, L) + eps I and X0.
+#pragma once
+
+#include "common.cuh"
+
+namespace lapl {
+namespace ns_detail {
+
+
+constexpr int kMS = 68;   // stored row stride: 64 columns (padded) + 4, 16-byte aligned, and
+                          // column-direction stores spread over more banks than with 64
+
+constexpr int kRedFloats = 8 * 64 + 4;   // partial column sums of up to 8 row groups, maxima
+
+template <int S>
+struct NsShape {
+  static constexpr int M = S * S;
+  static constexpr int MK = (M + 3) & ~3;            // k range actually summed
+  static constexpr int NWT = (M + 31) / 32;          // 32x32 warp tiles per side (1 or 2)
+  static constexpr int PART_FLOATS = 4 * 3 * 32 * 32;  // 4 tiles x 3 upper slices x 32 x 32
+};
+
+// Shared-memory layout of both kernels.
+struct NsSmem {
+  float* W;
+  float* X;
+  float* P;
+  float* Y;
+  float* red;
+  float* part;
+  float* sL;
+};
+
+template <int S>
+__device__ __forceinline__ NsSmem ns_smem_layout(float* smem) {
+  NsSmem m;
+  m.W = smem;                   // [64][kMS]
+  m.X = m.W + 64 * kMS;
+  m.P = m.X + 64 * kMS;
+  m.Y = m.P + 64 * kMS;
+  m.red = m.Y + 64 * kMS;       // partial column sums and maxima [kRedFloats]
+  m.part = m.red + kRedFloats;  // partial tiles of the k slices
+  m.sL = m.part + NsShape<S>::PART_FLOATS;   // [d][64], channel-major
+  return m;
+}
+
+// W = k(L, L) + eps I and X0 = W^T / (|W|_1 |W|_inf) in shared memory (zero-padded to 64 x 64,
+// row stride kMS), for a CTA of NT threads.  The debug copies of D_LL and W are written when
+// write_debug is set.  red holds NT / 64 x 64 partial column sums plus two maxima
+// (kRedFloats).  Ends synchronised.
+//
+// Thread t owns column k = t % 64 and the RPG = 64 / (NT / 64) rows starting at
+// (t / 64) * RPG; per channel it reads its own landmark value and RPG / 4 broadcast 16-byte
+// pieces, and keeps RPG independent sums.  Each distance adds |L_ic - L_kc| over c ascending,
+// the same terms in the same order for (i, k) and (k, i), so W is exactly symmetric.
+template <int S, int NT>
+__device__ __forceinline__ void ns_prologue(const NsSmem& sm, const float* __restrict__ Lg, int d,
+                                            float eps, float c_exp, bool write_debug,
+                                            float* __restrict__ dbg_dll,
+                                            float* __restrict__ dbg_w, long bh) {
+  constexpr int M = S * S, MP = kMS;
+  constexpr int G = NT / 64, RPG = 64 / G;
+  static_assert(NT % 64 == 0 && RPG % 4 == 0, "row groups of a multiple of 4 rows");
+  float* W = sm.W;
+  float* X = sm.X;
+  float* red = sm.red;
+  float* sL = sm.sL;
+  // Landmarks, stored channel-major (sL[c * 64 + j], zero for j >= m).
+  for (int i = threadIdx.x; i < 64 * d; i += NT) {
+    const int c = i >> 6, j = i & 63;
+    sL[i] = j < M ? Lg[j * d + c] : 0.f;
+  }
+  __syncthreads();
+
+  const int k = threadIdx.x & 63, g = threadIdx.x >> 6, i0 = g * RPG;
+  float acc[RPG];
+#pragma unroll
+  for (int r = 0; r < RPG; ++r) acc[r] = 0.f;
+  if (i0 < M) {                                   // uniform over the 64 threads of a group
+#pragma unroll 4
+    for (int c = 0; c < d; ++c) {
+      const float lk = sL[c * 64 + k];
+#pragma unroll
+      for (int r4 = 0; r4 < RPG / 4; ++r4) {
+        const float4 li = *reinterpret_cast<const float4*>(&sL[c * 64 + i0 + 4 * r4]);
+        acc[4 * r4 + 0] += fabsf(li.x - lk);
+        acc[4 * r4 + 1] += fabsf(li.y - lk);
+        acc[4 * r4 + 2] += fabsf(li.z - lk);
+        acc[4 * r4 + 3] += fabsf(li.w - lk);
+      }
+    }
+  }
+  // W = exp(-D_LL / lambda) + eps I, zero outside m x m; k(x, x) = 1 exactly (D_LL[i][i] = 0).
+  float cs = 0.f;
+#pragma unroll
+  for (int r = 0; r < RPG; ++r) {
+    const int i = i0 + r;
+    float w = 0.f;
+    if (i < M && k < M) {
+      w = (i == k) ? 1.f + eps : laplacian_from_distance(acc[r], c_exp);
+      if (write_debug) {
+        const size_t o = ((size_t)bh * M + i) * M + k;
+        if (dbg_dll) dbg_dll[o] = acc[r];
+        if (dbg_w) dbg_w[o] = w;
+      }
+    }
+    acc[r] = w;
+    W[i * MP + k] = w;
+    cs += fabsf(w);
+  }
+  red[g * 64 + k] = cs;
+  __syncthreads();
+  // |W|_1 = largest absolute column sum; W is exactly symmetric, so |W|_inf (largest absolute
+  // row sum) equals it.
+  if (threadIdx.x < 64) {
+    float col = 0.f;
+#pragma unroll
+    for (int q = 0; q < G; ++q) col += red[q * 64 + threadIdx.x];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) col = fmaxf(col, __shfl_xor_sync(0xffffffffu, col, o));
+    if ((threadIdx.x & 31) == 0) red[G * 64 + (threadIdx.x >> 5)] = col;
+  }
+  __syncthreads();
+  const float n1 = fmaxf(red[G * 64], red[G * 64 + 1]);
+  const float scale = n1 * n1;                    // |W|_1 |W|_inf
+#pragma unroll
+  for (int r = 0; r < RPG; ++r) X[(i0 + r) * MP + k] = acc[r] / scale;   // X0 = W^T / scale
+  __syncthreads();
+}
+
+}  // namespace ns_detail
+}  // namespace lapl

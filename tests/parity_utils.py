@@ -52,8 +52,8 @@ def to_device(arr: np.ndarray, dtype: str):
 def run_gpu(w, q, k, v, bias=None, debug=False, out_dtype="f32", info=None, **cfg_over):
     """Run the CUDA path via the C ABI.  Returns (out float64 ndarray, dict of intermediates).
 
-    info: optional dict that receives "uses_tma" (distance kernel fed by TMA) and
-    "device_errors" (the device error word after the forward, then cleared)."""
+    info: optional dict that receives the plan's launch choices (lapl_attn_plan_info fields)
+    and "device_errors" (the device error word after the forward, then cleared)."""
     import torch
     import laplacian_nystr_attention_gb300 as lna
     cfg = w.config()
@@ -74,7 +74,7 @@ def run_gpu(w, q, k, v, bias=None, debug=False, out_dtype="f32", info=None, **cf
     out = att.forward(dq, dk, dv, bias=db, debug=dbg)
     torch.cuda.synchronize()
     if info is not None:
-        info["uses_tma"] = lna.lapl_attn_uses_tma(att.handle)
+        info.update(lna.lapl_attn_plan_info_get(att.handle))
         flags = ctypes.c_uint(0)
         lna._lib.LIB.lapl_attn_device_errors(att.handle, torch.cuda.current_stream().cuda_stream,
                                             ctypes.byref(flags))

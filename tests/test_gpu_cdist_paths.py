@@ -80,7 +80,7 @@ def test_both_feeds_match_oracle_and_each_other(case, monkeypatch):
         info = {}
         out, g = run_gpu(w, q, k, v, debug=True, info=info)
         assert info["device_errors"] == 0, feed
-        assert info["uses_tma"] == (expect_tma and feed == "tma"), feed
+        assert info["cdist_tma"] == int(expect_tma and feed == "tma"), feed
         for name in ("d_ql", "d_lk", "d_ll", "landmarks"):
             if _dyadic_window(w):
                 assert np.array_equal(g[name], o[name]), (feed, name)
@@ -106,7 +106,7 @@ def test_workload_shape_feeds_agree(name, monkeypatch):
         monkeypatch.setenv("LAPL_ATTN_CDIST_FEED", feed)
         info = {}
         outs[feed] = run_gpu(w, q, k, v, debug=True, info=info)
-        assert info["uses_tma"] == (feed == "tma")
+        assert info["cdist_tma"] == int(feed == "tma")
         assert info["device_errors"] == 0
     (o1, g1), (o2, g2) = outs["tma"], outs["cp.async"]
     assert np.array_equal(g1["d_ql"], g2["d_ql"])
@@ -126,6 +126,6 @@ def test_automatic_feed_choice(over, expect, monkeypatch):
     w = TINY.replace(**over)
     h = lna.lapl_attn_create(lna.make_config(**{**w.config(), "in_dtype": w.dtype}))
     try:
-        assert lna.lapl_attn_uses_tma(h) == expect
+        assert lna.lapl_attn_plan_info_get(h)["cdist_tma"] == int(expect)
     finally:
         lna.lapl_attn_destroy(h)
