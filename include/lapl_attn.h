@@ -17,8 +17,10 @@
  *
  * Layouts: Q, K, V, O are [B, H, N, d] contiguous (C order), token n = r * grid_w + c.
  * Every buffer is owned by the caller.  The handle holds host state only: the configuration,
- * three CUDA events and one auxiliary stream (highest priority) that runs pooling and the
- * Newton-Schulz solve while the launching stream runs the distance kernel.  The library's
+ * two CUDA events and one auxiliary stream.  After pooling the forward splits into two
+ * chains, the Newton-Schulz solve and the distance + B V kernels; the longer one runs on the
+ * launching stream, the other on the auxiliary stream, and they join before M = X (B V).  The
+ * library's
  * device globals are a 4-byte error word and the scratch of lapl_attn_forward_noalloc.  No
  * entry point allocates device memory; forward() never synchronises the host.
  *
@@ -138,13 +140,14 @@ lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void
 
 /*
  * Stage timing, a profiling aid.  After lapl_attn_set_timing(h, 1) every forward records CUDA
- * events (created here, host-owned) around its six stages: on the side stream for pooling
- * (from the start of the forward on the launching stream) and Newton-Schulz, on the launching
- * stream for distances (from the end of pooling), B V, finish and output.
+ * events (created here, host-owned) on the stream that runs each kernel (the solve runs on the
+ * launching stream and the distance and B V kernels on the side stream when plan_info's
+ * ns_exclusive is 1; the other way round otherwise).
  * lapl_attn_stage_times() waits for the events of the last forward (it synchronises the host
  * with them) and writes the elapsed milliseconds of
- *   ms[0] pooling, ms[1] Newton-Schulz, ms[2] distance kernel, ms[3] B V, ms[4] finish,
- *   ms[5] output.
+ *   ms[0] pooling, ms[1] Newton-Schulz, ms[2] distance kernel, ms[3] B V partials, ms[4]
+ *   finish (the wait for the solve, then the B V reduction and M = X (B V)), ms[5] output
+ *   (column statistics, whitening and O = A^ M).
  * LAPL_ERR_INVALID_ARG if timing is off or no forward ran since it was switched on.
  */
 lapl_status lapl_attn_set_timing(lapl_attn_handle h, int enable);
@@ -154,8 +157,8 @@ lapl_status lapl_attn_stage_times(lapl_attn_handle h, float* ms);
  * Timeline of the last timed forward (same events as lapl_attn_stage_times, same waiting and
  * errors): milliseconds since the start of the forward on the launching stream of
  *   ms[0] start (0), ms[1] pooling done, ms[2] Newton-Schulz start, ms[3] Newton-Schulz done,
- *   ms[4] distance kernel start (the launching stream has seen pooling done), ms[5] distance
- *   kernel done, ms[6] B V done, ms[7] finish done, ms[8] output done.
+ *   ms[4] distance kernel start (its stream has seen pooling done), ms[5] distance kernel
+ *   done, ms[6] B V partials done, ms[7] M = X (B V) done, ms[8] output done.
  */
 lapl_status lapl_attn_stage_marks(lapl_attn_handle h, float* ms);
 
@@ -183,7 +186,8 @@ typedef struct {
                          m > 32, on request); same X bit for bit                            */
   int ns_tensor_core; /* 1: the solve's products run on the tensor cores (TF32 high/low
                          split, fp32 accumulation); X agrees to rounding                     */
-  int ns_exclusive;   /* 1: the solve's CTAs have their SMs to themselves                    */
+  int ns_exclusive;   /* 1: the solve is the longer chain and runs first, on the launching
+                         stream, with SMs to itself; 0: the distance kernel is               */
   int bv_splits;      /* CTAs per head of the B V kernel                                     */
 } lapl_attn_plan_info;
 

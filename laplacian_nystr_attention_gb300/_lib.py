@@ -182,7 +182,7 @@ def lapl_attn_stage_times(handle) -> dict:
 
 
 MARKS = ("start", "pool_done", "ns_start", "ns_done", "cdist_start", "cdist_done", "bv_done",
-         "finish_done", "output_done")
+         "mix_done", "output_done")
 
 
 def lapl_attn_stage_marks(handle) -> dict:

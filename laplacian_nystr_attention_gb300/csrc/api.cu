@@ -1,18 +1,23 @@
 // api.cu -- the C ABI (include/lapl_attn.h): validation, plan, workspace layout, and the
 // stream-ordered launch sequence of one forward pass.
 //
-//   fork ---------------------------------------------> side stream (highest priority):
-//                                                          K1 pool     L = avg-pool(K)
-//   wait (L) <-------------------------------------------- pooled
-//   K2 cdist     A^T + run statistics (queries), B^T (keys) K3 Newton-Schulz (W, X)
-//   K2b bv       B V partials per token split
-//   join (X) <-------------------------------------------- solved
-//   K4 finish    mean/rstd, B V, M = X (B V)              stream
-//   K5 output    O = whiten(A) M                          stream
+// When the solve is the longer chain and needs few SMs (B*H <= SMs/4; the solve's CTAs then
+// get SMs of their own):
+//   launching stream                               side stream
+//   K1 pool      L = avg-pool(K)
+//   fork (L) -------------------------------------> K2 cdist  A^T + run statistics, B^T
+//   K3 solve     W, X (Newton-Schulz)               K2b bv    B V partials per token split
+//   join <----------------------------------------- done (long before the solve)
+//   K4 mix       B V = sum of partials, M = X (B V)
+//   K5 output    column statistics, O = whiten(A) M
+// The solve follows pooling on the same stream, so its CTAs are placed the moment pooling
+// ends; the distance kernel takes the SMs that are left.
 //
-// The solve is the longest dependency chain.  It follows pooling on the same stream, so its
-// CTAs are dispatched the moment pooling ends; the distance kernel waits for pooling across
-// streams and takes the SMs that are left.
+// Otherwise the distance kernel is the longest chain: K1 pool, K2 cdist and K2b bv run on the
+// launching stream and the solve on the side stream, joined before K4.
+//
+// K5 is a programmatic dependent launch of K4: it merges the column statistics and loads and
+// whitens its A tile while M is computed.
 #include <math.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -149,9 +154,14 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
       g.ns_tc = false;
     }
     if (nk && strcmp(nk, "tc") == 0) g.ns_tc = true;
-    // With few heads the solve's CTAs ask for (almost) a whole SM's shared memory, so no other
-    // kernel's CTA shares their SM.
-    g.ns_exclusive = g.bh * g.ns_cluster <= p->num_sms / 4;
+    // The solve goes first, on SMs of its own (its CTAs ask for almost a whole SM's shared
+    // memory, so no other kernel's CTA shares their SM), when it uses few SMs and is the
+    // longer of the two chains after pooling.  Chain estimates, from GB300 measurements: the
+    // solve about 15 us + 2.2 us per step (4 us on the CUDA cores); the distance and B V
+    // kernels about 6e6 (token, landmark, channel) elements per us.
+    const double ns_us = 15.0 + (g.ns_tc ? 2.2 : 4.0) * cfg->ns_steps;
+    const double cd_us = 2.0 * (double)g.bh * g.n * g.m * g.d / 6e6;
+    g.ns_exclusive = g.bh * g.ns_cluster <= p->num_sms / 4 && ns_us >= cd_us;
     int smem_max = 0;
     e = cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
     g.ns_smem = g.ns_tc ? ns_tc_smem_bytes(g.d) : ns_smem_bytes(g.m, g.d);
@@ -212,8 +222,8 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
     if (g.ns_exclusive) slots -= g.bh * g.ns_cluster * per_sm;
     const long long ctas = std::min<long long>(slots, chunks);
     setup_cdist_partition(g, (int)std::max<long long>(ctas, 1));
-    g.fin_smem = finish_smem_bytes(g.m, g.cd_runs_q, g.bv_splits);
-    e = finish_configure(g.fin_smem);
+    g.fin_smem = mix_smem_bytes(g.m, g.bv_splits);
+    e = mix_configure(g.fin_smem);
     if (e != cudaSuccess) {
       set_error(p, e, "create/configure-finish");
       delete p;
@@ -236,24 +246,19 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   w.bt = take(bh * m * n);
   w.stats = take(bh * g.cd_runs_q * 3 * m);
   w.bvp = take(bh * g.bv_splits * m * d);
+
   w.mmat = take(bh * m * d);
-  w.mu = take(bh * m);
-  w.rstd = take(bh * m);
   w.total = off;
 
-  // The side stream (Newton-Schulz, the longest dependency chain) gets the highest priority.
-  int prio_least = 0, prio_greatest = 0;
-  e = cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest);
-  if (e == cudaSuccess)
-    e = cudaStreamCreateWithPriority(&p->side_stream, cudaStreamNonBlocking, prio_greatest);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
+  // The side stream runs the shorter of the two chains (see the launch sequence).
+  e = cudaStreamCreateWithFlags(&p->side_stream, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_pool, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     set_error(p, e, "create/stream");
     if (p->side_stream) cudaStreamDestroy(p->side_stream);
-    if (p->ev_fork) cudaEventDestroy(p->ev_fork);
     if (p->ev_join) cudaEventDestroy(p->ev_join);
+    if (p->ev_pool) cudaEventDestroy(p->ev_pool);
     delete p;
     return LAPL_ERR_CUDA;
   }
@@ -293,9 +298,9 @@ static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k,
   float* Bt = reinterpret_cast<float*>(ws + p->ws.bt);
   float* stats = reinterpret_cast<float*>(ws + p->ws.stats);
   float* bvp = reinterpret_cast<float*>(ws + p->ws.bvp);
+
   float* M = reinterpret_cast<float*>(ws + p->ws.mmat);
-  float* mu = reinterpret_cast<float*>(ws + p->ws.mu);
-  float* rstd = reinterpret_cast<float*>(ws + p->ws.rstd);
+
   const lapl_attn_debug none = {};
   const lapl_attn_debug& D = dbg ? *dbg : none;
 
@@ -312,30 +317,53 @@ static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k,
 #define LAPL_MARK(i, s)                                              \
   if (tm) LAPL_TRY(cudaEventRecord(p->ev_stage[i], s), "forward/timing")
 
-  LAPL_MARK(0, st);
-  LAPL_TRY(cudaEventRecord(p->ev_fork, st), "forward/fork");
-  LAPL_TRY(cudaStreamWaitEvent(p->side_stream, p->ev_fork, 0), "forward/fork-wait");
-  LAPL_TRY(launch_pool(*p, k, L, D.landmarks, p->side_stream), "forward/pool");
-  LAPL_MARK(1, p->side_stream);
-  LAPL_TRY(cudaEventRecord(p->ev_pool, p->side_stream), "forward/pooled");
-  LAPL_MARK(5, p->side_stream);
-  LAPL_TRY(p->geo.ns_tc ? launch_ns_tc(*p, L, X, D.d_ll, D.w, D.x, p->side_stream)
-                        : launch_ns(*p, L, X, D.d_ll, D.w, D.x, p->side_stream),
-           "forward/newton-schulz");
-  LAPL_MARK(6, p->side_stream);
-  LAPL_TRY(cudaEventRecord(p->ev_join, p->side_stream), "forward/join");
-  LAPL_TRY(cudaStreamWaitEvent(st, p->ev_pool, 0), "forward/pooled-wait");
-  LAPL_MARK(8, st);
-  LAPL_TRY(launch_cdist(*p, q, k, v, L, At, Bt, stats, D.d_ql, D.d_lk, D.a, st), "forward/cdist");
-  LAPL_MARK(2, st);
-  LAPL_TRY(launch_bv(*p, Bt, v, bvp, st), "forward/bv");
-  LAPL_MARK(7, st);
+  cudaStream_t side = p->side_stream;
+  auto launch_solve = [&](cudaStream_t s) {
+    return p->geo.ns_tc ? launch_ns_tc(*p, L, X, D.d_ll, D.w, D.x, s)
+                        : launch_ns(*p, L, X, D.d_ll, D.w, D.x, s);
+  };
+  LAPL_MARK(kMarkStart, st);
+  if (p->geo.ns_exclusive) {
+    // The solve is the longest chain: pooling -> solve -> M -> output on the launching stream;
+    // the solve's CTAs are placed the moment pooling ends.  The distance kernel and
+    // B V run next to it on the side stream, which is done long before the solve.
+    LAPL_TRY(launch_pool(*p, k, L, D.landmarks, st), "forward/pool");
+    LAPL_MARK(kMarkPoolDone, st);
+    LAPL_TRY(cudaEventRecord(p->ev_pool, st), "forward/pooled");
+    LAPL_MARK(kMarkNsStart, st);
+    LAPL_TRY(launch_solve(st), "forward/newton-schulz");
+    LAPL_MARK(kMarkNsDone, st);
+    LAPL_TRY(cudaStreamWaitEvent(side, p->ev_pool, 0), "forward/pooled-wait");
+    LAPL_MARK(kMarkCdistStart, side);
+    LAPL_TRY(launch_cdist(*p, q, k, v, L, At, Bt, stats, D.d_ql, D.d_lk, D.a, side),
+             "forward/cdist");
+    LAPL_MARK(kMarkCdistDone, side);
+    LAPL_TRY(launch_bv(*p, Bt, v, bvp, side), "forward/bv");
+    LAPL_MARK(kMarkBvDone, side);
+    LAPL_TRY(cudaEventRecord(p->ev_join, side), "forward/join");
+  } else {
+    // Pooling -> distances -> B V is the longest chain and runs on the launching stream; the
+    // solve runs next to it on the side stream.
+    LAPL_TRY(launch_pool(*p, k, L, D.landmarks, st), "forward/pool");
+    LAPL_MARK(kMarkPoolDone, st);
+    LAPL_TRY(cudaEventRecord(p->ev_pool, st), "forward/pooled");
+    LAPL_TRY(cudaStreamWaitEvent(side, p->ev_pool, 0), "forward/pooled-wait");
+    LAPL_MARK(kMarkNsStart, side);
+    LAPL_TRY(launch_solve(side), "forward/newton-schulz");
+    LAPL_MARK(kMarkNsDone, side);
+    LAPL_TRY(cudaEventRecord(p->ev_join, side), "forward/join");
+    LAPL_MARK(kMarkCdistStart, st);
+    LAPL_TRY(launch_cdist(*p, q, k, v, L, At, Bt, stats, D.d_ql, D.d_lk, D.a, st),
+             "forward/cdist");
+    LAPL_MARK(kMarkCdistDone, st);
+    LAPL_TRY(launch_bv(*p, Bt, v, bvp, st), "forward/bv");
+    LAPL_MARK(kMarkBvDone, st);
+  }
   LAPL_TRY(cudaStreamWaitEvent(st, p->ev_join, 0), "forward/join-wait");
-  LAPL_TRY(launch_finish(*p, stats, bvp, X, M, mu, rstd, D.mu, D.rstd, D.bv, D.m, st),
-           "forward/finish");
-  LAPL_MARK(3, st);
-  LAPL_TRY(launch_output(*p, At, M, mu, rstd, bias, out, st), "forward/output");
-  LAPL_MARK(4, st);
+  LAPL_TRY(launch_mix(*p, X, bvp, M, D.bv, D.m, st), "forward/mix");
+  LAPL_MARK(kMarkMixDone, st);
+  LAPL_TRY(launch_output(*p, At, M, stats, bias, out, D.mu, D.rstd, st), "forward/output");
+  LAPL_MARK(kMarkOutputDone, st);
   if (tm) p->timed_once = true;
 #undef LAPL_MARK
 #undef LAPL_TRY
@@ -427,7 +455,7 @@ lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void
 lapl_status lapl_attn_set_timing(lapl_attn_handle h, int enable) {
   if (!h) return LAPL_ERR_INVALID_ARG;
   if (enable && !h->ev_stage[0]) {
-    for (int i = 0; i < 9; ++i) {
+    for (int i = 0; i < kMarks; ++i) {
       cudaError_t e = cudaEventCreate(&h->ev_stage[i]);
       if (e != cudaSuccess) {
         set_error(h, e, "set_timing");
@@ -440,11 +468,18 @@ lapl_status lapl_attn_set_timing(lapl_attn_handle h, int enable) {
   return LAPL_OK;
 }
 
+static cudaError_t wait_marks(lapl_attn_handle h) {
+  cudaError_t e = cudaEventSynchronize(h->ev_stage[kMarkOutputDone]);
+  if (e == cudaSuccess) e = cudaEventSynchronize(h->ev_stage[kMarkNsDone]);
+  return e;
+}
+
 lapl_status lapl_attn_stage_times(lapl_attn_handle h, float* ms) {
   if (!h || !ms || !h->timing || !h->timed_once) return LAPL_ERR_INVALID_ARG;
-  cudaError_t e = cudaEventSynchronize(h->ev_stage[4]);
-  if (e == cudaSuccess) e = cudaEventSynchronize(h->ev_stage[6]);
-  const int pairs[6][2] = {{0, 1}, {5, 6}, {1, 2}, {2, 7}, {7, 3}, {3, 4}};
+  cudaError_t e = wait_marks(h);
+  const int pairs[6][2] = {{kMarkStart, kMarkPoolDone},     {kMarkNsStart, kMarkNsDone},
+                           {kMarkCdistStart, kMarkCdistDone}, {kMarkCdistDone, kMarkBvDone},
+                           {kMarkBvDone, kMarkMixDone},       {kMarkMixDone, kMarkOutputDone}};
   for (int i = 0; i < 6 && e == cudaSuccess; ++i)
     e = cudaEventElapsedTime(&ms[i], h->ev_stage[pairs[i][0]], h->ev_stage[pairs[i][1]]);
   if (e != cudaSuccess) {
@@ -456,12 +491,9 @@ lapl_status lapl_attn_stage_times(lapl_attn_handle h, float* ms) {
 
 lapl_status lapl_attn_stage_marks(lapl_attn_handle h, float* ms) {
   if (!h || !ms || !h->timing || !h->timed_once) return LAPL_ERR_INVALID_ARG;
-  cudaError_t e = cudaEventSynchronize(h->ev_stage[4]);
-  if (e == cudaSuccess) e = cudaEventSynchronize(h->ev_stage[6]);
-  // start, pool end, NS start, NS end, cdist start, cdist end, bv end, finish end, output end
-  const int order[9] = {0, 1, 5, 6, 8, 2, 7, 3, 4};
-  for (int i = 0; i < 9 && e == cudaSuccess; ++i)
-    e = cudaEventElapsedTime(&ms[i], h->ev_stage[0], h->ev_stage[order[i]]);
+  cudaError_t e = wait_marks(h);
+  for (int i = 0; i < kMarks && e == cudaSuccess; ++i)
+    e = cudaEventElapsedTime(&ms[i], h->ev_stage[kMarkStart], h->ev_stage[i]);
   if (e != cudaSuccess) {
     set_error(h, e, "stage_marks");
     return LAPL_ERR_CUDA;
@@ -506,11 +538,10 @@ lapl_status lapl_attn_plan_info_get(lapl_attn_handle h, lapl_attn_plan_info* inf
 
 lapl_status lapl_attn_destroy(lapl_attn_handle h) {
   if (!h) return LAPL_OK;
-  for (int i = 0; i < 9; ++i)
+  for (int i = 0; i < kMarks; ++i)
     if (h->ev_stage[i]) cudaEventDestroy(h->ev_stage[i]);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
   if (h->ev_pool) cudaEventDestroy(h->ev_pool);
-  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
   if (h->side_stream) cudaStreamDestroy(h->side_stream);
   delete h;
   return LAPL_OK;

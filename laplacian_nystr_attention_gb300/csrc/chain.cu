@@ -9,13 +9,13 @@
 // bv_kernel (one CTA per (batch, head, token split)):
 //   partial B V of the split's tokens from B^T [BH, m, N] and V, register-tiled on the CUDA
 //   cores (4 landmarks x 4 channels per thread, 8 shared loads per 64 FMAs).
-// finish_kernel (one CTA per (batch, head)):
-//   merges the per-tile (mean, M2) of the distance kernel in tile order (Chan's pairwise
-//   update), reduces the per-split partials of B V in split order, and forms M = X (B V).
+// mix_kernel (per (batch, head, 8 value columns)), after the Newton-Schulz solve is joined:
+//   reduces the per-split partials of B V in split order and forms M = X (B V).
 //   Fixed reduction orders: the result is bit-reproducible run to run.
 // output_kernel (one CTA per (batch, head, token tile)):
-//   loads the A^T tile, whitens it on the way into shared memory, and writes O = A^ M with a
-//   4 tokens x 4 channels register tile per thread.
+//   merges the head's per-run (mean, M2) of the distance kernel in CTA order (Chan's pairwise
+//   update), loads the A^T tile and whitens it on the way into shared memory, then (after the
+//   M kernel) writes O = A^ M with a 4 tokens x 4 channels register tile per thread.
 #include "common.cuh"
 
 namespace lapl {
@@ -154,6 +154,7 @@ bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __r
     for (int q = 0; q < KS; ++q) sum += red[(r * 4 + cc) * nthreads + q * set + lgi * cqn + cqi];
     dst[i] = sum;
   }
+
 }
 
 constexpr int kFinishThreads = 256;
@@ -164,16 +165,13 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(src) : "memory");
 }
 
-// grid (BH * column chunks): CTA (bh, cc) reduces the B V partials of columns
-// [cc*8, cc*8+8) and forms those columns of M = X (B V); chunk 0 also merges the statistics.
-// Every global read is issued up front as an asynchronous copy, so the kernel waits for one
-// round trip to memory instead of one per dependent load.
+// mix_kernel, grid (BH * column chunks) -- the one step that waits for the Newton-Schulz solve:
+// CTA (bh, cc) sums the B V partials of columns [cc*8, cc*8+8) over the token splits (in split
+// order) and forms those columns of M = X (B V).  Every read is issued up front as an
+// asynchronous copy, so the kernel waits for one round trip to memory.
 __global__ void __launch_bounds__(kFinishThreads)
-finish_kernel(const float* __restrict__ stats, const float* __restrict__ bvp,
-              const float* __restrict__ xg, float* __restrict__ mmat, float* __restrict__ mu,
-              float* __restrict__ rstd, float* __restrict__ dbg_mu, float* __restrict__ dbg_rstd,
-              float* __restrict__ dbg_bv, float* __restrict__ dbg_m, int m, int d, int n,
-              const Partition pt, int runs_q, int bv_splits, float delta) {
+mix_kernel(const float* __restrict__ xg, const float* __restrict__ bvp, float* __restrict__ mmat,
+           float* __restrict__ dbg_bv, float* __restrict__ dbg_m, int m, int d, int bv_splits) {
   extern __shared__ float4 smem_fin4[];
   float* smem = reinterpret_cast<float*>(smem_fin4);
   const int chunks = (d + kFinishCols - 1) / kFinishCols;
@@ -181,18 +179,12 @@ finish_kernel(const float* __restrict__ stats, const float* __restrict__ bvp,
   const int cc = blockIdx.x % chunks;
   const int c0 = cc * kFinishCols;
   const int cw = min(kFinishCols, d - c0);
-
-  // Statistics slots of this head: one per distance-kernel CTA range that met its query
-  // tokens, in CTA order.
-  const long long fq = (long long)bh * n;
-  const int slot0 = part_owner(pt, fq);
-  const int nq = part_owner(pt, fq + n - 1) - slot0 + 1;
-
-  float* sX = smem;                                 // [m][m]
-  float* sP = sX + m * m;                           // [bv_splits][m][kFinishCols] partials
-  float* sS = sP + (size_t)bv_splits * m * kFinishCols;   // [nq][3][m] statistics slots
-  float* sBV = sS + (size_t)runs_q * 3 * m;         // [m][kFinishCols]
-
+  float* sX = smem;                                        // [m][m]
+  float* sP = sX + m * m;                                  // [bv_splits][m][kFinishCols]
+  float* sBV = sP + (size_t)bv_splits * m * kFinishCols;   // [m][kFinishCols]
+  // The output kernel may start now: it prepares its A tile and waits for this grid before
+  // it reads M.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   for (int i = threadIdx.x; i < m * m; i += kFinishThreads) cp_async4(&sX[i], &xg[(size_t)bh * m * m + i]);
   const float* pbase = bvp + (size_t)bh * bv_splits * m * d + c0;
   for (int i = threadIdx.x; i < bv_splits * m * cw; i += kFinishThreads) {
@@ -200,14 +192,8 @@ finish_kernel(const float* __restrict__ stats, const float* __restrict__ bvp,
     const int j = rest / cw, c = rest % cw;
     cp_async4(&sP[(sp * m + j) * kFinishCols + c], &pbase[((size_t)sp * m + j) * d + c]);
   }
-  if (cc == 0) {
-    const float* sbase = stats + (size_t)bh * runs_q * 3 * m;
-    for (int i = threadIdx.x; i < nq * 3 * m; i += kFinishThreads) cp_async4(&sS[i], &sbase[i]);
-  }
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
   __syncthreads();
-
-  // B V columns of this chunk: sum over the token splits in order.
   for (int i = threadIdx.x; i < m * cw; i += kFinishThreads) {
     const int j = i / cw, c = i % cw;
     float acc = 0.f;
@@ -215,32 +201,7 @@ finish_kernel(const float* __restrict__ stats, const float* __restrict__ bvp,
     sBV[j * kFinishCols + c] = acc;
     if (dbg_bv) dbg_bv[((size_t)bh * m + j) * d + c0 + c] = acc;
   }
-
-  // Column statistics (chunk 0): Chan's merge of the slots' (count, mean, M2), in order.
-  if (cc == 0) {
-    for (int j = threadIdx.x; j < m; j += kFinishThreads) {
-      float cnt = 0.f, mean = 0.f, m2 = 0.f;
-      for (int sp = 0; sp < nq; ++sp) {
-        const float nb = sS[sp * 3 * m + j];
-        const float mb = sS[sp * 3 * m + m + j];
-        const float m2b = sS[sp * 3 * m + 2 * m + j];
-        const float tot = cnt + nb;
-        const float dlt = mb - mean;
-        mean += dlt * (nb / tot);
-        m2 += m2b + dlt * dlt * (cnt * nb / tot);
-        cnt = tot;
-      }
-      const float var = m2 / (float)n;
-      const float rs = 1.f / sqrtf(var + delta);
-      mu[(size_t)bh * m + j] = mean;
-      rstd[(size_t)bh * m + j] = rs;
-      if (dbg_mu) dbg_mu[(size_t)bh * m + j] = mean;
-      if (dbg_rstd) dbg_rstd[(size_t)bh * m + j] = rs;
-    }
-  }
   __syncthreads();
-
-  // M[:, chunk] = X (B V)[:, chunk].
   for (int i = threadIdx.x; i < m * cw; i += kFinishThreads) {
     const int j = i / cw, c = i % cw;
     float acc = 0.f;
@@ -256,9 +217,10 @@ constexpr int kOutThreads = 256;
 template <bool kOutBf16>
 __global__ void __launch_bounds__(kOutThreads)
 output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
-              const float* __restrict__ mu, const float* __restrict__ rstd,
-              const float* __restrict__ bias, void* __restrict__ out, int m, int d, int n,
-              int heads, int tile, int tiles, int whiten) {
+              const float* __restrict__ stats, const float* __restrict__ bias,
+              void* __restrict__ out, float* __restrict__ dbg_mu, float* __restrict__ dbg_rstd,
+              int m, int d, int n, int heads, int tile, int tiles, int whiten,
+              const Partition pt, int runs_q, float delta) {
   extern __shared__ float4 smem_out4[];
   float* smem = reinterpret_cast<float*>(smem_out4);
   const long bh = blockIdx.x / tiles;
@@ -269,17 +231,41 @@ output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
   float* sA = sM + m * d;           // [m][tile] whitened A, landmark-major
   float* sCoef = sA + m * tile;     // mean [m], scale [m], bias [m]
 
-  for (int i = threadIdx.x; i < m * d; i += kOutThreads) sM[i] = mmat[(size_t)bh * m * d + i];
-  for (int j = threadIdx.x; j < m; j += kOutThreads) {
-    float mean = 0.f, scale = 1.f, b = 0.f;
-    if (whiten) {
-      mean = mu[(size_t)bh * m + j];
-      scale = rstd[(size_t)bh * m + j];
-      b = bias ? bias[(size_t)h * m + j] : 0.f;
+  // Everything up to the wait below reads results of earlier kernels only (A^T, the
+  // statistics), so with a programmatic launch it overlaps the M = X (B V) kernel before it.
+  // Column statistics of the head: Chan's pairwise merge of the distance kernel's per-run
+  // (count, mean, M2) in CTA order; variance over the N tokens.
+  if (whiten) {
+    const long long fq = (long long)bh * n;
+    const int nq = part_owner(pt, fq + n - 1) - part_owner(pt, fq) + 1;
+    const float* st = stats + (size_t)bh * runs_q * 3 * m;
+    for (int j = threadIdx.x; j < m; j += kOutThreads) {
+      float cnt = 0.f, mean = 0.f, m2 = 0.f;
+      for (int q = 0; q < nq; ++q) {
+        const float nb = st[q * 3 * m + j];
+        const float mb = st[q * 3 * m + m + j];
+        const float m2b = st[q * 3 * m + 2 * m + j];
+        const float tot = cnt + nb;
+        const float dlt = mb - mean;
+        mean += dlt * (nb / tot);
+        m2 += m2b + dlt * dlt * (cnt * nb / tot);
+        cnt = tot;
+      }
+      const float rs = 1.f / sqrtf(m2 / (float)n + delta);
+      sCoef[j] = mean;
+      sCoef[m + j] = rs;
+      sCoef[2 * m + j] = bias ? bias[(size_t)h * m + j] : 0.f;
+      if (tix == 0) {
+        if (dbg_mu) dbg_mu[(size_t)bh * m + j] = mean;
+        if (dbg_rstd) dbg_rstd[(size_t)bh * m + j] = rs;
+      }
     }
-    sCoef[j] = mean;
-    sCoef[m + j] = scale;
-    sCoef[2 * m + j] = b;
+  } else {
+    for (int j = threadIdx.x; j < m; j += kOutThreads) {
+      sCoef[j] = 0.f;
+      sCoef[m + j] = 1.f;
+      sCoef[2 * m + j] = 0.f;
+    }
   }
   __syncthreads();
   // A^T tile -> whitened, landmark-major shared tile.  With N % 4 == 0 every row piece is
@@ -337,6 +323,8 @@ output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
       }
     }
   }
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");      // M is complete and visible
+  for (int i = threadIdx.x; i < m * d; i += kOutThreads) sM[i] = mmat[(size_t)bh * m * d + i];
   __syncthreads();
 
   const int cg = d >> 2;                     // channel quads
@@ -379,13 +367,12 @@ output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
 
 }  // namespace
 
-size_t finish_smem_bytes(int m, int runs_q, int bv_splits) {
-  return sizeof(float) * ((size_t)m * m + (size_t)bv_splits * m * kFinishCols +
-                          (size_t)runs_q * 3 * m + (size_t)m * kFinishCols);
+size_t mix_smem_bytes(int m, int bv_splits) {
+  return sizeof(float) * ((size_t)m * m + ((size_t)bv_splits + 1) * m * kFinishCols);
 }
 
-cudaError_t finish_configure(size_t smem) {
-  return cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+cudaError_t mix_configure(size_t smem) {
+  return cudaFuncSetAttribute(mix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
 int output_tile_tokens(int d) {
@@ -440,32 +427,41 @@ cudaError_t launch_bv(const lapl_attn_plan& p, const float* bt, const void* v, f
   return cudaGetLastError();
 }
 
-cudaError_t launch_finish(const lapl_attn_plan& p, const float* stats, const float* bvp,
-                          const float* x, float* mmat, float* mu, float* rstd, float* dbg_mu,
-                          float* dbg_rstd, float* dbg_bv, float* dbg_m, cudaStream_t st) {
+cudaError_t launch_mix(const lapl_attn_plan& p, const float* x, const float* bvp, float* mmat,
+                       float* dbg_bv, float* dbg_m, cudaStream_t st) {
   const Geometry& g = p.geo;
   const int chunks = (g.d + kFinishCols - 1) / kFinishCols;
-  finish_kernel<<<(unsigned)(g.bh * chunks), kFinishThreads, g.fin_smem, st>>>(
-      stats, bvp, x, mmat, mu, rstd, dbg_mu, dbg_rstd, dbg_bv, dbg_m, g.m, g.d, g.n,
-      g.cd_part, g.cd_runs_q, g.bv_splits, p.cfg.delta);
+  mix_kernel<<<(unsigned)(g.bh * chunks), kFinishThreads, g.fin_smem, st>>>(
+      x, bvp, mmat, dbg_bv, dbg_m, g.m, g.d, g.bv_splits);
   return cudaGetLastError();
 }
 
 cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float* mmat,
-                          const float* mu, const float* rstd, const float* bias, void* out,
-                          cudaStream_t st) {
+                          const float* stats, const float* bias, void* out, float* dbg_mu,
+                          float* dbg_rstd, cudaStream_t st) {
   const Geometry& g = p.geo;
-  const int tiles = (g.n + g.out_tile - 1) / g.out_tile;
-  const unsigned grid = (unsigned)(g.bh * tiles);
+  int tiles = (g.n + g.out_tile - 1) / g.out_tile;
+  // Programmatic dependent launch: the kernel may begin while the preceding M kernel runs.
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)(g.bh * tiles));
+  cfg.blockDim = dim3(kOutThreads);
+  cfg.dynamicSmemBytes = g.out_smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int m = g.m, d = g.d, n = g.n, heads = p.cfg.heads, tile = g.out_tile, whiten = p.cfg.whiten;
+  int runs_q = g.cd_runs_q;
+  float delta = p.cfg.delta;
   if (p.cfg.out_dtype == LAPL_BF16)
-    output_kernel<true><<<grid, kOutThreads, g.out_smem, st>>>(
-        at, mmat, mu, rstd, bias, out, g.m, g.d, g.n, p.cfg.heads, g.out_tile, tiles,
-        p.cfg.whiten);
-  else
-    output_kernel<false><<<grid, kOutThreads, g.out_smem, st>>>(
-        at, mmat, mu, rstd, bias, out, g.m, g.d, g.n, p.cfg.heads, g.out_tile, tiles,
-        p.cfg.whiten);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, output_kernel<true>, at, mmat, stats, bias, out, dbg_mu,
+                              dbg_rstd, m, d, n, heads, tile, tiles, whiten, g.cd_part, runs_q,
+                              delta);
+  return cudaLaunchKernelEx(&cfg, output_kernel<false>, at, mmat, stats, bias, out, dbg_mu,
+                            dbg_rstd, m, d, n, heads, tile, tiles, whiten, g.cd_part, runs_q,
+                            delta);
 }
 
 }  // namespace lapl

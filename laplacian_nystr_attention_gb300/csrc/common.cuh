@@ -54,8 +54,6 @@ struct WorkspaceLayout {
   size_t stats;        // [BH, runs_q, 3, m]  per-CTA-run (count, mean, M2) of the columns of A
   size_t bvp;          // [BH, bv_splits, m, d]  per-split partial sums of B V
   size_t mmat;         // [BH, m, d]         M = X (B V)
-  size_t mu;           // [BH, m]            column means
-  size_t rstd;         // [BH, m]            1 / sqrt(var + delta)
   size_t total;
 };
 
@@ -85,6 +83,12 @@ struct Geometry {
   size_t pool_threads;
 };
 
+// Timing marks of one forward (events recorded when timing is on).
+enum Mark {
+  kMarkStart, kMarkPoolDone, kMarkNsStart, kMarkNsDone, kMarkCdistStart, kMarkCdistDone,
+  kMarkBvDone, kMarkMixDone, kMarkOutputDone, kMarks
+};
+
 }  // namespace lapl
 
 struct lapl_attn_plan {
@@ -94,14 +98,11 @@ struct lapl_attn_plan {
   int device;
   int num_sms;
   float neg_log2e_over_lambda;  // exp(-D/lambda) == exp2(D * this)
-  cudaStream_t side_stream;     // runs pooling and the Newton-Schulz solve next to the
-                                // distance kernel
-  cudaEvent_t ev_fork, ev_pool, ev_join;
+  cudaStream_t side_stream;     // runs the shorter of the two chains of a forward
+  cudaEvent_t ev_pool, ev_join;   // pooling done; side-stream chain done
   bool timing;                  // record stage events in forward
   bool timed_once;              // a forward ran with timing on
-  cudaEvent_t ev_stage[9];      // start, pool end (side), cdist, finish, output ends; ns
-                                // start, ns end (side); bv end; cdist start (after the wait
-                                // for pooling)
+  cudaEvent_t ev_stage[lapl::kMarks];   // indexed by lapl::Mark
   unsigned* dev_err;            // the library's device error word on this device
   // Tensor maps of Q and K for the TMA-fed distance kernel, re-encoded when the pointers change.
   mutable CUtensorMap tmap_q, tmap_k;
@@ -122,12 +123,11 @@ cudaError_t launch_cdist(const lapl_attn_plan& p, const void* q, const void* k, 
                          float* dbg_dql, float* dbg_dlk, float* dbg_a, cudaStream_t st);
 cudaError_t launch_bv(const lapl_attn_plan& p, const float* bt, const void* v, float* bvp,
                       cudaStream_t st);
-cudaError_t launch_finish(const lapl_attn_plan& p, const float* stats, const float* bvp,
-                          const float* x, float* mmat, float* mu, float* rstd, float* dbg_mu,
-                          float* dbg_rstd, float* dbg_bv, float* dbg_m, cudaStream_t st);
+cudaError_t launch_mix(const lapl_attn_plan& p, const float* x, const float* bvp, float* mmat,
+                       float* dbg_bv, float* dbg_m, cudaStream_t st);
 cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float* mmat,
-                          const float* mu, const float* rstd, const float* bias, void* out,
-                          cudaStream_t st);
+                          const float* stats, const float* bias, void* out, float* dbg_mu,
+                          float* dbg_rstd, cudaStream_t st);
 
 // Distance kernel choice for a plan: sets geo.cd_tma, cd_tile, cd_rows, cd_threads and cd_smem,
 // opts in to the shared memory and returns the resident CTAs per SM.
@@ -150,8 +150,8 @@ size_t bv_smem_bytes(int m, int d, int threads, bool bf16);
 int bv_threads(int m, int d);
 int bv_tile_tokens();
 cudaError_t bv_configure(size_t smem);
-size_t finish_smem_bytes(int m, int runs_q, int bv_splits);
-cudaError_t finish_configure(size_t smem);
+size_t mix_smem_bytes(int m, int bv_splits);
+cudaError_t mix_configure(size_t smem);
 
 // ---- device helpers ---------------------------------------------------------------------
 __device__ __forceinline__ float laplacian_from_distance(float dist, float neg_log2e_over_lambda) {

@@ -67,10 +67,20 @@ __device__ __forceinline__ void ns_prologue(const NsSmem& sm, const float* __res
   float* X = sm.X;
   float* red = sm.red;
   float* sL = sm.sL;
-  // Landmarks, stored channel-major (sL[c * 64 + j], zero for j >= m).
-  for (int i = threadIdx.x; i < 64 * d; i += NT) {
-    const int c = i >> 6, j = i & 63;
-    sL[i] = j < M ? Lg[j * d + c] : 0.f;
+  // Landmarks, stored channel-major (sL[c * 64 + j], zero for j >= m).  Up to 8 loads per
+  // thread are issued before any is stored.
+  for (int i0 = threadIdx.x; i0 < 64 * d; i0 += 8 * NT) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * NT, c = i >> 6, j = i & 63;
+      v[u] = (i < 64 * d && j < M) ? __ldg(&Lg[j * d + c]) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * NT;
+      if (i < 64 * d) sL[i] = v[u];
+    }
   }
   __syncthreads();
 
