@@ -72,8 +72,7 @@ bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 
 size_t elem_bytes(int dtype) { return dtype == LAPL_BF16 ? 2 : 4; }
 
-// Split of the distance kernel over `ctas` persistent CTAs (see Partition).  runs_q bounds
-// how many CTA ranges can meet one head's query tokens (slots of the per-run statistics).
+// Split of the distance kernel over `ctas` persistent CTAs (see Partition).
 void setup_cdist_partition(Geometry& g, int ctas) {
   Partition& pt = g.cd_part;
   pt.uq = (long long)g.bh * g.n;
@@ -82,7 +81,6 @@ void setup_cdist_partition(Geometry& g, int ctas) {
   pt.ctas = ctas;
   pt.q = pt.total / ctas;
   pt.rem = (int)(pt.total % ctas);
-  g.cd_runs_q = pt.q > 0 ? (int)std::min<long long>((g.n + pt.q - 1) / pt.q + 1, ctas) : ctas;
 }
 }  // namespace
 }  // namespace lapl
@@ -211,6 +209,9 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
     want = std::max<long long>(1, std::min<long long>(want, tiles));
     g.bv_tiles_per_split = (int)((tiles + want - 1) / want);
     g.bv_splits = (tiles + g.bv_tiles_per_split - 1) / g.bv_tiles_per_split;
+    // Column statistics of A: one warp per landmark column, appended to the B V grid.
+    const int warps = g.bv_threads / 32;
+    g.stat_ctas = cfg->whiten ? (int)(g.bh * ((g.m + warps - 1) / warps)) : 0;
   }
   {
     // No more CTAs than chunks of work.
@@ -244,10 +245,11 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   w.x = take(bh * m * m);
   w.at = take(bh * m * n);
   w.bt = take(bh * m * n);
-  w.stats = take(bh * g.cd_runs_q * 3 * m);
   w.bvp = take(bh * g.bv_splits * m * d);
 
   w.mmat = take(bh * m * d);
+  w.mu = take(bh * m);
+  w.rstd = take(bh * m);
   w.total = off;
 
   // The side stream runs the shorter of the two chains (see the launch sequence).
@@ -296,7 +298,8 @@ static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k,
   float* X = reinterpret_cast<float*>(ws + p->ws.x);
   float* At = reinterpret_cast<float*>(ws + p->ws.at);
   float* Bt = reinterpret_cast<float*>(ws + p->ws.bt);
-  float* stats = reinterpret_cast<float*>(ws + p->ws.stats);
+  float* mu = reinterpret_cast<float*>(ws + p->ws.mu);
+  float* rstd = reinterpret_cast<float*>(ws + p->ws.rstd);
   float* bvp = reinterpret_cast<float*>(ws + p->ws.bvp);
 
   float* M = reinterpret_cast<float*>(ws + p->ws.mmat);
@@ -335,10 +338,10 @@ static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k,
     LAPL_MARK(kMarkNsDone, st);
     LAPL_TRY(cudaStreamWaitEvent(side, p->ev_pool, 0), "forward/pooled-wait");
     LAPL_MARK(kMarkCdistStart, side);
-    LAPL_TRY(launch_cdist(*p, q, k, v, L, At, Bt, stats, D.d_ql, D.d_lk, D.a, side),
+    LAPL_TRY(launch_cdist(*p, q, k, v, L, At, Bt, D.d_ql, D.d_lk, D.a, side),
              "forward/cdist");
     LAPL_MARK(kMarkCdistDone, side);
-    LAPL_TRY(launch_bv(*p, Bt, v, bvp, side), "forward/bv");
+    LAPL_TRY(launch_bv(*p, Bt, v, bvp, At, mu, rstd, D.mu, D.rstd, side), "forward/bv");
     LAPL_MARK(kMarkBvDone, side);
     LAPL_TRY(cudaEventRecord(p->ev_join, side), "forward/join");
   } else {
@@ -353,16 +356,16 @@ static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k,
     LAPL_MARK(kMarkNsDone, side);
     LAPL_TRY(cudaEventRecord(p->ev_join, side), "forward/join");
     LAPL_MARK(kMarkCdistStart, st);
-    LAPL_TRY(launch_cdist(*p, q, k, v, L, At, Bt, stats, D.d_ql, D.d_lk, D.a, st),
+    LAPL_TRY(launch_cdist(*p, q, k, v, L, At, Bt, D.d_ql, D.d_lk, D.a, st),
              "forward/cdist");
     LAPL_MARK(kMarkCdistDone, st);
-    LAPL_TRY(launch_bv(*p, Bt, v, bvp, st), "forward/bv");
+    LAPL_TRY(launch_bv(*p, Bt, v, bvp, At, mu, rstd, D.mu, D.rstd, st), "forward/bv");
     LAPL_MARK(kMarkBvDone, st);
   }
   LAPL_TRY(cudaStreamWaitEvent(st, p->ev_join, 0), "forward/join-wait");
   LAPL_TRY(launch_mix(*p, X, bvp, M, D.bv, D.m, st), "forward/mix");
   LAPL_MARK(kMarkMixDone, st);
-  LAPL_TRY(launch_output(*p, At, M, stats, bias, out, D.mu, D.rstd, st), "forward/output");
+  LAPL_TRY(launch_output(*p, At, M, mu, rstd, bias, out, st), "forward/output");
   LAPL_MARK(kMarkOutputDone, st);
   if (tm) p->timed_once = true;
 #undef LAPL_MARK

@@ -1,7 +1,7 @@
 // cdist.cu -- host side of the fused L1 distance + exp kernels: kernel choice, tensor maps,
 // shared memory, occupancy and launch.
 //
-// Two kernels compute the same outputs (A^T, B^T and the per-run statistics of A):
+// Two kernels compute the same outputs (A^T and B^T):
 //   cdist_tma_kernel (cdist_tma.cuh)   token chunks loaded by the Tensor Memory Accelerator into
 //                                      a ring of 128B-swizzled stages, producer warp + consumer
 //                                      warps on mbarriers; instantiated for fp32 with d in
@@ -133,8 +133,8 @@ cudaError_t cdist_plan(lapl_attn_plan& p, int* ctas_per_sm) {
 }
 
 cudaError_t launch_cdist(const lapl_attn_plan& p, const void* q, const void* k, const void* v,
-                         const float* landmarks, float* at, float* bt, float* stats,
-                         float* dbg_dql, float* dbg_dlk, float* dbg_a, cudaStream_t st) {
+                         const float* landmarks, float* at, float* bt, float* dbg_dql,
+                         float* dbg_dlk, float* dbg_a, cudaStream_t st) {
   const Geometry& g = p.geo;
   const bool bf16 = p.cfg.in_dtype == LAPL_BF16;
   if (g.cd_tma) {
@@ -148,11 +148,11 @@ cudaError_t launch_cdist(const lapl_attn_plan& p, const void* q, const void* k, 
       p.tmap_k_ptr = k;
     }
     cdist_tma::TmaArgs a;
-    a.landmarks = landmarks; a.at = at; a.bt = bt; a.stats = stats; a.err = p.dev_err;
+    a.landmarks = landmarks; a.at = at; a.bt = bt; a.err = p.dev_err;
     a.dbg_dql = dbg_dql; a.dbg_dlk = dbg_dlk; a.dbg_a = dbg_a;
     a.part = g.cd_part;
     a.bh_count = g.bh;
-    a.n = g.n; a.runs_q = g.cd_runs_q;
+    a.n = g.n;
     a.c_exp = p.neg_log2e_over_lambda;
     const void* f = cdist_tma::pick(g.s, g.d, bf16);
     if (!f) return cudaErrorInvalidValue;
@@ -161,11 +161,11 @@ cudaError_t launch_cdist(const lapl_attn_plan& p, const void* q, const void* k, 
                             st);
   }
   cdist_impl::CdistArgs a;
-  a.q = q; a.k = k; a.v = v; a.landmarks = landmarks; a.at = at; a.bt = bt; a.stats = stats;
+  a.q = q; a.k = k; a.v = v; a.landmarks = landmarks; a.at = at; a.bt = bt;
   a.dbg_dql = dbg_dql; a.dbg_dlk = dbg_dlk; a.dbg_a = dbg_a;
   a.part = g.cd_part;
   a.bh_count = g.bh;
-  a.n = g.n; a.d = g.d; a.runs_q = g.cd_runs_q;
+  a.n = g.n; a.d = g.d;
   a.c_exp = p.neg_log2e_over_lambda;
   const void* f = cdist_impl::pick(g.s, g.d, bf16);
   if (!f) return cudaErrorInvalidValue;

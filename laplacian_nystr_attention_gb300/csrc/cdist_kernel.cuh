@@ -13,11 +13,10 @@
 // Persistent CTAs walk an equal share of the (side, head, token) positions (see Partition) in
 // chunks of up to 32*R tokens of one head:
 //   query chunk:  A = k(Q, L) is written from registers into A^T [BH, m, N] (each warp store
-//                 covers 32 consecutive tokens) and its per-landmark (mean, M2) is reduced with
-//                 warp shuffles and merged (Chan's update) into the CTA's running statistics of
-//                 that head, written once when the CTA leaves the head.
+//                 covers 32 consecutive tokens); its column statistics are taken from A^T
+//                 afterwards (statistics CTAs of bv_kernel, chain.cu).
 //   key chunk:    B = k(L, K) is written the same way into B^T [BH, m, N]; the contraction with
-//                 V runs in bv_kernel (chain.cu).
+//                 V runs in bv_kernel.
 //
 // Block: s warps for m = s*s landmarks.  Warp w owns landmarks w*s .. w*s+s-1 (so every
 // landmark read from shared memory is a warp-wide broadcast), lane l owns tokens
@@ -38,13 +37,12 @@ struct CdistArgs {
   const float* landmarks;
   float* at;        // [BH, m, N]  A^T
   float* bt;        // [BH, m, N]  B^T
-  float* stats;     // [BH, runs_q, 3, m]  (count, mean, M2)
   float* dbg_dql;   // [BH, N, m]
   float* dbg_dlk;   // [BH, m, N]
   float* dbg_a;     // [BH, N, m]
   Partition part;
   long long bh_count;
-  int n, d, runs_q;
+  int n, d;
   float c_exp;
 };
 
@@ -140,29 +138,6 @@ __device__ __forceinline__ void l1_distances(const float* __restrict__ sX,
   }
 }
 
-__device__ __forceinline__ float warp_sum8_transposed(const float (&v)[8], int lane) {
-  float w[4], x[2];
-  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float send = b4 ? v[i] : v[i + 4];
-    const float keep = b4 ? v[i + 4] : v[i];
-    w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float send = b3 ? w[i] : w[i + 2];
-    const float keep = b3 ? w[i + 2] : w[i];
-    x[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-  }
-  const float send = b2 ? x[0] : x[1];
-  const float keep = b2 ? x[1] : x[0];
-  float y = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-  y += __shfl_xor_sync(0xffffffffu, y, 2);
-  y += __shfl_xor_sync(0xffffffffu, y, 1);
-  return y;
-}
-
 template <int S, int R, int D, bool kBf16>
 __global__ void __launch_bounds__(32 * S)
 cdist_exp_kernel(const CdistArgs a) {
@@ -218,23 +193,7 @@ cdist_exp_kernel(const CdistArgs a) {
     cp_async_commit();
   };
 
-  // Query side, running statistics of landmark warp*S + ((lane >> 2) & 7), kept by that lane
-  // group (all four lanes hold the same values).
-  const int st_jj = (lane >> 2) & 7;
-  float run_n = 0.f, run_mean = 0.f, run_m2 = 0.f;
-  int cur_side = -1;
   long long cur_bh = -1;
-  auto flush = [&]() {
-    if (cur_side != 0) return;
-    const int slot = cta - part_owner(pt, cur_bh * n);
-    if ((lane & 3) == 0 && st_jj < S) {
-      float* st = a.stats + ((size_t)cur_bh * a.runs_q + slot) * 3 * M;
-      const int j = warp * S + st_jj;
-      st[j] = run_n;
-      st[M + j] = run_mean;
-      st[2 * M + j] = run_m2;
-    }
-  };
 
   issue(cur, 0);
   int buf = 0;
@@ -250,16 +209,11 @@ cdist_exp_kernel(const CdistArgs a) {
     }
     const int side = cur.side, n0 = cur.n0, valid = cur.valid;
     const long long bh = cur.bh;
-    if (side != cur_side || bh != cur_bh) {
-      flush();
-      if (bh != cur_bh) {
-        const float4* Lg = reinterpret_cast<const float4*>(a.landmarks + (size_t)bh * M * d);
-        for (int i = threadIdx.x; i < (M * d) >> 2; i += kThreads)
-          reinterpret_cast<float4*>(sL)[i] = Lg[i];
-      }
-      cur_side = side;
+    if (bh != cur_bh) {
+      const float4* Lg = reinterpret_cast<const float4*>(a.landmarks + (size_t)bh * M * d);
+      for (int i = threadIdx.x; i < (M * d) >> 2; i += kThreads)
+        reinterpret_cast<float4*>(sL)[i] = Lg[i];
       cur_bh = bh;
-      run_n = run_mean = run_m2 = 0.f;
     }
     const float* sX;
     if constexpr (kBf16) {
@@ -311,46 +265,11 @@ cdist_exp_kernel(const CdistArgs a) {
       for (int r = 0; r < R; ++r)
         if (lane + 32 * r < valid) dst[lane + 32 * r] = acc[r][jj];
     }
-    if (side == 0) {
-      // Chunk statistics per landmark (two passes), merged into the running ones.
-      float v8[8];
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        float sum = 0.f;
-        if (jj < S) {
-#pragma unroll
-          for (int r = 0; r < R; ++r) sum += acc[r][jj];    // invalid tokens hold 0
-        }
-        v8[jj] = sum;
-      }
-      const float nb = (float)valid;
-      const float mean_b = warp_sum8_transposed(v8, lane) / nb;
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        const float mj = __shfl_sync(0xffffffffu, mean_b, 4 * jj);
-        float ss = 0.f;
-        if (jj < S) {
-#pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const float dv = acc[r][jj] - mj;
-            ss = (lane + 32 * r < valid) ? fmaf(dv, dv, ss) : ss;
-          }
-        }
-        v8[jj] = ss;
-      }
-      const float m2_b = warp_sum8_transposed(v8, lane);
-      const float tot = run_n + nb;
-      const float dlt = mean_b - run_mean;
-      run_mean += dlt * (nb / tot);
-      run_m2 += m2_b + dlt * dlt * (run_n * nb / tot);
-      run_n = tot;
-    }
     if (!more) break;
     pos = pnext;
     cur = nxt;
     buf ^= 1;
   }
-  flush();
 }
 
 

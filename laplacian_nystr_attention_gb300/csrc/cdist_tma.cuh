@@ -3,7 +3,7 @@
 // Same computation and outputs as cdist_exp_kernel (cdist_kernel.cuh): for a balanced range of
 // (side, head, token) positions, A = k(Q, L) or B = k(L, K) with k(x, y) = exp(-|x - y|_1 /
 // lambda) ("LaplacianFormer: Rethinking Linear Attention with Laplacian Kernel", English
-// explainer page, 2.A), stored landmark-major, plus the per-run column statistics of A.
+// explainer page, 2.A), stored landmark-major.
 //
 // Pipeline (warp-specialised, no CTA-wide barrier per chunk):
 //   * producer warp (warp s): one lane issues cp.async.bulk.tensor loads of 128-token chunks of
@@ -30,7 +30,6 @@ namespace lapl {
 namespace cdist_tma {
 
 using cdist_impl::abs_diff_acc;
-using cdist_impl::warp_sum8_transposed;
 
 constexpr int kStages = 2;
 constexpr int kLmSlots = kStages;
@@ -42,14 +41,13 @@ struct TmaArgs {
   const float* landmarks;    // [BH, m, d]
   float* at;                 // [BH, m, N]
   float* bt;                 // [BH, m, N]
-  float* stats;              // [BH, runs_q, 3, m]
   unsigned* err;             // device error word (kErrTimeout)
   float* dbg_dql;
   float* dbg_dlk;
   float* dbg_a;
   Partition part;
   long long bh_count;
-  int n, runs_q;
+  int n;
   float c_exp;
 };
 
@@ -289,34 +287,17 @@ cdist_tma_kernel(const TmaArgs a, const __grid_constant__ CUtensorMap map_q,
   }
 
   // ---------------- consumers ----------------
-  const int st_jj = (lane >> 2) & 7;
-  float run_n = 0.f, run_mean = 0.f, run_m2 = 0.f;
-  int cur_side = -1;
   long long cur_bh = -1;
   int lm_slot = -1;
   const bool debug = a.dbg_dql || a.dbg_dlk || a.dbg_a;
-  auto flush = [&]() {
-    if (cur_side != 0) return;
-    const int slot = cta - part_owner(a.part, cur_bh * n);
-    if ((lane & 3) == 0 && st_jj < S) {
-      float* st = a.stats + ((size_t)cur_bh * a.runs_q + slot) * 3 * M;
-      const int j = warp * S + st_jj;
-      st[j] = run_n;
-      st[M + j] = run_mean;
-      st[2 * M + j] = run_m2;
-    }
-  };
 
   for (int i = 0; !it.done(); ++i) {
     const int s = i % kStages;
     const int side = it.side, n0 = it.n0, valid = it.valid;
     const long long bh = it.bh;
-    if (bh != cur_bh) lm_slot = (lm_slot + 1) % kLmSlots;
-    if (side != cur_side || bh != cur_bh) {
-      flush();
-      cur_side = side;
+    if (bh != cur_bh) {
+      lm_slot = (lm_slot + 1) % kLmSlots;
       cur_bh = bh;
-      run_n = run_mean = run_m2 = 0.f;
     }
     // Every lane waits (acquiring the copied bytes); the warp leaves together on a timeout.
     if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (i / kStages) & 1))) {
@@ -362,42 +343,8 @@ cdist_tma_kernel(const TmaArgs a, const __grid_constant__ CUtensorMap map_q,
       for (int r = 0; r < 4; ++r)
         if (lane + 32 * r < valid) dst[lane + 32 * r] = acc[r][jj];
     }
-    if (side == 0) {
-      float v8[8];
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        float sum = 0.f;
-        if (jj < S) {
-#pragma unroll
-          for (int r = 0; r < 4; ++r) sum += acc[r][jj];
-        }
-        v8[jj] = sum;
-      }
-      const float nb = (float)valid;
-      const float mean_b = warp_sum8_transposed(v8, lane) / nb;
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        const float mj = __shfl_sync(0xffffffffu, mean_b, 4 * jj);
-        float ss = 0.f;
-        if (jj < S) {
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const float dv = acc[r][jj] - mj;
-            ss = (lane + 32 * r < valid) ? fmaf(dv, dv, ss) : ss;
-          }
-        }
-        v8[jj] = ss;
-      }
-      const float m2_b = warp_sum8_transposed(v8, lane);
-      const float tot = run_n + nb;
-      const float dlt = mean_b - run_mean;
-      run_mean += dlt * (nb / tot);
-      run_m2 += m2_b + dlt * dlt * (run_n * nb / tot);
-      run_n = tot;
-    }
     it.next(n, a.bh_count);
   }
-  flush();
 }
 
 }  // namespace cdist_tma

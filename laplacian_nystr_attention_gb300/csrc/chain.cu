@@ -6,16 +6,15 @@
 //    column, taken over the N tokens of the (batch, head) slice (variance divides by N);
 //  * low-rank product without the N x N matrix (Chinese page, 2.2), evaluated right to left.
 //
-// bv_kernel (one CTA per (batch, head, token split)):
+// bv_kernel (one CTA per (batch, head, token split), then the column-statistics CTAs):
 //   partial B V of the split's tokens from B^T [BH, m, N] and V, register-tiled on the CUDA
 //   cores (4 landmarks x 4 channels per thread, 8 shared loads per 64 FMAs).
 // mix_kernel (per (batch, head, 8 value columns)), after the Newton-Schulz solve is joined:
 //   reduces the per-split partials of B V in split order and forms M = X (B V).
 //   Fixed reduction orders: the result is bit-reproducible run to run.
 // output_kernel (one CTA per (batch, head, token tile)):
-//   merges the head's per-run (mean, M2) of the distance kernel in CTA order (Chan's pairwise
-//   update), loads the A^T tile and whitens it on the way into shared memory, then (after the
-//   M kernel) writes O = A^ M with a 4 tokens x 4 channels register tile per thread.
+//   loads the A^T tile and whitens it on the way into shared memory, then (after the M
+//   kernel) writes O = A^ M with a 4 tokens x 4 channels register tile per thread.
 #include "common.cuh"
 
 namespace lapl {
@@ -35,12 +34,90 @@ __device__ __forceinline__ void cp_async4_zfill(void* dst, const void* src, int 
                : "memory");
 }
 
+__device__ __forceinline__ float warp_allsum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Column statistics of A for the whitening: warp w of statistics CTA sidx takes landmark column
+// j of head bh, the contiguous row A^T[bh][j][0..N), and makes two passes over it -- the sum,
+// then the sum of squared deviations from the mean -- each lane over every 32nd 16-byte piece
+// (or element), the lanes combined by a fixed xor tree.  var = M2 / N (divides by N).
+__device__ __forceinline__ void column_stats(const float* __restrict__ at, float* __restrict__ mu,
+                                             float* __restrict__ rstd, float* __restrict__ dbg_mu,
+                                             float* __restrict__ dbg_rstd, int m, int n,
+                                             float delta, long sidx) {
+  const int warps = (int)(blockDim.x >> 5), warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per_head = (m + warps - 1) / warps;
+  const long bh = sidx / per_head;
+  const int j = (int)(sidx % per_head) * warps + warp;
+  if (j >= m) return;
+  const float* row = at + ((size_t)bh * m + j) * n;
+  constexpr int kB = 4;                   // loads in flight per lane
+  float mean = 0.f, m2 = 0.f;
+  for (int pass = 0; pass < 2; ++pass) {
+    float acc = 0.f;
+    if ((n & 3) == 0) {
+      const float4* r4 = reinterpret_cast<const float4*>(row);
+      const int n4 = n >> 2;
+      for (int i0 = lane; i0 < n4; i0 += 32 * kB) {
+        float4 v[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+          const int i = i0 + 32 * u;
+          v[u] = i < n4 ? __ldcg(&r4[i]) : make_float4(mean, mean, mean, mean);
+        }
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+          if (pass == 0) {
+            acc += (v[u].x + v[u].y) + (v[u].z + v[u].w);
+          } else {
+            const float a = v[u].x - mean, b = v[u].y - mean, c = v[u].z - mean, e = v[u].w - mean;
+            acc += (a * a + b * b) + (c * c + e * e);
+          }
+        }
+      }
+    } else {
+      for (int i0 = lane; i0 < n; i0 += 32 * kB) {
+        float v[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+          const int i = i0 + 32 * u;
+          v[u] = i < n ? __ldcg(&row[i]) : mean;
+        }
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+          const float a = v[u] - mean;
+          acc += pass == 0 ? v[u] : a * a;
+        }
+      }
+    }
+    acc = warp_allsum(acc);
+    if (pass == 0) mean = acc / (float)n;
+    else m2 = acc;
+  }
+  if (lane == 0) {
+    const float rs = 1.f / sqrtf(m2 / (float)n + delta);
+    mu[(size_t)bh * m + j] = mean;
+    rstd[(size_t)bh * m + j] = rs;
+    if (dbg_mu) dbg_mu[(size_t)bh * m + j] = mean;
+    if (dbg_rstd) dbg_rstd[(size_t)bh * m + j] = rs;
+  }
+}
+
 // Partial B V of the split's tokens.  Chunks of 128 tokens (B^T rows and V rows) are copied
 // asynchronously into one of two shared buffers while the other is contracted.
 template <bool kBf16>
 __global__ void __launch_bounds__(512)
 bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __restrict__ bvp,
-          int m, int d, int n, int tiles_per_split, int splits) {
+          int m, int d, int n, int tiles_per_split, int splits, const float* __restrict__ at,
+          float* __restrict__ mu, float* __restrict__ rstd, float* __restrict__ dbg_mu,
+          float* __restrict__ dbg_rstd, long bv_ctas, float delta) {
+  if ((long)blockIdx.x >= bv_ctas) {     // a column-statistics CTA (uniform per CTA)
+    column_stats(at, mu, rstd, dbg_mu, dbg_rstd, m, n, delta, (long)blockIdx.x - bv_ctas);
+    return;
+  }
   extern __shared__ float4 smem_bv4[];
   float* smem = reinterpret_cast<float*>(smem_bv4);
   const int nthreads = blockDim.x;
@@ -217,10 +294,9 @@ constexpr int kOutThreads = 256;
 template <bool kOutBf16>
 __global__ void __launch_bounds__(kOutThreads)
 output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
-              const float* __restrict__ stats, const float* __restrict__ bias,
-              void* __restrict__ out, float* __restrict__ dbg_mu, float* __restrict__ dbg_rstd,
-              int m, int d, int n, int heads, int tile, int tiles, int whiten,
-              const Partition pt, int runs_q, float delta) {
+              const float* __restrict__ mu, const float* __restrict__ rstd,
+              const float* __restrict__ bias, void* __restrict__ out, int m, int d, int n,
+              int heads, int tile, int tiles, int whiten) {
   extern __shared__ float4 smem_out4[];
   float* smem = reinterpret_cast<float*>(smem_out4);
   const long bh = blockIdx.x / tiles;
@@ -231,41 +307,18 @@ output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
   float* sA = sM + m * d;           // [m][tile] whitened A, landmark-major
   float* sCoef = sA + m * tile;     // mean [m], scale [m], bias [m]
 
-  // Everything up to the wait below reads results of earlier kernels only (A^T, the
-  // statistics), so with a programmatic launch it overlaps the M = X (B V) kernel before it.
-  // Column statistics of the head: Chan's pairwise merge of the distance kernel's per-run
-  // (count, mean, M2) in CTA order; variance over the N tokens.
-  if (whiten) {
-    const long long fq = (long long)bh * n;
-    const int nq = part_owner(pt, fq + n - 1) - part_owner(pt, fq) + 1;
-    const float* st = stats + (size_t)bh * runs_q * 3 * m;
-    for (int j = threadIdx.x; j < m; j += kOutThreads) {
-      float cnt = 0.f, mean = 0.f, m2 = 0.f;
-      for (int q = 0; q < nq; ++q) {
-        const float nb = st[q * 3 * m + j];
-        const float mb = st[q * 3 * m + m + j];
-        const float m2b = st[q * 3 * m + 2 * m + j];
-        const float tot = cnt + nb;
-        const float dlt = mb - mean;
-        mean += dlt * (nb / tot);
-        m2 += m2b + dlt * dlt * (cnt * nb / tot);
-        cnt = tot;
-      }
-      const float rs = 1.f / sqrtf(m2 / (float)n + delta);
-      sCoef[j] = mean;
-      sCoef[m + j] = rs;
-      sCoef[2 * m + j] = bias ? bias[(size_t)h * m + j] : 0.f;
-      if (tix == 0) {
-        if (dbg_mu) dbg_mu[(size_t)bh * m + j] = mean;
-        if (dbg_rstd) dbg_rstd[(size_t)bh * m + j] = rs;
-      }
+  // Everything up to the wait below reads results of earlier kernels only (A^T, mean, rstd),
+  // so with a programmatic launch it overlaps the M = X (B V) kernel before it.
+  for (int j = threadIdx.x; j < m; j += kOutThreads) {
+    float mean = 0.f, scale = 1.f, b = 0.f;
+    if (whiten) {
+      mean = mu[(size_t)bh * m + j];
+      scale = rstd[(size_t)bh * m + j];
+      b = bias ? bias[(size_t)h * m + j] : 0.f;
     }
-  } else {
-    for (int j = threadIdx.x; j < m; j += kOutThreads) {
-      sCoef[j] = 0.f;
-      sCoef[m + j] = 1.f;
-      sCoef[2 * m + j] = 0.f;
-    }
+    sCoef[j] = mean;
+    sCoef[m + j] = scale;
+    sCoef[2 * m + j] = b;
   }
   __syncthreads();
   // A^T tile -> whitened, landmark-major shared tile.  With N % 4 == 0 every row piece is
@@ -415,15 +468,22 @@ cudaError_t bv_configure(size_t smem) {
 }
 
 cudaError_t launch_bv(const lapl_attn_plan& p, const float* bt, const void* v, float* bvp,
+                      const float* at, float* mu, float* rstd, float* dbg_mu, float* dbg_rstd,
                       cudaStream_t st) {
   const Geometry& g = p.geo;
-  const unsigned grid = (unsigned)(g.bh * g.bv_splits);
+  const long bv_ctas = g.bh * g.bv_splits;
+  const unsigned grid = (unsigned)(bv_ctas + g.stat_ctas);
+  const float delta = p.cfg.delta;
   if (p.cfg.in_dtype == LAPL_BF16)
     bv_kernel<true><<<grid, g.bv_threads, g.bv_smem, st>>>(bt, v, bvp, g.m, g.d, g.n,
-                                                           g.bv_tiles_per_split, g.bv_splits);
+                                                           g.bv_tiles_per_split, g.bv_splits, at,
+                                                           mu, rstd, dbg_mu, dbg_rstd, bv_ctas,
+                                                           delta);
   else
     bv_kernel<false><<<grid, g.bv_threads, g.bv_smem, st>>>(bt, v, bvp, g.m, g.d, g.n,
-                                                            g.bv_tiles_per_split, g.bv_splits);
+                                                            g.bv_tiles_per_split, g.bv_splits, at,
+                                                            mu, rstd, dbg_mu, dbg_rstd, bv_ctas,
+                                                            delta);
   return cudaGetLastError();
 }
 
@@ -437,8 +497,8 @@ cudaError_t launch_mix(const lapl_attn_plan& p, const float* x, const float* bvp
 }
 
 cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float* mmat,
-                          const float* stats, const float* bias, void* out, float* dbg_mu,
-                          float* dbg_rstd, cudaStream_t st) {
+                          const float* mu, const float* rstd, const float* bias, void* out,
+                          cudaStream_t st) {
   const Geometry& g = p.geo;
   int tiles = (g.n + g.out_tile - 1) / g.out_tile;
   // Programmatic dependent launch: the kernel may begin while the preceding M kernel runs.
@@ -453,15 +513,11 @@ cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float*
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int m = g.m, d = g.d, n = g.n, heads = p.cfg.heads, tile = g.out_tile, whiten = p.cfg.whiten;
-  int runs_q = g.cd_runs_q;
-  float delta = p.cfg.delta;
   if (p.cfg.out_dtype == LAPL_BF16)
-    return cudaLaunchKernelEx(&cfg, output_kernel<true>, at, mmat, stats, bias, out, dbg_mu,
-                              dbg_rstd, m, d, n, heads, tile, tiles, whiten, g.cd_part, runs_q,
-                              delta);
-  return cudaLaunchKernelEx(&cfg, output_kernel<false>, at, mmat, stats, bias, out, dbg_mu,
-                            dbg_rstd, m, d, n, heads, tile, tiles, whiten, g.cd_part, runs_q,
-                            delta);
+    return cudaLaunchKernelEx(&cfg, output_kernel<true>, at, mmat, mu, rstd, bias, out, m, d, n,
+                              heads, tile, tiles, whiten);
+  return cudaLaunchKernelEx(&cfg, output_kernel<false>, at, mmat, mu, rstd, bias, out, m, d, n,
+                            heads, tile, tiles, whiten);
 }
 
 }  // namespace lapl

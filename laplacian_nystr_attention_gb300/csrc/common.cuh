@@ -51,9 +51,10 @@ struct WorkspaceLayout {
   size_t x;            // [BH, m, m]         Newton-Schulz result X
   size_t at;           // [BH, m, N]         A = k(Q, L), landmark-major (A transposed)
   size_t bt;           // [BH, m, N]         B = k(L, K)
-  size_t stats;        // [BH, runs_q, 3, m]  per-CTA-run (count, mean, M2) of the columns of A
   size_t bvp;          // [BH, bv_splits, m, d]  per-split partial sums of B V
   size_t mmat;         // [BH, m, d]         M = X (B V)
+  size_t mu;           // [BH, m]            column means of A
+  size_t rstd;         // [BH, m]            1 / sqrt(column variance + delta)
   size_t total;
 };
 
@@ -66,8 +67,8 @@ struct Geometry {
   bool cd_tma;             // distance kernel fed by TMA (cdist_tma.cuh), else by cp.async
   int cd_threads;          // threads of a distance-kernel CTA
   Partition cd_part;       // balanced split over cd_part.ctas persistent CTAs
-  int cd_runs_q;           // most CTAs whose range meets one head's query tokens
   int bv_splits;           // B V: CTAs per head
+  int stat_ctas;           // column-statistics CTAs appended to the B V grid (0: no whitening)
   int bv_tiles_per_split;  // B V: 128-token chunks per CTA
   int bv_threads;
   size_t bv_smem;
@@ -119,15 +120,16 @@ cudaError_t launch_pool(const lapl_attn_plan& p, const void* k, float* landmarks
 cudaError_t launch_ns(const lapl_attn_plan& p, const float* landmarks, float* x, float* dbg_dll,
                       float* dbg_w, float* dbg_x, cudaStream_t st);
 cudaError_t launch_cdist(const lapl_attn_plan& p, const void* q, const void* k, const void* v,
-                         const float* landmarks, float* at, float* bt, float* stats,
-                         float* dbg_dql, float* dbg_dlk, float* dbg_a, cudaStream_t st);
+                         const float* landmarks, float* at, float* bt, float* dbg_dql,
+                         float* dbg_dlk, float* dbg_a, cudaStream_t st);
 cudaError_t launch_bv(const lapl_attn_plan& p, const float* bt, const void* v, float* bvp,
+                      const float* at, float* mu, float* rstd, float* dbg_mu, float* dbg_rstd,
                       cudaStream_t st);
 cudaError_t launch_mix(const lapl_attn_plan& p, const float* x, const float* bvp, float* mmat,
                        float* dbg_bv, float* dbg_m, cudaStream_t st);
 cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float* mmat,
-                          const float* stats, const float* bias, void* out, float* dbg_mu,
-                          float* dbg_rstd, cudaStream_t st);
+                          const float* mu, const float* rstd, const float* bias, void* out,
+                          cudaStream_t st);
 
 // Distance kernel choice for a plan: sets geo.cd_tma, cd_tile, cd_rows, cd_threads and cd_smem,
 // opts in to the shared memory and returns the resident CTAs per SM.
