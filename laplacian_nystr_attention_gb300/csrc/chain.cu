@@ -41,9 +41,11 @@ __device__ __forceinline__ float warp_allsum(float v) {
 }
 
 // Column statistics of A for the whitening: warp w of statistics CTA sidx takes landmark column
-// j of head bh, the contiguous row A^T[bh][j][0..N), and makes two passes over it -- the sum,
-// then the sum of squared deviations from the mean -- each lane over every 32nd 16-byte piece
-// (or element), the lanes combined by a fixed xor tree.  var = M2 / N (divides by N).
+// j of head bh, the contiguous row A^T[bh][j][0..N), in one pass.  The values are shifted by c,
+// the mean of the row's first (up to) 128 values, and each lane sums a - c and (a - c)^2 over
+// every 32nd 16-byte piece (or element); the lanes are combined by a fixed xor tree.  Then
+// mean = c + S1 / N and M2 = S2 - S1^2 / N (var = M2 / N).  c lies within a few standard
+// deviations of the mean, so the subtraction keeps fp32 accuracy.
 __device__ __forceinline__ void column_stats(const float* __restrict__ at, float* __restrict__ mu,
                                              float* __restrict__ rstd, float* __restrict__ dbg_mu,
                                              float* __restrict__ dbg_rstd, int m, int n,
@@ -54,51 +56,54 @@ __device__ __forceinline__ void column_stats(const float* __restrict__ at, float
   const int j = (int)(sidx % per_head) * warps + warp;
   if (j >= m) return;
   const float* row = at + ((size_t)bh * m + j) * n;
+  // Shift: mean of the first min(N, 128) values.
+  const int nc = n < 128 ? n : 128;
+  float c = 0.f;
+  for (int i = lane; i < nc; i += 32) c += __ldcg(&row[i]);
+  c = warp_allsum(c) / (float)nc;
+
   constexpr int kB = 4;                   // loads in flight per lane
-  float mean = 0.f, m2 = 0.f;
-  for (int pass = 0; pass < 2; ++pass) {
-    float acc = 0.f;
-    if ((n & 3) == 0) {
-      const float4* r4 = reinterpret_cast<const float4*>(row);
-      const int n4 = n >> 2;
-      for (int i0 = lane; i0 < n4; i0 += 32 * kB) {
-        float4 v[kB];
+  float s1 = 0.f, s2 = 0.f;
+  if ((n & 3) == 0) {
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    const int n4 = n >> 2;
+    for (int i0 = lane; i0 < n4; i0 += 32 * kB) {
+      float4 v[kB];
 #pragma unroll
-        for (int u = 0; u < kB; ++u) {
-          const int i = i0 + 32 * u;
-          v[u] = i < n4 ? __ldcg(&r4[i]) : make_float4(mean, mean, mean, mean);
-        }
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-          if (pass == 0) {
-            acc += (v[u].x + v[u].y) + (v[u].z + v[u].w);
-          } else {
-            const float a = v[u].x - mean, b = v[u].y - mean, c = v[u].z - mean, e = v[u].w - mean;
-            acc += (a * a + b * b) + (c * c + e * e);
-          }
-        }
+      for (int u = 0; u < kB; ++u) {
+        const int i = i0 + 32 * u;
+        v[u] = i < n4 ? __ldcg(&r4[i]) : make_float4(c, c, c, c);   // c contributes 0
       }
-    } else {
-      for (int i0 = lane; i0 < n; i0 += 32 * kB) {
-        float v[kB];
 #pragma unroll
-        for (int u = 0; u < kB; ++u) {
-          const int i = i0 + 32 * u;
-          v[u] = i < n ? __ldcg(&row[i]) : mean;
-        }
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-          const float a = v[u] - mean;
-          acc += pass == 0 ? v[u] : a * a;
-        }
+      for (int u = 0; u < kB; ++u) {
+        const float a = v[u].x - c, b = v[u].y - c, e = v[u].z - c, f = v[u].w - c;
+        s1 += (a + b) + (e + f);
+        s2 += (a * a + b * b) + (e * e + f * f);
       }
     }
-    acc = warp_allsum(acc);
-    if (pass == 0) mean = acc / (float)n;
-    else m2 = acc;
+  } else {
+    for (int i0 = lane; i0 < n; i0 += 32 * kB) {
+      float v[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const int i = i0 + 32 * u;
+        v[u] = i < n ? __ldcg(&row[i]) : c;
+      }
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const float a = v[u] - c;
+        s1 += a;
+        s2 = fmaf(a, a, s2);
+      }
+    }
   }
+  s1 = warp_allsum(s1);
+  s2 = warp_allsum(s2);
   if (lane == 0) {
-    const float rs = 1.f / sqrtf(m2 / (float)n + delta);
+    const float inv_n = 1.f / (float)n;
+    const float mean = c + s1 * inv_n;
+    const float m2 = fmaxf(s2 - s1 * s1 * inv_n, 0.f);
+    const float rs = 1.f / sqrtf(m2 * inv_n + delta);
     mu[(size_t)bh * m + j] = mean;
     rstd[(size_t)bh * m + j] = rs;
     if (dbg_mu) dbg_mu[(size_t)bh * m + j] = mean;

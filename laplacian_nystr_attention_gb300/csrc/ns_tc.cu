@@ -6,7 +6,7 @@
 // exactly T steps; W = k(L, L) + eps I.  Same iterate as the CUDA-core kernels of ns.cu, with
 // the products evaluated differently.
 //
-// One CTA (8 warps) per (batch, head).  The m x m matrices are zero-padded to 64 x 64.  A
+// One CTA (16 warps) per (batch, head).  The m x m matrices are zero-padded to 64 x 64.  A
 // product C = A B is one accumulation of ceil(m / 8) tcgen05.mma instructions, M = N = 128,
 // K = 8 each, into 128 columns of tensor memory:
 //     D = [A_hi; A_lo] [Bt_hi; Bt_lo]^T
@@ -32,7 +32,7 @@ namespace lapl {
 using namespace ns_detail;
 namespace {
 
-constexpr int kTcThreads = 256;
+constexpr int kTcThreads = 512;
 constexpr unsigned kLbo = 16 * 128;            // bytes between K-adjacent core matrices
 constexpr unsigned kSbo = 128;                 // bytes between row-adjacent core matrices
 constexpr unsigned kOpBytes = 128 * 64 * 4;    // one 128 x 64 TF32 operand
@@ -61,10 +61,11 @@ __device__ __forceinline__ unsigned op_off(int r, int k) {
   return (unsigned)((k >> 2) * kLbo + (r >> 3) * kSbo + (r & 7) * 16 + (k & 3) * 4);
 }
 
+// Round to the nearest TF32 value (10 explicit mantissa bits), ties away from zero: add half
+// of the dropped 13 bits' range to the sign-magnitude pattern and clear them (a carry moves
+// into the exponent exactly when rounding up crosses a binade).  Finite inputs only.
 __device__ __forceinline__ float tf32_rna(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
 
 // Store 4 consecutive k of operand row r (r < 64) as high part (row r) and low part (r + 64).
@@ -146,29 +147,27 @@ __device__ __forceinline__ bool wait_product(unsigned bar, unsigned parity) {
   return __syncthreads_and(ok ? 1 : 0) != 0;
 }
 
-// 32 consecutive fp32 columns of this warp's 32 tensor-memory lanes.
-__device__ __forceinline__ void tmem_ld32(unsigned addr, float (&v)[32]) {
-  unsigned r[32];
+// 16 consecutive fp32 columns of this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_ld16(unsigned addr, float (&v)[16]) {
+  unsigned r[16];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];\n"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        "=r"(r[14]), "=r"(r[15])
       : "r"(addr));
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-// C = sum of the four blocks of D, 16 columns of one row per thread.  Warp w reads tensor-memory
-// lanes 32(w % 4).. (D rows dr) and columns 32h.. and 64 + 32h.. (h = w / 4); D rows dr and
+// C = sum of the four blocks of D, 8 columns of one row per thread.  Warp w reads tensor-memory
+// lanes 32(w % 4).. (D rows dr) and columns 16h.. and 64 + 16h.. (h = w / 4); D rows dr and
 // dr + 64 hold the A_hi and A_lo parts of C row i = dr % 64.  The A_hi thread keeps columns
-// 32h..32h+15 and the A_lo thread 32h+16..32h+31; each hands the other half of its sums to
-// the other through sc.  On return c holds C[i][col0 .. col0+15].
-__device__ __forceinline__ void combine_product(unsigned tmem, float* sc, float (&c)[16], int& i,
+// 16h..16h+7 and the A_lo thread 16h+8..16h+15; each hands the other half of its sums to the
+// other through sc.  On return c holds C[i][col0 .. col0+7].
+__device__ __forceinline__ void combine_product(unsigned tmem, float* sc, float (&c)[8], int& i,
                                                 int& col0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sp = warp & 3, h = warp >> 2;
@@ -176,28 +175,28 @@ __device__ __forceinline__ void combine_product(unsigned tmem, float* sc, float 
   i = dr & 63;
   const bool low = dr >= 64;
   const unsigned lane_base = (unsigned)(32 * sp) << 16;
-  float a[32], v[32];
-  tmem_ld32(tmem + lane_base + 32 * h, a);
-  tmem_ld32(tmem + lane_base + 64 + 32 * h, v);
+  float a[16], v[16];
+  tmem_ld16(tmem + lane_base + 16 * h, a);
+  tmem_ld16(tmem + lane_base + 64 + 16 * h, v);
 #pragma unroll
-  for (int j = 0; j < 32; ++j) a[j] += v[j];
-  // kept half: a[16..31] for the low thread, a[0..15] for the high one (selects, so that a
-  // stays in registers)
-  float kept[16], given[16];
+  for (int j = 0; j < 16; ++j) a[j] += v[j];
+  // kept half: a[8..15] for the low thread, a[0..7] for the high one (selects, so that a stays
+  // in registers)
+  float kept[8], given[8];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    kept[j] = low ? a[16 + j] : a[j];
-    given[j] = low ? a[j] : a[16 + j];
+  for (int j = 0; j < 8; ++j) {
+    kept[j] = low ? a[8 + j] : a[j];
+    given[j] = low ? a[j] : a[8 + j];
   }
-  col0 = 32 * h + (low ? 16 : 0);
-  const int give0 = 32 * h + (low ? 0 : 16);
+  col0 = 16 * h + (low ? 8 : 0);
+  const int give0 = 16 * h + (low ? 0 : 8);
 #pragma unroll
-  for (int j = 0; j < 16; j += 4)
+  for (int j = 0; j < 8; j += 4)
     *reinterpret_cast<float4*>(&sc[i * kMS + give0 + j]) =
         make_float4(given[j], given[j + 1], given[j + 2], given[j + 3]);
   __syncthreads();
 #pragma unroll
-  for (int j = 0; j < 16; j += 4) {
+  for (int j = 0; j < 8; j += 4) {
     const float4 o = *reinterpret_cast<const float4*>(&sc[i * kMS + col0 + j]);
     c[j] = kept[j] + o.x;
     c[j + 1] = kept[j + 1] + o.y;
@@ -249,9 +248,10 @@ ns_tc_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
   ns_prologue<S, kTcThreads>(sm, landmarks + (size_t)bh * M * d, d, eps, c_exp, true, dbg_dll,
                              dbg_w, bh);
 
-  // Operands W and X0 as TF32 high/low pairs.
+  // Operands W and X0 as TF32 high/low pairs.  A warp takes 32 consecutive rows of one
+  // 4-column piece: its 16-byte stores are contiguous in the operand layout.
   for (int g = threadIdx.x; g < 64 * 16; g += kTcThreads) {
-    const int r = g >> 4, k0 = (g & 15) * 4;
+    const int r = g & 63, k0 = (g >> 6) * 4;
     store_split(WW, r, k0, *reinterpret_cast<const float4*>(&sc[r * kMS + k0]));
     store_split(XX, r, k0, *reinterpret_cast<const float4*>(&Xf[r * kMS + k0]));
   }
@@ -273,11 +273,11 @@ ns_tc_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
     if (!ok) break;
     tc_fence_after();
     {
-      float c[16];
+      float c[8];
       int i, col0;
       combine_product(tmem, sc, c, i, col0);
 #pragma unroll
-      for (int j = 0; j < 16; j += 4)
+      for (int j = 0; j < 8; j += 4)
         store_split(PP, i, col0 + j, make_float4(c[j], c[j + 1], c[j + 2], c[j + 3]));
     }
     proxy_fence();
@@ -291,11 +291,11 @@ ns_tc_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
     phase ^= 1;
     if (!ok) break;
     tc_fence_after();
-    float y[16];
+    float y[8];
     int i, col0;
     combine_product(tmem, sc, y, i, col0);
 #pragma unroll
-    for (int j = 0; j < 16; j += 4) {
+    for (int j = 0; j < 8; j += 4) {
       float* px = &Xf[i * kMS + col0 + j];
       const float4 xo = *reinterpret_cast<const float4*>(px);
       y[j] = 2.f * xo.x - y[j];
@@ -307,16 +307,20 @@ ns_tc_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
     __syncthreads();
     // Lower triangle from the upper one: entries (i, j < i) read (j, i), which no thread writes
     // in this pass.
+    float yt[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < 8; ++j) {              // all reads first, then the writes
       const int col = col0 + j;
-      if (col < i) {
-        y[j] = Xf[col * kMS + i];
-        Xf[i * kMS + col] = y[j];
-      }
+      yt[j] = col < i ? Xf[col * kMS + i] : y[j];
     }
 #pragma unroll
-    for (int j = 0; j < 16; j += 4)
+    for (int j = 0; j < 8; ++j) {
+      const int col = col0 + j;
+      if (col < i) Xf[i * kMS + col] = yt[j];
+      y[j] = yt[j];
+    }
+#pragma unroll
+    for (int j = 0; j < 8; j += 4)
       store_split(XX, i, col0 + j, make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]));
     proxy_fence();
     tc_fence_before();
