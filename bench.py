@@ -40,7 +40,10 @@ CLEAN_BYTES = 256 * 1024 * 1024
 # DRAM traffic (read + write bytes) of one launch of the distance kernel, from an ncu capture
 # (summaries under profiles/), per (feed, workload) with the sha256 of the distance kernel's
 # source files it was taken on; reported as null when the sources have changed since.
-CDIST_TRAFFIC = {}
+CDIST_TRAFFIC = {
+    ("tma", "stage1_f32"): (13020928 + 4608,
+                            "3db0ab4992276b73df98d260eab727a1d29c627171284f86ad02d2729121d5de"),
+}
 CDIST_SOURCES = ["cdist_kernel.cuh", "cdist_tma.cuh", "cdist.cu", "cdist_d32.cu", "cdist_d64.cu",
                  "cdist_d0.cu", "cdist_tma_f32.cu", "cdist_tma_bf16.cu"]
 CDIST_KERNEL = {
@@ -67,6 +70,7 @@ def parse():
                     help="budget of the oracle CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
     return ap.parse_args()
 
 
@@ -159,56 +163,83 @@ class ClockSampler:
                 "reasons": reasons}
 
 
-def cpu_baseline(w, q, k, v, budget_s: float) -> dict:
-    """The fp64 oracle on a bounded sample: whole (b,h) slices until the budget is spent."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def oracle_rate(w, q, k, v, budget_s: float, threads: int):
+    """Whole (b,h) slices of the fp64 oracle, `threads` at a time (the oracle's C call releases
+    the GIL), until the budget is spent.  Returns (tokens/s, slices done, seconds)."""
+    import concurrent.futures as cf
     import oracle
     oracle.build()
     cfg = w.config()
+    q64, k64, v64 = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
     slices = w.batch * w.heads
     done, t0 = 0, time.perf_counter()
-    while done < slices:
-        oracle.forward(cfg, q, k, v, slices=(done, 1))
-        done += 1
-        if time.perf_counter() - t0 > budget_s:
-            break
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        while done < slices and time.perf_counter() - t0 < budget_s:
+            wave = min(threads, slices - done)
+            list(ex.map(lambda s0: oracle.forward(cfg, q64, k64, v64, slices=(s0, 1)),
+                        range(done, done + wave)))
+            done += wave
     dt = time.perf_counter() - t0
-    tokens = done * w.n / w.heads          # tokens are counted once across heads
-    return {"value": tokens / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{done} of {slices} (batch, head) slices of {w.name} in {dt:.2f} s, "
-                      "single-threaded fp64 C oracle; tokens/s = slices * N / H / seconds"}
+    return done * w.n / w.heads / dt, done, dt      # tokens are counted once across heads
+
+
+def cpu_baseline(w, q, k, v, budget_s: float) -> dict:
+    """The fp64 oracle on a bounded sample: whole (b,h) slices on all host cores until the
+    budget is spent, and the same on one core for reference."""
+    cores = host_cores()
+    one, n1, t1 = oracle_rate(w, q, k, v, budget_s / 4, 1)
+    allc, na, ta = oracle_rate(w, q, k, v, budget_s, cores)
+    return {"value": allc, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "value_1_core": one,
+            "sample": f"{na} of {w.batch * w.heads} (batch, head) slices of {w.name} in "
+                      f"{ta:.2f} s on {cores} threads (one slice per thread), and {n1} slices in "
+                      f"{t1:.2f} s on 1 thread; fp64 C oracle; tokens/s = slices * N / H / "
+                      "seconds"}
 
 
 def run_reference(args, w):
     world, rank, _ = dist_env()
     if rank != 0:
         return
+    import concurrent.futures as cf
     q, k, v = make_inputs(w)
     import oracle
     oracle.build()
     cfg = w.config()
+    q64, k64, v64 = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
     slices = w.batch * w.heads
-    per_step = max(1, min(slices, 2))
+    cores = host_cores()
+    per_step = max(1, min(slices, cores))
     times = []
-    for step in range(args.warmup + args.steps):
-        s0 = (step * per_step) % slices
-        cnt = min(per_step, slices - s0)
-        t0 = time.perf_counter()
-        oracle.forward(cfg, q, k, v, slices=(s0, cnt))
-        dt = time.perf_counter() - t0
-        if step >= args.warmup:
-            times.append((dt, cnt))
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        for step in range(args.warmup + args.steps):
+            s0 = (step * per_step) % slices
+            cnt = min(per_step, slices - s0)
+            t0 = time.perf_counter()
+            list(ex.map(lambda s: oracle.forward(cfg, q64, k64, v64, slices=(s, 1)),
+                        range(s0, s0 + cnt)))
+            dt = time.perf_counter() - t0
+            if step >= args.warmup:
+                times.append((dt, cnt))
     tot_t = sum(t for t, _ in times)
     tot_tok = sum(c for _, c in times) * w.n / w.heads
     value = tot_tok / tot_t
-    sample = (f"{per_step} (batch, head) slice(s) of {w.name} per step, single-threaded fp64 C "
-              "oracle; tokens/s = slices * N / H / seconds")
+    sample = (f"{per_step} (batch, head) slice(s) of {w.name} per step, one per thread on "
+              f"{cores} threads, fp64 C oracle; tokens/s = slices * N / H / seconds")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_t / len(times), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_desc(w),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -295,6 +326,35 @@ def run_ours(args, w):
     lna.lapl_attn_set_timing(att.handle, False)
     stage_ms = {key: sum(vals) / len(vals) for key, vals in stage.items()}
 
+    # ---- the same forward captured once in a CUDA graph and replayed ----
+    graph = None
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            flush_l2()
+            g.replay()
+        barrier()
+        g0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        g1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush_l2()
+            g0[i].record(stream)
+            g.replay()
+            g1[i].record(stream)
+        barrier()
+        gms = sum(a.elapsed_time(b) for a, b in zip(g0, g1)) / args.steps
+        if world > 1:
+            t = torch.tensor([gms], device=dev)
+            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+            gms = float(t.item())
+        graph = {"value": world * w.tokens / (gms / 1e3), "unit": UNIT, "ms_per_step": gms,
+                 "note": "lapl_attn_forward captured in one CUDA graph (both streams), "
+                         "replayed; L2 flushed before each replay"}
+        del g
+
     # ---- end to end through the C ABI with host buffers (pinned) ----
     e2e = None
     if not args.no_e2e:
@@ -367,6 +427,10 @@ def run_ours(args, w):
         "stage_ms": stage_ms,
         "cpu_baseline": None,
         "e2e": e2e,
+        "graph": graph,
+        "memory": {"workspace_bytes": att.workspace_bytes,
+                   "io_bytes": sum(x.numel() * x.element_size() for x in (dq, dk, dv, out)),
+                   "note": "device memory of one forward: Q, K, V, O and the workspace"},
         "gpu_launches": gpu_launches,
         "clocks": clk,
         "impl": "ours",
