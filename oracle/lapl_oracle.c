@@ -50,6 +50,20 @@ static double l1_distance(const double* x, const double* y, int d) {
   return sum;
 }
 
+/* The Gaussian kernel the pages compare against (English page, 1 "Theoretical Mismatch":
+ * similarity decaying with the squared l2 distance): k(x,y) = exp(-||x - y||_2^2 / lambda),
+ * the squared differences summed over the d channels in ascending order. */
+static double sq_l2_distance(const double* x, const double* y, int d) {
+  double sum = 0.0;
+  for (int c = 0; c < d; ++c) sum += (x[c] - y[c]) * (x[c] - y[c]);
+  return sum;
+}
+
+static double kernel_distance(const orc_config* cfg, const double* x, const double* y, int d) {
+  return cfg->kernel == 1 ? sq_l2_distance(x, y, d) : l1_distance(x, y, d);
+}
+
+/* exp(-distance / lambda), for either distance. */
 static double laplacian_of_distance(double dist, double lambda) { return exp(-dist / lambda); }
 
 /* ---- step 3: Newton-Schulz inverse of W ---------------------------------------------
@@ -175,6 +189,7 @@ static int check_config(const orc_config* c) {
     return ORC_ERR_ARG;
   if (!(c->lambda > 0.0) || !(c->eps >= 0.0)) return ORC_ERR_ARG;
   if (c->whiten && !(c->delta > 0.0)) return ORC_ERR_ARG;
+  if (c->kernel != 0 && c->kernel != 1) return ORC_ERR_ARG;
   const int s = isqrt_exact(c->num_landmarks);
   if (s < 0 || c->grid_h % s != 0 || c->grid_w % s != 0) return ORC_ERR_UNSUPPORTED;
   return ORC_OK;
@@ -216,17 +231,17 @@ static int forward_slice(const orc_config* cfg, int h, const double* Q, const do
   /* 2. kernel blocks: A = k(Q,L) [N,m], B = k(L,K) [m,N], W = k(L,L) + eps I [m,m] */
   for (int i = 0; i < N; ++i)
     for (int j = 0; j < m; ++j) {
-      Dql[(size_t)i * m + j] = l1_distance(Q + (size_t)i * d, L + (size_t)j * d, d);
+      Dql[(size_t)i * m + j] = kernel_distance(cfg, Q + (size_t)i * d, L + (size_t)j * d, d);
       A[(size_t)i * m + j] = laplacian_of_distance(Dql[(size_t)i * m + j], cfg->lambda);
     }
   for (int j = 0; j < m; ++j)
     for (int n = 0; n < N; ++n) {
-      Dlk[(size_t)j * N + n] = l1_distance(L + (size_t)j * d, K + (size_t)n * d, d);
+      Dlk[(size_t)j * N + n] = kernel_distance(cfg, L + (size_t)j * d, K + (size_t)n * d, d);
       Bm[(size_t)j * N + n] = laplacian_of_distance(Dlk[(size_t)j * N + n], cfg->lambda);
     }
   for (int j = 0; j < m; ++j)
     for (int k = 0; k < m; ++k) {
-      Dll[(size_t)j * m + k] = l1_distance(L + (size_t)j * d, L + (size_t)k * d, d);
+      Dll[(size_t)j * m + k] = kernel_distance(cfg, L + (size_t)j * d, L + (size_t)k * d, d);
       W[(size_t)j * m + k] = laplacian_of_distance(Dll[(size_t)j * m + k], cfg->lambda) +
                              (j == k ? cfg->eps : 0.0);
     }

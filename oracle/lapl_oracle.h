@@ -17,6 +17,9 @@
  *   4. whitening of A column by column with a diagonal estimator:
  *      A_hat = (A - mean) / sqrt(var + delta) + bias                      (Korean page, 2.2)
  *   5. O = A_hat * (X * (B * V)): the N x N matrix is never formed        (Chinese page, 2.2)
+ * With kernel = 1 the kernel of step 2 is the Gaussian one the pages compare against,
+ * k(x,y) = exp(-||x-y||_2^2 / lambda): similarity decaying with the squared l2 distance
+ * (English page, 1 "Theoretical Mismatch"); every other step is unchanged.
  */
 #ifndef LAPL_ORACLE_H
 #define LAPL_ORACLE_H
@@ -37,12 +40,14 @@ typedef struct {
   double delta;            /* whitening variance floor, > 0 when whiten != 0 */
   int ns_steps;            /* T >= 0 Newton-Schulz steps, no early exit */
   int whiten;              /* 1: whiten A; 0: A_hat = A (bias ignored) */
+  int kernel;              /* 0: Laplacian, distance sum_c |x_c - y_c|;
+                              1: Gaussian, distance sum_c (x_c - y_c)^2 */
 } orc_config;
 
 /* Every pointer may be NULL.  Shapes are for the whole [B,H] batch, C order. */
 typedef struct {
   double* landmarks; /* [B,H,m,d]   L                              */
-  double* d_ql;      /* [B,H,N,m]   sum_c |Q_ic - L_jc|             */
+  double* d_ql;      /* [B,H,N,m]   sum_c |Q_ic - L_jc| (squared terms when Gaussian) */
   double* d_ll;      /* [B,H,m,m]   sum_c |L_jc - L_kc|             */
   double* d_lk;      /* [B,H,m,N]   sum_c |L_jc - K_nc|             */
   double* a;         /* [B,H,N,m]   exp(-D_QL / lambda)             */
