@@ -11,6 +11,10 @@ Prints one JSON line (rank 0).  Multi-GPU (torchrun): every rank runs its own co
 workload (independent (batch, head) slices, no data-path collective): weak scaling.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+                  [--kernel laplacian|gaussian]
+
+--kernel gaussian runs the same pipeline with the Gaussian kernel exp(-|x - y|_2^2 / lambda)
+in place of the Laplacian one (the softmax-free baseline the method is set against).
 """
 from __future__ import annotations
 
@@ -38,18 +42,31 @@ FLUSH_BYTES = 512 * 1024 * 1024
 CLEAN_BYTES = 256 * 1024 * 1024
 
 # DRAM traffic (read + write bytes) of one launch of the distance kernel, from an ncu capture
-# (summaries under profiles/), per (feed, workload) with the sha256 of the distance kernel's
+# (summaries under profiles/), per (feed, workload, kernel) with the sha256 of the distance kernel's
 # source files it was taken on; reported as null when the sources have changed since.
 CDIST_TRAFFIC = {
-    ("tma", "stage1_f32"): (13020928 + 4608,
-                            "3db0ab4992276b73df98d260eab727a1d29c627171284f86ad02d2729121d5de"),
+    ("tma", "stage1_f32", "laplacian"): (
+        13019904 + 4608, "f4b35b7f8fd1127af71c0e7d6fe76d03c474923fbba7229c9325ced339798112"),
+    ("cp.async", "stage1_f32", "gaussian"): (
+        13016576 + 0, "f4b35b7f8fd1127af71c0e7d6fe76d03c474923fbba7229c9325ced339798112"),
 }
 CDIST_SOURCES = ["cdist_kernel.cuh", "cdist_tma.cuh", "cdist.cu", "cdist_d32.cu", "cdist_d64.cu",
-                 "cdist_d0.cu", "cdist_tma_f32.cu", "cdist_tma_bf16.cu"]
+                 "cdist_d0.cu", "cdist_tma_f32.cu", "cdist_tma_bf16.cu", "cdist_gauss_d32.cu",
+                 "cdist_gauss_d64.cu", "cdist_gauss_d0.cu"]
 CDIST_KERNEL = {
-    "tma": "cdist_tma_kernel (fused L1 distance + exp, query and key blocks; TMA-fed)",
-    "cp.async": "cdist_exp_kernel (fused L1 distance + exp, query and key blocks; cp.async-fed)",
+    ("tma", "laplacian"): "cdist_tma_kernel (fused L1 distance + exp, query and key blocks; "
+                          "TMA-fed)",
+    ("cp.async", "laplacian"): "cdist_exp_kernel (fused L1 distance + exp, query and key "
+                               "blocks; cp.async-fed)",
+    ("cp.async", "gaussian"): "cdist_exp_kernel (fused squared-l2 distance + exp, query and key "
+                              "blocks; cp.async-fed)",
 }
+OPS_CONVENTION = {
+    "laplacian": "3 per (token, landmark, channel): subtract, abs, add (2 FP32 instructions)",
+    "gaussian": "3 per (token, landmark, channel): subtract, multiply, add (a subtract and an "
+                "FMA)",
+}
+KERNEL_IDS = {"laplacian": 0, "gaussian": 1}
 
 
 def cdist_sources_sha() -> str:
@@ -66,6 +83,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="stage1_f32", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--kernel", default="laplacian", choices=sorted(KERNEL_IDS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="budget of the oracle CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -81,19 +99,27 @@ def dist_env():
     return world, rank, local
 
 
-def workload_desc(w) -> dict:
+def workload_desc(w, kernel: str) -> dict:
     return {
         "workload": (f"{w.name}: B={w.batch} H={w.heads} grid {w.grid_h}x{w.grid_w} "
                      f"(N={w.n}) d={w.head_dim} m={w.num_landmarks} T={w.ns_steps} "
-                     f"lambda={w.lam:g} eps={w.eps:g} delta={w.delta:g} {w.dtype} {w.dist}"),
+                     f"lambda={w.lam:g} eps={w.eps:g} delta={w.delta:g} {w.dtype} {w.dist}"
+                     + ("" if kernel == "laplacian" else f"; {kernel} kernel")),
         "batch": w.batch, "heads": w.heads, "seq_len": w.n, "head_dim": w.head_dim,
-        "landmarks": w.num_landmarks, "ns_steps": w.ns_steps,
+        "landmarks": w.num_landmarks, "ns_steps": w.ns_steps, "kernel": kernel,
     }
 
 
+def oracle_cfg(w, kernel: str) -> dict:
+    cfg = w.config()
+    cfg["kernel"] = KERNEL_IDS[kernel]
+    return cfg
+
+
 def cdist_ops_per_launch(w) -> float:
-    """Algorithmic FP32 operations of the distance kernel: 3 (subtract, absolute value, add)
-    per (token, landmark, channel) element, for the query block and the key block."""
+    """Algorithmic FP32 operations of the distance kernel: 3 (subtract, absolute value, add; or
+    for the Gaussian kernel subtract, multiply, add) per (token, landmark, channel) element, for
+    the query block and the key block."""
     return 3.0 * 2.0 * w.batch * w.heads * w.n * w.num_landmarks * w.head_dim
 
 
@@ -170,13 +196,13 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def oracle_rate(w, q, k, v, budget_s: float, threads: int):
+def oracle_rate(w, q, k, v, budget_s: float, threads: int, kernel: str = "laplacian"):
     """Whole (b,h) slices of the fp64 oracle, `threads` at a time (the oracle's C call releases
     the GIL), until the budget is spent.  Returns (tokens/s, slices done, seconds)."""
     import concurrent.futures as cf
     import oracle
     oracle.build()
-    cfg = w.config()
+    cfg = oracle_cfg(w, kernel)
     q64, k64, v64 = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
     slices = w.batch * w.heads
     done, t0 = 0, time.perf_counter()
@@ -190,12 +216,12 @@ def oracle_rate(w, q, k, v, budget_s: float, threads: int):
     return done * w.n / w.heads / dt, done, dt      # tokens are counted once across heads
 
 
-def cpu_baseline(w, q, k, v, budget_s: float) -> dict:
+def cpu_baseline(w, q, k, v, budget_s: float, kernel: str = "laplacian") -> dict:
     """The fp64 oracle on a bounded sample: whole (b,h) slices on all host cores until the
     budget is spent, and the same on one core for reference."""
     cores = host_cores()
-    one, n1, t1 = oracle_rate(w, q, k, v, budget_s / 4, 1)
-    allc, na, ta = oracle_rate(w, q, k, v, budget_s, cores)
+    one, n1, t1 = oracle_rate(w, q, k, v, budget_s / 4, 1, kernel)
+    allc, na, ta = oracle_rate(w, q, k, v, budget_s, cores, kernel)
     return {"value": allc, "unit": UNIT, "cores": cores, "kind": "oracle",
             "value_1_core": one,
             "sample": f"{na} of {w.batch * w.heads} (batch, head) slices of {w.name} in "
@@ -212,7 +238,7 @@ def run_reference(args, w):
     q, k, v = make_inputs(w)
     import oracle
     oracle.build()
-    cfg = w.config()
+    cfg = oracle_cfg(w, args.kernel)
     q64, k64, v64 = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
     slices = w.batch * w.heads
     cores = host_cores()
@@ -238,7 +264,7 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_t / len(times), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_desc(w),
+        "config": workload_desc(w, args.kernel),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -267,7 +293,7 @@ def run_ours(args, w):
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     hq, hk, hv = (torch.from_numpy(x).to(tdt).pin_memory() for x in (q, k, v))
     dq, dk, dv = (x.to(dev) for x in (hq, hk, hv))
-    cfg = lna.make_config(**{**w.config(), "in_dtype": w.dtype})
+    cfg = lna.make_config(**{**w.config(), "in_dtype": w.dtype, "kernel": args.kernel})
     att = lna.LaplacianNystromAttention(cfg)
     out = torch.empty((w.batch, w.heads, w.n, w.head_dim), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -401,7 +427,7 @@ def run_ours(args, w):
     achieved = cdist_ops_per_launch(w) / (stage_ms["cdist"] / 1e3) / 1e12
     plan = lna.lapl_attn_plan_info_get(att.handle)
     feed = "tma" if plan["cdist_tma"] else "cp.async"
-    rec = CDIST_TRAFFIC.get((feed, w.name))
+    rec = CDIST_TRAFFIC.get((feed, w.name, args.kernel))
     traffic = rec[0] if rec and rec[1] == cdist_sources_sha() else None
     clk = clocks.summary()
     line = {
@@ -409,19 +435,19 @@ def run_ours(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic",
-        "config": {**workload_desc(w),
+        "config": {**workload_desc(w, args.kernel),
                    "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write, "
                          f"then a {CLEAN_BYTES >> 20} MiB read; not timed)",
                    "parallelism": f"replicas x{world} (independent (batch, head) slices)",
                    "plan": plan},
         "roofline": {
-            "kernel": CDIST_KERNEL[feed],
+            "kernel": CDIST_KERNEL[(feed, args.kernel)],
             "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": traffic,
             "peak_source": (f"derived: {props.multi_processor_count} SMs x 128 FP32 lanes x 2 x "
                             f"{sm_max:g} MHz (max SM clock, MEASURED_PEAKS {peaks_src})"),
             "ops_per_launch": cdist_ops_per_launch(w),
-            "ops_convention": "3 per (token, landmark, channel): subtract, abs, add",
+            "ops_convention": OPS_CONVENTION[args.kernel],
             "kernel_ms": stage_ms["cdist"],
         },
         "stage_ms": stage_ms,
@@ -436,7 +462,7 @@ def run_ours(args, w):
         "impl": "ours",
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, q, k, v, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(w, q, k, v, args.cpu_seconds, args.kernel)
     print(json.dumps(line), flush=True)
     att.close()
     if world > 1:

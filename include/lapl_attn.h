@@ -53,6 +53,16 @@ typedef enum {
 
 typedef enum { LAPL_F32 = 0, LAPL_BF16 = 1 } lapl_dtype;
 
+/*
+ * Similarity kernel k(x, y) = exp(-D(x, y) / lambda) of A, B and W.
+ *   LAPL_KERNEL_LAPLACIAN: D = sum_c |x_c - y_c| (the method: English page, 2.A).
+ *   LAPL_KERNEL_GAUSSIAN:  D = sum_c (x_c - y_c)^2, the Gaussian kernel of earlier linear
+ *     attention that the pages set the Laplacian one against (English page, 1 "Theoretical
+ *     Mismatch": similarity decaying with the squared l2 distance); a drop-in that keeps every
+ *     other step, eps I included.
+ */
+typedef enum { LAPL_KERNEL_LAPLACIAN = 0, LAPL_KERNEL_GAUSSIAN = 1 } lapl_kernel;
+
 typedef struct {
   int batch;          /* B >= 0 (B == 0: forward is a no-op)                                */
   int heads;          /* H >= 1                                                             */
@@ -66,15 +76,17 @@ typedef struct {
   int whiten;         /* 1: whiten A (default); 0: A^ = A and bias is ignored                */
   int in_dtype;       /* lapl_dtype of Q, K, V                                               */
   int out_dtype;      /* lapl_dtype of O (LAPL_F32 recommended; LAPL_BF16 rounds at the end) */
+  int kernel;         /* lapl_kernel (0, the Laplacian kernel, when the struct is zeroed)     */
 } lapl_attn_config;
 
 typedef struct lapl_attn_plan* lapl_attn_handle;
 
 /* Nullable device pointers for intermediate results (all fp32, C order). */
 typedef struct {
-  float* d_ql;       /* [B,H,N,m] raw L1 distances sum_c |Q_ic - L_jc|  */
-  float* d_ll;       /* [B,H,m,m] raw L1 distances between landmarks    */
-  float* d_lk;       /* [B,H,m,N] raw L1 distances sum_c |L_jc - K_nc|  */
+  float* d_ql;       /* [B,H,N,m] raw distances D(Q_i, L_j) (L1 sum_c |Q_ic - L_jc|, or
+                        the squared l2 distance for the Gaussian kernel)                    */
+  float* d_ll;       /* [B,H,m,m] raw distances between landmarks       */
+  float* d_lk;       /* [B,H,m,N] raw distances D(L_j, K_n)             */
   float* landmarks;  /* [B,H,m,d] L                                      */
   float* w;          /* [B,H,m,m] W = k(L,L) + eps I                     */
   float* x;          /* [B,H,m,m] X after T Newton-Schulz steps          */
@@ -192,8 +204,8 @@ typedef struct {
 } lapl_attn_plan_info;
 
 /*
- * Fill *info.  Choices made at create: the TMA feed for fp32 inputs with d = 32 and m <= 49,
- * cp.async otherwise; for the solve one CTA per head, with tensor-core products for m >= 25
+ * Fill *info.  Choices made at create: the TMA feed for fp32 inputs with d = 32 and m <= 49 and
+ * the Laplacian kernel, cp.async otherwise (always for the Gaussian kernel); for the solve one CTA per head, with tensor-core products for m >= 25
  * and CUDA-core products for m <= 16.  Environment
  * variables read at create override them: LAPL_ATTN_CDIST_FEED = "cp.async" (always) or "tma"
  * (wherever the TMA kernel exists: fp32 with d = 32 or 64, bf16 with d = 64, and

@@ -23,6 +23,8 @@ LAPL_ERR_NOT_IMPLEMENTED = 7
 
 LAPL_F32 = 0
 LAPL_BF16 = 1
+LAPL_KERNEL_LAPLACIAN = 0
+LAPL_KERNEL_GAUSSIAN = 1
 
 
 class lapl_attn_config(ctypes.Structure):
@@ -33,6 +35,7 @@ class lapl_attn_config(ctypes.Structure):
         ("lam", ctypes.c_float), ("eps", ctypes.c_float), ("delta", ctypes.c_float),
         ("ns_steps", ctypes.c_int), ("whiten", ctypes.c_int),
         ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
+        ("kernel", ctypes.c_int),
     ]
 
 

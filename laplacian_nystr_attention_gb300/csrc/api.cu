@@ -52,6 +52,8 @@ lapl_status validate(const lapl_attn_config* c) {
   if ((c->in_dtype != LAPL_F32 && c->in_dtype != LAPL_BF16) ||
       (c->out_dtype != LAPL_F32 && c->out_dtype != LAPL_BF16))
     return LAPL_ERR_INVALID_ARG;
+  if (c->kernel != LAPL_KERNEL_LAPLACIAN && c->kernel != LAPL_KERNEL_GAUSSIAN)
+    return LAPL_ERR_INVALID_ARG;
   const int s = isqrt_exact(c->num_landmarks);
   if (s < 0 || s > kMaxS) return LAPL_ERR_UNSUPPORTED;
   if (c->grid_h % s != 0 || c->grid_w % s != 0) return LAPL_ERR_UNSUPPORTED;

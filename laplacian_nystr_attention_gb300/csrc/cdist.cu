@@ -7,8 +7,9 @@
 //                                      warps on mbarriers; instantiated for fp32 with d in
 //                                      {32, 64} and bf16 with d = 64;
 //   cdist_exp_kernel (cdist_kernel.cuh) chunks loaded with cp.async by the whole CTA, every
-//                                      shape.
-// Automatic choice: the TMA feed for fp32, d = 32, s <= 7 (as fast as cp.async there); cp.async
+//                                      shape, and the only one with Gaussian-kernel (squared
+//                                      l2 distance) instantiations.
+// Automatic choice for the Laplacian kernel: the TMA feed for fp32, d = 32, s <= 7 (as fast as cp.async there); cp.async
 // elsewhere (faster where the TMA kernel's extra producer warp costs registers, s = 8, or its
 // consumer warps each widen the same bf16 chunk).  The environment variable
 // LAPL_ATTN_CDIST_FEED=tma or =cp.async, read at plan creation, overrides the choice (tma only
@@ -23,12 +24,21 @@ namespace cdist_impl {
 const void* kernel_d32(int s, bool bf16);
 const void* kernel_d64(int s, bool bf16);
 const void* kernel_d0(int s, bool bf16);
+const void* gauss_d32(int s, bool bf16);
+const void* gauss_d64(int s, bool bf16);
+const void* gauss_d0(int s, bool bf16);
 
 constexpr int kRows = 4;   // tokens per thread; chunk = 128 tokens
 
-// Kernel for (s, d, dtype): head dims 32 and 64 have compile-time instantiations (their channel
-// loop is fully resolved at compile time); other dims use the runtime-d instantiation.
-const void* pick(int s, int d, bool bf16) {
+// Kernel for (s, d, dtype, distance): head dims 32 and 64 have compile-time instantiations
+// (their channel loop is fully resolved at compile time); other dims use the runtime-d
+// instantiation.
+const void* pick(int s, int d, bool bf16, bool gauss) {
+  if (gauss) {
+    if (d == 32) return gauss_d32(s, bf16);
+    if (d == 64) return gauss_d64(s, bf16);
+    return gauss_d0(s, bf16);
+  }
   if (d == 32) return kernel_d32(s, bf16);
   if (d == 64) return kernel_d64(s, bf16);
   return kernel_d0(s, bf16);
@@ -112,9 +122,10 @@ cudaError_t cdist_plan(lapl_attn_plan& p, int* ctas_per_sm) {
   const char* feed = getenv("LAPL_ATTN_CDIST_FEED");
   const bool want_tma = feed && strcmp(feed, "tma") == 0;
   const bool want_cpasync = feed && strcmp(feed, "cp.async") == 0;
+  const bool gauss = p.cfg.kernel == LAPL_KERNEL_GAUSSIAN;
   const bool auto_tma = !bf16 && g.d == 32 && g.s <= 7;
   const long long rows = (long long)g.bh * g.n;
-  const void* f = cdist_tma::pick(g.s, g.d, bf16);
+  const void* f = gauss ? nullptr : cdist_tma::pick(g.s, g.d, bf16);
   // Tensor-map coordinates are 32-bit; a box must not be taller than the tensor.
   g.cd_tma = f && (want_tma || (auto_tma && !want_cpasync)) && rows >= cdist_tma::kTile &&
              rows < (1LL << 31) && cdist_tma::encoder() != nullptr;
@@ -122,7 +133,7 @@ cudaError_t cdist_plan(lapl_attn_plan& p, int* ctas_per_sm) {
     g.cd_threads = 32 * (g.s + 1);
     g.cd_smem = cdist_tma::smem_bytes(g.s, g.d, bf16);
   } else {
-    f = cdist_impl::pick(g.s, g.d, bf16);
+    f = cdist_impl::pick(g.s, g.d, bf16, gauss);
     g.cd_threads = 32 * g.s;
     g.cd_smem = cdist_impl::smem_bytes(g.s, g.d, g.cd_tile, bf16);
   }
@@ -167,7 +178,7 @@ cudaError_t launch_cdist(const lapl_attn_plan& p, const void* q, const void* k, 
   a.bh_count = g.bh;
   a.n = g.n; a.d = g.d;
   a.c_exp = p.neg_log2e_over_lambda;
-  const void* f = cdist_impl::pick(g.s, g.d, bf16);
+  const void* f = cdist_impl::pick(g.s, g.d, bf16, p.cfg.kernel == LAPL_KERNEL_GAUSSIAN);
   if (!f) return cudaErrorInvalidValue;
   void* args[] = {&a};
   return cudaLaunchKernel(f, dim3((unsigned)g.cd_part.ctas), dim3(g.cd_threads), args, g.cd_smem, st);

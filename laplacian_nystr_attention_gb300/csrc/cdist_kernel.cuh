@@ -107,8 +107,22 @@ __device__ __forceinline__ void abs_diff_acc(float& t, float x, float l) {
       : "f"(x), "f"(l));
 }
 
-// acc[r][jj] = sum_c |x_{lane+32r, c} - L_{jj, c}| for the first RV row groups (the others 0).
-template <int S, int R, int RV>
+// t += (x - l)^2: a subtract and a fused multiply-add (the Gaussian kernel's squared l2
+// distance; also two FP32-pipe instructions per element).
+__device__ __forceinline__ void sq_diff_acc(float& t, float x, float l) {
+  const float dd = x - l;
+  t = fmaf(dd, dd, t);
+}
+
+template <bool kGauss>
+__device__ __forceinline__ void dist_acc(float& t, float x, float l) {
+  if constexpr (kGauss) sq_diff_acc(t, x, l);
+  else abs_diff_acc(t, x, l);
+}
+
+// acc[r][jj] = sum_c |x_{lane+32r, c} - L_{jj, c}| (squared terms for the Gaussian kernel) for
+// the first RV row groups (the others 0).
+template <int S, int R, int RV, bool kGauss>
 __device__ __forceinline__ void l1_distances(const float* __restrict__ sX,
                                              const float* __restrict__ lrow, int d, int lane,
                                              int sw, float (&acc)[R][S]) {
@@ -128,17 +142,17 @@ __device__ __forceinline__ void l1_distances(const float* __restrict__ sX,
 #pragma unroll
       for (int r = 0; r < RV; ++r) {
         float t = acc[r][jj];
-        abs_diff_acc(t, x[r].x, l.x);
-        abs_diff_acc(t, x[r].y, l.y);
-        abs_diff_acc(t, x[r].z, l.z);
-        abs_diff_acc(t, x[r].w, l.w);
+        dist_acc<kGauss>(t, x[r].x, l.x);
+        dist_acc<kGauss>(t, x[r].y, l.y);
+        dist_acc<kGauss>(t, x[r].z, l.z);
+        dist_acc<kGauss>(t, x[r].w, l.w);
         acc[r][jj] = t;
       }
     }
   }
 }
 
-template <int S, int R, int D, bool kBf16>
+template <int S, int R, int D, bool kBf16, bool kGauss = false>
 __global__ void __launch_bounds__(32 * S)
 cdist_exp_kernel(const CdistArgs a) {
   static_assert(S <= 8 && R == 4, "at most 8 landmarks per warp; 4 row groups");
@@ -231,10 +245,10 @@ cdist_exp_kernel(const CdistArgs a) {
     const float* lrow = sL + warp * S * d;
     const int sw = lane & mask;
     const int groups = (valid + 31) >> 5;
-    if (groups == 4) l1_distances<S, R, 4>(sX, lrow, d, lane, sw, acc);
-    else if (groups == 3) l1_distances<S, R, 3>(sX, lrow, d, lane, sw, acc);
-    else if (groups == 2) l1_distances<S, R, 2>(sX, lrow, d, lane, sw, acc);
-    else l1_distances<S, R, 1>(sX, lrow, d, lane, sw, acc);
+    if (groups == 4) l1_distances<S, R, 4, kGauss>(sX, lrow, d, lane, sw, acc);
+    else if (groups == 3) l1_distances<S, R, 3, kGauss>(sX, lrow, d, lane, sw, acc);
+    else if (groups == 2) l1_distances<S, R, 2, kGauss>(sX, lrow, d, lane, sw, acc);
+    else l1_distances<S, R, 1, kGauss>(sX, lrow, d, lane, sw, acc);
 
     // ---- kernel values ----
 #pragma unroll

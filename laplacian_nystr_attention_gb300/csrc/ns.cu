@@ -10,12 +10,15 @@
 // to 64 x 64 (the padding stays exactly zero through the iteration).
 //
 // Symmetry.  W is symmetric, X0 = W^T / c is symmetric, and X_{t+1} = X_t (2I - W X_t) is
-// symmetric whenever X_t is a polynomial in W.  The update X <- 2X - X P is therefore evaluated
-// on the upper-triangle tiles only and mirrored, so every iterate is exactly symmetric.
-// P = W X is computed in full: mirroring it as well drops its commutator part [W, X]/2, and in
-// fp32 that error grows through the slow first phase of the iteration until it diverges
-// (kappa(W) ~ 65 already does), whereas mirroring one of the two products stays within
-// rounding of the plain iteration.  With A symmetric both factors are row reads,
+// symmetric whenever X_t is a polynomial in W.  Every iterate is kept exactly symmetric: the
+// update V = 2X - X P is evaluated in full and X_{t+1} = (V + V^T) / 2, entry by entry (the
+// two sums of a mirrored pair are the same fp32 addition).  Averaging drops the antisymmetric
+// part of V's rounding error; keeping one triangle instead turns that part into a symmetric
+// error of the same size, which the slow (unconverged) modes of an ill-conditioned W double at
+// every step (a Gaussian-kernel W with kappa ~ 3e3 and 20 steps loses about 10x in O).
+// P = W X is computed in full and not symmetrised: symmetrising it drops its commutator part
+// [W, X]/2, and in fp32 that error grows through the slow first phase of the iteration until
+// it diverges (kappa(W) ~ 65 already does).  With A symmetric both factors are row reads,
 // (A B)[i][j] = sum_k A[k][i] B[k][j].
 //
 // Products.  Matrices are stored 64 x 64 (zero padding, row stride kMS).  A warp owns a 32 x 32
@@ -40,30 +43,28 @@ namespace {
 
 constexpr int kNsThreads = 512;
 
+// Barrier of the first `threads` threads of the CTA (whole warps), named barrier 1.
+__device__ __forceinline__ void warps_barrier(int threads) {
+  asm volatile("bar.sync 1, %0;\n" ::"r"(threads) : "memory");
+}
+
 // C = A B for symmetric A (row stride kMS): (A B)[i][j] = sum_k A[k][i] B[k][j].
-// kMirror: only warp tiles tr <= tc, C = 2 Xs - A B written to (i, j) and (j, i) (on a diagonal
-// tile only the entries with i <= j, so C is exactly symmetric).  Otherwise every tile, C = A B.
+// kUpdate: C = (V + V^T) / 2 with V = 2 Xs - A B (exactly symmetric).  Otherwise C = A B.
 // Warp w: tile w % NTILES, k quarter w / NTILES (the four slice-0 warps land on four different
-// sub-partitions).  Ends with a __syncthreads().
-template <int MK, int NWT, bool kMirror>
+// sub-partitions); the slice-0 warps (0 .. NTILES-1) reduce and store, and for kUpdate meet at
+// a named barrier between writing V and reading its transpose.  Ends with a __syncthreads().
+template <int MK, int NWT, bool kUpdate>
 __device__ __forceinline__ void sym_product(const float* __restrict__ A,
                                             const float* __restrict__ B,
                                             const float* __restrict__ Xs, float* __restrict__ C,
                                             float* __restrict__ part) {
-  constexpr int NTILES = kMirror ? NWT * (NWT + 1) / 2 : NWT * NWT;
+  constexpr int NTILES = NWT * NWT;
   constexpr int KS = 4;
   constexpr int KQ = MK / KS;                        // MK is a multiple of 4
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = warp % NTILES, ks = warp / NTILES;
   const bool active = ks < KS;
-  int tr = 0, tc = 0;
-  if (kMirror) {
-    tr = (tile == 2) ? 1 : 0;                        // tiles (0,0), (0,1), (1,1)
-    tc = (tile >= 1) ? 1 : 0;
-  } else {
-    tr = tile / NWT;
-    tc = tile % NWT;
-  }
+  const int tr = tile / NWT, tc = tile % NWT;
   const int rq = lane >> 3, cq = lane & 7;
   const int r0 = 32 * tr + 8 * rq, c0 = 32 * tc + 4 * cq;
   float acc[8][4];
@@ -107,7 +108,7 @@ __device__ __forceinline__ void sym_product(const float* __restrict__ A,
 #pragma unroll
       for (int e = 0; e < 32; ++e)
         acc[e >> 2][e & 3] += part[(((q - 1) * NTILES + tile) * 32 + e) * 32 + lane];
-    if constexpr (kMirror) {
+    if constexpr (kUpdate) {
       float v[8][4];
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
@@ -116,31 +117,24 @@ __device__ __forceinline__ void sym_product(const float* __restrict__ A,
         v[r][1] = 2.f * x4.y - acc[r][1];
         v[r][2] = 2.f * x4.z - acc[r][2];
         v[r][3] = 2.f * x4.w - acc[r][3];
+        *reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]) =
+            make_float4(v[r][0], v[r][1], v[r][2], v[r][3]);
       }
-      if (tr == tc) {
+      warps_barrier(32 * NTILES);                    // V complete
+      float vt[8][4];                                // vt[r][c] = V[c0 + c][r0 + r]
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int i = r0 + r, j = c0 + c;
-            if (i <= j) {
-              C[i * kMS + j] = v[r][c];
-              C[j * kMS + i] = v[r][c];
-            }
-          }
-      } else {
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-          *reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]) =
-              make_float4(v[r][0], v[r][1], v[r][2], v[r][3]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          *reinterpret_cast<float4*>(&C[(c0 + c) * kMS + r0]) =
-              make_float4(v[0][c], v[1][c], v[2][c], v[3][c]);
-          *reinterpret_cast<float4*>(&C[(c0 + c) * kMS + r0 + 4]) =
-              make_float4(v[4][c], v[5][c], v[6][c], v[7][c]);
-        }
+      for (int c = 0; c < 4; ++c) {
+        const float4 t0 = *reinterpret_cast<const float4*>(&C[(c0 + c) * kMS + r0]);
+        const float4 t1 = *reinterpret_cast<const float4*>(&C[(c0 + c) * kMS + r0 + 4]);
+        vt[0][c] = t0.x; vt[1][c] = t0.y; vt[2][c] = t0.z; vt[3][c] = t0.w;
+        vt[4][c] = t1.x; vt[5][c] = t1.y; vt[6][c] = t1.z; vt[7][c] = t1.w;
       }
+      warps_barrier(32 * NTILES);                    // every transpose read before any write
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        *reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]) =
+            make_float4(0.5f * (v[r][0] + vt[r][0]), 0.5f * (v[r][1] + vt[r][1]),
+                        0.5f * (v[r][2] + vt[r][2]), 0.5f * (v[r][3] + vt[r][3]));
     } else {
 #pragma unroll
       for (int r = 0; r < 8; ++r)
@@ -155,14 +149,14 @@ template <int S>
 __global__ void __launch_bounds__(kNsThreads)
 ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
                   float* __restrict__ dbg_dll, float* __restrict__ dbg_w,
-                  float* __restrict__ dbg_x, int d, int T, float eps, float c_exp) {
+                  float* __restrict__ dbg_x, int d, int T, float eps, float c_exp, int gauss) {
   using Sh = NsShape<S>;
   constexpr int M = Sh::M, MP = kMS;
   extern __shared__ float4 smem_ns4[];
   const NsSmem sm = ns_smem_layout<S>(reinterpret_cast<float*>(smem_ns4));
   const long bh = blockIdx.x;
-  ns_prologue<S, kNsThreads>(sm, landmarks + (size_t)bh * M * d, d, eps, c_exp, true, dbg_dll,
-                             dbg_w, bh);
+  ns_prologue<S, kNsThreads>(sm, landmarks + (size_t)bh * M * d, d, eps, c_exp, gauss != 0, true,
+                             dbg_dll, dbg_w, bh);
   float* W = sm.W;
   float* X = sm.X;
   float* P = sm.P;
@@ -183,34 +177,27 @@ ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
   }
 }
 
-// One product on a CTA pair (m > 32, 2 x 2 warp tiles).  The product's output strips (8 rows x
-// 32 columns, four per 32 x 32 tile, tile-major) are cut in two: CTA rank `crank` computes
-// strips [crank * n / 2, (crank + 1) * n / 2), n = 16 (plain) or 12 (mirrored: the upper
-// tiles).  A warp job is two adjacent strips, 16 rows of one tile; lane (rq, cq) = (lane / 8,
-// lane % 8) holds rows 4rq..4rq+3 and columns 4cq..4cq+3 of it, and warp w takes job w % 4
-// over k quarter w / 4.  Results (with their mirror images) are stored into C; pair_publish
-// then copies this CTA's region into the peer.
-template <int MK, bool kMirror>
+// One product on a CTA pair (m > 32, 2 x 2 warp tiles).  The product's 16 output strips (8 rows
+// x 32 columns, four per 32 x 32 tile, tile-major) are cut in two: CTA rank `crank` computes
+// strips 8 crank .. 8 crank + 7, i.e. rows 32 crank .. 32 crank + 31.  A warp job is two
+// adjacent strips, 16 rows of one tile; lane (rq, cq) = (lane / 8, lane % 8) holds rows
+// 4rq..4rq+3 and columns 4cq..4cq+3 of it, and warp w takes job w % 4 over k quarter w / 4.
+// Results are stored into C (kUpdate: V = 2 Xs - A B; otherwise A B); pair_publish then copies
+// this CTA's rows into the peer, and for kUpdate pair_symmetrise averages V with V^T.
+template <int MK, bool kUpdate>
 __device__ __forceinline__ void pair_product(const float* __restrict__ A,
                                              const float* __restrict__ B,
                                              const float* __restrict__ Xs, float* C,
                                              float* __restrict__ part, int crank) {
   constexpr int KS = 4;
   constexpr int KQ = MK / KS;
-  constexpr int NJOBS = kMirror ? 3 : 4;             // two-strip jobs per CTA
+  constexpr int NJOBS = 4;                           // two-strip jobs per CTA
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int job = warp & 3, ks = warp >> 2;
   const bool active = job < NJOBS;
   const int pair = crank * NJOBS + job;
   const int tile = pair >> 1, half = pair & 1;
-  int tr, tc;
-  if (kMirror) {
-    tr = (tile == 2) ? 1 : 0;                        // tiles (0,0), (0,1), (1,1)
-    tc = (tile >= 1) ? 1 : 0;
-  } else {
-    tr = tile >> 1;
-    tc = tile & 1;
-  }
+  const int tr = tile >> 1, tc = tile & 1;
   const int rq = lane >> 3, cq = lane & 7;
   const int r0 = 32 * tr + 16 * half + 4 * rq, c0 = 32 * tc + 4 * cq;
   float acc[4][4];
@@ -250,38 +237,13 @@ __device__ __forceinline__ void pair_product(const float* __restrict__ A,
 #pragma unroll
       for (int e = 0; e < 16; ++e)
         acc[e >> 2][e & 3] += part[(((q - 1) * 4 + job) * 16 + e) * 32 + lane];
-    if constexpr (kMirror) {
-      float v[4][4];
+    if constexpr (kUpdate) {
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const float4 x4 = *reinterpret_cast<const float4*>(&Xs[(r0 + r) * kMS + c0]);
-        v[r][0] = 2.f * x4.x - acc[r][0];
-        v[r][1] = 2.f * x4.y - acc[r][1];
-        v[r][2] = 2.f * x4.z - acc[r][2];
-        v[r][3] = 2.f * x4.w - acc[r][3];
-      }
-      if (tr == tc) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int i = r0 + r, j = c0 + c;
-            if (i <= j) {
-              C[i * kMS + j] = v[r][c];
-              C[j * kMS + i] = v[r][c];
-            }
-          }
-      } else {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          *reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]) =
-              make_float4(v[r][0], v[r][1], v[r][2], v[r][3]);
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          *reinterpret_cast<float4*>(&C[(c0 + c) * kMS + r0]) =
-              make_float4(v[0][c], v[1][c], v[2][c], v[3][c]);
-        }
+        *reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]) =
+            make_float4(2.f * x4.x - acc[r][0], 2.f * x4.y - acc[r][1], 2.f * x4.z - acc[r][2],
+                        2.f * x4.w - acc[r][3]);
       }
     } else {
 #pragma unroll
@@ -294,44 +256,30 @@ __device__ __forceinline__ void pair_product(const float* __restrict__ A,
   __syncthreads();
 }
 
-// Copy this CTA's part of a pair product from C into the peer's copy Cpeer: one 16-byte
-// store per thread (512 threads x 4 floats = 2048 floats, a half of the 64 x 64 matrix).
-// Plain product: rank r owns rows 32r..32r+31.  Mirrored product (strips 0-5 / 6-11 of the
-// upper tiles, with their mirror images): rank 0 owns rows 0-31 x columns 0-31, rows 0-15 x
-// columns 32-63 and rows 32-63 x columns 0-15; rank 1 owns the rest.
-template <bool kMirror>
+// Copy this CTA's rows of a pair product (rows 32 crank .. 32 crank + 31) from C into the
+// peer's copy Cpeer: one 16-byte store per thread (512 threads x 4 floats = 2048 floats).
 __device__ __forceinline__ void pair_publish(const float* __restrict__ C, float* Cpeer,
                                              int crank) {
   const int t = threadIdx.x;             // 0 .. 511
-  int row, col;
-  if (!kMirror) {
-    row = 32 * crank + (t >> 4);
-    col = 4 * (t & 15);
-  } else if (crank == 0) {
-    if (t < 256) {                       // rows 0-31, columns 0-31
-      row = t >> 3;
-      col = 4 * (t & 7);
-    } else if (t < 384) {                // rows 0-15, columns 32-63
-      row = (t - 256) >> 3;
-      col = 32 + 4 * (t & 7);
-    } else {                             // rows 32-63, columns 0-15
-      row = 32 + ((t - 384) >> 2);
-      col = 4 * (t & 3);
-    }
-  } else {
-    if (t < 128) {                       // rows 16-31, columns 32-63
-      row = 16 + (t >> 3);
-      col = 32 + 4 * (t & 7);
-    } else if (t < 256) {                // rows 32-63, columns 16-31
-      row = 32 + ((t - 128) >> 2);
-      col = 16 + 4 * (t & 3);
-    } else {                             // rows 32-63, columns 32-63
-      row = 32 + ((t - 256) >> 3);
-      col = 32 + 4 * (t & 7);
-    }
-  }
+  const int row = 32 * crank + (t >> 4), col = 4 * (t & 15);
   *reinterpret_cast<float4*>(&Cpeer[row * kMS + col]) =
       *reinterpret_cast<const float4*>(&C[row * kMS + col]);
+}
+
+// C <- (C + C^T) / 2 over the m x m block, in place: each unordered pair (i < j) is read and
+// written by one thread.  Both CTAs of a pair hold the same V and compute the same result.
+// Ends with a __syncthreads().
+template <int M>
+__device__ __forceinline__ void pair_symmetrise(float* C) {
+  for (int idx = threadIdx.x; idx < M * M; idx += kNsThreads) {
+    const int i = idx / M, j = idx - i * M;
+    if (i < j) {
+      const float a = 0.5f * (C[i * kMS + j] + C[j * kMS + i]);
+      C[i * kMS + j] = a;
+      C[j * kMS + i] = a;
+    }
+  }
+  __syncthreads();
 }
 
 // One head per cluster of two CTAs (m > 32).  Both CTAs build W and X0; each product is split
@@ -340,7 +288,7 @@ template <int S>
 __global__ void __launch_bounds__(kNsThreads)
 ns_pair_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
                float* __restrict__ dbg_dll, float* __restrict__ dbg_w,
-               float* __restrict__ dbg_x, int d, int T, float eps, float c_exp) {
+               float* __restrict__ dbg_x, int d, int T, float eps, float c_exp, int gauss) {
   using Sh = NsShape<S>;
   static_assert(Sh::NWT == 2, "the pair split assumes 2 x 2 warp tiles");
   constexpr int M = Sh::M, MP = kMS;
@@ -350,8 +298,8 @@ ns_pair_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
   extern __shared__ float4 smem_ns4[];
   const NsSmem sm = ns_smem_layout<S>(reinterpret_cast<float*>(smem_ns4));
   const long bh = blockIdx.x >> 1;
-  ns_prologue<S, kNsThreads>(sm, landmarks + (size_t)bh * M * d, d, eps, c_exp, crank == 0,
-                             dbg_dll, dbg_w, bh);
+  ns_prologue<S, kNsThreads>(sm, landmarks + (size_t)bh * M * d, d, eps, c_exp, gauss != 0,
+                             crank == 0, dbg_dll, dbg_w, bh);
   float* X = sm.X;
   float* Y = sm.Y;
   float* Yp = cluster.map_shared_rank(sm.Y, crank ^ 1);
@@ -361,11 +309,12 @@ ns_pair_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
 
   for (int t = 0; t < T; ++t) {
     pair_product<Sh::MK, false>(sm.W, X, nullptr, sm.P, sm.part, crank);   // P = W X
-    pair_publish<false>(sm.P, Pp, crank);
+    pair_publish(sm.P, Pp, crank);
     cluster.sync();
-    pair_product<Sh::MK, true>(X, sm.P, X, Y, sm.part, crank);            // Y = 2X - X P
-    pair_publish<true>(Y, Yp, crank);
+    pair_product<Sh::MK, true>(X, sm.P, X, Y, sm.part, crank);            // V = 2X - X P
+    pair_publish(Y, Yp, crank);
     cluster.sync();
+    pair_symmetrise<M>(Y);                                                // Y = (V + V^T) / 2
     float* tmp = X; X = Y; Y = tmp;
     tmp = Xp; Xp = Yp; Yp = tmp;
   }
@@ -460,7 +409,8 @@ cudaError_t launch_ns(const lapl_attn_plan& p, const float* landmarks, float* x,
   if (!f) return cudaErrorInvalidValue;
   int d = g.d, T = p.cfg.ns_steps;
   float eps = p.cfg.eps, c_exp = p.neg_log2e_over_lambda;
-  void* args[] = {&landmarks, &x, &dbg_dll, &dbg_w, &dbg_x, &d, &T, &eps, &c_exp};
+  int gauss = p.cfg.kernel == LAPL_KERNEL_GAUSSIAN;
+  void* args[] = {&landmarks, &x, &dbg_dll, &dbg_w, &dbg_x, &d, &T, &eps, &c_exp, &gauss};
   if (g.ns_cluster == 1)
     return cudaLaunchKernel(f, dim3((unsigned)g.bh), dim3(kNsThreads), args, g.ns_smem, st);
   cudaLaunchConfig_t cfg = {};

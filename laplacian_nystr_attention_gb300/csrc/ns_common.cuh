@@ -53,11 +53,40 @@ __device__ __forceinline__ NsSmem ns_smem_layout(float* smem) {
 //
 // Thread t owns column k = t % 64 and the RPG = 64 / (NT / 64) rows starting at
 // (t / 64) * RPG; per channel it reads its own landmark value and RPG / 4 broadcast 16-byte
-// pieces, and keeps RPG independent sums.  Each distance adds |L_ic - L_kc| over c ascending,
-// the same terms in the same order for (i, k) and (k, i), so W is exactly symmetric.
+// pieces, and keeps RPG independent sums.  Each distance adds |L_ic - L_kc| (or its square, for
+// the Gaussian kernel) over c ascending, the same terms in the same order for (i, k) and (k, i),
+// so W is exactly symmetric.
+// acc[r] += D(L_{i0 + r}, L_k) over the d channels of the channel-major landmarks sL: the L1
+// distance, or the squared l2 distance (gauss).  x - y and y - x are exact negatives of each
+// other, so both distances are exactly symmetric in (i, k).
+template <int RPG, bool kGauss>
+__device__ __forceinline__ void landmark_distances(const float* __restrict__ sL, int d, int k,
+                                                   int i0, float (&acc)[RPG]) {
+#pragma unroll 4
+  for (int c = 0; c < d; ++c) {
+    const float lk = sL[c * 64 + k];
+#pragma unroll
+    for (int r4 = 0; r4 < RPG / 4; ++r4) {
+      const float4 li = *reinterpret_cast<const float4*>(&sL[c * 64 + i0 + 4 * r4]);
+      const float e0 = li.x - lk, e1 = li.y - lk, e2 = li.z - lk, e3 = li.w - lk;
+      if constexpr (kGauss) {
+        acc[4 * r4 + 0] = fmaf(e0, e0, acc[4 * r4 + 0]);
+        acc[4 * r4 + 1] = fmaf(e1, e1, acc[4 * r4 + 1]);
+        acc[4 * r4 + 2] = fmaf(e2, e2, acc[4 * r4 + 2]);
+        acc[4 * r4 + 3] = fmaf(e3, e3, acc[4 * r4 + 3]);
+      } else {
+        acc[4 * r4 + 0] += fabsf(e0);
+        acc[4 * r4 + 1] += fabsf(e1);
+        acc[4 * r4 + 2] += fabsf(e2);
+        acc[4 * r4 + 3] += fabsf(e3);
+      }
+    }
+  }
+}
+
 template <int S, int NT>
 __device__ __forceinline__ void ns_prologue(const NsSmem& sm, const float* __restrict__ Lg, int d,
-                                            float eps, float c_exp, bool write_debug,
+                                            float eps, float c_exp, bool gauss, bool write_debug,
                                             float* __restrict__ dbg_dll,
                                             float* __restrict__ dbg_w, long bh) {
   constexpr int M = S * S, MP = kMS;
@@ -89,18 +118,8 @@ __device__ __forceinline__ void ns_prologue(const NsSmem& sm, const float* __res
 #pragma unroll
   for (int r = 0; r < RPG; ++r) acc[r] = 0.f;
   if (i0 < M) {                                   // uniform over the 64 threads of a group
-#pragma unroll 4
-    for (int c = 0; c < d; ++c) {
-      const float lk = sL[c * 64 + k];
-#pragma unroll
-      for (int r4 = 0; r4 < RPG / 4; ++r4) {
-        const float4 li = *reinterpret_cast<const float4*>(&sL[c * 64 + i0 + 4 * r4]);
-        acc[4 * r4 + 0] += fabsf(li.x - lk);
-        acc[4 * r4 + 1] += fabsf(li.y - lk);
-        acc[4 * r4 + 2] += fabsf(li.z - lk);
-        acc[4 * r4 + 3] += fabsf(li.w - lk);
-      }
-    }
+    if (gauss) landmark_distances<RPG, true>(sL, d, k, i0, acc);
+    else landmark_distances<RPG, false>(sL, d, k, i0, acc);
   }
   // W = exp(-D_LL / lambda) + eps I, zero outside m x m; k(x, x) = 1 exactly (D_LL[i][i] = 0).
   float cs = 0.f;

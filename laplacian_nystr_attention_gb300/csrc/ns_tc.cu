@@ -18,8 +18,9 @@
 // Both products take A = X.  The first forms P^T = X W, which equals (W X)^T because X and W
 // are exactly symmetric; its rows are the K-major rows of the second product's Bt, so
 // Q = X P needs no transpose.  The epilogues write whole operand rows (contiguous 16-byte
-// pieces).  X_{t+1} = 2X - Q is made exactly symmetric, upper triangle kept and lower
-// mirrored, as in the CUDA-core kernel: the first product relies on X^T == X.
+// pieces).  As in the CUDA-core kernel, X_{t+1} = (V + V^T) / 2 with V = 2X - Q, exactly
+// symmetric (the first product relies on X^T == X), and averaging drops the antisymmetric part
+// of V's rounding error instead of doubling it into the slow modes.
 //
 // Operands live in shared memory in the tensor cores' K-major layout without swizzle: core
 // matrices of 8 rows x 16 bytes (8 x 4 TF32), cores adjacent in K kLbo bytes apart, adjacent in
@@ -209,7 +210,7 @@ template <int S>
 __global__ void __launch_bounds__(kTcThreads, 1)
 ns_tc_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
              float* __restrict__ dbg_dll, float* __restrict__ dbg_w, float* __restrict__ dbg_x,
-             int d, int T, float eps, float c_exp, unsigned* __restrict__ err) {
+             int d, int T, float eps, float c_exp, int gauss, unsigned* __restrict__ err) {
   using Sh = NsShape<S>;
   constexpr int M = Sh::M;
   constexpr int KSTEPS = (Sh::MK + 7) / 8;
@@ -245,8 +246,8 @@ ns_tc_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
   sm.red = reinterpret_cast<float*>(smem_tc + kOffRed);
   sm.part = nullptr;
   sm.sL = reinterpret_cast<float*>(smem_tc + kOffL);
-  ns_prologue<S, kTcThreads>(sm, landmarks + (size_t)bh * M * d, d, eps, c_exp, true, dbg_dll,
-                             dbg_w, bh);
+  ns_prologue<S, kTcThreads>(sm, landmarks + (size_t)bh * M * d, d, eps, c_exp, gauss != 0, true,
+                             dbg_dll, dbg_w, bh);
 
   // Operands W and X0 as TF32 high/low pairs.  A warp takes 32 consecutive rows of one
   // 4-column piece: its 16-byte stores are contiguous in the operand layout.
@@ -285,7 +286,7 @@ ns_tc_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
     __syncthreads();
     tc_fence_after();
 
-    // ---- Q = X P;  X <- 2X - Q, exactly symmetric ----
+    // ---- Q = X P;  V = 2X - Q;  X <- (V + V^T) / 2, exactly symmetric ----
     if (threadIdx.x == 0) issue_product(tmem, xx_a, pp_a, KSTEPS, bar_a);
     ok = wait_product(bar_a, phase);
     phase ^= 1;
@@ -294,31 +295,25 @@ ns_tc_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
     float y[8];
     int i, col0;
     combine_product(tmem, sc, y, i, col0);
+    // V into sc, at the entries this thread alone read in combine_product.
 #pragma unroll
     for (int j = 0; j < 8; j += 4) {
-      float* px = &Xf[i * kMS + col0 + j];
-      const float4 xo = *reinterpret_cast<const float4*>(px);
+      const float4 xo = *reinterpret_cast<const float4*>(&Xf[i * kMS + col0 + j]);
       y[j] = 2.f * xo.x - y[j];
       y[j + 1] = 2.f * xo.y - y[j + 1];
       y[j + 2] = 2.f * xo.z - y[j + 2];
       y[j + 3] = 2.f * xo.w - y[j + 3];
-      *reinterpret_cast<float4*>(px) = make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
+      *reinterpret_cast<float4*>(&sc[i * kMS + col0 + j]) =
+          make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
     }
     __syncthreads();
-    // Lower triangle from the upper one: entries (i, j < i) read (j, i), which no thread writes
-    // in this pass.
-    float yt[8];
+    // (i, col) and (col, i) add the same two values: the result is exactly symmetric.
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {              // all reads first, then the writes
-      const int col = col0 + j;
-      yt[j] = col < i ? Xf[col * kMS + i] : y[j];
-    }
+    for (int j = 0; j < 8; ++j) y[j] = 0.5f * (y[j] + sc[(col0 + j) * kMS + i]);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int col = col0 + j;
-      if (col < i) Xf[i * kMS + col] = yt[j];
-      y[j] = yt[j];
-    }
+    for (int j = 0; j < 8; j += 4)
+      *reinterpret_cast<float4*>(&Xf[i * kMS + col0 + j]) =
+          make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
 #pragma unroll
     for (int j = 0; j < 8; j += 4)
       store_split(XX, i, col0 + j, make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]));
@@ -384,7 +379,8 @@ cudaError_t launch_ns_tc(const lapl_attn_plan& p, const float* landmarks, float*
   int d = g.d, T = p.cfg.ns_steps;
   float eps = p.cfg.eps, c_exp = p.neg_log2e_over_lambda;
   unsigned* err = p.dev_err;
-  void* args[] = {&landmarks, &x, &dbg_dll, &dbg_w, &dbg_x, &d, &T, &eps, &c_exp, &err};
+  int gauss = p.cfg.kernel == LAPL_KERNEL_GAUSSIAN;
+  void* args[] = {&landmarks, &x, &dbg_dll, &dbg_w, &dbg_x, &d, &T, &eps, &c_exp, &gauss, &err};
   return cudaLaunchKernel(f, dim3((unsigned)g.bh), dim3(kTcThreads), args, g.ns_smem, st);
 }
 

@@ -53,6 +53,21 @@ def test_status_strings(lib):
     assert lib.lapl_attn_version() >= 100
 
 
+def test_config_struct_matches_header(lib):
+    """The ctypes mirror of lapl_attn_config lists the header's fields, in order, all 4 bytes."""
+    src = open(os.path.join(ROOT, "include", "lapl_attn.h")).read()
+    body = re.search(r"typedef struct \{(.*?)\} lapl_attn_config;", src, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if decl:
+            names += [t.strip().split()[-1] for t in decl.split(",")]
+    py = [n if n != "lam" else "lambda" for n, _ in lib.lapl_attn_config._fields_]
+    assert py == names
+    assert ctypes.sizeof(lib.lapl_attn_config) == 4 * len(names)
+
+
 def base_cfg(lib, **kw):
     c = dict(batch=1, heads=1, grid_h=16, grid_w=16, head_dim=32, num_landmarks=16, lam=4.0,
              eps=1e-3, delta=1e-5, ns_steps=20, whiten=1, in_dtype=0, out_dtype=0)
@@ -76,6 +91,8 @@ def base_cfg(lib, **kw):
     (dict(batch=-1), 1),
     (dict(in_dtype=7), 1),
     (dict(whiten=2), 1),
+    (dict(kernel=2), 1),
+    (dict(kernel=-1), 1),
 ])
 def test_create_rejects_bad_configs(lib, bad, status):
     h = ctypes.c_void_p()
