@@ -46,6 +46,7 @@ class _Config(ctypes.Structure):
         ("head_dim", ctypes.c_int), ("num_landmarks", ctypes.c_int),
         ("lam", ctypes.c_double), ("eps", ctypes.c_double), ("delta", ctypes.c_double),
         ("ns_steps", ctypes.c_int), ("whiten", ctypes.c_int), ("kernel", ctypes.c_int),
+        ("solver", ctypes.c_int),
     ]
 
 
@@ -88,7 +89,9 @@ def forward(cfg: dict, q, k, v, bias=None, intermediates: bool = False, slices=N
     """Run the oracle.
 
     cfg: dict with batch, heads, grid_h, grid_w, head_dim, num_landmarks, lam, eps, delta,
-    ns_steps, whiten, and optionally kernel (0 Laplacian, the default; 1 Gaussian).  q, k, v: [B,H,N,d] (converted exactly to float64).  bias: [H,m] or None.
+    ns_steps, whiten, and optionally kernel (0 Laplacian, the default; 1 Gaussian) and solver
+    (0 Newton-Schulz, the default; 1 conjugate gradient, ns_steps iterations).  q, k, v:
+    [B,H,N,d] (converted exactly to float64).  bias: [H,m] or None.
     slices: None for all (b,h) slices, else (begin, count) over s = b*H + h; outputs of other
     slices are left at zero.  Returns (out, inter) where inter is a dict of float64 arrays
     (empty unless ``intermediates``).
@@ -117,7 +120,7 @@ def forward(cfg: dict, q, k, v, bias=None, intermediates: bool = False, slices=N
         im = _Intermediates(**{name: _ptr(inter[name]) for name in _INTERMEDIATES})
     c = _Config(B, H, int(cfg["grid_h"]), int(cfg["grid_w"]), d, m, float(cfg["lam"]),
                 float(cfg["eps"]), float(cfg["delta"]), T, int(cfg["whiten"]),
-                int(cfg.get("kernel", 0)))
+                int(cfg.get("kernel", 0)), int(cfg.get("solver", 0)))
     begin, count = (0, B * H) if slices is None else (int(slices[0]), int(slices[1]))
     rc = _load().orc_forward_slices(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(bias),
                                     _ptr(out), ctypes.byref(im) if im is not None else None,

@@ -133,6 +133,77 @@ static int newton_schulz(const double* W, int m, int T, double* X, double* resid
   return ORC_OK;
 }
 
+/* ---- step 3, alternative: conjugate-gradient solve of W M = B V (solver = 1) -----------
+ * German page, 4 (Ablationsstudien), English page, 4 ("Solver Robustness") and Chinese page,
+ * 4 (ablation): the pages compare the Newton-Schulz iteration with a conjugate-gradient (CG)
+ * solver and report CG as less accurate and less stable on ill-conditioned matrices; they
+ * give no details of the CG variant.
+ * Reading: the classical (Hestenes-Stiefel) CG method for the symmetric positive definite W,
+ * applied to W y = b for each column b of B V separately, from y0 = 0 (so r0 = p0 = b), with
+ * the residual updated recursively; exactly T iterations, the same count T as the
+ * Newton-Schulz steps.  Iteration t: q = W p; alpha = (r.r) / (p.q); y += alpha p;
+ * r -= alpha q; beta = (r.r)_new / (r.r)_old; p = r + beta p.  A column stops early only
+ * where no further step is defined: r.r == 0 (solved exactly) or p.q <= 0.  M gathers the
+ * columns y.  resid[t] = sqrt(sum over columns of r.r after t iterations) / ||B V||_F
+ * (0 when B V = 0).
+ */
+static int conjugate_gradient(const double* W, const double* BV, int m, int d, int T, double* M,
+                              double* resid) {
+  double* y = (double*)malloc(sizeof(double) * (size_t)m);
+  double* r = (double*)malloc(sizeof(double) * (size_t)m);
+  double* p = (double*)malloc(sizeof(double) * (size_t)m);
+  double* q = (double*)malloc(sizeof(double) * (size_t)m);
+  double* rr_hist = (double*)calloc((size_t)(T + 1), sizeof(double));
+  if (!y || !r || !p || !q || !rr_hist) {
+    free(y); free(r); free(p); free(q); free(rr_hist);
+    return ORC_ERR_NOMEM;
+  }
+  for (int j = 0; j < d; ++j) {
+    double rr = 0.0;
+    for (int i = 0; i < m; ++i) {
+      y[i] = 0.0;
+      r[i] = BV[(size_t)i * d + j];
+      p[i] = r[i];
+      rr += r[i] * r[i];
+    }
+    rr_hist[0] += rr;
+    int stopped = rr == 0.0;
+    for (int t = 1; t <= T; ++t) {
+      if (!stopped) {
+        double pq = 0.0;
+        for (int i = 0; i < m; ++i) {
+          double acc = 0.0;
+          for (int k = 0; k < m; ++k) acc += W[(size_t)i * m + k] * p[k];
+          q[i] = acc;
+          pq += p[i] * q[i];
+        }
+        if (!(pq > 0.0)) {
+          stopped = 1;
+        } else {
+          const double alpha = rr / pq;
+          double rr_new = 0.0;
+          for (int i = 0; i < m; ++i) {
+            y[i] += alpha * p[i];
+            r[i] -= alpha * q[i];
+            rr_new += r[i] * r[i];
+          }
+          const double beta = rr_new / rr;
+          for (int i = 0; i < m; ++i) p[i] = r[i] + beta * p[i];
+          rr = rr_new;
+          if (rr == 0.0) stopped = 1;
+        }
+      }
+      rr_hist[t] += rr;
+    }
+    for (int i = 0; i < m; ++i) M[(size_t)i * d + j] = y[i];
+  }
+  if (resid)
+    for (int t = 0; t <= T; ++t)
+      resid[t] = rr_hist[0] > 0.0 ? sqrt(rr_hist[t]) / sqrt(rr_hist[0]) : 0.0;
+  free(y); free(r); free(p); free(q); free(rr_hist);
+  return ORC_OK;
+}
+
 /* ---- step 4: whitening (injective feature map) ----------------------------------------
  * Korean page, 2.2: z_i = Sigma^{-1/2} (k(q_i, .) - mean) + bias, with Sigma replaced by a
  * diagonal estimator of the empirical variance (English page, 2.B; Japanese page, 2.2).
@@ -190,6 +261,7 @@ static int check_config(const orc_config* c) {
   if (!(c->lambda > 0.0) || !(c->eps >= 0.0)) return ORC_ERR_ARG;
   if (c->whiten && !(c->delta > 0.0)) return ORC_ERR_ARG;
   if (c->kernel != 0 && c->kernel != 1) return ORC_ERR_ARG;
+  if (c->solver != 0 && c->solver != 1) return ORC_ERR_ARG;
   const int s = isqrt_exact(c->num_landmarks);
   if (s < 0 || c->grid_h % s != 0 || c->grid_w % s != 0) return ORC_ERR_UNSUPPORTED;
   return ORC_OK;
@@ -246,9 +318,13 @@ static int forward_slice(const orc_config* cfg, int h, const double* Q, const do
                              (j == k ? cfg->eps : 0.0);
     }
 
-  /* 3. Newton-Schulz */
-  rc = newton_schulz(W, m, T, X, resid);
-  if (rc != ORC_OK) goto done;
+  /* 3. Newton-Schulz (solver 0); with the CG solver (1) X is not formed and stays zero */
+  if (cfg->solver == 0) {
+    rc = newton_schulz(W, m, T, X, resid);
+    if (rc != ORC_OK) goto done;
+  } else {
+    memset(X, 0, sizeof(double) * mm);
+  }
 
   /* 4. whitening */
   if (cfg->whiten) {
@@ -268,9 +344,14 @@ static int forward_slice(const orc_config* cfg, int h, const double* Q, const do
     }
   }
 
-  /* 5. output chain, right to left */
+  /* 5. output chain, right to left: M = X (B V), or the CG solution of W M = B V */
   matmul(Bm, V, m, N, d, BV);
-  matmul(X, BV, m, m, d, M);
+  if (cfg->solver == 0) {
+    matmul(X, BV, m, m, d, M);
+  } else {
+    rc = conjugate_gradient(W, BV, m, d, T, M, resid);
+    if (rc != ORC_OK) goto done;
+  }
   matmul(Ahat, M, N, m, d, O);
 
   if (im) {

@@ -20,6 +20,9 @@
  * With kernel = 1 the kernel of step 2 is the Gaussian one the pages compare against,
  * k(x,y) = exp(-||x-y||_2^2 / lambda): similarity decaying with the squared l2 distance
  * (English page, 1 "Theoretical Mismatch"); every other step is unchanged.
+ * With solver = 1 steps 3 and 5 take the conjugate-gradient solver the pages compare the
+ * Newton-Schulz iteration with (German page, 4; English page, 4 "Solver Robustness"):
+ * M = T CG iterations on W M = B V, column by column from zero, replaces X (B V).
  */
 #ifndef LAPL_ORACLE_H
 #define LAPL_ORACLE_H
@@ -42,6 +45,8 @@ typedef struct {
   int whiten;              /* 1: whiten A; 0: A_hat = A (bias ignored) */
   int kernel;              /* 0: Laplacian, distance sum_c |x_c - y_c|;
                               1: Gaussian, distance sum_c (x_c - y_c)^2 */
+  int solver;              /* 0: Newton-Schulz X, M = X (B V);
+                              1: T conjugate-gradient iterations on W M = B V */
 } orc_config;
 
 /* Every pointer may be NULL.  Shapes are for the whole [B,H] batch, C order. */
@@ -53,13 +58,14 @@ typedef struct {
   double* a;         /* [B,H,N,m]   exp(-D_QL / lambda)             */
   double* b;         /* [B,H,m,N]   exp(-D_LK / lambda)             */
   double* w;         /* [B,H,m,m]   exp(-D_LL / lambda) + eps I     */
-  double* x;         /* [B,H,m,m]   X_T                             */
+  double* x;         /* [B,H,m,m]   X_T (zeros with the CG solver)  */
   double* mu;        /* [B,H,m]     column means of A               */
   double* var;       /* [B,H,m]     column variances of A (divide by N) */
   double* a_hat;     /* [B,H,N,m]   whitened A                      */
   double* bv;        /* [B,H,m,d]   B V                             */
-  double* m_mat;     /* [B,H,m,d]   X (B V)                         */
-  double* ns_resid;  /* [B,H,T+1]   Frobenius norm of I - W X_t, t = 0..T */
+  double* m_mat;     /* [B,H,m,d]   X (B V), or the CG solution     */
+  double* ns_resid;  /* [B,H,T+1]   Frobenius norm of I - W X_t, t = 0..T; with the CG
+                                    solver the relative residual ||R_t||_F / ||B V||_F */
 } orc_intermediates;
 
 /* Status codes. */
