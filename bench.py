@@ -11,10 +11,12 @@ Prints one JSON line (rank 0).  Multi-GPU (torchrun): every rank runs its own co
 workload (independent (batch, head) slices, no data-path collective): weak scaling.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
-                  [--kernel laplacian|gaussian]
+                  [--kernel laplacian|gaussian] [--solver newton_schulz|cg]
 
 --kernel gaussian runs the same pipeline with the Gaussian kernel exp(-|x - y|_2^2 / lambda)
 in place of the Laplacian one (the softmax-free baseline the method is set against).
+--solver cg replaces the Newton-Schulz inverse by T conjugate-gradient iterations on
+W M = B V (the solver the method is compared with).
 """
 from __future__ import annotations
 
@@ -67,6 +69,7 @@ OPS_CONVENTION = {
                 "FMA)",
 }
 KERNEL_IDS = {"laplacian": 0, "gaussian": 1}
+SOLVER_IDS = {"newton_schulz": 0, "cg": 1}
 
 
 def cdist_sources_sha() -> str:
@@ -84,6 +87,7 @@ def parse():
     ap.add_argument("--workload", default="stage1_f32", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--kernel", default="laplacian", choices=sorted(KERNEL_IDS))
+    ap.add_argument("--solver", default="newton_schulz", choices=sorted(SOLVER_IDS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="budget of the oracle CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -99,20 +103,23 @@ def dist_env():
     return world, rank, local
 
 
-def workload_desc(w, kernel: str) -> dict:
+def workload_desc(w, kernel: str, solver: str = "newton_schulz") -> dict:
     return {
         "workload": (f"{w.name}: B={w.batch} H={w.heads} grid {w.grid_h}x{w.grid_w} "
                      f"(N={w.n}) d={w.head_dim} m={w.num_landmarks} T={w.ns_steps} "
                      f"lambda={w.lam:g} eps={w.eps:g} delta={w.delta:g} {w.dtype} {w.dist}"
-                     + ("" if kernel == "laplacian" else f"; {kernel} kernel")),
+                     + ("" if kernel == "laplacian" else f"; {kernel} kernel")
+                     + ("" if solver == "newton_schulz" else f"; {solver} solver")),
         "batch": w.batch, "heads": w.heads, "seq_len": w.n, "head_dim": w.head_dim,
         "landmarks": w.num_landmarks, "ns_steps": w.ns_steps, "kernel": kernel,
+        "solver": solver,
     }
 
 
-def oracle_cfg(w, kernel: str) -> dict:
+def oracle_cfg(w, kernel: str, solver: str = "newton_schulz") -> dict:
     cfg = w.config()
     cfg["kernel"] = KERNEL_IDS[kernel]
+    cfg["solver"] = SOLVER_IDS[solver]
     return cfg
 
 
@@ -196,13 +203,14 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def oracle_rate(w, q, k, v, budget_s: float, threads: int, kernel: str = "laplacian"):
+def oracle_rate(w, q, k, v, budget_s: float, threads: int, kernel: str = "laplacian",
+                solver: str = "newton_schulz"):
     """Whole (b,h) slices of the fp64 oracle, `threads` at a time (the oracle's C call releases
     the GIL), until the budget is spent.  Returns (tokens/s, slices done, seconds)."""
     import concurrent.futures as cf
     import oracle
     oracle.build()
-    cfg = oracle_cfg(w, kernel)
+    cfg = oracle_cfg(w, kernel, solver)
     q64, k64, v64 = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
     slices = w.batch * w.heads
     done, t0 = 0, time.perf_counter()
@@ -216,12 +224,13 @@ def oracle_rate(w, q, k, v, budget_s: float, threads: int, kernel: str = "laplac
     return done * w.n / w.heads / dt, done, dt      # tokens are counted once across heads
 
 
-def cpu_baseline(w, q, k, v, budget_s: float, kernel: str = "laplacian") -> dict:
+def cpu_baseline(w, q, k, v, budget_s: float, kernel: str = "laplacian",
+                 solver: str = "newton_schulz") -> dict:
     """The fp64 oracle on a bounded sample: whole (b,h) slices on all host cores until the
     budget is spent, and the same on one core for reference."""
     cores = host_cores()
-    one, n1, t1 = oracle_rate(w, q, k, v, budget_s / 4, 1, kernel)
-    allc, na, ta = oracle_rate(w, q, k, v, budget_s, cores, kernel)
+    one, n1, t1 = oracle_rate(w, q, k, v, budget_s / 4, 1, kernel, solver)
+    allc, na, ta = oracle_rate(w, q, k, v, budget_s, cores, kernel, solver)
     return {"value": allc, "unit": UNIT, "cores": cores, "kind": "oracle",
             "value_1_core": one,
             "sample": f"{na} of {w.batch * w.heads} (batch, head) slices of {w.name} in "
@@ -238,7 +247,7 @@ def run_reference(args, w):
     q, k, v = make_inputs(w)
     import oracle
     oracle.build()
-    cfg = oracle_cfg(w, args.kernel)
+    cfg = oracle_cfg(w, args.kernel, args.solver)
     q64, k64, v64 = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
     slices = w.batch * w.heads
     cores = host_cores()
@@ -264,7 +273,7 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_t / len(times), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_desc(w, args.kernel),
+        "config": workload_desc(w, args.kernel, args.solver),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -293,7 +302,8 @@ def run_ours(args, w):
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     hq, hk, hv = (torch.from_numpy(x).to(tdt).pin_memory() for x in (q, k, v))
     dq, dk, dv = (x.to(dev) for x in (hq, hk, hv))
-    cfg = lna.make_config(**{**w.config(), "in_dtype": w.dtype, "kernel": args.kernel})
+    cfg = lna.make_config(**{**w.config(), "in_dtype": w.dtype, "kernel": args.kernel,
+                             "solver": args.solver})
     att = lna.LaplacianNystromAttention(cfg)
     out = torch.empty((w.batch, w.heads, w.n, w.head_dim), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -435,7 +445,7 @@ def run_ours(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic",
-        "config": {**workload_desc(w, args.kernel),
+        "config": {**workload_desc(w, args.kernel, args.solver),
                    "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write, "
                          f"then a {CLEAN_BYTES >> 20} MiB read; not timed)",
                    "parallelism": f"replicas x{world} (independent (batch, head) slices)",
@@ -462,7 +472,8 @@ def run_ours(args, w):
         "impl": "ours",
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, q, k, v, args.cpu_seconds, args.kernel)
+        line["cpu_baseline"] = cpu_baseline(w, q, k, v, args.cpu_seconds, args.kernel,
+                                            args.solver)
     print(json.dumps(line), flush=True)
     att.close()
     if world > 1:

@@ -63,6 +63,17 @@ typedef enum { LAPL_F32 = 0, LAPL_BF16 = 1 } lapl_dtype;
  */
 typedef enum { LAPL_KERNEL_LAPLACIAN = 0, LAPL_KERNEL_GAUSSIAN = 1 } lapl_kernel;
 
+/*
+ * How M ~ W^-1 (B V) is obtained.
+ *   LAPL_SOLVER_NEWTON_SCHULZ: X = T Newton-Schulz steps, M = X (B V) (the method).
+ *   LAPL_SOLVER_CG: M = T conjugate-gradient iterations on W M = B V, each column from zero,
+ *     a column stopping early only where no step is defined (r.r = 0 or p.Wp <= 0); X is
+ *     not formed.  The solver the pages compare Newton-Schulz with (German page, 4; English
+ *     page, 4 "Solver Robustness").  All of its work runs after the B V kernel, on the
+ *     launching stream.
+ */
+typedef enum { LAPL_SOLVER_NEWTON_SCHULZ = 0, LAPL_SOLVER_CG = 1 } lapl_solver;
+
 typedef struct {
   int batch;          /* B >= 0 (B == 0: forward is a no-op)                                */
   int heads;          /* H >= 1                                                             */
@@ -72,11 +83,13 @@ typedef struct {
   float lambda;       /* kernel scale, > 0 (the pages' best value is 4)                    */
   float eps;          /* >= 0, added to the diagonal of W                                    */
   float delta;        /* > 0 when whiten != 0: variance floor inside the square root         */
-  int ns_steps;       /* T, 0 <= T <= 1000, exactly T Newton-Schulz steps                    */
+  int ns_steps;       /* T, 0 <= T <= 1000: exactly T Newton-Schulz steps (or at most T CG
+                         iterations per column with LAPL_SOLVER_CG)                         */
   int whiten;         /* 1: whiten A (default); 0: A^ = A and bias is ignored                */
   int in_dtype;       /* lapl_dtype of Q, K, V                                               */
   int out_dtype;      /* lapl_dtype of O (LAPL_F32 recommended; LAPL_BF16 rounds at the end) */
   int kernel;         /* lapl_kernel (0, the Laplacian kernel, when the struct is zeroed)     */
+  int solver;         /* lapl_solver (0, Newton-Schulz, when the struct is zeroed)            */
 } lapl_attn_config;
 
 typedef struct lapl_attn_plan* lapl_attn_handle;
@@ -89,12 +102,12 @@ typedef struct {
   float* d_lk;       /* [B,H,m,N] raw distances D(L_j, K_n)             */
   float* landmarks;  /* [B,H,m,d] L                                      */
   float* w;          /* [B,H,m,m] W = k(L,L) + eps I                     */
-  float* x;          /* [B,H,m,m] X after T Newton-Schulz steps          */
+  float* x;          /* [B,H,m,m] X after T Newton-Schulz steps (not written with CG) */
   float* a;          /* [B,H,N,m] A = k(Q,L), before whitening           */
   float* mu;         /* [B,H,m]   column means of A                      */
   float* rstd;       /* [B,H,m]   1/sqrt(var + delta) (var divides by N) */
   float* bv;         /* [B,H,m,d] B V                                    */
-  float* m;          /* [B,H,m,d] X (B V)                                */
+  float* m;          /* [B,H,m,d] M = X (B V), or the CG solution        */
 } lapl_attn_debug;
 
 /* Library version: major * 10000 + minor * 100 + patch. */
@@ -158,8 +171,9 @@ lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void
  * lapl_attn_stage_times() waits for the events of the last forward (it synchronises the host
  * with them) and writes the elapsed milliseconds of
  *   ms[0] pooling, ms[1] Newton-Schulz, ms[2] distance kernel, ms[3] B V partials, ms[4]
- *   finish (the wait for the solve, then the B V reduction and M = X (B V)), ms[5] output
- *   (column statistics, whitening and O = A^ M).
+ *   finish (the wait for the solve, then the B V reduction and M = X (B V); with the CG
+ *   solver, the CG kernel, W included, and ms[1] is 0), ms[5] output (column statistics,
+ *   whitening and O = A^ M).
  * LAPL_ERR_INVALID_ARG if timing is off or no forward ran since it was switched on.
  */
 lapl_status lapl_attn_set_timing(lapl_attn_handle h, int enable);
@@ -174,7 +188,8 @@ lapl_status lapl_attn_stage_times(lapl_attn_handle h, float* ms);
  */
 lapl_status lapl_attn_stage_marks(lapl_attn_handle h, float* ms);
 
-/* Number of kernels one forward launches (for launch accounting). */
+/* Number of kernels one forward launches (for launch accounting): 6, or 5 with the CG
+ * solver. */
 int lapl_attn_kernels_per_forward(lapl_attn_handle h);
 
 /*

@@ -16,7 +16,7 @@ import ctypes
 
 from . import _lib
 from ._lib import (LAPL_BF16, LAPL_F32, LAPL_KERNEL_GAUSSIAN, LAPL_KERNEL_LAPLACIAN,
-                   LaplAttnError, lapl_attn_config, lapl_attn_create,
+                   LAPL_SOLVER_CG, LAPL_SOLVER_NEWTON_SCHULZ, LaplAttnError, lapl_attn_config, lapl_attn_create,
                    lapl_attn_debug, lapl_attn_destroy, lapl_attn_device_errors,
                    lapl_attn_forward,
                    lapl_attn_forward_debug, lapl_attn_forward_host, lapl_attn_host_staging_size,
@@ -32,22 +32,27 @@ __all__ = [
     "lapl_attn_status_string", "lapl_attn_version", "lapl_attn_workspace_size", "LAPL_F32",
     "LAPL_BF16", "lapl_attn_set_timing", "lapl_attn_stage_times", "lapl_attn_stage_marks",
     "lapl_attn_kernels_per_forward", "lapl_attn_device_errors", "lapl_attn_plan_info_get",
-    "make_config", "LAPL_KERNEL_LAPLACIAN", "LAPL_KERNEL_GAUSSIAN",
+    "make_config", "LAPL_KERNEL_LAPLACIAN", "LAPL_KERNEL_GAUSSIAN", "LAPL_SOLVER_NEWTON_SCHULZ",
+    "LAPL_SOLVER_CG",
 ]
 
 _DTYPES = {"f32": LAPL_F32, "bf16": LAPL_BF16}
 _KERNELS = {"laplacian": LAPL_KERNEL_LAPLACIAN, "gaussian": LAPL_KERNEL_GAUSSIAN}
+_SOLVERS = {"newton_schulz": LAPL_SOLVER_NEWTON_SCHULZ, "cg": LAPL_SOLVER_CG}
 
 
 def make_config(batch, heads, grid_h, grid_w, head_dim, num_landmarks, lam=4.0, eps=1e-3,
                 delta=1e-5, ns_steps=20, whiten=1, in_dtype="f32", out_dtype="f32",
-                kernel="laplacian", **_ignored) -> lapl_attn_config:
+                kernel="laplacian", solver="newton_schulz", **_ignored) -> lapl_attn_config:
     """kernel: "laplacian" (exp(-L1 / lam), the method) or "gaussian" (exp(-squared l2 / lam)),
-    or the lapl_kernel integer."""
+    or the lapl_kernel integer.  solver: "newton_schulz" (X by ns_steps Newton-Schulz steps,
+    M = X (B V)) or "cg" (ns_steps conjugate-gradient iterations on W M = B V), or the
+    lapl_solver integer."""
     return lapl_attn_config(int(batch), int(heads), int(grid_h), int(grid_w), int(head_dim),
                             int(num_landmarks), float(lam), float(eps), float(delta),
                             int(ns_steps), int(whiten), _DTYPES.get(in_dtype, in_dtype),
-                            _DTYPES.get(out_dtype, out_dtype), _KERNELS.get(kernel, kernel))
+                            _DTYPES.get(out_dtype, out_dtype), _KERNELS.get(kernel, kernel),
+                            _SOLVERS.get(solver, solver))
 
 
 class LaplacianNystromAttention:

@@ -25,6 +25,8 @@ LAPL_F32 = 0
 LAPL_BF16 = 1
 LAPL_KERNEL_LAPLACIAN = 0
 LAPL_KERNEL_GAUSSIAN = 1
+LAPL_SOLVER_NEWTON_SCHULZ = 0
+LAPL_SOLVER_CG = 1
 
 
 class lapl_attn_config(ctypes.Structure):
@@ -35,7 +37,7 @@ class lapl_attn_config(ctypes.Structure):
         ("lam", ctypes.c_float), ("eps", ctypes.c_float), ("delta", ctypes.c_float),
         ("ns_steps", ctypes.c_int), ("whiten", ctypes.c_int),
         ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
-        ("kernel", ctypes.c_int),
+        ("kernel", ctypes.c_int), ("solver", ctypes.c_int),
     ]
 
 

@@ -54,6 +54,8 @@ lapl_status validate(const lapl_attn_config* c) {
     return LAPL_ERR_INVALID_ARG;
   if (c->kernel != LAPL_KERNEL_LAPLACIAN && c->kernel != LAPL_KERNEL_GAUSSIAN)
     return LAPL_ERR_INVALID_ARG;
+  if (c->solver != LAPL_SOLVER_NEWTON_SCHULZ && c->solver != LAPL_SOLVER_CG)
+    return LAPL_ERR_INVALID_ARG;
   const int s = isqrt_exact(c->num_landmarks);
   if (s < 0 || s > kMaxS) return LAPL_ERR_UNSUPPORTED;
   if (c->grid_h % s != 0 || c->grid_w % s != 0) return LAPL_ERR_UNSUPPORTED;
@@ -140,7 +142,15 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   int per_sm = 1;
   e = device_error_word(&p->dev_err);
   if (e == cudaSuccess) e = cdist_plan(*p, &per_sm);
-  if (e == cudaSuccess) {
+  g.cg = cfg->solver == LAPL_SOLVER_CG;
+  if (e == cudaSuccess && g.cg) {
+    // Conjugate gradient: one kernel after B V, on the launching stream; no Newton-Schulz.
+    g.ns_cluster = 1;
+    g.ns_tc = false;
+    g.ns_exclusive = false;
+    g.cg_smem = cg_smem_bytes(g.m, g.d);
+    e = cg_configure(g.s, g.d, g.cg_smem);
+  } else if (e == cudaSuccess) {
     // Newton-Schulz is the longest dependency chain of the forward.  Kernels: "tc" (one CTA per
     // head, products on the tensor cores; the default for m >= 25), "ffma" (one CTA per head,
     // CUDA-core products; the default for m <= 16) and "pair" (a cluster of two CTAs per head
@@ -204,11 +214,14 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   }
   if (per_sm < 1) per_sm = 1;
   {
-    // B V: about two CTAs per SM in total, whole 128-token chunks per CTA.
+    // B V: about two CTAs per SM in total, whole 128-token chunks per CTA, and at most
+    // kMaxBvSplits CTAs per head: the M kernel stages every split's partial of its 8 columns
+    // in shared memory (64 splits at m = 64: 146 KB).
+    constexpr long long kMaxBvSplits = 64;
     const long long bh1 = g.bh > 0 ? g.bh : 1;
     const int tiles = (g.n + bv_tile_tokens() - 1) / bv_tile_tokens();
     long long want = (2LL * p->num_sms + bh1 - 1) / bh1;
-    want = std::max<long long>(1, std::min<long long>(want, tiles));
+    want = std::max<long long>(1, std::min<long long>(std::min(want, kMaxBvSplits), tiles));
     g.bv_tiles_per_split = (int)((tiles + want - 1) / want);
     g.bv_splits = (tiles + g.bv_tiles_per_split - 1) / g.bv_tiles_per_split;
     // Column statistics of A: one warp per landmark column, appended to the B V grid.
@@ -328,6 +341,26 @@ static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k,
                         : launch_ns(*p, L, X, D.d_ll, D.w, D.x, s);
   };
   LAPL_MARK(kMarkStart, st);
+  if (p->geo.cg) {
+    // Conjugate gradient: pooling -> distances -> B V -> CG (which builds W itself) -> output,
+    // all on the launching stream; the CG kernel is a programmatic dependent of the B V kernel
+    // and the output kernel of the CG kernel.  The solve marks are recorded back to back.
+    LAPL_TRY(launch_pool(*p, k, L, D.landmarks, st), "forward/pool");
+    LAPL_MARK(kMarkPoolDone, st);
+    LAPL_MARK(kMarkNsStart, st);
+    LAPL_MARK(kMarkNsDone, st);
+    LAPL_MARK(kMarkCdistStart, st);
+    LAPL_TRY(launch_cdist(*p, q, k, v, L, At, Bt, D.d_ql, D.d_lk, D.a, st), "forward/cdist");
+    LAPL_MARK(kMarkCdistDone, st);
+    LAPL_TRY(launch_bv(*p, Bt, v, bvp, At, mu, rstd, D.mu, D.rstd, st), "forward/bv");
+    LAPL_MARK(kMarkBvDone, st);
+    LAPL_TRY(launch_cg(*p, L, bvp, M, D.d_ll, D.w, D.bv, D.m, st), "forward/cg");
+    LAPL_MARK(kMarkMixDone, st);
+    LAPL_TRY(launch_output(*p, At, M, mu, rstd, bias, out, st), "forward/output");
+    LAPL_MARK(kMarkOutputDone, st);
+    if (tm) p->timed_once = true;
+    return LAPL_OK;
+  }
   if (p->geo.ns_exclusive) {
     // The solve is the longest chain: pooling -> solve -> M -> output on the launching stream;
     // the solve's CTAs are placed the moment pooling ends.  The distance kernel and
@@ -506,7 +539,10 @@ lapl_status lapl_attn_stage_marks(lapl_attn_handle h, float* ms) {
   return LAPL_OK;
 }
 
-int lapl_attn_kernels_per_forward(lapl_attn_handle h) { return (h && h->geo.bh > 0) ? 6 : 0; }
+int lapl_attn_kernels_per_forward(lapl_attn_handle h) {
+  if (!h || h->geo.bh == 0) return 0;
+  return h->geo.cg ? 5 : 6;
+}
 
 lapl_status lapl_attn_device_errors(lapl_attn_handle h, void* stream, unsigned* flags) {
   if (!h || !flags) return LAPL_ERR_INVALID_ARG;

@@ -119,6 +119,9 @@ bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __r
           int m, int d, int n, int tiles_per_split, int splits, const float* __restrict__ at,
           float* __restrict__ mu, float* __restrict__ rstd, float* __restrict__ dbg_mu,
           float* __restrict__ dbg_rstd, long bv_ctas, float delta) {
+  // A kernel launched as this grid's programmatic dependent (the conjugate-gradient solver)
+  // may start its own preparation now; it waits for this grid before it reads any result.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   if ((long)blockIdx.x >= bv_ctas) {     // a column-statistics CTA (uniform per CTA)
     column_stats(at, mu, rstd, dbg_mu, dbg_rstd, m, n, delta, (long)blockIdx.x - bv_ctas);
     return;

@@ -81,6 +81,8 @@ struct Geometry {
   int ns_cluster;          // Newton-Schulz CTAs per head (a cluster of 1 or 2)
   bool ns_tc;              // Newton-Schulz products on the tensor cores (ns_tc.cu)
   bool ns_exclusive;       // Newton-Schulz CTAs own their SMs (few heads)
+  bool cg;                 // conjugate-gradient solver (cg.cu) instead of Newton-Schulz
+  size_t cg_smem;
   size_t pool_threads;
 };
 
@@ -154,6 +156,12 @@ int bv_tile_tokens();
 cudaError_t bv_configure(size_t smem);
 size_t mix_smem_bytes(int m, int bv_splits);
 cudaError_t mix_configure(size_t smem);
+// Conjugate-gradient solver: M = T CG iterations on W M = B V (replaces Newton-Schulz + mix).
+size_t cg_smem_bytes(int m, int d);
+cudaError_t cg_configure(int s, int d, size_t smem);
+cudaError_t launch_cg(const lapl_attn_plan& p, const float* landmarks, const float* bvp,
+                      float* mmat, float* dbg_dll, float* dbg_w, float* dbg_bv, float* dbg_m,
+                      cudaStream_t st);
 
 // ---- device helpers ---------------------------------------------------------------------
 __device__ __forceinline__ float laplacian_from_distance(float dist, float neg_log2e_over_lambda) {

@@ -93,6 +93,8 @@ def base_cfg(lib, **kw):
     (dict(whiten=2), 1),
     (dict(kernel=2), 1),
     (dict(kernel=-1), 1),
+    (dict(solver=2), 1),
+    (dict(solver=-1), 1),
 ])
 def test_create_rejects_bad_configs(lib, bad, status):
     h = ctypes.c_void_p()

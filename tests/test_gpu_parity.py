@@ -113,6 +113,19 @@ def test_workload_sampled_slices(name):
     assert np.isfinite(out).all()
 
 
+@pytest.mark.parametrize("name", ["hires_bf16", "sweep_f32_65536"])
+def test_single_head_long_sequence(name):
+    """B * H = 1 with 128 or 512 token chunks: the B V kernel's split count reaches its cap of
+    64 CTAs per head (the M kernel stages every split's partial in shared memory)."""
+    w = WORKLOADS[name].replace(batch=1, heads=1)
+    q, k, v = make_inputs(w)
+    info = {}
+    out, _ = run_gpu(w, q, k, v, info=info)
+    ref, _ = oracle_run(w, q, k, v)
+    assert info["bv_splits"] == 64
+    assert slice_rel_err(out, ref) < tol_of(w)
+
+
 # ---- edge cases ----------------------------------------------------------------------------
 TINY = WORKLOADS["tiny_f32"]
 
