@@ -239,6 +239,25 @@ def cpu_baseline(w, q, k, v, budget_s: float, kernel: str = "laplacian",
                       "seconds"}
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's `value` (the job's time is its slowest rank's); the value
+    itself on one rank.  Works on any process-group backend (NCCL with a CUDA device, gloo on
+    the CPU)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, tokens_per_rank: int, ms: float) -> float:
+    """Whole-job tokens/s: every rank processes its own copy of the workload (independent
+    (batch, head) slices), in the max-over-ranks time `ms`."""
+    return world * tokens_per_rank / (ms / 1e3)
+
+
 def run_reference(args, w):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -343,11 +362,7 @@ def run_ours(args, w):
             ends[i].record(stream)
         barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
     kernels = lna.lapl_attn_kernels_per_forward(att.handle)
     gpu_launches = kernels * args.steps
 
@@ -381,12 +396,9 @@ def run_ours(args, w):
             g.replay()
             g1[i].record(stream)
         barrier()
-        gms = sum(a.elapsed_time(b) for a, b in zip(g0, g1)) / args.steps
-        if world > 1:
-            t = torch.tensor([gms], device=dev)
-            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-            gms = float(t.item())
-        graph = {"value": world * w.tokens / (gms / 1e3), "unit": UNIT, "ms_per_step": gms,
+        gms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(g0, g1)) / args.steps,
+                             world, dev)
+        graph = {"value": job_rate(world, w.tokens, gms), "unit": UNIT, "ms_per_step": gms,
                  "note": "lapl_attn_forward captured in one CUDA graph (both streams), "
                          "replayed; L2 flushed before each replay"}
         del g
@@ -409,13 +421,9 @@ def run_ours(args, w):
             lna.lapl_attn_forward_host(*args_h)
         e1.record(stream)
         barrier()
-        e2e_ms = e0.elapsed_time(e1) / args.steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
         in_b = hq.numel() * hq.element_size()
-        e2e = {"value": world * w.tokens / (e2e_ms / 1e3), "unit": UNIT,
+        e2e = {"value": job_rate(world, w.tokens, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": 3 * in_b,
                "d2h_bytes_per_step": hout.numel() * hout.element_size(),
                "ms_per_step": e2e_ms}
@@ -441,7 +449,7 @@ def run_ours(args, w):
     traffic = rec[0] if rec and rec[1] == cdist_sources_sha() else None
     clk = clocks.summary()
     line = {
-        "metric": METRIC, "value": world * w.tokens / (ms / 1e3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": job_rate(world, w.tokens, ms), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic",
