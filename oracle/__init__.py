@@ -64,11 +64,14 @@ def _load():
     with _lock:
         if _lib is None:
             lib = ctypes.CDLL(build())
-            for fn in (lib.orc_forward_slices,):
+            for fn in (lib.orc_forward_slices, lib.orc_backward_slices):
                 fn.restype = ctypes.c_int
             lib.orc_forward_slices.argtypes = [
                 ctypes.POINTER(_Config), _DP, _DP, _DP, _DP, _DP,
                 ctypes.POINTER(_Intermediates), ctypes.c_long, ctypes.c_long]
+            lib.orc_backward_slices.argtypes = [
+                ctypes.POINTER(_Config), _DP, _DP, _DP, _DP, _DP, _DP, _DP, _DP, _DP, _DP, _DP,
+                ctypes.c_double, ctypes.c_long, ctypes.c_long]
             _lib = lib
     return _lib
 
@@ -83,6 +86,42 @@ def _as_f64(a):
 
 class OracleError(RuntimeError):
     pass
+
+
+def _config(cfg: dict) -> _Config:
+    return _Config(int(cfg["batch"]), int(cfg["heads"]), int(cfg["grid_h"]), int(cfg["grid_w"]),
+                   int(cfg["head_dim"]), int(cfg["num_landmarks"]), float(cfg["lam"]),
+                   float(cfg["eps"]), float(cfg["delta"]), int(cfg["ns_steps"]),
+                   int(cfg["whiten"]), int(cfg.get("kernel", 0)), int(cfg.get("solver", 0)))
+
+
+def backward(cfg: dict, q, k, v, dout, bias=None, slices=None, tau: float = 2.0 ** -15):
+    """Gradients of a loss with dLoss/dO = dout, through the whole forward (the chain rule
+    step by step; see the C source).
+
+    Returns (dq, dk, dv, dbias, amb_dq, amb_dk): float64 arrays [B,H,N,d] (zero outside the
+    requested slices), dbias [H,m] (summed over the requested slices' batches), and for the
+    Laplacian kernel the bounds on how far each dq / dk entry can move when a sign decision
+    sgn(x - y) with |x - y| <= tau (|x| + |y|) is taken the other way (zeros otherwise)."""
+    B, H = int(cfg["batch"]), int(cfg["heads"])
+    N = int(cfg["grid_h"]) * int(cfg["grid_w"])
+    d, m = int(cfg["head_dim"]), int(cfg["num_landmarks"])
+    q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    for t in (q, k, v, dout):
+        if t.shape != (B, H, N, d):
+            raise ValueError(f"expected [B,H,N,d]={(B, H, N, d)}, got {t.shape}")
+    bias = None if bias is None else _as_f64(bias)
+    outs = [np.zeros((B, H, N, d)) for _ in range(5)]
+    dbias = np.zeros((H, m))
+    begin, count = (0, B * H) if slices is None else (int(slices[0]), int(slices[1]))
+    c = _config(cfg)
+    dq, dk, dv, aq, ak = outs
+    rc = _load().orc_backward_slices(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(bias),
+                                     _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias),
+                                     _ptr(aq), _ptr(ak), float(tau), begin, count)
+    if rc != 0:
+        raise OracleError(f"oracle backward returned status {rc}")
+    return dq, dk, dv, dbias, aq, ak
 
 
 def forward(cfg: dict, q, k, v, bias=None, intermediates: bool = False, slices=None):
@@ -118,9 +157,7 @@ def forward(cfg: dict, q, k, v, bias=None, intermediates: bool = False, slices=N
     if intermediates:
         inter = {name: np.zeros(shapes[name], dtype=np.float64) for name in _INTERMEDIATES}
         im = _Intermediates(**{name: _ptr(inter[name]) for name in _INTERMEDIATES})
-    c = _Config(B, H, int(cfg["grid_h"]), int(cfg["grid_w"]), d, m, float(cfg["lam"]),
-                float(cfg["eps"]), float(cfg["delta"]), T, int(cfg["whiten"]),
-                int(cfg.get("kernel", 0)), int(cfg.get("solver", 0)))
+    c = _config(cfg)
     begin, count = (0, B * H) if slices is None else (int(slices[0]), int(slices[1]))
     rc = _load().orc_forward_slices(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(bias),
                                     _ptr(out), ctypes.byref(im) if im is not None else None,

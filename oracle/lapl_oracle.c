@@ -405,3 +405,322 @@ int orc_forward(const orc_config* cfg, const double* q, const double* k, const d
   if (rc != ORC_OK) return rc;
   return orc_forward_slices(cfg, q, k, v, bias, out, im, 0, (long)cfg->batch * cfg->heads);
 }
+
+/* =========================================================================================
+ * Backward: reverse-mode derivative of the forward above for a scalar loss whose gradient
+ * with respect to O is G (dO).  The pages claim CUDA kernels for the forward and the backward
+ * pass (English page, 2 "CUDA Acceleration"; German page, 2) and describe no gradient; every
+ * step below is the chain rule applied to the forward step named beside it, in the reverse
+ * order of the forward.  The non-differentiable points take these readings:
+ *   |x - y| at x == y: derivative 0 (the sign function with sgn(0) = 0; for D_LL's diagonal,
+ *     D_jj == 0 identically, so 0 is the derivative);
+ *   the max in |W|_1 and |W|_inf: the derivative of the first maximal column (row) sum.
+ * Only the Newton-Schulz solver is differentiated (solver = 1 is rejected).
+ * ======================================================================================= */
+
+/* d D(x, y) / d x for the kernel's distance: sgn(x - y) (Laplacian) or 2 (x - y) (Gaussian). */
+static double distance_slope(const orc_config* cfg, double x, double y) {
+  if (cfg->kernel == 1) return 2.0 * (x - y);
+  return x > y ? 1.0 : (x < y ? -1.0 : 0.0);
+}
+
+/* A pair whose sign decision a float32 computation may take the other way. */
+static int near_tie(const orc_config* cfg, double x, double y, double tau) {
+  return cfg->kernel == 0 && fabs(x - y) <= tau * (fabs(x) + fabs(y));
+}
+
+/* Newton-Schulz as in step 3, keeping every iterate X_0 .. X_T ([T+1][m][m]) and the first
+ * maximal column (jc) and row (ir) of the norms of X0. */
+static int newton_schulz_history(const double* W, int m, int T, double* Xs, double* scale,
+                                 int* jc, int* ir) {
+  double n1 = -1.0, ninf = -1.0;
+  for (int j = 0; j < m; ++j) {
+    double s = 0.0;
+    for (int i = 0; i < m; ++i) s += fabs(W[(size_t)i * m + j]);
+    if (s > n1) { n1 = s; *jc = j; }
+  }
+  for (int i = 0; i < m; ++i) {
+    double s = 0.0;
+    for (int j = 0; j < m; ++j) s += fabs(W[(size_t)i * m + j]);
+    if (s > ninf) { ninf = s; *ir = i; }
+  }
+  *scale = n1 * ninf;
+  const size_t mm = (size_t)m * m;
+  for (int i = 0; i < m; ++i)
+    for (int j = 0; j < m; ++j) Xs[(size_t)i * m + j] = W[(size_t)j * m + i] / *scale;
+  double* P = (double*)malloc(sizeof(double) * mm);
+  if (!P) return ORC_ERR_NOMEM;
+  for (int t = 0; t < T; ++t) {
+    const double* X = Xs + (size_t)t * mm;
+    double* Xn = Xs + (size_t)(t + 1) * mm;
+    matmul(W, X, m, m, m, P);                               /* P = W X */
+    for (int i = 0; i < m; ++i) /* X_{t+1} = X (2I - P) */
+      for (int j = 0; j < m; ++j) {
+        double s = 0.0;
+        for (int k = 0; k < m; ++k)
+          s += X[(size_t)i * m + k] * ((k == j ? 2.0 : 0.0) - P[(size_t)k * m + j]);
+        Xn[(size_t)i * m + j] = s;
+      }
+  }
+  free(P);
+  return ORC_OK;
+}
+
+/* C = A^T B for A [inner, rows], B [inner, cols]. */
+static void matmul_tn(const double* Aop, const double* Bop, int rows, int inner, int cols,
+                      double* C) {
+  for (int i = 0; i < rows; ++i)
+    for (int j = 0; j < cols; ++j) {
+      double s = 0.0;
+      for (int k = 0; k < inner; ++k) s += Aop[(size_t)k * rows + i] * Bop[(size_t)k * cols + j];
+      C[(size_t)i * cols + j] = s;
+    }
+}
+
+/* C = A B^T for A [rows, inner], B [cols, inner]. */
+static void matmul_nt(const double* Aop, const double* Bop, int rows, int inner, int cols,
+                      double* C) {
+  for (int i = 0; i < rows; ++i)
+    for (int j = 0; j < cols; ++j) {
+      double s = 0.0;
+      for (int k = 0; k < inner; ++k) s += Aop[(size_t)i * inner + k] * Bop[(size_t)j * inner + k];
+      C[(size_t)i * cols + j] = s;
+    }
+}
+
+static int backward_slice(const orc_config* cfg, int h, const double* Q, const double* K,
+                          const double* V, const double* bias, const double* G, double* dQ,
+                          double* dK, double* dV, double* dbias, double* amb_q, double* amb_k,
+                          double tau) {
+  const int N = cfg->grid_h * cfg->grid_w, d = cfg->head_dim, m = cfg->num_landmarks;
+  const int s = isqrt_exact(m), ph = cfg->grid_h / s, pw = cfg->grid_w / s;
+  const int T = cfg->ns_steps;
+  const double lam = cfg->lambda;
+  const size_t nm = (size_t)N * m, mm = (size_t)m * m, md = (size_t)m * d;
+  double* L = (double*)malloc(sizeof(double) * md);
+  double* A = (double*)malloc(sizeof(double) * nm);
+  double* Bm = (double*)malloc(sizeof(double) * nm);
+  double* W = (double*)malloc(sizeof(double) * mm);
+  double* Xs = (double*)malloc(sizeof(double) * mm * (size_t)(T + 1));
+  double* mu = (double*)malloc(sizeof(double) * m);
+  double* var = (double*)malloc(sizeof(double) * m);
+  double* Ahat = (double*)malloc(sizeof(double) * nm);
+  double* Z = (double*)malloc(sizeof(double) * nm);
+  double* BV = (double*)malloc(sizeof(double) * md);
+  double* M = (double*)malloc(sizeof(double) * md);
+  double* dAhat = (double*)malloc(sizeof(double) * nm);
+  double* dM = (double*)malloc(sizeof(double) * md);
+  double* gq = (double*)malloc(sizeof(double) * nm);      /* dLoss / dD_QL */
+  double* dL = (double*)calloc(md, sizeof(double));
+  double* ambL = (double*)calloc(md, sizeof(double));
+  double* dBV = (double*)malloc(sizeof(double) * md);
+  double* dX = (double*)malloc(sizeof(double) * mm);
+  double* dXp = (double*)malloc(sizeof(double) * mm);
+  double* dW = (double*)calloc(mm, sizeof(double));
+  double* gk = (double*)malloc(sizeof(double) * nm);      /* dLoss / dD_LK, [m][N] */
+  double* t1 = (double*)malloc(sizeof(double) * mm);
+  double* t2 = (double*)malloc(sizeof(double) * mm);
+  double scale = 1.0;
+  int jc = 0, ir = 0, rc = ORC_OK;
+  if (!L || !A || !Bm || !W || !Xs || !mu || !var || !Ahat || !Z || !BV || !M || !dAhat || !dM ||
+      !gq || !dL || !ambL || !dBV || !dX || !dXp || !dW || !gk || !t1 || !t2) {
+    rc = ORC_ERR_NOMEM;
+    goto done;
+  }
+
+  /* forward, steps 1-5, keeping what the backward needs */
+  landmarks_avgpool(K, cfg->grid_w, d, s, ph, pw, L);
+  for (int i = 0; i < N; ++i)
+    for (int j = 0; j < m; ++j)
+      A[(size_t)i * m + j] =
+          laplacian_of_distance(kernel_distance(cfg, Q + (size_t)i * d, L + (size_t)j * d, d), lam);
+  for (int j = 0; j < m; ++j)
+    for (int n = 0; n < N; ++n)
+      Bm[(size_t)j * N + n] =
+          laplacian_of_distance(kernel_distance(cfg, L + (size_t)j * d, K + (size_t)n * d, d), lam);
+  for (int j = 0; j < m; ++j)
+    for (int k = 0; k < m; ++k)
+      W[(size_t)j * m + k] =
+          laplacian_of_distance(kernel_distance(cfg, L + (size_t)j * d, L + (size_t)k * d, d), lam) +
+          (j == k ? cfg->eps : 0.0);
+  rc = newton_schulz_history(W, m, T, Xs, &scale, &jc, &ir);
+  if (rc != ORC_OK) goto done;
+  const double* X = Xs + (size_t)T * mm;
+  if (cfg->whiten) {
+    whiten_columns(A, N, m, cfg->delta, bias ? bias + (size_t)h * m : NULL, mu, var, Ahat);
+    for (int i = 0; i < N; ++i)
+      for (int j = 0; j < m; ++j)
+        Z[(size_t)i * m + j] = (A[(size_t)i * m + j] - mu[j]) / sqrt(var[j] + cfg->delta);
+  } else {
+    memcpy(Ahat, A, sizeof(double) * nm);
+  }
+  matmul(Bm, V, m, N, d, BV);
+  matmul(X, BV, m, m, d, M);
+
+  /* step 5 back: O = A_hat M  ->  dA_hat = G M^T, dM = A_hat^T G */
+  matmul_nt(G, M, N, d, m, dAhat);
+  matmul_tn(Ahat, G, m, N, d, dM);
+
+  /* step 4 back: A_hat = Z + bias, Z = (A - mu) r, r = 1/sqrt(var + delta), var over N:
+   * dbias_j = sum_i dA_hat_ij;  dA_ij = r_j (dZ_ij - mean_i dZ_ij - Z_ij mean_i(dZ_ij Z_ij)) */
+  if (cfg->whiten) {
+    for (int j = 0; j < m; ++j) {
+      double s1 = 0.0, s2 = 0.0;
+      for (int i = 0; i < N; ++i) {
+        s1 += dAhat[(size_t)i * m + j];
+        s2 += dAhat[(size_t)i * m + j] * Z[(size_t)i * m + j];
+      }
+      if (dbias) dbias[j] += s1;
+      const double r = 1.0 / sqrt(var[j] + cfg->delta);
+      for (int i = 0; i < N; ++i) {
+        const double da = r * (dAhat[(size_t)i * m + j] - s1 / (double)N -
+                               Z[(size_t)i * m + j] * s2 / (double)N);
+        gq[(size_t)i * m + j] = -A[(size_t)i * m + j] / lam * da;   /* step 2 back: d exp */
+      }
+    }
+  } else {
+    for (size_t e = 0; e < nm; ++e) gq[e] = -A[e] / lam * dAhat[e];
+  }
+
+  /* step 2 back, query block: D_QL[i][j] = sum_c D(Q_ic, L_jc) */
+  for (int i = 0; i < N; ++i)
+    for (int c = 0; c < d; ++c) {
+      double acc = 0.0, amb = 0.0;
+      const double qv = Q[(size_t)i * d + c];
+      for (int j = 0; j < m; ++j) {
+        const double lv = L[(size_t)j * d + c], g = gq[(size_t)i * m + j];
+        const double sl = distance_slope(cfg, qv, lv);
+        acc += g * sl;
+        dL[(size_t)j * d + c] -= g * sl;
+        if (near_tie(cfg, qv, lv, tau)) {
+          amb += 2.0 * fabs(g);
+          ambL[(size_t)j * d + c] += 2.0 * fabs(g);
+        }
+      }
+      dQ[(size_t)i * d + c] = acc;
+      if (amb_q) amb_q[(size_t)i * d + c] = amb;
+    }
+
+  /* step 5 back: M = X BV  ->  dBV = X^T dM, dX = dM BV^T */
+  matmul_tn(X, dM, m, m, d, dBV);
+  matmul_nt(dM, BV, m, d, m, dX);
+  /* BV = B V  ->  dB = dBV V^T, dV = B^T dBV; step 2 back, key block: gk = -B/lambda dB */
+  matmul_tn(Bm, dBV, N, m, d, dV);
+  for (int j = 0; j < m; ++j)
+    for (int n = 0; n < N; ++n) {
+      double db = 0.0;
+      for (int c = 0; c < d; ++c) db += dBV[(size_t)j * d + c] * V[(size_t)n * d + c];
+      gk[(size_t)j * N + n] = -Bm[(size_t)j * N + n] / lam * db;
+    }
+  /* D_LK[j][n] = sum_c D(L_jc, K_nc) */
+  for (int n = 0; n < N; ++n)
+    for (int c = 0; c < d; ++c) {
+      double acc = 0.0, amb = 0.0;
+      const double kv = K[(size_t)n * d + c];
+      for (int j = 0; j < m; ++j) {
+        const double lv = L[(size_t)j * d + c], g = gk[(size_t)j * N + n];
+        const double sl = distance_slope(cfg, lv, kv);
+        dL[(size_t)j * d + c] += g * sl;
+        acc -= g * sl;
+        if (near_tie(cfg, lv, kv, tau)) {
+          amb += 2.0 * fabs(g);
+          ambL[(size_t)j * d + c] += 2.0 * fabs(g);
+        }
+      }
+      dK[(size_t)n * d + c] = acc;
+      if (amb_k) amb_k[(size_t)n * d + c] = amb;
+    }
+
+  /* step 3 back: X_{t+1} = X_t Y_t, Y_t = 2I - W X_t:
+   *   dW += -X_t^T dX_{t+1} X_t^T;  dX_t = dX_{t+1} Y_t^T - W^T X_t^T dX_{t+1} */
+  for (int t = T - 1; t >= 0; --t) {
+    const double* Xt = Xs + (size_t)t * mm;
+    matmul_tn(Xt, dX, m, m, m, t1);                  /* t1 = X_t^T dX_{t+1} */
+    matmul_nt(t1, Xt, m, m, m, t2);                  /* t2 = t1 X_t^T */
+    for (size_t e = 0; e < mm; ++e) dW[e] -= t2[e];
+    matmul(W, Xt, m, m, m, t2);                      /* t2 = W X_t, Y_t = 2I - t2 */
+    for (int i = 0; i < m; ++i)
+      for (int j = 0; j < m; ++j) {
+        double sy = 0.0, sw = 0.0;
+        for (int k = 0; k < m; ++k) {
+          sy += dX[(size_t)i * m + k] * ((j == k ? 2.0 : 0.0) - t2[(size_t)j * m + k]);
+          sw += W[(size_t)k * m + i] * t1[(size_t)k * m + j];
+        }
+        dXp[(size_t)i * m + j] = sy - sw;
+      }
+    memcpy(dX, dXp, sizeof(double) * mm);
+  }
+  /* X_0 = W^T / (|W|_1 |W|_inf) */
+  {
+    double dsc = 0.0;
+    for (int i = 0; i < m; ++i)
+      for (int j = 0; j < m; ++j) {
+        dW[(size_t)j * m + i] += dX[(size_t)i * m + j] / scale;
+        dsc -= dX[(size_t)i * m + j] * W[(size_t)j * m + i] / (scale * scale);
+      }
+    double n1 = 0.0, ninf = 0.0;
+    for (int i = 0; i < m; ++i) n1 += fabs(W[(size_t)i * m + jc]);
+    for (int j = 0; j < m; ++j) ninf += fabs(W[(size_t)ir * m + j]);
+    for (int i = 0; i < m; ++i) {
+      const double w = W[(size_t)i * m + jc];
+      dW[(size_t)i * m + jc] += dsc * ninf * (w > 0.0 ? 1.0 : (w < 0.0 ? -1.0 : 0.0));
+    }
+    for (int j = 0; j < m; ++j) {
+      const double w = W[(size_t)ir * m + j];
+      dW[(size_t)ir * m + j] += dsc * n1 * (w > 0.0 ? 1.0 : (w < 0.0 ? -1.0 : 0.0));
+    }
+  }
+  /* step 2 back, landmark block: W = exp(-D_LL / lambda) + eps I; D_LL[j][k] = sum_c D(L_j, L_k):
+   * dL_pc += sum_k (gw[p][k] + gw[k][p]) slope(L_pc, L_kc) */
+  for (int p = 0; p < m; ++p)
+    for (int k = 0; k < m; ++k) {
+      if (k == p) continue;
+      const double kpk = W[(size_t)p * m + k], kkp = W[(size_t)k * m + p];
+      const double g = -kpk / lam * dW[(size_t)p * m + k] - kkp / lam * dW[(size_t)k * m + p];
+      for (int c = 0; c < d; ++c) {
+        const double lp = L[(size_t)p * d + c], lk = L[(size_t)k * d + c];
+        dL[(size_t)p * d + c] += g * distance_slope(cfg, lp, lk);
+        if (near_tie(cfg, lp, lk, tau)) ambL[(size_t)p * d + c] += 2.0 * fabs(g);
+      }
+    }
+
+  /* step 1 back: L_j = mean of K over window j  ->  dK_n += dL_j(n) / (ph pw) */
+  for (int r = 0; r < cfg->grid_h; ++r)
+    for (int cc = 0; cc < cfg->grid_w; ++cc) {
+      const int j = (r / ph) * s + cc / pw;
+      const size_t n = (size_t)r * cfg->grid_w + cc;
+      for (int c = 0; c < d; ++c) {
+        dK[n * d + c] += dL[(size_t)j * d + c] / (double)(ph * pw);
+        if (amb_k) amb_k[n * d + c] += ambL[(size_t)j * d + c] / (double)(ph * pw);
+      }
+    }
+
+done:
+  free(L); free(A); free(Bm); free(W); free(Xs); free(mu); free(var); free(Ahat); free(Z);
+  free(BV); free(M); free(dAhat); free(dM); free(gq); free(dL); free(ambL); free(dBV); free(dX);
+  free(dXp); free(dW); free(gk); free(t1); free(t2);
+  return rc;
+}
+
+int orc_backward_slices(const orc_config* cfg, const double* q, const double* k, const double* v,
+                        const double* bias, const double* dout, double* dq, double* dk,
+                        double* dv, double* dbias, double* amb_dq, double* amb_dk, double tau,
+                        long slice_begin, long slice_count) {
+  const int rc = check_config(cfg);
+  if (rc != ORC_OK) return rc;
+  if (cfg->solver != 0) return ORC_ERR_UNSUPPORTED;
+  const long slices = (long)cfg->batch * cfg->heads;
+  if (slice_begin < 0 || slice_count < 0 || slice_begin + slice_count > slices) return ORC_ERR_ARG;
+  if (slice_count == 0) return ORC_OK;
+  if (!q || !k || !v || !dout || !dq || !dk || !dv) return ORC_ERR_ARG;
+  const size_t nd = (size_t)cfg->grid_h * cfg->grid_w * cfg->head_dim;
+  for (long sl = slice_begin; sl < slice_begin + slice_count; ++sl) {
+    const int h = (int)(sl % cfg->heads);
+    const size_t o = (size_t)sl * nd;
+    const int r = backward_slice(cfg, h, q + o, k + o, v + o, bias, dout + o, dq + o, dk + o,
+                                 dv + o, dbias ? dbias + (size_t)h * cfg->num_landmarks : NULL,
+                                 amb_dq ? amb_dq + o : NULL, amb_dk ? amb_dk + o : NULL, tau);
+    if (r != ORC_OK) return r;
+  }
+  return ORC_OK;
+}

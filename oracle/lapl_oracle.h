@@ -82,6 +82,22 @@ int orc_forward(const orc_config* cfg, const double* q, const double* k, const d
  * Same, restricted to the slices s = b*H + h with slice_begin <= s < slice_begin + slice_count.
  * Arrays are still the full [B,H,...] arrays; only those slices are read or written.
  */
+/*
+ * Backward of the forward for a loss with gradient dout = dLoss/dO ([B,H,N,d]), over the
+ * slices s = b*H + h with slice_begin <= s < slice_begin + slice_count: dq, dk, dv
+ * ([B,H,N,d]) are written for those slices; dbias ([H,m], or NULL) receives += each slice's
+ * column sums of dLoss/dA_hat (zero when whiten = 0), so the caller zeroes it first.
+ * amb_dq, amb_dk (nullable, [B,H,N,d]): for the Laplacian kernel, a bound on how far each
+ * entry can move when a float32 computation takes a sign decision sgn(x - y) the other way:
+ * the sum of 2 |gradient weight| over the pairs with |x - y| <= tau (|x| + |y|), landmark
+ * pairs included and carried through the pooling (zero for the Gaussian kernel).
+ * Newton-Schulz solver only (ORC_ERR_UNSUPPORTED for solver = 1).
+ */
+int orc_backward_slices(const orc_config* cfg, const double* q, const double* k, const double* v,
+                        const double* bias, const double* dout, double* dq, double* dk,
+                        double* dv, double* dbias, double* amb_dq, double* amb_dk, double tau,
+                        long slice_begin, long slice_count);
+
 int orc_forward_slices(const orc_config* cfg, const double* q, const double* k, const double* v,
                        const double* bias, double* out, const orc_intermediates* im,
                        long slice_begin, long slice_count);
