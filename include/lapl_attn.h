@@ -249,6 +249,34 @@ lapl_status lapl_attn_plan_info_get(lapl_attn_handle h, lapl_attn_plan_info* inf
 lapl_status lapl_attn_forward_noalloc(lapl_attn_handle h, const void* q, const void* k,
                                       const void* v, const float* bias, void* out, void* stream);
 
+/*
+ * Backward pass: the gradients of a loss with dLoss/dO = dout through the whole forward (the
+ * pages claim forward and backward CUDA kernels: English page, 2 "CUDA Acceleration"; German
+ * page, 2; they give no gradient, so it is the chain rule through every forward step).
+ *
+ *   q, k, v, bias   the forward's inputs (bias NULL = zeros), unchanged since that forward;
+ *   dout            device [B,H,N,d] fp32, dLoss/dO;
+ *   dq, dk, dv      device [B,H,N,d] fp32, written (fp32 also for bf16 inputs);
+ *   dbias           device [H,m] fp32 or NULL: written with the sum over the batch of
+ *                   dLoss/dbias (zeros when whiten = 0);
+ *   fwd_workspace   the workspace of that forward (lapl_attn_forward on the same handle),
+ *                   untouched since: the backward reads the landmarks, X, A, B, the column
+ *                   statistics, the B V partials and M from it;
+ *   bwd_workspace   device, >= lapl_attn_backward_workspace_size bytes, overwritten.
+ * Derivative conventions: d|x - y|/dx = sgn(x - y) with sgn(0) = 0 (for the Gaussian kernel
+ * 2 (x - y)); the norms of X0 = W^T / (|W|_1 |W|_inf) differentiate through their first
+ * maximal column / row.  Stream-ordered, asynchronous, no allocation; 7 launches.
+ * LAPL_ERR_UNSUPPORTED with the CG solver.  Other errors as for forward().
+ */
+lapl_status lapl_attn_backward_workspace_size(lapl_attn_handle h, size_t* bytes);
+lapl_status lapl_attn_backward(lapl_attn_handle h, const void* q, const void* k, const void* v,
+                               const float* bias, const float* dout, float* dq, float* dk,
+                               float* dv, float* dbias, const void* fwd_workspace,
+                               size_t fwd_workspace_bytes, void* bwd_workspace,
+                               size_t bwd_workspace_bytes, void* stream);
+/* Number of kernels one backward launches (0 with the CG solver or an empty batch). */
+int lapl_attn_backward_kernels(lapl_attn_handle h);
+
 /* Release the plan (host state only).  NULL is accepted. */
 lapl_status lapl_attn_destroy(lapl_attn_handle h);
 

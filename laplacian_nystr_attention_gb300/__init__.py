@@ -23,7 +23,9 @@ from ._lib import (LAPL_BF16, LAPL_F32, LAPL_KERNEL_GAUSSIAN, LAPL_KERNEL_LAPLAC
                    lapl_attn_kernels_per_forward, lapl_attn_last_error,
                    lapl_attn_set_timing, lapl_attn_stage_marks, lapl_attn_stage_times,
                    lapl_attn_status_string,
-                   lapl_attn_plan_info_get, lapl_attn_version, lapl_attn_workspace_size)
+                   lapl_attn_plan_info_get, lapl_attn_version, lapl_attn_workspace_size,
+                   lapl_attn_backward, lapl_attn_backward_kernels,
+                   lapl_attn_backward_workspace_size)
 
 __all__ = [
     "LaplacianNystromAttention", "LaplAttnError", "lapl_attn_config", "lapl_attn_debug",
@@ -32,7 +34,8 @@ __all__ = [
     "lapl_attn_status_string", "lapl_attn_version", "lapl_attn_workspace_size", "LAPL_F32",
     "LAPL_BF16", "lapl_attn_set_timing", "lapl_attn_stage_times", "lapl_attn_stage_marks",
     "lapl_attn_kernels_per_forward", "lapl_attn_device_errors", "lapl_attn_plan_info_get",
-    "make_config", "LAPL_KERNEL_LAPLACIAN", "LAPL_KERNEL_GAUSSIAN", "LAPL_SOLVER_NEWTON_SCHULZ",
+    "make_config", "lapl_attn_backward", "lapl_attn_backward_kernels",
+    "lapl_attn_backward_workspace_size", "LAPL_KERNEL_LAPLACIAN", "LAPL_KERNEL_GAUSSIAN", "LAPL_SOLVER_NEWTON_SCHULZ",
     "LAPL_SOLVER_CG",
 ]
 
@@ -119,6 +122,41 @@ class LaplacianNystromAttention:
         return out
 
     __call__ = forward
+
+    def backward(self, q, k, v, dout, bias=None, grads=None, stream=None):
+        """(dq, dk, dv, dbias) for a loss with dLoss/dO = dout, after forward(q, k, v, bias) on
+        this object (whose workspace holds what that forward saved; run nothing else on it in
+        between).  dout: fp32 [B,H,N,d].  grads: optional dict with preallocated fp32 "dq",
+        "dk", "dv" ([B,H,N,d]) and "dbias" ([H,m]) tensors.  The backward workspace is
+        allocated on first use."""
+        import torch
+        c = self.cfg
+        for name, t in (("q", q), ("k", k), ("v", v)):
+            self._check_io(t, c.in_dtype, name)
+        self._check_io(dout, LAPL_F32, "dout")
+        shape = (c.batch, c.heads, c.grid_h * c.grid_w, c.head_dim)
+        g = dict(grads or {})
+        for name in ("dq", "dk", "dv"):
+            if name not in g:
+                g[name] = torch.empty(shape, dtype=torch.float32, device=q.device)
+            self._check_io(g[name], LAPL_F32, name)
+        if "dbias" not in g:
+            g["dbias"] = torch.empty((c.heads, c.num_landmarks), dtype=torch.float32,
+                                     device=q.device)
+        if bias is not None:
+            bias = bias.contiguous()
+        if getattr(self, "bwd_workspace", None) is None:
+            self.bwd_workspace_bytes = lapl_attn_backward_workspace_size(self.handle)
+            self.bwd_workspace = torch.empty(max(self.bwd_workspace_bytes, 256),
+                                             dtype=torch.uint8, device=q.device)
+        st = stream if stream is not None else torch.cuda.current_stream()
+        lapl_attn_backward(self.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                           bias.data_ptr() if bias is not None else None, dout.data_ptr(),
+                           g["dq"].data_ptr(), g["dk"].data_ptr(), g["dv"].data_ptr(),
+                           g["dbias"].data_ptr(), self.workspace.data_ptr(),
+                           self.workspace_bytes, self.bwd_workspace.data_ptr(),
+                           self.bwd_workspace_bytes, st.cuda_stream)
+        return g["dq"], g["dk"], g["dv"], g["dbias"]
 
     def close(self):
         if getattr(self, "handle", None) is not None:

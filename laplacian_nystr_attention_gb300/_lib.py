@@ -87,6 +87,9 @@ def _load():
         "lapl_attn_forward_noalloc": ([H, vp, vp, vp, vp, vp, vp], st),
         "lapl_attn_device_errors": ([H, vp, ctypes.POINTER(ctypes.c_uint)], st),
         "lapl_attn_plan_info_get": ([H, ctypes.POINTER(lapl_attn_plan_info)], st),
+        "lapl_attn_backward_workspace_size": ([H, ctypes.POINTER(sz)], st),
+        "lapl_attn_backward": ([H, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, sz, vp], st),
+        "lapl_attn_backward_kernels": ([H], ctypes.c_int),
         "lapl_attn_destroy": ([H], st),
     }
     for name, (args, res) in sigs.items():
@@ -103,7 +106,8 @@ EXPORTED = ["lapl_attn_version", "lapl_attn_status_string", "lapl_attn_last_erro
             "lapl_attn_set_timing", "lapl_attn_stage_times", "lapl_attn_stage_marks",
             "lapl_attn_kernels_per_forward",
             "lapl_attn_forward_noalloc", "lapl_attn_device_errors", "lapl_attn_plan_info_get",
-            "lapl_attn_destroy"]
+            "lapl_attn_backward_workspace_size", "lapl_attn_backward",
+            "lapl_attn_backward_kernels", "lapl_attn_destroy"]
 
 
 def status_string(status: int) -> str:
@@ -198,6 +202,24 @@ def lapl_attn_stage_marks(handle) -> dict:
 
 def lapl_attn_kernels_per_forward(handle) -> int:
     return LIB.lapl_attn_kernels_per_forward(handle)
+
+
+def lapl_attn_backward_workspace_size(handle) -> int:
+    n = ctypes.c_size_t()
+    _check(LIB.lapl_attn_backward_workspace_size(handle, ctypes.byref(n)),
+           "lapl_attn_backward_workspace_size", handle)
+    return n.value
+
+
+def lapl_attn_backward(handle, q, k, v, bias, dout, dq, dk, dv, dbias, fwd_workspace,
+                       fwd_workspace_bytes, bwd_workspace, bwd_workspace_bytes, stream) -> None:
+    _check(LIB.lapl_attn_backward(handle, q, k, v, bias, dout, dq, dk, dv, dbias, fwd_workspace,
+                                  fwd_workspace_bytes, bwd_workspace, bwd_workspace_bytes,
+                                  stream), "lapl_attn_backward", handle)
+
+
+def lapl_attn_backward_kernels(handle) -> int:
+    return LIB.lapl_attn_backward_kernels(handle)
 
 
 def lapl_attn_device_errors(handle, stream) -> int:

@@ -202,6 +202,7 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
     delete p;
     return LAPL_ERR_CUDA;
   }
+  if (e == cudaSuccess && !g.cg) e = bwd_configure(*p);
   if (e == cudaSuccess) {
     g.bv_threads = bv_threads(g.m, g.d);
     g.bv_smem = bv_smem_bytes(g.m, g.d, g.bv_threads, cfg->in_dtype == LAPL_BF16);
@@ -406,6 +407,51 @@ static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k,
 #undef LAPL_MARK
 #undef LAPL_TRY
   return LAPL_OK;
+}
+
+lapl_status lapl_attn_backward_workspace_size(lapl_attn_handle h, size_t* bytes) {
+  if (!h || !bytes) return LAPL_ERR_INVALID_ARG;
+  if (h->geo.cg) return LAPL_ERR_UNSUPPORTED;
+  *bytes = bwd_layout(*h).total;
+  return LAPL_OK;
+}
+
+lapl_status lapl_attn_backward(lapl_attn_handle h, const void* q, const void* k, const void* v,
+                               const float* bias, const float* dout, float* dq, float* dk,
+                               float* dv, float* dbias, const void* fwd_workspace,
+                               size_t fwd_workspace_bytes, void* bwd_workspace,
+                               size_t bwd_workspace_bytes, void* stream) {
+  if (!h) return LAPL_ERR_INVALID_ARG;
+  if (h->geo.cg) return LAPL_ERR_UNSUPPORTED;
+  if (h->geo.bh == 0) return LAPL_OK;
+  if (!q || !k || !v || !dout || !dq || !dk || !dv || !fwd_workspace || !bwd_workspace)
+    return LAPL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || !aligned16(fwd_workspace) ||
+      !aligned16(bwd_workspace) || (bias && ((uintptr_t)bias & 3u)) ||
+      (dbias && ((uintptr_t)dbias & 3u)))
+    return LAPL_ERR_ALIGNMENT;
+  if (fwd_workspace_bytes < h->ws.total || bwd_workspace_bytes < bwd_layout(*h).total)
+    return LAPL_ERR_WORKSPACE;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error(h, e, "backward/device");
+    return LAPL_ERR_CUDA;
+  }
+  if (dev != h->device) return LAPL_ERR_INVALID_ARG;
+  e = launch_backward(*h, q, k, v, bias, dout, dq, dk, dv, dbias,
+                      static_cast<const char*>(fwd_workspace), static_cast<char*>(bwd_workspace),
+                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    set_error(h, e, "backward");
+    return LAPL_ERR_CUDA;
+  }
+  return LAPL_OK;
+}
+
+int lapl_attn_backward_kernels(lapl_attn_handle h) {
+  return (h && h->geo.bh > 0 && !h->geo.cg) ? 7 : 0;
 }
 
 lapl_status lapl_attn_forward(lapl_attn_handle h, const void* q, const void* k, const void* v,

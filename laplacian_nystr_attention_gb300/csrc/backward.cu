@@ -1,0 +1,737 @@
+// backward.cu -- gradients of a loss with dLoss/dO = G with respect to Q, K, V and the bias.
+//
+// The pages claim CUDA kernels for the forward and the backward pass ("LaplacianFormer:
+// Rethinking Linear Attention with Laplacian Kernel", English explainer page, 2 "CUDA
+// Acceleration"; German page, 2) and give no gradient: every kernel below applies the chain
+// rule to one forward step, in reverse order.  The forward's workspace supplies what it saved
+// (landmarks L, X, A^T, B^T, the column statistics, the B V partials and M).
+//
+//   bwd_ahat_kernel   (head, token split)   dA^ = G M^T (stored), partials of dM = A^T G and
+//                                           of the column sums s1 = sum dA^, s2 = sum dA^ Z
+//   bwd_head_kernel   (head)                dM, dBV = X^T dM, dX = dM BV^T; Newton-Schulz
+//                                           recomputed with every iterate kept, then run
+//                                           backwards to dW; the landmark-block term of dL
+//   bwd_query_kernel  (head, token tile)    g = dLoss/dD_QL = -(A / lambda) dA (stored) with
+//                                           dA from the whitening backward; dQ
+//   bwd_key_kernel    (head, token tile)    h = dLoss/dD_LK = -(B / lambda) (dBV V^T) (stored);
+//                                           dK's distance term and dV = B^T dBV
+//   bwd_lm_kernel     (head, split, side)   partials of dL from the query and key blocks
+//   bwd_dl_kernel     (head)                dL = sum of the partials + the landmark term;
+//                                           dbias = sum over the batch of s1
+//   bwd_pool_kernel   (head, token tile)    dK += dL of the token's window / window size
+//
+// The distance derivative is sgn(x - y) with sgn(0) = 0 (Laplacian kernel) or 2 (x - y)
+// (Gaussian kernel).  Reductions run in fixed orders: results are reproducible bit for bit.
+#include "ns_common.cuh"
+
+namespace lapl {
+using namespace ns_detail;
+namespace {
+
+constexpr int kBwdTile = 128;          // tokens per staged tile (bwd_ahat, bwd_lm)
+constexpr int kBwdThreads = 256;
+constexpr int kHeadThreads = 512;
+constexpr int kMaxPairs = (kMaxM * kMaxD + kBwdThreads - 1) / kBwdThreads;   // 32
+
+template <bool kGauss>
+__device__ __forceinline__ float slope(float x, float y) {
+  if constexpr (kGauss) return 2.f * (x - y);
+  return x > y ? 1.f : (x < y ? -1.f : 0.f);
+}
+
+// Element e of a [.., d] input row in fp32 or bf16.
+__device__ __forceinline__ float load_in(const void* p, size_t e, bool bf16) {
+  if (bf16) {
+    const unsigned short u = reinterpret_cast<const unsigned short*>(p)[e];
+    return __uint_as_float((unsigned)u << 16);
+  }
+  return reinterpret_cast<const float*>(p)[e];
+}
+
+// ---- dA^ = G M^T and the partial reductions over one token split -----------------------
+__global__ void __launch_bounds__(kBwdThreads)
+bwd_ahat_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
+                const float* __restrict__ mu, const float* __restrict__ rstd,
+                const float* __restrict__ bias, const float* __restrict__ gout,
+                float* __restrict__ dahat, float* __restrict__ part_dm,
+                float* __restrict__ part_s, int m, int d, int n, int heads, int tiles_per_split,
+                int splits, int whiten) {
+  extern __shared__ float4 smem_a4[];
+  float* smem = reinterpret_cast<float*>(smem_a4);
+  const int dp = d + 1, tp = kBwdTile + 1;
+  float* sM = smem;                       // [m][d + 1]
+  float* sG = sM + m * dp;                // [tile][d + 1]
+  float* sZ = sG + kBwdTile * dp;         // [m][tile + 1]   Z (whitened, no bias) or A
+  float* sD = sZ + m * tp;                // [m][tile + 1]   dA^
+  float* sc = sD + m * tp;                // mu, r, beta [3][m]
+  const long bh = blockIdx.x / splits;
+  const int sp = blockIdx.x % splits;
+  const int h = (int)(bh % heads);
+  for (int i = threadIdx.x; i < m * d; i += kBwdThreads)
+    sM[(i / d) * dp + i % d] = mmat[(size_t)bh * m * d + i];
+  for (int j = threadIdx.x; j < m; j += kBwdThreads) {
+    sc[j] = mu[(size_t)bh * m + j];
+    sc[m + j] = rstd[(size_t)bh * m + j];
+    sc[2 * m + j] = (whiten && bias) ? bias[(size_t)h * m + j] : 0.f;
+  }
+  float s1 = 0.f, s2 = 0.f;
+  float acc[kMaxPairs];
+#pragma unroll
+  for (int u = 0; u < kMaxPairs; ++u) acc[u] = 0.f;
+  const int pairs = m * d;
+  const int t0 = sp * tiles_per_split;
+  const int tiles = (n + kBwdTile - 1) / kBwdTile;
+  const int t1 = min(tiles, t0 + tiles_per_split);
+  __syncthreads();
+  for (int t = t0; t < t1; ++t) {
+    const int n0 = t * kBwdTile;
+    for (int i = threadIdx.x; i < m * kBwdTile; i += kBwdThreads) {
+      const int j = i / kBwdTile, tt = i % kBwdTile, tok = n0 + tt;
+      float z = 0.f;
+      if (tok < n) {
+        const float a = at[((size_t)bh * m + j) * n + tok];
+        z = whiten ? (a - sc[j]) * sc[m + j] : a;
+      }
+      sZ[j * tp + tt] = z;
+    }
+    for (int i = threadIdx.x; i < kBwdTile * d; i += kBwdThreads) {
+      const int tt = i / d, c = i % d, tok = n0 + tt;
+      sG[tt * dp + c] = tok < n ? gout[((size_t)bh * n + tok) * d + c] : 0.f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < m * kBwdTile; i += kBwdThreads) {
+      const int j = i / kBwdTile, tt = i % kBwdTile, tok = n0 + tt;
+      float v = 0.f;
+      for (int c = 0; c < d; ++c) v = fmaf(sG[tt * dp + c], sM[j * dp + c], v);
+      sD[j * tp + tt] = v;
+      if (tok < n) dahat[((size_t)bh * m + j) * n + tok] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < m) {
+      const int j = threadIdx.x;
+      for (int tt = 0; tt < kBwdTile; ++tt) {
+        const float v = sD[j * tp + tt];
+        s1 += v;
+        s2 = fmaf(v, sZ[j * tp + tt], s2);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kMaxPairs; ++u) {
+      const int p = threadIdx.x + kBwdThreads * u;
+      if (p < pairs) {
+        const int j = p / d, c = p % d;
+        const float beta = sc[2 * m + j];
+        float a = acc[u];
+        for (int tt = 0; tt < kBwdTile; ++tt)
+          a = fmaf(sZ[j * tp + tt] + beta, sG[tt * dp + c], a);
+        acc[u] = a;
+      }
+    }
+    __syncthreads();
+  }
+  float* pdm = part_dm + ((size_t)bh * splits + sp) * m * d;
+#pragma unroll
+  for (int u = 0; u < kMaxPairs; ++u) {
+    const int p = threadIdx.x + kBwdThreads * u;
+    if (p < pairs) pdm[p] = acc[u];
+  }
+  if (threadIdx.x < m) {
+    float* ps = part_s + ((size_t)bh * splits + sp) * 2 * m;
+    ps[threadIdx.x] = s1;
+    ps[m + threadIdx.x] = s2;
+  }
+}
+
+// ---- per head: dM, dBV, dX, Newton-Schulz backwards, the landmark-block term of dL ----------
+// C[i][j] (i, j < M) = sum_k A(i, k) B(k, j) with A(i, k) = A[i][k] or A[k][i] (ta), likewise
+// B; row stride kMS.  Then C = alpha C_prev + beta (the product), per flags below.
+template <int M, bool kTa, bool kTb>
+__device__ __forceinline__ float mm_elem(const float* __restrict__ A, const float* __restrict__ B,
+                                         int i, int j) {
+  float s = 0.f;
+#pragma unroll 4
+  for (int k = 0; k < M; ++k) {
+    const float a = kTa ? A[k * kMS + i] : A[i * kMS + k];
+    const float b = kTb ? B[j * kMS + k] : B[k * kMS + j];
+    s = fmaf(a, b, s);
+  }
+  return s;
+}
+
+template <int S>
+__global__ void __launch_bounds__(kHeadThreads, 1)
+bwd_head_kernel(const float* __restrict__ landmarks, const float* __restrict__ xg,
+                const float* __restrict__ bvp, const float* __restrict__ part_dm,
+                const float* __restrict__ part_s, float* __restrict__ dbv,
+                float* __restrict__ dll, float* __restrict__ s12, float* __restrict__ dbias_bh,
+                float* __restrict__ xs, float* __restrict__ ps, int d, int T, float eps,
+                float c_exp, float lam, int gauss, int splits, int whiten) {
+  using Sh = NsShape<S>;
+  constexpr int M = Sh::M;
+  constexpr int MM = 64 * kMS;
+  extern __shared__ float4 smem_h4[];
+  float* smem = reinterpret_cast<float*>(smem_h4);
+  float* Wb = smem;
+  float* Xt = Wb + MM;
+  float* Pt = Xt + MM;
+  float* dX = Pt + MM;
+  float* T1 = dX + MM;
+  float* T2 = T1 + MM;
+  float* dW = T2 + MM;
+  float* red = dW + MM;                    // [kRedFloats]
+  float* R = red + kRedFloats;             // landmarks, then dM and BV ([2][m][d])
+  const long bh = blockIdx.x;
+  const int tid = threadIdx.x;
+  const size_t mm = (size_t)M * M;
+
+  NsSmem sm;
+  sm.W = Wb;
+  sm.X = Xt;
+  sm.P = nullptr;
+  sm.Y = nullptr;
+  sm.red = red;
+  sm.part = nullptr;
+  sm.sL = R;
+  ns_prologue<S, kHeadThreads>(sm, landmarks + (size_t)bh * M * d, d, eps, c_exp, gauss != 0,
+                               false, nullptr, nullptr, bh);
+  float* xsh = xs + (size_t)bh * (T + 1) * mm;
+  float* psh = ps + (size_t)bh * (T > 0 ? T : 1) * mm;
+  // Newton-Schulz again, every iterate X_t and product P_t = W X_t kept.
+  for (int t = 0;; ++t) {
+    for (int e = tid; e < M * M; e += kHeadThreads) xsh[(size_t)t * mm + e] = Xt[(e / M) * kMS + e % M];
+    if (t == T) break;
+    for (int e = tid; e < M * M; e += kHeadThreads) {
+      const int i = e / M, j = e % M;
+      const float v = mm_elem<M, false, false>(Wb, Xt, i, j);
+      Pt[i * kMS + j] = v;
+      psh[(size_t)t * mm + e] = v;
+    }
+    __syncthreads();
+    for (int e = tid; e < M * M; e += kHeadThreads) {       // X (2I - P) = 2X - X P
+      const int i = e / M, j = e % M;
+      T1[i * kMS + j] = 2.f * Xt[i * kMS + j] - mm_elem<M, false, false>(Xt, Pt, i, j);
+    }
+    __syncthreads();
+    for (int e = tid; e < M * M; e += kHeadThreads) Xt[(e / M) * kMS + e % M] = T1[(e / M) * kMS + e % M];
+    __syncthreads();
+  }
+
+  // dM and BV (split partials summed in split order), s1, s2.
+  float* sdM = R;
+  float* sBV = R + M * d;
+  for (int e = tid; e < M * d; e += kHeadThreads) {
+    float a = 0.f, b = 0.f;
+    for (int sp = 0; sp < splits; ++sp) {
+      a += part_dm[((size_t)bh * splits + sp) * M * d + e];
+      b += bvp[((size_t)bh * splits + sp) * M * d + e];
+    }
+    sdM[e] = a;
+    sBV[e] = b;
+  }
+  if (tid < M) {
+    float a = 0.f, b = 0.f;
+    for (int sp = 0; sp < splits; ++sp) {
+      a += part_s[((size_t)bh * splits + sp) * 2 * M + tid];
+      b += part_s[((size_t)bh * splits + sp) * 2 * M + M + tid];
+    }
+    s12[(size_t)bh * 2 * M + tid] = a;
+    s12[(size_t)bh * 2 * M + M + tid] = b;
+    dbias_bh[(size_t)bh * M + tid] = whiten ? a : 0.f;
+  }
+  for (int e = tid; e < MM; e += kHeadThreads) dW[e] = 0.f;
+  __syncthreads();
+  // dBV = X^T dM (the forward's X); dX = dM BV^T.
+  for (int e = tid; e < M * d; e += kHeadThreads) {
+    const int j = e / d, c = e % d;
+    float s = 0.f;
+    for (int k = 0; k < M; ++k) s = fmaf(xg[(size_t)bh * mm + (size_t)k * M + j], sdM[k * d + c], s);
+    dbv[(size_t)bh * M * d + e] = s;
+  }
+  for (int e = tid; e < M * M; e += kHeadThreads) {
+    const int i = e / M, j = e % M;
+    float s = 0.f;
+    for (int c = 0; c < d; ++c) s = fmaf(sdM[i * d + c], sBV[j * d + c], s);
+    dX[i * kMS + j] = s;
+  }
+  __syncthreads();
+
+  // Backwards through X_{t+1} = X_t (2I - P_t), P_t = W X_t:
+  //   T1 = X_t^T dX;  dW -= T1 X_t^T;  dX <- 2 dX - dX P_t^T - W^T T1.
+  for (int t = T - 1; t >= 0; --t) {
+    for (int e = tid; e < M * M; e += kHeadThreads) {
+      Xt[(e / M) * kMS + e % M] = xsh[(size_t)t * mm + e];
+      Pt[(e / M) * kMS + e % M] = psh[(size_t)t * mm + e];
+    }
+    __syncthreads();
+    for (int e = tid; e < M * M; e += kHeadThreads) {
+      const int i = e / M, j = e % M;
+      T1[i * kMS + j] = mm_elem<M, true, false>(Xt, dX, i, j);
+    }
+    __syncthreads();
+    for (int e = tid; e < M * M; e += kHeadThreads) {
+      const int i = e / M, j = e % M;
+      dW[i * kMS + j] -= mm_elem<M, false, true>(T1, Xt, i, j);
+      T2[i * kMS + j] = 2.f * dX[i * kMS + j] - mm_elem<M, false, true>(dX, Pt, i, j) -
+                        mm_elem<M, true, false>(Wb, T1, i, j);
+    }
+    __syncthreads();
+    for (int e = tid; e < M * M; e += kHeadThreads) dX[(e / M) * kMS + e % M] = T2[(e / M) * kMS + e % M];
+    __syncthreads();
+  }
+
+  // X0 = W^T / (|W|_1 |W|_inf): column sums (first maximum) and the scale's derivative.
+  if (tid < 32) {
+    const int lane = tid;
+    float best_c = -1.f, best_r = -1.f;
+    int jc = 0, ir = 0;
+    float dsc = 0.f;
+    for (int j = 0; j < M; ++j) {
+      float cs = 0.f, rs = 0.f;
+      for (int i = 0; i < M; ++i) {
+        cs += fabsf(Wb[i * kMS + j]);
+        rs += fabsf(Wb[j * kMS + i]);
+      }
+      if (cs > best_c) { best_c = cs; jc = j; }
+      if (rs > best_r) { best_r = rs; ir = j; }
+    }
+    const float scale = best_c * best_r;
+    for (int e = lane; e < M * M; e += 32) {
+      const int i = e / M, j = e % M;
+      dsc -= dX[i * kMS + j] * Wb[j * kMS + i];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dsc += __shfl_xor_sync(0xffffffffu, dsc, o);
+    dsc /= scale * scale;
+    if (lane == 0) {
+      red[0] = scale;
+      red[1] = dsc * best_r;       // d|W|_1
+      red[2] = dsc * best_c;       // d|W|_inf
+      red[3] = __int_as_float(jc);
+      red[4] = __int_as_float(ir);
+    }
+  }
+  __syncthreads();
+  {
+    const float scale = red[0], dn1 = red[1], dninf = red[2];
+    const int jc = __float_as_int(red[3]), ir = __float_as_int(red[4]);
+    for (int e = tid; e < M * M; e += kHeadThreads) {
+      const int i = e / M, j = e % M;
+      float g = dW[i * kMS + j] + dX[j * kMS + i] / scale;
+      const float w = Wb[i * kMS + j];
+      const float sw = w > 0.f ? 1.f : (w < 0.f ? -1.f : 0.f);
+      if (j == jc) g += dn1 * sw;
+      if (i == ir) g += dninf * sw;
+      // W = exp(-D_LL / lambda) + eps I: dLoss/dD_LL off the diagonal
+      T1[i * kMS + j] = (i == j) ? 0.f : -w / lam * g;
+    }
+  }
+  __syncthreads();
+  // dL_pc (landmark block) = sum_k (g[p][k] + g[k][p]) slope(L_pc, L_kc)
+  const float* Lh = landmarks + (size_t)bh * M * d;
+  for (int e = tid; e < M * d; e += kHeadThreads) {
+    const int p = e / d, c = e % d;
+    const float lp = Lh[p * d + c];
+    float s = 0.f;
+    for (int k = 0; k < M; ++k) {
+      if (k == p) continue;
+      const float g = T1[p * kMS + k] + T1[k * kMS + p];
+      const float lk = Lh[k * d + c];
+      s = fmaf(g, gauss ? 2.f * (lp - lk) : (lp > lk ? 1.f : (lp < lk ? -1.f : 0.f)), s);
+    }
+    dll[(size_t)bh * M * d + e] = s;
+  }
+}
+
+// ---- query side: g = -(A / lambda) dA, dQ ------------------------------------------------
+template <bool kGauss>
+__global__ void __launch_bounds__(512)
+bwd_query_kernel(const void* __restrict__ q, const float* __restrict__ at,
+                 const float* __restrict__ dahat, const float* __restrict__ mu,
+                 const float* __restrict__ rstd, const float* __restrict__ s12,
+                 const float* __restrict__ landmarks, float* __restrict__ gq,
+                 float* __restrict__ dq, int m, int d, int n, float lam, int whiten, int tpc,
+                 int tiles, int bf16) {
+  extern __shared__ float4 smem_q4[];
+  float* smem = reinterpret_cast<float*>(smem_q4);
+  float* sL = smem;                    // [m][d]
+  float* sg = sL + m * d;              // [m][tpc]
+  const long bh = blockIdx.x / tiles;
+  const int n0 = (blockIdx.x % tiles) * tpc;
+  for (int i = threadIdx.x; i < m * d; i += blockDim.x) sL[i] = landmarks[(size_t)bh * m * d + i];
+  const float inv_n = 1.f / (float)n;
+  for (int i = threadIdx.x; i < m * tpc; i += blockDim.x) {
+    const int j = i / tpc, tt = i % tpc, tok = n0 + tt;
+    float g = 0.f;
+    if (tok < n) {
+      const size_t o = ((size_t)bh * m + j) * n + tok;
+      const float a = at[o], dz = dahat[o];
+      float da = dz;
+      if (whiten) {
+        const float r = rstd[(size_t)bh * m + j];
+        const float z = (a - mu[(size_t)bh * m + j]) * r;
+        const float s1 = s12[(size_t)bh * 2 * m + j], s2 = s12[(size_t)bh * 2 * m + m + j];
+        da = r * (dz - s1 * inv_n - z * s2 * inv_n);
+      }
+      g = -a / lam * da;
+      gq[o] = g;
+    }
+    sg[j * tpc + tt] = g;
+  }
+  __syncthreads();
+  const int groups = d >> 3;
+  const int tt = threadIdx.x / groups, c0 = (threadIdx.x % groups) * 8, tok = n0 + tt;
+  if (tt >= tpc || tok >= n) return;
+  float x[8], acc[8];
+  const size_t row = ((size_t)bh * n + tok) * d + c0;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    x[c] = load_in(q, row + c, bf16 != 0);
+    acc[c] = 0.f;
+  }
+  for (int j = 0; j < m; ++j) {
+    const float g = sg[j * tpc + tt];
+    const float* l = sL + j * d + c0;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[c] = fmaf(g, slope<kGauss>(x[c], l[c]), acc[c]);
+  }
+  float4* out = reinterpret_cast<float4*>(dq + row);
+  out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+// ---- key side: h = -(B / lambda) (dBV V^T), dK's distance term, dV = B^T dBV --------------
+template <bool kGauss>
+__global__ void __launch_bounds__(512)
+bwd_key_kernel(const void* __restrict__ k, const void* __restrict__ v,
+               const float* __restrict__ bt, const float* __restrict__ dbv,
+               const float* __restrict__ landmarks, float* __restrict__ hk,
+               float* __restrict__ dk, float* __restrict__ dv, int m, int d, int n, float lam,
+               int tpc, int tiles, int bf16) {
+  extern __shared__ float4 smem_k4[];
+  float* smem = reinterpret_cast<float*>(smem_k4);
+  const int dp = d + 1;
+  float* sL = smem;                    // [m][d]
+  float* sdBV = sL + m * d;            // [m][d]
+  float* sV = sdBV + m * d;            // [tpc][d + 1]
+  float* sh = sV + tpc * dp;           // [m][tpc]
+  float* sB = sh + m * tpc;            // [m][tpc]
+  const long bh = blockIdx.x / tiles;
+  const int n0 = (blockIdx.x % tiles) * tpc;
+  for (int i = threadIdx.x; i < m * d; i += blockDim.x) {
+    sL[i] = landmarks[(size_t)bh * m * d + i];
+    sdBV[i] = dbv[(size_t)bh * m * d + i];
+  }
+  for (int i = threadIdx.x; i < tpc * d; i += blockDim.x) {
+    const int tt = i / d, c = i % d, tok = n0 + tt;
+    sV[tt * dp + c] = tok < n ? load_in(v, ((size_t)bh * n + tok) * d + c, bf16 != 0) : 0.f;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < m * tpc; i += blockDim.x) {
+    const int j = i / tpc, tt = i % tpc, tok = n0 + tt;
+    float h = 0.f, b = 0.f;
+    if (tok < n) {
+      const size_t o = ((size_t)bh * m + j) * n + tok;
+      b = bt[o];
+      float db = 0.f;
+      for (int c = 0; c < d; ++c) db = fmaf(sdBV[j * d + c], sV[tt * dp + c], db);
+      h = -b / lam * db;
+      hk[o] = h;
+    }
+    sh[j * tpc + tt] = h;
+    sB[j * tpc + tt] = b;
+  }
+  __syncthreads();
+  const int groups = d >> 3;
+  const int tt = threadIdx.x / groups, c0 = (threadIdx.x % groups) * 8, tok = n0 + tt;
+  if (tt >= tpc || tok >= n) return;
+  float x[8], gk[8], gv[8];
+  const size_t row = ((size_t)bh * n + tok) * d + c0;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    x[c] = load_in(k, row + c, bf16 != 0);
+    gk[c] = 0.f;
+    gv[c] = 0.f;
+  }
+  for (int j = 0; j < m; ++j) {
+    const float h = sh[j * tpc + tt], b = sB[j * tpc + tt];
+    const float* l = sL + j * d + c0;
+    const float* w = sdBV + j * d + c0;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      gk[c] = fmaf(-h, slope<kGauss>(l[c], x[c]), gk[c]);
+      gv[c] = fmaf(b, w[c], gv[c]);
+    }
+  }
+  float4* ok = reinterpret_cast<float4*>(dk + row);
+  ok[0] = make_float4(gk[0], gk[1], gk[2], gk[3]);
+  ok[1] = make_float4(gk[4], gk[5], gk[6], gk[7]);
+  float4* ov = reinterpret_cast<float4*>(dv + row);
+  ov[0] = make_float4(gv[0], gv[1], gv[2], gv[3]);
+  ov[1] = make_float4(gv[4], gv[5], gv[6], gv[7]);
+}
+
+// ---- partials of dL over one token split: side 0 from the query block, 1 from the key block --
+template <bool kGauss>
+__global__ void __launch_bounds__(kBwdThreads)
+bwd_lm_kernel(const void* __restrict__ q, const void* __restrict__ k,
+              const float* __restrict__ gq, const float* __restrict__ hk,
+              const float* __restrict__ landmarks, float* __restrict__ part_dl, int m, int d,
+              int n, int tiles_per_split, int splits, int bf16) {
+  extern __shared__ float4 smem_l4[];
+  float* smem = reinterpret_cast<float*>(smem_l4);
+  const int dp = d + 1, tp = kBwdTile + 1;
+  float* sX = smem;                      // [tile][d + 1]
+  float* sw = sX + kBwdTile * dp;        // [m][tile + 1]
+  const int side = blockIdx.x & 1;
+  const long rest = blockIdx.x >> 1;
+  const long bh = rest / splits;
+  const int sp = (int)(rest % splits);
+  const void* x = side == 0 ? q : k;
+  const float* wgt = side == 0 ? gq : hk;
+  const float* Lh = landmarks + (size_t)bh * m * d;
+  const int pairs = m * d;
+  float acc[kMaxPairs], lv[kMaxPairs];
+#pragma unroll
+  for (int u = 0; u < kMaxPairs; ++u) {
+    const int p = threadIdx.x + kBwdThreads * u;
+    acc[u] = 0.f;
+    lv[u] = p < pairs ? Lh[p] : 0.f;
+  }
+  const int tiles = (n + kBwdTile - 1) / kBwdTile;
+  const int t0 = sp * tiles_per_split, t1 = min(tiles, t0 + tiles_per_split);
+  for (int t = t0; t < t1; ++t) {
+    const int n0 = t * kBwdTile;
+    for (int i = threadIdx.x; i < kBwdTile * d; i += kBwdThreads) {
+      const int tt = i / d, c = i % d, tok = n0 + tt;
+      sX[tt * dp + c] = tok < n ? load_in(x, ((size_t)bh * n + tok) * d + c, bf16 != 0) : 0.f;
+    }
+    for (int i = threadIdx.x; i < m * kBwdTile; i += kBwdThreads) {
+      const int j = i / kBwdTile, tt = i % kBwdTile, tok = n0 + tt;
+      sw[j * tp + tt] = tok < n ? wgt[((size_t)bh * m + j) * n + tok] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kMaxPairs; ++u) {
+      const int p = threadIdx.x + kBwdThreads * u;
+      if (p < pairs) {
+        const int j = p / d, c = p % d;
+        const float l = lv[u];
+        float a = acc[u];
+        if (side == 0) {
+          for (int tt = 0; tt < kBwdTile; ++tt)
+            a = fmaf(-sw[j * tp + tt], slope<kGauss>(sX[tt * dp + c], l), a);
+        } else {
+          for (int tt = 0; tt < kBwdTile; ++tt)
+            a = fmaf(sw[j * tp + tt], slope<kGauss>(l, sX[tt * dp + c]), a);
+        }
+        acc[u] = a;
+      }
+    }
+    __syncthreads();
+  }
+  float* out = part_dl + (((size_t)bh * 2 + side) * splits + sp) * m * d;
+#pragma unroll
+  for (int u = 0; u < kMaxPairs; ++u) {
+    const int p = threadIdx.x + kBwdThreads * u;
+    if (p < pairs) out[p] = acc[u];
+  }
+}
+
+// ---- dL per head; dbias = sum over the batch ----------------------------------------------
+__global__ void __launch_bounds__(kBwdThreads)
+bwd_dl_kernel(const float* __restrict__ part_dl, const float* __restrict__ dll,
+              const float* __restrict__ dbias_bh, float* __restrict__ dl,
+              float* __restrict__ dbias, int m, int d, int splits, int batch, int heads) {
+  const long bh = blockIdx.x;
+  for (int e = threadIdx.x; e < m * d; e += kBwdThreads) {
+    float s = 0.f;
+    for (int side = 0; side < 2; ++side)
+      for (int sp = 0; sp < splits; ++sp)
+        s += part_dl[(((size_t)bh * 2 + side) * splits + sp) * m * d + e];
+    dl[(size_t)bh * m * d + e] = s + dll[(size_t)bh * m * d + e];
+  }
+  if (dbias && bh < heads) {              // batch 0's CTAs: head h = bh sums over the batch
+    for (int j = threadIdx.x; j < m; j += kBwdThreads) {
+      float s = 0.f;
+      for (int b = 0; b < batch; ++b) s += dbias_bh[((size_t)b * heads + bh) * m + j];
+      dbias[(size_t)bh * m + j] = s;
+    }
+  }
+}
+
+// ---- pooling backward: dK_n += dL_{window(n)} / (ph pw) ----------------------------------
+__global__ void __launch_bounds__(kBwdThreads)
+bwd_pool_kernel(const float* __restrict__ dl, float* __restrict__ dk, int m, int d, int n,
+                int grid_w, int s, int ph, int pw, int tiles) {
+  const long bh = blockIdx.x / tiles;
+  const int n0 = (blockIdx.x % tiles) * kBwdTile;
+  const float inv = 1.f / (float)(ph * pw);
+  for (int i = threadIdx.x; i < kBwdTile * d; i += kBwdThreads) {
+    const int tt = i / d, c = i % d, tok = n0 + tt;
+    if (tok >= n) continue;
+    const int r = tok / grid_w, col = tok % grid_w;
+    const int j = (r / ph) * s + col / pw;
+    dk[((size_t)bh * n + tok) * d + c] += dl[((size_t)bh * m + j) * d + c] * inv;
+  }
+}
+
+template <int S>
+const void* head_ptr() { return reinterpret_cast<const void*>(&bwd_head_kernel<S>); }
+
+const void* pick_head(int s) {
+  switch (s) {
+    case 1: return head_ptr<1>();
+    case 2: return head_ptr<2>();
+    case 3: return head_ptr<3>();
+    case 4: return head_ptr<4>();
+    case 5: return head_ptr<5>();
+    case 6: return head_ptr<6>();
+    case 7: return head_ptr<7>();
+    case 8: return head_ptr<8>();
+    default: return nullptr;
+  }
+}
+
+int token_tile(int d) {
+  const int groups = d / 8;
+  int t = 512 / groups;
+  return t > kBwdTile ? kBwdTile : t;
+}
+
+size_t ahat_smem(int m, int d) {
+  return sizeof(float) * ((size_t)m * (d + 1) + (size_t)kBwdTile * (d + 1) +
+                          2 * (size_t)m * (kBwdTile + 1) + 3 * (size_t)m);
+}
+size_t head_smem(int m, int d) {
+  const size_t region = 64 * (size_t)d > 2 * (size_t)m * d ? 64 * (size_t)d : 2 * (size_t)m * d;
+  return sizeof(float) * (7 * 64 * (size_t)kMS + kRedFloats + region);
+}
+size_t query_smem(int m, int d, int tpc) { return sizeof(float) * ((size_t)m * d + (size_t)m * tpc); }
+size_t key_smem(int m, int d, int tpc) {
+  return sizeof(float) * (2 * (size_t)m * d + (size_t)tpc * (d + 1) + 2 * (size_t)m * tpc);
+}
+size_t lm_smem(int m, int d) {
+  return sizeof(float) * ((size_t)kBwdTile * (d + 1) + (size_t)m * (kBwdTile + 1));
+}
+
+}  // namespace
+
+BwdLayout bwd_layout(const lapl_attn_plan& p) {
+  const Geometry& g = p.geo;
+  const size_t bh = (size_t)g.bh, m = g.m, d = g.d, n = g.n, sp = g.bv_splits;
+  const size_t T = (size_t)p.cfg.ns_steps;
+  BwdLayout L;
+  size_t off = 0;
+  auto take = [&](size_t floats) {
+    const size_t at = off;
+    off = align_up(off + floats * sizeof(float), kAlign);
+    return at;
+  };
+  L.dahat = take(bh * m * n);
+  L.part_dm = take(bh * sp * m * d);
+  L.part_s = take(bh * sp * 2 * m);
+  L.s12 = take(bh * 2 * m);
+  L.dbv = take(bh * m * d);
+  L.dll = take(bh * m * d);
+  L.dbias_bh = take(bh * m);
+  L.xs = take(bh * (T + 1) * m * m);
+  L.ps = take(bh * (T > 0 ? T : 1) * m * m);
+  L.gq = take(bh * m * n);
+  L.hk = take(bh * m * n);
+  L.part_dl = take(bh * 2 * sp * m * d);
+  L.dl = take(bh * m * d);
+  L.total = off;
+  return L;
+}
+
+cudaError_t bwd_configure(const lapl_attn_plan& p) {
+  const Geometry& g = p.geo;
+  const int tpc = token_tile(g.d);
+  cudaError_t e = cudaFuncSetAttribute(bwd_ahat_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)ahat_smem(g.m, g.d));
+  const void* hf = pick_head(g.s);
+  if (!hf) return cudaErrorInvalidValue;
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(hf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)head_smem(g.m, g.d));
+  const int qs = (int)query_smem(g.m, g.d, tpc), ks = (int)key_smem(g.m, g.d, tpc),
+            ls = (int)lm_smem(g.m, g.d);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_query_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, qs);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_query_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, qs);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_key_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, ks);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_key_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, ks);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_lm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, ls);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_lm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, ls);
+  return e;
+}
+
+cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* k, const void* v,
+                            const float* bias, const float* gout, float* dq, float* dk,
+                            float* dv, float* dbias, const char* fws, char* bws,
+                            cudaStream_t st) {
+  const Geometry& g = p.geo;
+  const WorkspaceLayout& F = p.ws;
+  const BwdLayout B = bwd_layout(p);
+  const int m = g.m, d = g.d, n = g.n, splits = g.bv_splits, tps = g.bv_tiles_per_split;
+  const int heads = p.cfg.heads, whiten = p.cfg.whiten, bf16 = p.cfg.in_dtype == LAPL_BF16;
+  const bool gauss = p.cfg.kernel == LAPL_KERNEL_GAUSSIAN;
+  const float lam = p.cfg.lambda;
+  const float* L = reinterpret_cast<const float*>(fws + F.landmarks);
+  const float* X = reinterpret_cast<const float*>(fws + F.x);
+  const float* At = reinterpret_cast<const float*>(fws + F.at);
+  const float* Bt = reinterpret_cast<const float*>(fws + F.bt);
+  const float* bvp = reinterpret_cast<const float*>(fws + F.bvp);
+  const float* M = reinterpret_cast<const float*>(fws + F.mmat);
+  const float* mu = reinterpret_cast<const float*>(fws + F.mu);
+  const float* rstd = reinterpret_cast<const float*>(fws + F.rstd);
+  auto W = [&](size_t off) { return reinterpret_cast<float*>(bws + off); };
+  float *dahat = W(B.dahat), *part_dm = W(B.part_dm), *part_s = W(B.part_s), *s12 = W(B.s12),
+        *dbv = W(B.dbv), *dll = W(B.dll), *dbias_bh = W(B.dbias_bh), *xs = W(B.xs),
+        *ps = W(B.ps), *gq = W(B.gq), *hk = W(B.hk), *part_dl = W(B.part_dl), *dl = W(B.dl);
+  const unsigned bh = (unsigned)g.bh;
+  const int tpc = token_tile(d);
+  const int qtiles = (n + tpc - 1) / tpc;
+  const int ptiles = (n + kBwdTile - 1) / kBwdTile;
+
+  bwd_ahat_kernel<<<bh * splits, kBwdThreads, ahat_smem(m, d), st>>>(
+      At, M, mu, rstd, bias, gout, dahat, part_dm, part_s, m, d, n, heads, tps, splits, whiten);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  {
+    const void* f = pick_head(g.s);
+    int T = p.cfg.ns_steps, gs = gauss, sp = splits, wh = whiten;
+    float eps = p.cfg.eps, c_exp = p.neg_log2e_over_lambda, lm = lam;
+    int dd = d;
+    void* args[] = {&L, &X, &bvp, &part_dm, &part_s, &dbv, &dll, &s12, &dbias_bh, &xs, &ps,
+                    &dd, &T, &eps, &c_exp, &lm, &gs, &sp, &wh};
+    e = cudaLaunchKernel(f, dim3(bh), dim3(kHeadThreads), args, head_smem(m, d), st);
+    if (e != cudaSuccess) return e;
+  }
+  const unsigned tthreads = (unsigned)(tpc * (d / 8));
+  if (gauss) {
+    bwd_query_kernel<true><<<bh * qtiles, tthreads, query_smem(m, d, tpc), st>>>(
+        q, At, dahat, mu, rstd, s12, L, gq, dq, m, d, n, lam, whiten, tpc, qtiles, bf16);
+    bwd_key_kernel<true><<<bh * qtiles, tthreads, key_smem(m, d, tpc), st>>>(
+        k, v, Bt, dbv, L, hk, dk, dv, m, d, n, lam, tpc, qtiles, bf16);
+    bwd_lm_kernel<true><<<bh * splits * 2, kBwdThreads, lm_smem(m, d), st>>>(
+        q, k, gq, hk, L, part_dl, m, d, n, tps, splits, bf16);
+  } else {
+    bwd_query_kernel<false><<<bh * qtiles, tthreads, query_smem(m, d, tpc), st>>>(
+        q, At, dahat, mu, rstd, s12, L, gq, dq, m, d, n, lam, whiten, tpc, qtiles, bf16);
+    bwd_key_kernel<false><<<bh * qtiles, tthreads, key_smem(m, d, tpc), st>>>(
+        k, v, Bt, dbv, L, hk, dk, dv, m, d, n, lam, tpc, qtiles, bf16);
+    bwd_lm_kernel<false><<<bh * splits * 2, kBwdThreads, lm_smem(m, d), st>>>(
+        q, k, gq, hk, L, part_dl, m, d, n, tps, splits, bf16);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_dl_kernel<<<bh, kBwdThreads, 0, st>>>(part_dl, dll, dbias_bh, dl, dbias, m, d, splits,
+                                             p.cfg.batch, heads);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int s = g.s;
+  bwd_pool_kernel<<<bh * ptiles, kBwdThreads, 0, st>>>(dl, dk, m, d, n, p.cfg.grid_w, s,
+                                                        p.cfg.grid_h / s, p.cfg.grid_w / s, ptiles);
+  return cudaGetLastError();
+}
+
+}  // namespace lapl

@@ -58,6 +58,24 @@ struct WorkspaceLayout {
   size_t total;
 };
 
+// Offsets (bytes) of the backward pass's own workspace regions.  All fp32.
+struct BwdLayout {
+  size_t dahat;      // [BH, m, N]          dLoss/dA^ (landmark-major)
+  size_t part_dm;    // [BH, splits, m, d]  partial dM = A^T G
+  size_t part_s;     // [BH, splits, 2, m]  partial column sums of dA^ and dA^ Z
+  size_t s12;        // [BH, 2, m]          the sums
+  size_t dbv;        // [BH, m, d]          dLoss/d(B V)
+  size_t dll;        // [BH, m, d]          the landmark block's term of dL
+  size_t dbias_bh;   // [BH, m]             per-slice bias gradient
+  size_t xs;         // [BH, T + 1, m, m]   Newton-Schulz iterates
+  size_t ps;         // [BH, max(T, 1), m, m]  products W X_t
+  size_t gq;         // [BH, m, N]          dLoss/dD_QL
+  size_t hk;         // [BH, m, N]          dLoss/dD_LK
+  size_t part_dl;    // [BH, 2, splits, m, d]  partial dL (query side, key side)
+  size_t dl;         // [BH, m, d]          dLoss/dL
+  size_t total;
+};
+
 // Launch geometry decided once per plan.
 struct Geometry {
   int s, m, d, n;          // landmark grid side, landmarks, head dim, tokens per head
@@ -156,6 +174,13 @@ int bv_tile_tokens();
 cudaError_t bv_configure(size_t smem);
 size_t mix_smem_bytes(int m, int bv_splits);
 cudaError_t mix_configure(size_t smem);
+// Backward pass (backward.cu).
+BwdLayout bwd_layout(const lapl_attn_plan& p);
+cudaError_t bwd_configure(const lapl_attn_plan& p);
+cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* k, const void* v,
+                            const float* bias, const float* gout, float* dq, float* dk,
+                            float* dv, float* dbias, const char* fws, char* bws,
+                            cudaStream_t st);
 // Conjugate-gradient solver: M = T CG iterations on W M = B V (replaces Newton-Schulz + mix).
 size_t cg_smem_bytes(int m, int d);
 cudaError_t cg_configure(int s, int d, size_t smem);
