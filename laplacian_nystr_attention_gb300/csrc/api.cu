@@ -259,6 +259,7 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   };
   w.landmarks = take(bh * m * d);
   w.x = take(bh * m * m);
+  w.xs = take(g.cg ? 0 : bh * ((size_t)cfg->ns_steps + 1) * m * m);
   w.at = take(bh * m * n);
   w.bt = take(bh * m * n);
   w.bvp = take(bh * g.bv_splits * m * d);
@@ -312,6 +313,7 @@ static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k,
   char* ws = static_cast<char*>(workspace);
   float* L = reinterpret_cast<float*>(ws + p->ws.landmarks);
   float* X = reinterpret_cast<float*>(ws + p->ws.x);
+  float* Xs = reinterpret_cast<float*>(ws + p->ws.xs);
   float* At = reinterpret_cast<float*>(ws + p->ws.at);
   float* Bt = reinterpret_cast<float*>(ws + p->ws.bt);
   float* mu = reinterpret_cast<float*>(ws + p->ws.mu);
@@ -338,8 +340,8 @@ static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k,
 
   cudaStream_t side = p->side_stream;
   auto launch_solve = [&](cudaStream_t s) {
-    return p->geo.ns_tc ? launch_ns_tc(*p, L, X, D.d_ll, D.w, D.x, s)
-                        : launch_ns(*p, L, X, D.d_ll, D.w, D.x, s);
+    return p->geo.ns_tc ? launch_ns_tc(*p, L, X, D.d_ll, D.w, D.x, Xs, s)
+                        : launch_ns(*p, L, X, D.d_ll, D.w, D.x, Xs, s);
   };
   LAPL_MARK(kMarkStart, st);
   if (p->geo.cg) {

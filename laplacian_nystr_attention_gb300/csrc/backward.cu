@@ -8,9 +8,10 @@
 //
 //   bwd_ahat_kernel   (head, token split)   dA^ = G M^T (stored), partials of dM = A^T G and
 //                                           of the column sums s1 = sum dA^, s2 = sum dA^ Z
-//   bwd_head_kernel   (head)                dM, dBV = X^T dM, dX = dM BV^T; Newton-Schulz
-//                                           recomputed with every iterate kept, then run
-//                                           backwards to dW; the landmark-block term of dL
+//   bwd_mid_kernel    (head)                dM, dBV = X^T dM, S_T = sym(dM BV^T), the sums
+//   bwd_ns_kernel     (head; side stream)   the Newton-Schulz steps backwards through the
+//                                           forward's saved iterates to dW; the landmark-
+//                                           block term of dL
 //   bwd_query_kernel  (head, token tile)    g = dLoss/dD_QL = -(A / lambda) dA (stored) with
 //                                           dA from the whitening backward; dQ
 //   bwd_key_kernel    (head, token tile)    h = dLoss/dD_LK = -(B / lambda) (dBV V^T) (stored);
@@ -142,51 +143,111 @@ bwd_ahat_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
   }
 }
 
-// ---- per head: dM, dBV, dX, Newton-Schulz backwards, the landmark-block term of dL ----------
-// C[i][j] (i, j < M) = sum_k A(i, k) B(k, j) with A(i, k) = A[i][k] or A[k][i] (ta), likewise
-// B; row stride kMS.  Then C = alpha C_prev + beta (the product), per flags below.
-template <int M, bool kTa, bool kTb>
-__device__ __forceinline__ float mm_elem(const float* __restrict__ A, const float* __restrict__ B,
-                                         int i, int j) {
-  float s = 0.f;
-#pragma unroll 4
-  for (int k = 0; k < M; ++k) {
-    const float a = kTa ? A[k * kMS + i] : A[i * kMS + k];
-    const float b = kTb ? B[j * kMS + k] : B[k * kMS + j];
-    s = fmaf(a, b, s);
+// ---- per head: dM, dBV = X^T dM, S_T = sym(dM BV^T), the whitening sums ------------------
+__global__ void __launch_bounds__(kBwdThreads)
+bwd_mid_kernel(const float* __restrict__ xs, const float* __restrict__ bvp,
+               const float* __restrict__ part_dm, const float* __restrict__ part_s,
+               float* __restrict__ dbv, float* __restrict__ st, float* __restrict__ s12,
+               float* __restrict__ dbias_bh, int m, int d, int T, int splits, int whiten) {
+  extern __shared__ float4 smem_m4[];
+  float* smem = reinterpret_cast<float*>(smem_m4);
+  const int dp = d + 1;               // padded rows: threads of a warp read different rows
+  float* sdM = smem;                  // [m][d + 1]
+  float* sBV = sdM + m * dp;          // [m][d + 1]
+  float* sX = sBV + m * dp;           // [m][m]  X_T
+  const long bh = blockIdx.x;
+  const int tid = threadIdx.x;
+  const size_t mm = (size_t)m * m;
+  for (int e = tid; e < m * d; e += kBwdThreads) {
+    float a = 0.f, b = 0.f;
+    const float* pa = part_dm + (size_t)bh * splits * m * d + e;
+    const float* pb = bvp + (size_t)bh * splits * m * d + e;
+#pragma unroll 8
+    for (int sp = 0; sp < splits; ++sp) {
+      a += pa[(size_t)sp * m * d];
+      b += pb[(size_t)sp * m * d];
+    }
+    sdM[(e / d) * dp + e % d] = a;
+    sBV[(e / d) * dp + e % d] = b;
   }
-  return s;
+  for (int e = tid; e < m * m; e += kBwdThreads) sX[e] = xs[((size_t)bh * (T + 1) + T) * mm + e];
+  if (tid < m) {
+    float a = 0.f, b = 0.f;
+    for (int sp = 0; sp < splits; ++sp) {
+      a += part_s[((size_t)bh * splits + sp) * 2 * m + tid];
+      b += part_s[((size_t)bh * splits + sp) * 2 * m + m + tid];
+    }
+    s12[(size_t)bh * 2 * m + tid] = a;
+    s12[(size_t)bh * 2 * m + m + tid] = b;
+    dbias_bh[(size_t)bh * m + tid] = whiten ? a : 0.f;
+  }
+  __syncthreads();
+  for (int e = tid; e < m * d; e += kBwdThreads) {
+    const int j = e / d, c = e % d;
+    float s = 0.f;
+    for (int k = 0; k < m; ++k) s = fmaf(sX[k * m + j], sdM[k * dp + c], s);
+    dbv[(size_t)bh * m * d + e] = s;
+  }
+  // (i, j) and (j, i) add the same two dot products: S_T is exactly symmetric.
+  for (int e = tid; e < m * m; e += kBwdThreads) {
+    const int i = e / m, j = e % m;
+    float a = 0.f, b = 0.f;
+    for (int c = 0; c < d; ++c) {
+      a = fmaf(sdM[i * dp + c], sBV[j * dp + c], a);
+      b = fmaf(sdM[j * dp + c], sBV[i * dp + c], b);
+    }
+    st[(size_t)bh * mm + e] = 0.5f * (a + b);
+  }
 }
 
+// ---- per head: the Newton-Schulz steps backwards, the landmark-block term of dL ------------
+// Only the symmetric part of dLoss/dW matters (W and D_LL are symmetric, and dL takes
+// dW + dW^T), and X_t, W are exactly symmetric, so the reverse iteration carries
+// S_t = sym(dLoss/dX_t):
+//   S_t = 2 S - W X_t S - (W X_t S)^T;  dW -= X_t S_{t+1} X_t,
+// three 64 x 64 products per step (U = X_t S and its transpose, W U, X_t U^T) on the tiled
+// CUDA-core product of the Newton-Schulz kernels.  The iterates X_t are the ones the forward
+// saved; X_{t-1} is copied in (cp.async) while step t's products run.  This kernel runs on
+// the side stream, next to the token kernels that do not need its result.
 template <int S>
 __global__ void __launch_bounds__(kHeadThreads, 1)
-bwd_head_kernel(const float* __restrict__ landmarks, const float* __restrict__ xg,
-                const float* __restrict__ bvp, const float* __restrict__ part_dm,
-                const float* __restrict__ part_s, float* __restrict__ dbv,
-                float* __restrict__ dll, float* __restrict__ s12, float* __restrict__ dbias_bh,
-                float* __restrict__ xs, float* __restrict__ ps, int d, int T, float eps,
-                float c_exp, float lam, int gauss, int splits, int whiten) {
+bwd_ns_kernel(const float* __restrict__ landmarks, const float* __restrict__ xs,
+              const float* __restrict__ st, float* __restrict__ dll, int d, int T, float eps,
+              float c_exp, float lam, int gauss) {
   using Sh = NsShape<S>;
-  constexpr int M = Sh::M;
+  constexpr int M = Sh::M, MK = Sh::MK, NWT = Sh::NWT;
   constexpr int MM = 64 * kMS;
   extern __shared__ float4 smem_h4[];
   float* smem = reinterpret_cast<float*>(smem_h4);
   float* Wb = smem;
-  float* Xt = Wb + MM;
-  float* Pt = Xt + MM;
-  float* dX = Pt + MM;
-  float* T1 = dX + MM;
-  float* T2 = T1 + MM;
-  float* dW = T2 + MM;
-  float* red = dW + MM;                    // [kRedFloats]
-  float* R = red + kRedFloats;             // landmarks, then dM and BV ([2][m][d])
+  float* Xb[2] = {Wb + MM, Wb + 2 * MM};
+  float* Sb = Wb + 3 * MM;
+  float* Sn = Wb + 4 * MM;
+  float* U = Wb + 5 * MM;
+  float* Ut = Wb + 6 * MM;
+  float* dW = Wb + 7 * MM;
+  float* part = Wb + 8 * MM;               // [Sh::PART_FLOATS]
+  float* red = part + Sh::PART_FLOATS;     // [kRedFloats]
+  float* R = red + kRedFloats;             // landmarks (prologue)
   const long bh = blockIdx.x;
   const int tid = threadIdx.x;
   const size_t mm = (size_t)M * M;
+  for (int e = tid; e < 7 * MM; e += kHeadThreads) Xb[0][e] = 0.f;   // zero padding
+  __syncthreads();
+  const float* xsh = xs + (size_t)bh * (T + 1) * mm;
+  auto fetch = [&](int t, float* dst) {
+    for (int e = tid; e < M * M; e += kHeadThreads) {
+      const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(&dst[(e / M) * kMS + e % M]));
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(a), "l"(xsh + (size_t)t * mm + e)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  };
+  if (T > 0) fetch(T - 1, Xb[0]);
 
   NsSmem sm;
   sm.W = Wb;
-  sm.X = Xt;
+  sm.X = U;                                // X0 of the prologue: not used
   sm.P = nullptr;
   sm.Y = nullptr;
   sm.red = red;
@@ -194,97 +255,29 @@ bwd_head_kernel(const float* __restrict__ landmarks, const float* __restrict__ x
   sm.sL = R;
   ns_prologue<S, kHeadThreads>(sm, landmarks + (size_t)bh * M * d, d, eps, c_exp, gauss != 0,
                                false, nullptr, nullptr, bh);
-  float* xsh = xs + (size_t)bh * (T + 1) * mm;
-  float* psh = ps + (size_t)bh * (T > 0 ? T : 1) * mm;
-  // Newton-Schulz again, every iterate X_t and product P_t = W X_t kept.
-  for (int t = 0;; ++t) {
-    for (int e = tid; e < M * M; e += kHeadThreads) xsh[(size_t)t * mm + e] = Xt[(e / M) * kMS + e % M];
-    if (t == T) break;
-    for (int e = tid; e < M * M; e += kHeadThreads) {
-      const int i = e / M, j = e % M;
-      const float v = mm_elem<M, false, false>(Wb, Xt, i, j);
-      Pt[i * kMS + j] = v;
-      psh[(size_t)t * mm + e] = v;
-    }
-    __syncthreads();
-    for (int e = tid; e < M * M; e += kHeadThreads) {       // X (2I - P) = 2X - X P
-      const int i = e / M, j = e % M;
-      T1[i * kMS + j] = 2.f * Xt[i * kMS + j] - mm_elem<M, false, false>(Xt, Pt, i, j);
-    }
-    __syncthreads();
-    for (int e = tid; e < M * M; e += kHeadThreads) Xt[(e / M) * kMS + e % M] = T1[(e / M) * kMS + e % M];
-    __syncthreads();
-  }
+  for (int e = tid; e < MM; e += kHeadThreads) U[e] = 0.f;
+  for (int e = tid; e < M * M; e += kHeadThreads) Sb[(e / M) * kMS + e % M] = st[(size_t)bh * mm + e];
 
-  // dM and BV (split partials summed in split order), s1, s2.
-  float* sdM = R;
-  float* sBV = R + M * d;
-  for (int e = tid; e < M * d; e += kHeadThreads) {
-    float a = 0.f, b = 0.f;
-    for (int sp = 0; sp < splits; ++sp) {
-      a += part_dm[((size_t)bh * splits + sp) * M * d + e];
-      b += bvp[((size_t)bh * splits + sp) * M * d + e];
-    }
-    sdM[e] = a;
-    sBV[e] = b;
-  }
-  if (tid < M) {
-    float a = 0.f, b = 0.f;
-    for (int sp = 0; sp < splits; ++sp) {
-      a += part_s[((size_t)bh * splits + sp) * 2 * M + tid];
-      b += part_s[((size_t)bh * splits + sp) * 2 * M + M + tid];
-    }
-    s12[(size_t)bh * 2 * M + tid] = a;
-    s12[(size_t)bh * 2 * M + M + tid] = b;
-    dbias_bh[(size_t)bh * M + tid] = whiten ? a : 0.f;
-  }
-  for (int e = tid; e < MM; e += kHeadThreads) dW[e] = 0.f;
-  __syncthreads();
-  // dBV = X^T dM (the forward's X); dX = dM BV^T.
-  for (int e = tid; e < M * d; e += kHeadThreads) {
-    const int j = e / d, c = e % d;
-    float s = 0.f;
-    for (int k = 0; k < M; ++k) s = fmaf(xg[(size_t)bh * mm + (size_t)k * M + j], sdM[k * d + c], s);
-    dbv[(size_t)bh * M * d + e] = s;
-  }
-  for (int e = tid; e < M * M; e += kHeadThreads) {
-    const int i = e / M, j = e % M;
-    float s = 0.f;
-    for (int c = 0; c < d; ++c) s = fmaf(sdM[i * d + c], sBV[j * d + c], s);
-    dX[i * kMS + j] = s;
-  }
-  __syncthreads();
-
-  // Backwards through X_{t+1} = X_t (2I - P_t), P_t = W X_t:
-  //   T1 = X_t^T dX;  dW -= T1 X_t^T;  dX <- 2 dX - dX P_t^T - W^T T1.
+  int cur = 0;
   for (int t = T - 1; t >= 0; --t) {
-    for (int e = tid; e < M * M; e += kHeadThreads) {
-      Xt[(e / M) * kMS + e % M] = xsh[(size_t)t * mm + e];
-      Pt[(e / M) * kMS + e % M] = psh[(size_t)t * mm + e];
-    }
-    __syncthreads();
-    for (int e = tid; e < M * M; e += kHeadThreads) {
-      const int i = e / M, j = e % M;
-      T1[i * kMS + j] = mm_elem<M, true, false>(Xt, dX, i, j);
-    }
-    __syncthreads();
-    for (int e = tid; e < M * M; e += kHeadThreads) {
-      const int i = e / M, j = e % M;
-      dW[i * kMS + j] -= mm_elem<M, false, true>(T1, Xt, i, j);
-      T2[i * kMS + j] = 2.f * dX[i * kMS + j] - mm_elem<M, false, true>(dX, Pt, i, j) -
-                        mm_elem<M, true, false>(Wb, T1, i, j);
-    }
-    __syncthreads();
-    for (int e = tid; e < M * M; e += kHeadThreads) dX[(e / M) * kMS + e % M] = T2[(e / M) * kMS + e % M];
-    __syncthreads();
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+    __syncthreads();                                                  // X_t in Xb[cur]
+    if (t > 0) fetch(t - 1, Xb[cur ^ 1]);
+    const float* Xt = Xb[cur];
+    sym_product<MK, NWT, kPlain>(Xt, Sb, nullptr, U, part, Ut);      // U = X_t S, Ut = U^T
+    sym_product<MK, NWT, kSymRecur>(Wb, U, Sb, Sn, part);            // 2S - W U - (W U)^T
+    sym_product<MK, NWT, kSubtract>(Xt, Ut, nullptr, dW, part);      // dW -= X_t S X_t
+    float* tmp = Sb; Sb = Sn; Sn = tmp;
+    cur ^= 1;
   }
+  __syncthreads();
 
-  // X0 = W^T / (|W|_1 |W|_inf): column sums (first maximum) and the scale's derivative.
+  // X0 = W^T / (|W|_1 |W|_inf): the symmetric part of dX0^T / scale, and the scale's
+  // derivative through the first maximal column (row) sum.
   if (tid < 32) {
     const int lane = tid;
     float best_c = -1.f, best_r = -1.f;
     int jc = 0, ir = 0;
-    float dsc = 0.f;
     for (int j = 0; j < M; ++j) {
       float cs = 0.f, rs = 0.f;
       for (int i = 0; i < M; ++i) {
@@ -295,10 +288,8 @@ bwd_head_kernel(const float* __restrict__ landmarks, const float* __restrict__ x
       if (rs > best_r) { best_r = rs; ir = j; }
     }
     const float scale = best_c * best_r;
-    for (int e = lane; e < M * M; e += 32) {
-      const int i = e / M, j = e % M;
-      dsc -= dX[i * kMS + j] * Wb[j * kMS + i];
-    }
+    float dsc = 0.f;
+    for (int e = lane; e < M * M; e += 32) dsc -= Sb[(e / M) * kMS + e % M] * Wb[(e / M) * kMS + e % M];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dsc += __shfl_xor_sync(0xffffffffu, dsc, o);
     dsc /= scale * scale;
@@ -316,13 +307,13 @@ bwd_head_kernel(const float* __restrict__ landmarks, const float* __restrict__ x
     const int jc = __float_as_int(red[3]), ir = __float_as_int(red[4]);
     for (int e = tid; e < M * M; e += kHeadThreads) {
       const int i = e / M, j = e % M;
-      float g = dW[i * kMS + j] + dX[j * kMS + i] / scale;
+      float g = dW[i * kMS + j] + Sb[i * kMS + j] / scale;
       const float w = Wb[i * kMS + j];
       const float sw = w > 0.f ? 1.f : (w < 0.f ? -1.f : 0.f);
       if (j == jc) g += dn1 * sw;
       if (i == ir) g += dninf * sw;
       // W = exp(-D_LL / lambda) + eps I: dLoss/dD_LL off the diagonal
-      T1[i * kMS + j] = (i == j) ? 0.f : -w / lam * g;
+      U[i * kMS + j] = (i == j) ? 0.f : -w / lam * g;
     }
   }
   __syncthreads();
@@ -334,7 +325,7 @@ bwd_head_kernel(const float* __restrict__ landmarks, const float* __restrict__ x
     float s = 0.f;
     for (int k = 0; k < M; ++k) {
       if (k == p) continue;
-      const float g = T1[p * kMS + k] + T1[k * kMS + p];
+      const float g = U[p * kMS + k] + U[k * kMS + p];
       const float lk = Lh[k * d + c];
       s = fmaf(g, gauss ? 2.f * (lp - lk) : (lp > lk ? 1.f : (lp < lk ? -1.f : 0.f)), s);
     }
@@ -471,6 +462,41 @@ bwd_key_kernel(const void* __restrict__ k, const void* __restrict__ v,
 }
 
 // ---- partials of dL over one token split: side 0 from the query block, 1 from the key block --
+// Thread: quads (landmark j, channels 4 c4 .. 4 c4 + 3); per staged token one float4 of the
+// token row and one weight, shared by the four channels.
+constexpr int kMaxQuads = kMaxPairs / 4;    // 8
+
+template <bool kGauss, int kSide>
+__device__ __forceinline__ void lm_tile(const float* __restrict__ sX, const float* __restrict__ sw,
+                                        int dp, int tp, int d4, int quads, const float4 (&lv)[kMaxQuads],
+                                        float4 (&acc)[kMaxQuads]) {
+#pragma unroll
+  for (int u = 0; u < kMaxQuads; ++u) {
+    const int qd = threadIdx.x + kBwdThreads * u;
+    if (qd < quads) {
+      const int j = qd / d4, c4 = qd % d4;
+      const float4 l = lv[u];
+      float4 a = acc[u];
+      for (int tt = 0; tt < kBwdTile; ++tt) {
+        const float4 x = *reinterpret_cast<const float4*>(&sX[tt * dp + 4 * c4]);
+        const float w = sw[j * tp + tt];
+        if (kSide == 0) {            // dL -= g sgn(Q - L)
+          a.x = fmaf(-w, slope<kGauss>(x.x, l.x), a.x);
+          a.y = fmaf(-w, slope<kGauss>(x.y, l.y), a.y);
+          a.z = fmaf(-w, slope<kGauss>(x.z, l.z), a.z);
+          a.w = fmaf(-w, slope<kGauss>(x.w, l.w), a.w);
+        } else {                     // dL += h sgn(L - K)
+          a.x = fmaf(w, slope<kGauss>(l.x, x.x), a.x);
+          a.y = fmaf(w, slope<kGauss>(l.y, x.y), a.y);
+          a.z = fmaf(w, slope<kGauss>(l.z, x.z), a.z);
+          a.w = fmaf(w, slope<kGauss>(l.w, x.w), a.w);
+        }
+      }
+      acc[u] = a;
+    }
+  }
+}
+
 template <bool kGauss>
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_lm_kernel(const void* __restrict__ q, const void* __restrict__ k,
@@ -479,8 +505,8 @@ bwd_lm_kernel(const void* __restrict__ q, const void* __restrict__ k,
               int n, int tiles_per_split, int splits, int bf16) {
   extern __shared__ float4 smem_l4[];
   float* smem = reinterpret_cast<float*>(smem_l4);
-  const int dp = d + 1, tp = kBwdTile + 1;
-  float* sX = smem;                      // [tile][d + 1]
+  const int dp = d + 4, tp = kBwdTile + 1;
+  float* sX = smem;                      // [tile][d + 4]
   float* sw = sX + kBwdTile * dp;        // [m][tile + 1]
   const int side = blockIdx.x & 1;
   const long rest = blockIdx.x >> 1;
@@ -489,68 +515,68 @@ bwd_lm_kernel(const void* __restrict__ q, const void* __restrict__ k,
   const void* x = side == 0 ? q : k;
   const float* wgt = side == 0 ? gq : hk;
   const float* Lh = landmarks + (size_t)bh * m * d;
-  const int pairs = m * d;
-  float acc[kMaxPairs], lv[kMaxPairs];
+  const int d4 = d >> 2, quads = m * d4;
+  float4 acc[kMaxQuads], lv[kMaxQuads];
 #pragma unroll
-  for (int u = 0; u < kMaxPairs; ++u) {
-    const int p = threadIdx.x + kBwdThreads * u;
-    acc[u] = 0.f;
-    lv[u] = p < pairs ? Lh[p] : 0.f;
+  for (int u = 0; u < kMaxQuads; ++u) {
+    const int qd = threadIdx.x + kBwdThreads * u;
+    acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    lv[u] = qd < quads ? *reinterpret_cast<const float4*>(&Lh[4 * qd]) : acc[u];
   }
   const int tiles = (n + kBwdTile - 1) / kBwdTile;
   const int t0 = sp * tiles_per_split, t1 = min(tiles, t0 + tiles_per_split);
   for (int t = t0; t < t1; ++t) {
     const int n0 = t * kBwdTile;
-    for (int i = threadIdx.x; i < kBwdTile * d; i += kBwdThreads) {
-      const int tt = i / d, c = i % d, tok = n0 + tt;
-      sX[tt * dp + c] = tok < n ? load_in(x, ((size_t)bh * n + tok) * d + c, bf16 != 0) : 0.f;
+    for (int i = threadIdx.x; i < kBwdTile * d4; i += kBwdThreads) {
+      const int tt = i / d4, c4 = i % d4, tok = n0 + tt;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (tok < n) {
+        const size_t e = ((size_t)bh * n + tok) * d + 4 * c4;
+        if (bf16) {
+          v = make_float4(load_in(x, e, true), load_in(x, e + 1, true), load_in(x, e + 2, true),
+                          load_in(x, e + 3, true));
+        } else {
+          v = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + e);
+        }
+      }
+      *reinterpret_cast<float4*>(&sX[tt * dp + 4 * c4]) = v;
     }
     for (int i = threadIdx.x; i < m * kBwdTile; i += kBwdThreads) {
       const int j = i / kBwdTile, tt = i % kBwdTile, tok = n0 + tt;
       sw[j * tp + tt] = tok < n ? wgt[((size_t)bh * m + j) * n + tok] : 0.f;
     }
     __syncthreads();
-#pragma unroll
-    for (int u = 0; u < kMaxPairs; ++u) {
-      const int p = threadIdx.x + kBwdThreads * u;
-      if (p < pairs) {
-        const int j = p / d, c = p % d;
-        const float l = lv[u];
-        float a = acc[u];
-        if (side == 0) {
-          for (int tt = 0; tt < kBwdTile; ++tt)
-            a = fmaf(-sw[j * tp + tt], slope<kGauss>(sX[tt * dp + c], l), a);
-        } else {
-          for (int tt = 0; tt < kBwdTile; ++tt)
-            a = fmaf(sw[j * tp + tt], slope<kGauss>(l, sX[tt * dp + c]), a);
-        }
-        acc[u] = a;
-      }
-    }
+    if (side == 0) lm_tile<kGauss, 0>(sX, sw, dp, tp, d4, quads, lv, acc);
+    else lm_tile<kGauss, 1>(sX, sw, dp, tp, d4, quads, lv, acc);
     __syncthreads();
   }
   float* out = part_dl + (((size_t)bh * 2 + side) * splits + sp) * m * d;
 #pragma unroll
-  for (int u = 0; u < kMaxPairs; ++u) {
-    const int p = threadIdx.x + kBwdThreads * u;
-    if (p < pairs) out[p] = acc[u];
+  for (int u = 0; u < kMaxQuads; ++u) {
+    const int qd = threadIdx.x + kBwdThreads * u;
+    if (qd < quads) *reinterpret_cast<float4*>(&out[4 * qd]) = acc[u];
   }
 }
 
-// ---- dL per head; dbias = sum over the batch ----------------------------------------------
+// ---- dL per head (one element per thread, every partial load in flight); dbias ----------
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_dl_kernel(const float* __restrict__ part_dl, const float* __restrict__ dll,
               const float* __restrict__ dbias_bh, float* __restrict__ dl,
-              float* __restrict__ dbias, int m, int d, int splits, int batch, int heads) {
-  const long bh = blockIdx.x;
-  for (int e = threadIdx.x; e < m * d; e += kBwdThreads) {
+              float* __restrict__ dbias, int m, int d, int splits, int batch, int heads,
+              int chunks) {
+  const long bh = blockIdx.x / chunks;
+  const int e = (blockIdx.x % chunks) * kBwdThreads + threadIdx.x;
+  const size_t md = (size_t)m * d;
+  if (e < m * d) {
     float s = 0.f;
-    for (int side = 0; side < 2; ++side)
-      for (int sp = 0; sp < splits; ++sp)
-        s += part_dl[(((size_t)bh * 2 + side) * splits + sp) * m * d + e];
-    dl[(size_t)bh * m * d + e] = s + dll[(size_t)bh * m * d + e];
+    for (int side = 0; side < 2; ++side) {
+      const float* src = part_dl + ((size_t)bh * 2 + side) * splits * md + e;
+#pragma unroll 16
+      for (int sp = 0; sp < splits; ++sp) s += src[(size_t)sp * md];
+    }
+    dl[(size_t)bh * md + e] = s + dll[(size_t)bh * md + e];
   }
-  if (dbias && bh < heads) {              // batch 0's CTAs: head h = bh sums over the batch
+  if (dbias && bh < heads && blockIdx.x % chunks == 0) {   // batch 0: head h = bh sums the batch
     for (int j = threadIdx.x; j < m; j += kBwdThreads) {
       float s = 0.f;
       for (int b = 0; b < batch; ++b) s += dbias_bh[((size_t)b * heads + bh) * m + j];
@@ -576,18 +602,18 @@ bwd_pool_kernel(const float* __restrict__ dl, float* __restrict__ dk, int m, int
 }
 
 template <int S>
-const void* head_ptr() { return reinterpret_cast<const void*>(&bwd_head_kernel<S>); }
+const void* ns_bwd_ptr() { return reinterpret_cast<const void*>(&bwd_ns_kernel<S>); }
 
-const void* pick_head(int s) {
+const void* pick_ns_bwd(int s) {
   switch (s) {
-    case 1: return head_ptr<1>();
-    case 2: return head_ptr<2>();
-    case 3: return head_ptr<3>();
-    case 4: return head_ptr<4>();
-    case 5: return head_ptr<5>();
-    case 6: return head_ptr<6>();
-    case 7: return head_ptr<7>();
-    case 8: return head_ptr<8>();
+    case 1: return ns_bwd_ptr<1>();
+    case 2: return ns_bwd_ptr<2>();
+    case 3: return ns_bwd_ptr<3>();
+    case 4: return ns_bwd_ptr<4>();
+    case 5: return ns_bwd_ptr<5>();
+    case 6: return ns_bwd_ptr<6>();
+    case 7: return ns_bwd_ptr<7>();
+    case 8: return ns_bwd_ptr<8>();
     default: return nullptr;
   }
 }
@@ -602,16 +628,16 @@ size_t ahat_smem(int m, int d) {
   return sizeof(float) * ((size_t)m * (d + 1) + (size_t)kBwdTile * (d + 1) +
                           2 * (size_t)m * (kBwdTile + 1) + 3 * (size_t)m);
 }
-size_t head_smem(int m, int d) {
-  const size_t region = 64 * (size_t)d > 2 * (size_t)m * d ? 64 * (size_t)d : 2 * (size_t)m * d;
-  return sizeof(float) * (7 * 64 * (size_t)kMS + kRedFloats + region);
+size_t ns_bwd_smem(int d) {
+  return sizeof(float) * (8 * 64 * (size_t)kMS + 4 * 3 * 32 * 32 + kRedFloats + 64 * (size_t)d);
 }
+size_t mid_smem(int m, int d) { return sizeof(float) * (2 * (size_t)m * (d + 1) + (size_t)m * m); }
 size_t query_smem(int m, int d, int tpc) { return sizeof(float) * ((size_t)m * d + (size_t)m * tpc); }
 size_t key_smem(int m, int d, int tpc) {
   return sizeof(float) * (2 * (size_t)m * d + (size_t)tpc * (d + 1) + 2 * (size_t)m * tpc);
 }
 size_t lm_smem(int m, int d) {
-  return sizeof(float) * ((size_t)kBwdTile * (d + 1) + (size_t)m * (kBwdTile + 1));
+  return sizeof(float) * ((size_t)kBwdTile * (d + 4) + (size_t)m * (kBwdTile + 1));
 }
 
 }  // namespace
@@ -619,7 +645,6 @@ size_t lm_smem(int m, int d) {
 BwdLayout bwd_layout(const lapl_attn_plan& p) {
   const Geometry& g = p.geo;
   const size_t bh = (size_t)g.bh, m = g.m, d = g.d, n = g.n, sp = g.bv_splits;
-  const size_t T = (size_t)p.cfg.ns_steps;
   BwdLayout L;
   size_t off = 0;
   auto take = [&](size_t floats) {
@@ -634,12 +659,11 @@ BwdLayout bwd_layout(const lapl_attn_plan& p) {
   L.dbv = take(bh * m * d);
   L.dll = take(bh * m * d);
   L.dbias_bh = take(bh * m);
-  L.xs = take(bh * (T + 1) * m * m);
-  L.ps = take(bh * (T > 0 ? T : 1) * m * m);
   L.gq = take(bh * m * n);
   L.hk = take(bh * m * n);
   L.part_dl = take(bh * 2 * sp * m * d);
   L.dl = take(bh * m * d);
+  L.st = take(bh * m * m);
   L.total = off;
   return L;
 }
@@ -649,10 +673,13 @@ cudaError_t bwd_configure(const lapl_attn_plan& p) {
   const int tpc = token_tile(g.d);
   cudaError_t e = cudaFuncSetAttribute(bwd_ahat_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)ahat_smem(g.m, g.d));
-  const void* hf = pick_head(g.s);
+  const void* hf = pick_ns_bwd(g.s);
   if (!hf) return cudaErrorInvalidValue;
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(hf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)head_smem(g.m, g.d));
+    e = cudaFuncSetAttribute(hf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ns_bwd_smem(g.d));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_mid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)mid_smem(g.m, g.d));
   const int qs = (int)query_smem(g.m, g.d, tpc), ks = (int)key_smem(g.m, g.d, tpc),
             ls = (int)lm_smem(g.m, g.d);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_query_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, qs);
@@ -676,7 +703,7 @@ cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* 
   const bool gauss = p.cfg.kernel == LAPL_KERNEL_GAUSSIAN;
   const float lam = p.cfg.lambda;
   const float* L = reinterpret_cast<const float*>(fws + F.landmarks);
-  const float* X = reinterpret_cast<const float*>(fws + F.x);
+  const float* Xs = reinterpret_cast<const float*>(fws + F.xs);
   const float* At = reinterpret_cast<const float*>(fws + F.at);
   const float* Bt = reinterpret_cast<const float*>(fws + F.bt);
   const float* bvp = reinterpret_cast<const float*>(fws + F.bvp);
@@ -685,8 +712,8 @@ cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* 
   const float* rstd = reinterpret_cast<const float*>(fws + F.rstd);
   auto W = [&](size_t off) { return reinterpret_cast<float*>(bws + off); };
   float *dahat = W(B.dahat), *part_dm = W(B.part_dm), *part_s = W(B.part_s), *s12 = W(B.s12),
-        *dbv = W(B.dbv), *dll = W(B.dll), *dbias_bh = W(B.dbias_bh), *xs = W(B.xs),
-        *ps = W(B.ps), *gq = W(B.gq), *hk = W(B.hk), *part_dl = W(B.part_dl), *dl = W(B.dl);
+        *dbv = W(B.dbv), *dll = W(B.dll), *dbias_bh = W(B.dbias_bh), *gq = W(B.gq),
+        *hk = W(B.hk), *part_dl = W(B.part_dl), *dl = W(B.dl), *sT = W(B.st);
   const unsigned bh = (unsigned)g.bh;
   const int tpc = token_tile(d);
   const int qtiles = (n + tpc - 1) / tpc;
@@ -696,14 +723,24 @@ cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* 
       At, M, mu, rstd, bias, gout, dahat, part_dm, part_s, m, d, n, heads, tps, splits, whiten);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  bwd_mid_kernel<<<bh, kBwdThreads, mid_smem(m, d), st>>>(Xs, bvp, part_dm, part_s, dbv, sT, s12,
+                                                         dbias_bh, m, d, p.cfg.ns_steps, splits,
+                                                         whiten);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // The Newton-Schulz backward (only the landmark-block term of dL needs it) on the side
+  // stream, next to the token kernels.
+  cudaStream_t side = p.side_stream;
+  e = cudaEventRecord(p.ev_pool, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side, p.ev_pool, 0);
+  if (e != cudaSuccess) return e;
   {
-    const void* f = pick_head(g.s);
-    int T = p.cfg.ns_steps, gs = gauss, sp = splits, wh = whiten;
+    const void* f = pick_ns_bwd(g.s);
+    int T = p.cfg.ns_steps, gs = gauss, dd = d;
     float eps = p.cfg.eps, c_exp = p.neg_log2e_over_lambda, lm = lam;
-    int dd = d;
-    void* args[] = {&L, &X, &bvp, &part_dm, &part_s, &dbv, &dll, &s12, &dbias_bh, &xs, &ps,
-                    &dd, &T, &eps, &c_exp, &lm, &gs, &sp, &wh};
-    e = cudaLaunchKernel(f, dim3(bh), dim3(kHeadThreads), args, head_smem(m, d), st);
+    void* args[] = {&L, &Xs, &sT, &dll, &dd, &T, &eps, &c_exp, &lm, &gs};
+    e = cudaLaunchKernel(f, dim3(bh), dim3(kHeadThreads), args, ns_bwd_smem(d), side);
+    if (e == cudaSuccess) e = cudaEventRecord(p.ev_join, side);
     if (e != cudaSuccess) return e;
   }
   const unsigned tthreads = (unsigned)(tpc * (d / 8));
@@ -723,9 +760,11 @@ cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* 
         q, k, gq, hk, L, part_dl, m, d, n, tps, splits, bf16);
   }
   e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, p.ev_join, 0);
   if (e != cudaSuccess) return e;
-  bwd_dl_kernel<<<bh, kBwdThreads, 0, st>>>(part_dl, dll, dbias_bh, dl, dbias, m, d, splits,
-                                             p.cfg.batch, heads);
+  const unsigned dl_chunks = (unsigned)((m * d + kBwdThreads - 1) / kBwdThreads);
+  bwd_dl_kernel<<<bh * dl_chunks, kBwdThreads, 0, st>>>(part_dl, dll, dbias_bh, dl, dbias, m, d,
+                                                         splits, p.cfg.batch, heads, dl_chunks);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int s = g.s;

@@ -49,6 +49,8 @@ __host__ __device__ inline int part_owner(const Partition& pt, long long x) {
 struct WorkspaceLayout {
   size_t landmarks;    // [BH, m, d]         pooled keys L
   size_t x;            // [BH, m, m]         Newton-Schulz result X
+  size_t xs;           // [BH, T + 1, m, m]  every Newton-Schulz iterate X_0 .. X_T (kept
+                       //                    for the backward pass; Newton-Schulz plans only)
   size_t at;           // [BH, m, N]         A = k(Q, L), landmark-major (A transposed)
   size_t bt;           // [BH, m, N]         B = k(L, K)
   size_t bvp;          // [BH, bv_splits, m, d]  per-split partial sums of B V
@@ -67,12 +69,11 @@ struct BwdLayout {
   size_t dbv;        // [BH, m, d]          dLoss/d(B V)
   size_t dll;        // [BH, m, d]          the landmark block's term of dL
   size_t dbias_bh;   // [BH, m]             per-slice bias gradient
-  size_t xs;         // [BH, T + 1, m, m]   Newton-Schulz iterates
-  size_t ps;         // [BH, max(T, 1), m, m]  products W X_t
   size_t gq;         // [BH, m, N]          dLoss/dD_QL
   size_t hk;         // [BH, m, N]          dLoss/dD_LK
   size_t part_dl;    // [BH, 2, splits, m, d]  partial dL (query side, key side)
   size_t dl;         // [BH, m, d]          dLoss/dL
+  size_t st;         // [BH, m, m]          sym(dLoss/dX_T)
   size_t total;
 };
 
@@ -138,7 +139,7 @@ namespace lapl {
 cudaError_t launch_pool(const lapl_attn_plan& p, const void* k, float* landmarks,
                         float* dbg_landmarks, cudaStream_t st);
 cudaError_t launch_ns(const lapl_attn_plan& p, const float* landmarks, float* x, float* dbg_dll,
-                      float* dbg_w, float* dbg_x, cudaStream_t st);
+                      float* dbg_w, float* dbg_x, float* xs, cudaStream_t st);
 cudaError_t launch_cdist(const lapl_attn_plan& p, const void* q, const void* k, const void* v,
                          const float* landmarks, float* at, float* bt, float* dbg_dql,
                          float* dbg_dlk, float* dbg_a, cudaStream_t st);
@@ -165,7 +166,7 @@ cudaError_t ns_configure(int s, int cluster, size_t smem, int* clusters_per_gpu)
 size_t ns_tc_smem_bytes(int d);
 cudaError_t ns_tc_configure(int s, size_t smem);
 cudaError_t launch_ns_tc(const lapl_attn_plan& p, const float* landmarks, float* x,
-                         float* dbg_dll, float* dbg_w, float* dbg_x, cudaStream_t st);
+                         float* dbg_dll, float* dbg_w, float* dbg_x, float* xs, cudaStream_t st);
 size_t output_smem_bytes(int m, int d, int tile);
 cudaError_t output_configure(size_t smem);
 size_t bv_smem_bytes(int m, int d, int threads, bool bf16);

@@ -43,113 +43,12 @@ namespace {
 
 constexpr int kNsThreads = 512;
 
-// Barrier of the first `threads` threads of the CTA (whole warps), named barrier 1.
-__device__ __forceinline__ void warps_barrier(int threads) {
-  asm volatile("bar.sync 1, %0;\n" ::"r"(threads) : "memory");
-}
-
-// C = A B for symmetric A (row stride kMS): (A B)[i][j] = sum_k A[k][i] B[k][j].
-// kUpdate: C = (V + V^T) / 2 with V = 2 Xs - A B (exactly symmetric).  Otherwise C = A B.
-// Warp w: tile w % NTILES, k quarter w / NTILES (the four slice-0 warps land on four different
-// sub-partitions); the slice-0 warps (0 .. NTILES-1) reduce and store, and for kUpdate meet at
-// a named barrier between writing V and reading its transpose.  Ends with a __syncthreads().
-template <int MK, int NWT, bool kUpdate>
-__device__ __forceinline__ void sym_product(const float* __restrict__ A,
-                                            const float* __restrict__ B,
-                                            const float* __restrict__ Xs, float* __restrict__ C,
-                                            float* __restrict__ part) {
-  constexpr int NTILES = NWT * NWT;
-  constexpr int KS = 4;
-  constexpr int KQ = MK / KS;                        // MK is a multiple of 4
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = warp % NTILES, ks = warp / NTILES;
-  const bool active = ks < KS;
-  const int tr = tile / NWT, tc = tile % NWT;
-  const int rq = lane >> 3, cq = lane & 7;
-  const int r0 = 32 * tr + 8 * rq, c0 = 32 * tc + 4 * cq;
-  float acc[8][4];
-#pragma unroll
-  for (int r = 0; r < 8; ++r)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
-  if (active) {
-    const float* a = A + (ks * KQ) * kMS + r0;
-    const float* b = B + (ks * KQ) * kMS + c0;
-    // Operands of step kk+1 are loaded while the 32 FMAs of step kk issue.
-    float4 a0 = *reinterpret_cast<const float4*>(a);
-    float4 a1 = *reinterpret_cast<const float4*>(a + 4);
-    float4 bv = *reinterpret_cast<const float4*>(b);
-#pragma unroll
-    for (int kk = 0; kk < KQ; ++kk) {
-      const int kn = kk + 1 < KQ ? kk + 1 : kk;
-      const float4 na0 = *reinterpret_cast<const float4*>(a + kn * kMS);
-      const float4 na1 = *reinterpret_cast<const float4*>(a + kn * kMS + 4);
-      const float4 nbv = *reinterpret_cast<const float4*>(b + kn * kMS);
-      const float ar[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float br[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-      for (int r = 0; r < 8; ++r)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(ar[r], br[c], acc[r][c]);
-      a0 = na0;
-      a1 = na1;
-      bv = nbv;
-    }
-    if (ks > 0) {
-#pragma unroll
-      for (int e = 0; e < 32; ++e)
-        part[(((ks - 1) * NTILES + tile) * 32 + e) * 32 + lane] = acc[e >> 2][e & 3];
-    }
-  }
-  __syncthreads();
-  if (active && ks == 0) {
-#pragma unroll
-    for (int q = 1; q < KS; ++q)
-#pragma unroll
-      for (int e = 0; e < 32; ++e)
-        acc[e >> 2][e & 3] += part[(((q - 1) * NTILES + tile) * 32 + e) * 32 + lane];
-    if constexpr (kUpdate) {
-      float v[8][4];
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const float4 x4 = *reinterpret_cast<const float4*>(&Xs[(r0 + r) * kMS + c0]);
-        v[r][0] = 2.f * x4.x - acc[r][0];
-        v[r][1] = 2.f * x4.y - acc[r][1];
-        v[r][2] = 2.f * x4.z - acc[r][2];
-        v[r][3] = 2.f * x4.w - acc[r][3];
-        *reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]) =
-            make_float4(v[r][0], v[r][1], v[r][2], v[r][3]);
-      }
-      warps_barrier(32 * NTILES);                    // V complete
-      float vt[8][4];                                // vt[r][c] = V[c0 + c][r0 + r]
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float4 t0 = *reinterpret_cast<const float4*>(&C[(c0 + c) * kMS + r0]);
-        const float4 t1 = *reinterpret_cast<const float4*>(&C[(c0 + c) * kMS + r0 + 4]);
-        vt[0][c] = t0.x; vt[1][c] = t0.y; vt[2][c] = t0.z; vt[3][c] = t0.w;
-        vt[4][c] = t1.x; vt[5][c] = t1.y; vt[6][c] = t1.z; vt[7][c] = t1.w;
-      }
-      warps_barrier(32 * NTILES);                    // every transpose read before any write
-#pragma unroll
-      for (int r = 0; r < 8; ++r)
-        *reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]) =
-            make_float4(0.5f * (v[r][0] + vt[r][0]), 0.5f * (v[r][1] + vt[r][1]),
-                        0.5f * (v[r][2] + vt[r][2]), 0.5f * (v[r][3] + vt[r][3]));
-    } else {
-#pragma unroll
-      for (int r = 0; r < 8; ++r)
-        *reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]) =
-            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-    }
-  }
-  __syncthreads();
-}
-
 template <int S>
 __global__ void __launch_bounds__(kNsThreads)
 ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
                   float* __restrict__ dbg_dll, float* __restrict__ dbg_w,
-                  float* __restrict__ dbg_x, int d, int T, float eps, float c_exp, int gauss) {
+                  float* __restrict__ dbg_x, float* __restrict__ xs, int d, int T, float eps,
+                  float c_exp, int gauss) {
   using Sh = NsShape<S>;
   constexpr int M = Sh::M, MP = kMS;
   extern __shared__ float4 smem_ns4[];
@@ -162,11 +61,14 @@ ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
   float* P = sm.P;
   float* Y = sm.Y;
   float* part = sm.part;
+  float* xsh = xs ? xs + (size_t)bh * (T + 1) * M * M : nullptr;
 
+  save_iterate<M, kNsThreads>(X, xsh);
   for (int t = 0; t < T; ++t) {
-    sym_product<Sh::MK, Sh::NWT, false>(W, X, nullptr, P, part);   // P = W X
-    sym_product<Sh::MK, Sh::NWT, true>(X, P, X, Y, part);          // Y = 2X - X P
+    sym_product<Sh::MK, Sh::NWT, kPlain>(W, X, nullptr, P, part);   // P = W X
+    sym_product<Sh::MK, Sh::NWT, kAvgUpdate>(X, P, X, Y, part);          // Y = 2X - X P
     float* tmp = X; X = Y; Y = tmp;
+    save_iterate<M, kNsThreads>(X, xsh ? xsh + (size_t)(t + 1) * M * M : nullptr);
   }
 
   for (int idx = threadIdx.x; idx < M * M; idx += kNsThreads) {
@@ -288,7 +190,8 @@ template <int S>
 __global__ void __launch_bounds__(kNsThreads)
 ns_pair_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
                float* __restrict__ dbg_dll, float* __restrict__ dbg_w,
-               float* __restrict__ dbg_x, int d, int T, float eps, float c_exp, int gauss) {
+               float* __restrict__ dbg_x, float* __restrict__ xs, int d, int T, float eps,
+               float c_exp, int gauss) {
   using Sh = NsShape<S>;
   static_assert(Sh::NWT == 2, "the pair split assumes 2 x 2 warp tiles");
   constexpr int M = Sh::M, MP = kMS;
@@ -306,6 +209,8 @@ ns_pair_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
   float* Xp = cluster.map_shared_rank(sm.X, crank ^ 1);
   float* Pp = cluster.map_shared_rank(sm.P, crank ^ 1);
   cluster.sync();                  // the peer is running before anything is stored into it
+  float* xsh = (xs && crank == 0) ? xs + (size_t)bh * (T + 1) * M * M : nullptr;
+  save_iterate<M, kNsThreads>(X, xsh);
 
   for (int t = 0; t < T; ++t) {
     pair_product<Sh::MK, false>(sm.W, X, nullptr, sm.P, sm.part, crank);   // P = W X
@@ -317,6 +222,7 @@ ns_pair_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
     pair_symmetrise<M>(Y);                                                // Y = (V + V^T) / 2
     float* tmp = X; X = Y; Y = tmp;
     tmp = Xp; Xp = Yp; Yp = tmp;
+    save_iterate<M, kNsThreads>(X, xsh ? xsh + (size_t)(t + 1) * M * M : nullptr);
   }
 
   // Both CTAs hold the final X; each writes half of it.
@@ -403,14 +309,14 @@ cudaError_t ns_configure(int s, int cluster, size_t smem, int* clusters_per_gpu)
 }
 
 cudaError_t launch_ns(const lapl_attn_plan& p, const float* landmarks, float* x, float* dbg_dll,
-                      float* dbg_w, float* dbg_x, cudaStream_t st) {
+                      float* dbg_w, float* dbg_x, float* xs, cudaStream_t st) {
   const Geometry& g = p.geo;
   const void* f = pick_ns(g.s, g.ns_cluster);
   if (!f) return cudaErrorInvalidValue;
   int d = g.d, T = p.cfg.ns_steps;
   float eps = p.cfg.eps, c_exp = p.neg_log2e_over_lambda;
   int gauss = p.cfg.kernel == LAPL_KERNEL_GAUSSIAN;
-  void* args[] = {&landmarks, &x, &dbg_dll, &dbg_w, &dbg_x, &d, &T, &eps, &c_exp, &gauss};
+  void* args[] = {&landmarks, &x, &dbg_dll, &dbg_w, &dbg_x, &xs, &d, &T, &eps, &c_exp, &gauss};
   if (g.ns_cluster == 1)
     return cudaLaunchKernel(f, dim3((unsigned)g.bh), dim3(kNsThreads), args, g.ns_smem, st);
   cudaLaunchConfig_t cfg = {};

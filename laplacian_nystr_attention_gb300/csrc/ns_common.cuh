@@ -159,5 +159,142 @@ __device__ __forceinline__ void ns_prologue(const NsSmem& sm, const float* __res
   __syncthreads();
 }
 
+// Barrier of the first `threads` threads of the CTA (whole warps), named barrier 1.
+__device__ __forceinline__ void warps_barrier(int threads) {
+  asm volatile("bar.sync 1, %0;\n" ::"r"(threads) : "memory");
+}
+
+// What sym_product does with the product P = A^T B.
+enum ProductMode {
+  kPlain = 0,      // C = P (and Ct = P^T when Ct is given)
+  kAvgUpdate = 1,  // C = (V + V^T) / 2 with V = 2 Xs - P   (the Newton-Schulz update)
+  kSymRecur = 2,   // C = V + V^T with V = Xs - P           (2 Xs - P - P^T for symmetric Xs)
+  kSubtract = 3    // C -= P
+};
+
+// P = A^T B for 64 x 64 matrices with row stride kMS: P[i][j] = sum_k A[k][i] B[k][j], so
+// for a symmetric A it is A B and both operands are read by rows; 512 threads.
+// Warp w: tile w % NTILES, k quarter w / NTILES (the four slice-0 warps land on four different
+// sub-partitions); the slice-0 warps (0 .. NTILES-1) reduce and store, and for the symmetrising
+// modes meet at a named barrier between writing V and reading its transpose.  Ends with a
+// __syncthreads().
+template <int MK, int NWT, int kMode>
+__device__ __forceinline__ void sym_product(const float* __restrict__ A,
+                                            const float* __restrict__ B,
+                                            const float* __restrict__ Xs, float* __restrict__ C,
+                                            float* __restrict__ part, float* __restrict__ Ct = nullptr) {
+  constexpr int NTILES = NWT * NWT;
+  constexpr int KS = 4;
+  constexpr int KQ = MK / KS;                        // MK is a multiple of 4
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = warp % NTILES, ks = warp / NTILES;
+  const bool active = ks < KS;
+  const int tr = tile / NWT, tc = tile % NWT;
+  const int rq = lane >> 3, cq = lane & 7;
+  const int r0 = 32 * tr + 8 * rq, c0 = 32 * tc + 4 * cq;
+  float acc[8][4];
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+  if (active) {
+    const float* a = A + (ks * KQ) * kMS + r0;
+    const float* b = B + (ks * KQ) * kMS + c0;
+    // Operands of step kk+1 are loaded while the 32 FMAs of step kk issue.
+    float4 a0 = *reinterpret_cast<const float4*>(a);
+    float4 a1 = *reinterpret_cast<const float4*>(a + 4);
+    float4 bv = *reinterpret_cast<const float4*>(b);
+#pragma unroll
+    for (int kk = 0; kk < KQ; ++kk) {
+      const int kn = kk + 1 < KQ ? kk + 1 : kk;
+      const float4 na0 = *reinterpret_cast<const float4*>(a + kn * kMS);
+      const float4 na1 = *reinterpret_cast<const float4*>(a + kn * kMS + 4);
+      const float4 nbv = *reinterpret_cast<const float4*>(b + kn * kMS);
+      const float ar[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float br[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(ar[r], br[c], acc[r][c]);
+      a0 = na0;
+      a1 = na1;
+      bv = nbv;
+    }
+    if (ks > 0) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        part[(((ks - 1) * NTILES + tile) * 32 + e) * 32 + lane] = acc[e >> 2][e & 3];
+    }
+  }
+  __syncthreads();
+  if (active && ks == 0) {
+#pragma unroll
+    for (int q = 1; q < KS; ++q)
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        acc[e >> 2][e & 3] += part[(((q - 1) * NTILES + tile) * 32 + e) * 32 + lane];
+    if constexpr (kMode == kAvgUpdate || kMode == kSymRecur) {
+      constexpr float kx = kMode == kAvgUpdate ? 2.f : 1.f;     // V = kx Xs - P
+      constexpr float kc = kMode == kAvgUpdate ? 0.5f : 1.f;    // C = kc (V + V^T)
+      float v[8][4];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float4 x4 = *reinterpret_cast<const float4*>(&Xs[(r0 + r) * kMS + c0]);
+        v[r][0] = kx * x4.x - acc[r][0];
+        v[r][1] = kx * x4.y - acc[r][1];
+        v[r][2] = kx * x4.z - acc[r][2];
+        v[r][3] = kx * x4.w - acc[r][3];
+        *reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]) =
+            make_float4(v[r][0], v[r][1], v[r][2], v[r][3]);
+      }
+      warps_barrier(32 * NTILES);                    // V complete
+      float vt[8][4];                                // vt[r][c] = V[c0 + c][r0 + r]
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 t0 = *reinterpret_cast<const float4*>(&C[(c0 + c) * kMS + r0]);
+        const float4 t1 = *reinterpret_cast<const float4*>(&C[(c0 + c) * kMS + r0 + 4]);
+        vt[0][c] = t0.x; vt[1][c] = t0.y; vt[2][c] = t0.z; vt[3][c] = t0.w;
+        vt[4][c] = t1.x; vt[5][c] = t1.y; vt[6][c] = t1.z; vt[7][c] = t1.w;
+      }
+      warps_barrier(32 * NTILES);                    // every transpose read before any write
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        *reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]) =
+            make_float4(kc * (v[r][0] + vt[r][0]), kc * (v[r][1] + vt[r][1]),
+                        kc * (v[r][2] + vt[r][2]), kc * (v[r][3] + vt[r][3]));
+    } else if constexpr (kMode == kSubtract) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        float4* cp = reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]);
+        const float4 o = *cp;
+        *cp = make_float4(o.x - acc[r][0], o.y - acc[r][1], o.z - acc[r][2], o.w - acc[r][3]);
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        *reinterpret_cast<float4*>(&C[(r0 + r) * kMS + c0]) =
+            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      if (Ct) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          *reinterpret_cast<float4*>(&Ct[(c0 + c) * kMS + r0]) =
+              make_float4(acc[0][c], acc[1][c], acc[2][c], acc[3][c]);
+          *reinterpret_cast<float4*>(&Ct[(c0 + c) * kMS + r0 + 4]) =
+              make_float4(acc[4][c], acc[5][c], acc[6][c], acc[7][c]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Copy the M x M block of X (row stride kMS) to dst, row-major, with the CTA's NT threads (the
+// iterates the backward pass runs through).  Nothing when dst is null.
+template <int M, int NT>
+__device__ __forceinline__ void save_iterate(const float* __restrict__ X, float* __restrict__ dst) {
+  if (!dst) return;
+  for (int e = threadIdx.x; e < M * M; e += NT) dst[e] = X[(e / M) * kMS + e % M];
+}
+
 }  // namespace ns_detail
 }  // namespace lapl

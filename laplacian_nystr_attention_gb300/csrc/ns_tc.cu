@@ -210,7 +210,8 @@ template <int S>
 __global__ void __launch_bounds__(kTcThreads, 1)
 ns_tc_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
              float* __restrict__ dbg_dll, float* __restrict__ dbg_w, float* __restrict__ dbg_x,
-             int d, int T, float eps, float c_exp, int gauss, unsigned* __restrict__ err) {
+             float* __restrict__ xs, int d, int T, float eps, float c_exp, int gauss,
+             unsigned* __restrict__ err) {
   using Sh = NsShape<S>;
   constexpr int M = Sh::M;
   constexpr int KSTEPS = (Sh::MK + 7) / 8;
@@ -266,9 +267,12 @@ ns_tc_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
 
   unsigned phase = 0;
   bool ok = true;
+  float* xsh = xs ? xs + (size_t)bh * (T + 1) * M * M : nullptr;
   for (int t = 0; t < T && ok; ++t) {
     // ---- P^T = X W ----
     if (threadIdx.x == 0) issue_product(tmem, xx_a, ww_a, KSTEPS, bar_a);
+    // X_t is kept for the backward pass while the tensor cores work (they read XX, not Xf).
+    save_iterate<M, kTcThreads>(Xf, xsh ? xsh + (size_t)t * M * M : nullptr);
     ok = wait_product(bar_a, phase);
     phase ^= 1;
     if (!ok) break;
@@ -322,6 +326,7 @@ ns_tc_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
     __syncthreads();
     tc_fence_after();
   }
+  if (ok) save_iterate<M, kTcThreads>(Xf, xsh ? xsh + (size_t)T * M * M : nullptr);
 
   if (!ok) {
     if (threadIdx.x == 0) atomicOr(err, kErrTimeout);
@@ -372,7 +377,7 @@ cudaError_t ns_tc_configure(int s, size_t smem) {
 }
 
 cudaError_t launch_ns_tc(const lapl_attn_plan& p, const float* landmarks, float* x,
-                         float* dbg_dll, float* dbg_w, float* dbg_x, cudaStream_t st) {
+                         float* dbg_dll, float* dbg_w, float* dbg_x, float* xs, cudaStream_t st) {
   const Geometry& g = p.geo;
   const void* f = pick_tc(g.s);
   if (!f) return cudaErrorInvalidValue;
@@ -380,7 +385,7 @@ cudaError_t launch_ns_tc(const lapl_attn_plan& p, const float* landmarks, float*
   float eps = p.cfg.eps, c_exp = p.neg_log2e_over_lambda;
   unsigned* err = p.dev_err;
   int gauss = p.cfg.kernel == LAPL_KERNEL_GAUSSIAN;
-  void* args[] = {&landmarks, &x, &dbg_dll, &dbg_w, &dbg_x, &d, &T, &eps, &c_exp, &gauss, &err};
+  void* args[] = {&landmarks, &x, &dbg_dll, &dbg_w, &dbg_x, &xs, &d, &T, &eps, &c_exp, &gauss, &err};
   return cudaLaunchKernel(f, dim3((unsigned)g.bh), dim3(kTcThreads), args, g.ns_smem, st);
 }
 
