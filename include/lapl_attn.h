@@ -140,6 +140,16 @@ lapl_status lapl_attn_forward(lapl_attn_handle h, const void* q, const void* k, 
                               const float* bias, void* out, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/*
+ * forward() that also keeps in the workspace what lapl_attn_backward needs beyond the forward's
+ * own intermediates: every Newton-Schulz iterate X_0 .. X_T (about 2-3 us more at the stage-1
+ * shape).  Same arguments, results bit for bit equal to forward().  LAPL_ERR_UNSUPPORTED with
+ * the CG solver.
+ */
+lapl_status lapl_attn_forward_train(lapl_attn_handle h, const void* q, const void* k,
+                                    const void* v, const float* bias, void* out,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* forward() that also writes the non-NULL fields of *dbg (device buffers, fp32). */
 lapl_status lapl_attn_forward_debug(lapl_attn_handle h, const void* q, const void* k,
                                     const void* v, const float* bias, void* out,
@@ -259,8 +269,9 @@ lapl_status lapl_attn_forward_noalloc(lapl_attn_handle h, const void* q, const v
  *   dq, dk, dv      device [B,H,N,d] fp32, written (fp32 also for bf16 inputs);
  *   dbias           device [H,m] fp32 or NULL: written with the sum over the batch of
  *                   dLoss/dbias (zeros when whiten = 0);
- *   fwd_workspace   the workspace of that forward (lapl_attn_forward on the same handle),
- *                   untouched since: the backward reads the landmarks, X, A, B, the column
+ *   fwd_workspace   the workspace of that forward, which must have been
+ *                   lapl_attn_forward_train on the same handle, untouched since: the backward
+ *                   reads the landmarks, the Newton-Schulz iterates, A, B, the column
  *                   statistics, the B V partials and M from it;
  *   bwd_workspace   device, >= lapl_attn_backward_workspace_size bytes, overwritten.
  * Derivative conventions: d|x - y|/dx = sgn(x - y) with sgn(0) = 0 (for the Gaussian kernel

@@ -24,7 +24,7 @@ from ._lib import (LAPL_BF16, LAPL_F32, LAPL_KERNEL_GAUSSIAN, LAPL_KERNEL_LAPLAC
                    lapl_attn_set_timing, lapl_attn_stage_marks, lapl_attn_stage_times,
                    lapl_attn_status_string,
                    lapl_attn_plan_info_get, lapl_attn_version, lapl_attn_workspace_size,
-                   lapl_attn_backward, lapl_attn_backward_kernels,
+                   lapl_attn_backward, lapl_attn_backward_kernels, lapl_attn_forward_train,
                    lapl_attn_backward_workspace_size)
 
 __all__ = [
@@ -34,7 +34,7 @@ __all__ = [
     "lapl_attn_status_string", "lapl_attn_version", "lapl_attn_workspace_size", "LAPL_F32",
     "LAPL_BF16", "lapl_attn_set_timing", "lapl_attn_stage_times", "lapl_attn_stage_marks",
     "lapl_attn_kernels_per_forward", "lapl_attn_device_errors", "lapl_attn_plan_info_get",
-    "make_config", "lapl_attn_backward", "lapl_attn_backward_kernels",
+    "make_config", "lapl_attn_backward", "lapl_attn_backward_kernels", "lapl_attn_forward_train",
     "lapl_attn_backward_workspace_size", "LAPL_KERNEL_LAPLACIAN", "LAPL_KERNEL_GAUSSIAN", "LAPL_SOLVER_NEWTON_SCHULZ",
     "LAPL_SOLVER_CG",
 ]
@@ -93,10 +93,13 @@ class LaplacianNystromAttention:
             raise ValueError(f"{name}: must be a contiguous CUDA tensor")
         return t
 
-    def forward(self, q, k, v, bias=None, out=None, stream=None, debug: dict | None = None):
+    def forward(self, q, k, v, bias=None, out=None, stream=None, debug: dict | None = None,
+                keep_for_backward: bool = False):
         """O = attention(q, k, v) on ``stream`` (default: torch's current stream).
 
         debug: optional dict name -> fp32 CUDA tensor for the lapl_attn_debug fields.
+        keep_for_backward: run lapl_attn_forward_train, which keeps the Newton-Schulz iterates
+        that backward() needs.
         """
         import torch
         c = self.cfg
@@ -117,20 +120,25 @@ class LaplacianNystromAttention:
         if debug:
             dbg = lapl_attn_debug(**{kname: t.data_ptr() for kname, t in debug.items()})
             lapl_attn_forward_debug(*args, dbg)
+        elif keep_for_backward:
+            lapl_attn_forward_train(*args)
         else:
             lapl_attn_forward(*args)
+        self._kept = bool(keep_for_backward) and not debug
         return out
 
     __call__ = forward
 
     def backward(self, q, k, v, dout, bias=None, grads=None, stream=None):
-        """(dq, dk, dv, dbias) for a loss with dLoss/dO = dout, after forward(q, k, v, bias) on
-        this object (whose workspace holds what that forward saved; run nothing else on it in
-        between).  dout: fp32 [B,H,N,d].  grads: optional dict with preallocated fp32 "dq",
+        """(dq, dk, dv, dbias) for a loss with dLoss/dO = dout, after
+        forward(q, k, v, bias, keep_for_backward=True) on this object (whose workspace holds
+        what that forward kept; run nothing else on it in between).  dout: fp32 [B,H,N,d].  grads: optional dict with preallocated fp32 "dq",
         "dk", "dv" ([B,H,N,d]) and "dbias" ([H,m]) tensors.  The backward workspace is
         allocated on first use."""
         import torch
         c = self.cfg
+        if not getattr(self, "_kept", False):
+            raise RuntimeError("backward() needs a preceding forward(..., keep_for_backward=True)")
         for name, t in (("q", q), ("k", k), ("v", v)):
             self._check_io(t, c.in_dtype, name)
         self._check_io(dout, LAPL_F32, "dout")

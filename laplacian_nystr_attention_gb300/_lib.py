@@ -76,6 +76,7 @@ def _load():
         "lapl_attn_create": ([ctypes.POINTER(lapl_attn_config), ctypes.POINTER(H)], st),
         "lapl_attn_workspace_size": ([H, ctypes.POINTER(sz)], st),
         "lapl_attn_forward": ([H, vp, vp, vp, vp, vp, vp, sz, vp], st),
+        "lapl_attn_forward_train": ([H, vp, vp, vp, vp, vp, vp, sz, vp], st),
         "lapl_attn_forward_debug": ([H, vp, vp, vp, vp, vp, vp, sz, vp,
                                      ctypes.POINTER(lapl_attn_debug)], st),
         "lapl_attn_host_staging_size": ([H, ctypes.POINTER(sz)], st),
@@ -102,6 +103,7 @@ def _load():
 LIB = _load()
 EXPORTED = ["lapl_attn_version", "lapl_attn_status_string", "lapl_attn_last_error",
             "lapl_attn_create", "lapl_attn_workspace_size", "lapl_attn_forward",
+            "lapl_attn_forward_train",
             "lapl_attn_forward_debug", "lapl_attn_host_staging_size", "lapl_attn_forward_host",
             "lapl_attn_set_timing", "lapl_attn_stage_times", "lapl_attn_stage_marks",
             "lapl_attn_kernels_per_forward",
@@ -157,6 +159,12 @@ def lapl_attn_host_staging_size(handle) -> int:
 def lapl_attn_forward(handle, q, k, v, bias, out, workspace, workspace_bytes, stream) -> None:
     _check(LIB.lapl_attn_forward(handle, q, k, v, bias, out, workspace, workspace_bytes, stream),
            "lapl_attn_forward", handle)
+
+
+def lapl_attn_forward_train(handle, q, k, v, bias, out, workspace, workspace_bytes,
+                            stream) -> None:
+    _check(LIB.lapl_attn_forward_train(handle, q, k, v, bias, out, workspace, workspace_bytes,
+                                       stream), "lapl_attn_forward_train", handle)
 
 
 def lapl_attn_forward_debug(handle, q, k, v, bias, out, workspace, workspace_bytes, stream,

@@ -259,7 +259,7 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   };
   w.landmarks = take(bh * m * d);
   w.x = take(bh * m * m);
-  w.xs = take(g.cg ? 0 : bh * ((size_t)cfg->ns_steps + 1) * m * m);
+  w.xs = take(g.cg ? 0 : bh * ((size_t)cfg->ns_steps + 1) * m * ((m + 3) & ~(size_t)3));
   w.at = take(bh * m * n);
   w.bt = take(bh * m * n);
   w.bvp = take(bh * g.bv_splits * m * d);
@@ -294,7 +294,7 @@ lapl_status lapl_attn_workspace_size(lapl_attn_handle h, size_t* bytes) {
 static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k, const void* v,
                                const float* bias, void* out, void* workspace,
                                size_t workspace_bytes, cudaStream_t st,
-                               const lapl_attn_debug* dbg) {
+                               const lapl_attn_debug* dbg, bool keep = false) {
   if (!p) return LAPL_ERR_INVALID_ARG;
   if (p->geo.bh == 0) return LAPL_OK;   // empty batch
   if (!q || !k || !v || !out || !workspace) return LAPL_ERR_INVALID_ARG;
@@ -313,7 +313,8 @@ static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k,
   char* ws = static_cast<char*>(workspace);
   float* L = reinterpret_cast<float*>(ws + p->ws.landmarks);
   float* X = reinterpret_cast<float*>(ws + p->ws.x);
-  float* Xs = reinterpret_cast<float*>(ws + p->ws.xs);
+  // The Newton-Schulz iterates, kept only for a backward pass.
+  float* Xs = keep ? reinterpret_cast<float*>(ws + p->ws.xs) : nullptr;
   float* At = reinterpret_cast<float*>(ws + p->ws.at);
   float* Bt = reinterpret_cast<float*>(ws + p->ws.bt);
   float* mu = reinterpret_cast<float*>(ws + p->ws.mu);
@@ -461,6 +462,14 @@ lapl_status lapl_attn_forward(lapl_attn_handle h, const void* q, const void* k, 
                               size_t workspace_bytes, void* stream) {
   return run_forward(h, q, k, v, bias, out, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream), nullptr);
+}
+
+lapl_status lapl_attn_forward_train(lapl_attn_handle h, const void* q, const void* k,
+                                    const void* v, const float* bias, void* out,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (h && h->geo.cg) return LAPL_ERR_UNSUPPORTED;
+  return run_forward(h, q, k, v, bias, out, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream), nullptr, true);
 }
 
 lapl_status lapl_attn_forward_debug(lapl_attn_handle h, const void* q, const void* k,

@@ -170,7 +170,9 @@ bwd_mid_kernel(const float* __restrict__ xs, const float* __restrict__ bvp,
     sdM[(e / d) * dp + e % d] = a;
     sBV[(e / d) * dp + e % d] = b;
   }
-  for (int e = tid; e < m * m; e += kBwdThreads) sX[e] = xs[((size_t)bh * (T + 1) + T) * mm + e];
+  const int mk = (m + 3) & ~3;           // row length of the saved iterates
+  for (int e = tid; e < m * m; e += kBwdThreads)
+    sX[e] = xs[((size_t)bh * (T + 1) + T) * m * mk + (e / m) * mk + e % m];
   if (tid < m) {
     float a = 0.f, b = 0.f;
     for (int sp = 0; sp < splits; ++sp) {
@@ -234,11 +236,14 @@ bwd_ns_kernel(const float* __restrict__ landmarks, const float* __restrict__ xs,
   const size_t mm = (size_t)M * M;
   for (int e = tid; e < 7 * MM; e += kHeadThreads) Xb[0][e] = 0.f;   // zero padding
   __syncthreads();
-  const float* xsh = xs + (size_t)bh * (T + 1) * mm;
+  constexpr int Q = MK / 4;                // float4 per saved row
+  const float* xsh = xs + (size_t)bh * (T + 1) * M * MK;
   auto fetch = [&](int t, float* dst) {
-    for (int e = tid; e < M * M; e += kHeadThreads) {
-      const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(&dst[(e / M) * kMS + e % M]));
-      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(a), "l"(xsh + (size_t)t * mm + e)
+    for (int e = tid; e < M * Q; e += kHeadThreads) {
+      const int r = e / Q, c4 = e - r * Q;
+      const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(&dst[r * kMS + 4 * c4]));
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(a),
+                   "l"(xsh + (size_t)t * M * MK + 4 * e)
                    : "memory");
     }
     asm volatile("cp.async.commit_group;\n" ::: "memory");

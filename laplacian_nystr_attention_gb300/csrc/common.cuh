@@ -49,8 +49,9 @@ __host__ __device__ inline int part_owner(const Partition& pt, long long x) {
 struct WorkspaceLayout {
   size_t landmarks;    // [BH, m, d]         pooled keys L
   size_t x;            // [BH, m, m]         Newton-Schulz result X
-  size_t xs;           // [BH, T + 1, m, m]  every Newton-Schulz iterate X_0 .. X_T (kept
-                       //                    for the backward pass; Newton-Schulz plans only)
+  size_t xs;           // [BH, T + 1, m, mk] every Newton-Schulz iterate X_0 .. X_T, rows
+                       //                    padded to mk = 4 ceil(m / 4) (kept for the
+                       //                    backward pass; Newton-Schulz plans only)
   size_t at;           // [BH, m, N]         A = k(Q, L), landmark-major (A transposed)
   size_t bt;           // [BH, m, N]         B = k(L, K)
   size_t bvp;          // [BH, bv_splits, m, d]  per-split partial sums of B V

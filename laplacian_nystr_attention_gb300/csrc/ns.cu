@@ -61,14 +61,14 @@ ns_inverse_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
   float* P = sm.P;
   float* Y = sm.Y;
   float* part = sm.part;
-  float* xsh = xs ? xs + (size_t)bh * (T + 1) * M * M : nullptr;
+  float* xsh = xs ? xs + (size_t)bh * (T + 1) * M * Sh::MK : nullptr;
 
   save_iterate<M, kNsThreads>(X, xsh);
   for (int t = 0; t < T; ++t) {
     sym_product<Sh::MK, Sh::NWT, kPlain>(W, X, nullptr, P, part);   // P = W X
     sym_product<Sh::MK, Sh::NWT, kAvgUpdate>(X, P, X, Y, part);          // Y = 2X - X P
     float* tmp = X; X = Y; Y = tmp;
-    save_iterate<M, kNsThreads>(X, xsh ? xsh + (size_t)(t + 1) * M * M : nullptr);
+    save_iterate<M, kNsThreads>(X, xsh ? xsh + (size_t)(t + 1) * M * Sh::MK : nullptr);
   }
 
   for (int idx = threadIdx.x; idx < M * M; idx += kNsThreads) {
@@ -209,7 +209,7 @@ ns_pair_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
   float* Xp = cluster.map_shared_rank(sm.X, crank ^ 1);
   float* Pp = cluster.map_shared_rank(sm.P, crank ^ 1);
   cluster.sync();                  // the peer is running before anything is stored into it
-  float* xsh = (xs && crank == 0) ? xs + (size_t)bh * (T + 1) * M * M : nullptr;
+  float* xsh = (xs && crank == 0) ? xs + (size_t)bh * (T + 1) * M * Sh::MK : nullptr;
   save_iterate<M, kNsThreads>(X, xsh);
 
   for (int t = 0; t < T; ++t) {
@@ -222,7 +222,7 @@ ns_pair_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
     pair_symmetrise<M>(Y);                                                // Y = (V + V^T) / 2
     float* tmp = X; X = Y; Y = tmp;
     tmp = Xp; Xp = Yp; Yp = tmp;
-    save_iterate<M, kNsThreads>(X, xsh ? xsh + (size_t)(t + 1) * M * M : nullptr);
+    save_iterate<M, kNsThreads>(X, xsh ? xsh + (size_t)(t + 1) * M * Sh::MK : nullptr);
   }
 
   // Both CTAs hold the final X; each writes half of it.

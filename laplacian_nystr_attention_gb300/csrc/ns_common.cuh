@@ -288,12 +288,18 @@ __device__ __forceinline__ void sym_product(const float* __restrict__ A,
   __syncthreads();
 }
 
-// Copy the M x M block of X (row stride kMS) to dst, row-major, with the CTA's NT threads (the
-// iterates the backward pass runs through).  Nothing when dst is null.
+// Copy the first M rows of X (row stride kMS) to dst as M rows of MK = 4 ceil(M / 4) floats
+// (the columns past M are X's zero padding), one float4 per thread and step, with the CTA's
+// NT threads: the iterates the backward pass runs through.  Nothing when dst is null.
 template <int M, int NT>
 __device__ __forceinline__ void save_iterate(const float* __restrict__ X, float* __restrict__ dst) {
   if (!dst) return;
-  for (int e = threadIdx.x; e < M * M; e += NT) dst[e] = X[(e / M) * kMS + e % M];
+  constexpr int Q = (M + 3) / 4;            // float4 per row
+  for (int e = threadIdx.x; e < M * Q; e += NT) {
+    const int r = e / Q, c4 = e - r * Q;
+    *reinterpret_cast<float4*>(&dst[(r * Q + c4) * 4]) =
+        *reinterpret_cast<const float4*>(&X[r * kMS + 4 * c4]);
+  }
 }
 
 }  // namespace ns_detail

@@ -267,12 +267,12 @@ ns_tc_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
 
   unsigned phase = 0;
   bool ok = true;
-  float* xsh = xs ? xs + (size_t)bh * (T + 1) * M * M : nullptr;
+  float* xsh = xs ? xs + (size_t)bh * (T + 1) * M * Sh::MK : nullptr;
   for (int t = 0; t < T && ok; ++t) {
     // ---- P^T = X W ----
     if (threadIdx.x == 0) issue_product(tmem, xx_a, ww_a, KSTEPS, bar_a);
     // X_t is kept for the backward pass while the tensor cores work (they read XX, not Xf).
-    save_iterate<M, kTcThreads>(Xf, xsh ? xsh + (size_t)t * M * M : nullptr);
+    save_iterate<M, kTcThreads>(Xf, xsh ? xsh + (size_t)t * M * Sh::MK : nullptr);
     ok = wait_product(bar_a, phase);
     phase ^= 1;
     if (!ok) break;
@@ -326,7 +326,7 @@ ns_tc_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
     __syncthreads();
     tc_fence_after();
   }
-  if (ok) save_iterate<M, kTcThreads>(Xf, xsh ? xsh + (size_t)T * M * M : nullptr);
+  if (ok) save_iterate<M, kTcThreads>(Xf, xsh ? xsh + (size_t)T * M * Sh::MK : nullptr);
 
   if (!ok) {
     if (threadIdx.x == 0) atomicOr(err, kErrTimeout);

@@ -48,7 +48,7 @@ def gpu_backward(w, q, k, v, G, bias=None, **over):
     dq_, dk_, dv_ = (to_device(x, cfg["in_dtype"]) for x in (q, k, v))
     db = None if bias is None else torch.from_numpy(np.asarray(bias, np.float32)).cuda()
     dG = torch.from_numpy(np.ascontiguousarray(G, np.float32)).cuda()
-    att.forward(dq_, dk_, dv_, bias=db)
+    att.forward(dq_, dk_, dv_, bias=db, keep_for_backward=True)
     gq, gk, gv, gb = att.backward(dq_, dk_, dv_, dG, bias=db)
     torch.cuda.synchronize()
     res = tuple(t.cpu().numpy().astype(np.float64) for t in (gq, gk, gv, gb))
@@ -203,4 +203,19 @@ def test_unsupported_with_cg_and_errors():
     assert L.lapl_attn_backward(att.handle, p + 4, p, p, None, p, p, p, p, None,
                                 att.workspace.data_ptr(), att.workspace_bytes, ws.data_ptr(),
                                 nbytes, st) == _lib.LAPL_ERR_ALIGNMENT
+    att.close()
+
+
+def test_training_forward_same_output_and_backward_needs_it():
+    import torch
+    import laplacian_nystr_attention_gb300 as lna
+    w = WORKLOADS["stage1_f32"].replace(batch=1)
+    q, k, v = (to_device(x, "f32") for x in make_inputs(w))
+    att = lna.LaplacianNystromAttention(lna.make_config(**w.config()))
+    a = att.forward(q, k, v).clone()
+    with pytest.raises(RuntimeError):
+        att.backward(q, k, v, torch.zeros_like(q))
+    b = att.forward(q, k, v, keep_for_backward=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
     att.close()
