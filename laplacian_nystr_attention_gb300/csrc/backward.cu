@@ -50,7 +50,15 @@ __device__ __forceinline__ float load_in(const void* p, size_t e, bool bf16) {
 }
 
 // ---- dA^ = G M^T and the partial reductions over one token split -----------------------
-__global__ void __launch_bounds__(kBwdThreads)
+// 512 threads, register tiles of 4 x 4 outputs over float4 operands in shared memory:
+//   dA^[j][t]: warp w owns landmark quad w (w < m / 4), lane l tokens l, l + 32, l + 64,
+//     l + 96 (rows a lane-stride apart: the eight lanes of a quarter-warp hit distinct banks;
+//     the landmark rows are warp-wide broadcasts); the channels run in quads;
+//   dM[j][c] += sum_t (Z[j][t] + beta_j) G[t][c]: thread (landmark quad, channel quad, token
+//     class), token quads of its class, classes summed in order at the end.
+constexpr int kAhatThreads = 512;
+
+__global__ void __launch_bounds__(kAhatThreads)
 bwd_ahat_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
                 const float* __restrict__ mu, const float* __restrict__ rstd,
                 const float* __restrict__ bias, const float* __restrict__ gout,
@@ -59,87 +67,148 @@ bwd_ahat_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
                 int splits, int whiten) {
   extern __shared__ float4 smem_a4[];
   float* smem = reinterpret_cast<float*>(smem_a4);
-  const int dp = d + 1, tp = kBwdTile + 1;
-  float* sM = smem;                       // [m][d + 1]
-  float* sG = sM + m * dp;                // [tile][d + 1]
-  float* sZ = sG + kBwdTile * dp;         // [m][tile + 1]   Z (whitened, no bias) or A
-  float* sD = sZ + m * tp;                // [m][tile + 1]   dA^
-  float* sc = sD + m * tp;                // mu, r, beta [3][m]
+  const int mp4 = (m + 3) & ~3;
+  const int dq = d + 4, tq = kBwdTile + 4;     // padded row lengths (multiples of 4)
+  float* sM = smem;                            // [mp4][d + 4]
+  float* sG = sM + mp4 * dq;                   // [tile][d + 4]  token-major
+  float* sZ = sG + kBwdTile * dq;              // [mp4][tile + 4] Z + beta (A^ without the bias
+                                               //                 when whitening is off: A)
+  float* sD = sZ + mp4 * tq;                   // [mp4][tile + 4] dA^
+  float* sc = sD + mp4 * tq;                   // mu, r, beta [3][mp4]
+  float* red = sG;                             // [16][threads] after the last tile
   const long bh = blockIdx.x / splits;
   const int sp = blockIdx.x % splits;
   const int h = (int)(bh % heads);
-  for (int i = threadIdx.x; i < m * d; i += kBwdThreads)
-    sM[(i / d) * dp + i % d] = mmat[(size_t)bh * m * d + i];
-  for (int j = threadIdx.x; j < m; j += kBwdThreads) {
-    sc[j] = mu[(size_t)bh * m + j];
-    sc[m + j] = rstd[(size_t)bh * m + j];
-    sc[2 * m + j] = (whiten && bias) ? bias[(size_t)h * m + j] : 0.f;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < mp4 * d; i += kAhatThreads) {
+    const int j = i / d, c = i % d;
+    sM[j * dq + c] = j < m ? mmat[((size_t)bh * m + j) * d + c] : 0.f;
   }
-  float s1 = 0.f, s2 = 0.f;
-  float acc[kMaxPairs];
+  for (int j = tid; j < mp4; j += kAhatThreads) {
+    sc[j] = j < m ? mu[(size_t)bh * m + j] : 0.f;
+    sc[mp4 + j] = j < m ? rstd[(size_t)bh * m + j] : 0.f;
+    sc[2 * mp4 + j] = (j < m && whiten && bias) ? bias[(size_t)h * m + j] : 0.f;
+  }
+  // dM thread slots: (landmark quad lg, channel quad cq), KS token classes.
+  const int cqn = d >> 2, set = (mp4 >> 2) * cqn;
+  const int KS = max(1, kAhatThreads / set);
+  const int ks = tid / set, lg = (tid % set) / cqn, cq = tid % cqn;
+  const bool on = ks < KS;
+  float acc[4][4];
 #pragma unroll
-  for (int u = 0; u < kMaxPairs; ++u) acc[u] = 0.f;
-  const int pairs = m * d;
-  const int t0 = sp * tiles_per_split;
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+  float s1 = 0.f, s2 = 0.f;
   const int tiles = (n + kBwdTile - 1) / kBwdTile;
-  const int t1 = min(tiles, t0 + tiles_per_split);
+  const int t0 = sp * tiles_per_split, t1 = min(tiles, t0 + tiles_per_split);
   __syncthreads();
   for (int t = t0; t < t1; ++t) {
     const int n0 = t * kBwdTile;
-    for (int i = threadIdx.x; i < m * kBwdTile; i += kBwdThreads) {
+    for (int i = tid; i < mp4 * kBwdTile; i += kAhatThreads) {
       const int j = i / kBwdTile, tt = i % kBwdTile, tok = n0 + tt;
       float z = 0.f;
-      if (tok < n) {
+      if (tok < n && j < m) {
         const float a = at[((size_t)bh * m + j) * n + tok];
-        z = whiten ? (a - sc[j]) * sc[m + j] : a;
+        z = whiten ? (a - sc[j]) * sc[mp4 + j] : a;
       }
-      sZ[j * tp + tt] = z;
+      sZ[j * tq + tt] = z;
     }
-    for (int i = threadIdx.x; i < kBwdTile * d; i += kBwdThreads) {
-      const int tt = i / d, c = i % d, tok = n0 + tt;
-      sG[tt * dp + c] = tok < n ? gout[((size_t)bh * n + tok) * d + c] : 0.f;
+    for (int i = tid; i < kBwdTile * cqn; i += kAhatThreads) {
+      const int tt = i / cqn, c4 = i % cqn, tok = n0 + tt;
+      const float4 g = tok < n ? *reinterpret_cast<const float4*>(&gout[((size_t)bh * n + tok) * d + 4 * c4])
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(&sG[tt * dq + 4 * c4]) = g;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < m * kBwdTile; i += kBwdThreads) {
-      const int j = i / kBwdTile, tt = i % kBwdTile, tok = n0 + tt;
-      float v = 0.f;
-      for (int c = 0; c < d; ++c) v = fmaf(sG[tt * dp + c], sM[j * dp + c], v);
-      sD[j * tp + tt] = v;
-      if (tok < n) dahat[((size_t)bh * m + j) * n + tok] = v;
-    }
-    __syncthreads();
-    if (threadIdx.x < m) {
-      const int j = threadIdx.x;
-      for (int tt = 0; tt < kBwdTile; ++tt) {
-        const float v = sD[j * tp + tt];
-        s1 += v;
-        s2 = fmaf(v, sZ[j * tp + tt], s2);
-      }
-    }
+    // dA^ = G M^T
+    for (int lq = warp; lq < (mp4 >> 2); lq += kAhatThreads / 32) {
+      float o[4][4];
 #pragma unroll
-    for (int u = 0; u < kMaxPairs; ++u) {
-      const int p = threadIdx.x + kBwdThreads * u;
-      if (p < pairs) {
-        const int j = p / d, c = p % d;
-        const float beta = sc[2 * m + j];
-        float a = acc[u];
-        for (int tt = 0; tt < kBwdTile; ++tt)
-          a = fmaf(sZ[j * tp + tt] + beta, sG[tt * dp + c], a);
-        acc[u] = a;
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) o[a][b] = 0.f;
+      for (int c4 = 0; c4 < cqn; ++c4) {
+        float4 g[4], mv[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) g[b] = *reinterpret_cast<const float4*>(&sG[(lane + 32 * b) * dq + 4 * c4]);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) mv[a] = *reinterpret_cast<const float4*>(&sM[(4 * lq + a) * dq + 4 * c4]);
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            o[a][b] = fmaf(g[b].x, mv[a].x, o[a][b]);
+            o[a][b] = fmaf(g[b].y, mv[a].y, o[a][b]);
+            o[a][b] = fmaf(g[b].z, mv[a].z, o[a][b]);
+            o[a][b] = fmaf(g[b].w, mv[a].w, o[a][b]);
+          }
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const int j = 4 * lq + a;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int tt = lane + 32 * b, tok = n0 + tt;
+          sD[j * tq + tt] = o[a][b];
+          if (j < m && tok < n) dahat[((size_t)bh * m + j) * n + tok] = o[a][b];
+        }
+      }
+    }
+    // dM partial: sum over the tile's token quads of this thread's class
+    if (on) {
+      for (int q = ks; q < kBwdTile / 4; q += KS) {
+        const int tt = 4 * q;
+        float4 z4[4], g4[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float beta = sc[2 * mp4 + 4 * lg + r];
+          const float4 zz = *reinterpret_cast<const float4*>(&sZ[(4 * lg + r) * tq + tt]);
+          z4[r] = make_float4(zz.x + beta, zz.y + beta, zz.z + beta, zz.w + beta);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) g4[u] = *reinterpret_cast<const float4*>(&sG[(tt + u) * dq + 4 * cq]);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float zu[4] = {z4[r].x, z4[r].y, z4[r].z, z4[r].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            acc[r][0] = fmaf(zu[u], g4[u].x, acc[r][0]);
+            acc[r][1] = fmaf(zu[u], g4[u].y, acc[r][1]);
+            acc[r][2] = fmaf(zu[u], g4[u].z, acc[r][2]);
+            acc[r][3] = fmaf(zu[u], g4[u].w, acc[r][3]);
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (tid < m) {
+      for (int tt = 0; tt < kBwdTile; tt += 4) {
+        const float4 dv = *reinterpret_cast<const float4*>(&sD[tid * tq + tt]);
+        const float4 zv = *reinterpret_cast<const float4*>(&sZ[tid * tq + tt]);
+        s1 += dv.x; s1 += dv.y; s1 += dv.z; s1 += dv.w;
+        s2 = fmaf(dv.x, zv.x, s2); s2 = fmaf(dv.y, zv.y, s2);
+        s2 = fmaf(dv.z, zv.z, s2); s2 = fmaf(dv.w, zv.w, s2);
       }
     }
     __syncthreads();
   }
+  // Token classes combined in order (padding tokens contribute zeros: G is zero there).
+#pragma unroll
+  for (int e = 0; e < 16; ++e) red[e * kAhatThreads + tid] = on ? acc[e >> 2][e & 3] : 0.f;
+  __syncthreads();
   float* pdm = part_dm + ((size_t)bh * splits + sp) * m * d;
-#pragma unroll
-  for (int u = 0; u < kMaxPairs; ++u) {
-    const int p = threadIdx.x + kBwdThreads * u;
-    if (p < pairs) pdm[p] = acc[u];
+  for (int i = tid; i < m * d; i += kAhatThreads) {
+    const int j = i / d, c = i % d;
+    const int lgi = j >> 2, r = j & 3, cqi = c >> 2, cc = c & 3;
+    float sum = 0.f;
+    for (int qq = 0; qq < KS; ++qq) sum += red[(r * 4 + cc) * kAhatThreads + qq * set + lgi * cqn + cqi];
+    pdm[i] = sum;
   }
-  if (threadIdx.x < m) {
+  if (tid < m) {
     float* ps = part_s + ((size_t)bh * splits + sp) * 2 * m;
-    ps[threadIdx.x] = s1;
-    ps[m + threadIdx.x] = s2;
+    ps[tid] = s1;
+    ps[m + tid] = s2;
   }
 }
 
@@ -339,24 +408,30 @@ bwd_ns_kernel(const float* __restrict__ landmarks, const float* __restrict__ xs,
 }
 
 // ---- query side: g = -(A / lambda) dA, dQ ------------------------------------------------
-template <bool kGauss>
+// One CTA (512 threads) per (head, 128-token tile): g for the tile (stored), then thread
+// (token quad, channel quad) runs over the landmarks with g (float4 over its tokens) and L
+// (float4 over its channels) for 16 dQ entries.
+template <bool kGauss, int TU>
 __global__ void __launch_bounds__(512)
 bwd_query_kernel(const void* __restrict__ q, const float* __restrict__ at,
                  const float* __restrict__ dahat, const float* __restrict__ mu,
                  const float* __restrict__ rstd, const float* __restrict__ s12,
                  const float* __restrict__ landmarks, float* __restrict__ gq,
-                 float* __restrict__ dq, int m, int d, int n, float lam, int whiten, int tpc,
-                 int tiles, int bf16) {
+                 float* __restrict__ dq, int m, int d, int n, float lam, int whiten, int tiles,
+                 int bf16) {
   extern __shared__ float4 smem_q4[];
   float* smem = reinterpret_cast<float*>(smem_q4);
-  float* sL = smem;                    // [m][d]
-  float* sg = sL + m * d;              // [m][tpc]
+  const int dq4 = d + 4, tq = kBwdTile + 4;
+  float* sL = smem;                    // [m][d + 4]
+  float* sg = sL + m * dq4;            // [m][tile + 4]
   const long bh = blockIdx.x / tiles;
-  const int n0 = (blockIdx.x % tiles) * tpc;
-  for (int i = threadIdx.x; i < m * d; i += blockDim.x) sL[i] = landmarks[(size_t)bh * m * d + i];
+  const int n0 = (blockIdx.x % tiles) * kBwdTile;
+  const int tid = threadIdx.x;
+  const int cqn = d >> 2;
+  for (int i = tid; i < m * d; i += 512) sL[(i / d) * dq4 + i % d] = landmarks[(size_t)bh * m * d + i];
   const float inv_n = 1.f / (float)n;
-  for (int i = threadIdx.x; i < m * tpc; i += blockDim.x) {
-    const int j = i / tpc, tt = i % tpc, tok = n0 + tt;
+  for (int i = tid; i < m * kBwdTile; i += 512) {
+    const int j = i / kBwdTile, tt = i % kBwdTile, tok = n0 + tt;
     float g = 0.f;
     if (tok < n) {
       const size_t o = ((size_t)bh * m + j) * n + tok;
@@ -371,99 +446,169 @@ bwd_query_kernel(const void* __restrict__ q, const float* __restrict__ at,
       g = -a / lam * da;
       gq[o] = g;
     }
-    sg[j * tpc + tt] = g;
+    sg[j * tq + tt] = g;
   }
   __syncthreads();
-  const int groups = d >> 3;
-  const int tt = threadIdx.x / groups, c0 = (threadIdx.x % groups) * 8, tok = n0 + tt;
-  if (tt >= tpc || tok >= n) return;
-  float x[8], acc[8];
-  const size_t row = ((size_t)bh * n + tok) * d + c0;
+  for (int slot = tid; slot < (kBwdTile / TU) * cqn; slot += 512) {
+    const int c4 = slot % cqn, t0 = TU * (slot / cqn);
+    float x[TU][4], acc[TU][4];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    x[c] = load_in(q, row + c, bf16 != 0);
-    acc[c] = 0.f;
-  }
-  for (int j = 0; j < m; ++j) {
-    const float g = sg[j * tpc + tt];
-    const float* l = sL + j * d + c0;
+    for (int u = 0; u < TU; ++u) {
+      const int tok = n0 + t0 + u;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) acc[c] = fmaf(g, slope<kGauss>(x[c], l[c]), acc[c]);
+      for (int c = 0; c < 4; ++c) {
+        x[u][c] = tok < n ? load_in(q, ((size_t)bh * n + tok) * d + 4 * c4 + c, bf16 != 0) : 0.f;
+        acc[u][c] = 0.f;
+      }
+    }
+    for (int jj = 0; jj < m; ++jj) {
+      float gg[TU];
+      if constexpr (TU == 4) {
+        const float4 g4 = *reinterpret_cast<const float4*>(&sg[jj * tq + t0]);
+        gg[0] = g4.x; gg[1] = g4.y; gg[2] = g4.z; gg[3] = g4.w;
+      } else {
+        const float2 g2 = *reinterpret_cast<const float2*>(&sg[jj * tq + t0]);
+        gg[0] = g2.x; gg[1] = g2.y;
+      }
+      const float4 l4 = *reinterpret_cast<const float4*>(&sL[jj * dq4 + 4 * c4]);
+      const float ll[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+      for (int u = 0; u < TU; ++u)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[u][c] = fmaf(gg[u], slope<kGauss>(x[u][c], ll[c]), acc[u][c]);
+    }
+#pragma unroll
+    for (int u = 0; u < TU; ++u) {
+      const int tok = n0 + t0 + u;
+      if (tok < n)
+        *reinterpret_cast<float4*>(dq + ((size_t)bh * n + tok) * d + 4 * c4) =
+            make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+    }
   }
-  float4* out = reinterpret_cast<float4*>(dq + row);
-  out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
 // ---- key side: h = -(B / lambda) (dBV V^T), dK's distance term, dV = B^T dBV --------------
-template <bool kGauss>
+// One CTA (512 threads) per (head, 128-token tile).  dB = dBV V^T on 4 x 4 register tiles as in
+// bwd_ahat_kernel; then thread (token quad, channel quad) runs over the landmarks with h, B
+// (float4 over its tokens) and L, dBV (float4 over its channels) for 16 dK and 16 dV entries.
+template <bool kGauss, int TU>
 __global__ void __launch_bounds__(512)
 bwd_key_kernel(const void* __restrict__ k, const void* __restrict__ v,
                const float* __restrict__ bt, const float* __restrict__ dbv,
                const float* __restrict__ landmarks, float* __restrict__ hk,
                float* __restrict__ dk, float* __restrict__ dv, int m, int d, int n, float lam,
-               int tpc, int tiles, int bf16) {
+               int tiles, int bf16) {
   extern __shared__ float4 smem_k4[];
   float* smem = reinterpret_cast<float*>(smem_k4);
-  const int dp = d + 1;
-  float* sL = smem;                    // [m][d]
-  float* sdBV = sL + m * d;            // [m][d]
-  float* sV = sdBV + m * d;            // [tpc][d + 1]
-  float* sh = sV + tpc * dp;           // [m][tpc]
-  float* sB = sh + m * tpc;            // [m][tpc]
+  const int mp4 = (m + 3) & ~3;
+  const int dq = d + 4, tq = kBwdTile + 4;
+  float* sL = smem;                    // [mp4][d + 4]
+  float* sW = sL + mp4 * dq;           // [mp4][d + 4]  dBV
+  float* sV = sW + mp4 * dq;           // [tile][d + 4]
+  float* sh = sV + kBwdTile * dq;      // [mp4][tile + 4]
+  float* sB = sh + mp4 * tq;           // [mp4][tile + 4]
   const long bh = blockIdx.x / tiles;
-  const int n0 = (blockIdx.x % tiles) * tpc;
-  for (int i = threadIdx.x; i < m * d; i += blockDim.x) {
-    sL[i] = landmarks[(size_t)bh * m * d + i];
-    sdBV[i] = dbv[(size_t)bh * m * d + i];
+  const int n0 = (blockIdx.x % tiles) * kBwdTile;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cqn = d >> 2;
+  for (int i = tid; i < mp4 * d; i += 512) {
+    const int j = i / d, c = i % d;
+    sL[j * dq + c] = j < m ? landmarks[((size_t)bh * m + j) * d + c] : 0.f;
+    sW[j * dq + c] = j < m ? dbv[((size_t)bh * m + j) * d + c] : 0.f;
   }
-  for (int i = threadIdx.x; i < tpc * d; i += blockDim.x) {
+  for (int i = tid; i < kBwdTile * d; i += 512) {
     const int tt = i / d, c = i % d, tok = n0 + tt;
-    sV[tt * dp + c] = tok < n ? load_in(v, ((size_t)bh * n + tok) * d + c, bf16 != 0) : 0.f;
+    sV[tt * dq + c] = tok < n ? load_in(v, ((size_t)bh * n + tok) * d + c, bf16 != 0) : 0.f;
+  }
+  for (int i = tid; i < mp4 * kBwdTile; i += 512) {
+    const int j = i / kBwdTile, tt = i % kBwdTile, tok = n0 + tt;
+    sB[j * tq + tt] = (j < m && tok < n) ? bt[((size_t)bh * m + j) * n + tok] : 0.f;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < m * tpc; i += blockDim.x) {
-    const int j = i / tpc, tt = i % tpc, tok = n0 + tt;
-    float h = 0.f, b = 0.f;
-    if (tok < n) {
-      const size_t o = ((size_t)bh * m + j) * n + tok;
-      b = bt[o];
-      float db = 0.f;
-      for (int c = 0; c < d; ++c) db = fmaf(sdBV[j * d + c], sV[tt * dp + c], db);
-      h = -b / lam * db;
-      hk[o] = h;
+  // h = -(B / lambda) (dBV V^T): warp w landmark quad w, lane l tokens l + 32 b
+  for (int lq = warp; lq < (mp4 >> 2); lq += 16) {
+    float o[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) o[a][b] = 0.f;
+    for (int c4 = 0; c4 < cqn; ++c4) {
+      float4 vv[4], wv[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) vv[b] = *reinterpret_cast<const float4*>(&sV[(lane + 32 * b) * dq + 4 * c4]);
+#pragma unroll
+      for (int a = 0; a < 4; ++a) wv[a] = *reinterpret_cast<const float4*>(&sW[(4 * lq + a) * dq + 4 * c4]);
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          o[a][b] = fmaf(wv[a].x, vv[b].x, o[a][b]);
+          o[a][b] = fmaf(wv[a].y, vv[b].y, o[a][b]);
+          o[a][b] = fmaf(wv[a].z, vv[b].z, o[a][b]);
+          o[a][b] = fmaf(wv[a].w, vv[b].w, o[a][b]);
+        }
     }
-    sh[j * tpc + tt] = h;
-    sB[j * tpc + tt] = b;
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int j = 4 * lq + a;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int tt = lane + 32 * b, tok = n0 + tt;
+        const float h = -sB[j * tq + tt] / lam * o[a][b];
+        sh[j * tq + tt] = h;
+        if (j < m && tok < n) hk[((size_t)bh * m + j) * n + tok] = h;
+      }
+    }
   }
   __syncthreads();
-  const int groups = d >> 3;
-  const int tt = threadIdx.x / groups, c0 = (threadIdx.x % groups) * 8, tok = n0 + tt;
-  if (tt >= tpc || tok >= n) return;
-  float x[8], gk[8], gv[8];
-  const size_t row = ((size_t)bh * n + tok) * d + c0;
+  for (int slot = tid; slot < (kBwdTile / TU) * cqn; slot += 512) {
+    const int c4 = slot % cqn;
+    const int t0 = TU * (slot / cqn);
+    float x[TU][4], gk[TU][4], gv[TU][4];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    x[c] = load_in(k, row + c, bf16 != 0);
-    gk[c] = 0.f;
-    gv[c] = 0.f;
-  }
-  for (int j = 0; j < m; ++j) {
-    const float h = sh[j * tpc + tt], b = sB[j * tpc + tt];
-    const float* l = sL + j * d + c0;
-    const float* w = sdBV + j * d + c0;
+    for (int u = 0; u < TU; ++u) {
+      const int tok = n0 + t0 + u;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      gk[c] = fmaf(-h, slope<kGauss>(l[c], x[c]), gk[c]);
-      gv[c] = fmaf(b, w[c], gv[c]);
+      for (int c = 0; c < 4; ++c) {
+        x[u][c] = tok < n ? load_in(k, ((size_t)bh * n + tok) * d + 4 * c4 + c, bf16 != 0) : 0.f;
+        gk[u][c] = 0.f;
+        gv[u][c] = 0.f;
+      }
+    }
+    for (int j = 0; j < m; ++j) {
+      float hh[TU], bb[TU];
+      if constexpr (TU == 4) {
+        const float4 h4 = *reinterpret_cast<const float4*>(&sh[j * tq + t0]);
+        const float4 b4 = *reinterpret_cast<const float4*>(&sB[j * tq + t0]);
+        hh[0] = h4.x; hh[1] = h4.y; hh[2] = h4.z; hh[3] = h4.w;
+        bb[0] = b4.x; bb[1] = b4.y; bb[2] = b4.z; bb[3] = b4.w;
+      } else {
+        const float2 h2 = *reinterpret_cast<const float2*>(&sh[j * tq + t0]);
+        const float2 b2 = *reinterpret_cast<const float2*>(&sB[j * tq + t0]);
+        hh[0] = h2.x; hh[1] = h2.y;
+        bb[0] = b2.x; bb[1] = b2.y;
+      }
+      const float4 l4 = *reinterpret_cast<const float4*>(&sL[j * dq + 4 * c4]);
+      const float4 w4 = *reinterpret_cast<const float4*>(&sW[j * dq + 4 * c4]);
+      const float ll[4] = {l4.x, l4.y, l4.z, l4.w}, ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+      for (int u = 0; u < TU; ++u)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          gk[u][c] = fmaf(-hh[u], slope<kGauss>(ll[c], x[u][c]), gk[u][c]);
+          gv[u][c] = fmaf(bb[u], ww[c], gv[u][c]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < TU; ++u) {
+      const int tok = n0 + t0 + u;
+      if (tok < n) {
+        const size_t row = ((size_t)bh * n + tok) * d + 4 * c4;
+        *reinterpret_cast<float4*>(dk + row) = make_float4(gk[u][0], gk[u][1], gk[u][2], gk[u][3]);
+        *reinterpret_cast<float4*>(dv + row) = make_float4(gv[u][0], gv[u][1], gv[u][2], gv[u][3]);
+      }
     }
   }
-  float4* ok = reinterpret_cast<float4*>(dk + row);
-  ok[0] = make_float4(gk[0], gk[1], gk[2], gk[3]);
-  ok[1] = make_float4(gk[4], gk[5], gk[6], gk[7]);
-  float4* ov = reinterpret_cast<float4*>(dv + row);
-  ov[0] = make_float4(gv[0], gv[1], gv[2], gv[3]);
-  ov[1] = make_float4(gv[4], gv[5], gv[6], gv[7]);
 }
 
 // ---- partials of dL over one token split: side 0 from the query block, 1 from the key block --
@@ -623,23 +768,25 @@ const void* pick_ns_bwd(int s) {
   }
 }
 
-int token_tile(int d) {
-  const int groups = d / 8;
-  int t = 512 / groups;
-  return t > kBwdTile ? kBwdTile : t;
-}
 
 size_t ahat_smem(int m, int d) {
-  return sizeof(float) * ((size_t)m * (d + 1) + (size_t)kBwdTile * (d + 1) +
-                          2 * (size_t)m * (kBwdTile + 1) + 3 * (size_t)m);
+  const size_t mp4 = (m + 3) & ~3;
+  const size_t stage = mp4 * (d + 4) + (size_t)kBwdTile * (d + 4) + 2 * mp4 * (kBwdTile + 4) +
+                       3 * mp4;
+  const size_t red = 16 * (size_t)kAhatThreads + mp4 * (d + 4);   // red aliases sG onwards
+  return sizeof(float) * (stage > red ? stage : red);
 }
 size_t ns_bwd_smem(int d) {
   return sizeof(float) * (8 * 64 * (size_t)kMS + 4 * 3 * 32 * 32 + kRedFloats + 64 * (size_t)d);
 }
 size_t mid_smem(int m, int d) { return sizeof(float) * (2 * (size_t)m * (d + 1) + (size_t)m * m); }
-size_t query_smem(int m, int d, int tpc) { return sizeof(float) * ((size_t)m * d + (size_t)m * tpc); }
-size_t key_smem(int m, int d, int tpc) {
-  return sizeof(float) * (2 * (size_t)m * d + (size_t)tpc * (d + 1) + 2 * (size_t)m * tpc);
+size_t query_smem(int m, int d) {
+  return sizeof(float) * ((size_t)m * (d + 4) + (size_t)m * (kBwdTile + 4));
+}
+size_t key_smem(int m, int d) {
+  const size_t mp4 = (m + 3) & ~3;
+  return sizeof(float) * (2 * mp4 * (d + 4) + (size_t)kBwdTile * (d + 4) +
+                          2 * mp4 * (kBwdTile + 4));
 }
 size_t lm_smem(int m, int d) {
   return sizeof(float) * ((size_t)kBwdTile * (d + 4) + (size_t)m * (kBwdTile + 1));
@@ -675,7 +822,6 @@ BwdLayout bwd_layout(const lapl_attn_plan& p) {
 
 cudaError_t bwd_configure(const lapl_attn_plan& p) {
   const Geometry& g = p.geo;
-  const int tpc = token_tile(g.d);
   cudaError_t e = cudaFuncSetAttribute(bwd_ahat_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)ahat_smem(g.m, g.d));
   const void* hf = pick_ns_bwd(g.s);
@@ -685,12 +831,19 @@ cudaError_t bwd_configure(const lapl_attn_plan& p) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(bwd_mid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)mid_smem(g.m, g.d));
-  const int qs = (int)query_smem(g.m, g.d, tpc), ks = (int)key_smem(g.m, g.d, tpc),
+  const int qs = (int)query_smem(g.m, g.d), ks = (int)key_smem(g.m, g.d),
             ls = (int)lm_smem(g.m, g.d);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_query_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, qs);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_query_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, qs);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_key_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, ks);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_key_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, ks);
+  const void* tok_kernels[] = {
+      reinterpret_cast<const void*>(&bwd_query_kernel<false, 2>),
+      reinterpret_cast<const void*>(&bwd_query_kernel<false, 4>),
+      reinterpret_cast<const void*>(&bwd_query_kernel<true, 2>),
+      reinterpret_cast<const void*>(&bwd_query_kernel<true, 4>),
+      reinterpret_cast<const void*>(&bwd_key_kernel<false, 2>),
+      reinterpret_cast<const void*>(&bwd_key_kernel<false, 4>),
+      reinterpret_cast<const void*>(&bwd_key_kernel<true, 2>),
+      reinterpret_cast<const void*>(&bwd_key_kernel<true, 4>)};
+  for (int i = 0; i < 8 && e == cudaSuccess; ++i)
+    e = cudaFuncSetAttribute(tok_kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, i < 4 ? qs : ks);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_lm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, ls);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_lm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, ls);
   return e;
@@ -720,11 +873,9 @@ cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* 
         *dbv = W(B.dbv), *dll = W(B.dll), *dbias_bh = W(B.dbias_bh), *gq = W(B.gq),
         *hk = W(B.hk), *part_dl = W(B.part_dl), *dl = W(B.dl), *sT = W(B.st);
   const unsigned bh = (unsigned)g.bh;
-  const int tpc = token_tile(d);
-  const int qtiles = (n + tpc - 1) / tpc;
   const int ptiles = (n + kBwdTile - 1) / kBwdTile;
 
-  bwd_ahat_kernel<<<bh * splits, kBwdThreads, ahat_smem(m, d), st>>>(
+  bwd_ahat_kernel<<<bh * splits, kAhatThreads, ahat_smem(m, d), st>>>(
       At, M, mu, rstd, bias, gout, dahat, part_dm, part_s, m, d, n, heads, tps, splits, whiten);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -748,19 +899,23 @@ cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* 
     if (e == cudaSuccess) e = cudaEventRecord(p.ev_join, side);
     if (e != cudaSuccess) return e;
   }
-  const unsigned tthreads = (unsigned)(tpc * (d / 8));
+  // Tokens per thread in the token kernels: 4, or 2 when 32 token quads x d / 4 channel quads
+  // would leave threads idle.
+  const bool tu4 = (kBwdTile / 4) * (d / 4) >= 512;
+  auto launch_tok = [&](auto qk, auto kk) {
+    qk<<<bh * ptiles, 512, query_smem(m, d), st>>>(q, At, dahat, mu, rstd, s12, L, gq, dq, m, d,
+                                                   n, lam, whiten, ptiles, bf16);
+    kk<<<bh * ptiles, 512, key_smem(m, d), st>>>(k, v, Bt, dbv, L, hk, dk, dv, m, d, n, lam,
+                                                 ptiles, bf16);
+  };
   if (gauss) {
-    bwd_query_kernel<true><<<bh * qtiles, tthreads, query_smem(m, d, tpc), st>>>(
-        q, At, dahat, mu, rstd, s12, L, gq, dq, m, d, n, lam, whiten, tpc, qtiles, bf16);
-    bwd_key_kernel<true><<<bh * qtiles, tthreads, key_smem(m, d, tpc), st>>>(
-        k, v, Bt, dbv, L, hk, dk, dv, m, d, n, lam, tpc, qtiles, bf16);
+    if (tu4) launch_tok(bwd_query_kernel<true, 4>, bwd_key_kernel<true, 4>);
+    else launch_tok(bwd_query_kernel<true, 2>, bwd_key_kernel<true, 2>);
     bwd_lm_kernel<true><<<bh * splits * 2, kBwdThreads, lm_smem(m, d), st>>>(
         q, k, gq, hk, L, part_dl, m, d, n, tps, splits, bf16);
   } else {
-    bwd_query_kernel<false><<<bh * qtiles, tthreads, query_smem(m, d, tpc), st>>>(
-        q, At, dahat, mu, rstd, s12, L, gq, dq, m, d, n, lam, whiten, tpc, qtiles, bf16);
-    bwd_key_kernel<false><<<bh * qtiles, tthreads, key_smem(m, d, tpc), st>>>(
-        k, v, Bt, dbv, L, hk, dk, dv, m, d, n, lam, tpc, qtiles, bf16);
+    if (tu4) launch_tok(bwd_query_kernel<false, 4>, bwd_key_kernel<false, 4>);
+    else launch_tok(bwd_query_kernel<false, 2>, bwd_key_kernel<false, 2>);
     bwd_lm_kernel<false><<<bh * splits * 2, kBwdThreads, lm_smem(m, d), st>>>(
         q, k, gq, hk, L, part_dl, m, d, n, tps, splits, bf16);
   }
