@@ -11,12 +11,15 @@ Prints one JSON line (rank 0).  Multi-GPU (torchrun): every rank runs its own co
 workload (independent (batch, head) slices, no data-path collective): weak scaling.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
-                  [--kernel laplacian|gaussian] [--solver newton_schulz|cg]
+                  [--kernel laplacian|gaussian] [--solver newton_schulz|cg] [--backward]
 
 --kernel gaussian runs the same pipeline with the Gaussian kernel exp(-|x - y|_2^2 / lambda)
 in place of the Laplacian one (the softmax-free baseline the method is set against).
 --solver cg replaces the Newton-Schulz inverse by T conjugate-gradient iterations on
 W M = B V (the solver the method is compared with).
+--backward times a training step instead: lapl_attn_forward_train followed by
+lapl_attn_backward for a fixed synthetic dLoss/dO (its own metric line; the forward line
+above is the headline).
 """
 from __future__ import annotations
 
@@ -93,6 +96,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time forward (keeping the backward's state) + backward instead")
     return ap.parse_args()
 
 
@@ -488,11 +493,102 @@ def run_ours(args, w):
         tdist.destroy_process_group()
 
 
+METRIC_BWD = "Laplacian-Nyström attn fwd+bwd tokens/s on 1 GB300"
+
+
+def run_backward(args, w):
+    """Training step: forward keeping the backward's state, then the backward for a fixed
+    synthetic dLoss/dO; L2 flushed before every step; CUDA events on the launching stream."""
+    import torch
+    import torch.distributed as tdist
+
+    world, rank, local = dist_env()
+    if world > 1:
+        tdist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if not os.path.exists(os.path.join(ROOT, "laplacian_nystr_attention_gb300",
+                                       "liblapl_attn.so")):
+        import __graft_entry__
+        __graft_entry__.build()
+    import laplacian_nystr_attention_gb300 as lna
+
+    q, k, v = make_inputs(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    dq_, dk_, dv_ = (torch.from_numpy(x).to(tdt).to(dev) for x in (q, k, v))
+    gen = torch.Generator(device=dev).manual_seed(21)
+    G = torch.randn(dq_.shape, generator=gen, device=dev, dtype=torch.float32)
+    cfg = lna.make_config(**{**w.config(), "in_dtype": w.dtype, "kernel": args.kernel})
+    att = lna.LaplacianNystromAttention(cfg)
+    out = torch.empty(dq_.shape, dtype=torch.float32, device=dev)
+    grads = None
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    clean = torch.ones(CLEAN_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def flush_l2():
+        flush.zero_()
+        clean.sum()
+
+    def barrier():
+        if world > 1:
+            tdist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush_l2()
+        att.forward(dq_, dk_, dv_, out=out, keep_for_backward=True)
+        gq, gk, gv, gb = att.backward(dq_, dk_, dv_, G, grads=grads)
+        grads = dict(dq=gq, dk=gk, dv=gv, dbias=gb)
+    barrier()
+    e = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        barrier()
+        for i in range(args.steps):
+            flush_l2()
+            e[i][0].record(stream)
+            att.forward(dq_, dk_, dv_, out=out, keep_for_backward=True)
+            e[i][1].record(stream)
+            att.backward(dq_, dk_, dv_, G, grads=grads)
+            e[i][2].record(stream)
+        barrier()
+    fwd = sum(a.elapsed_time(b) for a, b, _ in e) / args.steps
+    bwd = sum(b.elapsed_time(c) for _, b, c in e) / args.steps
+    ms = max_over_ranks(fwd + bwd, world, dev)
+    launches = (lna.lapl_attn_kernels_per_forward(att.handle) +
+                lna.lapl_attn_backward_kernels(att.handle)) * args.steps
+    flags = lna.lapl_attn_device_errors(att.handle, stream.cuda_stream)
+    assert flags == 0, flags
+    if rank == 0:
+        line = {
+            "metric": METRIC_BWD, "value": job_rate(world, w.tokens, ms), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {**workload_desc(w, args.kernel),
+                       "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write, "
+                             f"then a {CLEAN_BYTES >> 20} MiB read; not timed)",
+                       "parallelism": f"replicas x{world} (independent (batch, head) slices)",
+                       "step": "lapl_attn_forward_train + lapl_attn_backward (dq, dk, dv, "
+                               "dbias for a fixed synthetic dLoss/dO)"},
+            "forward_ms": fwd, "backward_ms": bwd,
+            "memory": {"workspace_bytes": att.workspace_bytes,
+                       "backward_workspace_bytes": att.bwd_workspace_bytes},
+            "gpu_launches": launches, "clocks": clocks.summary(), "impl": "ours",
+        }
+        print(json.dumps(line), flush=True)
+    att.close()
+    if world > 1:
+        tdist.destroy_process_group()
+
+
 def main():
     args = parse()
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.backward:
+        run_backward(args, w)
     else:
         run_ours(args, w)
 
