@@ -34,10 +34,15 @@ constexpr int kBwdThreads = 256;
 constexpr int kHeadThreads = 512;
 constexpr int kMaxPairs = (kMaxM * kMaxD + kBwdThreads - 1) / kBwdThreads;   // 32
 
+// sgn(x - y) with sgn(0) = 0 as [x > y] - [x < y] (set.f32 yields 1.0 or 0.0: two compares
+// and a subtract), or 2 (x - y) for the Gaussian kernel.
 template <bool kGauss>
 __device__ __forceinline__ float slope(float x, float y) {
   if constexpr (kGauss) return 2.f * (x - y);
-  return x > y ? 1.f : (x < y ? -1.f : 0.f);
+  float gt, lt;
+  asm("set.gt.f32.f32 %0, %1, %2;" : "=f"(gt) : "f"(x), "f"(y));
+  asm("set.lt.f32.f32 %0, %1, %2;" : "=f"(lt) : "f"(x), "f"(y));
+  return gt - lt;
 }
 
 // Element e of a [.., d] input row in fp32 or bf16.
