@@ -23,6 +23,8 @@
 //
 // The distance derivative is sgn(x - y) with sgn(0) = 0 (Laplacian kernel) or 2 (x - y)
 // (Gaussian kernel).  Reductions run in fixed orders: results are reproducible bit for bit.
+#include <algorithm>
+
 #include "ns_common.cuh"
 
 namespace lapl {
@@ -34,15 +36,20 @@ constexpr int kBwdThreads = 256;
 constexpr int kHeadThreads = 512;
 constexpr int kMaxPairs = (kMaxM * kMaxD + kBwdThreads - 1) / kBwdThreads;   // 32
 
-// sgn(x - y) with sgn(0) = 0 as [x > y] - [x < y] (set.f32 yields 1.0 or 0.0: two compares
-// and a subtract), or 2 (x - y) for the Gaussian kernel.
-template <bool kGauss>
-__device__ __forceinline__ float slope(float x, float y) {
-  if constexpr (kGauss) return 2.f * (x - y);
-  float gt, lt;
-  asm("set.gt.f32.f32 %0, %1, %2;" : "=f"(gt) : "f"(x), "f"(y));
-  asm("set.lt.f32.f32 %0, %1, %2;" : "=f"(lt) : "f"(x), "f"(y));
-  return gt - lt;
+// The Gaussian kernel's distance slope d(x - y)^2 / dx.
+__device__ __forceinline__ float gauss_slope(float x, float y) { return 2.f * (x - y); }
+
+// The Laplacian kernel's sign on the multiply-add pipe.  With nc2 = -c 2^24,
+//   step(x, nc2) = [x > c] + [x == c] / 2, exactly 0, 1/2 or 1,
+// so that sgn(x - c) = 2 step - 1.  x - c is a multiple of 2^-149, so (x - c) 2^24, rounded
+// once by the first multiply-add, is zero exactly when x == c and at least 2^-125 in magnitude
+// otherwise (and keeps its sign); the second scales that to at least 1 in magnitude, adds 1/2
+// and saturates to [0, 1].  Exact for all finite x and |c| < 2^104, denormals included (no flush
+// to zero).  Three multiply-adds per element in all, against two compares, a subtract and a
+// multiply-add for [x > c] - [x < c]; the weights' sum supplies the -1.
+__device__ __forceinline__ float neg_scaled(float c) { return c * -0x1p24f; }
+__device__ __forceinline__ float step(float x, float nc2) {
+  return __saturatef(__fmaf_rn(__fmaf_rn(x, 0x1p24f, nc2), 0x1p125f, 0.5f));
 }
 
 // Element e of a [.., d] input row in fp32 or bf16.
@@ -434,7 +441,7 @@ bwd_query_kernel(const void* __restrict__ q, const float* __restrict__ at,
   const int tid = threadIdx.x;
   const int cqn = d >> 2;
   for (int i = tid; i < m * d; i += 512) sL[(i / d) * dq4 + i % d] = landmarks[(size_t)bh * m * d + i];
-  const float inv_n = 1.f / (float)n;
+  const float inv_n = 1.f / (float)n, inv_lam = 1.f / lam;
   for (int i = tid; i < m * kBwdTile; i += 512) {
     const int j = i / kBwdTile, tt = i % kBwdTile, tok = n0 + tt;
     float g = 0.f;
@@ -448,7 +455,7 @@ bwd_query_kernel(const void* __restrict__ q, const float* __restrict__ at,
         const float s1 = s12[(size_t)bh * 2 * m + j], s2 = s12[(size_t)bh * 2 * m + m + j];
         da = r * (dz - s1 * inv_n - z * s2 * inv_n);
       }
-      g = -a / lam * da;
+      g = -a * inv_lam * da;
       gq[o] = g;
     }
     sg[j * tq + tt] = g;
@@ -456,13 +463,17 @@ bwd_query_kernel(const void* __restrict__ q, const float* __restrict__ at,
   __syncthreads();
   for (int slot = tid; slot < (kBwdTile / TU) * cqn; slot += 512) {
     const int c4 = slot % cqn, t0 = TU * (slot / cqn);
-    float x[TU][4], acc[TU][4];
+    // Laplacian: x holds -Q 2^24, acc sums g step(L, -Q 2^24) = g ([L > Q] + [L == Q] / 2) and
+    // gs the weights: dQ = sum_j g sgn(Q - L) = gs - 2 acc.
+    float x[TU][4], acc[TU][4], gs[TU];
 #pragma unroll
     for (int u = 0; u < TU; ++u) {
       const int tok = n0 + t0 + u;
+      gs[u] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         x[u][c] = tok < n ? load_in(q, ((size_t)bh * n + tok) * d + 4 * c4 + c, bf16 != 0) : 0.f;
+        if constexpr (!kGauss) x[u][c] = neg_scaled(x[u][c]);
         acc[u][c] = 0.f;
       }
     }
@@ -478,13 +489,24 @@ bwd_query_kernel(const void* __restrict__ q, const float* __restrict__ at,
       const float4 l4 = *reinterpret_cast<const float4*>(&sL[jj * dq4 + 4 * c4]);
       const float ll[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-      for (int u = 0; u < TU; ++u)
+      for (int u = 0; u < TU; ++u) {
+        if constexpr (kGauss) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[u][c] = fmaf(gg[u], slope<kGauss>(x[u][c], ll[c]), acc[u][c]);
+          for (int c = 0; c < 4; ++c) acc[u][c] = fmaf(gg[u], gauss_slope(x[u][c], ll[c]), acc[u][c]);
+        } else {
+          gs[u] += gg[u];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[u][c] = fmaf(gg[u], step(ll[c], x[u][c]), acc[u][c]);
+        }
+      }
     }
 #pragma unroll
     for (int u = 0; u < TU; ++u) {
       const int tok = n0 + t0 + u;
+      if constexpr (!kGauss) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[u][c] = fmaf(-2.f, acc[u][c], gs[u]);
+      }
       if (tok < n)
         *reinterpret_cast<float4*>(dq + ((size_t)bh * n + tok) * d + 4 * c4) =
             make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
@@ -531,6 +553,7 @@ bwd_key_kernel(const void* __restrict__ k, const void* __restrict__ v,
   }
   __syncthreads();
   // h = -(B / lambda) (dBV V^T): warp w landmark quad w, lane l tokens l + 32 b
+  const float inv_lam = 1.f / lam;
   for (int lq = warp; lq < (mp4 >> 2); lq += 16) {
     float o[4][4];
 #pragma unroll
@@ -559,7 +582,7 @@ bwd_key_kernel(const void* __restrict__ k, const void* __restrict__ v,
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         const int tt = lane + 32 * b, tok = n0 + tt;
-        const float h = -sB[j * tq + tt] / lam * o[a][b];
+        const float h = -sB[j * tq + tt] * inv_lam * o[a][b];
         sh[j * tq + tt] = h;
         if (j < m && tok < n) hk[((size_t)bh * m + j) * n + tok] = h;
       }
@@ -569,13 +592,17 @@ bwd_key_kernel(const void* __restrict__ k, const void* __restrict__ v,
   for (int slot = tid; slot < (kBwdTile / TU) * cqn; slot += 512) {
     const int c4 = slot % cqn;
     const int t0 = TU * (slot / cqn);
-    float x[TU][4], gk[TU][4], gv[TU][4];
+    // Laplacian: x holds -K 2^24, gk sums h step(L, -K 2^24) = h ([L > K] + [L == K] / 2) and
+    // hs the weights: dK's distance term -sum_j h sgn(L - K) = hs - 2 gk.
+    float x[TU][4], gk[TU][4], gv[TU][4], hs[TU];
 #pragma unroll
     for (int u = 0; u < TU; ++u) {
       const int tok = n0 + t0 + u;
+      hs[u] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         x[u][c] = tok < n ? load_in(k, ((size_t)bh * n + tok) * d + 4 * c4 + c, bf16 != 0) : 0.f;
+        if constexpr (!kGauss) x[u][c] = neg_scaled(x[u][c]);
         gk[u][c] = 0.f;
         gv[u][c] = 0.f;
       }
@@ -597,16 +624,23 @@ bwd_key_kernel(const void* __restrict__ k, const void* __restrict__ v,
       const float4 w4 = *reinterpret_cast<const float4*>(&sW[j * dq + 4 * c4]);
       const float ll[4] = {l4.x, l4.y, l4.z, l4.w}, ww[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-      for (int u = 0; u < TU; ++u)
+      for (int u = 0; u < TU; ++u) {
+        if constexpr (!kGauss) hs[u] += hh[u];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          gk[u][c] = fmaf(-hh[u], slope<kGauss>(ll[c], x[u][c]), gk[u][c]);
+          if constexpr (kGauss) gk[u][c] = fmaf(-hh[u], gauss_slope(ll[c], x[u][c]), gk[u][c]);
+          else gk[u][c] = fmaf(hh[u], step(ll[c], x[u][c]), gk[u][c]);
           gv[u][c] = fmaf(bb[u], ww[c], gv[u][c]);
         }
+      }
     }
 #pragma unroll
     for (int u = 0; u < TU; ++u) {
       const int tok = n0 + t0 + u;
+      if constexpr (!kGauss) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) gk[u][c] = fmaf(-2.f, gk[u][c], hs[u]);
+      }
       if (tok < n) {
         const size_t row = ((size_t)bh * n + tok) * d + 4 * c4;
         *reinterpret_cast<float4*>(dk + row) = make_float4(gk[u][0], gk[u][1], gk[u][2], gk[u][3]);
@@ -617,42 +651,59 @@ bwd_key_kernel(const void* __restrict__ k, const void* __restrict__ v,
 }
 
 // ---- partials of dL over one token split: side 0 from the query block, 1 from the key block --
-// Thread: quads (landmark j, channels 4 c4 .. 4 c4 + 3); per staged token one float4 of the
-// token row and one weight, shared by the four channels.
-constexpr int kMaxQuads = kMaxPairs / 4;    // 8
+// Both sides add -w sgn(X - L) (side 0: X = Q, w = g; side 1: X = K, w = h, from
+// +h sgn(L - K)).  Thread: quads (landmark j, channels 4 c4 .. 4 c4 + 3); per staged token one
+// float4 of the token row and one weight, shared by the four channels.  Laplacian kernel: l holds
+// -L 2^24, acc sums w step(X, -L 2^24) and ws the weights, and the partial is ws - 2 acc.
+constexpr int kMaxQuads = kMaxPairs / 4;    // 8 quads per thread at m = 64, d = 128
 
-template <bool kGauss, int kSide>
+// Quads per thread of the dL-partials kernel: 2, 4 or 8 (m d / 4 quads over 256 threads).
+int lm_quads_per_thread(int m, int d) {
+  const int need = (m * (d / 4) + kBwdThreads - 1) / kBwdThreads;
+  return need <= 2 ? 2 : (need <= 4 ? 4 : kMaxQuads);
+}
+
+template <bool kGauss, int QPT>
 __device__ __forceinline__ void lm_tile(const float* __restrict__ sX, const float* __restrict__ sw,
-                                        int dp, int tp, int d4, int quads, const float4 (&lv)[kMaxQuads],
-                                        float4 (&acc)[kMaxQuads]) {
+                                        int dp, int tp, int d4, int quads, const float4 (&lv)[QPT],
+                                        float4 (&acc)[QPT], float (&ws)[QPT]) {
 #pragma unroll
-  for (int u = 0; u < kMaxQuads; ++u) {
+  for (int u = 0; u < QPT; ++u) {
     const int qd = threadIdx.x + kBwdThreads * u;
     if (qd < quads) {
       const int j = qd / d4, c4 = qd % d4;
       const float4 l = lv[u];
       float4 a = acc[u];
-      for (int tt = 0; tt < kBwdTile; ++tt) {
-        const float4 x = *reinterpret_cast<const float4*>(&sX[tt * dp + 4 * c4]);
-        const float w = sw[j * tp + tt];
-        if (kSide == 0) {            // dL -= g sgn(Q - L)
-          a.x = fmaf(-w, slope<kGauss>(x.x, l.x), a.x);
-          a.y = fmaf(-w, slope<kGauss>(x.y, l.y), a.y);
-          a.z = fmaf(-w, slope<kGauss>(x.z, l.z), a.z);
-          a.w = fmaf(-w, slope<kGauss>(x.w, l.w), a.w);
-        } else {                     // dL += h sgn(L - K)
-          a.x = fmaf(w, slope<kGauss>(l.x, x.x), a.x);
-          a.y = fmaf(w, slope<kGauss>(l.y, x.y), a.y);
-          a.z = fmaf(w, slope<kGauss>(l.z, x.z), a.z);
-          a.w = fmaf(w, slope<kGauss>(l.w, x.w), a.w);
+      float s = ws[u];
+      const float* xp = sX + 4 * c4;
+      const float* wp = sw + j * tp;
+      for (int tt = 0; tt < kBwdTile; tt += 4) {
+        const float4 w4 = *reinterpret_cast<const float4*>(wp + tt);
+        const float w[4] = {w4.x, w4.y, w4.z, w4.w};
+        if constexpr (!kGauss) s += (w4.x + w4.y) + (w4.z + w4.w);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float4 x = *reinterpret_cast<const float4*>(xp + (tt + r) * dp);
+          if constexpr (kGauss) {
+            a.x = fmaf(-w[r], gauss_slope(x.x, l.x), a.x);
+            a.y = fmaf(-w[r], gauss_slope(x.y, l.y), a.y);
+            a.z = fmaf(-w[r], gauss_slope(x.z, l.z), a.z);
+            a.w = fmaf(-w[r], gauss_slope(x.w, l.w), a.w);
+          } else {
+            a.x = fmaf(w[r], step(x.x, l.x), a.x);
+            a.y = fmaf(w[r], step(x.y, l.y), a.y);
+            a.z = fmaf(w[r], step(x.z, l.z), a.z);
+            a.w = fmaf(w[r], step(x.w, l.w), a.w);
+          }
         }
       }
       acc[u] = a;
+      ws[u] = s;
     }
   }
 }
 
-template <bool kGauss>
+template <bool kGauss, int QPT>
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_lm_kernel(const void* __restrict__ q, const void* __restrict__ k,
               const float* __restrict__ gq, const float* __restrict__ hk,
@@ -660,9 +711,9 @@ bwd_lm_kernel(const void* __restrict__ q, const void* __restrict__ k,
               int n, int tiles_per_split, int splits, int bf16) {
   extern __shared__ float4 smem_l4[];
   float* smem = reinterpret_cast<float*>(smem_l4);
-  const int dp = d + 4, tp = kBwdTile + 1;
+  const int dp = d + 4, tp = kBwdTile + 4;
   float* sX = smem;                      // [tile][d + 4]
-  float* sw = sX + kBwdTile * dp;        // [m][tile + 1]
+  float* sw = sX + kBwdTile * dp;        // [m][tile + 4]
   const int side = blockIdx.x & 1;
   const long rest = blockIdx.x >> 1;
   const long bh = rest / splits;
@@ -671,12 +722,17 @@ bwd_lm_kernel(const void* __restrict__ q, const void* __restrict__ k,
   const float* wgt = side == 0 ? gq : hk;
   const float* Lh = landmarks + (size_t)bh * m * d;
   const int d4 = d >> 2, quads = m * d4;
-  float4 acc[kMaxQuads], lv[kMaxQuads];
+  float4 acc[QPT], lv[QPT];
+  float ws[QPT];
 #pragma unroll
-  for (int u = 0; u < kMaxQuads; ++u) {
+  for (int u = 0; u < QPT; ++u) {
     const int qd = threadIdx.x + kBwdThreads * u;
     acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    ws[u] = 0.f;
     lv[u] = qd < quads ? *reinterpret_cast<const float4*>(&Lh[4 * qd]) : acc[u];
+    if constexpr (!kGauss)
+      lv[u] = make_float4(neg_scaled(lv[u].x), neg_scaled(lv[u].y), neg_scaled(lv[u].z),
+                          neg_scaled(lv[u].w));
   }
   const int tiles = (n + kBwdTile - 1) / kBwdTile;
   const int t0 = sp * tiles_per_split, t1 = min(tiles, t0 + tiles_per_split);
@@ -701,15 +757,18 @@ bwd_lm_kernel(const void* __restrict__ q, const void* __restrict__ k,
       sw[j * tp + tt] = tok < n ? wgt[((size_t)bh * m + j) * n + tok] : 0.f;
     }
     __syncthreads();
-    if (side == 0) lm_tile<kGauss, 0>(sX, sw, dp, tp, d4, quads, lv, acc);
-    else lm_tile<kGauss, 1>(sX, sw, dp, tp, d4, quads, lv, acc);
+    lm_tile<kGauss, QPT>(sX, sw, dp, tp, d4, quads, lv, acc, ws);
     __syncthreads();
   }
   float* out = part_dl + (((size_t)bh * 2 + side) * splits + sp) * m * d;
 #pragma unroll
-  for (int u = 0; u < kMaxQuads; ++u) {
+  for (int u = 0; u < QPT; ++u) {
     const int qd = threadIdx.x + kBwdThreads * u;
-    if (qd < quads) *reinterpret_cast<float4*>(&out[4 * qd]) = acc[u];
+    float4 a = acc[u];
+    if constexpr (!kGauss)
+      a = make_float4(fmaf(-2.f, a.x, ws[u]), fmaf(-2.f, a.y, ws[u]), fmaf(-2.f, a.z, ws[u]),
+                      fmaf(-2.f, a.w, ws[u]));
+    if (qd < quads) *reinterpret_cast<float4*>(&out[4 * qd]) = a;
   }
 }
 
@@ -794,7 +853,17 @@ size_t key_smem(int m, int d) {
                           2 * mp4 * (kBwdTile + 4));
 }
 size_t lm_smem(int m, int d) {
-  return sizeof(float) * ((size_t)kBwdTile * (d + 4) + (size_t)m * (kBwdTile + 1));
+  return sizeof(float) * ((size_t)kBwdTile * (d + 4) + (size_t)m * (kBwdTile + 4));
+}
+const void* lm_kernel(bool gauss, int qpt) {
+  if (gauss) {
+    if (qpt == 2) return reinterpret_cast<const void*>(&bwd_lm_kernel<true, 2>);
+    if (qpt == 4) return reinterpret_cast<const void*>(&bwd_lm_kernel<true, 4>);
+    return reinterpret_cast<const void*>(&bwd_lm_kernel<true, kMaxQuads>);
+  }
+  if (qpt == 2) return reinterpret_cast<const void*>(&bwd_lm_kernel<false, 2>);
+  if (qpt == 4) return reinterpret_cast<const void*>(&bwd_lm_kernel<false, 4>);
+  return reinterpret_cast<const void*>(&bwd_lm_kernel<false, kMaxQuads>);
 }
 
 }  // namespace
@@ -818,15 +887,15 @@ BwdLayout bwd_layout(const lapl_attn_plan& p) {
   L.dbias_bh = take(bh * m);
   L.gq = take(bh * m * n);
   L.hk = take(bh * m * n);
-  L.part_dl = take(bh * 2 * sp * m * d);
+  L.part_dl = take(bh * 2 * (size_t)g.lm_splits * m * d);
   L.dl = take(bh * m * d);
   L.st = take(bh * m * m);
   L.total = off;
   return L;
 }
 
-cudaError_t bwd_configure(const lapl_attn_plan& p) {
-  const Geometry& g = p.geo;
+cudaError_t bwd_configure(lapl_attn_plan& p) {
+  Geometry& g = p.geo;
   cudaError_t e = cudaFuncSetAttribute(bwd_ahat_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)ahat_smem(g.m, g.d));
   const void* hf = pick_ns_bwd(g.s);
@@ -849,9 +918,32 @@ cudaError_t bwd_configure(const lapl_attn_plan& p) {
       reinterpret_cast<const void*>(&bwd_key_kernel<true, 4>)};
   for (int i = 0; i < 8 && e == cudaSuccess; ++i)
     e = cudaFuncSetAttribute(tok_kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, i < 4 ? qs : ks);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_lm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, ls);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_lm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, ls);
-  return e;
+  const bool gauss = p.cfg.kernel == LAPL_KERNEL_GAUSSIAN;
+  const void* lmk = lm_kernel(gauss, lm_quads_per_thread(g.m, g.d));
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(lmk, cudaFuncAttributeMaxDynamicSharedMemorySize, ls);
+  // dL partials: (head, side) units of `tiles` token chunks each, cut into equal splits.  The
+  // kernel's time is the number of waves of resident CTAs times the chunks of one CTA (plus
+  // about half a chunk for its prologue and the write of its partial): pick the split count
+  // that minimises that product, the fewest CTAs among equals.
+  int occ = 0;
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, lmk, kBwdThreads, ls);
+  if (e != cudaSuccess) return e;
+  const long long slots = (long long)p.num_sms * std::max(occ, 1);
+  const long long units = 2LL * std::max<long long>(g.bh, 1);
+  const int tiles = std::max(1, (g.n + kBwdTile - 1) / kBwdTile);
+  double best = 0.0;
+  for (int want = 1; want <= std::min(tiles, 256); ++want) {
+    const int tps = (tiles + want - 1) / want, splits = (tiles + tps - 1) / tps;
+    const long long waves = (units * splits + slots - 1) / slots;
+    const double cost = (double)waves * (tps + 0.5);
+    if (want == 1 || cost < best) {
+      best = cost;
+      g.lm_tiles_per_split = tps;
+      g.lm_splits = splits;
+    }
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* k, const void* v,
@@ -862,6 +954,7 @@ cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* 
   const WorkspaceLayout& F = p.ws;
   const BwdLayout B = bwd_layout(p);
   const int m = g.m, d = g.d, n = g.n, splits = g.bv_splits, tps = g.bv_tiles_per_split;
+  const int lsp = g.lm_splits, ltps = g.lm_tiles_per_split;
   const int heads = p.cfg.heads, whiten = p.cfg.whiten, bf16 = p.cfg.in_dtype == LAPL_BF16;
   const bool gauss = p.cfg.kernel == LAPL_KERNEL_GAUSSIAN;
   const float lam = p.cfg.lambda;
@@ -916,20 +1009,23 @@ cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* 
   if (gauss) {
     if (tu4) launch_tok(bwd_query_kernel<true, 4>, bwd_key_kernel<true, 4>);
     else launch_tok(bwd_query_kernel<true, 2>, bwd_key_kernel<true, 2>);
-    bwd_lm_kernel<true><<<bh * splits * 2, kBwdThreads, lm_smem(m, d), st>>>(
-        q, k, gq, hk, L, part_dl, m, d, n, tps, splits, bf16);
   } else {
     if (tu4) launch_tok(bwd_query_kernel<false, 4>, bwd_key_kernel<false, 4>);
     else launch_tok(bwd_query_kernel<false, 2>, bwd_key_kernel<false, 2>);
-    bwd_lm_kernel<false><<<bh * splits * 2, kBwdThreads, lm_smem(m, d), st>>>(
-        q, k, gq, hk, L, part_dl, m, d, n, tps, splits, bf16);
   }
   e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  {
+    const void* f = lm_kernel(gauss, lm_quads_per_thread(m, d));
+    int mm = m, dd = d, nn = n, ltps_ = ltps, lsp_ = lsp, bf = bf16;
+    void* args[] = {&q, &k, &gq, &hk, &L, &part_dl, &mm, &dd, &nn, &ltps_, &lsp_, &bf};
+    e = cudaLaunchKernel(f, dim3(bh * lsp * 2), dim3(kBwdThreads), args, lm_smem(m, d), st);
+  }
   if (e == cudaSuccess) e = cudaStreamWaitEvent(st, p.ev_join, 0);
   if (e != cudaSuccess) return e;
   const unsigned dl_chunks = (unsigned)((m * d + kBwdThreads - 1) / kBwdThreads);
   bwd_dl_kernel<<<bh * dl_chunks, kBwdThreads, 0, st>>>(part_dl, dll, dbias_bh, dl, dbias, m, d,
-                                                         splits, p.cfg.batch, heads, dl_chunks);
+                                                         lsp, p.cfg.batch, heads, dl_chunks);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int s = g.s;

@@ -104,6 +104,8 @@ struct Geometry {
   bool cg;                 // conjugate-gradient solver (cg.cu) instead of Newton-Schulz
   size_t cg_smem;
   size_t pool_threads;
+  int lm_splits;           // backward dL partials: CTAs per (head, side)
+  int lm_tiles_per_split;  // backward dL partials: 128-token chunks per CTA
 };
 
 // Timing marks of one forward (events recorded when timing is on).
@@ -178,7 +180,7 @@ size_t mix_smem_bytes(int m, int bv_splits);
 cudaError_t mix_configure(size_t smem);
 // Backward pass (backward.cu).
 BwdLayout bwd_layout(const lapl_attn_plan& p);
-cudaError_t bwd_configure(const lapl_attn_plan& p);
+cudaError_t bwd_configure(lapl_attn_plan& p);
 cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* k, const void* v,
                             const float* bias, const float* gout, float* dq, float* dk,
                             float* dv, float* dbias, const char* fws, char* bws,

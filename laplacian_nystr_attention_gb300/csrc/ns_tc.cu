@@ -163,6 +163,32 @@ __device__ __forceinline__ void tmem_ld16(unsigned addr, float (&v)[16]) {
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// Two 16-column loads, one wait: both round trips to tensor memory overlap.
+__device__ __forceinline__ void tmem_ld16x2(unsigned addr_a, unsigned addr_b, float (&a)[16],
+                                            float (&b)[16]) {
+  unsigned r[16], q[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(addr_a));
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];\n"
+      : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]),
+        "=r"(q[7]), "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]), "=r"(q[13]),
+        "=r"(q[14]), "=r"(q[15])
+      : "r"(addr_b));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    a[j] = __uint_as_float(r[j]);
+    b[j] = __uint_as_float(q[j]);
+  }
+}
+
 // C = sum of the four blocks of D, 8 columns of one row per thread.  Warp w reads tensor-memory
 // lanes 32(w % 4).. (D rows dr) and columns 16h.. and 64 + 16h.. (h = w / 4); D rows dr and
 // dr + 64 hold the A_hi and A_lo parts of C row i = dr % 64.  The A_hi thread keeps columns
@@ -177,8 +203,7 @@ __device__ __forceinline__ void combine_product(unsigned tmem, float* sc, float 
   const bool low = dr >= 64;
   const unsigned lane_base = (unsigned)(32 * sp) << 16;
   float a[16], v[16];
-  tmem_ld16(tmem + lane_base + 16 * h, a);
-  tmem_ld16(tmem + lane_base + 64 + 16 * h, v);
+  tmem_ld16x2(tmem + lane_base + 16 * h, tmem + lane_base + 64 + 16 * h, a, v);
 #pragma unroll
   for (int j = 0; j < 16; ++j) a[j] += v[j];
   // kept half: a[8..15] for the low thread, a[0..7] for the high one (selects, so that a stays
