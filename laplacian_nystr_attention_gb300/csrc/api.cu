@@ -215,19 +215,33 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   }
   if (per_sm < 1) per_sm = 1;
   {
-    // B V: about two CTAs per SM in total, whole 128-token chunks per CTA, and at most
-    // kMaxBvSplits CTAs per head: the M kernel stages every split's partial of its 8 columns
-    // in shared memory (64 splits at m = 64: 146 KB).
-    constexpr long long kMaxBvSplits = 64;
-    const long long bh1 = g.bh > 0 ? g.bh : 1;
-    const int tiles = (g.n + bv_tile_tokens() - 1) / bv_tile_tokens();
-    long long want = (2LL * p->num_sms + bh1 - 1) / bh1;
-    want = std::max<long long>(1, std::min<long long>(std::min(want, kMaxBvSplits), tiles));
-    g.bv_tiles_per_split = (int)((tiles + want - 1) / want);
-    g.bv_splits = (tiles + g.bv_tiles_per_split - 1) / g.bv_tiles_per_split;
-    // Column statistics of A: one warp per landmark column, appended to the B V grid.
+    // Column statistics of A: one warp per landmark column, placed before the B V CTAs in
+    // their grid.
     const int warps = g.bv_threads / 32;
     g.stat_ctas = cfg->whiten ? (int)(g.bh * ((g.m + warps - 1) / warps)) : 0;
+    // B V: whole 64-token chunks per CTA, on the SMs the solve leaves free (it keeps its own
+    // when ns_exclusive).  The kernel's time is about the waves of resident CTAs (statistics
+    // CTAs counted as B V CTAs) times the chunks of one CTA plus one for its prologue and
+    // partial store: pick the split count that minimises it, the fewest CTAs among equals.  At
+    // most kMaxBvSplits CTAs per head: the M kernel stages every split's partial of its 8
+    // columns in shared memory (64 splits at m = 64: 146 KB).
+    constexpr int kMaxBvSplits = 64;
+    const long long bh1 = g.bh > 0 ? g.bh : 1;
+    const int tiles = std::max(1, (g.n + bv_tile_tokens() - 1) / bv_tile_tokens());
+    long long sms = p->num_sms;
+    if (g.ns_exclusive) sms -= g.bh * g.ns_cluster;
+    const long long slots = std::max<long long>(sms, 1) * bv_occupancy(g.bv_threads, g.bv_smem);
+    long long best = -1;
+    for (int want = 1; want <= std::min(tiles, kMaxBvSplits); ++want) {
+      const int tps = (tiles + want - 1) / want, splits = (tiles + tps - 1) / tps;
+      const long long waves = (bh1 * splits + g.stat_ctas + slots - 1) / slots;
+      const long long cost = waves * (tps + 1);
+      if (best < 0 || cost < best) {
+        best = cost;
+        g.bv_tiles_per_split = tps;
+        g.bv_splits = splits;
+      }
+    }
   }
   {
     // No more CTAs than chunks of work.

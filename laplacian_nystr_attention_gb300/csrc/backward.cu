@@ -229,7 +229,8 @@ __global__ void __launch_bounds__(kBwdThreads)
 bwd_mid_kernel(const float* __restrict__ xs, const float* __restrict__ bvp,
                const float* __restrict__ part_dm, const float* __restrict__ part_s,
                float* __restrict__ dbv, float* __restrict__ st, float* __restrict__ s12,
-               float* __restrict__ dbias_bh, int m, int d, int T, int splits, int whiten) {
+               float* __restrict__ dbias_bh, int m, int d, int T, int splits, int bv_splits,
+               int whiten) {
   extern __shared__ float4 smem_m4[];
   float* smem = reinterpret_cast<float*>(smem_m4);
   const int dp = d + 1;               // padded rows: threads of a warp read different rows
@@ -242,12 +243,11 @@ bwd_mid_kernel(const float* __restrict__ xs, const float* __restrict__ bvp,
   for (int e = tid; e < m * d; e += kBwdThreads) {
     float a = 0.f, b = 0.f;
     const float* pa = part_dm + (size_t)bh * splits * m * d + e;
-    const float* pb = bvp + (size_t)bh * splits * m * d + e;
+    const float* pb = bvp + (size_t)bh * bv_splits * m * d + e;
 #pragma unroll 8
-    for (int sp = 0; sp < splits; ++sp) {
-      a += pa[(size_t)sp * m * d];
-      b += pb[(size_t)sp * m * d];
-    }
+    for (int sp = 0; sp < splits; ++sp) a += pa[(size_t)sp * m * d];
+#pragma unroll 8
+    for (int sp = 0; sp < bv_splits; ++sp) b += pb[(size_t)sp * m * d];   // the forward's order
     sdM[(e / d) * dp + e % d] = a;
     sBV[(e / d) * dp + e % d] = b;
   }
@@ -868,9 +868,28 @@ const void* lm_kernel(bool gauss, int qpt) {
 
 }  // namespace
 
+// Token splits of a kernel over `units` independent units of `tiles` chunks each: its time is
+// about the waves of resident CTAs times the chunks of one CTA (plus half a chunk for its
+// prologue and the store of its partial); take the split count that minimises that, the
+// fewest CTAs among equals.
+static void choose_splits(long long slots, long long units, int tiles, int max_splits,
+                          int* splits_out, int* tps_out) {
+  double best = 0.0;
+  for (int want = 1; want <= std::min(tiles, max_splits); ++want) {
+    const int tps = (tiles + want - 1) / want, splits = (tiles + tps - 1) / tps;
+    const long long waves = (units * splits + slots - 1) / slots;
+    const double cost = (double)waves * (tps + 0.5);
+    if (want == 1 || cost < best) {
+      best = cost;
+      *tps_out = tps;
+      *splits_out = splits;
+    }
+  }
+}
+
 BwdLayout bwd_layout(const lapl_attn_plan& p) {
   const Geometry& g = p.geo;
-  const size_t bh = (size_t)g.bh, m = g.m, d = g.d, n = g.n, sp = g.bv_splits;
+  const size_t bh = (size_t)g.bh, m = g.m, d = g.d, n = g.n, sp = g.ahat_splits;
   BwdLayout L;
   size_t off = 0;
   auto take = [&](size_t floats) {
@@ -921,28 +940,19 @@ cudaError_t bwd_configure(lapl_attn_plan& p) {
   const bool gauss = p.cfg.kernel == LAPL_KERNEL_GAUSSIAN;
   const void* lmk = lm_kernel(gauss, lm_quads_per_thread(g.m, g.d));
   if (e == cudaSuccess) e = cudaFuncSetAttribute(lmk, cudaFuncAttributeMaxDynamicSharedMemorySize, ls);
-  // dL partials: (head, side) units of `tiles` token chunks each, cut into equal splits.  The
-  // kernel's time is the number of waves of resident CTAs times the chunks of one CTA (plus
-  // about half a chunk for its prologue and the write of its partial): pick the split count
-  // that minimises that product, the fewest CTAs among equals.
-  int occ = 0;
+  int occ = 0, aocc = 0;
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, lmk, kBwdThreads, ls);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&aocc, bwd_ahat_kernel, kAhatThreads,
+                                                      ahat_smem(g.m, g.d));
   if (e != cudaSuccess) return e;
-  const long long slots = (long long)p.num_sms * std::max(occ, 1);
-  const long long units = 2LL * std::max<long long>(g.bh, 1);
   const int tiles = std::max(1, (g.n + kBwdTile - 1) / kBwdTile);
-  double best = 0.0;
-  for (int want = 1; want <= std::min(tiles, 256); ++want) {
-    const int tps = (tiles + want - 1) / want, splits = (tiles + tps - 1) / tps;
-    const long long waves = (units * splits + slots - 1) / slots;
-    const double cost = (double)waves * (tps + 0.5);
-    if (want == 1 || cost < best) {
-      best = cost;
-      g.lm_tiles_per_split = tps;
-      g.lm_splits = splits;
-    }
-  }
+  const long long heads = std::max<long long>(g.bh, 1);
+  choose_splits((long long)p.num_sms * std::max(occ, 1), 2 * heads, tiles, 256, &g.lm_splits,
+                &g.lm_tiles_per_split);
+  choose_splits((long long)p.num_sms * std::max(aocc, 1), heads, tiles, 64, &g.ahat_splits,
+                &g.ahat_tiles_per_split);
   return cudaSuccess;
 }
 
@@ -953,7 +963,7 @@ cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* 
   const Geometry& g = p.geo;
   const WorkspaceLayout& F = p.ws;
   const BwdLayout B = bwd_layout(p);
-  const int m = g.m, d = g.d, n = g.n, splits = g.bv_splits, tps = g.bv_tiles_per_split;
+  const int m = g.m, d = g.d, n = g.n, splits = g.ahat_splits, tps = g.ahat_tiles_per_split;
   const int lsp = g.lm_splits, ltps = g.lm_tiles_per_split;
   const int heads = p.cfg.heads, whiten = p.cfg.whiten, bf16 = p.cfg.in_dtype == LAPL_BF16;
   const bool gauss = p.cfg.kernel == LAPL_KERNEL_GAUSSIAN;
@@ -979,7 +989,7 @@ cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* 
   if (e != cudaSuccess) return e;
   bwd_mid_kernel<<<bh, kBwdThreads, mid_smem(m, d), st>>>(Xs, bvp, part_dm, part_s, dbv, sT, s12,
                                                          dbias_bh, m, d, p.cfg.ns_steps, splits,
-                                                         whiten);
+                                                         g.bv_splits, whiten);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // The Newton-Schulz backward (only the landmark-block term of dL needs it) on the side

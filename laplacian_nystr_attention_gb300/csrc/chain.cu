@@ -6,11 +6,12 @@
 //    column, taken over the N tokens of the (batch, head) slice (variance divides by N);
 //  * low-rank product without the N x N matrix (Chinese page, 2.2), evaluated right to left.
 //
-// bv_kernel (one CTA per (batch, head, token split), then the column-statistics CTAs):
+// bv_kernel (the column-statistics CTAs, then one CTA per (batch, head, token split)):
 //   partial B V of the split's tokens from B^T [BH, m, N] and V, register-tiled on the CUDA
 //   cores (4 landmarks x 4 channels per thread, 8 shared loads per 64 FMAs).
-// mix_kernel (per (batch, head, 8 value columns)), after the Newton-Schulz solve is joined:
-//   reduces the per-split partials of B V in split order and forms M = X (B V).
+// mix_kernel (per (batch, head, 8 value columns)), after B V and the Newton-Schulz solve:
+//   reduces the per-split partials of B V in split order (while the solve may still run, when
+//   it is this kernel's programmatic predecessor) and forms M = X (B V).
 //   Fixed reduction orders: the result is bit-reproducible run to run.
 // output_kernel (one CTA per (batch, head, token tile)):
 //   loads the A^T tile and whitens it on the way into shared memory, then (after the M
@@ -20,7 +21,7 @@
 namespace lapl {
 namespace {
 
-constexpr int kBvTile = 128;          // tokens per staged chunk
+constexpr int kBvTile = 64;           // tokens per staged chunk
 constexpr int kBvTileP = kBvTile + 4;  // padded row of the B^T chunk
 
 __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, int src_bytes) {
@@ -111,21 +112,24 @@ __device__ __forceinline__ void column_stats(const float* __restrict__ at, float
   }
 }
 
-// Partial B V of the split's tokens.  Chunks of 128 tokens (B^T rows and V rows) are copied
+// Partial B V of the split's tokens.  Chunks of 64 tokens (B^T rows and V rows) are copied
 // asynchronously into one of two shared buffers while the other is contracted.
 template <bool kBf16>
 __global__ void __launch_bounds__(512)
 bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __restrict__ bvp,
           int m, int d, int n, int tiles_per_split, int splits, const float* __restrict__ at,
           float* __restrict__ mu, float* __restrict__ rstd, float* __restrict__ dbg_mu,
-          float* __restrict__ dbg_rstd, long bv_ctas, float delta) {
+          float* __restrict__ dbg_rstd, long stat_ctas, float delta) {
   // A kernel launched as this grid's programmatic dependent (the conjugate-gradient solver)
   // may start its own preparation now; it waits for this grid before it reads any result.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  if ((long)blockIdx.x >= bv_ctas) {     // a column-statistics CTA (uniform per CTA)
-    column_stats(at, mu, rstd, dbg_mu, dbg_rstd, m, n, delta, (long)blockIdx.x - bv_ctas);
+  // The column-statistics CTAs come first: they are placed in the first wave, next to the
+  // B V CTAs, instead of after them.
+  if ((long)blockIdx.x < stat_ctas) {    // a column-statistics CTA (uniform per CTA)
+    column_stats(at, mu, rstd, dbg_mu, dbg_rstd, m, n, delta, (long)blockIdx.x);
     return;
   }
+  const long cta = (long)blockIdx.x - stat_ctas;
   extern __shared__ float4 smem_bv4[];
   float* smem = reinterpret_cast<float*>(smem_bv4);
   const int nthreads = blockDim.x;
@@ -134,8 +138,8 @@ bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __r
   float* sB0 = smem;                                       // 2 x [mp4][kBvTileP]
   char* sV0 = reinterpret_cast<char*>(sB0 + 2 * mp4 * kBvTileP);   // 2 x [kBvTile][d]
   float* red = smem;   // [16][nthreads], reuses the staging buffers after the last chunk
-  const long bh = blockIdx.x / splits;
-  const int sp = blockIdx.x % splits;
+  const long bh = cta / splits;
+  const int sp = (int)(cta % splits);
   const int tiles = (n + kBvTile - 1) / kBvTile;
   const int t_begin = sp * tiles_per_split;
   const int t_end = min(tiles, t_begin + tiles_per_split);
@@ -165,13 +169,13 @@ bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __r
     float* sB = sB0 + buf * mp4 * kBvTileP;
     if (vec) {
       for (int i = threadIdx.x; i < m * (kBvTile / 4); i += nthreads) {
-        const int j = i >> 5, q4 = i & 31;
+        const int j = i / (kBvTile / 4), q4 = i % (kBvTile / 4);
         const float* src = &bt[((size_t)bh * m + j) * n + n0 + (4 * q4 < valid ? 4 * q4 : 0)];
         cp_async16_zfill(&sB[j * kBvTileP + 4 * q4], src, 4 * q4 < valid ? 16 : 0);
       }
     } else {
       for (int i = threadIdx.x; i < m * kBvTile; i += nthreads) {
-        const int j = i >> 7, t = i & 127;
+        const int j = i / kBvTile, t = i % kBvTile;
         const float* src = &bt[((size_t)bh * m + j) * n + n0 + (t < valid ? t : 0)];
         cp_async4_zfill(&sB[j * kBvTileP + t], src, t < valid ? 4 : 0);
       }
@@ -226,18 +230,26 @@ bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __r
     }
     buf ^= 1;
   }
-  // Combine the KS token classes in order, store the split's partial B V.
+  // Combine the KS token classes in order: the class-0 thread of (lg, cq) adds the others'
+  // register tiles to its own and stores the split's partial B V rows, 16 bytes at a time.
   __syncthreads();
+  if (ks > 0 && on) {
 #pragma unroll
-  for (int e = 0; e < 16; ++e) red[e * nthreads + threadIdx.x] = on ? acc[e >> 2][e & 3] : 0.f;
+    for (int e = 0; e < 16; ++e) red[e * nthreads + threadIdx.x] = acc[e >> 2][e & 3];
+  }
   __syncthreads();
-  float* dst = bvp + ((size_t)bh * splits + sp) * m * d;
-  for (int i = threadIdx.x; i < m * d; i += nthreads) {
-    const int j = i / d, c = i % d;
-    const int lgi = j >> 2, r = j & 3, cqi = c >> 2, cc = c & 3;
-    float sum = 0.f;
-    for (int q = 0; q < KS; ++q) sum += red[(r * 4 + cc) * nthreads + q * set + lgi * cqn + cqi];
-    dst[i] = sum;
+  if (ks == 0) {
+    for (int q = 1; q < KS; ++q)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) acc[e >> 2][e & 3] += red[e * nthreads + q * set + threadIdx.x];
+    float* dst = bvp + ((size_t)bh * splits + sp) * m * d + 4 * cq;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int j = 4 * lg + r;
+      if (j < m)
+        *reinterpret_cast<float4*>(&dst[(size_t)j * d]) =
+            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+    }
   }
 
 }
@@ -252,43 +264,47 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
 
 // mix_kernel, grid (BH * column chunks) -- the one step that waits for the Newton-Schulz solve:
 // CTA (bh, cc) sums the B V partials of columns [cc*8, cc*8+8) over the token splits (in split
-// order) and forms those columns of M = X (B V).  Every read is issued up front as an
-// asynchronous copy, so the kernel waits for one round trip to memory.
+// order) and forms those columns of M = X (B V).  The partials are complete when the kernel
+// starts (B V precedes it on the stream, or through an event when the solve has SMs of its
+// own); X is read after griddepcontrol.wait, which waits for the solve when this kernel is its
+// programmatic dependent, so the partial sums overlap the end of the solve.  Rows of 8 columns
+// are 32 bytes (d is a multiple of 8): every read is a 16-byte asynchronous copy but X's.
 __global__ void __launch_bounds__(kFinishThreads)
 mix_kernel(const float* __restrict__ xg, const float* __restrict__ bvp, float* __restrict__ mmat,
            float* __restrict__ dbg_bv, float* __restrict__ dbg_m, int m, int d, int bv_splits) {
   extern __shared__ float4 smem_fin4[];
   float* smem = reinterpret_cast<float*>(smem_fin4);
-  const int chunks = (d + kFinishCols - 1) / kFinishCols;
+  const int chunks = d / kFinishCols;
   const long bh = blockIdx.x / chunks;
   const int cc = blockIdx.x % chunks;
   const int c0 = cc * kFinishCols;
-  const int cw = min(kFinishCols, d - c0);
-  float* sX = smem;                                        // [m][m]
-  float* sP = sX + m * m;                                  // [bv_splits][m][kFinishCols]
-  float* sBV = sP + (size_t)bv_splits * m * kFinishCols;   // [m][kFinishCols]
+  float* sP = smem;                                        // [bv_splits][m][8]
+  float* sBV = sP + (size_t)bv_splits * m * kFinishCols;   // [m][8]
+  float* sX = sBV + (size_t)m * kFinishCols;               // [m][m]
   // The output kernel may start now: it prepares its A tile and waits for this grid before
   // it reads M.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  for (int i = threadIdx.x; i < m * m; i += kFinishThreads) cp_async4(&sX[i], &xg[(size_t)bh * m * m + i]);
   const float* pbase = bvp + (size_t)bh * bv_splits * m * d + c0;
-  for (int i = threadIdx.x; i < bv_splits * m * cw; i += kFinishThreads) {
-    const int sp = i / (m * cw), rest = i % (m * cw);
-    const int j = rest / cw, c = rest % cw;
-    cp_async4(&sP[(sp * m + j) * kFinishCols + c], &pbase[((size_t)sp * m + j) * d + c]);
+  const int rows = bv_splits * m;                          // (split, landmark) rows
+  for (int i = threadIdx.x; i < 2 * rows; i += kFinishThreads) {
+    const int r = i >> 1, h = i & 1;
+    cp_async16_zfill(&sP[r * kFinishCols + 4 * h], &pbase[(size_t)r * d + 4 * h], 16);
   }
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
   __syncthreads();
-  for (int i = threadIdx.x; i < m * cw; i += kFinishThreads) {
-    const int j = i / cw, c = i % cw;
+  for (int i = threadIdx.x; i < m * kFinishCols; i += kFinishThreads) {
+    const int j = i >> 3, c = i & 7;
     float acc = 0.f;
     for (int sp = 0; sp < bv_splits; ++sp) acc += sP[(sp * m + j) * kFinishCols + c];
-    sBV[j * kFinishCols + c] = acc;
+    sBV[i] = acc;
     if (dbg_bv) dbg_bv[((size_t)bh * m + j) * d + c0 + c] = acc;
   }
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");     // X is complete and visible
+  for (int i = threadIdx.x; i < m * m; i += kFinishThreads) cp_async4(&sX[i], &xg[(size_t)bh * m * m + i]);
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
   __syncthreads();
-  for (int i = threadIdx.x; i < m * cw; i += kFinishThreads) {
-    const int j = i / cw, c = i % cw;
+  for (int i = threadIdx.x; i < m * kFinishCols; i += kFinishThreads) {
+    const int j = i >> 3, c = i & 7;
     float acc = 0.f;
     for (int k = 0; k < m; ++k) acc = fmaf(sX[j * m + k], sBV[k * kFinishCols + c], acc);
     const size_t o = ((size_t)bh * m + j) * d + c0 + c;
@@ -429,7 +445,7 @@ output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
 }  // namespace
 
 size_t mix_smem_bytes(int m, int bv_splits) {
-  return sizeof(float) * ((size_t)m * m + ((size_t)bv_splits + 1) * m * kFinishCols);
+  return sizeof(float) * (((size_t)bv_splits + 1) * m * kFinishCols + (size_t)m * m);
 }
 
 cudaError_t mix_configure(size_t smem) {
@@ -468,6 +484,14 @@ int bv_threads(int m, int d) {
 
 int bv_tile_tokens() { return kBvTile; }
 
+int bv_occupancy(int threads, size_t smem) {
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, bv_kernel<false>, threads, smem) !=
+      cudaSuccess)
+    return 1;
+  return occ > 0 ? occ : 1;
+}
+
 cudaError_t bv_configure(size_t smem) {
   cudaError_t e = cudaFuncSetAttribute(bv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
@@ -479,18 +503,18 @@ cudaError_t launch_bv(const lapl_attn_plan& p, const float* bt, const void* v, f
                       const float* at, float* mu, float* rstd, float* dbg_mu, float* dbg_rstd,
                       cudaStream_t st) {
   const Geometry& g = p.geo;
-  const long bv_ctas = g.bh * g.bv_splits;
-  const unsigned grid = (unsigned)(bv_ctas + g.stat_ctas);
+  const long bv_ctas = g.bh * g.bv_splits, stat_ctas = g.stat_ctas;
+  const unsigned grid = (unsigned)(bv_ctas + stat_ctas);
   const float delta = p.cfg.delta;
   if (p.cfg.in_dtype == LAPL_BF16)
     bv_kernel<true><<<grid, g.bv_threads, g.bv_smem, st>>>(bt, v, bvp, g.m, g.d, g.n,
                                                            g.bv_tiles_per_split, g.bv_splits, at,
-                                                           mu, rstd, dbg_mu, dbg_rstd, bv_ctas,
+                                                           mu, rstd, dbg_mu, dbg_rstd, stat_ctas,
                                                            delta);
   else
     bv_kernel<false><<<grid, g.bv_threads, g.bv_smem, st>>>(bt, v, bvp, g.m, g.d, g.n,
                                                             g.bv_tiles_per_split, g.bv_splits, at,
-                                                            mu, rstd, dbg_mu, dbg_rstd, bv_ctas,
+                                                            mu, rstd, dbg_mu, dbg_rstd, stat_ctas,
                                                             delta);
   return cudaGetLastError();
 }
@@ -498,10 +522,22 @@ cudaError_t launch_bv(const lapl_attn_plan& p, const float* bt, const void* v, f
 cudaError_t launch_mix(const lapl_attn_plan& p, const float* x, const float* bvp, float* mmat,
                        float* dbg_bv, float* dbg_m, cudaStream_t st) {
   const Geometry& g = p.geo;
-  const int chunks = (g.d + kFinishCols - 1) / kFinishCols;
-  mix_kernel<<<(unsigned)(g.bh * chunks), kFinishThreads, g.fin_smem, st>>>(
-      x, bvp, mmat, dbg_bv, dbg_m, g.m, g.d, g.bv_splits);
-  return cudaGetLastError();
+  const int chunks = g.d / kFinishCols;
+  // With the solve on SMs of its own it precedes this kernel on the stream (B V comes through
+  // an event): a programmatic dependent of the solve.  Otherwise B V precedes it, and its
+  // partials must be complete at launch: a plain launch.
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)(g.bh * chunks));
+  cfg.blockDim = dim3(kFinishThreads);
+  cfg.dynamicSmemBytes = g.fin_smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = g.ns_exclusive ? 1 : 0;
+  int m = g.m, d = g.d, splits = g.bv_splits;
+  return cudaLaunchKernelEx(&cfg, mix_kernel, x, bvp, mmat, dbg_bv, dbg_m, m, d, splits);
 }
 
 cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float* mmat,

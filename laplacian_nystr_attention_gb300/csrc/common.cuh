@@ -89,7 +89,7 @@ struct Geometry {
   Partition cd_part;       // balanced split over cd_part.ctas persistent CTAs
   int bv_splits;           // B V: CTAs per head
   int stat_ctas;           // column-statistics CTAs appended to the B V grid (0: no whitening)
-  int bv_tiles_per_split;  // B V: 128-token chunks per CTA
+  int bv_tiles_per_split;  // B V: 64-token chunks per CTA
   int bv_threads;
   size_t bv_smem;
   size_t fin_smem;
@@ -104,6 +104,8 @@ struct Geometry {
   bool cg;                 // conjugate-gradient solver (cg.cu) instead of Newton-Schulz
   size_t cg_smem;
   size_t pool_threads;
+  int ahat_splits;         // backward dA^ / dM partials: CTAs per head
+  int ahat_tiles_per_split;  // backward dA^ / dM partials: 128-token chunks per CTA
   int lm_splits;           // backward dL partials: CTAs per (head, side)
   int lm_tiles_per_split;  // backward dL partials: 128-token chunks per CTA
 };
@@ -176,6 +178,7 @@ size_t bv_smem_bytes(int m, int d, int threads, bool bf16);
 int bv_threads(int m, int d);
 int bv_tile_tokens();
 cudaError_t bv_configure(size_t smem);
+int bv_occupancy(int threads, size_t smem);   // resident B V CTAs per SM
 size_t mix_smem_bytes(int m, int bv_splits);
 cudaError_t mix_configure(size_t smem);
 // Backward pass (backward.cu).

@@ -250,6 +250,8 @@ ns_tc_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
   unsigned* slot = reinterpret_cast<unsigned*>(smem_tc + kOffSlot);
   const int warp = threadIdx.x >> 5;
   const long bh = blockIdx.x;
+  // The M kernel after this one reduces the B V partials before it waits for this grid.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
@@ -262,6 +264,9 @@ ns_tc_kernel(const float* __restrict__ landmarks, float* __restrict__ xout,
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(bar)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
+
+  // Launched as a programmatic dependent of the pooling kernel: L is complete past this wait.
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
   // W (into sc) and X0 (into Xf), fp32, row stride kMS.
   NsSmem sm;
@@ -411,7 +416,19 @@ cudaError_t launch_ns_tc(const lapl_attn_plan& p, const float* landmarks, float*
   unsigned* err = p.dev_err;
   int gauss = p.cfg.kernel == LAPL_KERNEL_GAUSSIAN;
   void* args[] = {&landmarks, &x, &dbg_dll, &dbg_w, &dbg_x, &xs, &d, &T, &eps, &c_exp, &gauss, &err};
-  return cudaLaunchKernel(f, dim3((unsigned)g.bh), dim3(kTcThreads), args, g.ns_smem, st);
+  // When the solve follows the pooling kernel on the same stream (the solve has SMs of its
+  // own), it is a programmatic dependent of it: its launch and set-up overlap the pooling.
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)g.bh);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = g.ns_smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = g.ns_exclusive ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, f, args);
 }
 
 }  // namespace lapl

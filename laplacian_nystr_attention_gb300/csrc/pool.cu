@@ -27,6 +27,9 @@ pool_landmarks_kernel(const void* __restrict__ kin, float* __restrict__ landmark
                       int per_row) {
   constexpr int CH = kBf16 ? 8 : 4;          // channels per lane (16 bytes)
   __shared__ float part[kPoolWarps][32][CH];
+  // A programmatic dependent (the Newton-Schulz solve on this stream) may be placed now: it
+  // sets up its tensor memory and barriers, then waits for this grid before it reads L.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = s * s;
   long bh;
