@@ -142,9 +142,9 @@ lapl_status lapl_attn_forward(lapl_attn_handle h, const void* q, const void* k, 
 
 /*
  * forward() that also keeps in the workspace what lapl_attn_backward needs beyond the forward's
- * own intermediates: every Newton-Schulz iterate X_0 .. X_T (about 2-3 us more at the stage-1
- * shape).  Same arguments, results bit for bit equal to forward().  LAPL_ERR_UNSUPPORTED with
- * the CG solver.
+ * own intermediates: every Newton-Schulz iterate X_0 .. X_T and the reduced B V (about 2-3 us
+ * more at the stage-1 shape).  Same arguments, results bit for bit equal to forward().
+ * LAPL_ERR_UNSUPPORTED with the CG solver.
  */
 lapl_status lapl_attn_forward_train(lapl_attn_handle h, const void* q, const void* k,
                                     const void* v, const float* bias, void* out,

@@ -277,6 +277,7 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   w.at = take(bh * m * n);
   w.bt = take(bh * m * n);
   w.bvp = take(bh * g.bv_splits * m * d);
+  w.bv = take(g.cg ? 0 : bh * m * d);
 
   w.mmat = take(bh * m * d);
   w.mu = take(bh * m);
@@ -416,7 +417,8 @@ static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k,
     LAPL_MARK(kMarkBvDone, st);
   }
   LAPL_TRY(cudaStreamWaitEvent(st, p->ev_join, 0), "forward/join-wait");
-  LAPL_TRY(launch_mix(*p, X, bvp, M, D.bv, D.m, st), "forward/mix");
+  float* bv_keep = keep ? reinterpret_cast<float*>(ws + p->ws.bv) : nullptr;
+  LAPL_TRY(launch_mix(*p, X, bvp, M, bv_keep, D.bv, D.m, st), "forward/mix");
   LAPL_MARK(kMarkMixDone, st);
   LAPL_TRY(launch_output(*p, At, M, mu, rstd, bias, out, st), "forward/output");
   LAPL_MARK(kMarkOutputDone, st);

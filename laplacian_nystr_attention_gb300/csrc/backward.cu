@@ -4,11 +4,11 @@
 // Rethinking Linear Attention with Laplacian Kernel", English explainer page, 2 "CUDA
 // Acceleration"; German page, 2) and give no gradient: every kernel below applies the chain
 // rule to one forward step, in reverse order.  The forward's workspace supplies what it saved
-// (landmarks L, X, A^T, B^T, the column statistics, the B V partials and M).
+// (landmarks L, the iterates X_0 .. X_T, A^T, B^T, the column statistics, B V and M).
 //
 //   bwd_ahat_kernel   (head, token split)   dA^ = G M^T (stored), partials of dM = A^T G and
 //                                           of the column sums s1 = sum dA^, s2 = sum dA^ Z
-//   bwd_mid_kernel    (head)                dM, dBV = X^T dM, S_T = sym(dM BV^T), the sums
+//   bwd_mid_kernel    (head, row quarter)   dM, dBV = X^T dM, S_T = sym(dM BV^T), the sums
 //   bwd_ns_kernel     (head; side stream)   the Newton-Schulz steps backwards through the
 //                                           forward's saved iterates to dW; the landmark-
 //                                           block term of dL
@@ -225,36 +225,56 @@ bwd_ahat_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
 }
 
 // ---- per head: dM, dBV = X^T dM, S_T = sym(dM BV^T), the whitening sums ------------------
+// kMidParts CTAs per head.  Each sums the dM partials (every thread's elements loaded
+// together, one split at a time, in split order) and forms its quarter of the rows of dBV and
+// of S_T; part 0 also writes the whitening sums.
+constexpr int kMidParts = 4;
+constexpr int kMidElems = (kMaxM * kMaxD + kBwdThreads - 1) / kBwdThreads;   // 32
+
 __global__ void __launch_bounds__(kBwdThreads)
-bwd_mid_kernel(const float* __restrict__ xs, const float* __restrict__ bvp,
+bwd_mid_kernel(const float* __restrict__ xs, const float* __restrict__ bvg,
                const float* __restrict__ part_dm, const float* __restrict__ part_s,
                float* __restrict__ dbv, float* __restrict__ st, float* __restrict__ s12,
-               float* __restrict__ dbias_bh, int m, int d, int T, int splits, int bv_splits,
-               int whiten) {
+               float* __restrict__ dbias_bh, int m, int d, int T, int splits, int whiten) {
   extern __shared__ float4 smem_m4[];
   float* smem = reinterpret_cast<float*>(smem_m4);
   const int dp = d + 1;               // padded rows: threads of a warp read different rows
   float* sdM = smem;                  // [m][d + 1]
   float* sBV = sdM + m * dp;          // [m][d + 1]
   float* sX = sBV + m * dp;           // [m][m]  X_T
-  const long bh = blockIdx.x;
+  const long bh = blockIdx.x / kMidParts;
+  const int part = blockIdx.x % kMidParts;
+  const int rows = (m + kMidParts - 1) / kMidParts;
+  const int r0 = part * rows, r1 = min(m, r0 + rows);
   const int tid = threadIdx.x;
   const size_t mm = (size_t)m * m;
-  for (int e = tid; e < m * d; e += kBwdThreads) {
-    float a = 0.f, b = 0.f;
-    const float* pa = part_dm + (size_t)bh * splits * m * d + e;
-    const float* pb = bvp + (size_t)bh * bv_splits * m * d + e;
-#pragma unroll 8
-    for (int sp = 0; sp < splits; ++sp) a += pa[(size_t)sp * m * d];
-#pragma unroll 8
-    for (int sp = 0; sp < bv_splits; ++sp) b += pb[(size_t)sp * m * d];   // the forward's order
-    sdM[(e / d) * dp + e % d] = a;
-    sBV[(e / d) * dp + e % d] = b;
+  const int md = m * d;
+  {
+    float a[kMidElems];
+#pragma unroll
+    for (int u = 0; u < kMidElems; ++u) a[u] = 0.f;
+    const float* pa = part_dm + (size_t)bh * splits * md;
+    for (int sp = 0; sp < splits; ++sp) {
+      const float* src = pa + (size_t)sp * md;
+#pragma unroll
+      for (int u = 0; u < kMidElems; ++u) {
+        const int e = tid + kBwdThreads * u;
+        if (e < md) a[u] += src[e];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kMidElems; ++u) {
+      const int e = tid + kBwdThreads * u;
+      if (e < md) {
+        sdM[(e / d) * dp + e % d] = a[u];
+        sBV[(e / d) * dp + e % d] = bvg[(size_t)bh * md + e];   // kept by the training forward
+      }
+    }
   }
   const int mk = (m + 3) & ~3;           // row length of the saved iterates
   for (int e = tid; e < m * m; e += kBwdThreads)
     sX[e] = xs[((size_t)bh * (T + 1) + T) * m * mk + (e / m) * mk + e % m];
-  if (tid < m) {
+  if (part == 0 && tid < m) {
     float a = 0.f, b = 0.f;
     for (int sp = 0; sp < splits; ++sp) {
       a += part_s[((size_t)bh * splits + sp) * 2 * m + tid];
@@ -265,14 +285,14 @@ bwd_mid_kernel(const float* __restrict__ xs, const float* __restrict__ bvp,
     dbias_bh[(size_t)bh * m + tid] = whiten ? a : 0.f;
   }
   __syncthreads();
-  for (int e = tid; e < m * d; e += kBwdThreads) {
+  for (int e = r0 * d + tid; e < r1 * d; e += kBwdThreads) {
     const int j = e / d, c = e % d;
     float s = 0.f;
     for (int k = 0; k < m; ++k) s = fmaf(sX[k * m + j], sdM[k * dp + c], s);
-    dbv[(size_t)bh * m * d + e] = s;
+    dbv[(size_t)bh * md + e] = s;
   }
   // (i, j) and (j, i) add the same two dot products: S_T is exactly symmetric.
-  for (int e = tid; e < m * m; e += kBwdThreads) {
+  for (int e = r0 * m + tid; e < r1 * m; e += kBwdThreads) {
     const int i = e / m, j = e % m;
     float a = 0.f, b = 0.f;
     for (int c = 0; c < d; ++c) {
@@ -800,18 +820,32 @@ bwd_dl_kernel(const float* __restrict__ part_dl, const float* __restrict__ dll,
 }
 
 // ---- pooling backward: dK_n += dL_{window(n)} / (ph pw) ----------------------------------
+// Thread: one 4-channel piece c4 of every tpp-th token of the tile; the token's window is
+// found once per token, and dK moves in 16-byte pieces.
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_pool_kernel(const float* __restrict__ dl, float* __restrict__ dk, int m, int d, int n,
                 int grid_w, int s, int ph, int pw, int tiles) {
   const long bh = blockIdx.x / tiles;
   const int n0 = (blockIdx.x % tiles) * kBwdTile;
   const float inv = 1.f / (float)(ph * pw);
-  for (int i = threadIdx.x; i < kBwdTile * d; i += kBwdThreads) {
-    const int tt = i / d, c = i % d, tok = n0 + tt;
-    if (tok >= n) continue;
-    const int r = tok / grid_w, col = tok % grid_w;
+  const int d4 = d >> 2, tpp = kBwdThreads / d4;
+  const int c4 = threadIdx.x % d4, t0 = threadIdx.x / d4;
+  if (t0 >= tpp) return;
+  const float* dlh = dl + (size_t)bh * m * d + 4 * c4;
+#pragma unroll 4
+  for (int tt = t0; tt < kBwdTile; tt += tpp) {
+    const int tok = n0 + tt;
+    if (tok >= n) break;
+    const int r = tok / grid_w, col = tok - r * grid_w;
     const int j = (r / ph) * s + col / pw;
-    dk[((size_t)bh * n + tok) * d + c] += dl[((size_t)bh * m + j) * d + c] * inv;
+    const float4 g = *reinterpret_cast<const float4*>(dlh + (size_t)j * d);
+    float4* p = reinterpret_cast<float4*>(dk + ((size_t)bh * n + tok) * d + 4 * c4);
+    float4 v = *p;
+    v.x += g.x * inv;
+    v.y += g.y * inv;
+    v.z += g.z * inv;
+    v.w += g.w * inv;
+    *p = v;
   }
 }
 
@@ -972,7 +1006,7 @@ cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* 
   const float* Xs = reinterpret_cast<const float*>(fws + F.xs);
   const float* At = reinterpret_cast<const float*>(fws + F.at);
   const float* Bt = reinterpret_cast<const float*>(fws + F.bt);
-  const float* bvp = reinterpret_cast<const float*>(fws + F.bvp);
+  const float* BV = reinterpret_cast<const float*>(fws + F.bv);
   const float* M = reinterpret_cast<const float*>(fws + F.mmat);
   const float* mu = reinterpret_cast<const float*>(fws + F.mu);
   const float* rstd = reinterpret_cast<const float*>(fws + F.rstd);
@@ -987,9 +1021,8 @@ cudaError_t launch_backward(const lapl_attn_plan& p, const void* q, const void* 
       At, M, mu, rstd, bias, gout, dahat, part_dm, part_s, m, d, n, heads, tps, splits, whiten);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  bwd_mid_kernel<<<bh, kBwdThreads, mid_smem(m, d), st>>>(Xs, bvp, part_dm, part_s, dbv, sT, s12,
-                                                         dbias_bh, m, d, p.cfg.ns_steps, splits,
-                                                         g.bv_splits, whiten);
+  bwd_mid_kernel<<<bh * kMidParts, kBwdThreads, mid_smem(m, d), st>>>(
+      Xs, BV, part_dm, part_s, dbv, sT, s12, dbias_bh, m, d, p.cfg.ns_steps, splits, whiten);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // The Newton-Schulz backward (only the landmark-block term of dL needs it) on the side

@@ -271,7 +271,8 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
 // are 32 bytes (d is a multiple of 8): every read is a 16-byte asynchronous copy but X's.
 __global__ void __launch_bounds__(kFinishThreads)
 mix_kernel(const float* __restrict__ xg, const float* __restrict__ bvp, float* __restrict__ mmat,
-           float* __restrict__ dbg_bv, float* __restrict__ dbg_m, int m, int d, int bv_splits) {
+           float* __restrict__ bv_keep, float* __restrict__ dbg_bv, float* __restrict__ dbg_m,
+           int m, int d, int bv_splits) {
   extern __shared__ float4 smem_fin4[];
   float* smem = reinterpret_cast<float*>(smem_fin4);
   const int chunks = d / kFinishCols;
@@ -297,6 +298,7 @@ mix_kernel(const float* __restrict__ xg, const float* __restrict__ bvp, float* _
     float acc = 0.f;
     for (int sp = 0; sp < bv_splits; ++sp) acc += sP[(sp * m + j) * kFinishCols + c];
     sBV[i] = acc;
+    if (bv_keep) bv_keep[((size_t)bh * m + j) * d + c0 + c] = acc;
     if (dbg_bv) dbg_bv[((size_t)bh * m + j) * d + c0 + c] = acc;
   }
   asm volatile("griddepcontrol.wait;\n" ::: "memory");     // X is complete and visible
@@ -520,7 +522,7 @@ cudaError_t launch_bv(const lapl_attn_plan& p, const float* bt, const void* v, f
 }
 
 cudaError_t launch_mix(const lapl_attn_plan& p, const float* x, const float* bvp, float* mmat,
-                       float* dbg_bv, float* dbg_m, cudaStream_t st) {
+                       float* bv_keep, float* dbg_bv, float* dbg_m, cudaStream_t st) {
   const Geometry& g = p.geo;
   const int chunks = g.d / kFinishCols;
   // With the solve on SMs of its own it precedes this kernel on the stream (B V comes through
@@ -537,7 +539,8 @@ cudaError_t launch_mix(const lapl_attn_plan& p, const float* x, const float* bvp
   cfg.attrs = attr;
   cfg.numAttrs = g.ns_exclusive ? 1 : 0;
   int m = g.m, d = g.d, splits = g.bv_splits;
-  return cudaLaunchKernelEx(&cfg, mix_kernel, x, bvp, mmat, dbg_bv, dbg_m, m, d, splits);
+  return cudaLaunchKernelEx(&cfg, mix_kernel, x, bvp, mmat, bv_keep, dbg_bv, dbg_m, m, d,
+                            splits);
 }
 
 cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float* mmat,

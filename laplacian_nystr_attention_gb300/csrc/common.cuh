@@ -55,6 +55,7 @@ struct WorkspaceLayout {
   size_t at;           // [BH, m, N]         A = k(Q, L), landmark-major (A transposed)
   size_t bt;           // [BH, m, N]         B = k(L, K)
   size_t bvp;          // [BH, bv_splits, m, d]  per-split partial sums of B V
+  size_t bv;           // [BH, m, d]         B V (kept for the backward pass)
   size_t mmat;         // [BH, m, d]         M = X (B V)
   size_t mu;           // [BH, m]            column means of A
   size_t rstd;         // [BH, m]            1 / sqrt(column variance + delta)
@@ -152,7 +153,7 @@ cudaError_t launch_bv(const lapl_attn_plan& p, const float* bt, const void* v, f
                       const float* at, float* mu, float* rstd, float* dbg_mu, float* dbg_rstd,
                       cudaStream_t st);
 cudaError_t launch_mix(const lapl_attn_plan& p, const float* x, const float* bvp, float* mmat,
-                       float* dbg_bv, float* dbg_m, cudaStream_t st);
+                       float* bv_keep, float* dbg_bv, float* dbg_m, cudaStream_t st);
 cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float* mmat,
                           const float* mu, const float* rstd, const float* bias, void* out,
                           cudaStream_t st);
