@@ -115,7 +115,7 @@ __device__ __forceinline__ void column_stats(const float* __restrict__ at, float
 // Partial B V of the split's tokens.  Chunks of 64 tokens (B^T rows and V rows) are copied
 // asynchronously into one of two shared buffers while the other is contracted.
 template <bool kBf16>
-__global__ void __launch_bounds__(512)
+__global__ void __launch_bounds__(512, 2)
 bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __restrict__ bvp,
           int m, int d, int n, int tiles_per_split, int splits, const float* __restrict__ at,
           float* __restrict__ mu, float* __restrict__ rstd, float* __restrict__ dbg_mu,
