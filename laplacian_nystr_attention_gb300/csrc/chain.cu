@@ -137,6 +137,9 @@ bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __r
   const int vrow = d * (kBf16 ? 2 : 4);                    // bytes per staged V row
   float* sB0 = smem;                                       // 2 x [mp4][kBvTileP]
   char* sV0 = reinterpret_cast<char*>(sB0 + 2 * mp4 * kBvTileP);   // 2 x [kBvTile][d]
+  // bf16: each chunk of V is widened once into sVf (fp32 [kBvTile][d]) when it lands, instead
+  // of at every use (each V value serves every landmark quad).
+  float* sVf = reinterpret_cast<float*>(sV0 + 2 * kBvTile * d * (kBf16 ? 2 : 4));
   float* red = smem;   // [16][nthreads], reuses the staging buffers after the last chunk
   const long bh = cta / splits;
   const int sp = (int)(cta % splits);
@@ -196,10 +199,21 @@ bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __r
   for (int tile = t_begin; tile < t_end; ++tile) {
     asm volatile("cp.async.wait_group 0;\n" ::: "memory");
     __syncthreads();
+    if constexpr (kBf16) {
+      const uint4* raw = reinterpret_cast<const uint4*>(sV0 + buf * kBvTile * vrow);
+      for (int i = threadIdx.x; i < kBvTile * d / 8; i += nthreads) {
+        const uint4 r = raw[i];
+        float4* dst = reinterpret_cast<float4*>(sVf + 8 * i);
+        dst[0] = make_float4(bf16_lo(r.x), bf16_hi(r.x), bf16_lo(r.y), bf16_hi(r.y));
+        dst[1] = make_float4(bf16_lo(r.z), bf16_hi(r.z), bf16_lo(r.w), bf16_hi(r.w));
+      }
+      __syncthreads();
+    }
     if (tile + 1 < t_end) issue(tile + 1, buf ^ 1);
     if (on) {
       const float* sB = sB0 + buf * mp4 * kBvTileP;
-      const char* sV = sV0 + buf * kBvTile * vrow;
+      const char* sV = kBf16 ? reinterpret_cast<const char*>(sVf) : sV0 + buf * kBvTile * vrow;
+      const int vrow_f = d * 4;                            // bytes per fp32 row
       for (int q = ks; q < kBvTile / 4; q += KS) {
         const int t = 4 * q;
         float4 b4[4], v4[4];
@@ -207,14 +221,8 @@ bv_kernel(const float* __restrict__ bt, const void* __restrict__ vin, float* __r
         for (int r = 0; r < 4; ++r)
           b4[r] = *reinterpret_cast<const float4*>(&sB[(4 * lg + r) * kBvTileP + t]);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if constexpr (kBf16) {
-            const uint2 raw = *reinterpret_cast<const uint2*>(sV + (t + u) * vrow + 8 * cq);
-            v4[u] = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
-          } else {
-            v4[u] = *reinterpret_cast<const float4*>(sV + (t + u) * vrow + 16 * cq);
-          }
-        }
+        for (int u = 0; u < 4; ++u)
+          v4[u] = *reinterpret_cast<const float4*>(sV + (t + u) * vrow_f + 16 * cq);
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const float bu[4] = {b4[r].x, b4[r].y, b4[r].z, b4[r].w};
@@ -415,6 +423,7 @@ output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
   for (int r = 0; r < 4; ++r)
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+#pragma unroll 4
   for (int j = 0; j < m; ++j) {
     const float4 a4 = *reinterpret_cast<const float4*>(&sA[j * tile + 4 * tg]);
     const float4 m4 = *reinterpret_cast<const float4*>(&sM[j * d + 4 * q]);
@@ -474,7 +483,8 @@ cudaError_t output_configure(size_t smem) {
 size_t bv_smem_bytes(int m, int d, int threads, bool bf16) {
   const int mp4 = (m + 3) & ~3;
   const size_t staging = sizeof(float) * 2 * (size_t)mp4 * kBvTileP +
-                         2 * (size_t)kBvTile * d * (bf16 ? 2 : 4);
+                         2 * (size_t)kBvTile * d * (bf16 ? 2 : 4) +
+                         (bf16 ? sizeof(float) * (size_t)kBvTile * d : 0);
   const size_t red = sizeof(float) * 16 * (size_t)threads;
   return staging > red ? staging : red;
 }
