@@ -325,7 +325,9 @@ mix_kernel(const float* __restrict__ xg, const float* __restrict__ bvp, float* _
 
 constexpr int kOutThreads = 256;
 
-template <bool kOutBf16>
+// TPT: tokens per thread (4, or 8 for d >= 64: 128-token tiles, so that each CTA's M load and
+// A-tile prologue serve twice the work).
+template <bool kOutBf16, int TPT>
 __global__ void __launch_bounds__(kOutThreads)
 output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
               const float* __restrict__ mu, const float* __restrict__ rstd,
@@ -416,27 +418,33 @@ output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
 
   const int cg = d >> 2;                     // channel quads
   const int q = threadIdx.x % cg;
-  const int tg = threadIdx.x / cg;           // token quad
-  if (4 * tg >= tile) return;
-  float acc[4][4];
+  const int tg = threadIdx.x / cg;           // token group of TPT tokens
+  if (TPT * tg >= tile) return;
+  float acc[TPT][4];
 #pragma unroll
-  for (int r = 0; r < 4; ++r)
+  for (int r = 0; r < TPT; ++r)
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
-#pragma unroll 4
   for (int j = 0; j < m; ++j) {
-    const float4 a4 = *reinterpret_cast<const float4*>(&sA[j * tile + 4 * tg]);
+    float av[TPT];
+#pragma unroll
+    for (int h = 0; h < TPT / 4; ++h) {
+      const float4 a4 = *reinterpret_cast<const float4*>(&sA[j * tile + TPT * tg + 4 * h]);
+      av[4 * h] = a4.x;
+      av[4 * h + 1] = a4.y;
+      av[4 * h + 2] = a4.z;
+      av[4 * h + 3] = a4.w;
+    }
     const float4 m4 = *reinterpret_cast<const float4*>(&sM[j * d + 4 * q]);
-    const float av[4] = {a4.x, a4.y, a4.z, a4.w};
     const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int r = 0; r < TPT; ++r)
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], mv[c], acc[r][c]);
   }
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int tok = n0 + 4 * tg + r;
+  for (int r = 0; r < TPT; ++r) {
+    const int tok = n0 + TPT * tg + r;
     if (tok >= n) break;
     const size_t o = ((size_t)bh * n + tok) * d + 4 * q;
     if constexpr (kOutBf16) {
@@ -463,9 +471,11 @@ cudaError_t mix_configure(size_t smem) {
   return cudaFuncSetAttribute(mix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
+int output_tokens_per_thread(int d) { return d >= 64 ? 8 : 4; }
+
 int output_tile_tokens(int d) {
   const int cg = d / 4;
-  return 4 * (kOutThreads / cg);
+  return output_tokens_per_thread(d) * (kOutThreads / cg);
 }
 
 size_t output_smem_bytes(int m, int d, int tile) {
@@ -473,11 +483,14 @@ size_t output_smem_bytes(int m, int d, int tile) {
 }
 
 cudaError_t output_configure(size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(output_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(output_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem);
+  const void* fs[] = {reinterpret_cast<const void*>(&output_kernel<false, 4>),
+                      reinterpret_cast<const void*>(&output_kernel<false, 8>),
+                      reinterpret_cast<const void*>(&output_kernel<true, 4>),
+                      reinterpret_cast<const void*>(&output_kernel<true, 8>)};
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+    e = cudaFuncSetAttribute(fs[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return e;
 }
 
 size_t bv_smem_bytes(int m, int d, int threads, bool bf16) {
@@ -570,11 +583,14 @@ cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float*
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int m = g.m, d = g.d, n = g.n, heads = p.cfg.heads, tile = g.out_tile, whiten = p.cfg.whiten;
+  auto go = [&](auto kernel) {
+    return cudaLaunchKernelEx(&cfg, kernel, at, mmat, mu, rstd, bias, out, m, d, n, heads, tile,
+                              tiles, whiten);
+  };
+  const bool t8 = output_tokens_per_thread(d) == 8;
   if (p.cfg.out_dtype == LAPL_BF16)
-    return cudaLaunchKernelEx(&cfg, output_kernel<true>, at, mmat, mu, rstd, bias, out, m, d, n,
-                              heads, tile, tiles, whiten);
-  return cudaLaunchKernelEx(&cfg, output_kernel<false>, at, mmat, mu, rstd, bias, out, m, d, n,
-                            heads, tile, tiles, whiten);
+    return t8 ? go(output_kernel<true, 8>) : go(output_kernel<true, 4>);
+  return t8 ? go(output_kernel<false, 8>) : go(output_kernel<false, 4>);
 }
 
 }  // namespace lapl
