@@ -30,7 +30,7 @@
 
 namespace lapl {
 
-int output_tile_tokens(int d);
+int output_tile_tokens(int d, long bh, int n, int num_sms);
 
 namespace {
 
@@ -192,7 +192,7 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
       e = ns_configure(g.s, 1, g.ns_smem, nullptr);
   }
   if (e == cudaSuccess) {
-    g.out_tile = output_tile_tokens(g.d);
+    g.out_tile = output_tile_tokens(g.d, g.bh, g.n, p->num_sms);
     g.out_threads = 256;
     g.out_smem = output_smem_bytes(g.m, g.d, g.out_tile);
     e = output_configure(g.out_smem);

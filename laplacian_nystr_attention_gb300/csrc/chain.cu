@@ -325,8 +325,8 @@ mix_kernel(const float* __restrict__ xg, const float* __restrict__ bvp, float* _
 
 constexpr int kOutThreads = 256;
 
-// TPT: tokens per thread (4, or 8 for d >= 64: 128-token tiles, so that each CTA's M load and
-// A-tile prologue serve twice the work).
+// TPT: tokens per thread (4, or 8 for d >= 64 when the grid stays large: twice the tokens per
+// CTA, so that each CTA's M load and A-tile prologue serve twice the work).
 template <bool kOutBf16, int TPT>
 __global__ void __launch_bounds__(kOutThreads)
 output_kernel(const float* __restrict__ at, const float* __restrict__ mmat,
@@ -471,11 +471,13 @@ cudaError_t mix_configure(size_t smem) {
   return cudaFuncSetAttribute(mix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
-int output_tokens_per_thread(int d) { return d >= 64 ? 8 : 4; }
-
-int output_tile_tokens(int d) {
+// Tokens per thread of the output kernel: 8 for d >= 64 when the 8192/d-token tiles still
+// give at least two CTAs per SM, else 4.
+int output_tile_tokens(int d, long bh, int n, int num_sms) {
   const int cg = d / 4;
-  return output_tokens_per_thread(d) * (kOutThreads / cg);
+  const int t8 = 8 * (kOutThreads / cg);
+  const long ctas8 = bh * ((n + t8 - 1) / t8);
+  return (d >= 64 && ctas8 >= 2L * num_sms ? 8 : 4) * (kOutThreads / cg);
 }
 
 size_t output_smem_bytes(int m, int d, int tile) {
@@ -587,7 +589,7 @@ cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float*
     return cudaLaunchKernelEx(&cfg, kernel, at, mmat, mu, rstd, bias, out, m, d, n, heads, tile,
                               tiles, whiten);
   };
-  const bool t8 = output_tokens_per_thread(d) == 8;
+  const bool t8 = tile * (d / 4) == 8 * kOutThreads;
   if (p.cfg.out_dtype == LAPL_BF16)
     return t8 ? go(output_kernel<true, 8>) : go(output_kernel<true, 4>);
   return t8 ? go(output_kernel<false, 8>) : go(output_kernel<false, 4>);
