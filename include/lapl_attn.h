@@ -285,7 +285,7 @@ lapl_status lapl_attn_backward(lapl_attn_handle h, const void* q, const void* k,
                                float* dv, float* dbias, const void* fwd_workspace,
                                size_t fwd_workspace_bytes, void* bwd_workspace,
                                size_t bwd_workspace_bytes, void* stream);
-/* Number of kernels one backward launches (0 with the CG solver or an empty batch). */
+/* Number of kernels one backward launches: 8 (0 with the CG solver or an empty batch). */
 int lapl_attn_backward_kernels(lapl_attn_handle h);
 
 /* Release the plan (host state only).  NULL is accepted. */

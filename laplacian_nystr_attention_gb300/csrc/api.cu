@@ -470,7 +470,7 @@ lapl_status lapl_attn_backward(lapl_attn_handle h, const void* q, const void* k,
 }
 
 int lapl_attn_backward_kernels(lapl_attn_handle h) {
-  return (h && h->geo.bh > 0 && !h->geo.cg) ? 7 : 0;
+  return (h && h->geo.bh > 0 && !h->geo.cg) ? 8 : 0;
 }
 
 lapl_status lapl_attn_forward(lapl_attn_handle h, const void* q, const void* k, const void* v,
