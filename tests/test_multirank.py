@@ -4,7 +4,8 @@ The forward shards over independent (batch, head) slices: every rank runs its ow
 workload and no data-path collective exists.  What the ranks share is the timing: the job's
 time is the slowest rank's (a MAX all-reduce), the whole-job rate is world x tokens / that
 time, and only rank 0 prints.  Those pieces run here as two gloo processes; the reference arm's
-rule that ranks other than 0 exit at once without work is checked by running it as rank 1.
+rule that ranks other than 0 exit at once without work is checked by running it as rank 1, and
+its rank-0 JSON line (the oracle timed on the host cores) against the contract's keys.
 """
 import json
 import os
@@ -63,3 +64,27 @@ def test_reference_arm_other_ranks_exit_without_work():
                        text=True, timeout=120)
     assert p.returncode == 0, p.stderr
     assert p.stdout.strip() == ""
+
+
+def test_reference_arm_line_on_rank0():
+    """The reference arm (the fp64 oracle on the host cores) prints one JSON line with the
+    contract's keys: the same metric and unit as the GPU arm, impl = reference, a cpu_baseline
+    describing the run and an e2e object with no host-device bytes."""
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_f32", "--steps", "2", "--warmup", "1"], env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert p.returncode == 0, p.stderr
+    lines = [l for l in p.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    import bench
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["higher_is_better"] is True and line["value"] > 0
+    assert line["steps"] == 2 and line["warmup"] == 1 and line["n_gpus"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["value"] == line["value"] and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"].startswith("tiny_f32")
