@@ -539,9 +539,26 @@ lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void
   const size_t elems = (size_t)h->geo.bh * h->geo.n * h->geo.d;
   const size_t in_b = elems * elem_bytes(h->cfg.in_dtype);
   const size_t out_b = elems * elem_bytes(h->cfg.out_dtype);
-  cudaError_t e = cudaMemcpyAsync(base + s.q, q, in_b, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.k, k, in_b, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.v, v, in_b, cudaMemcpyHostToDevice, st);
+  cudaError_t e = cudaSuccess;
+  if (h->geo.ns_exclusive && !h->geo.cg) {
+    // The solve chain (pooling first) needs K only; Q and V are first read by the distance and
+    // B V kernels, which run on the side stream.  So the side stream copies K, Q, V in that
+    // order (after everything enqueued on the launching stream so far) and the launching
+    // stream waits for K alone: pooling and the solve start one copy after the call instead of
+    // three, and Q and V land while they run.
+    cudaStream_t side = h->side_stream;
+    e = cudaEventRecord(h->ev_pool, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->ev_pool, 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.k, k, in_b, cudaMemcpyHostToDevice, side);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_join, side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_join, 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.q, q, in_b, cudaMemcpyHostToDevice, side);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.v, v, in_b, cudaMemcpyHostToDevice, side);
+  } else {
+    e = cudaMemcpyAsync(base + s.q, q, in_b, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.k, k, in_b, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.v, v, in_b, cudaMemcpyHostToDevice, st);
+  }
   float* dbias = nullptr;
   if (e == cudaSuccess && bias) {
     dbias = reinterpret_cast<float*>(base + s.bias);
