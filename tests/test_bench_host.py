@@ -1,0 +1,44 @@
+"""Host-side pieces of bench.py that the JSON line depends on, checked on the CPU: the clock
+sampler's parsing of nvidia-smi rows (the throttle reasons decide whether a run is kept), and
+the roofline's operation count and derived FP32 peak."""
+import pytest
+
+import bench
+from lapl_workloads import WORKLOADS
+
+
+def _summary_of(tmp_path, text):
+    path = tmp_path / "clocks.csv"
+    path.write_text(text)
+    cs = bench.ClockSampler(0)
+    cs.path = str(path)
+    return cs.summary()
+
+
+def test_clock_summary_median_max_and_reasons(tmp_path):
+    rows = ("0, 2070, 2070, 900.10, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n"
+            "0, 2060, 2070, 1300.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n"
+            "0, 2040, 2070, 1390.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n")
+    s = _summary_of(tmp_path, rows)
+    assert s["sm_mhz"] == 2060.0 and s["sm_max_mhz"] == 2070.0 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_summary_reports_every_slowdown_reason(tmp_path):
+    rows = ("0, 1500, 2070, 1400.0, 0x48, Active, Active, Active, Not Active\n"
+            "0, 1600, 2070, 1400.0, 0x48, Not Active, Not Active, Not Active, Not Active\n")
+    s = _summary_of(tmp_path, rows)
+    assert s["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+    assert s["sm_mhz"] == 1550.0
+
+
+def test_clock_summary_without_samples(tmp_path):
+    s = _summary_of(tmp_path, "")
+    assert s == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+
+
+def test_roofline_operation_count_and_peak():
+    w = WORKLOADS["stage1_f32"]
+    # 3 ops x (query block + key block) x B x H x N x m x d
+    assert bench.cdist_ops_per_launch(w) == 3 * 2 * 8 * 2 * 3136 * 49 * 32 == 472055808
+    assert bench.fp32_peak_tflops(152, 2070.0) == pytest.approx(80.54784)
