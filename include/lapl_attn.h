@@ -244,17 +244,21 @@ lapl_status lapl_attn_plan_info_get(lapl_attn_handle h, lapl_attn_plan_info* inf
  * host application that owns every allocation, or a plugin that must not call cudaMalloc).
  * The paper has no counterpart: this is a deployment convenience of this library.
  *
- * Same inputs, outputs and results as lapl_attn_forward, but no workspace argument: the
- * workspace lives in a 32 MiB array in the library's own device memory, which every GPU that
- * loads the library holds until the process exits.  Configurations whose workspace
- * (lapl_attn_workspace_size) exceeds 32 MiB are rejected with LAPL_ERR_WORKSPACE and a message
- * in lapl_attn_last_error().  Allocates nothing.
+ * Same inputs, outputs and results as lapl_attn_forward (bit for bit), but no workspace
+ * argument: the workspace lives in a 32 MiB array in the library's own device memory, which
+ * every GPU that loads the library holds until the process exits.  Only the part of the
+ * workspace a plain forward uses is placed there (not the regions lapl_attn_forward_train keeps
+ * for the backward pass).  It fits the stage-1 vision shape (B=8, H=2, 56x56 tokens, d=32,
+ * m=49: about 23 MB) and smaller problems; larger ones (the 28x28, B=32, H=4 shape already
+ * needs 42 MB) are rejected with LAPL_ERR_WORKSPACE and a message in lapl_attn_last_error()
+ * that states the bytes needed.  Allocates nothing.
  *
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.  All calls share the
- * one array: calls that may overlap on the GPU (other streams, other handles, other threads)
- * race on it and must be serialised by the caller.  Every region of the workspace is written
- * before it is read, so nothing needs clearing between calls.
+ * that device current and keeps it for the life of the process; make that first call before
+ * any stream capture, and do not use this entry point on a device after cudaDeviceReset.  All
+ * calls share the one array: calls that may overlap on the GPU (other streams, other handles,
+ * other threads) race on it and must be serialised by the caller.  Every region the forward
+ * uses is written before it is read, so nothing needs clearing between calls.
  */
 lapl_status lapl_attn_forward_noalloc(lapl_attn_handle h, const void* q, const void* k,
                                       const void* v, const float* bias, void* out, void* stream);

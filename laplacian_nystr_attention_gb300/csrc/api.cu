@@ -273,15 +273,16 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   };
   w.landmarks = take(bh * m * d);
   w.x = take(bh * m * m);
-  w.xs = take(g.cg ? 0 : bh * ((size_t)cfg->ns_steps + 1) * m * ((m + 3) & ~(size_t)3));
   w.at = take(bh * m * n);
   w.bt = take(bh * m * n);
   w.bvp = take(bh * g.bv_splits * m * d);
-  w.bv = take(g.cg ? 0 : bh * m * d);
-
   w.mmat = take(bh * m * d);
   w.mu = take(bh * m);
   w.rstd = take(bh * m);
+  w.fwd_total = off;
+  // Written only by lapl_attn_forward_train, read only by the backward pass.
+  w.xs = take(g.cg ? 0 : bh * ((size_t)cfg->ns_steps + 1) * m * ((m + 3) & ~(size_t)3));
+  w.bv = take(g.cg ? 0 : bh * m * d);
   w.total = off;
 
   // The side stream runs the shorter of the two chains (see the launch sequence).
@@ -306,17 +307,20 @@ lapl_status lapl_attn_workspace_size(lapl_attn_handle h, size_t* bytes) {
   return LAPL_OK;
 }
 
+// min_workspace: the workspace size the caller must provide (0: lapl_attn_workspace_size).
 static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k, const void* v,
                                const float* bias, void* out, void* workspace,
                                size_t workspace_bytes, cudaStream_t st,
-                               const lapl_attn_debug* dbg, bool keep = false) {
+                               const lapl_attn_debug* dbg, bool keep = false,
+                               size_t min_workspace = 0) {
   if (!p) return LAPL_ERR_INVALID_ARG;
   if (p->geo.bh == 0) return LAPL_OK;   // empty batch
   if (!q || !k || !v || !out || !workspace) return LAPL_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
       !aligned16(workspace) || (bias && ((uintptr_t)bias & 3u)))
     return LAPL_ERR_ALIGNMENT;
-  if (workspace_bytes < p->ws.total) return LAPL_ERR_WORKSPACE;
+  if (keep || min_workspace == 0) min_workspace = p->ws.total;
+  if (workspace_bytes < min_workspace) return LAPL_ERR_WORKSPACE;
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) {
@@ -534,13 +538,29 @@ lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void
   if (!aligned16(staging)) return LAPL_ERR_ALIGNMENT;
   const StagingLayout s = staging_layout(h);
   if (staging_bytes < s.total) return LAPL_ERR_WORKSPACE;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error(h, e, "forward_host/device");
+    return LAPL_ERR_CUDA;
+  }
+  if (dev != h->device) return LAPL_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* base = static_cast<char*>(staging);
   const size_t elems = (size_t)h->geo.bh * h->geo.n * h->geo.d;
   const size_t in_b = elems * elem_bytes(h->cfg.in_dtype);
   const size_t out_b = elems * elem_bytes(h->cfg.out_dtype);
-  cudaError_t e = cudaSuccess;
-  if (h->geo.ns_exclusive && !h->geo.cg) {
+  const bool side_copies = h->geo.ns_exclusive && !h->geo.cg;
+  // After the side stream has been given copies, every exit joins it back into the launching
+  // stream, so that a caller who synchronises that stream also waits for those copies before
+  // it frees or reuses the host inputs or the staging buffer.
+  auto fail = [&](lapl_status r, cudaError_t err, const char* where) {
+    if (err != cudaSuccess) set_error(h, err, where);
+    if (side_copies && cudaEventRecord(h->ev_join, h->side_stream) == cudaSuccess)
+      cudaStreamWaitEvent(st, h->ev_join, 0);
+    return r;
+  };
+  if (side_copies) {
     // The solve chain (pooling first) needs K only; Q and V are first read by the distance and
     // B V kernels, which run on the side stream.  So the side stream copies K, Q, V in that
     // order (after everything enqueued on the launching stream so far) and the launching
@@ -549,7 +569,11 @@ lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void
     cudaStream_t side = h->side_stream;
     e = cudaEventRecord(h->ev_pool, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->ev_pool, 0);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.k, k, in_b, cudaMemcpyHostToDevice, side);
+    if (e != cudaSuccess) {
+      set_error(h, e, "forward_host/h2d");
+      return LAPL_ERR_CUDA;
+    }
+    e = cudaMemcpyAsync(base + s.k, k, in_b, cudaMemcpyHostToDevice, side);
     if (e == cudaSuccess) e = cudaEventRecord(h->ev_join, side);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_join, 0);
     if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.q, q, in_b, cudaMemcpyHostToDevice, side);
@@ -565,18 +589,12 @@ lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void
     e = cudaMemcpyAsync(dbias, bias, (size_t)h->cfg.heads * h->geo.m * sizeof(float),
                         cudaMemcpyHostToDevice, st);
   }
-  if (e != cudaSuccess) {
-    set_error(h, e, "forward_host/h2d");
-    return LAPL_ERR_CUDA;
-  }
+  if (e != cudaSuccess) return fail(LAPL_ERR_CUDA, e, "forward_host/h2d");
   lapl_status r = run_forward(h, base + s.q, base + s.k, base + s.v, dbias, base + s.out,
                               base + s.ws, h->ws.total, st, nullptr);
-  if (r != LAPL_OK) return r;
+  if (r != LAPL_OK) return fail(r, cudaSuccess, "");
   e = cudaMemcpyAsync(out, base + s.out, out_b, cudaMemcpyDeviceToHost, st);
-  if (e != cudaSuccess) {
-    set_error(h, e, "forward_host/d2h");
-    return LAPL_ERR_CUDA;
-  }
+  if (e != cudaSuccess) return fail(LAPL_ERR_CUDA, e, "forward_host/d2h");
   return LAPL_OK;
 }
 
@@ -681,11 +699,13 @@ lapl_status lapl_attn_destroy(lapl_attn_handle h) {
 }  // extern "C"
 
 namespace lapl {
-// Internal: the plain forward on a caller-chosen workspace (used by noalloc.cu).
+// Internal: the plain forward on a caller-chosen workspace of at least ws.fwd_total bytes
+// (used by noalloc.cu; the regions only the training forward writes are not needed).
 lapl_status forward_on_workspace(lapl_attn_handle p, const void* q, const void* k, const void* v,
                                  const float* bias, void* out, void* workspace,
                                  size_t workspace_bytes, cudaStream_t st) {
-  return run_forward(p, q, k, v, bias, out, workspace, workspace_bytes, st, nullptr);
+  return run_forward(p, q, k, v, bias, out, workspace, workspace_bytes, st, nullptr, false,
+                     p ? p->ws.fwd_total : 0);
 }
 
 void record_error(lapl_attn_handle p, const char* text) {

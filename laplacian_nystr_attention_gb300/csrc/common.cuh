@@ -45,20 +45,23 @@ __host__ __device__ inline int part_owner(const Partition& pt, long long x) {
   return pt.rem + (int)((x - big) / pt.q);
 }
 
-// Offsets (bytes) of the workspace regions for one configuration.  All fp32.
+// Offsets (bytes) of the workspace regions for one configuration.  All fp32.  The regions
+// only the training forward writes (xs, bv) come last, so a plain forward needs only the
+// first fwd_total bytes.
 struct WorkspaceLayout {
   size_t landmarks;    // [BH, m, d]         pooled keys L
   size_t x;            // [BH, m, m]         Newton-Schulz result X
-  size_t xs;           // [BH, T + 1, m, mk] every Newton-Schulz iterate X_0 .. X_T, rows
-                       //                    padded to mk = 4 ceil(m / 4) (kept for the
-                       //                    backward pass; Newton-Schulz plans only)
   size_t at;           // [BH, m, N]         A = k(Q, L), landmark-major (A transposed)
   size_t bt;           // [BH, m, N]         B = k(L, K)
   size_t bvp;          // [BH, bv_splits, m, d]  per-split partial sums of B V
-  size_t bv;           // [BH, m, d]         B V (kept for the backward pass)
   size_t mmat;         // [BH, m, d]         M = X (B V)
   size_t mu;           // [BH, m]            column means of A
   size_t rstd;         // [BH, m]            1 / sqrt(column variance + delta)
+  size_t fwd_total;    // bytes a plain forward reads or writes (everything above)
+  size_t xs;           // [BH, T + 1, m, mk] every Newton-Schulz iterate X_0 .. X_T, rows
+                       //                    padded to mk = 4 ceil(m / 4) (kept for the
+                       //                    backward pass; Newton-Schulz plans only)
+  size_t bv;           // [BH, m, d]         B V (kept for the backward pass)
   size_t total;
 };
 

@@ -10,7 +10,13 @@
 // The array is a file-scope __device__ variable: every GPU that loads this library holds it
 // (kNoAllocScratchBytes) until the process exits.  Host code cannot use the array's name as a
 // device address, so the address is looked up once per device with cudaGetSymbolAddress, on the
-// first call made while that device is current.
+// first call made while that device is current, and cached for the life of the process.  A
+// cudaDeviceReset unloads the module, after which the cached address is stale: this entry
+// point must not be used on a device after it has been reset.
+//
+// Only the plain forward's regions are placed in the array (WorkspaceLayout::fwd_total): the
+// regions a training forward keeps for the backward pass lie past that offset and are never
+// touched here.
 #include <mutex>
 #include <stdio.h>
 
@@ -39,12 +45,12 @@ extern "C" lapl_status lapl_attn_forward_noalloc(lapl_attn_handle h, const void*
                                                  const void* k, const void* v,
                                                  const float* bias, void* out, void* stream) {
   if (!h) return LAPL_ERR_INVALID_ARG;
-  if (h->ws.total > kNoAllocScratchBytes) {
+  if (h->ws.fwd_total > kNoAllocScratchBytes) {
     char msg[160];
     snprintf(msg, sizeof(msg),
              "forward_noalloc: this configuration needs %zu workspace bytes, the static scratch "
              "holds %zu",
-             h->ws.total, kNoAllocScratchBytes);
+             h->ws.fwd_total, kNoAllocScratchBytes);
     lapl::record_error(h, msg);
     return LAPL_ERR_WORKSPACE;
   }

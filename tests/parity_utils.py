@@ -83,3 +83,48 @@ def run_gpu(w, q, k, v, bias=None, debug=False, out_dtype="f32", info=None, **cf
     inter = {kname: t.cpu().numpy().astype(np.float64) for kname, t in (dbg or {}).items()}
     att.close()
     return res, inter
+
+
+def host_threads() -> int:
+    import os
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def oracle_each_slice(cfg: dict, q, k, v, bias=None, slices=None):
+    """The oracle's output for each (b, h) slice, computed one slice per host thread (the
+    oracle's C call releases the GIL).  Each slice is its own 1 x 1 problem: every step of the
+    method is per (batch, head), so this is the same arithmetic as the full call.
+
+    Returns {s: [N, d] float64} for s = b * H + h over ``slices`` (default: all)."""
+    import concurrent.futures as cf
+
+    import oracle
+    B, H = int(cfg["batch"]), int(cfg["heads"])
+    one = dict(cfg, batch=1, heads=1)
+    todo = range(B * H) if slices is None else slices
+
+    def run(s):
+        b, h = divmod(s, H)
+        bb = None if bias is None else np.asarray(bias)[h:h + 1]
+        out, _ = oracle.forward(one, q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1],
+                                v[b:b + 1, h:h + 1], bias=bb)
+        return s, out[0, 0]
+
+    oracle.build()
+    with cf.ThreadPoolExecutor(max_workers=host_threads()) as ex:
+        return dict(ex.map(run, todo))
+
+
+def worst_slice(out: np.ndarray, refs: dict) -> tuple:
+    """(largest per-slice normwise error, its slice) of ``out`` [B,H,N,d] against
+    ``oracle_each_slice`` results."""
+    H = out.shape[1]
+    worst = (0.0, -1)
+    for s, r in refs.items():
+        b, h = divmod(s, H)
+        e = slice_rel_err(out[b, h][None, None], r[None, None])
+        worst = max(worst, (e, s))
+    return worst

@@ -19,7 +19,8 @@ import numpy as np
 import pytest
 
 from lapl_workloads import WORKLOADS, make_bias, make_inputs
-from parity_utils import TOL_BF16, TOL_F32, elem_rel, rel_to_max, run_gpu, slice_rel_err
+from parity_utils import (TOL_BF16, TOL_F32, elem_rel, oracle_each_slice, rel_to_max, run_gpu,
+                          slice_rel_err, worst_slice)
 
 pytestmark = pytest.mark.gpu
 
@@ -106,16 +107,18 @@ def test_workload_full(name):
 
 
 @pytest.mark.parametrize("name", ["hires_bf16", "sweep_f32_16384", "sweep_bf16_65536"])
-def test_workload_sampled_slices(name):
+def test_workload_every_slice(name):
+    """Full-size launch; the oracle computes every (b, h) slice, one per host thread."""
     w = WORKLOADS[name]
     q, k, v = make_inputs(w)
     out, _ = gpu_run(w, q, k, v)
-    nslices = w.batch * w.heads
-    for s0 in sorted({0, nslices - 1}):
-        ref, _ = oracle_run(w, q, k, v, slices=(s0, 1))
-        b, h = divmod(s0, w.heads)
-        err = slice_rel_err(out[b, h][None, None], ref[b, h][None, None])
-        assert err < tol_of(w), (s0, err)
+    assert np.isfinite(out).all()
+    cfg = w.config()
+    cfg["solver"] = CG
+    refs = oracle_each_slice(cfg, q, k, v)
+    assert len(refs) == w.batch * w.heads
+    err, s = worst_slice(out, refs)
+    assert err < tol_of(w), (s, err)
 
 
 EDGE = {

@@ -11,8 +11,8 @@ import numpy as np
 import pytest
 
 from lapl_workloads import WORKLOADS, make_bias, make_inputs
-from parity_utils import (TOL_BF16, TOL_F32, elem_rel, rel_to_max, run_gpu, slice_rel_err,
-                          to_device)
+from parity_utils import (TOL_BF16, TOL_F32, elem_rel, oracle_each_slice, rel_to_max, run_gpu,
+                          slice_rel_err, to_device, worst_slice)
 
 pytestmark = pytest.mark.gpu
 
@@ -84,8 +84,11 @@ def test_integer_variant_of_each_shape_bit_exact(name):
 
 # ---- the five workloads, end to end --------------------------------------------------------
 FULL = ["tiny_f32", "stage1_f32", "stage23_bf16"]
-SAMPLED = ["hires_bf16", "sweep_f32_1024", "sweep_f32_4096", "sweep_f32_16384",
-           "sweep_f32_65536", "sweep_bf16_1024", "sweep_bf16_65536"]
+# Large launches: the full-size forward on the GPU, then the oracle on every (b, h) slice, one
+# slice per host thread.  Covers the high-resolution shape and the whole sequence-length
+# sweep (fp32 and bf16, N = 1024 ... 65536).
+EVERY_SLICE = ["hires_bf16"] + [f"sweep_{dt}_{n}" for dt in ("f32", "bf16")
+                                for n in (1024, 4096, 16384, 65536)]
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -98,19 +101,17 @@ def test_workload_full(name):
     assert err < tol_of(w), err
 
 
-@pytest.mark.parametrize("name", SAMPLED)
-def test_workload_sampled_slices(name):
-    """Full-size launch; the oracle computes the first and the last (b,h) slice."""
+@pytest.mark.parametrize("name", EVERY_SLICE)
+def test_workload_every_slice(name):
+    """Full-size launch; the oracle computes every (b, h) slice."""
     w = WORKLOADS[name]
     q, k, v = make_inputs(w)
     out, _ = run_gpu(w, q, k, v)
-    nslices = w.batch * w.heads
-    for s0 in sorted({0, nslices - 1}):
-        ref, _ = oracle_run(w, q, k, v, slices=(s0, 1))
-        b, h = divmod(s0, w.heads)
-        err = slice_rel_err(out[b, h][None, None], ref[b, h][None, None])
-        assert err < tol_of(w), (s0, err)
     assert np.isfinite(out).all()
+    refs = oracle_each_slice(w.config(), q, k, v)
+    assert len(refs) == w.batch * w.heads
+    err, s = worst_slice(out, refs)
+    assert err < tol_of(w), (s, err)
 
 
 @pytest.mark.parametrize("name", ["hires_bf16", "sweep_f32_65536"])
