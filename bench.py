@@ -55,10 +55,13 @@ CDIST_TRAFFIC = {
     ("cp.async", "stage1_f32", "gaussian"): (
         13016576 + 0, "f4b35b7f8fd1127af71c0e7d6fe76d03c474923fbba7229c9325ced339798112"),
 }
-CDIST_SOURCES = ["cdist_kernel.cuh", "cdist_tma.cuh", "cdist.cu", "cdist_d32.cu", "cdist_d64.cu",
-                 "cdist_d0.cu", "cdist_tma_f32.cu", "cdist_tma_bf16.cu", "cdist_gauss_d32.cu",
-                 "cdist_gauss_d64.cu", "cdist_gauss_d0.cu"]
+CDIST_SOURCES = ["cdist_kernel.cuh", "cdist_tma.cuh", "cdist_l1.cuh", "cdist.cu", "cdist_d32.cu",
+                 "cdist_d64.cu", "cdist_d0.cu", "cdist_tma_f32.cu", "cdist_tma_bf16.cu",
+                 "cdist_l1.cu", "cdist_gauss_d32.cu", "cdist_gauss_d64.cu", "cdist_gauss_d0.cu"]
 CDIST_KERNEL = {
+    ("l1", "laplacian"): "cdist_l1_kernel (fused L1 distance + exp, query and key blocks; "
+                         "TMA-fed, helper warp, element terms split between the FP32 and ALU "
+                         "pipes)",
     ("tma", "laplacian"): "cdist_tma_kernel (fused L1 distance + exp, query and key blocks; "
                           "TMA-fed)",
     ("cp.async", "laplacian"): "cdist_exp_kernel (fused L1 distance + exp, query and key "
@@ -67,7 +70,7 @@ CDIST_KERNEL = {
                               "blocks; cp.async-fed)",
 }
 OPS_CONVENTION = {
-    "laplacian": "3 per (token, landmark, channel): subtract, abs, add (2 FP32 instructions)",
+    "laplacian": "3 per (token, landmark, channel): subtract, absolute value, add",
     "gaussian": "3 per (token, landmark, channel): subtract, multiply, add (a subtract and an "
                 "FMA)",
 }
@@ -449,7 +452,7 @@ def run_ours(args, w):
     peak = fp32_peak_tflops(props.multi_processor_count, sm_max)
     achieved = cdist_ops_per_launch(w) / (stage_ms["cdist"] / 1e3) / 1e12
     plan = lna.lapl_attn_plan_info_get(att.handle)
-    feed = "tma" if plan["cdist_tma"] else "cp.async"
+    feed = {2: "l1", 1: "tma"}.get(plan["cdist_tma"], "cp.async")
     rec = CDIST_TRAFFIC.get((feed, w.name, args.kernel))
     traffic = rec[0] if rec and rec[1] == cdist_sources_sha() else None
     clk = clocks.summary()

@@ -203,20 +203,38 @@ lapl_status lapl_attn_stage_marks(lapl_attn_handle h, float* ms);
 int lapl_attn_kernels_per_forward(lapl_attn_handle h);
 
 /*
- * Device-side failure report.  The distance kernel's TMA pipeline waits on shared-memory
- * barriers; every such wait gives up after one second, sets bit 1 of a device error word (one
- * per device, shared by all handles), and the waiting warp leaves the kernel, so a failed
- * forward ends instead of hanging and its outputs are undefined.  This call copies the word to
- * *flags, clears it, and synchronises `stream` (a cudaStream_t; enqueue it after the forwards
- * to be checked).  Returns LAPL_ERR_DEVICE_TIMEOUT (with a message in lapl_attn_last_error)
- * when a flag was set, LAPL_OK when none was, LAPL_ERR_CUDA if the copy fails.
+ * Device-side failure report.  Kernels that wait on shared-memory barriers (the distance
+ * kernel's TMA pipeline, the tensor-core Newton-Schulz solve) bound every such wait (one second
+ * by default); a wait that gives up sets a bit of a device error word (one per device, shared
+ * by all handles) -- bit 1 the distance kernel, bit 2 the tensor-core solve -- and the waiting
+ * warps leave the kernel after the copies and tensor-core operations they issued have
+ * completed, so a failed forward ends instead of hanging, the context stays usable, and its
+ * outputs are undefined.  This call copies the word to *flags, clears it, and synchronises
+ * `stream` (a cudaStream_t; enqueue it after the forwards to be checked).  Returns
+ * LAPL_ERR_DEVICE_TIMEOUT (with a message naming the kernel in lapl_attn_last_error) when a
+ * flag was set, LAPL_OK when none was, LAPL_ERR_CUDA if the copy fails.
  */
 lapl_status lapl_attn_device_errors(lapl_attn_handle h, void* stream, unsigned* flags);
 
+/*
+ * Fault injection, for testing the failure report above without faulting the GPU (the pages
+ * have no counterpart).  wait_ns: the bound of every barrier wait of this plan's distance kernel
+ * (0 restores the default of one second).  skip_last_copy = 1: the distance kernel's producer
+ * never issues the copy of each CTA's last chunk, so the waits on that chunk run out after
+ * wait_ns; nothing else is outstanding when they do.  Applies to the split-pipe distance kernel
+ * (plan_info cdist_tma = 2) and to forwards launched after the call.  0 = normal operation.
+ */
+lapl_status lapl_attn_set_fault_injection(lapl_attn_handle h, unsigned long long wait_ns,
+                                          int skip_last_copy);
+
 /* Launch choices of a plan (fixed at create). */
 typedef struct {
-  int cdist_tma;      /* 1: the distance kernel's token chunks are loaded by the Tensor Memory
-                         Accelerator; 0: by cp.async.  Same distances bit for bit.          */
+  int cdist_tma;      /* 2: the distance kernel's token chunks are loaded by the Tensor Memory
+                         Accelerator and half of each warp's landmarks take the
+                         q + l - 2 min(q, l) form on the ALU pipe (same distances bit for bit
+                         on integer inputs, to rounding otherwise); 1: TMA-fed, every term
+                         as |q - l|; 0: cp.async-fed, every term as |q - l|.  1 and 0 give
+                         the same distances bit for bit.                                    */
   int cdist_ctas;     /* persistent CTAs of the distance kernel                              */
   int cdist_threads;  /* threads per distance-kernel CTA                                     */
   int ns_cluster;     /* CTAs per head in the Newton-Schulz solve: 1, or 2 (a cluster pair,
@@ -229,13 +247,14 @@ typedef struct {
 } lapl_attn_plan_info;
 
 /*
- * Fill *info.  Choices made at create: the TMA feed for fp32 inputs with d = 32 and m <= 49 and
- * the Laplacian kernel, cp.async otherwise (always for the Gaussian kernel); for the solve one CTA per head, with tensor-core products for m >= 25
- * and CUDA-core products for m <= 16.  Environment
- * variables read at create override them: LAPL_ATTN_CDIST_FEED = "cp.async" (always) or "tma"
- * (wherever the TMA kernel exists: fp32 with d = 32 or 64, bf16 with d = 64, and
- * B*H*N >= 128); LAPL_ATTN_NS_KERNEL = "ffma", "pair" (a CTA pair per head, m > 32) or "tc"
- * (tensor-core products).
+ * Fill *info.  Choices made at create: for the Laplacian kernel with fp32 inputs, d = 32 or 64
+ * and m <= 49 the split-pipe TMA kernel (cdist_tma = 2); cp.async otherwise (always for the
+ * Gaussian kernel); for the solve one CTA per head, with tensor-core products for m >= 25 and
+ * CUDA-core products for m <= 16.  Environment variables read at create override them:
+ * LAPL_ATTN_CDIST_FEED = "cp.async" (always), "tma" (wherever the plain TMA kernel exists: fp32
+ * with d = 32 or 64, bf16 with d = 64) or "l1" (the split-pipe kernel, where it exists), both
+ * only with B*H*N >= 128; LAPL_ATTN_NS_KERNEL = "ffma", "pair" (a CTA pair per head, m > 32) or
+ * "tc" (tensor-core products).
  */
 lapl_status lapl_attn_plan_info_get(lapl_attn_handle h, lapl_attn_plan_info* info);
 

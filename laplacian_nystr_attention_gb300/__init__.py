@@ -18,7 +18,7 @@ from . import _lib
 from ._lib import (LAPL_BF16, LAPL_F32, LAPL_KERNEL_GAUSSIAN, LAPL_KERNEL_LAPLACIAN,
                    LAPL_SOLVER_CG, LAPL_SOLVER_NEWTON_SCHULZ, LaplAttnError, lapl_attn_config, lapl_attn_create,
                    lapl_attn_debug, lapl_attn_destroy, lapl_attn_device_errors,
-                   lapl_attn_forward,
+                   lapl_attn_forward, lapl_attn_set_fault_injection,
                    lapl_attn_forward_debug, lapl_attn_forward_host, lapl_attn_host_staging_size,
                    lapl_attn_kernels_per_forward, lapl_attn_last_error,
                    lapl_attn_set_timing, lapl_attn_stage_marks, lapl_attn_stage_times,
@@ -33,7 +33,8 @@ __all__ = [
     "lapl_attn_forward_host", "lapl_attn_host_staging_size", "lapl_attn_last_error",
     "lapl_attn_status_string", "lapl_attn_version", "lapl_attn_workspace_size", "LAPL_F32",
     "LAPL_BF16", "lapl_attn_set_timing", "lapl_attn_stage_times", "lapl_attn_stage_marks",
-    "lapl_attn_kernels_per_forward", "lapl_attn_device_errors", "lapl_attn_plan_info_get",
+    "lapl_attn_kernels_per_forward", "lapl_attn_device_errors", "lapl_attn_set_fault_injection",
+    "lapl_attn_plan_info_get",
     "make_config", "lapl_attn_backward", "lapl_attn_backward_kernels", "lapl_attn_forward_train",
     "lapl_attn_backward_workspace_size", "LAPL_KERNEL_LAPLACIAN", "LAPL_KERNEL_GAUSSIAN", "LAPL_SOLVER_NEWTON_SCHULZ",
     "LAPL_SOLVER_CG",

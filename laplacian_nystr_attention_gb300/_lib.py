@@ -87,6 +87,7 @@ def _load():
         "lapl_attn_kernels_per_forward": ([H], ctypes.c_int),
         "lapl_attn_forward_noalloc": ([H, vp, vp, vp, vp, vp, vp], st),
         "lapl_attn_device_errors": ([H, vp, ctypes.POINTER(ctypes.c_uint)], st),
+        "lapl_attn_set_fault_injection": ([H, ctypes.c_ulonglong, ctypes.c_int], st),
         "lapl_attn_plan_info_get": ([H, ctypes.POINTER(lapl_attn_plan_info)], st),
         "lapl_attn_backward_workspace_size": ([H, ctypes.POINTER(sz)], st),
         "lapl_attn_backward": ([H, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, sz, vp], st),
@@ -107,7 +108,8 @@ EXPORTED = ["lapl_attn_version", "lapl_attn_status_string", "lapl_attn_last_erro
             "lapl_attn_forward_debug", "lapl_attn_host_staging_size", "lapl_attn_forward_host",
             "lapl_attn_set_timing", "lapl_attn_stage_times", "lapl_attn_stage_marks",
             "lapl_attn_kernels_per_forward",
-            "lapl_attn_forward_noalloc", "lapl_attn_device_errors", "lapl_attn_plan_info_get",
+            "lapl_attn_forward_noalloc", "lapl_attn_device_errors",
+            "lapl_attn_set_fault_injection", "lapl_attn_plan_info_get",
             "lapl_attn_backward_workspace_size", "lapl_attn_backward",
             "lapl_attn_backward_kernels", "lapl_attn_destroy"]
 
@@ -236,6 +238,11 @@ def lapl_attn_device_errors(handle, stream) -> int:
     _check(LIB.lapl_attn_device_errors(handle, stream, ctypes.byref(flags)),
            "lapl_attn_device_errors", handle)
     return flags.value
+
+
+def lapl_attn_set_fault_injection(handle, wait_ns: int, skip_last_copy: int) -> None:
+    _check(LIB.lapl_attn_set_fault_injection(handle, int(wait_ns), int(skip_last_copy)),
+           "lapl_attn_set_fault_injection", handle)
 
 
 def lapl_attn_plan_info_get(handle) -> dict:

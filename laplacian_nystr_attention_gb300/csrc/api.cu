@@ -121,6 +121,8 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   if (!p) return LAPL_ERR_INVALID_ARG;
   p->cfg = *cfg;
   p->last_error[0] = '\0';
+  p->cd_wait_ns = 1000000000ull;   // one second
+  p->cd_skip_last_copy = 0;
   p->neg_log2e_over_lambda = (float)(-1.4426950408889634 / (double)cfg->lambda);
 
   Geometry& g = p->geo;
@@ -666,16 +668,27 @@ lapl_status lapl_attn_device_errors(lapl_attn_handle h, void* stream, unsigned* 
   *flags = word;
   if (word) {
     snprintf(h->last_error, sizeof(h->last_error),
-             "device error flags 0x%x: a pipeline wait in the distance kernel gave up", word);
+             "device error flags 0x%x: a bounded barrier wait gave up in%s%s%s", word,
+             (word & kErrBitCdist) ? " the distance kernel" : "",
+             ((word & kErrBitCdist) && (word & kErrBitSolve)) ? " and" : "",
+             (word & kErrBitSolve) ? " the tensor-core Newton-Schulz solve" : "");
     return LAPL_ERR_DEVICE_TIMEOUT;
   }
+  return LAPL_OK;
+}
+
+lapl_status lapl_attn_set_fault_injection(lapl_attn_handle h, unsigned long long wait_ns,
+                                          int skip_last_copy) {
+  if (!h || (skip_last_copy != 0 && skip_last_copy != 1)) return LAPL_ERR_INVALID_ARG;
+  h->cd_wait_ns = wait_ns ? wait_ns : 1000000000ull;
+  h->cd_skip_last_copy = skip_last_copy;
   return LAPL_OK;
 }
 
 lapl_status lapl_attn_plan_info_get(lapl_attn_handle h, lapl_attn_plan_info* info) {
   if (!h || !info) return LAPL_ERR_INVALID_ARG;
   const Geometry& g = h->geo;
-  info->cdist_tma = g.cd_tma ? 1 : 0;
+  info->cdist_tma = g.cd_l1 ? 2 : (g.cd_tma ? 1 : 0);
   info->cdist_ctas = g.cd_part.ctas;
   info->cdist_threads = g.cd_threads;
   info->ns_cluster = g.ns_cluster;

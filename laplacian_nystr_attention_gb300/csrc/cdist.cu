@@ -9,14 +9,19 @@
 //   cdist_exp_kernel (cdist_kernel.cuh) chunks loaded with cp.async by the whole CTA, every
 //                                      shape, and the only one with Gaussian-kernel (squared
 //                                      l2 distance) instantiations.
-// Automatic choice for the Laplacian kernel: the TMA feed for fp32, d = 32, s <= 7 (as fast as cp.async there); cp.async
-// elsewhere (faster where the TMA kernel's extra producer warp costs registers, s = 8, or its
-// consumer warps each widen the same bf16 chunk).  The environment variable
-// LAPL_ATTN_CDIST_FEED=tma or =cp.async, read at plan creation, overrides the choice (tma only
-// where it is instantiated and the tensor holds at least one chunk of rows).
+//   cdist_l1_kernel (cdist_l1.cuh)     TMA-fed like cdist_tma_kernel, with a helper warp and the
+//                                      element work split between the FP32 and ALU pipes;
+//                                      fp32, d in {32, 64}, s <= 7, Laplacian kernel.
+// Automatic choice for the Laplacian kernel: cdist_l1_kernel wherever it is instantiated;
+// otherwise the TMA feed for fp32, d = 32, s <= 7; cp.async elsewhere (faster where the TMA
+// kernel's extra producer warp costs registers, s = 8, or its consumer warps each widen the
+// same bf16 chunk).  The environment variable LAPL_ATTN_CDIST_FEED=l1, =tma or =cp.async, read at
+// plan creation, overrides the choice (l1 and tma only where instantiated and the tensor holds
+// at least one chunk of rows).
 #include <stdlib.h>
 #include <string.h>
 
+#include "cdist_l1.cuh"
 #include "cdist_tma.cuh"
 
 namespace lapl {
@@ -120,22 +125,36 @@ cudaError_t cdist_plan(lapl_attn_plan& p, int* ctas_per_sm) {
   g.cd_rows = cdist_impl::kRows;
   g.cd_tile = 32 * g.cd_rows;
   const char* feed = getenv("LAPL_ATTN_CDIST_FEED");
+  const bool want_l1 = feed && strcmp(feed, "l1") == 0;
   const bool want_tma = feed && strcmp(feed, "tma") == 0;
   const bool want_cpasync = feed && strcmp(feed, "cp.async") == 0;
   const bool gauss = p.cfg.kernel == LAPL_KERNEL_GAUSSIAN;
-  const bool auto_tma = !bf16 && g.d == 32 && g.s <= 7;
   const long long rows = (long long)g.bh * g.n;
-  const void* f = gauss ? nullptr : cdist_tma::pick(g.s, g.d, bf16);
   // Tensor-map coordinates are 32-bit; a box must not be taller than the tensor.
-  g.cd_tma = f && (want_tma || (auto_tma && !want_cpasync)) && rows >= cdist_tma::kTile &&
-             rows < (1LL << 31) && cdist_tma::encoder() != nullptr;
-  if (g.cd_tma) {
+  const bool tma_ok = rows >= cdist_tma::kTile && rows < (1LL << 31) &&
+                      cdist_tma::encoder() != nullptr;
+  // The split-pipe kernel: fp32, d = 32 or 64, the Laplacian kernel, s <= 7 (eight landmarks
+  // per warp overflow the register budget of two CTAs per SM).
+  const void* fl1 = (!bf16 && !gauss && g.s <= 7) ? cdist_l1::kernel(g.s, g.d) : nullptr;
+  g.cd_l1 = fl1 && tma_ok && (want_l1 || (!want_tma && !want_cpasync));
+  const void* f = nullptr;
+  if (g.cd_l1) {
+    f = fl1;
+    g.cd_tma = false;
     g.cd_threads = 32 * (g.s + 1);
-    g.cd_smem = cdist_tma::smem_bytes(g.s, g.d, bf16);
+    g.cd_smem = cdist_l1::smem_bytes(g.s, g.d);
   } else {
-    f = cdist_impl::pick(g.s, g.d, bf16, gauss);
-    g.cd_threads = 32 * g.s;
-    g.cd_smem = cdist_impl::smem_bytes(g.s, g.d, g.cd_tile, bf16);
+    const bool auto_tma = !bf16 && g.d == 32 && g.s <= 7;
+    f = gauss ? nullptr : cdist_tma::pick(g.s, g.d, bf16);
+    g.cd_tma = f && (want_tma || (auto_tma && !want_cpasync)) && tma_ok;
+    if (g.cd_tma) {
+      g.cd_threads = 32 * (g.s + 1);
+      g.cd_smem = cdist_tma::smem_bytes(g.s, g.d, bf16);
+    } else {
+      f = cdist_impl::pick(g.s, g.d, bf16, gauss);
+      g.cd_threads = 32 * g.s;
+      g.cd_smem = cdist_impl::smem_bytes(g.s, g.d, g.cd_tile, bf16);
+    }
   }
   if (!f) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.cd_smem);
@@ -148,7 +167,7 @@ cudaError_t launch_cdist(const lapl_attn_plan& p, const void* q, const void* k, 
                          float* dbg_dlk, float* dbg_a, cudaStream_t st) {
   const Geometry& g = p.geo;
   const bool bf16 = p.cfg.in_dtype == LAPL_BF16;
-  if (g.cd_tma) {
+  if (g.cd_tma || g.cd_l1) {
     const long long rows = (long long)g.bh * g.n;
     if (p.tmap_q_ptr != q) {
       if (!cdist_tma::encode(&p.tmap_q, q, rows, g.d, bf16)) return cudaErrorInvalidValue;
@@ -157,6 +176,22 @@ cudaError_t launch_cdist(const lapl_attn_plan& p, const void* q, const void* k, 
     if (p.tmap_k_ptr != k) {
       if (!cdist_tma::encode(&p.tmap_k, k, rows, g.d, bf16)) return cudaErrorInvalidValue;
       p.tmap_k_ptr = k;
+    }
+    if (g.cd_l1) {
+      cdist_l1::Args a;
+      a.landmarks = landmarks; a.at = at; a.bt = bt; a.err = p.dev_err;
+      a.dbg_dql = dbg_dql; a.dbg_dlk = dbg_dlk; a.dbg_a = dbg_a;
+      a.part = g.cd_part;
+      a.bh_count = g.bh;
+      a.n = g.n;
+      a.c_exp = p.neg_log2e_over_lambda;
+      a.wait_ns = p.cd_wait_ns;
+      a.skip_last_copy = p.cd_skip_last_copy;
+      const void* f = cdist_l1::kernel(g.s, g.d);
+      if (!f) return cudaErrorInvalidValue;
+      void* args[] = {&a, &p.tmap_q, &p.tmap_k};
+      return cudaLaunchKernel(f, dim3((unsigned)g.cd_part.ctas), dim3(g.cd_threads), args,
+                              g.cd_smem, st);
     }
     cdist_tma::TmaArgs a;
     a.landmarks = landmarks; a.at = at; a.bt = bt; a.err = p.dev_err;

@@ -34,7 +34,7 @@ using cdist_impl::abs_diff_acc;
 constexpr int kStages = 2;
 constexpr int kLmSlots = kStages;
 constexpr int kTile = 128;                          // tokens per chunk (rows of a TMA box)
-constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrTimeout = kErrBitCdist;
 constexpr unsigned long long kWaitNs = 1000000000ull;   // bound of one mbarrier wait
 
 struct TmaArgs {
@@ -233,8 +233,10 @@ cdist_tma_kernel(const TmaArgs a, const __grid_constant__ CUtensorMap map_q,
   constexpr unsigned kLmBytes = M * DH * 4;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // Stages need 1024-byte alignment (128-byte swizzle atom).
-  unsigned char* base = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte alignment of the stages (128-byte swizzle atom), by pointer arithmetic on the
+  // shared array itself so that every access stays a shared-memory access (a round trip through
+  // an integer would turn them into generic loads).
+  unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* stages = base;                                          // kStages x kStageBytes
   float* lms = reinterpret_cast<float*>(stages + kStages * kStageBytes);  // kLmSlots x [M][DH]
   unsigned long long* full = reinterpret_cast<unsigned long long*>(lms + kLmSlots * M * DH);

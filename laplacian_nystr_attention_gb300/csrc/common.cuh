@@ -14,6 +14,10 @@
 
 namespace lapl {
 
+// Bits of the device error word (set by a kernel whose bounded barrier wait gave up).
+constexpr unsigned kErrBitCdist = 1u;   // distance kernel (TMA pipeline)
+constexpr unsigned kErrBitSolve = 2u;   // Newton-Schulz solve on the tensor cores
+
 constexpr int kMaxS = 8;            // landmark grid side: m = s*s <= 64
 constexpr int kMaxM = kMaxS * kMaxS;
 constexpr int kMaxD = 128;
@@ -89,6 +93,8 @@ struct Geometry {
   int cd_rows;             // tokens per thread in the distance kernel
   int cd_tile;             // tokens per distance chunk = 32 * cd_rows
   bool cd_tma;             // distance kernel fed by TMA (cdist_tma.cuh), else by cp.async
+  bool cd_l1;              // the TMA-fed kernel with the split FP32/ALU element arithmetic
+                           // (cdist_l1.cuh); excludes cd_tma
   int cd_threads;          // threads of a distance-kernel CTA
   Partition cd_part;       // balanced split over cd_part.ctas persistent CTAs
   int bv_splits;           // B V: CTAs per head
@@ -139,6 +145,10 @@ struct lapl_attn_plan {
   mutable CUtensorMap tmap_q, tmap_k;
   mutable const void* tmap_q_ptr;
   mutable const void* tmap_k_ptr;
+  // Fault injection for tests (lapl_attn_set_fault_injection): bound of the distance kernel's
+  // barrier waits, and whether its producer skips each CTA's last copy.
+  unsigned long long cd_wait_ns;
+  int cd_skip_last_copy;
   char last_error[256];
 };
 
@@ -164,7 +174,8 @@ cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float*
 // Distance kernel choice for a plan: sets geo.cd_tma, cd_tile, cd_rows, cd_threads and cd_smem,
 // opts in to the shared memory and returns the resident CTAs per SM.
 cudaError_t cdist_plan(lapl_attn_plan& p, int* ctas_per_sm);
-// Address of the library's device error word (bit kErrTimeout: a bounded wait gave up).
+// Address of the library's device error word: one bit per kernel whose bounded wait gave up
+// (kErrBitCdist, kErrBitSolve).
 cudaError_t device_error_word(unsigned** word);
 // Shared-memory sizes, needed at plan time to size grids and opt in to > 48 KB.
 size_t ns_smem_bytes(int m, int d);

@@ -39,7 +39,7 @@ constexpr unsigned kSbo = 128;                 // bytes between row-adjacent cor
 constexpr unsigned kOpBytes = 128 * 64 * 4;    // one 128 x 64 TF32 operand
 constexpr unsigned kTmemCols = 128;
 constexpr unsigned long long kWaitNs = 1000000000ull;
-constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrTimeout = kErrBitSolve;
 
 // Offsets (bytes) in dynamic shared memory.
 constexpr unsigned kOffWW = 0;                         // [W_hi; W_lo]      (Bt of P^T = X W)

@@ -118,3 +118,10 @@ def test_python_binding_raises_typed_errors(lib):
     with pytest.raises(lib.LaplAttnError) as ei:
         lib.lapl_attn_create(base_cfg(lib, num_landmarks=15))
     assert ei.value.status == lib.LAPL_ERR_UNSUPPORTED
+
+
+def test_binding_wraps_every_declared_entry_point(lib):
+    """The Python binding carries a same-name wrapper for every entry point the header
+    declares (argument marshalling only)."""
+    for name in declared_entry_points():
+        assert callable(getattr(lib, name, None)), name

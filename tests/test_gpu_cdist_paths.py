@@ -1,14 +1,18 @@
-"""The two feeds of the fused distance + exp kernel against the oracle and each other.
+"""The three variants of the fused distance + exp kernel against the oracle and each other.
 
-The kernel exists twice: token chunks brought into shared memory by the Tensor Memory
-Accelerator (a producer warp and mbarriers; fp32 with d = 32 or 64, bf16 with d = 64) and by
-cp.async (every shape); LAPL_ATTN_CDIST_FEED=tma / =cp.async at plan creation forces either.  Both add
-|x_c - l_c| over the channels in the same order, so their distances agree bit for bit.  On
-small-integer inputs pooled over a power-of-two window the landmarks are dyadic and every
-distance is exact in fp32, so both feeds equal the oracle exactly; other windows round the
-landmark and are compared within 1e-5.  The partitions may differ (the two
-kernels have different occupancy), so the whitening statistics, and O, agree to rounding.
-Every case ends with the device error word clear (no bounded wait gave up).
+  "tma"       token chunks brought into shared memory by the Tensor Memory Accelerator (a
+              producer warp and mbarriers; fp32 with d = 32 or 64, bf16 with d = 64);
+  "cp.async"  chunks copied by the whole CTA (every shape);
+  "l1"        TMA-fed with a helper warp, and half of each warp's landmarks computed through
+              |q - l| = q + l - 2 min(q, l) on the ALU pipe (fp32, d = 32 or 64, s <= 7).
+LAPL_ATTN_CDIST_FEED at plan creation forces one.  "tma" and "cp.async" add |x_c - l_c| over
+the channels in the same order, so their distances agree bit for bit; "l1" rounds differently
+on float inputs (agreement to 1e-6 relative).  On small-integer inputs pooled over a
+power-of-two window the landmarks are dyadic and every partial sum of every form is exact in
+fp32, so all three equal the oracle exactly; other windows round the landmark and are compared
+within 1e-5.  The partitions may differ (the kernels have different occupancy), so the
+whitening statistics, and O, agree to rounding.  Every case ends with the device error word
+clear (no bounded wait gave up).
 """
 import numpy as np
 import pytest
@@ -46,6 +50,28 @@ CASES = {
 }
 
 
+FEEDS = ("tma", "cp.async", "l1")
+
+
+def _expected_variant(w, feed) -> int:
+    """plan_info cdist_tma for a forced feed: 2 (l1), 1 (tma) or 0 (cp.async); a feed that has
+    no instantiation for the shape falls back to the automatic choice."""
+    s = int(round(w.num_landmarks ** 0.5))
+    rows_ok = w.batch * w.heads * w.n >= 128
+    has_l1 = w.dtype == "f32" and w.head_dim in (32, 64) and s <= 7 and rows_ok
+    has_tma = rows_ok and ((w.dtype == "f32" and w.head_dim in (32, 64)) or
+                           (w.dtype == "bf16" and w.head_dim == 64))
+    if feed == "l1" and has_l1:
+        return 2
+    if feed == "tma" and has_tma:
+        return 1
+    if feed == "cp.async":
+        return 0
+    if has_l1:
+        return 2
+    return int(has_tma and w.dtype == "f32" and w.head_dim == 32 and s <= 7)
+
+
 def _dyadic_window(w) -> bool:
     s = int(round(w.num_landmarks ** 0.5))
     win = (w.grid_h // s) * (w.grid_w // s)
@@ -69,18 +95,18 @@ def _built():
 
 
 @pytest.mark.parametrize("case", sorted(CASES))
-def test_both_feeds_match_oracle_and_each_other(case, monkeypatch):
-    over, expect_tma = CASES[case]
+def test_all_feeds_match_oracle_and_each_other(case, monkeypatch):
+    over, _ = CASES[case]
     w = TINY.replace(dist="integer", **over)
     q, k, v = make_inputs(w, seed=3)
     ref, o = _oracle(w, q, k, v)
     runs = {}
-    for feed in ("tma", "cp.async"):
+    for feed in FEEDS:
         monkeypatch.setenv("LAPL_ATTN_CDIST_FEED", feed)
         info = {}
         out, g = run_gpu(w, q, k, v, debug=True, info=info)
         assert info["device_errors"] == 0, feed
-        assert info["cdist_tma"] == int(expect_tma and feed == "tma"), feed
+        assert info["cdist_tma"] == _expected_variant(w, feed), feed
         for name in ("d_ql", "d_lk", "d_ll", "landmarks"):
             if _dyadic_window(w):
                 assert np.array_equal(g[name], o[name]), (feed, name)
@@ -89,36 +115,50 @@ def test_both_feeds_match_oracle_and_each_other(case, monkeypatch):
         tol = TOL_BF16 if w.dtype == "bf16" else TOL_F32
         assert slice_rel_err(out, ref) < tol, feed
         runs[feed] = (out, g)
-    (o1, g1), (o2, g2) = runs["tma"], runs["cp.async"]
-    for name in ("d_ql", "d_lk", "a"):
-        assert np.array_equal(g1[name], g2[name]), name
-    assert slice_rel_err(o1, o2) < 1e-5
+    if _dyadic_window(w):
+        for feed in ("cp.async", "l1"):
+            for name in ("d_ql", "d_lk", "a"):
+                assert np.array_equal(runs["tma"][1][name], runs[feed][1][name]), (feed, name)
+    for feed in ("cp.async", "l1"):
+        assert slice_rel_err(runs["tma"][0], runs[feed][0]) < 1e-5, feed
 
 
-@pytest.mark.parametrize("name", ["stage1_f32", "stage23_bf16", "hires_bf16"])
+SHAPES = {name: WORKLOADS[name] for name in ("stage1_f32", "stage23_bf16", "hires_bf16")}
+SHAPES["stage23_as_f32"] = WORKLOADS["stage23_bf16"].replace(dtype="f32")   # d = 64, m = 49
+
+
+@pytest.mark.parametrize("name", sorted(SHAPES))
 def test_workload_shape_feeds_agree(name, monkeypatch):
-    """Full launch configuration of the workload, Gaussian-valued inputs: A from both feeds is
-    identical bit for bit, O agrees to rounding."""
-    w = WORKLOADS[name]
+    """Full launch configuration of the workload, float inputs: the distances of the tma and
+    cp.async feeds are identical bit for bit, those of the l1 kernel (where it exists) agree to
+    1e-6 relative; O agrees to rounding."""
+    w = SHAPES[name]
     q, k, v = make_inputs(w, seed=11)
     outs = {}
-    for feed in ("tma", "cp.async"):
+    for feed in FEEDS:
         monkeypatch.setenv("LAPL_ATTN_CDIST_FEED", feed)
         info = {}
         outs[feed] = run_gpu(w, q, k, v, debug=True, info=info)
-        assert info["cdist_tma"] == int(feed == "tma")
+        assert info["cdist_tma"] == _expected_variant(w, feed), feed
         assert info["device_errors"] == 0
-    (o1, g1), (o2, g2) = outs["tma"], outs["cp.async"]
-    assert np.array_equal(g1["d_ql"], g2["d_ql"])
-    assert np.array_equal(g1["d_lk"], g2["d_lk"])
+    (o1, g1), (o2, g2), (o3, g3) = outs["tma"], outs["cp.async"], outs["l1"]
+    if w.dtype == "bf16" or w.head_dim == 32:      # the plain TMA kernel exists
+        assert np.array_equal(g1["d_ql"], g2["d_ql"])
+        assert np.array_equal(g1["d_lk"], g2["d_lk"])
+    for name in ("d_ql", "d_lk"):
+        assert elem_rel(g3[name], g2[name]) < 1e-6, name
+    # A = exp(-D / lambda): a relative change e of D moves A by about e * D / lambda relative
+    # (D / lambda reaches 20 here), plus the exponential's few ulp.
+    assert elem_rel(g3["a"], g2["a"], floor_frac=1e-3) < 5e-5
     assert slice_rel_err(o1, o2) < 1e-5
+    assert slice_rel_err(o3, o2) < 1e-5
 
 
 @pytest.mark.parametrize("over,expect", [
-    (dict(grid_h=56, grid_w=56, num_landmarks=49), True),                    # fp32, d = 32
-    (dict(grid_h=56, grid_w=56, num_landmarks=64), False),                   # s = 8
-    (dict(grid_h=28, grid_w=28, head_dim=64, num_landmarks=49), False),      # d = 64
-    (dict(grid_h=28, grid_w=28, head_dim=64, num_landmarks=49, dtype="bf16"), False),
+    (dict(grid_h=56, grid_w=56, num_landmarks=49), 2),                      # fp32, d = 32
+    (dict(grid_h=56, grid_w=56, num_landmarks=64), 0),                      # s = 8
+    (dict(grid_h=28, grid_w=28, head_dim=64, num_landmarks=49), 2),         # fp32, d = 64
+    (dict(grid_h=28, grid_w=28, head_dim=64, num_landmarks=49, dtype="bf16"), 0),
 ])
 def test_automatic_feed_choice(over, expect, monkeypatch):
     import laplacian_nystr_attention_gb300 as lna
@@ -126,6 +166,6 @@ def test_automatic_feed_choice(over, expect, monkeypatch):
     w = TINY.replace(**over)
     h = lna.lapl_attn_create(lna.make_config(**{**w.config(), "in_dtype": w.dtype}))
     try:
-        assert lna.lapl_attn_plan_info_get(h)["cdist_tma"] == int(expect)
+        assert lna.lapl_attn_plan_info_get(h)["cdist_tma"] == expect
     finally:
         lna.lapl_attn_destroy(h)
