@@ -199,7 +199,8 @@ lapl_status lapl_attn_stage_times(lapl_attn_handle h, float* ms);
 lapl_status lapl_attn_stage_marks(lapl_attn_handle h, float* ms);
 
 /* Number of kernels one forward launches (for launch accounting): 6, or 5 with the CG
- * solver. */
+ * solver; one more when B V runs on the tensor cores with whitening on (plan_info
+ * bv_tensor_core: the column statistics are then a launch of their own). */
 int lapl_attn_kernels_per_forward(lapl_attn_handle h);
 
 /*
@@ -244,6 +245,8 @@ typedef struct {
   int ns_exclusive;   /* 1: the solve is the longer chain and runs first, on the launching
                          stream, with SMs to itself; 0: the distance kernel is               */
   int bv_splits;      /* CTAs per head of the B V kernel                                     */
+  int bv_tensor_core; /* 1: B V on the tensor cores (TF32 high/low split, fp32 accumulation;
+                         d a multiple of 16, N a multiple of 4); 0: CUDA-core FMA tiles     */
 } lapl_attn_plan_info;
 
 /*

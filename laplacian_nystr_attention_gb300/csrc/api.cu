@@ -206,9 +206,36 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   }
   if (e == cudaSuccess && !g.cg) e = bwd_configure(*p);
   if (e == cudaSuccess) {
-    g.bv_threads = bv_threads(g.m, g.d);
-    g.bv_smem = bv_smem_bytes(g.m, g.d, g.bv_threads, cfg->in_dtype == LAPL_BF16);
-    e = bv_configure(g.bv_smem);
+    // B V on the tensor cores where the shapes allow it: the MMA's N (d for bf16 V, 2d for
+    // fp32 V) at most 256, and d a multiple of 16 (the accumulator is read 16 columns at a
+    // time); LAPL_ATTN_BV=cuda forces the CUDA-core kernel.
+    const bool bf16 = cfg->in_dtype == LAPL_BF16;
+    const int nb = bf16 ? g.d : 2 * g.d;
+    const char* bvk = getenv("LAPL_ATTN_BV");
+    // The B^T tensor map needs rows of 16-byte multiples (N % 4 == 0); its boxes are m <= 64
+    // rows and the M kernel's reduction order is unchanged.
+    // Automatic choice: N >= 4096.  Shorter sequences give each CTA a few dozen 32-token
+    // chunks, too few to amortise the pipeline's start-up; there the CUDA-core kernel measured
+    // faster (stage-1 shape 16.4 vs 20.5 us) or equal.  LAPL_ATTN_BV=tc forces it.
+    const bool want_tc = bvk && strcmp(bvk, "tc") == 0;
+    const bool want_cuda = bvk && strcmp(bvk, "cuda") == 0;
+    g.bv_tc = g.d % 16 == 0 && nb <= 256 && g.n % 4 == 0 && g.bh * g.n < (1LL << 31) &&
+              g.bh * g.m < (1LL << 31) && !want_cuda && (want_tc || g.n >= 4096);
+    int smem_optin = 0;
+    if (g.bv_tc &&
+        cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device) ==
+            cudaSuccess &&
+        bv_tc_smem_bytes(g.d, bf16) > (size_t)smem_optin)
+      g.bv_tc = false;           // fp32 V with d = 128: the operand stages do not fit
+    if (g.bv_tc) {
+      g.bv_threads = bv_tc_threads();
+      g.bv_smem = bv_tc_smem_bytes(g.d, bf16);
+      e = bv_tc_configure(g.bv_smem);
+    } else {
+      g.bv_threads = bv_threads(g.m, g.d);
+      g.bv_smem = bv_smem_bytes(g.m, g.d, g.bv_threads, bf16);
+      e = bv_configure(g.bv_smem);
+    }
   }
   if (e != cudaSuccess) {
     set_error(p, e, "create/configure");
@@ -219,8 +246,11 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   {
     // Column statistics of A: one warp per landmark column, placed before the B V CTAs in
     // their grid.
-    const int warps = g.bv_threads / 32;
+    // With the tensor-core B V they are a launch of their own, 256 threads each.
+    g.stat_threads = g.bv_tc ? 256 : g.bv_threads;
+    const int warps = g.stat_threads / 32;
     g.stat_ctas = cfg->whiten ? (int)(g.bh * ((g.m + warps - 1) / warps)) : 0;
+    const long long stat_in_grid = g.bv_tc ? 0 : g.stat_ctas;
     // B V: whole 64-token chunks per CTA, on the SMs the solve leaves free (it keeps its own
     // when ns_exclusive).  The kernel's time is about the waves of resident CTAs (statistics
     // CTAs counted as B V CTAs) times the chunks of one CTA plus one for its prologue and
@@ -229,15 +259,21 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
     // columns in shared memory (64 splits at m = 64: 146 KB).
     constexpr int kMaxBvSplits = 64;
     const long long bh1 = g.bh > 0 ? g.bh : 1;
-    const int tiles = std::max(1, (g.n + bv_tile_tokens() - 1) / bv_tile_tokens());
+    const int tile_tokens = g.bv_tc ? bv_tc_tile_tokens() : bv_tile_tokens();
+    const int tiles = std::max(1, (g.n + tile_tokens - 1) / tile_tokens);
     long long sms = p->num_sms;
     if (g.ns_exclusive) sms -= g.bh * g.ns_cluster;
-    const long long slots = std::max<long long>(sms, 1) * bv_occupancy(g.bv_threads, g.bv_smem);
+    const int occ = g.bv_tc ? bv_tc_occupancy(g.bv_smem, cfg->in_dtype == LAPL_BF16)
+                            : bv_occupancy(g.bv_threads, g.bv_smem);
+    const long long slots = std::max<long long>(sms, 1) * occ;
     long long best = -1;
+    // The tensor-core kernel streams its tiles through a pipeline whose start-up and epilogue
+    // cost several tiles: one wave of as few CTAs as fill the SMs.
+    const int startup = g.bv_tc ? 8 : 1;
     for (int want = 1; want <= std::min(tiles, kMaxBvSplits); ++want) {
       const int tps = (tiles + want - 1) / want, splits = (tiles + tps - 1) / tps;
-      const long long waves = (bh1 * splits + g.stat_ctas + slots - 1) / slots;
-      const long long cost = waves * (tps + 1);
+      const long long waves = (bh1 * splits + stat_in_grid + slots - 1) / slots;
+      const long long cost = waves * (tps + startup);
       if (best < 0 || cost < best) {
         best = cost;
         g.bv_tiles_per_split = tps;
@@ -651,7 +687,9 @@ lapl_status lapl_attn_stage_marks(lapl_attn_handle h, float* ms) {
 
 int lapl_attn_kernels_per_forward(lapl_attn_handle h) {
   if (!h || h->geo.bh == 0) return 0;
-  return h->geo.cg ? 5 : 6;
+  // The tensor-core B V runs after a statistics launch of its own.
+  const int stats = (h->geo.bv_tc && h->geo.stat_ctas > 0) ? 1 : 0;
+  return (h->geo.cg ? 5 : 6) + stats;
 }
 
 lapl_status lapl_attn_device_errors(lapl_attn_handle h, void* stream, unsigned* flags) {
@@ -695,6 +733,7 @@ lapl_status lapl_attn_plan_info_get(lapl_attn_handle h, lapl_attn_plan_info* inf
   info->ns_tensor_core = g.ns_tc ? 1 : 0;
   info->ns_exclusive = g.ns_exclusive ? 1 : 0;
   info->bv_splits = g.bv_splits;
+  info->bv_tensor_core = g.bv_tc ? 1 : 0;
   return LAPL_OK;
 }
 

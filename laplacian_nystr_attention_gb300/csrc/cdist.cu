@@ -109,6 +109,19 @@ bool encode(CUtensorMap* map, const void* base, long long rows, int d, bool bf16
 }
 }  // namespace cdist_tma
 
+bool tma_encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint64_t inner,
+                   uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  const cdist_tma::EncodeTiledFn fn = cdist_tma::encoder();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Error bits raised by device-side bounded waits; read and cleared by lapl_attn_device_errors.
 __device__ unsigned g_device_errors;
 

@@ -530,6 +530,15 @@ cudaError_t launch_bv(const lapl_attn_plan& p, const float* bt, const void* v, f
                       const float* at, float* mu, float* rstd, float* dbg_mu, float* dbg_rstd,
                       cudaStream_t st) {
   const Geometry& g = p.geo;
+  if (g.bv_tc) {
+    // The column statistics (a launch of their own), then the tensor-core B V as its
+    // programmatic dependent.
+    if (g.stat_ctas > 0) {
+      const cudaError_t e = launch_col_stats(p, at, mu, rstd, dbg_mu, dbg_rstd, st);
+      if (e != cudaSuccess) return e;
+    }
+    return launch_bv_tc(p, bt, v, bvp, st);
+  }
   const long bv_ctas = g.bh * g.bv_splits, stat_ctas = g.stat_ctas;
   const unsigned grid = (unsigned)(bv_ctas + stat_ctas);
   const float delta = p.cfg.delta;

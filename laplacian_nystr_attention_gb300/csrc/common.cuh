@@ -102,6 +102,9 @@ struct Geometry {
   int bv_tiles_per_split;  // B V: 64-token chunks per CTA
   int bv_threads;
   size_t bv_smem;
+  bool bv_tc;              // B V on the tensor cores (bv_tc.cu), after a launch of the
+                           // statistics CTAs alone (stat_ctas of stat_threads threads)
+  int stat_threads;
   size_t fin_smem;
   size_t cd_smem;          // dynamic shared memory of the distance kernel
   int out_tile;            // tokens per output-kernel CTA
@@ -145,6 +148,10 @@ struct lapl_attn_plan {
   mutable CUtensorMap tmap_q, tmap_k;
   mutable const void* tmap_q_ptr;
   mutable const void* tmap_k_ptr;
+  // Tensor maps of B^T and V for the tensor-core B V kernel, re-encoded when the pointers change.
+  mutable CUtensorMap tmap_bt, tmap_v;
+  mutable const void* tmap_bt_ptr;
+  mutable const void* tmap_v_ptr;
   // Fault injection for tests (lapl_attn_set_fault_injection): bound of the distance kernel's
   // barrier waits, and whether its producer skips each CTA's last copy.
   unsigned long long cd_wait_ns;
@@ -171,6 +178,12 @@ cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float*
                           const float* mu, const float* rstd, const float* bias, void* out,
                           cudaStream_t st);
 
+// 2-D tensor map, no swizzle, rows past the extent read as zero: `inner` elements per row
+// (contiguous), `outer` rows `row_bytes` apart, boxes of box_inner x box_outer.  False if the
+// driver's encoder is unavailable or rejects the map.
+bool tma_encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint64_t inner,
+                   uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
 // Distance kernel choice for a plan: sets geo.cd_tma, cd_tile, cd_rows, cd_threads and cd_smem,
 // opts in to the shared memory and returns the resident CTAs per SM.
 cudaError_t cdist_plan(lapl_attn_plan& p, int* ctas_per_sm);
@@ -194,6 +207,17 @@ int bv_threads(int m, int d);
 int bv_tile_tokens();
 cudaError_t bv_configure(size_t smem);
 int bv_occupancy(int threads, size_t smem);   // resident B V CTAs per SM
+// B V on the tensor cores (bv_tc.cu).
+int bv_tc_threads();
+int bv_tc_tile_tokens();
+size_t bv_tc_smem_bytes(int d, bool bf16);
+cudaError_t bv_tc_configure(size_t smem);
+int bv_tc_occupancy(size_t smem, bool bf16);
+cudaError_t launch_bv_tc(const lapl_attn_plan& p, const float* bt, const void* v, float* bvp,
+                         cudaStream_t st);
+// Column statistics of A as a launch of their own (with the tensor-core B V).
+cudaError_t launch_col_stats(const lapl_attn_plan& p, const float* at, float* mu, float* rstd,
+                             float* dbg_mu, float* dbg_rstd, cudaStream_t st);
 size_t mix_smem_bytes(int m, int bv_splits);
 cudaError_t mix_configure(size_t smem);
 // Backward pass (backward.cu).

@@ -125,3 +125,13 @@ def test_binding_wraps_every_declared_entry_point(lib):
     declares (argument marshalling only)."""
     for name in declared_entry_points():
         assert callable(getattr(lib, name, None)), name
+
+
+def test_plan_info_struct_matches_header(lib):
+    """The ctypes mirror of lapl_attn_plan_info lists the header's int fields, in order."""
+    src = open(os.path.join(ROOT, "include", "lapl_attn.h")).read()
+    end = src.index("} lapl_attn_plan_info;")
+    body = src[src.rindex("typedef struct {", 0, end):end]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = re.findall(r"int\s+(\w+);", body)
+    assert names == [n for n, _ in lib.lapl_attn_plan_info._fields_]

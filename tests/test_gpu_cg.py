@@ -70,9 +70,12 @@ def test_tiny_intermediates():
 
 
 def test_kernels_per_forward():
+    """Pooling, distances, B V, CG, output; plus the column-statistics launch that precedes a
+    tensor-core B V."""
     import laplacian_nystr_attention_gb300 as lna
     att = lna.LaplacianNystromAttention(lna.make_config(**TINY.config(), solver="cg"))
-    assert lna.lapl_attn_kernels_per_forward(att.handle) == 5
+    stats = lna.lapl_attn_plan_info_get(att.handle)["bv_tensor_core"]
+    assert lna.lapl_attn_kernels_per_forward(att.handle) == 5 + stats
     att.close()
 
 
