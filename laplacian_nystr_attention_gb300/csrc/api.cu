@@ -222,14 +222,18 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
     g.bv_tc = g.d % 16 == 0 && nb <= 256 && g.n % 4 == 0 && g.bh * g.n < (1LL << 31) &&
               g.bh * g.m < (1LL << 31) && !want_cuda && (want_tc || g.n >= 4096);
     int smem_optin = 0;
-    if (g.bv_tc &&
-        cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device) ==
-            cudaSuccess &&
-        bv_tc_smem_bytes(g.d, bf16) > (size_t)smem_optin)
-      g.bv_tc = false;           // fp32 V with d = 128: the operand stages do not fit
+    if (g.bv_tc) {
+      if (cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                 p->device) != cudaSuccess)
+        smem_optin = 0;
+      // As many raw copy stages as fit (bytes in flight per SM); fp32 V with d = 128 leaves
+      // room for too few: the CUDA-core kernel then.
+      g.bv_raw_stages = bv_tc_raw_stages(g.d, bf16, (size_t)smem_optin);
+      if (g.bv_raw_stages == 0) g.bv_tc = false;
+    }
     if (g.bv_tc) {
       g.bv_threads = bv_tc_threads();
-      g.bv_smem = bv_tc_smem_bytes(g.d, bf16);
+      g.bv_smem = bv_tc_smem_bytes(g.d, bf16, g.bv_raw_stages);
       e = bv_tc_configure(g.bv_smem);
     } else {
       g.bv_threads = bv_threads(g.m, g.d);

@@ -22,7 +22,7 @@
 //   warp 5     owns the tensor memory; one thread issues tcgen05.mma (M = 128, N = 2d or d,
 //              K = 8) for each 8 tokens and commits each operand stage back to the converters.
 // The column statistics of A run as a separate launch just before this one (col_stats_kernel,
-// one warp per landmark column); this grid is its programmatic dependent, so the two overlap.
+// one CTA per landmark column); this grid is its programmatic dependent, so the two overlap.
 // The accumulator D then holds
 //   D[j][c] = B_hi V_hi,  D[j][d + c] = B_hi V_lo,  D[64 + j][c] = B_lo V_hi   (j < 64, c < d)
 // and the split's partial (B V)[j][c] = D[j][c] + D[j][d + c] + D[64 + j][c] (the product of the
@@ -30,13 +30,15 @@
 // reduces in split order.  Every barrier wait is bounded (one second); on a timeout the CTA sets
 // the solve bit of the device error word, waits (bounded) for its copies and its tensor-core
 // work, and frees its tensor memory.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace lapl {
 namespace {
 
 constexpr int kTok = 32;                    // tokens (K) per chunk
-constexpr int kRaw = 6;                     // raw (copied) stages
+constexpr int kRawMax = 12;                 // raw (copied) stages: as many as fit, <= 12
 constexpr int kOps = 3;                     // operand stages
 constexpr int kConvThreads = 128;           // warps 0-3
 constexpr int kTmaWarp = 4, kMmaWarp = 5;
@@ -133,11 +135,12 @@ __device__ __forceinline__ void tmem_ld16(unsigned addr, float (&v)[16]) {
 }
 
 // Column statistics of A for the whitening, a launch of its own before the tensor-core B V
-// (whose programmatic dependent it is): warp w of CTA b takes landmark column t = 8 b + w of
-// the (head, landmark) list, the row A^T[t][0..N), with 16 independent 16-byte loads per lane
-// (8 KB per warp) in flight.  The row is shifted by its own first value c, then
-// S1 = Sum (a - c), S2 = Sum (a - c)^2; mean = c + S1 / N and var = (S2 - S1^2 / N) / N.  c is
-// a value of the row, so the subtraction keeps fp32 accuracy.
+// (whose programmatic dependent it is).  CTA t takes landmark column t of the (head, landmark)
+// list, the row A^T[t][0..N); its 8 warps stream 8 contiguous segments of the row, up to 16
+// independent 16-byte loads per lane in flight.  Every segment is shifted by the row's first
+// value c, so the partial sums S1 = Sum (a - c) and S2 = Sum (a - c)^2 simply add (warp sums,
+// then the 8 warps in a fixed order); mean = c + S1 / N and var = (S2 - S1^2 / N) / N.  c is a
+// value of the row, so the subtraction keeps fp32 accuracy.
 constexpr int kStatThreads = 256;
 
 __device__ __forceinline__ float warp_allsum(float v) {
@@ -148,26 +151,28 @@ __device__ __forceinline__ float warp_allsum(float v) {
 
 __global__ void __launch_bounds__(kStatThreads)
 col_stats_kernel(const float* __restrict__ at, float* __restrict__ mu, float* __restrict__ rstd,
-                 float* __restrict__ dbg_mu, float* __restrict__ dbg_rstd, long tasks, int n,
-                 float delta) {
+                 float* __restrict__ dbg_mu, float* __restrict__ dbg_rstd, int n, float delta) {
   // The B V kernel after this one may start now (it does not read these results).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int lane = threadIdx.x & 31;
-  const long t = (long)blockIdx.x * (kStatThreads / 32) + (threadIdx.x >> 5);
-  if (t >= tasks) return;
+  __shared__ float part[2][kStatThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long t = blockIdx.x;
   const float* row = at + (size_t)t * n;
   const float c = __ldcg(row);
   float s1 = 0.f, s2 = 0.f;
+  constexpr int kW = kStatThreads / 32;
   if ((n & 3) == 0) {
     constexpr int kB = 16;
     const float4* r4 = reinterpret_cast<const float4*>(row);
     const int n4 = n >> 2;
-    for (int i0 = lane; i0 < n4; i0 += 32 * kB) {
+    const int per = (n4 + kW - 1) / kW;                 // float4 per warp segment
+    const int beg = warp * per, end = min(n4, beg + per);
+    for (int i0 = beg + lane; i0 < end; i0 += 32 * kB) {
       float4 v[kB];
 #pragma unroll
       for (int u = 0; u < kB; ++u) {
         const int i = i0 + 32 * u;
-        v[u] = i < n4 ? __ldcg(&r4[i]) : make_float4(c, c, c, c);
+        v[u] = i < end ? __ldcg(&r4[i]) : make_float4(c, c, c, c);
       }
 #pragma unroll
       for (int u = 0; u < kB; ++u) {
@@ -177,7 +182,7 @@ col_stats_kernel(const float* __restrict__ at, float* __restrict__ mu, float* __
       }
     }
   } else {
-    for (int i = lane; i < n; i += 32) {
+    for (int i = threadIdx.x; i < n; i += kStatThreads) {
       const float a = __ldcg(&row[i]) - c;
       s1 += a;
       s2 = fmaf(a, a, s2);
@@ -186,9 +191,20 @@ col_stats_kernel(const float* __restrict__ at, float* __restrict__ mu, float* __
   s1 = warp_allsum(s1);
   s2 = warp_allsum(s2);
   if (lane == 0) {
+    part[0][warp] = s1;
+    part[1][warp] = s2;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a1 = 0.f, a2 = 0.f;
+#pragma unroll
+    for (int w = 0; w < kW; ++w) {
+      a1 += part[0][w];
+      a2 += part[1][w];
+    }
     const float inv_n = 1.f / (float)n;
-    const float mean = c + s1 * inv_n;
-    const float m2 = fmaxf(s2 - s1 * s1 * inv_n, 0.f);
+    const float mean = c + a1 * inv_n;
+    const float m2 = fmaxf(a2 - a1 * a1 * inv_n, 0.f);
     const float rs = 1.f / sqrtf(m2 * inv_n + delta);
     mu[t] = mean;
     rstd[t] = rs;
@@ -202,6 +218,7 @@ struct BvTcArgs {
   unsigned* err;
   int m, d, n;
   int tiles_per_split, splits;
+  int nraw;             // raw stages (<= kRawMax)
 };
 
 template <bool kBf16>
@@ -218,13 +235,14 @@ bv_tc_kernel(const BvTcArgs a, const __grid_constant__ CUtensorMap map_bt,
   const unsigned raw_bytes = raw_stage_bytes(d, kBf16);
   const unsigned op_bytes = op_stage_bytes(nb);
   const unsigned lboB = lbo_b(nb);
+  const int kRaw = a.nraw;
   unsigned char* raw = smem_bv;                                        // kRaw raw stages
   unsigned char* ops = raw + kRaw * raw_bytes;                         // kOps operand stages
   unsigned long long* bars = reinterpret_cast<unsigned long long*>(ops + kOps * op_bytes);
-  const unsigned rfull0 = smem_u32(bars), rempty0 = rfull0 + 8 * kRaw,
-                 ofull0 = rempty0 + 8 * kRaw, oempty0 = ofull0 + 8 * kOps,
+  const unsigned rfull0 = smem_u32(bars), rempty0 = rfull0 + 8 * kRawMax,
+                 ofull0 = rempty0 + 8 * kRawMax, oempty0 = ofull0 + 8 * kOps,
                  done_bar = oempty0 + 8 * kOps;
-  unsigned* slot = reinterpret_cast<unsigned*>(bars + 2 * kRaw + 2 * kOps + 1);
+  unsigned* slot = reinterpret_cast<unsigned*>(bars + 2 * kRawMax + 2 * kOps + 1);
 
   const long bh = blockIdx.x / a.splits;
   const int sp = blockIdx.x % a.splits;
@@ -460,9 +478,8 @@ bv_tc_kernel(const BvTcArgs a, const __grid_constant__ CUtensorMap map_bt,
 cudaError_t launch_col_stats(const lapl_attn_plan& p, const float* at, float* mu, float* rstd,
                              float* dbg_mu, float* dbg_rstd, cudaStream_t st) {
   const Geometry& g = p.geo;
-  const long tasks = g.bh * g.m;
-  const unsigned grid = (unsigned)((tasks + kStatThreads / 32 - 1) / (kStatThreads / 32));
-  col_stats_kernel<<<grid, kStatThreads, 0, st>>>(at, mu, rstd, dbg_mu, dbg_rstd, tasks, g.n,
+  const unsigned grid = (unsigned)(g.bh * g.m);     // one CTA per (head, landmark) column
+  col_stats_kernel<<<grid, kStatThreads, 0, st>>>(at, mu, rstd, dbg_mu, dbg_rstd, g.n,
                                                    p.cfg.delta);
   return cudaGetLastError();
 }
@@ -470,10 +487,19 @@ cudaError_t launch_col_stats(const lapl_attn_plan& p, const float* at, float* mu
 int bv_tc_threads() { return kBvTcThreads; }
 int bv_tc_tile_tokens() { return kTok; }
 
-size_t bv_tc_smem_bytes(int d, bool bf16) {
+// Raw stages that fit next to the operand stages in `smem_limit` bytes (0 if fewer than 4).
+int bv_tc_raw_stages(int d, bool bf16, size_t smem_limit) {
   const int nb = bf16 ? d : 2 * d;
-  const size_t body = (size_t)kRaw * raw_stage_bytes(d, bf16) + (size_t)kOps * op_stage_bytes(nb);
-  return body + (2 * kRaw + 2 * kOps + 1) * 8 + 16;
+  const size_t fixed = (size_t)kOps * op_stage_bytes(nb) + (2 * kRawMax + 2 * kOps + 1) * 8 + 16;
+  if (smem_limit <= fixed) return 0;
+  const int n = (int)std::min<size_t>(kRawMax, (smem_limit - fixed) / raw_stage_bytes(d, bf16));
+  return n >= 4 ? n : 0;
+}
+
+size_t bv_tc_smem_bytes(int d, bool bf16, int nraw) {
+  const int nb = bf16 ? d : 2 * d;
+  const size_t body = (size_t)nraw * raw_stage_bytes(d, bf16) + (size_t)kOps * op_stage_bytes(nb);
+  return body + (2 * kRawMax + 2 * kOps + 1) * 8 + 16;
 }
 
 cudaError_t bv_tc_configure(size_t smem) {
@@ -520,6 +546,7 @@ cudaError_t launch_bv_tc(const lapl_attn_plan& p, const float* bt, const void* v
   a.bvp = bvp; a.err = p.dev_err;
   a.m = g.m; a.d = g.d; a.n = g.n;
   a.tiles_per_split = g.bv_tiles_per_split; a.splits = g.bv_splits;
+  a.nraw = g.bv_raw_stages;
   const void* f = bf16 ? reinterpret_cast<const void*>(&bv_tc_kernel<true>)
                        : reinterpret_cast<const void*>(&bv_tc_kernel<false>);
   void* args[] = {&a, &p.tmap_bt, &p.tmap_v};

@@ -105,6 +105,7 @@ struct Geometry {
   bool bv_tc;              // B V on the tensor cores (bv_tc.cu), after a launch of the
                            // statistics CTAs alone (stat_ctas of stat_threads threads)
   int stat_threads;
+  int bv_raw_stages;       // tensor-core B V: raw copy stages (as many as fit, <= 12)
   size_t fin_smem;
   size_t cd_smem;          // dynamic shared memory of the distance kernel
   int out_tile;            // tokens per output-kernel CTA
@@ -210,7 +211,8 @@ int bv_occupancy(int threads, size_t smem);   // resident B V CTAs per SM
 // B V on the tensor cores (bv_tc.cu).
 int bv_tc_threads();
 int bv_tc_tile_tokens();
-size_t bv_tc_smem_bytes(int d, bool bf16);
+int bv_tc_raw_stages(int d, bool bf16, size_t smem_limit);
+size_t bv_tc_smem_bytes(int d, bool bf16, int nraw);
 cudaError_t bv_tc_configure(size_t smem);
 int bv_tc_occupancy(size_t smem, bool bf16);
 cudaError_t launch_bv_tc(const lapl_attn_plan& p, const float* bt, const void* v, float* bvp,
