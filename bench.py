@@ -50,6 +50,8 @@ CLEAN_BYTES = 256 * 1024 * 1024
 # (summaries under profiles/), per (feed, workload, kernel) with the sha256 of the distance kernel's
 # source files it was taken on; reported as null when the sources have changed since.
 CDIST_TRAFFIC = {
+    ("l1", "stage1_f32", "laplacian"): (
+        13016576 + 4096, "11580dce3a30953b53f0ca1080d9299d5324bf61358acc1d91042f2c8a1049a5"),
     ("tma", "stage1_f32", "laplacian"): (
         13019904 + 4608, "f4b35b7f8fd1127af71c0e7d6fe76d03c474923fbba7229c9325ced339798112"),
     ("cp.async", "stage1_f32", "gaussian"): (
@@ -141,6 +143,33 @@ def cdist_ops_per_launch(w) -> float:
 def fp32_peak_tflops(num_sms: int, sm_mhz: float) -> float:
     """FP32 CUDA-core peak: SMs x 128 FP32 lanes x 2 (an FMA counts 2) x SM clock."""
     return num_sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def gemm_chain_roofline(w, stage_ms: dict, peaks: dict, plan: dict) -> list:
+    """The two contractions of the output chain against the measured HBM bandwidth: algorithmic
+    bytes per launch / the stage's in-step CUDA-event time.  B V's stage also holds the column
+    statistics of A (they read A^T once); the output stage reads A^T and writes O."""
+    bh, n, m, d = w.batch * w.heads, w.n, w.num_landmarks, w.head_dim
+    esz = 2 if w.dtype == "bf16" else 4
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    bv_bytes = bh * m * n * 4 + bh * n * d * esz + bh * m * n * 4
+    out_bytes = bh * m * n * 4 + bh * n * d * 4
+    flops = 2.0 * bh * n * m * d
+    tc = bool(plan.get("bv_tensor_core"))
+    entries = []
+    for name, key, nbytes, kern in (
+            ("B V + column statistics", "bv", bv_bytes,
+             "col_stats_kernel + bv_tc_kernel (tcgen05, TF32 high/low)" if tc
+             else "bv_kernel (statistics CTAs + CUDA-core FMA tiles)"),
+            ("O = A^ M (whitening applied on load)", "output", out_bytes,
+             "output_kernel (CUDA-core FMA tiles)")):
+        ms = stage_ms[key]
+        gbs = nbytes / (ms / 1e3) / 1e9
+        entries.append({"stage": name, "kernel": kern, "bound": "hbm", "achieved": gbs,
+                        "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "bytes": nbytes,
+                        "flops": flops, "tflops": flops / (ms / 1e3) / 1e12, "kernel_ms": ms,
+                        "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)"})
+    return entries
 
 
 def measured_peaks():
@@ -476,6 +505,7 @@ def run_ours(args, w):
             "ops_convention": OPS_CONVENTION[args.kernel],
             "kernel_ms": stage_ms["cdist"],
         },
+        "gemm_chain_roofline": gemm_chain_roofline(w, stage_ms, peaks, plan),
         "stage_ms": stage_ms,
         "cpu_baseline": None,
         "e2e": e2e,

@@ -42,3 +42,19 @@ def test_roofline_operation_count_and_peak():
     # 3 ops x (query block + key block) x B x H x N x m x d
     assert bench.cdist_ops_per_launch(w) == 3 * 2 * 8 * 2 * 3136 * 49 * 32 == 472055808
     assert bench.fp32_peak_tflops(152, 2070.0) == pytest.approx(80.54784)
+
+
+def test_gemm_chain_roofline_bytes_and_fraction():
+    """Algorithmic bytes of the two chain stages at the hires shape (bf16 inputs): B V stage
+    reads B^T, V and (statistics) A^T; the output stage reads A^T and writes fp32 O."""
+    import bench
+    from lapl_workloads import WORKLOADS
+    w = WORKLOADS["hires_bf16"]
+    bh, n, m, d = 32, 16384, 64, 64
+    e = bench.gemm_chain_roofline(w, {"bv": 0.1, "output": 0.05}, {"hbm_gbs": 5000.0},
+                                  {"bv_tensor_core": 1})
+    assert e[0]["bytes"] == bh * m * n * 4 * 2 + bh * n * d * 2
+    assert e[1]["bytes"] == bh * m * n * 4 + bh * n * d * 4
+    assert abs(e[0]["achieved"] - e[0]["bytes"] / 1e-4 / 1e9) < 1e-6
+    assert abs(e[1]["frac"] - e[1]["bytes"] / 5e-5 / 1e9 / 5000.0) < 1e-12
+    assert "tcgen05" in e[0]["kernel"] and e[0]["flops"] == 2.0 * bh * n * m * d
