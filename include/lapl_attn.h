@@ -207,7 +207,8 @@ int lapl_attn_kernels_per_forward(lapl_attn_handle h);
  * Device-side failure report.  Kernels that wait on shared-memory barriers (the distance
  * kernel's TMA pipeline, the tensor-core Newton-Schulz solve) bound every such wait (one second
  * by default); a wait that gives up sets a bit of a device error word (one per device, shared
- * by all handles) -- bit 1 the distance kernel, bit 2 the tensor-core solve -- and the waiting
+ * by all handles) -- bit 1 the distance kernel, bit 2 the tensor-core solve, bit 4 a tensor-core
+ * kernel of the output chain -- and the waiting
  * warps leave the kernel after the copies and tensor-core operations they issued have
  * completed, so a failed forward ends instead of hanging, the context stays usable, and its
  * outputs are undefined.  This call copies the word to *flags, clears it, and synchronises
@@ -247,6 +248,9 @@ typedef struct {
   int bv_splits;      /* CTAs per head of the B V kernel                                     */
   int bv_tensor_core; /* 1: B V on the tensor cores (TF32 high/low split, fp32 accumulation;
                          d a multiple of 16, N a multiple of 4); 0: CUDA-core FMA tiles     */
+  int out_tensor_core; /* 1: O = A^ M on the tensor cores (TF32 high/low split, fp32
+                         accumulation; d a multiple of 16 and <= 64, N a multiple of 4);
+                         0: CUDA-core FMA tiles                                             */
 } lapl_attn_plan_info;
 
 /*

@@ -52,7 +52,7 @@ class lapl_attn_debug(ctypes.Structure):
 class lapl_attn_plan_info(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in
                 ("cdist_tma", "cdist_ctas", "cdist_threads", "ns_cluster", "ns_tensor_core",
-                 "ns_exclusive", "bv_splits", "bv_tensor_core")]
+                 "ns_exclusive", "bv_splits", "bv_tensor_core", "out_tensor_core")]
 
 
 class LaplAttnError(RuntimeError):

@@ -194,10 +194,32 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
       e = ns_configure(g.s, 1, g.ns_smem, nullptr);
   }
   if (e == cudaSuccess) {
-    g.out_tile = output_tile_tokens(g.d, g.bh, g.n, p->num_sms);
-    g.out_threads = 256;
-    g.out_smem = output_smem_bytes(g.m, g.d, g.out_tile);
-    e = output_configure(g.out_smem);
+    // O = A^ M on the tensor cores where the shapes allow it (d a multiple of 16 and two
+    // accumulators of 2d columns in at most 256 tensor-memory columns; N a multiple of 4 for
+    // the 16-byte loads of A^T rows; the operand stages within the shared memory) and the
+    // sequence is long (N >= 4096: at the stage-1 shape the 2.6 tiles per persistent CTA do
+    // not amortise its set-up, and the CUDA-core kernel measured 12.5 against 16.4 us);
+    // LAPL_ATTN_OUT=cuda or =tc forces either.
+    const char* ok_env = getenv("LAPL_ATTN_OUT");
+    const bool want_tc = ok_env && strcmp(ok_env, "tc") == 0;
+    const bool want_cuda = (ok_env && strcmp(ok_env, "cuda") == 0) || (!want_tc && g.n < 4096);
+    int smem_optin = 0;
+    if (cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                               p->device) != cudaSuccess)
+      smem_optin = 0;
+    g.out_tc = !want_cuda && g.d % 16 == 0 && 4 * g.d <= 256 && g.n % 4 == 0 &&
+               out_tc_smem_bytes(g.m, g.d) <= (size_t)smem_optin;
+    if (g.out_tc) {
+      g.out_tile = 128;
+      g.out_threads = out_tc_threads();
+      g.out_smem = out_tc_smem_bytes(g.m, g.d);
+      e = out_tc_configure(g.out_smem);
+    } else {
+      g.out_tile = output_tile_tokens(g.d, g.bh, g.n, p->num_sms);
+      g.out_threads = 256;
+      g.out_smem = output_smem_bytes(g.m, g.d, g.out_tile);
+      e = output_configure(g.out_smem);
+    }
   }
   if (e != cudaSuccess) {
     set_error(p, e, "create/configure");
@@ -710,10 +732,10 @@ lapl_status lapl_attn_device_errors(lapl_attn_handle h, void* stream, unsigned* 
   *flags = word;
   if (word) {
     snprintf(h->last_error, sizeof(h->last_error),
-             "device error flags 0x%x: a bounded barrier wait gave up in%s%s%s", word,
-             (word & kErrBitCdist) ? " the distance kernel" : "",
-             ((word & kErrBitCdist) && (word & kErrBitSolve)) ? " and" : "",
-             (word & kErrBitSolve) ? " the tensor-core Newton-Schulz solve" : "");
+             "device error flags 0x%x: a bounded barrier wait gave up in:%s%s%s", word,
+             (word & kErrBitCdist) ? " the distance kernel;" : "",
+             (word & kErrBitSolve) ? " the tensor-core Newton-Schulz solve;" : "",
+             (word & kErrBitChain) ? " a tensor-core kernel of the output chain;" : "");
     return LAPL_ERR_DEVICE_TIMEOUT;
   }
   return LAPL_OK;
@@ -738,6 +760,7 @@ lapl_status lapl_attn_plan_info_get(lapl_attn_handle h, lapl_attn_plan_info* inf
   info->ns_exclusive = g.ns_exclusive ? 1 : 0;
   info->bv_splits = g.bv_splits;
   info->bv_tensor_core = g.bv_tc ? 1 : 0;
+  info->out_tensor_core = g.out_tc ? 1 : 0;
   return LAPL_OK;
 }
 

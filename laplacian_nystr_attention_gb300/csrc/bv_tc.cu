@@ -28,7 +28,7 @@
 // and the split's partial (B V)[j][c] = D[j][c] + D[j][d + c] + D[64 + j][c] (the product of the
 // two low parts, 2^-20 relative, is left out), written to the same partial buffer the M kernel
 // reduces in split order.  Every barrier wait is bounded (one second); on a timeout the CTA sets
-// the solve bit of the device error word, waits (bounded) for its copies and its tensor-core
+// the chain bit of the device error word, waits (bounded) for its copies and its tensor-core
 // work, and frees its tensor memory.
 #include <algorithm>
 
@@ -455,7 +455,7 @@ bv_tc_kernel(const BvTcArgs a, const __grid_constant__ CUtensorMap map_bt,
       }
     }
   } else if (!done && threadIdx.x == 0) {
-    atomicOr(a.err, kErrBitSolve);
+    atomicOr(a.err, kErrBitChain);
     // Wait (bounded) for whatever the tensor core may still be doing before the memory goes.
     mbar_wait(done_bar, 0);
   }

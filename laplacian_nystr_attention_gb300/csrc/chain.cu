@@ -581,6 +581,7 @@ cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float*
                           const float* mu, const float* rstd, const float* bias, void* out,
                           cudaStream_t st) {
   const Geometry& g = p.geo;
+  if (g.out_tc) return launch_output_tc(p, at, mmat, mu, rstd, bias, out, st);
   int tiles = (g.n + g.out_tile - 1) / g.out_tile;
   // Programmatic dependent launch: the kernel may begin while the preceding M kernel runs.
   cudaLaunchConfig_t cfg = {};

@@ -17,6 +17,7 @@ namespace lapl {
 // Bits of the device error word (set by a kernel whose bounded barrier wait gave up).
 constexpr unsigned kErrBitCdist = 1u;   // distance kernel (TMA pipeline)
 constexpr unsigned kErrBitSolve = 2u;   // Newton-Schulz solve on the tensor cores
+constexpr unsigned kErrBitChain = 4u;   // tensor-core B V or output product
 
 constexpr int kMaxS = 8;            // landmark grid side: m = s*s <= 64
 constexpr int kMaxM = kMaxS * kMaxS;
@@ -106,6 +107,7 @@ struct Geometry {
                            // statistics CTAs alone (stat_ctas of stat_threads threads)
   int stat_threads;
   int bv_raw_stages;       // tensor-core B V: raw copy stages (as many as fit, <= 12)
+  bool out_tc;             // O = A^ M on the tensor cores (out_tc.cu)
   size_t fin_smem;
   size_t cd_smem;          // dynamic shared memory of the distance kernel
   int out_tile;            // tokens per output-kernel CTA
@@ -217,6 +219,13 @@ cudaError_t bv_tc_configure(size_t smem);
 int bv_tc_occupancy(size_t smem, bool bf16);
 cudaError_t launch_bv_tc(const lapl_attn_plan& p, const float* bt, const void* v, float* bvp,
                          cudaStream_t st);
+// O = A^ M on the tensor cores (out_tc.cu).
+size_t out_tc_smem_bytes(int m, int d);
+int out_tc_threads();
+cudaError_t out_tc_configure(size_t smem);
+cudaError_t launch_output_tc(const lapl_attn_plan& p, const float* at, const float* mmat,
+                             const float* mu, const float* rstd, const float* bias, void* out,
+                             cudaStream_t st);
 // Column statistics of A as a launch of their own (with the tensor-core B V).
 cudaError_t launch_col_stats(const lapl_attn_plan& p, const float* at, float* mu, float* rstd,
                              float* dbg_mu, float* dbg_rstd, cudaStream_t st);
