@@ -103,6 +103,9 @@ def parse():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--backward", action="store_true",
                     help="time forward (keeping the backward's state) + backward instead")
+    ap.add_argument("--inner-loop", action="store_true",
+                    help="build and run bench_l1_loop.cu: elements/clock/SM of the L1-distance "
+                         "inner loop in its instruction forms (no forward)")
     return ap.parse_args()
 
 
@@ -615,9 +618,43 @@ def run_backward(args, w):
         tdist.destroy_process_group()
 
 
+def run_inner_loop(args):
+    """The L1-distance inner-loop microbenchmark (bench_l1_loop.cu), one JSON line: per form and
+    CTAs per SM, elements / clock / SM (mean over SMs), and the 3-op fraction of FP32 peak."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    build = os.path.join(ROOT, "_build")
+    os.makedirs(build, exist_ok=True)
+    exe = os.path.join(build, "bench_l1_loop")
+    src = os.path.join(ROOT, "bench_l1_loop.cu")
+    if not os.path.exists(exe) or os.path.getmtime(exe) < os.path.getmtime(src):
+        subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", exe,
+                        src], check=True)
+    outp = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
+    forms = []
+    for line in outp.splitlines():
+        parts = line.split()
+        if len(parts) < 5 or "=" not in parts[1]:
+            continue
+        kv = dict(tok.split("=") for tok in parts[1:] if tok.count("=") == 1)
+        mean = float(kv["mean"])
+        forms.append({"form": parts[0], "landmarks_per_warp": int(kv["C"]),
+                      "ctas_per_sm": int(kv["ctas_per_sm"]), "registers": int(kv["regs"]),
+                      "elem_per_clk_per_sm": mean, "min_over_sms": float(kv["min"]),
+                      "max_over_sms": float(kv["max"]),
+                      "frac_of_fp32_peak_3op": 3.0 * mean / 256.0})
+    print(json.dumps({"metric": "L1-distance inner loop elements/clock/SM", "unit": "elem/clk/SM",
+                      "forms": forms, "note": "3-op fraction = 3 x elements / (128 lanes x 2)"}),
+          flush=True)
+
+
 def main():
     args = parse()
     w = WORKLOADS[args.workload]
+    if args.inner_loop:
+        run_inner_loop(args)
+        return
     if args.impl == "reference":
         run_reference(args, w)
     elif args.backward:
