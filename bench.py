@@ -59,7 +59,8 @@ CDIST_TRAFFIC = {
 }
 CDIST_SOURCES = ["cdist_kernel.cuh", "cdist_tma.cuh", "cdist_l1.cuh", "cdist.cu", "cdist_d32.cu",
                  "cdist_d64.cu", "cdist_d0.cu", "cdist_tma_f32.cu", "cdist_tma_bf16.cu",
-                 "cdist_l1.cu", "cdist_gauss_d32.cu", "cdist_gauss_d64.cu", "cdist_gauss_d0.cu"]
+                 "cdist_l1.cu", "cdist_gauss_d32.cu", "cdist_gauss_d64.cu", "cdist_gauss_d0.cu",
+                 "cdist_gauss_tc.cu", "common.cuh"]
 CDIST_KERNEL = {
     ("l1", "laplacian"): "cdist_l1_kernel (fused L1 distance + exp, query and key blocks; "
                          "TMA-fed, helper warp, element terms split between the FP32 and ALU "
@@ -70,6 +71,9 @@ CDIST_KERNEL = {
                                "blocks; cp.async-fed)",
     ("cp.async", "gaussian"): "cdist_exp_kernel (fused squared-l2 distance + exp, query and key "
                               "blocks; cp.async-fed)",
+    ("gtc", "gaussian"): "gauss_tc_kernel (squared-l2 distance as |x|^2 + |l|^2 - 2 x.l with x.l "
+                         "on the tensor cores (tcgen05, TF32 high/low) + exp, query and key "
+                         "blocks)",
 }
 OPS_CONVENTION = {
     "laplacian": "3 per (token, landmark, channel): subtract, absolute value, add",
@@ -141,6 +145,14 @@ def cdist_ops_per_launch(w) -> float:
     for the Gaussian kernel subtract, multiply, add) per (token, landmark, channel) element, for
     the query block and the key block."""
     return 3.0 * 2.0 * w.batch * w.heads * w.n * w.num_landmarks * w.head_dim
+
+
+def cdist_bytes_per_launch(w) -> int:
+    """Algorithmic bytes of the distance kernel: Q and K read once, A^T and B^T (fp32) written
+    once; the landmarks (m x d per head, L2-resident) are not counted."""
+    esz = 2 if w.dtype == "bf16" else 4
+    bh = w.batch * w.heads
+    return 2 * bh * w.n * w.head_dim * esz + 2 * bh * w.n * w.num_landmarks * 4
 
 
 def fp32_peak_tflops(num_sms: int, sm_mhz: float) -> float:
@@ -484,9 +496,34 @@ def run_ours(args, w):
     peak = fp32_peak_tflops(props.multi_processor_count, sm_max)
     achieved = cdist_ops_per_launch(w) / (stage_ms["cdist"] / 1e3) / 1e12
     plan = lna.lapl_attn_plan_info_get(att.handle)
-    feed = {2: "l1", 1: "tma"}.get(plan["cdist_tma"], "cp.async")
+    feed = {3: "gtc", 2: "l1", 1: "tma"}.get(plan["cdist_tma"], "cp.async")
     rec = CDIST_TRAFFIC.get((feed, w.name, args.kernel))
     traffic = rec[0] if rec and rec[1] == cdist_sources_sha() else None
+    if feed == "gtc":
+        # The cross term is a contraction on the tensor cores; what is left is bound by HBM.
+        hbm = float(peaks.get("hbm_gbs", 6800.0))
+        nbytes = cdist_bytes_per_launch(w)
+        gbs = nbytes / (stage_ms["cdist"] / 1e3) / 1e9
+        roofline = {
+            "kernel": CDIST_KERNEL[(feed, args.kernel)],
+            "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+            "traffic": traffic,
+            "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peaks_src})",
+            "bytes_per_launch": nbytes,
+            "bytes_convention": "Q and K read once, A^T and B^T written once (fp32)",
+            "kernel_ms": stage_ms["cdist"],
+        }
+    else:
+        roofline = {
+            "kernel": CDIST_KERNEL[(feed, args.kernel)],
+            "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": traffic,
+            "peak_source": (f"derived: {props.multi_processor_count} SMs x 128 FP32 lanes x 2 x "
+                            f"{sm_max:g} MHz (max SM clock, MEASURED_PEAKS {peaks_src})"),
+            "ops_per_launch": cdist_ops_per_launch(w),
+            "ops_convention": OPS_CONVENTION[args.kernel],
+            "kernel_ms": stage_ms["cdist"],
+        }
     clk = clocks.summary()
     line = {
         "metric": METRIC, "value": job_rate(world, w.tokens, ms), "unit": UNIT, "n_gpus": world,
@@ -498,16 +535,7 @@ def run_ours(args, w):
                          f"then a {CLEAN_BYTES >> 20} MiB read; not timed)",
                    "parallelism": f"replicas x{world} (independent (batch, head) slices)",
                    "plan": plan},
-        "roofline": {
-            "kernel": CDIST_KERNEL[(feed, args.kernel)],
-            "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": traffic,
-            "peak_source": (f"derived: {props.multi_processor_count} SMs x 128 FP32 lanes x 2 x "
-                            f"{sm_max:g} MHz (max SM clock, MEASURED_PEAKS {peaks_src})"),
-            "ops_per_launch": cdist_ops_per_launch(w),
-            "ops_convention": OPS_CONVENTION[args.kernel],
-            "kernel_ms": stage_ms["cdist"],
-        },
+        "roofline": roofline,
         "gemm_chain_roofline": gemm_chain_roofline(w, stage_ms, peaks, plan),
         "stage_ms": stage_ms,
         "cpu_baseline": None,

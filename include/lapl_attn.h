@@ -224,19 +224,25 @@ lapl_status lapl_attn_device_errors(lapl_attn_handle h, void* stream, unsigned* 
  * (0 restores the default of one second).  skip_last_copy = 1: the distance kernel's producer
  * never issues the copy of each CTA's last chunk, so the waits on that chunk run out after
  * wait_ns; nothing else is outstanding when they do.  Applies to the split-pipe distance kernel
- * (plan_info cdist_tma = 2) and to forwards launched after the call.  0 = normal operation.
+ * (plan_info cdist_tma = 2; its producer skips the copy) and the Gaussian tensor-core kernel
+ * (cdist_tma = 3; its converter warps never publish the chunk), to forwards launched after the
+ * call.  0 = normal operation.
  */
 lapl_status lapl_attn_set_fault_injection(lapl_attn_handle h, unsigned long long wait_ns,
                                           int skip_last_copy);
 
 /* Launch choices of a plan (fixed at create). */
 typedef struct {
-  int cdist_tma;      /* 2: the distance kernel's token chunks are loaded by the Tensor Memory
-                         Accelerator and half of each warp's landmarks take the
-                         q + l - 2 min(q, l) form on the ALU pipe (same distances bit for bit
-                         on integer inputs, to rounding otherwise); 1: TMA-fed, every term
-                         as |q - l|; 0: cp.async-fed, every term as |q - l|.  1 and 0 give
-                         the same distances bit for bit.                                    */
+  int cdist_tma;      /* 3 (Gaussian kernel only): the squared distances are formed as
+                         |x|^2 + |l|^2 - 2 x.l with x.l on the tensor cores (TF32 high/low
+                         split, fp32 accumulation; bit for bit the direct sum on integer
+                         inputs, to rounding otherwise); 2: the distance kernel's token chunks
+                         are loaded by the Tensor Memory Accelerator and half of each warp's
+                         landmarks take the q + l - 2 min(q, l) form on the ALU pipe (same
+                         distances bit for bit on integer inputs, to rounding otherwise); 1:
+                         TMA-fed, every term as |q - l|; 0: cp.async-fed, every term as
+                         |q - l| (or (q - l)^2).  1 and 0 give the same distances bit for
+                         bit.                                                               */
   int cdist_ctas;     /* persistent CTAs of the distance kernel                              */
   int cdist_threads;  /* threads per distance-kernel CTA                                     */
   int ns_cluster;     /* CTAs per head in the Newton-Schulz solve: 1, or 2 (a cluster pair,
@@ -255,8 +261,9 @@ typedef struct {
 
 /*
  * Fill *info.  Choices made at create: for the Laplacian kernel with fp32 inputs, d = 32 or 64
- * and m <= 49 the split-pipe TMA kernel (cdist_tma = 2); cp.async otherwise (always for the
- * Gaussian kernel); for the solve one CTA per head, with tensor-core products for m >= 25 and
+ * and m <= 49 the split-pipe TMA kernel (cdist_tma = 2), cp.async otherwise; for the Gaussian
+ * kernel with d = 32 or 64 the tensor-core kernel (cdist_tma = 3), cp.async otherwise; for the
+ * solve one CTA per head, with tensor-core products for m >= 25 and
  * CUDA-core products for m <= 16.  Environment variables read at create override them:
  * LAPL_ATTN_CDIST_FEED = "cp.async" (always), "tma" (wherever the plain TMA kernel exists: fp32
  * with d = 32 or 64, bf16 with d = 64) or "l1" (the split-pipe kernel, where it exists), both

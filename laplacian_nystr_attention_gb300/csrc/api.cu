@@ -752,7 +752,7 @@ lapl_status lapl_attn_set_fault_injection(lapl_attn_handle h, unsigned long long
 lapl_status lapl_attn_plan_info_get(lapl_attn_handle h, lapl_attn_plan_info* info) {
   if (!h || !info) return LAPL_ERR_INVALID_ARG;
   const Geometry& g = h->geo;
-  info->cdist_tma = g.cd_l1 ? 2 : (g.cd_tma ? 1 : 0);
+  info->cdist_tma = g.cd_gtc ? 3 : g.cd_l1 ? 2 : (g.cd_tma ? 1 : 0);
   info->cdist_ctas = g.cd_part.ctas;
   info->cdist_threads = g.cd_threads;
   info->ns_cluster = g.ns_cluster;

@@ -12,12 +12,16 @@
 //   cdist_l1_kernel (cdist_l1.cuh)     TMA-fed like cdist_tma_kernel, with a helper warp and the
 //                                      element work split between the FP32 and ALU pipes;
 //                                      fp32, d in {32, 64}, s <= 7, Laplacian kernel.
+//   gauss_tc_kernel (cdist_gauss_tc.cu) Gaussian kernel only: |x|^2 + |l|^2 - 2 x.l with x.l on
+//                                      the tensor cores; fp32 or bf16, d in {32, 64}; the
+//                                      automatic choice for the Gaussian kernel there.
 // Automatic choice for the Laplacian kernel: cdist_l1_kernel wherever it is instantiated;
 // otherwise the TMA feed for fp32, d = 32, s <= 7; cp.async elsewhere (faster where the TMA
 // kernel's extra producer warp costs registers, s = 8, or its consumer warps each widen the
 // same bf16 chunk).  The environment variable LAPL_ATTN_CDIST_FEED=l1, =tma or =cp.async, read at
 // plan creation, overrides the choice (l1 and tma only where instantiated and the tensor holds
 // at least one chunk of rows).
+#include <algorithm>
 #include <stdlib.h>
 #include <string.h>
 
@@ -150,8 +154,26 @@ cudaError_t cdist_plan(lapl_attn_plan& p, int* ctas_per_sm) {
   // per warp overflow the register budget of two CTAs per SM).
   const void* fl1 = (!bf16 && !gauss && g.s <= 7) ? cdist_l1::kernel(g.s, g.d) : nullptr;
   g.cd_l1 = fl1 && tma_ok && (want_l1 || (!want_tma && !want_cpasync));
+  // Gaussian kernel: the cross term x.l on the tensor cores where instantiated (d = 32 or 64;
+  // the squared distance is |x|^2 + |l|^2 - 2 x.l); LAPL_ATTN_CDIST_FEED=cp.async forces the
+  // CUDA-core kernel (direct sum of squared differences).
+  const void* fg = gauss && !want_cpasync && g.m <= 64 ? gauss_tc_kernel_ptr(g.d, bf16) : nullptr;
+  int smem_optin = 0;
+  if (fg && (cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                    p.device) != cudaSuccess ||
+             gauss_tc_smem_bytes(g.m, g.d, bf16) > (size_t)smem_optin)) {
+    cudaGetLastError();
+    fg = nullptr;
+  }
+  g.cd_gtc = fg != nullptr;
   const void* f = nullptr;
-  if (g.cd_l1) {
+  if (g.cd_gtc) {
+    f = fg;
+    g.cd_l1 = false;
+    g.cd_tma = false;
+    g.cd_threads = gauss_tc_threads();
+    g.cd_smem = gauss_tc_smem_bytes(g.m, g.d, bf16);
+  } else if (g.cd_l1) {
     f = fl1;
     g.cd_tma = false;
     g.cd_threads = 32 * (g.s + 1);
@@ -172,6 +194,33 @@ cudaError_t cdist_plan(lapl_attn_plan& p, int* ctas_per_sm) {
   if (!f) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.cd_smem);
   if (e != cudaSuccess) return e;
+  if (g.cd_gtc) {
+    // The tensor-core kernel asks for the largest shared-memory carveout; its CTAs per SM
+    // follow from the SM's shared memory (with the per-CTA reservation), registers and
+    // threads.  (The occupancy query reported one CTA per SM at d = 32, where two are
+    // resident.)  Tensor memory is no limit: two CTAs take at most 2 x 128 of 512 columns.
+    e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    int smem_sm = 0, reserved = 0, regs_sm = 0, threads_sm = 0;
+    e = cudaFuncGetAttributes(&fa, f);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, p.device);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, p.device);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, p.device);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, p.device);
+    if (e != cudaSuccess) return e;
+    const int by_smem = smem_sm / (int)(g.cd_smem + (size_t)reserved);
+    const int regs_cta = ((fa.numRegs + 7) / 8 * 8) * g.cd_threads;
+    const int by_regs = regs_cta > 0 ? regs_sm / regs_cta : 1;
+    const int by_threads = threads_sm / g.cd_threads;
+    *ctas_per_sm = std::max(1, std::min(std::min(by_smem, by_regs), std::min(by_threads, 2)));
+    return cudaSuccess;
+  }
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, f, g.cd_threads, g.cd_smem);
 }
 
@@ -180,6 +229,8 @@ cudaError_t launch_cdist(const lapl_attn_plan& p, const void* q, const void* k, 
                          float* dbg_dlk, float* dbg_a, cudaStream_t st) {
   const Geometry& g = p.geo;
   const bool bf16 = p.cfg.in_dtype == LAPL_BF16;
+  if (g.cd_gtc)
+    return launch_gauss_tc(p, q, k, landmarks, at, bt, dbg_dql, dbg_dlk, dbg_a, st);
   if (g.cd_tma || g.cd_l1) {
     const long long rows = (long long)g.bh * g.n;
     if (p.tmap_q_ptr != q) {

@@ -144,41 +144,6 @@ __device__ __forceinline__ void min_acc2(float& t0, float& t1, float x0, float x
       : "f"(x0), "f"(x1), "f"(l0), "f"(l1));
 }
 
-// Chunk sequence of a CTA: (side, head, first token, token count), advanced without divisions.
-struct ChunkIter {
-  long long pos, pend;
-  int side;
-  long long bh;
-  int n0, valid;
-
-  __device__ void init(const Partition& pt, int cta, int n) {
-    pos = part_start(pt, cta);
-    pend = part_start(pt, cta + 1);
-    if (pos >= pend) return;
-    side = pos < pt.uq ? 0 : 1;
-    const long long local = pos - (side ? pt.uq : 0);
-    bh = local / n;
-    n0 = (int)(local % n);
-    valid = (int)min((long long)min(kTile, n - n0), pend - pos);
-  }
-  __device__ bool done() const { return pos >= pend; }
-  __device__ bool last() const { return pos + valid >= pend; }
-  __device__ void next(int n, long long bh_count) {
-    pos += valid;
-    if (pos >= pend) return;
-    n0 += valid;
-    if (n0 == n) {
-      n0 = 0;
-      bh += 1;
-      if (side == 0 && bh == bh_count) {
-        side = 1;
-        bh = 0;
-      }
-    }
-    valid = (int)min((long long)min(kTile, n - n0), pend - pos);
-  }
-};
-
 // Address of channel quad c4 of token row t in a swizzled stage.
 template <int DH>
 __device__ __forceinline__ const float4* stage_quad(const char* stage, int t, int c4) {

@@ -116,41 +116,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned b
       : "memory");
 }
 
-// Chunk sequence of a CTA: (side, head, first token, token count), advanced without
-// divisions.  Producer and consumers walk the same sequence.
-struct ChunkIter {
-  long long pos, pend;
-  int side;
-  long long bh;
-  int n0, valid;
-
-  __device__ void init(const Partition& pt, int cta, int n) {
-    pos = part_start(pt, cta);
-    pend = part_start(pt, cta + 1);
-    if (pos >= pend) return;
-    side = pos < pt.uq ? 0 : 1;
-    const long long local = pos - (side ? pt.uq : 0);
-    bh = local / n;
-    n0 = (int)(local % n);
-    valid = (int)min((long long)min(kTile, n - n0), pend - pos);
-  }
-  __device__ bool done() const { return pos >= pend; }
-  __device__ void next(int n, long long bh_count) {
-    pos += valid;
-    if (pos >= pend) return;
-    n0 += valid;
-    if (n0 == n) {
-      n0 = 0;
-      bh += 1;
-      if (side == 0 && bh == bh_count) {
-        side = 1;
-        bh = 0;
-      }
-    }
-    valid = (int)min((long long)min(kTile, n - n0), pend - pos);
-  }
-};
-
 // Distances of one chunk from the swizzled stage: acc[r][jj] = sum_c |x_t,c - L_(warp*S+jj),c|
 // for tokens t = lane + 32 r (r < RV; the other rows are zero).
 template <int S, int DH, bool kBf16, int RV>

@@ -50,6 +50,44 @@ __host__ __device__ inline int part_owner(const Partition& pt, long long x) {
   return pt.rem + (int)((x - big) / pt.q);
 }
 
+// Tokens per chunk of the persistent distance kernels that walk a Partition.
+constexpr int kChunkTokens = 128;
+
+// Chunk sequence of a CTA: (side, head, first token, token count), advanced without divisions.
+struct ChunkIter {
+  long long pos, pend;
+  int side;
+  long long bh;
+  int n0, valid;
+
+  __device__ void init(const Partition& pt, int cta, int n) {
+    pos = part_start(pt, cta);
+    pend = part_start(pt, cta + 1);
+    if (pos >= pend) return;
+    side = pos < pt.uq ? 0 : 1;
+    const long long local = pos - (side ? pt.uq : 0);
+    bh = local / n;
+    n0 = (int)(local % n);
+    valid = (int)min((long long)min(kChunkTokens, n - n0), pend - pos);
+  }
+  __device__ bool done() const { return pos >= pend; }
+  __device__ bool last() const { return pos + valid >= pend; }
+  __device__ void next(int n, long long bh_count) {
+    pos += valid;
+    if (pos >= pend) return;
+    n0 += valid;
+    if (n0 == n) {
+      n0 = 0;
+      bh += 1;
+      if (side == 0 && bh == bh_count) {
+        side = 1;
+        bh = 0;
+      }
+    }
+    valid = (int)min((long long)min(kChunkTokens, n - n0), pend - pos);
+  }
+};
+
 // Offsets (bytes) of the workspace regions for one configuration.  All fp32.  The regions
 // only the training forward writes (xs, bv) come last, so a plain forward needs only the
 // first fwd_total bytes.
@@ -96,6 +134,8 @@ struct Geometry {
   bool cd_tma;             // distance kernel fed by TMA (cdist_tma.cuh), else by cp.async
   bool cd_l1;              // the TMA-fed kernel with the split FP32/ALU element arithmetic
                            // (cdist_l1.cuh); excludes cd_tma
+  bool cd_gtc;             // Gaussian kernel with the cross term on the tensor cores
+                           // (cdist_gauss_tc.cu); excludes cd_tma and cd_l1
   int cd_threads;          // threads of a distance-kernel CTA
   Partition cd_part;       // balanced split over cd_part.ctas persistent CTAs
   int bv_splits;           // B V: CTAs per head
@@ -155,6 +195,11 @@ struct lapl_attn_plan {
   mutable CUtensorMap tmap_bt, tmap_v;
   mutable const void* tmap_bt_ptr;
   mutable const void* tmap_v_ptr;
+  // Tensor maps of A^T and B^T for the tensor stores of the Gaussian tensor-core distance
+  // kernel, re-encoded when the pointers change.
+  mutable CUtensorMap tmap_at_st, tmap_bt_st;
+  mutable const void* tmap_at_st_ptr;
+  mutable const void* tmap_bt_st_ptr;
   // Fault injection for tests (lapl_attn_set_fault_injection): bound of the distance kernel's
   // barrier waits, and whether its producer skips each CTA's last copy.
   unsigned long long cd_wait_ns;
@@ -226,6 +271,15 @@ cudaError_t out_tc_configure(size_t smem);
 cudaError_t launch_output_tc(const lapl_attn_plan& p, const float* at, const float* mmat,
                              const float* mu, const float* rstd, const float* bias, void* out,
                              cudaStream_t st);
+// Gaussian-kernel distances with the cross term on the tensor cores (cdist_gauss_tc.cu):
+// fp32 or bf16 inputs with d in {32, 64}, m <= 64.  smem 0 (and kernel_ptr null) where there is
+// no instantiation.
+size_t gauss_tc_smem_bytes(int m, int d, bool bf16);
+int gauss_tc_threads();
+const void* gauss_tc_kernel_ptr(int d, bool bf16);
+cudaError_t launch_gauss_tc(const lapl_attn_plan& p, const void* q, const void* k,
+                            const float* landmarks, float* at, float* bt, float* dbg_dql,
+                            float* dbg_dlk, float* dbg_a, cudaStream_t st);
 // Column statistics of A as a launch of their own (with the tensor-core B V).
 cudaError_t launch_col_stats(const lapl_attn_plan& p, const float* at, float* mu, float* rstd,
                              float* dbg_mu, float* dbg_rstd, cudaStream_t st);

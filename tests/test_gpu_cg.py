@@ -175,7 +175,11 @@ def test_ill_conditioned_gaussian_is_a_valid_solution(name):
         assert np.linalg.cond(W) > 1e3
         res_gpu = np.linalg.norm(BV - W @ g["m"][0, h]) / np.linalg.norm(BV)
         res_orc = o["ns_resid"][0, h, -1]
-        bound = 10 * max(res_orc, np.linalg.cond(W) * 2.0 ** -24)
+        # fp32 CG with a recursively updated residual: after k iterations the true residual
+        # may exceed the recursive one by about u k |W| max_j |x_j| <= u k kappa(W) |b|
+        # (rounding of every update accumulates), so the attainable level is T kappa u.
+        T = w.ns_steps
+        bound = 10 * max(res_orc, T * np.linalg.cond(W) * 2.0 ** -24)
         assert res_gpu < bound, (h, res_gpu, res_orc, bound)
 
 

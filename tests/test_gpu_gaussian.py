@@ -47,13 +47,32 @@ def tol_of(w):
     return TOL_BF16 if w.dtype == "bf16" else TOL_F32
 
 
+def expected_feed(w) -> int:
+    """plan_info cdist_tma: 3 where the tensor-core distance kernel is instantiated (d = 32 or
+    64), else 0 (the CUDA-core kernel)."""
+    return 3 if w.head_dim in (32, 64) else 0
+
+
+def expansion_bound(x, lm):
+    """Bound on |D_gpu - D| for D = |x - l|^2 evaluated as |x|^2 + |l|^2 - 2 x.l in fp32 with
+    the cross term from TF32 high/low pieces: each of the three sums of at most d <= 64 terms
+    rounds within (d + 4) 2^-24 of its sum of magnitudes, the dropped low x low product and the
+    TF32 truncation of the low pieces add under 2^-20 of sum |x_c l_c|, and the fp32 landmarks
+    differ from the exact ones by 2^-24 relative; 2^-17 covers all of it.  x [N, d], lm [m, d]
+    (fp64); returns [N, m]."""
+    ax, al = np.abs(x), np.abs(lm)
+    nx = (x * x).sum(-1)
+    nl = (lm * lm).sum(-1)
+    return 2.0 ** -17 * (nx[:, None] + nl[None, :] + 2.0 * ax @ al.T)
+
+
 def test_tiny_intermediates():
     w = WORKLOADS["tiny_f32"]
     q, k, v = make_inputs(w)
     info = {}
     out, g = gpu_run(w, q, k, v, debug=True, info=info)
     ref, o = oracle_run(w, q, k, v, inter=True)
-    assert info["cdist_tma"] == 0 and info["device_errors"] == 0
+    assert info["cdist_tma"] == expected_feed(w) and info["device_errors"] == 0
     assert rel_to_max(g["landmarks"], o["landmarks"]) < 1e-6
     # squared distances: same values as sum_c (x_c - y_c)^2 in fp64, to fp32 rounding
     qd = q[0, 0].astype(np.float64)
@@ -108,7 +127,7 @@ def test_workload_full(name):
     info = {}
     out, _ = gpu_run(w, q, k, v, info=info)
     ref, _ = oracle_run(w, q, k, v)
-    assert info["cdist_tma"] == 0 and info["device_errors"] == 0
+    assert info["cdist_tma"] == expected_feed(w) and info["device_errors"] == 0
     err = slice_rel_err(out, ref)
     assert err < tol_of(w), err
 
@@ -207,3 +226,107 @@ def test_bias_deterministic():
     assert np.array_equal(a, b)
     ref, _ = oracle_run(w, q, k, v, bias=bias)
     assert slice_rel_err(a, ref) < TOL_F32
+
+
+# Shapes for the tensor-core distance kernel against the direct sum: ragged chunks, one head,
+# fewer rows than a chunk, every padding of m to 16 columns, both input types and head dims.
+TC_CASES = {
+    "f32_d32_m49_ragged": dict(batch=2, heads=2, grid_h=14, grid_w=14, num_landmarks=49),
+    "f32_d64_m16_15heads": dict(batch=3, heads=5, grid_h=20, grid_w=12, head_dim=64,
+                                num_landmarks=16),
+    "bf16_d64_m49": dict(batch=2, heads=2, grid_h=28, grid_w=28, head_dim=64, num_landmarks=49,
+                         dtype="bf16"),
+    "bf16_d32_m16": dict(dtype="bf16"),
+    "f32_d32_m1_129": dict(grid_h=3, grid_w=43, num_landmarks=1),
+    "f32_d32_m64": dict(grid_h=16, grid_w=16, num_landmarks=64),
+    "f32_d64_m36": dict(batch=2, heads=3, grid_h=12, grid_w=24, head_dim=64, num_landmarks=36),
+    "f32_d32_m4_64_tokens": dict(grid_h=8, grid_w=8, num_landmarks=4),
+    "f32_d32_m9": dict(grid_h=12, grid_w=12, num_landmarks=9),
+    "f32_d32_m25": dict(grid_h=20, grid_w=20, num_landmarks=25),
+}
+
+
+def _dyadic_window(w) -> bool:
+    s = int(round(w.num_landmarks ** 0.5))
+    win = (w.grid_h // s) * (w.grid_w // s)
+    return win & (win - 1) == 0
+
+
+@pytest.mark.parametrize("case", sorted(TC_CASES))
+def test_tensor_core_distances(case, monkeypatch):
+    """The tensor-core kernel (|x|^2 + |l|^2 - 2 x.l) against the oracle and against the
+    CUDA-core kernel's direct sum: bit for bit on integer inputs with dyadic landmarks (every
+    term exact), within the expansion's rounding bound on float inputs; O within the bars."""
+    w = TINY.replace(**TC_CASES[case])
+    for dist in ("integer", "gaussian"):
+        wd = w.replace(dist=dist)
+        q, k, v = make_inputs(wd, seed=5)
+        ref, o = oracle_run(wd, q, k, v, inter=True)
+        runs = {}
+        for feed in ("auto", "cp.async"):
+            if feed == "auto":
+                monkeypatch.delenv("LAPL_ATTN_CDIST_FEED", raising=False)
+            else:
+                monkeypatch.setenv("LAPL_ATTN_CDIST_FEED", feed)
+            info = {}
+            runs[feed] = gpu_run(wd, q, k, v, debug=True, info=info)
+            assert info["device_errors"] == 0
+            assert info["cdist_tma"] == (expected_feed(wd) if feed == "auto" else 0)
+        (out, g), (out_d, g_d) = runs["auto"], runs["cp.async"]
+        if dist == "integer" and _dyadic_window(wd):
+            for name in ("d_ql", "d_lk", "a"):
+                assert np.array_equal(g[name], g_d[name]), name
+            assert np.array_equal(g["d_ql"], o["d_ql"])
+            assert np.array_equal(g["d_lk"], o["d_lk"])
+        else:
+            for b in range(wd.batch):
+                for h in range(wd.heads):
+                    lm = o["landmarks"][b, h]
+                    bq = expansion_bound(q[b, h].astype(np.float64), lm)
+                    bk = expansion_bound(k[b, h].astype(np.float64), lm)
+                    assert (np.abs(g["d_ql"][b, h] - o["d_ql"][b, h]) <= bq).all(), (b, h)
+                    assert (np.abs(g["d_lk"][b, h].T - o["d_lk"][b, h].T) <= bk).all(), (b, h)
+        # O against the oracle, and against the direct sum's O to the same bar: on integer
+        # inputs at d = 64 the kernel values reach the fp32 normal limit, where the
+        # exponential flushes to zero and a last-bit difference of D decides which entries do.
+        assert slice_rel_err(out, ref) < tol_of(wd)
+        assert slice_rel_err(out, out_d) < tol_of(wd)
+
+
+def test_tensor_core_timeout_reported():
+    """Fault injection reaches the tensor-core distance kernel: its converters never publish
+    each CTA's last chunk, the MMA and epilogue waits run out, the distance kernel's bit is
+    reported, and a normal forward afterwards matches the oracle."""
+    import ctypes
+    import torch
+    import laplacian_nystr_attention_gb300 as lna
+    from laplacian_nystr_attention_gb300 import _lib
+    from parity_utils import to_device
+    w = WORKLOADS["stage1_f32"].replace(batch=2)
+    q, k, v = make_inputs(w)
+    dq, dk, dv = (to_device(x, w.dtype) for x in (q, k, v))
+    cfg = {**w.config(), "in_dtype": w.dtype, "kernel": GAUSS}
+    h = lna.lapl_attn_create(lna.make_config(**cfg))
+    try:
+        assert lna.lapl_attn_plan_info_get(h)["cdist_tma"] == 3
+        nbytes = lna.lapl_attn_workspace_size(h)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        out = torch.empty(dq.shape, dtype=torch.float32, device="cuda")
+        st = torch.cuda.current_stream().cuda_stream
+        args = (h, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), None, out.data_ptr(),
+                ws.data_ptr(), nbytes, st)
+        lna.lapl_attn_device_errors(h, st)
+        lna.lapl_attn_set_fault_injection(h, 50_000, 1)
+        lna.lapl_attn_forward(*args)
+        flags = ctypes.c_uint(0)
+        assert _lib.LIB.lapl_attn_device_errors(h, st, ctypes.byref(flags)) == \
+            _lib.LAPL_ERR_DEVICE_TIMEOUT
+        assert flags.value == 1
+        lna.lapl_attn_set_fault_injection(h, 0, 0)
+        out.fill_(float("nan"))
+        lna.lapl_attn_forward(*args)
+        assert lna.lapl_attn_device_errors(h, st) == 0
+        ref, _ = oracle_run(w, q, k, v)
+        assert slice_rel_err(out.cpu().numpy().astype(np.float64), ref) < TOL_F32
+    finally:
+        lna.lapl_attn_destroy(h)
