@@ -51,11 +51,9 @@ CLEAN_BYTES = 256 * 1024 * 1024
 # source files it was taken on; reported as null when the sources have changed since.
 CDIST_TRAFFIC = {
     ("l1", "stage1_f32", "laplacian"): (
-        13016576 + 4096, "11580dce3a30953b53f0ca1080d9299d5324bf61358acc1d91042f2c8a1049a5"),
-    ("tma", "stage1_f32", "laplacian"): (
-        13019904 + 4608, "f4b35b7f8fd1127af71c0e7d6fe76d03c474923fbba7229c9325ced339798112"),
-    ("cp.async", "stage1_f32", "gaussian"): (
-        13016576 + 0, "f4b35b7f8fd1127af71c0e7d6fe76d03c474923fbba7229c9325ced339798112"),
+        13017344 + 4864, "e9880fb8efa2a8c52c3adbf6ed59c19d0760cd9f1ddb52e5a9acc5d3660ecbf5"),
+    ("gtc", "stage1_f32", "gaussian"): (
+        12994816 + 0, "e9880fb8efa2a8c52c3adbf6ed59c19d0760cd9f1ddb52e5a9acc5d3660ecbf5"),
 }
 CDIST_SOURCES = ["cdist_kernel.cuh", "cdist_tma.cuh", "cdist_l1.cuh", "cdist.cu", "cdist_d32.cu",
                  "cdist_d64.cu", "cdist_d0.cu", "cdist_tma_f32.cu", "cdist_tma_bf16.cu",
