@@ -169,13 +169,15 @@ def gemm_chain_roofline(w, stage_ms: dict, peaks: dict, plan: dict) -> list:
     out_bytes = bh * m * n * 4 + bh * n * d * 4
     flops = 2.0 * bh * n * m * d
     tc = bool(plan.get("bv_tensor_core"))
+    out_tc = bool(plan.get("out_tensor_core"))
     entries = []
     for name, key, nbytes, kern in (
             ("B V + column statistics", "bv", bv_bytes,
              "col_stats_kernel + bv_tc_kernel (tcgen05, TF32 high/low)" if tc
              else "bv_kernel (statistics CTAs + CUDA-core FMA tiles)"),
             ("O = A^ M (whitening applied on load)", "output", out_bytes,
-             "output_kernel (CUDA-core FMA tiles)")):
+             "out_tc_kernel (tcgen05, TF32 high/low)" if out_tc
+             else "output_kernel (CUDA-core FMA tiles)")):
         ms = stage_ms[key]
         gbs = nbytes / (ms / 1e3) / 1e9
         entries.append({"stage": name, "kernel": kern, "bound": "hbm", "achieved": gbs,
@@ -256,7 +258,8 @@ def host_cores() -> int:
 def oracle_rate(w, q, k, v, budget_s: float, threads: int, kernel: str = "laplacian",
                 solver: str = "newton_schulz"):
     """Whole (b,h) slices of the fp64 oracle, `threads` at a time (the oracle's C call releases
-    the GIL), until the budget is spent.  Returns (tokens/s, slices done, seconds)."""
+    the GIL), cycling over the workload's slices until the budget is spent (at least one wave).
+    Returns (tokens/s, slices done, seconds)."""
     import concurrent.futures as cf
     import oracle
     oracle.build()
@@ -265,9 +268,9 @@ def oracle_rate(w, q, k, v, budget_s: float, threads: int, kernel: str = "laplac
     slices = w.batch * w.heads
     done, t0 = 0, time.perf_counter()
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
-        while done < slices and time.perf_counter() - t0 < budget_s:
-            wave = min(threads, slices - done)
-            list(ex.map(lambda s0: oracle.forward(cfg, q64, k64, v64, slices=(s0, 1)),
+        while done == 0 or time.perf_counter() - t0 < budget_s:
+            wave = threads
+            list(ex.map(lambda j: oracle.forward(cfg, q64, k64, v64, slices=(j % slices, 1)),
                         range(done, done + wave)))
             done += wave
     dt = time.perf_counter() - t0
@@ -283,7 +286,8 @@ def cpu_baseline(w, q, k, v, budget_s: float, kernel: str = "laplacian",
     allc, na, ta = oracle_rate(w, q, k, v, budget_s, cores, kernel, solver)
     return {"value": allc, "unit": UNIT, "cores": cores, "kind": "oracle",
             "value_1_core": one,
-            "sample": f"{na} of {w.batch * w.heads} (batch, head) slices of {w.name} in "
+            "sample": f"{na} slices ({na / (w.batch * w.heads):.1f} passes over the "
+                      f"{w.batch * w.heads} (batch, head) slices of {w.name}) in "
                       f"{ta:.2f} s on {cores} threads (one slice per thread), and {n1} slices in "
                       f"{t1:.2f} s on 1 thread; fp64 C oracle; tokens/s = slices * N / H / "
                       "seconds"}

@@ -58,3 +58,7 @@ def test_gemm_chain_roofline_bytes_and_fraction():
     assert abs(e[0]["achieved"] - e[0]["bytes"] / 1e-4 / 1e9) < 1e-6
     assert abs(e[1]["frac"] - e[1]["bytes"] / 5e-5 / 1e9 / 5000.0) < 1e-12
     assert "tcgen05" in e[0]["kernel"] and e[0]["flops"] == 2.0 * bh * n * m * d
+    assert e[1]["kernel"].startswith("output_kernel")
+    e = bench.gemm_chain_roofline(w, {"bv": 0.1, "output": 0.05}, {"hbm_gbs": 5000.0},
+                                  {"bv_tensor_core": 0, "out_tensor_core": 1})
+    assert e[0]["kernel"].startswith("bv_kernel") and e[1]["kernel"].startswith("out_tc_kernel")
