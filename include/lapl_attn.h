@@ -260,8 +260,9 @@ typedef struct {
 } lapl_attn_plan_info;
 
 /*
- * Fill *info.  Choices made at create: for the Laplacian kernel with fp32 inputs, d = 32 or 64
- * and m <= 49 the split-pipe TMA kernel (cdist_tma = 2), cp.async otherwise; for the Gaussian
+ * Fill *info.  Choices made at create: for the Laplacian kernel with fp32 inputs and d = 32 or
+ * 64 the split-pipe TMA kernel (cdist_tma = 2; two CTAs per SM, one CTA of twice the warps for
+ * m = 64), cp.async otherwise; for the Gaussian
  * kernel with d = 32 or 64 the tensor-core kernel (cdist_tma = 3), cp.async otherwise; for the
  * solve one CTA per head, with tensor-core products for m >= 25 and
  * CUDA-core products for m <= 16.  Environment variables read at create override them:

@@ -151,22 +151,24 @@ __device__ __forceinline__ const float4* stage_quad(const char* stage, int t, in
                                          (((c4 & 7) ^ (t & 7)) << 4));
 }
 
-// Distances of one chunk for the first RV row groups: sub-path accumulators accS (landmarks
-// 0 .. NS-1 of the warp) and min-path pair accumulators accM (landmarks NS .. S-1).
-template <int S, int NS, int DH, int RV>
+// Distances of one chunk for the first RV of this warp's RPL row groups (token rows
+// row0 + lane + 32 r): sub-path accumulators accS (landmarks 0 .. NS-1 of the warp) and min-path
+// pair accumulators accM (landmarks NS .. S-1).
+template <int S, int NS, int DH, int RV, int RPL>
 __device__ __forceinline__ void chunk_sums(const char* __restrict__ stage,
-                                           const float* __restrict__ lrow, int lane,
-                                           float (&accS)[4][NS > 0 ? NS : 1],
-                                           float (&accM)[4][S - NS][2]) {
+                                           const float* __restrict__ lrow, int lane, int row0,
+                                           float (&accS)[RPL][NS > 0 ? NS : 1],
+                                           float (&accM)[RPL][S - NS][2]) {
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
+  for (int r = 0; r < RPL; ++r) {
 #pragma unroll
     for (int j = 0; j < NS; ++j) accS[r][j] = 0.f;
 #pragma unroll
     for (int j = 0; j < S - NS; ++j) accM[r][j][0] = accM[r][j][1] = 0.f;
   }
-  // Lane row base and swizzle: row t = lane + 32 r keeps t % 8 = lane % 8 for every r.
-  const char* rowp = stage + lane * 128;
+  // Lane row base and swizzle: row t = row0 + lane + 32 r keeps t % 8 = lane % 8 for every r
+  // (row0 is a multiple of 32).
+  const char* rowp = stage + (row0 + lane) * 128;
   const int sw = lane & 7;
 #pragma unroll 2
   for (int c4 = 0; c4 < DH / 4; ++c4) {
@@ -192,11 +194,18 @@ __device__ __forceinline__ void chunk_sums(const char* __restrict__ stage,
   }
 }
 
-template <int S, int DH>
-__global__ void __launch_bounds__(32 * (S + 1), 2)
+// G row groups: G * S consumer warps; warp w owns landmarks (w mod S) * S .. + S - 1 and the
+// token rows of group w / S (4 / G row groups of 32 tokens each).  G = 1: two CTAs per SM;
+// G = 2: one CTA per SM with the same 2 S consumer warps, all on the same chunk sequence (two
+// CTAs on one SM do not progress at the same rate: the warp scheduler favours the older CTA,
+// which finishes its equal share well before the other).
+template <int S, int DH, int G>
+__global__ void __launch_bounds__(32 * (G * S + 1), G == 1 ? 2 : 1)
 cdist_l1_kernel(const Args a, const __grid_constant__ CUtensorMap map_q,
                 const __grid_constant__ CUtensorMap map_k) {
   using C = Cfg<DH>;
+  constexpr int CW = G * S;                     // consumer warps; the helper warp is CW
+  constexpr int RPL = 4 / G;                    // 32-row groups per consumer warp
   constexpr int kStages = C::kStages;
   constexpr int kLmSlots = kStages;
   constexpr int M = S * S;
@@ -219,7 +228,7 @@ cdist_l1_kernel(const Args a, const __grid_constant__ CUtensorMap map_q,
   const int n = a.n;
   const unsigned long long bound = a.wait_ns;
 
-  if (threadIdx.x == 32 * S) {
+  if (threadIdx.x == 32 * CW) {
     // The producer's first copies need the tensor maps: fetch the descriptors now.
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<unsigned long long>(&map_q))
                  : "memory");
@@ -230,7 +239,7 @@ cdist_l1_kernel(const Args a, const __grid_constant__ CUtensorMap map_q,
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&ready[s], 32);
-      mbar_init(&empty[s], S);
+      mbar_init(&empty[s], CW);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -239,7 +248,7 @@ cdist_l1_kernel(const Args a, const __grid_constant__ CUtensorMap map_q,
   __syncthreads();
   if (it.done()) return;
 
-  if (warp == S) {
+  if (warp == CW) {
     // ---------------- helper warp: copies (lane 0), token and landmark sums ----------------
     ChunkIter is = it;             // next chunk to issue (lane 0)
     int issued = 0, skipped = -1;
@@ -339,6 +348,8 @@ cdist_l1_kernel(const Args a, const __grid_constant__ CUtensorMap map_q,
   }
 
   // ---------------- consumers ----------------
+  const int lg = warp % S;                       // landmark group
+  const int row0 = (warp / S) * RPL * 32;        // first token row of this warp's row groups
   long long cur_bh = -1;
   int lm_slot = -1;
   const bool debug = a.dbg_dql || a.dbg_dlk || a.dbg_a;
@@ -357,35 +368,36 @@ cdist_l1_kernel(const Args a, const __grid_constant__ CUtensorMap map_q,
       return;
     }
     const char* stage = reinterpret_cast<const char*>(stages + s * C::kStageBytes);
-    const float* lrow = lms + lm_slot * M * DH + warp * S * DH;
+    const float* lrow = lms + lm_slot * M * DH + lg * S * DH;
 
-    float accS[4][NS > 0 ? NS : 1];
-    float accM[4][S - NS][2];
-    const int groups = (valid + 31) >> 5;
-    if (groups == 4) chunk_sums<S, NS, DH, 4>(stage, lrow, lane, accS, accM);
-    else if (groups == 3) chunk_sums<S, NS, DH, 3>(stage, lrow, lane, accS, accM);
-    else if (groups == 2) chunk_sums<S, NS, DH, 2>(stage, lrow, lane, accS, accM);
-    else chunk_sums<S, NS, DH, 1>(stage, lrow, lane, accS, accM);
+    float accS[RPL][NS > 0 ? NS : 1];
+    float accM[RPL][S - NS][2];
+    // 32-row groups of the chunk that hold tokens, counted within this warp's groups.
+    const int rv = min(max(((valid + 31) >> 5) - row0 / 32, 0), RPL);
+    if (rv == RPL) chunk_sums<S, NS, DH, RPL, RPL>(stage, lrow, lane, row0, accS, accM);
+    else if (RPL > 3 && rv == 3) chunk_sums<S, NS, DH, 3, RPL>(stage, lrow, lane, row0, accS, accM);
+    else if (RPL > 2 && rv == 2) chunk_sums<S, NS, DH, 2, RPL>(stage, lrow, lane, row0, accS, accM);
+    else if (rv >= 1) chunk_sums<S, NS, DH, 1, RPL>(stage, lrow, lane, row0, accS, accM);
     if (!__all_sync(0xffffffffu, mbar_wait(&ready[s], (i / kStages) & 1, bound))) {
       if (lane == 0) atomicOr(a.err, kErrCdistTimeout);
       return;
     }
-    float sqr[4], slj[S - NS];
+    float sqr[RPL], slj[S - NS];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) sqr[r] = sq[s * kTile + lane + 32 * r];
+    for (int r = 0; r < RPL; ++r) sqr[r] = sq[s * kTile + row0 + lane + 32 * r];
 #pragma unroll
-    for (int j = 0; j < S - NS; ++j) slj[j] = sl[lm_slot * 64 + warp * S + NS + j];
+    for (int j = 0; j < S - NS; ++j) slj[j] = sl[lm_slot * 64 + lg * S + NS + j];
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);     // this warp is done with the stage
 
     // Kernel values, stored straight from registers: per (landmark, row group) one warp store of
     // 32 consecutive tokens.
-    float* dst0 = (side == 0 ? a.at : a.bt) + ((size_t)bh * M + warp * S) * n + n0;
+    float* dst0 = (side == 0 ? a.at : a.bt) + ((size_t)bh * M + lg * S) * n + n0;
 #pragma unroll
     for (int jj = 0; jj < S; ++jj) {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int t = lane + 32 * r;
+      for (int r = 0; r < RPL; ++r) {
+        const int t = row0 + lane + 32 * r;
         float dist;
         if (jj < NS) {
           dist = accS[r][jj < NS ? jj : 0];
@@ -397,7 +409,7 @@ cdist_l1_kernel(const Args a, const __grid_constant__ CUtensorMap map_q,
         if (t < valid) {
           dst0[(size_t)jj * n + t] = kv;
           if (debug) {
-            const int j = warp * S + jj;
+            const int j = lg * S + jj;
             const size_t tok = (size_t)bh * n + n0 + t;
             if (side == 0) {
               if (a.dbg_dql) a.dbg_dql[tok * M + j] = dist;
@@ -424,7 +436,7 @@ inline size_t smem_bytes(int s, int d) {
          3 * stages * 8;
 }
 
-const void* kernel(int s, int d);   // cdist_l1.cu
+const void* kernel(int s, int d, int g);   // cdist_l1.cu
 
 }  // namespace cdist_l1
 }  // namespace lapl

@@ -134,6 +134,7 @@ struct Geometry {
   bool cd_tma;             // distance kernel fed by TMA (cdist_tma.cuh), else by cp.async
   bool cd_l1;              // the TMA-fed kernel with the split FP32/ALU element arithmetic
                            // (cdist_l1.cuh); excludes cd_tma
+  int cd_groups;           // split-pipe kernel: row groups per CTA (1: two CTAs per SM, 2: one)
   bool cd_gtc;             // Gaussian kernel with the cross term on the tensor cores
                            // (cdist_gauss_tc.cu); excludes cd_tma and cd_l1
   int cd_threads;          // threads of a distance-kernel CTA
