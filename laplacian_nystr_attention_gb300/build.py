@@ -22,8 +22,8 @@ LIB = os.path.join(HERE, "liblapl_attn.so")
 
 SOURCES = ["api.cu", "pool.cu", "ns.cu", "cdist.cu", "cdist_d32.cu", "cdist_d64.cu", "cdist_d0.cu",
            "cdist_gauss_d32.cu", "cdist_gauss_d64.cu", "cdist_gauss_d0.cu",
-           "cdist_tma_f32.cu", "cdist_tma_bf16.cu", "cdist_l1.cu", "cdist_gauss_tc.cu", "chain.cu",
-           "bv_tc.cu", "out_tc.cu", "noalloc.cu", "ns_tc.cu", "cg.cu", "backward.cu"]
+           "cdist_tma_f32.cu", "cdist_tma_bf16.cu", "cdist_l1.cu", "cdist_l1_bf16.cu",
+           "cdist_gauss_tc.cu", "chain.cu", "bv_tc.cu", "out_tc.cu", "noalloc.cu", "ns_tc.cu", "cg.cu", "backward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -11,12 +11,13 @@
 //                                      l2 distance) instantiations.
 //   cdist_l1_kernel (cdist_l1.cuh)     TMA-fed like cdist_tma_kernel, with a helper warp and the
 //                                      element work split between the FP32 and ALU pipes;
-//                                      fp32, d in {32, 64}, Laplacian kernel.
+//                                      fp32 with d in {32, 64}, bf16 with d = 64, Laplacian
+//                                      kernel.
 //   gauss_tc_kernel (cdist_gauss_tc.cu) Gaussian kernel only: |x|^2 + |l|^2 - 2 x.l with x.l on
 //                                      the tensor cores; fp32 or bf16, d in {32, 64}; the
 //                                      automatic choice for the Gaussian kernel there.
-// Automatic choice for the Laplacian kernel: cdist_l1_kernel wherever it is instantiated (fp32,
-// d = 32 or 64); otherwise the TMA feed for fp32, d = 32, s <= 7; cp.async elsewhere (faster where the TMA
+// Automatic choice for the Laplacian kernel: cdist_l1_kernel wherever it is instantiated (fp32
+// with d = 32 or 64, bf16 with d = 64); otherwise the TMA feed for fp32, d = 32, s <= 7; cp.async elsewhere (faster where the TMA
 // kernel's extra producer warp costs registers, s = 8, or its consumer warps each widen the
 // same bf16 chunk).  The environment variable LAPL_ATTN_CDIST_FEED=l1, =tma or =cp.async, read at
 // plan creation, overrides the choice (l1 and tma only where instantiated and the tensor holds
@@ -150,7 +151,7 @@ cudaError_t cdist_plan(lapl_attn_plan& p, int* ctas_per_sm) {
   // Tensor-map coordinates are 32-bit; a box must not be taller than the tensor.
   const bool tma_ok = rows >= cdist_tma::kTile && rows < (1LL << 31) &&
                       cdist_tma::encoder() != nullptr;
-  // The split-pipe kernel: fp32, d = 32 or 64, the Laplacian kernel.
+  // The split-pipe kernel: fp32 with d = 32 or 64, or bf16 with d = 64; the Laplacian kernel.
   // Row groups per CTA: 1 (two CTAs of s consumer warps per SM) for s <= 7; 2 (one CTA of 2 s
   // consumer warps per SM) for s = 8, where one group's registers would not leave room for two
   // CTAs.  For s <= 7 two CTAs measured faster than one CTA of both groups (stage-1 shape 24.2
@@ -159,8 +160,7 @@ cudaError_t cdist_plan(lapl_attn_plan& p, int* ctas_per_sm) {
   const char* grp = getenv("LAPL_ATTN_CDIST_GROUPS");
   g.cd_groups = grp && strcmp(grp, "1") == 0 ? 1 : grp && strcmp(grp, "2") == 0 ? 2
                                                                                  : (g.s == 8 ? 2 : 1);
-  const void* fl1 =
-      (!bf16 && !gauss && g.s <= 8) ? cdist_l1::kernel(g.s, g.d, g.cd_groups) : nullptr;
+  const void* fl1 = !gauss ? cdist_l1::kernel(g.s, g.d, g.cd_groups, bf16) : nullptr;
   g.cd_l1 = fl1 && tma_ok && (want_l1 || (!want_tma && !want_cpasync));
   // Gaussian kernel: the cross term x.l on the tensor cores where instantiated (d = 32 or 64;
   // the squared distance is |x|^2 + |l|^2 - 2 x.l); LAPL_ATTN_CDIST_FEED=cp.async forces the
@@ -185,7 +185,7 @@ cudaError_t cdist_plan(lapl_attn_plan& p, int* ctas_per_sm) {
     f = fl1;
     g.cd_tma = false;
     g.cd_threads = 32 * (g.cd_groups * g.s + 1);
-    g.cd_smem = cdist_l1::smem_bytes(g.s, g.d);
+    g.cd_smem = cdist_l1::smem_bytes(g.s, g.d, bf16, g.cd_groups);
   } else {
     const bool auto_tma = !bf16 && g.d == 32 && g.s <= 7;
     f = gauss ? nullptr : cdist_tma::pick(g.s, g.d, bf16);
@@ -259,7 +259,7 @@ cudaError_t launch_cdist(const lapl_attn_plan& p, const void* q, const void* k, 
       a.c_exp = p.neg_log2e_over_lambda;
       a.wait_ns = p.cd_wait_ns;
       a.skip_last_copy = p.cd_skip_last_copy;
-      const void* f = cdist_l1::kernel(g.s, g.d, g.cd_groups);
+      const void* f = cdist_l1::kernel(g.s, g.d, g.cd_groups, bf16);
       if (!f) return cudaErrorInvalidValue;
       void* args[] = {&a, &p.tmap_q, &p.tmap_k};
       return cudaLaunchKernel(f, dim3((unsigned)g.cd_part.ctas), dim3(g.cd_threads), args,

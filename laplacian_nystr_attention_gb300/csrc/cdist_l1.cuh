@@ -18,9 +18,11 @@
 // distance bit for bit; on float inputs the identity's rounding is that of sums of magnitude
 // at most sum_c (|q_c| + |l_c|).
 //
-// CTA: s consumer warps (warp w owns landmarks w*s .. w*s+s-1; lane l owns tokens l, l+32,
-// l+64, l+96 of a 128-token chunk) and one helper warp.  Lane 0 of the helper issues the
-// cp.async.bulk.tensor loads of the chunks (128 rows of 128 bytes per box, SWIZZLE_128B:
+// CTA: G row groups of s consumer warps (warp w owns landmarks (w mod s)*s .. +s-1; in group
+// w / s, lane l owns tokens l, l+32, ... of its 4/G 32-row groups of a 128-token chunk) and one
+// helper warp.  Inputs are fp32 (d = 32 or 64) or bf16 (d = 64; each 4-channel piece of a row
+// is widened to fp32 once in registers for all of the warp's landmarks).  Lane 0 of the helper
+// issues the cp.async.bulk.tensor loads of the chunks (128 rows of 128 bytes per box, SWIZZLE_128B:
 // 16-byte piece c of row t lands at c ^ (t % 8)) into a ring of kStages stages, plus a bulk
 // copy of a head's landmarks when the head changes; the whole helper warp then computes, per
 // chunk, the token sums Sq (and for a new head the landmark sums Sl).  Barriers per stage: full
@@ -60,10 +62,19 @@ struct Args {
   int skip_last_copy;           // fault injection for tests: never issue the last chunk's copy
 };
 
-template <int DH>
+// Stages of the copy ring (and landmark slots, as many): 4 of one 128-byte box per row, 2 of
+// two; 3 for bf16 rows of 64 channels with one row group, so that two CTAs (stages plus slots of
+// 64 x 49 fp32 landmarks) fit in one SM's shared memory.
+__host__ __device__ constexpr int l1_stages(int boxes, bool bf16, int d, int g) {
+  return boxes == 1 ? (bf16 && d == 64 && g == 1 ? 3 : 4) : 2;
+}
+
+template <int DH, bool kBf16, int G>
 struct Cfg {
-  static constexpr int kBoxes = DH / 32;                          // 128-byte boxes per row
-  static constexpr int kStages = DH == 32 ? 4 : 2;
+  static constexpr int kElemBytes = kBf16 ? 2 : 4;
+  static constexpr int kBoxElems = 128 / kElemBytes;                 // elements per 128-byte box
+  static constexpr int kBoxes = DH / kBoxElems;                      // 128-byte boxes per row
+  static constexpr int kStages = l1_stages(kBoxes, kBf16, DH, G);
   static constexpr unsigned kStageBytes = kTile * 128 * kBoxes;
 };
 
@@ -144,17 +155,26 @@ __device__ __forceinline__ void min_acc2(float& t0, float& t1, float x0, float x
       : "f"(x0), "f"(x1), "f"(l0), "f"(l1));
 }
 
-// Address of channel quad c4 of token row t in a swizzled stage.
-template <int DH>
-__device__ __forceinline__ const float4* stage_quad(const char* stage, int t, int c4) {
-  return reinterpret_cast<const float4*>(stage + (c4 >> 3) * (kTile * 128) + t * 128 +
-                                         (((c4 & 7) ^ (t & 7)) << 4));
+// Channel quad c4 of token row t in a swizzled stage, as fp32 (bf16 rows widen exactly: a bf16
+// value is the upper half of the fp32 with the same value).
+template <bool kBf16>
+__device__ __forceinline__ float4 stage_quad(const char* stage, int t, int c4) {
+  if constexpr (kBf16) {
+    const int p = c4 >> 1;                        // 16-byte piece of 8 channels
+    const uint2 w = *reinterpret_cast<const uint2*>(stage + (p >> 3) * (kTile * 128) + t * 128 +
+                                                    (((p & 7) ^ (t & 7)) << 4) + (c4 & 1) * 8);
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                       __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+  } else {
+    return *reinterpret_cast<const float4*>(stage + (c4 >> 3) * (kTile * 128) + t * 128 +
+                                            (((c4 & 7) ^ (t & 7)) << 4));
+  }
 }
 
 // Distances of one chunk for the first RV of this warp's RPL row groups (token rows
 // row0 + lane + 32 r): sub-path accumulators accS (landmarks 0 .. NS-1 of the warp) and min-path
 // pair accumulators accM (landmarks NS .. S-1).
-template <int S, int NS, int DH, int RV, int RPL>
+template <int S, int NS, int DH, int RV, int RPL, bool kBf16>
 __device__ __forceinline__ void chunk_sums(const char* __restrict__ stage,
                                            const float* __restrict__ lrow, int lane, int row0,
                                            float (&accS)[RPL][NS > 0 ? NS : 1],
@@ -172,10 +192,22 @@ __device__ __forceinline__ void chunk_sums(const char* __restrict__ stage,
   const int sw = lane & 7;
 #pragma unroll 2
   for (int c4 = 0; c4 < DH / 4; ++c4) {
-    const char* pc = rowp + (c4 >> 3) * (kTile * 128) + (((c4 & 7) ^ sw) << 4);
     float4 x[RV];
+    if constexpr (kBf16) {
+      // 4 bf16 channels (8 bytes) per row, widened to fp32 once for all of the warp's landmarks.
+      const int p = c4 >> 1;
+      const char* pc = rowp + (p >> 3) * (kTile * 128) + (((p & 7) ^ sw) << 4) + (c4 & 1) * 8;
 #pragma unroll
-    for (int r = 0; r < RV; ++r) x[r] = *reinterpret_cast<const float4*>(pc + r * 32 * 128);
+      for (int r = 0; r < RV; ++r) {
+        const uint2 w = *reinterpret_cast<const uint2*>(pc + r * 32 * 128);
+        x[r] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                           __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+      }
+    } else {
+      const char* pc = rowp + (c4 >> 3) * (kTile * 128) + (((c4 & 7) ^ sw) << 4);
+#pragma unroll
+      for (int r = 0; r < RV; ++r) x[r] = *reinterpret_cast<const float4*>(pc + r * 32 * 128);
+    }
 #pragma unroll
     for (int jj = 0; jj < S; ++jj) {
       const float4 l = *reinterpret_cast<const float4*>(&lrow[jj * DH + 4 * c4]);
@@ -199,11 +231,11 @@ __device__ __forceinline__ void chunk_sums(const char* __restrict__ stage,
 // G = 2: one CTA per SM with the same 2 S consumer warps, all on the same chunk sequence (two
 // CTAs on one SM do not progress at the same rate: the warp scheduler favours the older CTA,
 // which finishes its equal share well before the other).
-template <int S, int DH, int G>
+template <int S, int DH, int G, bool kBf16>
 __global__ void __launch_bounds__(32 * (G * S + 1), G == 1 ? 2 : 1)
 cdist_l1_kernel(const Args a, const __grid_constant__ CUtensorMap map_q,
                 const __grid_constant__ CUtensorMap map_k) {
-  using C = Cfg<DH>;
+  using C = Cfg<DH, kBf16, G>;
   constexpr int CW = G * S;                     // consumer warps; the helper warp is CW
   constexpr int RPL = 4 / G;                    // 32-row groups per consumer warp
   constexpr int kStages = C::kStages;
@@ -285,8 +317,8 @@ cdist_l1_kernel(const Args a, const __grid_constant__ CUtensorMap map_q,
             const int row = (int)(is.bh * n + is.n0);
 #pragma unroll
             for (int b = 0; b < C::kBoxes; ++b)
-              tma_load_2d(stages + s * C::kStageBytes + b * (kTile * 128), map, b * 32, row,
-                          &full[s]);
+              tma_load_2d(stages + s * C::kStageBytes + b * (kTile * 128), map,
+                          b * C::kBoxElems, row, &full[s]);
             if (new_head)
               bulk_load(lms + issue_slot * M * DH, a.landmarks + (size_t)is.bh * M * DH,
                         kLmBytes, &full[s]);
@@ -325,7 +357,7 @@ cdist_l1_kernel(const Args a, const __grid_constant__ CUtensorMap map_q,
         float acc = 0.f;
 #pragma unroll
         for (int c4 = 0; c4 < DH / 4; ++c4) {
-          const float4 x = *stage_quad<DH>(stage, t, c4);
+          const float4 x = stage_quad<kBf16>(stage, t, c4);
           acc += x.x;
           acc += x.y;
           acc += x.z;
@@ -374,10 +406,10 @@ cdist_l1_kernel(const Args a, const __grid_constant__ CUtensorMap map_q,
     float accM[RPL][S - NS][2];
     // 32-row groups of the chunk that hold tokens, counted within this warp's groups.
     const int rv = min(max(((valid + 31) >> 5) - row0 / 32, 0), RPL);
-    if (rv == RPL) chunk_sums<S, NS, DH, RPL, RPL>(stage, lrow, lane, row0, accS, accM);
-    else if (RPL > 3 && rv == 3) chunk_sums<S, NS, DH, 3, RPL>(stage, lrow, lane, row0, accS, accM);
-    else if (RPL > 2 && rv == 2) chunk_sums<S, NS, DH, 2, RPL>(stage, lrow, lane, row0, accS, accM);
-    else if (rv >= 1) chunk_sums<S, NS, DH, 1, RPL>(stage, lrow, lane, row0, accS, accM);
+    if (rv == RPL) chunk_sums<S, NS, DH, RPL, RPL, kBf16>(stage, lrow, lane, row0, accS, accM);
+    else if (RPL > 3 && rv == 3) chunk_sums<S, NS, DH, 3, RPL, kBf16>(stage, lrow, lane, row0, accS, accM);
+    else if (RPL > 2 && rv == 2) chunk_sums<S, NS, DH, 2, RPL, kBf16>(stage, lrow, lane, row0, accS, accM);
+    else if (rv >= 1) chunk_sums<S, NS, DH, 1, RPL, kBf16>(stage, lrow, lane, row0, accS, accM);
     if (!__all_sync(0xffffffffu, mbar_wait(&ready[s], (i / kStages) & 1, bound))) {
       if (lane == 0) atomicOr(a.err, kErrCdistTimeout);
       return;
@@ -427,16 +459,19 @@ cdist_l1_kernel(const Args a, const __grid_constant__ CUtensorMap map_q,
 
 // Dynamic shared memory: 1024 bytes of alignment slack, stages, landmark slots, token sums,
 // landmark sums and 3 barriers per stage.
-inline size_t smem_bytes(int s, int d) {
+inline size_t smem_bytes(int s, int d, bool bf16, int g) {
   const size_t m = (size_t)s * s;
-  const int stages = d == 32 ? Cfg<32>::kStages : Cfg<64>::kStages;
-  const size_t stage = (size_t)kTile * 128 * (d / 32);
+  const int boxes = d * (bf16 ? 2 : 4) / 128;
+  const int stages = l1_stages(boxes, bf16, d, g);
+  const size_t stage = (size_t)kTile * 128 * boxes;
   return 1024 + stages * stage + (size_t)stages * m * d * sizeof(float) +
          (size_t)stages * kTile * sizeof(float) + (size_t)stages * 64 * sizeof(float) +
          3 * stages * 8;
 }
 
-const void* kernel(int s, int d, int g);   // cdist_l1.cu
+// Instantiations: fp32 with d = 32 or 64 (cdist_l1.cu), bf16 with d = 64 (cdist_l1_bf16.cu);
+// g row groups (1 or 2).
+const void* kernel(int s, int d, int g, bool bf16);
 
 }  // namespace cdist_l1
 }  // namespace lapl
