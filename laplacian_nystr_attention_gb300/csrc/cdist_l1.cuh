@@ -64,11 +64,11 @@ struct Args {
 
 // Stages of the copy ring (and landmark slots, as many): 4 of one 128-byte box per row, 2 of
 // two; 3 for bf16 rows of 64 channels with one row group, so that two CTAs (stages plus slots of
-// 64 x 49 fp32 landmarks) fit in one SM's shared memory.
+// 64 x 49 fp32 landmarks) fit in one SM's shared memory.  (Four stages of two boxes with one CTA
+// per SM measured no faster.)
 __host__ __device__ constexpr int l1_stages(int boxes, bool bf16, int d, int g) {
   return boxes == 1 ? (bf16 && d == 64 && g == 1 ? 3 : 4) : 2;
 }
-
 template <int DH, bool kBf16, int G>
 struct Cfg {
   static constexpr int kElemBytes = kBf16 ? 2 : 4;
@@ -423,32 +423,45 @@ cdist_l1_kernel(const Args a, const __grid_constant__ CUtensorMap map_q,
     if (lane == 0) mbar_arrive(&empty[s]);     // this warp is done with the stage
 
     // Kernel values, stored straight from registers: per (landmark, row group) one warp store of
-    // 32 consecutive tokens.
+    // 32 consecutive tokens.  Every value is formed first, without a branch, then stored; the
+    // debug copies have a loop of their own.
     float* dst0 = (side == 0 ? a.at : a.bt) + ((size_t)bh * M + lg * S) * n + n0;
+    float dist[S][RPL];
 #pragma unroll
     for (int jj = 0; jj < S; ++jj) {
 #pragma unroll
       for (int r = 0; r < RPL; ++r) {
-        const int t = row0 + lane + 32 * r;
-        float dist;
         if (jj < NS) {
-          dist = accS[r][jj < NS ? jj : 0];
+          dist[jj][r] = accS[r][jj < NS ? jj : 0];
         } else {
           const float* p = accM[r][jj >= NS ? jj - NS : 0];
-          dist = fmaf(-2.f, p[0] + p[1], sqr[r] + slj[jj >= NS ? jj - NS : 0]);
+          dist[jj][r] = fmaf(-2.f, p[0] + p[1], sqr[r] + slj[jj >= NS ? jj - NS : 0]);
         }
-        const float kv = laplacian_from_distance(dist, a.c_exp);
-        if (t < valid) {
-          dst0[(size_t)jj * n + t] = kv;
-          if (debug) {
-            const int j = lg * S + jj;
-            const size_t tok = (size_t)bh * n + n0 + t;
-            if (side == 0) {
-              if (a.dbg_dql) a.dbg_dql[tok * M + j] = dist;
-              if (a.dbg_a) a.dbg_a[tok * M + j] = kv;
-            } else if (a.dbg_dlk) {
-              a.dbg_dlk[((size_t)bh * M + j) * n + n0 + t] = dist;
-            }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < RPL; ++r) {
+      const int t = row0 + lane + 32 * r;
+      if (t < valid) {
+#pragma unroll
+        for (int jj = 0; jj < S; ++jj)
+          dst0[(size_t)jj * n + t] = laplacian_from_distance(dist[jj][r], a.c_exp);
+      }
+    }
+    if (debug) {
+#pragma unroll
+      for (int r = 0; r < RPL; ++r) {
+        const int t = row0 + lane + 32 * r;
+        if (t >= valid) continue;
+        const size_t tok = (size_t)bh * n + n0 + t;
+#pragma unroll
+        for (int jj = 0; jj < S; ++jj) {
+          const int j = lg * S + jj;
+          if (side == 0) {
+            if (a.dbg_dql) a.dbg_dql[tok * M + j] = dist[jj][r];
+            if (a.dbg_a) a.dbg_a[tok * M + j] = laplacian_from_distance(dist[jj][r], a.c_exp);
+          } else if (a.dbg_dlk) {
+            a.dbg_dlk[((size_t)bh * M + j) * n + n0 + t] = dist[jj][r];
           }
         }
       }
