@@ -158,7 +158,8 @@ lapl_status lapl_attn_forward_debug(lapl_attn_handle h, const void* q, const voi
 
 /*
  * Bytes of device staging memory forward_host() needs: device copies of Q, K, V, O and the
- * workspace, each 256-byte aligned.
+ * workspace, each 256-byte aligned (for a batch of two or more, one such region per half-batch
+ * forward, see forward_host()).
  */
 lapl_status lapl_attn_host_staging_size(lapl_attn_handle h, size_t* bytes);
 
@@ -168,6 +169,12 @@ lapl_status lapl_attn_host_staging_size(lapl_attn_handle h, size_t* bytes);
  * O back into out (host, out_dtype), all on `stream`.  Page-locked host buffers make the copies
  * asynchronous; with pageable memory the CUDA runtime stages them synchronously.  Returns
  * after enqueueing: synchronise the stream before reading out.
+ * With a batch of two or more the call runs two forwards of half the batch each (the first
+ * ceil(B/2) batches on `stream`, the others on a stream of the plan, joined back into `stream`
+ * before the call's work ends), so that one half's copies overlap the other's kernels and the
+ * first half's output is copied back while the second computes.  The results equal those of
+ * forward() bit for bit.  The environment variable LAPL_ATTN_HOST_SPLIT=0, read at create,
+ * keeps a single forward.
  */
 lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void* k,
                                    const void* v, const float* bias, void* out, void* staging,

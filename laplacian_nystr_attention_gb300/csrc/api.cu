@@ -89,6 +89,15 @@ void setup_cdist_partition(Geometry& g, int ctas) {
 }  // namespace
 }  // namespace lapl
 
+namespace lapl {
+namespace {
+// A plan for cfg.  force_tps > 0: B V takes force_tps tiles per split (the split count follows),
+// in place of the plan's own choice; the host entry point's half-batch plans use this so that
+// every slice is reduced in the same order as by the full plan.
+lapl_status create_plan(const lapl_attn_config* cfg, lapl_attn_plan** out, int force_tps);
+}  // namespace
+}  // namespace lapl
+
 using namespace lapl;
 
 extern "C" {
@@ -112,6 +121,58 @@ const char* lapl_attn_status_string(lapl_status s) {
 const char* lapl_attn_last_error(lapl_attn_handle h) { return h ? h->last_error : ""; }
 
 lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out) {
+  if (!out) return LAPL_ERR_INVALID_ARG;
+  *out = nullptr;
+  lapl_attn_plan* p = nullptr;
+  lapl_status st = create_plan(cfg, &p, 0);
+  if (st != LAPL_OK) return st;
+  // lapl_attn_forward_host runs two half-batch forwards on two streams, so that the copies of
+  // one half overlap the other's kernels and the first half's output leaves while the second
+  // computes.  LAPL_ATTN_HOST_SPLIT=0, read here, keeps one forward.
+  const char* split_env = getenv("LAPL_ATTN_HOST_SPLIT");
+  const bool split = cfg->batch >= 2 && !(split_env && strcmp(split_env, "0") == 0);
+  if (split) {
+    for (int i = 0; i < 2 && st == LAPL_OK; ++i) {
+      lapl_attn_config hc = *cfg;
+      hc.batch = i == 0 ? (cfg->batch + 1) / 2 : cfg->batch / 2;
+      st = create_plan(&hc, &p->half[i], p->geo.bv_tiles_per_split);
+    }
+    // The halves must compute every slice with the full plan's kernels (a half too small for a
+    // TMA box of rows, for instance, would take another distance kernel): else one forward.
+    for (int i = 0; i < 2 && st == LAPL_OK; ++i) {
+      const Geometry &a = p->geo, &b = p->half[i]->geo;
+      if (a.cd_l1 != b.cd_l1 || a.cd_tma != b.cd_tma || a.cd_gtc != b.cd_gtc ||
+          a.cd_groups != b.cd_groups || a.bv_tc != b.bv_tc || a.out_tc != b.out_tc ||
+          a.ns_tc != b.ns_tc || a.ns_cluster != b.ns_cluster || a.bv_splits != b.bv_splits) {
+        for (int j = 0; j < 2; ++j) {
+          lapl_attn_destroy(p->half[j]);
+          p->half[j] = nullptr;
+        }
+        *out = p;
+        return LAPL_OK;
+      }
+    }
+    cudaError_t e = cudaSuccess;
+    if (st == LAPL_OK) e = cudaStreamCreateWithFlags(&p->pipe_stream, cudaStreamNonBlocking);
+    if (st == LAPL_OK && e == cudaSuccess)
+      e = cudaEventCreateWithFlags(&p->ev_pipe_start, cudaEventDisableTiming);
+    if (st == LAPL_OK && e == cudaSuccess)
+      e = cudaEventCreateWithFlags(&p->ev_pipe_join, cudaEventDisableTiming);
+    if (st == LAPL_OK && e != cudaSuccess) st = LAPL_ERR_CUDA;
+    if (st != LAPL_OK) {
+      lapl_attn_destroy(p);
+      return st;
+    }
+  }
+  *out = p;
+  return LAPL_OK;
+}
+
+}  // extern "C"
+
+namespace lapl {
+namespace {
+lapl_status create_plan(const lapl_attn_config* cfg, lapl_attn_plan** out, int force_tps) {
   if (!out) return LAPL_ERR_INVALID_ARG;
   *out = nullptr;
   lapl_status st = validate(cfg);
@@ -306,6 +367,10 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
         g.bv_splits = splits;
       }
     }
+    if (force_tps > 0) {
+      g.bv_tiles_per_split = force_tps;
+      g.bv_splits = (tiles + force_tps - 1) / force_tps;
+    }
   }
   {
     // No more CTAs than chunks of work.
@@ -364,6 +429,10 @@ lapl_status lapl_attn_create(const lapl_attn_config* cfg, lapl_attn_handle* out)
   *out = p;
   return LAPL_OK;
 }
+}  // namespace
+}  // namespace lapl
+
+extern "C" {
 
 lapl_status lapl_attn_workspace_size(lapl_attn_handle h, size_t* bytes) {
   if (!h || !bytes) return LAPL_ERR_INVALID_ARG;
@@ -570,6 +639,16 @@ struct StagingLayout {
   size_t q, k, v, out, bias, ws, total;
 };
 
+StagingLayout staging_layout(const lapl_attn_plan* p);
+
+// Bytes of the host entry point's staging buffer: one forward's inputs, output and workspace,
+// or, with half-batch plans, the two halves' regions one after the other.
+size_t staging_bytes(const lapl_attn_plan* p) {
+  if (p->half[0])
+    return align_up(staging_layout(p->half[0]).total, kAlign) + staging_layout(p->half[1]).total;
+  return staging_layout(p).total;
+}
+
 StagingLayout staging_layout(const lapl_attn_plan* p) {
   StagingLayout s;
   const size_t elems = (size_t)p->geo.bh * p->geo.n * p->geo.d;
@@ -589,32 +668,24 @@ StagingLayout staging_layout(const lapl_attn_plan* p) {
 
 lapl_status lapl_attn_host_staging_size(lapl_attn_handle h, size_t* bytes) {
   if (!h || !bytes) return LAPL_ERR_INVALID_ARG;
-  *bytes = staging_layout(h).total;
+  *bytes = staging_bytes(h);
   return LAPL_OK;
 }
 
-lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void* k,
-                                   const void* v, const float* bias, void* out, void* staging,
-                                   size_t staging_bytes, void* stream) {
-  if (!h) return LAPL_ERR_INVALID_ARG;
-  if (h->geo.bh == 0) return LAPL_OK;
-  if (!q || !k || !v || !out || !staging) return LAPL_ERR_INVALID_ARG;
-  if (!aligned16(staging)) return LAPL_ERR_ALIGNMENT;
+}  // extern "C"
+
+namespace lapl {
+namespace {
+// One forward of plan h from host buffers through the staging region `base` (laid out by
+// staging_layout(h)), enqueued on st.  Arguments already checked.
+lapl_status forward_host_one(lapl_attn_handle h, const void* q, const void* k, const void* v,
+                             const float* bias, void* out, char* base, cudaStream_t st) {
   const StagingLayout s = staging_layout(h);
-  if (staging_bytes < s.total) return LAPL_ERR_WORKSPACE;
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    set_error(h, e, "forward_host/device");
-    return LAPL_ERR_CUDA;
-  }
-  if (dev != h->device) return LAPL_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  char* base = static_cast<char*>(staging);
   const size_t elems = (size_t)h->geo.bh * h->geo.n * h->geo.d;
   const size_t in_b = elems * elem_bytes(h->cfg.in_dtype);
   const size_t out_b = elems * elem_bytes(h->cfg.out_dtype);
   const bool side_copies = h->geo.ns_exclusive && !h->geo.cg;
+  cudaError_t e = cudaSuccess;
   // After the side stream has been given copies, every exit joins it back into the launching
   // stream, so that a caller who synchronises that stream also waits for those copies before
   // it frees or reuses the host inputs or the staging buffer.
@@ -643,8 +714,8 @@ lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void
     if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.q, q, in_b, cudaMemcpyHostToDevice, side);
     if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.v, v, in_b, cudaMemcpyHostToDevice, side);
   } else {
-    e = cudaMemcpyAsync(base + s.q, q, in_b, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.k, k, in_b, cudaMemcpyHostToDevice, st);
+    e = cudaMemcpyAsync(base + s.k, k, in_b, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.q, q, in_b, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(base + s.v, v, in_b, cudaMemcpyHostToDevice, st);
   }
   float* dbias = nullptr;
@@ -660,6 +731,63 @@ lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void
   e = cudaMemcpyAsync(out, base + s.out, out_b, cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return fail(LAPL_ERR_CUDA, e, "forward_host/d2h");
   return LAPL_OK;
+}
+}  // namespace
+}  // namespace lapl
+
+extern "C" {
+
+lapl_status lapl_attn_forward_host(lapl_attn_handle h, const void* q, const void* k,
+                                   const void* v, const float* bias, void* out, void* staging,
+                                   size_t staging_bytes_given, void* stream) {
+  if (!h) return LAPL_ERR_INVALID_ARG;
+  if (h->geo.bh == 0) return LAPL_OK;
+  if (!q || !k || !v || !out || !staging) return LAPL_ERR_INVALID_ARG;
+  if (!aligned16(staging)) return LAPL_ERR_ALIGNMENT;
+  if (staging_bytes_given < staging_bytes(h)) return LAPL_ERR_WORKSPACE;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error(h, e, "forward_host/device");
+    return LAPL_ERR_CUDA;
+  }
+  if (dev != h->device) return LAPL_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(staging);
+  if (!h->half[0]) return forward_host_one(h, q, k, v, bias, out, base, st);
+
+  // Two half-batch forwards: the first on the launching stream, the second on the pipe stream
+  // (after everything enqueued on the launching stream so far), joined back at the end.  Each
+  // half's slices are computed exactly as by the full plan (same kernels, the B V partition
+  // forced to the full plan's), so the output is the same bit for bit.
+  lapl_attn_plan* h0 = h->half[0];
+  lapl_attn_plan* h1 = h->half[1];
+  const size_t in0 = (size_t)h0->geo.bh * h0->geo.n * h0->geo.d * elem_bytes(h->cfg.in_dtype);
+  const size_t out0 = (size_t)h0->geo.bh * h0->geo.n * h0->geo.d * elem_bytes(h->cfg.out_dtype);
+  char* base1 = base + align_up(staging_layout(h0).total, kAlign);
+  e = cudaEventRecord(h->ev_pipe_start, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->pipe_stream, h->ev_pipe_start, 0);
+  if (e != cudaSuccess) {
+    set_error(h, e, "forward_host/fork");
+    return LAPL_ERR_CUDA;
+  }
+  lapl_status r = forward_host_one(h0, q, k, v, bias, out, base, st);
+  if (r != LAPL_OK) {
+    snprintf(h->last_error, sizeof(h->last_error), "%s", h0->last_error);
+    return r;
+  }
+  r = forward_host_one(h1, static_cast<const char*>(q) + in0, static_cast<const char*>(k) + in0,
+                       static_cast<const char*>(v) + in0, bias, static_cast<char*>(out) + out0,
+                       base1, h->pipe_stream);
+  if (r != LAPL_OK) snprintf(h->last_error, sizeof(h->last_error), "%s", h1->last_error);
+  // The launching stream waits for the second half whatever happened to it.
+  e = cudaEventRecord(h->ev_pipe_join, h->pipe_stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_pipe_join, 0);
+  if (r == LAPL_OK && e != cudaSuccess) {
+    set_error(h, e, "forward_host/join");
+    return LAPL_ERR_CUDA;
+  }
+  return r;
 }
 
 lapl_status lapl_attn_set_timing(lapl_attn_handle h, int enable) {
@@ -746,6 +874,8 @@ lapl_status lapl_attn_set_fault_injection(lapl_attn_handle h, unsigned long long
   if (!h || (skip_last_copy != 0 && skip_last_copy != 1)) return LAPL_ERR_INVALID_ARG;
   h->cd_wait_ns = wait_ns ? wait_ns : 1000000000ull;
   h->cd_skip_last_copy = skip_last_copy;
+  for (int i = 0; i < 2; ++i)
+    if (h->half[i]) lapl_attn_set_fault_injection(h->half[i], wait_ns, skip_last_copy);
   return LAPL_OK;
 }
 
@@ -766,6 +896,10 @@ lapl_status lapl_attn_plan_info_get(lapl_attn_handle h, lapl_attn_plan_info* inf
 
 lapl_status lapl_attn_destroy(lapl_attn_handle h) {
   if (!h) return LAPL_OK;
+  for (int i = 0; i < 2; ++i) lapl_attn_destroy(h->half[i]);
+  if (h->ev_pipe_start) cudaEventDestroy(h->ev_pipe_start);
+  if (h->ev_pipe_join) cudaEventDestroy(h->ev_pipe_join);
+  if (h->pipe_stream) cudaStreamDestroy(h->pipe_stream);
   for (int i = 0; i < kMarks; ++i)
     if (h->ev_stage[i]) cudaEventDestroy(h->ev_stage[i]);
   if (h->ev_join) cudaEventDestroy(h->ev_join);

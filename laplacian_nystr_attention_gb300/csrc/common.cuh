@@ -205,6 +205,11 @@ struct lapl_attn_plan {
   // barrier waits, and whether its producer skips each CTA's last copy.
   unsigned long long cd_wait_ns;
   int cd_skip_last_copy;
+  // lapl_attn_forward_host: two half-batch plans (first ceil(B/2), then floor(B/2) batches; null
+  // when it runs one forward), the stream the second half runs on, and its fork and join events.
+  lapl_attn_plan* half[2];
+  cudaStream_t pipe_stream;
+  cudaEvent_t ev_pipe_start, ev_pipe_join;
   char last_error[256];
 };
 

@@ -240,22 +240,46 @@ def test_error_paths():
     att.close()
 
 
-def test_forward_host_matches_device_path():
+HOST_CASES = {
+    "stage1_batch2": ("stage1_f32", dict(batch=2), False),
+    "stage1_full": ("stage1_f32", dict(), False),
+    "stage23_batch3_bias": ("stage23_bf16", dict(batch=3), True),
+    "tiny_batch1": ("tiny_f32", dict(), False),
+    "sweep_bf16_4096_batch2": ("sweep_bf16_4096", dict(batch=2, heads=4), True),
+}
+
+
+@pytest.mark.parametrize("split", ["1", "0"])
+@pytest.mark.parametrize("case", sorted(HOST_CASES))
+def test_forward_host_matches_device_path(case, split, monkeypatch):
+    """lapl_attn_forward_host (two half-batch forwards for a batch of two or more, or one with
+    LAPL_ATTN_HOST_SPLIT=0) gives O bit for bit equal to lapl_attn_forward."""
     import torch
     import laplacian_nystr_attention_gb300 as lna
-    from laplacian_nystr_attention_gb300 import _lib
-    w = WORKLOADS["stage1_f32"].replace(batch=2)
+    name, over, with_bias = HOST_CASES[case]
+    w = WORKLOADS[name].replace(**over)
     q, k, v = make_inputs(w)
-    dev, _ = run_gpu(w, q, k, v)
-    cfg = lna.make_config(**{**w.config(), "in_dtype": "f32"})
+    bias = make_bias(w) if with_bias else None
+    dev, _ = run_gpu(w, q, k, v, bias=bias)
+    monkeypatch.setenv("LAPL_ATTN_HOST_SPLIT", split)
+    cfg = lna.make_config(**{**w.config(), "in_dtype": w.dtype})
     h = lna.lapl_attn_create(cfg)
-    nbytes = lna.lapl_attn_host_staging_size(h)
-    staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    hq, hk, hv = (torch.from_numpy(x).pin_memory() for x in (q, k, v))
-    hout = torch.empty(q.shape, dtype=torch.float32).pin_memory()
-    st = torch.cuda.current_stream()
-    lna.lapl_attn_forward_host(h, hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), None,
-                               hout.data_ptr(), staging.data_ptr(), nbytes, st.cuda_stream)
-    st.synchronize()
-    assert np.array_equal(hout.numpy().astype(np.float64), dev)
-    lna.lapl_attn_destroy(h)
+    try:
+        nbytes = lna.lapl_attn_host_staging_size(h)
+        staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        tq, tk, tv = (torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)) for x in (q, k, v))
+        if w.dtype == "bf16":
+            tq, tk, tv = (t.to(torch.bfloat16) for t in (tq, tk, tv))
+        hq, hk, hv = (t.pin_memory() for t in (tq, tk, tv))
+        hb = torch.from_numpy(np.ascontiguousarray(bias, dtype=np.float32)).pin_memory() \
+            if with_bias else None
+        hout = torch.full(q.shape, float("nan"), dtype=torch.float32).pin_memory()
+        st = torch.cuda.current_stream()
+        lna.lapl_attn_forward_host(h, hq.data_ptr(), hk.data_ptr(), hv.data_ptr(),
+                                   hb.data_ptr() if hb is not None else None, hout.data_ptr(),
+                                   staging.data_ptr(), nbytes, st.cuda_stream)
+        st.synchronize()
+        assert np.array_equal(hout.numpy().astype(np.float64), dev)
+        assert lna.lapl_attn_device_errors(h, st.cuda_stream) == 0
+    finally:
+        lna.lapl_attn_destroy(h)
