@@ -204,7 +204,10 @@ cg_kernel(const float* __restrict__ landmarks, const float* __restrict__ bvp,
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         live[c] = live[c] && pq[c] > 0.f;
-        const float alpha = live[c] ? rr[c] / pq[c] : 0.f;
+        // alpha and beta by the fast division (within 2 ulp): the dot products they divide
+        // carry about n u of rounding already, and an IEEE division costs hundreds of cycles
+        // on this chain.
+        const float alpha = live[c] ? __fdividef(rr[c], pq[c]) : 0.f;
         rn[c] = 0.f;
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
@@ -219,7 +222,7 @@ cg_kernel(const float* __restrict__ landmarks, const float* __restrict__ bvp,
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         if (live[c]) {
-          const float beta = rn[c] / rr[c];
+          const float beta = __fdividef(rn[c], rr[c]);
           rr[c] = rn[c];
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
