@@ -410,10 +410,11 @@ bwd_ns_kernel(const float* __restrict__ landmarks, const float* __restrict__ xs,
   __syncthreads();
   {
     const float scale = red[0], dn1 = red[1], dninf = red[2];
+    const float inv_scale = 1.f / scale;          // one division, not one per element
     const int jc = __float_as_int(red[3]), ir = __float_as_int(red[4]);
     for (int e = tid; e < M * M; e += kHeadThreads) {
       const int i = e / M, j = e % M;
-      float g = dW[i * kMS + j] + Sb[i * kMS + j] / scale;
+      float g = dW[i * kMS + j] + Sb[i * kMS + j] * inv_scale;
       const float w = Wb[i * kMS + j];
       const float sw = w > 0.f ? 1.f : (w < 0.f ? -1.f : 0.f);
       if (j == jc) g += dn1 * sw;

@@ -108,11 +108,14 @@ pool_landmarks_kernel(const void* __restrict__ kin, float* __restrict__ landmark
       for (int t = 0; t < tlw; ++t)
 #pragma unroll
         for (int c = 0; c < CH; ++c) sum[c] += part[w][t * lpt + piece0][c];
-    const float cnt = (float)(ph * pw);
+    // The mean as a product with 1 / (window size): the same value as the division when the
+    // window size is a power of two (every workload's), within an ulp otherwise, without a
+    // division per value.
+    const float inv_cnt = 1.f / (float)(ph * pw);
     const size_t o = ((size_t)bh * m + jr * s + jc) * d + piece0 * CH;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
-      const float val = sum[c] / cnt;
+      const float val = sum[c] * inv_cnt;
       landmarks[o + c] = val;
       if (dbg) dbg[o + c] = val;
     }
