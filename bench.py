@@ -187,6 +187,30 @@ def gemm_chain_roofline(w, stage_ms: dict, peaks: dict, plan: dict) -> list:
     return entries
 
 
+def dominant_kernel_entry(w, stage_ms: dict, peaks: dict, plan: dict, ms: float):
+    """The Newton-Schulz solve, the stage-1 step's largest kernel (a launch-list share of about
+    47 %): a chain of 2T dependent products, bound by latency.  Its tensor-core work (the TF32
+    high/low split as one 128 x 128 x 8 MMA per K step, ceil(m/8) steps per product, 2T
+    products per head) against the TF32 peak (the measured bf16 peak / 2), and its time per
+    step."""
+    if not plan.get("ns_tensor_core"):
+        return None
+    bh, m, T = w.batch * w.heads, w.num_landmarks, w.ns_steps
+    ksteps = (((m + 3) // 4 * 4) + 7) // 8
+    flops = 2.0 * bh * 2 * T * ksteps * 128 * 128 * 8
+    t = stage_ms["newton_schulz"] / 1e3
+    peak = float(peaks.get("bf16_tflops", 1900.0)) / 2.0
+    ach = flops / t / 1e12
+    return {"kernel": "ns_tc_kernel (W, T Newton-Schulz steps; tcgen05 TF32 high/low)",
+            "bound": "latency", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+            "frac": ach / peak, "kernel_ms": stage_ms["newton_schulz"],
+            "stage_us_per_step": stage_ms["newton_schulz"] * 1e3 / max(T, 1),
+            "share_of_forward": stage_ms["newton_schulz"] / ms,
+            "note": "2T dependent products per head; the step waits on MMA issue (about 60 "
+                    "cycles per instruction), tensor-memory reads and CTA barriers, not on a "
+                    "pipe's throughput; peak = TF32 = measured bf16 / 2"}
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -539,6 +563,7 @@ def run_ours(args, w):
                    "plan": plan},
         "roofline": roofline,
         "gemm_chain_roofline": gemm_chain_roofline(w, stage_ms, peaks, plan),
+        "dominant_kernel": dominant_kernel_entry(w, stage_ms, peaks, plan, ms),
         "stage_ms": stage_ms,
         "cpu_baseline": None,
         "e2e": e2e,

@@ -62,3 +62,19 @@ def test_gemm_chain_roofline_bytes_and_fraction():
     e = bench.gemm_chain_roofline(w, {"bv": 0.1, "output": 0.05}, {"hbm_gbs": 5000.0},
                                   {"bv_tensor_core": 0, "out_tensor_core": 1})
     assert e[0]["kernel"].startswith("bv_kernel") and e[1]["kernel"].startswith("out_tc_kernel")
+
+
+def test_dominant_kernel_entry():
+    """The solve's tensor-core work: 2 x BH x 2T products x ceil(m'/8) MMAs of 128 x 128 x 8
+    (m' = m rounded up to 4), against half the measured bf16 peak; absent without the
+    tensor-core solve."""
+    import bench
+    from lapl_workloads import WORKLOADS
+    w = WORKLOADS["stage1_f32"]
+    e = bench.dominant_kernel_entry(w, {"newton_schulz": 0.05}, {"bf16_tflops": 2000.0},
+                                    {"ns_tensor_core": 1}, 0.1)
+    flops = 2.0 * 16 * 2 * 20 * 7 * 128 * 128 * 8
+    assert abs(e["achieved"] - flops / 5e-5 / 1e12) < 1e-9
+    assert e["peak"] == 1000.0 and e["bound"] == "latency" and e["share_of_forward"] == 0.5
+    assert bench.dominant_kernel_entry(w, {"newton_schulz": 0.05}, {}, {"ns_tensor_core": 0},
+                                       0.1) is None
