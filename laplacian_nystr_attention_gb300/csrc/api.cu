@@ -268,12 +268,15 @@ lapl_status create_plan(const lapl_attn_config* cfg, lapl_attn_plan** out, int f
     if (cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
                                p->device) != cudaSuccess)
       smem_optin = 0;
+    const bool out_bf16 = cfg->out_dtype == LAPL_BF16;
+    g.out_tma = out_tc_tma_store(g.d, out_bf16) && g.bh < (1LL << 31) && g.n < (1LL << 31);
     g.out_tc = !want_cuda && g.d % 16 == 0 && 4 * g.d <= 256 && g.n % 4 == 0 &&
-               out_tc_smem_bytes(g.m, g.d) <= (size_t)smem_optin;
+               out_tc_smem_bytes(g.m, g.d, g.out_tma, out_bf16) <= (size_t)smem_optin;
+    if (!g.out_tc) g.out_tma = false;
     if (g.out_tc) {
       g.out_tile = 128;
       g.out_threads = out_tc_threads();
-      g.out_smem = out_tc_smem_bytes(g.m, g.d);
+      g.out_smem = out_tc_smem_bytes(g.m, g.d, g.out_tma, out_bf16);
       e = out_tc_configure(g.out_smem);
     } else {
       g.out_tile = output_tile_tokens(g.d, g.bh, g.n, p->num_sms);

@@ -127,6 +127,20 @@ bool tma_encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool tma_encode_3d_sw128(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
+                         uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+                         uint32_t b0, uint32_t b1) {
+  const cdist_tma::EncodeTiledFn fn = cdist_tma::encoder();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+  const cuuint64_t strides[2] = {(cuuint64_t)s1, (cuuint64_t)s2};
+  const cuuint32_t box[3] = {b0, b1, 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  return fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, elem_strides,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Error bits raised by device-side bounded waits; read and cleared by lapl_attn_device_errors.
 __device__ unsigned g_device_errors;
 

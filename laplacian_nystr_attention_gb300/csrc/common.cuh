@@ -149,6 +149,7 @@ struct Geometry {
   int stat_threads;
   int bv_raw_stages;       // tensor-core B V: raw copy stages (as many as fit, <= 12)
   bool out_tc;             // O = A^ M on the tensor cores (out_tc.cu)
+  bool out_tma;            // ... with its rows written by TMA tensor stores
   size_t fin_smem;
   size_t cd_smem;          // dynamic shared memory of the distance kernel
   int out_tile;            // tokens per output-kernel CTA
@@ -199,6 +200,9 @@ struct lapl_attn_plan {
   // Tensor maps of A^T and B^T for the tensor stores of the Gaussian tensor-core distance
   // kernel, re-encoded when the pointers change.
   mutable CUtensorMap tmap_at_st, tmap_bt_st;
+  // Tensor map of O for the tensor stores of the tensor-core output kernel.
+  mutable CUtensorMap tmap_o;
+  mutable const void* tmap_o_ptr;
   mutable const void* tmap_at_st_ptr;
   mutable const void* tmap_bt_st_ptr;
   // Fault injection for tests (lapl_attn_set_fault_injection): bound of the distance kernel's
@@ -238,6 +242,11 @@ cudaError_t launch_output(const lapl_attn_plan& p, const float* at, const float*
 bool tma_encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint64_t inner,
                    uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 
+// 3-D tensor map with 128-byte swizzle, for tensor stores: dims d0 (contiguous) x d1 x d2,
+// strides s1 and s2 bytes, boxes of b0 x b1 x 1.
+bool tma_encode_3d_sw128(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
+                         uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+                         uint32_t b0, uint32_t b1);
 // Distance kernel choice for a plan: sets geo.cd_tma, cd_tile, cd_rows, cd_threads and cd_smem,
 // opts in to the shared memory and returns the resident CTAs per SM.
 cudaError_t cdist_plan(lapl_attn_plan& p, int* ctas_per_sm);
@@ -270,8 +279,10 @@ cudaError_t bv_tc_configure(size_t smem);
 int bv_tc_occupancy(size_t smem, bool bf16);
 cudaError_t launch_bv_tc(const lapl_attn_plan& p, const float* bt, const void* v, float* bvp,
                          cudaStream_t st);
-// O = A^ M on the tensor cores (out_tc.cu).
-size_t out_tc_smem_bytes(int m, int d);
+// O = A^ M on the tensor cores (out_tc.cu); tma_store: O rows written by TMA tensor stores
+// (fp32 O with d = 32 or 64, bf16 O with d = 64: out_tc_tma_store).
+size_t out_tc_smem_bytes(int m, int d, bool tma_store, bool out_bf16);
+bool out_tc_tma_store(int d, bool out_bf16);
 int out_tc_threads();
 cudaError_t out_tc_configure(size_t smem);
 cudaError_t launch_output_tc(const lapl_attn_plan& p, const float* at, const float* mmat,

@@ -19,10 +19,17 @@
 //        layout (core matrices of 8 rows x 16 bytes, row-group stride padded to 144 bytes so
 //        that a quarter-warp's stores fall in 8 bank groups); per head they also build
 //        [M_hi; M_lo] (2d rows, K = landmarks) from M after the programmatic wait;
-//   4-7  epilogue: read the accumulator (one row per thread), add the two halves, store O;
+//   4-7  epilogue: read the accumulator (one row per thread), add the two halves, store O: for
+//        fp32 O with d = 32 or 64 and bf16 O with d = 64 each warp stages its 32 rows in shared
+//        memory (128-byte swizzle: 16-byte piece c of row t at c ^ (t % 8), conflict-free) and
+//        writes them with TMA tensor stores of a [B H, N, d] view that clip at the head's end
+//        (per-thread row stores of 16 bytes touch 32 rows per warp instruction and measured
+//        about a quarter of the kernel's time at the high-resolution shape); otherwise each
+//        thread stores its row;
 //   8    owns the tensor memory; one thread issues the MMAs.
-// Two operand stages, two accumulators (2 x 2d tensor-memory columns), two M buffers (by head
-// parity): the conversion of tile i + 1 and the stores of tile i - 1 overlap the MMAs of tile i.
+// Two operand stages and two accumulators (2 x 2d tensor-memory columns): the conversion of
+// tile i + 1 and the stores of tile i - 1 overlap the MMAs of tile i.  One M buffer: a new
+// head's M is written once the previous tile's MMAs are complete.
 // The first tile's loads and whitening run before the programmatic wait, overlapping the M
 // kernel.  Every barrier wait is bounded (one second); on a timeout the CTA sets the chain bit
 // of the device error word, waits (bounded) for its tensor-core work and frees the tensor
@@ -108,6 +115,14 @@ __device__ __forceinline__ void mma(unsigned tmem, uint64_t ad, uint64_t bd, uin
       "l"(ad), "l"(bd), "r"(id), "r"(acc)
       : "memory");
 }
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];\n\t"
+      "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<unsigned long long>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
+      : "memory");
+}
 __device__ __forceinline__ void tmem_ld16(unsigned addr, float (&v)[16]) {
   unsigned r[16];
   asm volatile(
@@ -136,8 +151,15 @@ struct OutTcArgs {
   int whiten;
 };
 
-template <bool kOutBf16>
-__global__ void __launch_bounds__(kOutTcThreads, 1) out_tc_kernel(const OutTcArgs a) {
+// Shared memory after the operand stages and the M buffer, from a 1024-byte boundary: the
+// epilogue warps' store stages, 32 rows x d values each.
+__host__ __device__ inline unsigned ostage_bytes(int d, bool bf16) {
+  return 4u * 32u * (unsigned)d * (bf16 ? 2u : 4u);
+}
+
+template <bool kOutBf16, bool kTmaStore>
+__global__ void __launch_bounds__(kOutTcThreads, 1)
+    out_tc_kernel(const OutTcArgs a, const __grid_constant__ CUtensorMap map_o) {
   extern __shared__ __align__(128) unsigned char smem_o[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = a.m, d = a.d, n = a.n;
@@ -146,8 +168,15 @@ __global__ void __launch_bounds__(kOutTcThreads, 1) out_tc_kernel(const OutTcArg
   const unsigned bbytes = b_bytes(d, mk);
   const unsigned lboB = lbo_b(2 * d);
   unsigned char* astage = smem_o;                                       // [stage][hi, lo]
-  unsigned char* bbuf = astage + kStagesO * 2 * apart;                  // [2][2d x mk]
-  const unsigned kCoefOff = kStagesO * 2 * apart + 2 * align128(bbytes);
+  unsigned char* bbuf = astage + kStagesO * 2 * apart;                  // [2d x mk]
+  unsigned kCoefOff = kStagesO * 2 * apart + align128(bbytes);
+  unsigned char* ostage = nullptr;
+  if constexpr (kTmaStore) {
+    // 1024-byte aligned (the swizzle pattern's period), by pointer arithmetic on the array.
+    const unsigned at = smem_u32(smem_o + kCoefOff);
+    ostage = smem_o + kCoefOff + ((1024u - (at & 1023u)) & 1023u);
+    kCoefOff = (unsigned)(ostage - smem_o) + ostage_bytes(d, kOutBf16);
+  }
   unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem_o + kCoefOff + 4 * 48 * 4);
   const unsigned ofull0 = smem_u32(bars), oempty0 = ofull0 + 16, afull0 = oempty0 + 16,
                  aempty0 = afull0 + 16, done_bar = aempty0 + 16;
@@ -189,7 +218,6 @@ __global__ void __launch_bounds__(kOutTcThreads, 1) out_tc_kernel(const OutTcArg
     // This warp's whitening coefficients: mean, scale, bias of its 16 landmarks.
     float* coef = reinterpret_cast<float*>(smem_o + kCoefOff) + warp * 48;
     long prev_bh = -1;
-    int hcount = -1;
     bool waited = false;
     float4 nxt[kItems][4];
     auto load_tile = [&](int i, float4 (&v)[kItems][4]) {
@@ -221,7 +249,6 @@ __global__ void __launch_bounds__(kOutTcThreads, 1) out_tc_kernel(const OutTcArg
       if (i + 1 < ntiles) load_tile(i + 1, nxt);
       const bool new_head = bh != prev_bh;
       if (new_head) {
-        ++hcount;
         // Whitening coefficients of this head for this warp's 16 landmarks (4 quads); the warp
         // alone reads them, so a warp barrier orders the refresh.
         __syncwarp();
@@ -278,12 +305,18 @@ __global__ void __launch_bounds__(kOutTcThreads, 1) out_tc_kernel(const OutTcArg
         }
       }
       if (new_head) {
-        // M of this head: needs the M kernel (programmatic predecessor) complete.
+        // M of this head: needs the M kernel (programmatic predecessor) complete, and the
+        // previous tile's MMAs (the last readers of the one M buffer) done.
         if (!waited) {
           asm volatile("griddepcontrol.wait;" ::: "memory");
           waited = true;
         }
-        unsigned char* bb = bbuf + (hcount & 1) * align128(bbytes);
+        if (i >= 1 && !__all_sync(0xffffffffu,
+                                  mbar_wait(oempty0 + 8 * ((i - 1) & 1), ((i - 1) >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        unsigned char* bb = bbuf;
         const float* mg = a.mmat + (size_t)bh * m * d;
         // [M_hi; M_lo]: row c (c < d) = column c of M_hi, row d + c = column c of M_lo;
         // items (landmark quad p, value-column quad c4).
@@ -321,6 +354,11 @@ __global__ void __launch_bounds__(kOutTcThreads, 1) out_tc_kernel(const OutTcArg
     // ---------------- epilogue ----------------
     const int ew = warp - kEpiWarp0;                   // tensor-memory lanes 32 ew ..
     const int r = 32 * ew + lane;                      // token row of the tile
+    // This warp's store stage: boxes of 32 rows x 128 bytes, 16-byte piece c of row `lane` at
+    // (c ^ (lane % 8)) * 16.
+    unsigned char* stg = kTmaStore ? ostage + ew * (ostage_bytes(d, kOutBf16) / 4) : nullptr;
+    constexpr int kElt = kOutBf16 ? 2 : 4;
+    const int boxes = d * kElt / 128;
     for (int i = 0; i < ntiles; ++i) {
       const long tile = t_begin + i;
       const long bh = tile / a.tiles_per_head;
@@ -331,13 +369,42 @@ __global__ void __launch_bounds__(kOutTcThreads, 1) out_tc_kernel(const OutTcArg
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (kTmaStore && i > 0) {
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncwarp();                                  // the last tile's stores read the stage
+      }
       const unsigned row_addr = tmem + ((unsigned)(32 * ew) << 16) + (unsigned)(b * 2 * d);
       const int tok = n0 + r;
       for (int c0 = 0; c0 < d; c0 += 16) {
         float v[16], w[16];
         tmem_ld16(row_addr + c0, v);
         tmem_ld16(row_addr + d + c0, w);
-        if (tok < n) {
+        if constexpr (kTmaStore) {
+          if constexpr (kOutBf16) {
+            uint4 pk[2];
+            unsigned* pw = reinterpret_cast<unsigned*>(pk);
+#pragma unroll
+            for (int c = 0; c < 16; c += 2) {
+              __nv_bfloat162 t2 = __floats2bfloat162_rn(v[c] + w[c], v[c + 1] + w[c + 1]);
+              pw[c / 2] = *reinterpret_cast<unsigned*>(&t2);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int gc = c0 / 8 + u;                      // 16-byte piece of the row
+              *reinterpret_cast<uint4*>(stg + (gc >> 3) * 4096 + lane * 128 +
+                                        (((gc & 7) ^ (lane & 7)) << 4)) = pk[u];
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int gc = c0 / 4 + u;
+              *reinterpret_cast<float4*>(stg + (gc >> 3) * 4096 + lane * 128 +
+                                         (((gc & 7) ^ (lane & 7)) << 4)) =
+                  make_float4(v[4 * u] + w[4 * u], v[4 * u + 1] + w[4 * u + 1],
+                              v[4 * u + 2] + w[4 * u + 2], v[4 * u + 3] + w[4 * u + 3]);
+            }
+          }
+        } else if (tok < n) {
           const size_t o = ((size_t)bh * n + tok) * d + c0;
           if constexpr (kOutBf16) {
             uint4 pk[2];
@@ -360,21 +427,24 @@ __global__ void __launch_bounds__(kOutTcThreads, 1) out_tc_kernel(const OutTcArg
         }
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      if (kTmaStore) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(aempty0 + 8 * b);
+      if (lane == 0) {
+        mbar_arrive(aempty0 + 8 * b);
+        // Rows n0 + 32 ew .. of head bh; rows past the head's end are clipped, a box wholly
+        // past it is not issued.
+        if (kTmaStore && n0 + 32 * ew < n)
+          for (int bx = 0; bx < boxes; ++bx)
+            tma_store_3d(&map_o, stg + bx * 4096, bx * (128 / kElt), n0 + 32 * ew, (int)bh);
+      }
     }
+    if (kTmaStore && lane == 0)
+      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // stores done before exit
   } else {
     // ---------------- MMA issue ----------------
     if (lane == 0) {
-      long prev_bh = -1;
-      int hcount = -1;
       const uint32_t id2 = idesc((unsigned)(2 * d)), id1 = idesc((unsigned)d);
       for (int i = 0; i < ntiles; ++i) {
-        const long bh = (t_begin + i) / a.tiles_per_head;
-        if (bh != prev_bh) {
-          ++hcount;
-          prev_bh = bh;
-        }
         const int s = i & 1, b = i & 1;
         if (!mbar_wait(ofull0 + 8 * s, (i >> 1) & 1) ||
             (i >= 2 && !mbar_wait(aempty0 + 8 * b, ((i >> 1) - 1) & 1))) {
@@ -383,7 +453,7 @@ __global__ void __launch_bounds__(kOutTcThreads, 1) out_tc_kernel(const OutTcArg
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const unsigned ahi = smem_u32(astage + s * 2 * apart), alo = ahi + apart;
-        const unsigned bb = smem_u32(bbuf + (hcount & 1) * align128(bbytes));
+        const unsigned bb = smem_u32(bbuf);
         const unsigned acc_addr = tmem + (unsigned)(b * 2 * d);
         for (int kk = 0; kk < mk / 8; ++kk) {
           const uint64_t bd = op_desc(bb + kk * 2 * lboB, lboB);
@@ -415,26 +485,32 @@ __global__ void __launch_bounds__(kOutTcThreads, 1) out_tc_kernel(const OutTcArg
 
 }  // namespace
 
-size_t out_tc_smem_bytes(int m, int d) {
+size_t out_tc_smem_bytes(int m, int d, bool tma_store, bool out_bf16) {
   const int mk = mk8(m);
-  return (size_t)kStagesO * 2 * a_part_bytes(mk) + 2 * (size_t)align128(b_bytes(d, mk)) +
-         4 * 48 * 4 + 9 * 8 + 16;
+  return (size_t)kStagesO * 2 * a_part_bytes(mk) + (size_t)align128(b_bytes(d, mk)) +
+         (tma_store ? 1024 + (size_t)ostage_bytes(d, out_bf16) : 0) + 4 * 48 * 4 + 9 * 8 + 16;
 }
+
+bool out_tc_tma_store(int d, bool out_bf16) { return out_bf16 ? d == 64 : (d == 32 || d == 64); }
 
 int out_tc_threads() { return kOutTcThreads; }
 
 cudaError_t out_tc_configure(size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(out_tc_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(out_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem);
+  const void* fs[4] = {(const void*)out_tc_kernel<false, false>, (const void*)out_tc_kernel<true, false>,
+                       (const void*)out_tc_kernel<false, true>, (const void*)out_tc_kernel<true, true>};
+  for (const void* f : fs) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_output_tc(const lapl_attn_plan& p, const float* at, const float* mmat,
                              const float* mu, const float* rstd, const float* bias, void* out,
                              cudaStream_t st) {
   const Geometry& g = p.geo;
+  const bool bf16 = p.cfg.out_dtype == LAPL_BF16;
   OutTcArgs a;
   a.at = at; a.mmat = mmat; a.mu = mu; a.rstd = rstd; a.bias = bias; a.out = out;
   a.err = p.dev_err;
@@ -442,6 +518,16 @@ cudaError_t launch_output_tc(const lapl_attn_plan& p, const float* at, const flo
   a.tiles_per_head = (g.n + kTileT - 1) / kTileT;
   a.tiles = g.bh * a.tiles_per_head;
   a.whiten = p.cfg.whiten;
+  if (g.out_tma && p.tmap_o_ptr != out) {
+    // O as [B H, N, d]: boxes of 128 bytes x 32 rows of one head, 128-byte swizzle.
+    const int elt = bf16 ? 2 : 4;
+    if (!tma_encode_3d_sw128(&p.tmap_o, out,
+                             bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                             (uint64_t)g.d, (uint64_t)g.n, (uint64_t)g.bh, (uint64_t)g.d * elt,
+                             (uint64_t)g.n * g.d * elt, (uint32_t)(128 / elt), 32))
+      return cudaErrorInvalidValue;
+    p.tmap_o_ptr = out;
+  }
   const long grid = std::min<long>(a.tiles, p.num_sms);
   // Programmatic dependent launch: the first tile's loads and whitening overlap the kernel
   // before (the M kernel, or the CG solver).
@@ -455,8 +541,12 @@ cudaError_t launch_output_tc(const lapl_attn_plan& p, const float* at, const flo
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.cfg.out_dtype == LAPL_BF16) return cudaLaunchKernelEx(&cfg, out_tc_kernel<true>, a);
-  return cudaLaunchKernelEx(&cfg, out_tc_kernel<false>, a);
+  const CUtensorMap& map = p.tmap_o;
+  if (g.out_tma)
+    return bf16 ? cudaLaunchKernelEx(&cfg, out_tc_kernel<true, true>, a, map)
+                : cudaLaunchKernelEx(&cfg, out_tc_kernel<false, true>, a, map);
+  return bf16 ? cudaLaunchKernelEx(&cfg, out_tc_kernel<true, false>, a, map)
+              : cudaLaunchKernelEx(&cfg, out_tc_kernel<false, false>, a, map);
 }
 
 }  // namespace lapl
