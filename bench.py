@@ -57,7 +57,8 @@ CDIST_TRAFFIC = {
 }
 CDIST_SOURCES = ["cdist_kernel.cuh", "cdist_tma.cuh", "cdist_l1.cuh", "cdist.cu", "cdist_d32.cu",
                  "cdist_d64.cu", "cdist_d0.cu", "cdist_tma_f32.cu", "cdist_tma_bf16.cu",
-                 "cdist_l1.cu", "cdist_gauss_d32.cu", "cdist_gauss_d64.cu", "cdist_gauss_d0.cu",
+                 "cdist_l1.cu", "cdist_l1_bf16.cu", "cdist_gauss_d32.cu", "cdist_gauss_d64.cu",
+                 "cdist_gauss_d0.cu",
                  "cdist_gauss_tc.cu", "common.cuh"]
 CDIST_KERNEL = {
     ("l1", "laplacian"): "cdist_l1_kernel (fused L1 distance + exp, query and key blocks; "

@@ -150,6 +150,7 @@ struct Geometry {
   int bv_raw_stages;       // tensor-core B V: raw copy stages (as many as fit, <= 12)
   bool out_tc;             // O = A^ M on the tensor cores (out_tc.cu)
   bool out_tma;            // ... with its rows written by TMA tensor stores
+  int out_ahead;           // ... and A^T tiles prefetched into L2 this far ahead (0: off)
   size_t fin_smem;
   size_t cd_smem;          // dynamic shared memory of the distance kernel
   int out_tile;            // tokens per output-kernel CTA
@@ -203,6 +204,9 @@ struct lapl_attn_plan {
   // Tensor map of O for the tensor stores of the tensor-core output kernel.
   mutable CUtensorMap tmap_o;
   mutable const void* tmap_o_ptr;
+  // Tensor map of A^T for the output kernel's L2 prefetches.
+  mutable CUtensorMap tmap_at_pf;
+  mutable const void* tmap_at_pf_ptr;
   mutable const void* tmap_at_st_ptr;
   mutable const void* tmap_bt_st_ptr;
   // Fault injection for tests (lapl_attn_set_fault_injection): bound of the distance kernel's

@@ -123,6 +123,13 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
       "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
       : "memory");
 }
+// A^T tile (128 tokens x m landmark rows) into L2 only; coordinates past the tensor read nothing.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<unsigned long long>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
 __device__ __forceinline__ void tmem_ld16(unsigned addr, float (&v)[16]) {
   unsigned r[16];
   asm volatile(
@@ -149,6 +156,7 @@ struct OutTcArgs {
   int tiles_per_head;
   long tiles;
   int whiten;
+  int ahead;            // A^T tiles prefetched into L2 beyond the one loaded to registers (0: off)
 };
 
 // Shared memory after the operand stages and the M buffer, from a 1024-byte boundary: the
@@ -159,7 +167,8 @@ __host__ __device__ inline unsigned ostage_bytes(int d, bool bf16) {
 
 template <bool kOutBf16, bool kTmaStore>
 __global__ void __launch_bounds__(kOutTcThreads, 1)
-    out_tc_kernel(const OutTcArgs a, const __grid_constant__ CUtensorMap map_o) {
+    out_tc_kernel(const OutTcArgs a, const __grid_constant__ CUtensorMap map_o,
+                  const __grid_constant__ CUtensorMap map_at) {
   extern __shared__ __align__(128) unsigned char smem_o[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = a.m, d = a.d, n = a.n;
@@ -236,8 +245,20 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
         }
       }
     };
+    // One thread keeps the Tensor Memory Accelerator prefetching A^T into L2 `ahead` tiles
+    // beyond the register loads: tile j is prefetched while tile j - 1 - ahead is converted
+    // (bytes in flight without registers or shared memory).
+    auto prefetch = [&](int j) {
+      if (tid == 0 && j < ntiles) {
+        const long tile = t_begin + j;
+        tma_prefetch_l2_2d(&map_at, (int)(tile % a.tiles_per_head) * kTileT,
+                           (int)(tile / a.tiles_per_head) * m);
+      }
+    };
+    for (int j = 2; j <= a.ahead; ++j) prefetch(j);
     if (ntiles > 0) load_tile(0, nxt);
     for (int i = 0; i < ntiles; ++i) {
+      if (a.ahead > 0) prefetch(i + 1 + a.ahead);
       const long tile = t_begin + i;
       const long bh = tile / a.tiles_per_head;
       const int s = i & 1;
@@ -518,6 +539,14 @@ cudaError_t launch_output_tc(const lapl_attn_plan& p, const float* at, const flo
   a.tiles_per_head = (g.n + kTileT - 1) / kTileT;
   a.tiles = g.bh * a.tiles_per_head;
   a.whiten = p.cfg.whiten;
+  a.ahead = g.out_ahead;
+  if (a.ahead > 0 && p.tmap_at_pf_ptr != at) {
+    // A^T as [B H m, N] fp32, boxes of one tile: 128 tokens x m landmark rows.
+    if (!tma_encode_2d(&p.tmap_at_pf, at, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (uint64_t)g.n,
+                       (uint64_t)g.bh * g.m, (uint64_t)g.n * 4, kTileT, (uint32_t)g.m))
+      return cudaErrorInvalidValue;
+    p.tmap_at_pf_ptr = at;
+  }
   if (g.out_tma && p.tmap_o_ptr != out) {
     // O as [B H, N, d]: boxes of 128 bytes x 32 rows of one head, 128-byte swizzle.
     const int elt = bf16 ? 2 : 4;
@@ -542,11 +571,12 @@ cudaError_t launch_output_tc(const lapl_attn_plan& p, const float* at, const flo
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const CUtensorMap& map = p.tmap_o;
+  const CUtensorMap& map_at = p.tmap_at_pf;
   if (g.out_tma)
-    return bf16 ? cudaLaunchKernelEx(&cfg, out_tc_kernel<true, true>, a, map)
-                : cudaLaunchKernelEx(&cfg, out_tc_kernel<false, true>, a, map);
-  return bf16 ? cudaLaunchKernelEx(&cfg, out_tc_kernel<true, false>, a, map)
-              : cudaLaunchKernelEx(&cfg, out_tc_kernel<false, false>, a, map);
+    return bf16 ? cudaLaunchKernelEx(&cfg, out_tc_kernel<true, true>, a, map, map_at)
+                : cudaLaunchKernelEx(&cfg, out_tc_kernel<false, true>, a, map, map_at);
+  return bf16 ? cudaLaunchKernelEx(&cfg, out_tc_kernel<true, false>, a, map, map_at)
+              : cudaLaunchKernelEx(&cfg, out_tc_kernel<false, false>, a, map, map_at);
 }
 
 }  // namespace lapl
