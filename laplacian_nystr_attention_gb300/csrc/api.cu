@@ -271,12 +271,13 @@ lapl_status create_plan(const lapl_attn_config* cfg, lapl_attn_plan** out, int f
     const bool out_bf16 = cfg->out_dtype == LAPL_BF16;
     g.out_tma = out_tc_tma_store(g.d, out_bf16) && g.bh < (1LL << 31) && g.n < (1LL << 31);
     g.out_tc = !want_cuda && g.d % 16 == 0 && 4 * g.d <= 256 && g.n % 4 == 0 &&
+               g.bh * g.m < (1LL << 31) && g.n < (1LL << 31) &&
                out_tc_smem_bytes(g.m, g.d, g.out_tma, out_bf16) <= (size_t)smem_optin;
     if (!g.out_tc) g.out_tma = false;
     if (g.out_tc) {
-      // A^T tiles prefetched into L2 beyond the converters' register loads (which run one tile
-      // ahead): LAPL_ATTN_OUT_AHEAD overrides the distance, 0 turns it off.
-      g.out_ahead = g.bh * g.m < (1LL << 31) ? 3 : 0;
+      // A^T tiles prefetched into L2 beyond the tile being copied: LAPL_ATTN_OUT_AHEAD
+      // overrides the distance, 0 turns it off.
+      g.out_ahead = 3;
       if (const char* ah = getenv("LAPL_ATTN_OUT_AHEAD"))
         g.out_ahead = std::max(0, std::min(8, atoi(ah)));
       g.out_tile = 128;

@@ -204,7 +204,7 @@ struct lapl_attn_plan {
   // Tensor map of O for the tensor stores of the tensor-core output kernel.
   mutable CUtensorMap tmap_o;
   mutable const void* tmap_o_ptr;
-  // Tensor map of A^T for the output kernel's L2 prefetches.
+  // Tensor map of A^T for the tensor-core output kernel's tile copies and L2 prefetches.
   mutable CUtensorMap tmap_at_pf;
   mutable const void* tmap_at_pf_ptr;
   mutable const void* tmap_at_st_ptr;

@@ -43,18 +43,21 @@ constexpr int kTileT = 128;
 constexpr int kStagesO = 2;
 constexpr int kEpiWarp0 = 4, kMmaWarpO = 8;
 constexpr int kOutTcThreads = 32 * 9;
-constexpr unsigned kSboO = 144;                 // padded stride between 8-row core groups
+constexpr unsigned kSboO = 144;                 // A^: padded stride between 8-row core groups
 constexpr unsigned kLboA = 16 * kSboO;          // A^ operand: 128 rows
+constexpr unsigned kSboB = 128;                 // [M_hi; M_lo]: unpadded (written once per head)
 constexpr unsigned long long kWaitNs = 1000000000ull;
 constexpr int kItems = 4;                       // landmark quads per converter thread (m <= 64)
 
 __host__ __device__ inline int mk8(int m) { return (m + 7) & ~7; }
 __host__ __device__ inline unsigned a_part_bytes(int mk) { return (unsigned)(mk / 4) * kLboA; }
-__host__ __device__ inline unsigned lbo_b(int rows) { return (unsigned)(rows / 8) * kSboO; }
+__host__ __device__ inline unsigned lbo_b(int rows) { return (unsigned)(rows / 8) * kSboB; }
 __host__ __device__ inline unsigned b_bytes(int d, int mk) {
   return (unsigned)(mk / 4) * lbo_b(2 * d);
 }
 __host__ __device__ inline unsigned align128(unsigned x) { return (x + 127u) & ~127u; }
+// The copied A^T tile: m landmark rows x 128 tokens, fp32.
+__host__ __device__ inline unsigned raw_bytes(int m) { return align128((unsigned)m * kTileT * 4); }
 
 __device__ __forceinline__ unsigned smem_u32(const void* p) {
   return static_cast<unsigned>(__cvta_generic_to_shared(p));
@@ -62,11 +65,11 @@ __device__ __forceinline__ unsigned smem_u32(const void* p) {
 __device__ __forceinline__ float tf32_rna(float x) {
   return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
-__device__ __forceinline__ uint64_t op_desc(unsigned addr, unsigned lbo) {
+__device__ __forceinline__ uint64_t op_desc(unsigned addr, unsigned lbo, unsigned sbo) {
   uint64_t d = 0;
   d |= (uint64_t)((addr >> 4) & 0x3FFFu);
   d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((kSboO >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;
   return d;
 }
@@ -79,6 +82,10 @@ __device__ __forceinline__ void mbar_init(unsigned bar, unsigned count) {
 }
 __device__ __forceinline__ void mbar_arrive(unsigned bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(unsigned bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
 }
 __device__ __forceinline__ bool mbar_test(unsigned bar, unsigned parity) {
   unsigned done;
@@ -123,7 +130,16 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
       "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
       : "memory");
 }
-// A^T tile (128 tokens x m landmark rows) into L2 only; coordinates past the tensor read nothing.
+// A^T tile (128 tokens x m landmark rows) into shared memory; tokens past N read as zero.
+__device__ __forceinline__ void tma_load_2d(unsigned dst, const CUtensorMap* map, int x, int y,
+                                            unsigned bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<unsigned long long>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// The same tile into L2 only; coordinates past the tensor read nothing.
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                    reinterpret_cast<unsigned long long>(map)),
@@ -156,14 +172,12 @@ struct OutTcArgs {
   int tiles_per_head;
   long tiles;
   int whiten;
-  int ahead;            // A^T tiles prefetched into L2 beyond the one loaded to registers (0: off)
+  int ahead;            // A^T tiles prefetched into L2 beyond the one being copied (0: off)
 };
 
-// Shared memory after the operand stages and the M buffer, from a 1024-byte boundary: the
-// epilogue warps' store stages, 32 rows x d values each.
-__host__ __device__ inline unsigned ostage_bytes(int d, bool bf16) {
-  return 4u * 32u * (unsigned)d * (bf16 ? 2u : 4u);
-}
+// Shared memory after the operand stages, the M buffer and the A^T tile, from a 1024-byte
+// boundary: the epilogue warps' store stages, one box (32 rows x 128 bytes) each.
+constexpr unsigned kOstageBytes = 4u * 32u * 128u;
 
 template <bool kOutBf16, bool kTmaStore>
 __global__ void __launch_bounds__(kOutTcThreads, 1)
@@ -178,18 +192,20 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
   const unsigned lboB = lbo_b(2 * d);
   unsigned char* astage = smem_o;                                       // [stage][hi, lo]
   unsigned char* bbuf = astage + kStagesO * 2 * apart;                  // [2d x mk]
-  unsigned kCoefOff = kStagesO * 2 * apart + align128(bbytes);
+  unsigned char* raw = bbuf + align128(bbytes);                         // A^T tile [m][128]
+  unsigned kCoefOff = kStagesO * 2 * apart + align128(bbytes) + raw_bytes(m);
   unsigned char* ostage = nullptr;
   if constexpr (kTmaStore) {
     // 1024-byte aligned (the swizzle pattern's period), by pointer arithmetic on the array.
     const unsigned at = smem_u32(smem_o + kCoefOff);
     ostage = smem_o + kCoefOff + ((1024u - (at & 1023u)) & 1023u);
-    kCoefOff = (unsigned)(ostage - smem_o) + ostage_bytes(d, kOutBf16);
+    kCoefOff = (unsigned)(ostage - smem_o) + kOstageBytes;
   }
   unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem_o + kCoefOff + 4 * 48 * 4);
   const unsigned ofull0 = smem_u32(bars), oempty0 = ofull0 + 16, afull0 = oempty0 + 16,
-                 aempty0 = afull0 + 16, done_bar = aempty0 + 16;
-  unsigned* slot = reinterpret_cast<unsigned*>(bars + 9);
+                 aempty0 = afull0 + 16, done_bar = aempty0 + 16, rfull = done_bar + 8,
+                 rempty = rfull + 8;
+  unsigned* slot = reinterpret_cast<unsigned*>(bars + 11);
   const unsigned tmem_cols = 4 * d <= 64 ? 64u : 4 * d <= 128 ? 128u : 4 * d <= 256 ? 256u : 512u;
 
   const long t_begin = (long)blockIdx.x * a.tiles / gridDim.x;
@@ -211,6 +227,8 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
       mbar_init(aempty0 + 8 * s, 4);     // epilogue warps
     }
     mbar_init(done_bar, 1);
+    mbar_init(rfull, 1);                 // the copying thread's expect_tx arrival
+    mbar_init(rempty, 4);                // converter warps
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -218,36 +236,29 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const unsigned tmem = *slot;
   bool ok = true;
+  int copied = ntiles > 0 ? 1 : 0;     // A^T copies issued (thread 0)
 
   if (warp < 4) {
     // ---------------- converters ----------------
-    // Thread (warp w, lane q) handles token quad q of landmark quads w, w + 4, w + 8, w + 12:
-    // its 16 loads of tile i + 1 are issued before tile i is converted (two register sets).
+    // Thread (warp w, lane q) handles token quad q of landmark quads w, w + 4, w + 8, w + 12.
+    // Thread 0 copies each A^T tile with the Tensor Memory Accelerator into the one raw stage
+    // (16-byte register loads of the landmark-major rows, 32 KB per SM in flight, measured
+    // about 1600 cycles per tile just to issue); the converters move the tile to registers,
+    // free the stage (the copy of tile i + 1 starts) and convert tile i meanwhile.
     const int tid = threadIdx.x;
     // This warp's whitening coefficients: mean, scale, bias of its 16 landmarks.
     float* coef = reinterpret_cast<float*>(smem_o + kCoefOff) + warp * 48;
     long prev_bh = -1;
     bool waited = false;
-    float4 nxt[kItems][4];
-    auto load_tile = [&](int i, float4 (&v)[kItems][4]) {
-      const long tile = t_begin + i;
-      const long bh = tile / a.tiles_per_head;
-      const int tok = (int)(tile % a.tiles_per_head) * kTileT + 4 * lane;
-#pragma unroll
-      for (int it = 0; it < kItems; ++it) {
-        const int p = warp + 4 * it;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int j = 4 * p + u;
-          v[it][u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (j < m && tok < n)
-            v[it][u] = __ldcs(reinterpret_cast<const float4*>(&a.at[((size_t)bh * m + j) * n + tok]));
-        }
-      }
+    const unsigned tile_bytes = (unsigned)m * kTileT * 4;
+    auto copy_tile = [&](int j) {
+      const long tile = t_begin + j;
+      mbar_expect_tx(rfull, tile_bytes);
+      tma_load_2d(smem_u32(raw), &map_at, (int)(tile % a.tiles_per_head) * kTileT,
+                  (int)(tile / a.tiles_per_head) * m, rfull);
     };
-    // One thread keeps the Tensor Memory Accelerator prefetching A^T into L2 `ahead` tiles
-    // beyond the register loads: tile j is prefetched while tile j - 1 - ahead is converted
-    // (bytes in flight without registers or shared memory).
+    // Thread 0 also keeps the Tensor Memory Accelerator prefetching A^T into L2 `ahead` tiles
+    // beyond the copy: tile j is prefetched while tile j - 1 - ahead is converted.
     auto prefetch = [&](int j) {
       if (tid == 0 && j < ntiles) {
         const long tile = t_begin + j;
@@ -255,19 +266,43 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
                            (int)(tile / a.tiles_per_head) * m);
       }
     };
+    if (tid == 0 && ntiles > 0) copy_tile(0);
     for (int j = 2; j <= a.ahead; ++j) prefetch(j);
-    if (ntiles > 0) load_tile(0, nxt);
     for (int i = 0; i < ntiles; ++i) {
       if (a.ahead > 0) prefetch(i + 1 + a.ahead);
       const long tile = t_begin + i;
       const long bh = tile / a.tiles_per_head;
       const int s = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(rfull, i & 1))) {
+        ok = false;
+        break;
+      }
       float4 cur[kItems][4];
+      const float* rt = reinterpret_cast<const float*>(raw) + 4 * lane;
 #pragma unroll
-      for (int it = 0; it < kItems; ++it)
+      for (int it = 0; it < kItems; ++it) {
+        const int p = warp + 4 * it;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) cur[it][u] = nxt[it][u];
-      if (i + 1 < ntiles) load_tile(i + 1, nxt);
+        for (int u = 0; u < 4; ++u) {
+          const int j = 4 * p + u;
+          cur[it][u] = j < m ? *reinterpret_cast<const float4*>(rt + j * kTileT)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(rempty);
+      if (warp == 0 && i + 1 < ntiles) {
+        // The next copy overwrites the stage once all four warps hold this tile.
+        const bool freed = lane != 0 || mbar_wait(rempty, i & 1);
+        if (!__all_sync(0xffffffffu, freed)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          copied = i + 2;
+          copy_tile(i + 1);
+        }
+      }
       const bool new_head = bh != prev_bh;
       if (new_head) {
         // Whitening coefficients of this head for this warp's 16 landmarks (4 quads); the warp
@@ -360,8 +395,8 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
             const float4 hi = make_float4(tf32_rna(col.x), tf32_rna(col.y), tf32_rna(col.z),
                                           tf32_rna(col.w));
             const int row = 4 * c4 + c, lrow = d + row;
-            *reinterpret_cast<float4*>(bb + p * lboB + (row >> 3) * kSboO + (row & 7) * 16) = hi;
-            *reinterpret_cast<float4*>(bb + p * lboB + (lrow >> 3) * kSboO + (lrow & 7) * 16) =
+            *reinterpret_cast<float4*>(bb + p * lboB + (row >> 3) * kSboB + (row & 7) * 16) = hi;
+            *reinterpret_cast<float4*>(bb + p * lboB + (lrow >> 3) * kSboB + (lrow & 7) * 16) =
                 make_float4(col.x - hi.x, col.y - hi.y, col.z - hi.z, col.w - hi.w);
           }
         }
@@ -375,11 +410,10 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
     // ---------------- epilogue ----------------
     const int ew = warp - kEpiWarp0;                   // tensor-memory lanes 32 ew ..
     const int r = 32 * ew + lane;                      // token row of the tile
-    // This warp's store stage: boxes of 32 rows x 128 bytes, 16-byte piece c of row `lane` at
-    // (c ^ (lane % 8)) * 16.
-    unsigned char* stg = kTmaStore ? ostage + ew * (ostage_bytes(d, kOutBf16) / 4) : nullptr;
+    // This warp's store stage: one box of 32 rows x 128 bytes, 16-byte piece c of row `lane`
+    // at (c ^ (lane % 8)) * 16; a row of O is one or two boxes, staged and stored in turn.
+    unsigned char* stg = kTmaStore ? ostage + ew * (kOstageBytes / 4) : nullptr;
     constexpr int kElt = kOutBf16 ? 2 : 4;
-    const int boxes = d * kElt / 128;
     for (int i = 0; i < ntiles; ++i) {
       const long tile = t_begin + i;
       const long bh = tile / a.tiles_per_head;
@@ -390,17 +424,21 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      if (kTmaStore && i > 0) {
-        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-        __syncwarp();                                  // the last tile's stores read the stage
-      }
       const unsigned row_addr = tmem + ((unsigned)(32 * ew) << 16) + (unsigned)(b * 2 * d);
       const int tok = n0 + r;
+      // Rows n0 + 32 ew .. of head bh; rows past the head's end are clipped by the store, a
+      // box wholly past it is not issued.
+      const bool rows_in = n0 + 32 * ew < n;
       for (int c0 = 0; c0 < d; c0 += 16) {
         float v[16], w[16];
         tmem_ld16(row_addr + c0, v);
         tmem_ld16(row_addr + d + c0, w);
         if constexpr (kTmaStore) {
+          if ((c0 * kElt) % 128 == 0) {
+            // A new box: the stage's previous store has finished reading it.
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            __syncwarp();
+          }
           if constexpr (kOutBf16) {
             uint4 pk[2];
             unsigned* pw = reinterpret_cast<unsigned*>(pk);
@@ -412,18 +450,23 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
               const int gc = c0 / 8 + u;                      // 16-byte piece of the row
-              *reinterpret_cast<uint4*>(stg + (gc >> 3) * 4096 + lane * 128 +
-                                        (((gc & 7) ^ (lane & 7)) << 4)) = pk[u];
+              *reinterpret_cast<uint4*>(stg + lane * 128 + (((gc & 7) ^ (lane & 7)) << 4)) =
+                  pk[u];
             }
           } else {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int gc = c0 / 4 + u;
-              *reinterpret_cast<float4*>(stg + (gc >> 3) * 4096 + lane * 128 +
-                                         (((gc & 7) ^ (lane & 7)) << 4)) =
+              *reinterpret_cast<float4*>(stg + lane * 128 + (((gc & 7) ^ (lane & 7)) << 4)) =
                   make_float4(v[4 * u] + w[4 * u], v[4 * u + 1] + w[4 * u + 1],
                               v[4 * u + 2] + w[4 * u + 2], v[4 * u + 3] + w[4 * u + 3]);
             }
+          }
+          if (((c0 + 16) * kElt) % 128 == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0 && rows_in)
+              tma_store_3d(&map_o, stg, c0 + 16 - 128 / kElt, n0 + 32 * ew, (int)bh);
           }
         } else if (tok < n) {
           const size_t o = ((size_t)bh * n + tok) * d + c0;
@@ -448,16 +491,8 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
         }
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      if (kTmaStore) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(aempty0 + 8 * b);
-        // Rows n0 + 32 ew .. of head bh; rows past the head's end are clipped, a box wholly
-        // past it is not issued.
-        if (kTmaStore && n0 + 32 * ew < n)
-          for (int bx = 0; bx < boxes; ++bx)
-            tma_store_3d(&map_o, stg + bx * 4096, bx * (128 / kElt), n0 + 32 * ew, (int)bh);
-      }
+      if (lane == 0) mbar_arrive(aempty0 + 8 * b);
     }
     if (kTmaStore && lane == 0)
       asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // stores done before exit
@@ -477,9 +512,9 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
         const unsigned bb = smem_u32(bbuf);
         const unsigned acc_addr = tmem + (unsigned)(b * 2 * d);
         for (int kk = 0; kk < mk / 8; ++kk) {
-          const uint64_t bd = op_desc(bb + kk * 2 * lboB, lboB);
-          mma(acc_addr, op_desc(ahi + kk * 2 * kLboA, kLboA), bd, id2, kk > 0 ? 1u : 0u);
-          mma(acc_addr, op_desc(alo + kk * 2 * kLboA, kLboA), bd, id1, 1u);
+          const uint64_t bd = op_desc(bb + kk * 2 * lboB, lboB, kSboB);
+          mma(acc_addr, op_desc(ahi + kk * 2 * kLboA, kLboA, kSboO), bd, id2, kk > 0 ? 1u : 0u);
+          mma(acc_addr, op_desc(alo + kk * 2 * kLboA, kLboA, kSboO), bd, id1, 1u);
         }
         commit(oempty0 + 8 * s);
         commit(afull0 + 8 * b);
@@ -488,6 +523,8 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
     }
   }
 
+  // Every issued copy lands before the CTA may finish (at once unless a wait gave up).
+  if (threadIdx.x == 0 && copied > 0) mbar_wait(rfull, (copied - 1) & 1);
   ok = __syncthreads_and(ok ? 1 : 0) != 0;
   if (!ok && threadIdx.x == 0) {
     atomicOr(a.err, kErrBitChain);
@@ -508,8 +545,9 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
 
 size_t out_tc_smem_bytes(int m, int d, bool tma_store, bool out_bf16) {
   const int mk = mk8(m);
+  (void)out_bf16;
   return (size_t)kStagesO * 2 * a_part_bytes(mk) + (size_t)align128(b_bytes(d, mk)) +
-         (tma_store ? 1024 + (size_t)ostage_bytes(d, out_bf16) : 0) + 4 * 48 * 4 + 9 * 8 + 16;
+         raw_bytes(m) + (tma_store ? 1024 + (size_t)kOstageBytes : 0) + 4 * 48 * 4 + 11 * 8 + 16;
 }
 
 bool out_tc_tma_store(int d, bool out_bf16) { return out_bf16 ? d == 64 : (d == 32 || d == 64); }
@@ -540,8 +578,9 @@ cudaError_t launch_output_tc(const lapl_attn_plan& p, const float* at, const flo
   a.tiles = g.bh * a.tiles_per_head;
   a.whiten = p.cfg.whiten;
   a.ahead = g.out_ahead;
-  if (a.ahead > 0 && p.tmap_at_pf_ptr != at) {
-    // A^T as [B H m, N] fp32, boxes of one tile: 128 tokens x m landmark rows.
+  if (p.tmap_at_pf_ptr != at) {
+    // A^T as [B H m, N] fp32, boxes of one tile: 128 tokens x m landmark rows (the copies and
+    // the L2 prefetches).
     if (!tma_encode_2d(&p.tmap_at_pf, at, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (uint64_t)g.n,
                        (uint64_t)g.bh * g.m, (uint64_t)g.n * 4, kTileT, (uint32_t)g.m))
       return cudaErrorInvalidValue;
