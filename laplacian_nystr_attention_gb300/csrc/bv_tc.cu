@@ -5,11 +5,12 @@
 // O = A^ (X (B V)), evaluated right to left so that the N x N matrix is never formed (Chinese
 // explainer page, 2.2); B V is the first product, a contraction over the N tokens.
 //
-// One CTA per (batch, head, token split), 6 warps, chunks of 32 tokens:
-//   warp 4     one thread copies each chunk with the Tensor Memory Accelerator into a ring of
+// One CTA per (batch, head, token split), 10 warps, chunks of 32 tokens:
+//   warp 8     one thread copies each chunk with the Tensor Memory Accelerator into a ring of
 //              kRaw raw stages: B^T[bh] rows 0..m-1 x 32 tokens (landmark-major, as stored) and
 //              V[bh] 32 tokens x d (token-major, as stored); tokens past N read as zero.
-//   warps 0-3  converters: from a raw stage they build the two operands of one accumulation in
+//   warps 0-7  converters (two per scheduler: one warp alone left the conversion waiting on its
+//              own shared-memory latencies): from a raw stage they build the two operands of one accumulation in
 //              a ring of kOps operand stages (K-major, no swizzle, core matrices of 8 rows x 16
 //              bytes; the strides between core matrices are padded by 16 bytes so that the
 //              converters' 16-byte stores of a quarter-warp fall in 8 different bank groups):
@@ -18,8 +19,8 @@
 //                Bop = [V_hi; V_lo] rows c and d + c hold value column c (fp32 V), or V's rows
 //                                   alone (bf16 V is exact in TF32); 4 tokens x 4 columns are
 //                                   transposed in registers.
-//              After the last chunk the same warps read the accumulator back.
-//   warp 5     owns the tensor memory; one thread issues tcgen05.mma (M = 128, N = 2d or d,
+//              After the last chunk warps 0-3 read the accumulator back.
+//   warp 9     owns the tensor memory; one thread issues tcgen05.mma (M = 128, N = 2d or d,
 //              K = 8) for each 8 tokens and commits each operand stage back to the converters.
 // The column statistics of A run as a separate launch just before this one (col_stats_kernel,
 // one CTA per landmark column); this grid is its programmatic dependent, so the two overlap.
@@ -40,9 +41,9 @@ namespace {
 constexpr int kTok = 32;                    // tokens (K) per chunk
 constexpr int kRawMax = 12;                 // raw (copied) stages: as many as fit, <= 12
 constexpr int kOps = 3;                     // operand stages
-constexpr int kConvThreads = 128;           // warps 0-3
-constexpr int kTmaWarp = 4, kMmaWarp = 5;
-constexpr int kBvTcThreads = 32 * 6;
+constexpr int kConvThreads = 256;           // warps 0-7: two per scheduler
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr int kBvTcThreads = 32 * 10;
 constexpr unsigned kRawBt = 64 * kTok * 4;               // B^T part of a raw stage (m <= 64)
 constexpr unsigned kSboA = 128, kLboA = 16 * 128 + 16;   // A: 128 rows
 constexpr unsigned kOpABytes = (kTok / 4) * kLboA;       // 8 K-groups
@@ -304,7 +305,7 @@ bv_tc_kernel(const BvTcArgs a, const __grid_constant__ CUtensorMap map_bt,
       for (int i = max(0, issued - kRaw); i < issued; ++i)
         mbar_wait(rfull0 + 8 * (i % kRaw), (i / kRaw) & 1);
     }
-  } else if (warp < 4) {
+  } else if (warp < kConvThreads / 32) {
     // ---------------- converters ----------------
     const int tid = threadIdx.x;
     const int cq = d >> 2;
@@ -322,15 +323,28 @@ bv_tc_kernel(const BvTcArgs a, const __grid_constant__ CUtensorMap map_bt,
       const unsigned char* rv = raw + rs * raw_bytes + kRawBt;
       unsigned char* opa = ops + os * op_bytes;
       unsigned char* opb = opa + kOpABytes;
-      // A: (landmark j, token quad q); a quarter-warp covers one landmark row.
-      for (int e = tid; e < m * (kTok / 4); e += kConvThreads) {
-        const int j = e >> 3, q = e & 7;
-        const float4 v = *reinterpret_cast<const float4*>(&rbt[j * kTok + 4 * q]);
-        const float4 hi = make_float4(tf32_rna(v.x), tf32_rna(v.y), tf32_rna(v.z), tf32_rna(v.w));
-        const float4 lo = make_float4(v.x - hi.x, v.y - hi.y, v.z - hi.z, v.w - hi.w);
-        unsigned char* p = opa + q * kLboA + (j & 7) * 16;
-        *reinterpret_cast<float4*>(p + (j >> 3) * kSboA) = hi;
-        *reinterpret_cast<float4*>(p + ((64 + j) >> 3) * kSboA) = lo;
+      // A: (landmark j, token quad q); a quarter-warp covers one landmark row.  All of a
+      // thread's loads are issued before any is converted.
+      constexpr int kAItems = 64 * (kTok / 4) / kConvThreads;
+      float4 av[kAItems];
+#pragma unroll
+      for (int k = 0; k < kAItems; ++k) {
+        const int e = tid + k * kConvThreads, j = e >> 3, q = e & 7;
+        av[k] = j < m ? *reinterpret_cast<const float4*>(&rbt[j * kTok + 4 * q])
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < kAItems; ++k) {
+        const int e = tid + k * kConvThreads, j = e >> 3, q = e & 7;
+        if (j < m) {
+          const float4 v = av[k];
+          const float4 hi =
+              make_float4(tf32_rna(v.x), tf32_rna(v.y), tf32_rna(v.z), tf32_rna(v.w));
+          const float4 lo = make_float4(v.x - hi.x, v.y - hi.y, v.z - hi.z, v.w - hi.w);
+          unsigned char* p = opa + q * kLboA + (j & 7) * 16;
+          *reinterpret_cast<float4*>(p + (j >> 3) * kSboA) = hi;
+          *reinterpret_cast<float4*>(p + ((64 + j) >> 3) * kSboA) = lo;
+        }
       }
       // B: (token quad q, column quad c4); a quarter-warp covers consecutive column quads.
       for (int e = tid; e < (kTok / 4) * cq; e += kConvThreads) {
@@ -415,7 +429,10 @@ bv_tc_kernel(const BvTcArgs a, const __grid_constant__ CUtensorMap map_bt,
   bool done = ok && (ntiles == 0 || mbar_wait(done_bar, 0));
   done = __syncthreads_and(done ? 1 : 0) != 0;
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  float* xchg = reinterpret_cast<float*>(raw);     // [64][d]; every copy has been consumed
+  // [64][d + 4]: rows padded by 16 bytes so that the lanes' row-wise accesses spread over the
+  // banks (unpadded, every lane of a warp hit the same bank); every copy has been consumed.
+  float* xchg = reinterpret_cast<float*>(raw);
+  const int xs = d + 4;
   float* dst = a.bvp + ((size_t)bh * a.splits + sp) * m * d;
   if (done && warp < 4) {
     const int r = 32 * warp + lane;                // accumulator row = tensor-memory lane
@@ -426,7 +443,9 @@ bv_tc_kernel(const BvTcArgs a, const __grid_constant__ CUtensorMap map_bt,
         float v[16];
         tmem_ld16(row_addr + c0, v);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) xchg[(r - 64) * d + c0 + c] = v[c];
+        for (int c = 0; c < 16; c += 4)
+          *reinterpret_cast<float4*>(&xchg[(r - 64) * xs + c0 + c]) =
+              make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
       }
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -449,8 +468,8 @@ bv_tc_kernel(const BvTcArgs a, const __grid_constant__ CUtensorMap map_bt,
 #pragma unroll
           for (int c = 0; c < 16; c += 4)
             *reinterpret_cast<float4*>(&dst[(size_t)r * d + c0 + c]) = make_float4(
-                v[c] + xchg[r * d + c0 + c], v[c + 1] + xchg[r * d + c0 + c + 1],
-                v[c + 2] + xchg[r * d + c0 + c + 2], v[c + 3] + xchg[r * d + c0 + c + 3]);
+                v[c] + xchg[r * xs + c0 + c], v[c + 1] + xchg[r * xs + c0 + c + 1],
+                v[c + 2] + xchg[r * xs + c0 + c + 2], v[c + 3] + xchg[r * xs + c0 + c + 3]);
         }
       }
     }
