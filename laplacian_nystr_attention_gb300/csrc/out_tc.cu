@@ -13,20 +13,20 @@
 // so O[t][c] = D[t][c] + D[t][d + c]: the three cross products that reproduce fp32 operands to
 // about 2^-21, summed within one tensor-memory lane (no exchange between warps).
 // Warps:
-//   0-3  converters: load the A^T tile (landmark-major [m][N], 16-byte loads along tokens; the
-//        next tile's loads are in flight while this one is converted), whiten it, transpose
+//   0-7  converters (two per scheduler): take the A^T tile (landmark-major [m][N], copied into
+//        shared memory by TMA while the previous tile is converted), whiten it, transpose
 //        4 x 4 in registers and store A^_hi / A^_lo in the K-major operand
 //        layout (core matrices of 8 rows x 16 bytes, row-group stride padded to 144 bytes so
 //        that a quarter-warp's stores fall in 8 bank groups); per head they also build
 //        [M_hi; M_lo] (2d rows, K = landmarks) from M after the programmatic wait;
-//   4-7  epilogue: read the accumulator (one row per thread), add the two halves, store O: for
+//   8-11 epilogue: read the accumulator (one row per thread), add the two halves, store O: for
 //        fp32 O with d = 32 or 64 and bf16 O with d = 64 each warp stages its 32 rows in shared
 //        memory (128-byte swizzle: 16-byte piece c of row t at c ^ (t % 8), conflict-free) and
 //        writes them with TMA tensor stores of a [B H, N, d] view that clip at the head's end
 //        (per-thread row stores of 16 bytes touch 32 rows per warp instruction and measured
 //        about a quarter of the kernel's time at the high-resolution shape); otherwise each
 //        thread stores its row;
-//   8    owns the tensor memory; one thread issues the MMAs.
+//   12   owns the tensor memory; one thread issues the MMAs.
 // Two operand stages and two accumulators (2 x 2d tensor-memory columns): the conversion of
 // tile i + 1 and the stores of tile i - 1 overlap the MMAs of tile i.  One M buffer: a new
 // head's M is written once the previous tile's MMAs are complete.
@@ -41,13 +41,15 @@ namespace {
 
 constexpr int kTileT = 128;
 constexpr int kStagesO = 2;
-constexpr int kEpiWarp0 = 4, kMmaWarpO = 8;
-constexpr int kOutTcThreads = 32 * 9;
+constexpr int kConvWarps = 8;
+constexpr int kConvThreadsO = 32 * kConvWarps;
+constexpr int kEpiWarp0 = 8, kMmaWarpO = 12;
+constexpr int kOutTcThreads = 32 * 13;
 constexpr unsigned kSboO = 144;                 // A^: padded stride between 8-row core groups
 constexpr unsigned kLboA = 16 * kSboO;          // A^ operand: 128 rows
 constexpr unsigned kSboB = 128;                 // [M_hi; M_lo]: unpadded (written once per head)
 constexpr unsigned long long kWaitNs = 1000000000ull;
-constexpr int kItems = 4;                       // landmark quads per converter thread (m <= 64)
+constexpr int kItems = 16 / kConvWarps;         // landmark quads per converter thread (m <= 64)
 
 __host__ __device__ inline int mk8(int m) { return (m + 7) & ~7; }
 __host__ __device__ inline unsigned a_part_bytes(int mk) { return (unsigned)(mk / 4) * kLboA; }
@@ -221,14 +223,14 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(ofull0 + 8 * s, 4);      // converter warps
+      mbar_init(ofull0 + 8 * s, kConvWarps);
       mbar_init(oempty0 + 8 * s, 1);     // tensor-core commit
       mbar_init(afull0 + 8 * s, 1);      // tensor-core commit
       mbar_init(aempty0 + 8 * s, 4);     // epilogue warps
     }
     mbar_init(done_bar, 1);
     mbar_init(rfull, 1);                 // the copying thread's expect_tx arrival
-    mbar_init(rempty, 4);                // converter warps
+    mbar_init(rempty, kConvWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -238,16 +240,16 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
   bool ok = true;
   int copied = ntiles > 0 ? 1 : 0;     // A^T copies issued (thread 0)
 
-  if (warp < 4) {
+  if (warp < kConvWarps) {
     // ---------------- converters ----------------
-    // Thread (warp w, lane q) handles token quad q of landmark quads w, w + 4, w + 8, w + 12.
+    // Thread (warp w, lane q) handles token quad q of landmark quads w, w + 8.
     // Thread 0 copies each A^T tile with the Tensor Memory Accelerator into the one raw stage
     // (16-byte register loads of the landmark-major rows, 32 KB per SM in flight, measured
     // about 1600 cycles per tile just to issue); the converters move the tile to registers,
     // free the stage (the copy of tile i + 1 starts) and convert tile i meanwhile.
     const int tid = threadIdx.x;
-    // This warp's whitening coefficients: mean, scale, bias of its 16 landmarks.
-    float* coef = reinterpret_cast<float*>(smem_o + kCoefOff) + warp * 48;
+    // This warp's whitening coefficients: mean, scale, bias of its 4 kItems landmarks.
+    float* coef = reinterpret_cast<float*>(smem_o + kCoefOff) + warp * 12 * kItems;
     long prev_bh = -1;
     bool waited = false;
     const unsigned tile_bytes = (unsigned)m * kTileT * 4;
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
       const float* rt = reinterpret_cast<const float*>(raw) + 4 * lane;
 #pragma unroll
       for (int it = 0; it < kItems; ++it) {
-        const int p = warp + 4 * it;
+        const int p = warp + kConvWarps * it;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int j = 4 * p + u;
@@ -305,11 +307,11 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
       }
       const bool new_head = bh != prev_bh;
       if (new_head) {
-        // Whitening coefficients of this head for this warp's 16 landmarks (4 quads); the warp
-        // alone reads them, so a warp barrier orders the refresh.
+        // Whitening coefficients of this head for this warp's landmarks (kItems quads); the
+        // warp alone reads them, so a warp barrier orders the refresh.
         __syncwarp();
         if (lane < 4 * kItems) {
-          const int j = 4 * (warp + 4 * (lane >> 2)) + (lane & 3);
+          const int j = 4 * (warp + kConvWarps * (lane >> 2)) + (lane & 3);
           float mean = 0.f, sc = 1.f, b = 0.f;
           if (a.whiten && j < m) {
             const int h = (int)(bh % a.heads);
@@ -318,8 +320,8 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
             b = a.bias ? a.bias[(size_t)h * m + j] : 0.f;
           }
           coef[lane] = mean;
-          coef[16 + lane] = sc;
-          coef[32 + lane] = b;
+          coef[4 * kItems + lane] = sc;
+          coef[8 * kItems + lane] = b;
         }
         __syncwarp();
       }
@@ -332,14 +334,14 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
       unsigned char* alo = ahi + apart;
 #pragma unroll
       for (int it = 0; it < kItems; ++it) {
-        const int p = warp + 4 * it;
+        const int p = warp + kConvWarps * it;
         if (p < mk / 4) {
           float4 v[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int j = 4 * p + u;
-            const float mean = coef[4 * it + u], sc = coef[16 + 4 * it + u],
-                        b = coef[32 + 4 * it + u];
+            const float mean = coef[4 * it + u], sc = coef[4 * kItems + 4 * it + u],
+                        b = coef[8 * kItems + 4 * it + u];
             v[u] = j < m ? make_float4((cur[it][u].x - mean) * sc + b, (cur[it][u].y - mean) * sc + b,
                                        (cur[it][u].z - mean) * sc + b, (cur[it][u].w - mean) * sc + b)
                          : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -377,7 +379,7 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
         // [M_hi; M_lo]: row c (c < d) = column c of M_hi, row d + c = column c of M_lo;
         // items (landmark quad p, value-column quad c4).
         const int cq = d >> 2;
-        for (int e = tid; e < (mk / 4) * cq; e += 128) {
+        for (int e = tid; e < (mk / 4) * cq; e += kConvThreadsO) {
           const int c4 = e % cq, p = e / cq;
           float4 r[4];
 #pragma unroll
