@@ -257,13 +257,15 @@ lapl_status create_plan(const lapl_attn_config* cfg, lapl_attn_plan** out, int f
   if (e == cudaSuccess) {
     // O = A^ M on the tensor cores where the shapes allow it (d a multiple of 16 and two
     // accumulators of 2d columns in at most 256 tensor-memory columns; N a multiple of 4 for
-    // the 16-byte loads of A^T rows; the operand stages within the shared memory) and the
-    // sequence is long (N >= 4096: at the stage-1 shape the 2.6 tiles per persistent CTA do
-    // not amortise its set-up, and the CUDA-core kernel measured 12.5 against 16.4 us);
-    // LAPL_ATTN_OUT=cuda or =tc forces either.
+    // the A^T rows' tensor map; the operand stages within the shared memory) and where it
+    // measured faster: at d = 64 for every sequence length (stage-2/3 shape, N = 784 and 128
+    // heads: output 26.6 -> 19.5 us; N = 1024 and 4096 sweeps equal or faster), for smaller d
+    // from N = 4096 (stage-1 shape, d = 32 and 2.6 tiles per persistent CTA: 14.3 against
+    // 12.5 us for the CUDA-core kernel).  LAPL_ATTN_OUT=cuda or =tc forces either.
     const char* ok_env = getenv("LAPL_ATTN_OUT");
     const bool want_tc = ok_env && strcmp(ok_env, "tc") == 0;
-    const bool want_cuda = (ok_env && strcmp(ok_env, "cuda") == 0) || (!want_tc && g.n < 4096);
+    const bool want_cuda = (ok_env && strcmp(ok_env, "cuda") == 0) ||
+                           (!want_tc && g.d < 64 && g.n < 4096);
     int smem_optin = 0;
     if (cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
                                p->device) != cudaSuccess)
@@ -306,13 +308,15 @@ lapl_status create_plan(const lapl_attn_config* cfg, lapl_attn_plan** out, int f
     const char* bvk = getenv("LAPL_ATTN_BV");
     // The B^T tensor map needs rows of 16-byte multiples (N % 4 == 0); its boxes are m <= 64
     // rows and the M kernel's reduction order is unchanged.
-    // Automatic choice: N >= 4096.  Shorter sequences give each CTA a few dozen 32-token
-    // chunks, too few to amortise the pipeline's start-up; there the CUDA-core kernel measured
-    // faster (stage-1 shape 16.4 vs 20.5 us) or equal.  LAPL_ATTN_BV=tc forces it.
+    // Automatic choice, as measured: d = 64 at every sequence length (stage-2/3 shape, N =
+    // 784 and 128 heads: B V stage 69.8 -> 63.5 us; N = 4096 sweeps 20.5 -> 16.4 us; N = 1024
+    // equal), smaller d from N = 4096 (stage-1 shape, d = 32 fp32: the CUDA-core kernel 16.4
+    // against 19.7 us).  LAPL_ATTN_BV=tc or =cuda forces either.
     const bool want_tc = bvk && strcmp(bvk, "tc") == 0;
     const bool want_cuda = bvk && strcmp(bvk, "cuda") == 0;
     g.bv_tc = g.d % 16 == 0 && nb <= 256 && g.n % 4 == 0 && g.bh * g.n < (1LL << 31) &&
-              g.bh * g.m < (1LL << 31) && !want_cuda && (want_tc || g.n >= 4096);
+              g.bh * g.m < (1LL << 31) && !want_cuda &&
+              (want_tc || g.d >= 64 || g.n >= 4096);
     int smem_optin = 0;
     if (g.bv_tc) {
       if (cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,

@@ -1,7 +1,8 @@
 """B V on the tensor cores (bv_tc.cu) against the oracle.
 
-The kernel runs by default for sequences of at least 4096 tokens (covered end to end by the
-every-slice workload tests); LAPL_ATTN_BV=tc forces it here on short, ragged and edge shapes.
+The kernel runs by default for d = 64 and, for smaller head dims, for sequences of at least
+4096 tokens (covered end to end by the every-slice workload tests); LAPL_ATTN_BV=tc forces it
+here on short, ragged and edge shapes.
 B V itself is compared with the oracle's intermediate: the TF32 high/low split leaves out only
 the product of the two low parts (2^-20 relative), so the bar is 1e-5 of the largest entry.
 """
@@ -76,8 +77,8 @@ def test_bv_tensor_core_with_bias_and_cg(monkeypatch):
 
 
 def test_bv_choice(monkeypatch):
-    """Automatic: tensor cores from 4096 tokens; never for N not a multiple of 4 or d not a
-    multiple of 16; LAPL_ATTN_BV=cuda turns it off."""
+    """Automatic: tensor cores for d = 64, for smaller d from 4096 tokens; never for N not a
+    multiple of 4 or d not a multiple of 16; LAPL_ATTN_BV=cuda turns it off."""
     import laplacian_nystr_attention_gb300 as lna
 
     def choice(w):
@@ -90,7 +91,8 @@ def test_bv_choice(monkeypatch):
     monkeypatch.delenv("LAPL_ATTN_BV", raising=False)
     assert choice(WORKLOADS["hires_bf16"]) == 1
     assert choice(WORKLOADS["sweep_f32_4096"]) == 1
-    assert choice(WORKLOADS["stage1_f32"]) == 0
+    assert choice(WORKLOADS["stage1_f32"]) == 0                               # d = 32
+    assert choice(WORKLOADS["stage23_bf16"]) == 1                             # d = 64
     monkeypatch.setenv("LAPL_ATTN_BV", "tc")
     assert choice(TINY) == 1
     assert choice(TINY.replace(grid_h=3, grid_w=43, num_landmarks=1)) == 0    # N = 129

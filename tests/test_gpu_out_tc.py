@@ -1,7 +1,8 @@
 """O = A^ M on the tensor cores (out_tc.cu) against the oracle and the CUDA-core kernel.
 
-The kernel is the default for N >= 4096 wherever its shapes allow (d a multiple of 16 and at
-most 64, N a multiple of 4); LAPL_ATTN_OUT=tc / =cuda force either.  It whitens A on the way into the
+The kernel is the default wherever its shapes allow (d a multiple of 16 and at most 64, N a
+multiple of 4) for d = 64, and for smaller d from N = 4096; LAPL_ATTN_OUT=tc / =cuda force
+either.  It whitens A on the way into the
 operand and splits operands into TF32 high/low pairs (three cross products, about 2^-21
 relative), so O agrees with the CUDA-core kernel to rounding and with the oracle within the
 usual bars.
@@ -85,7 +86,8 @@ def test_out_choice(monkeypatch):
             lna.lapl_attn_destroy(h)
 
     monkeypatch.delenv("LAPL_ATTN_OUT", raising=False)
-    assert choice(WORKLOADS["stage1_f32"]) == 0                               # N < 4096
+    assert choice(WORKLOADS["stage1_f32"]) == 0                               # d 32, N < 4096
+    assert choice(WORKLOADS["stage23_bf16"]) == 1                             # d = 64
     assert choice(WORKLOADS["hires_bf16"]) == 1
     assert choice(WORKLOADS["sweep_f32_4096"]) == 1
     monkeypatch.setenv("LAPL_ATTN_OUT", "tc")
