@@ -227,13 +227,19 @@ lapl_status lapl_attn_device_errors(lapl_attn_handle h, void* stream, unsigned* 
 
 /*
  * Fault injection, for testing the failure report above without faulting the GPU (the pages
- * have no counterpart).  wait_ns: the bound of every barrier wait of this plan's distance kernel
- * (0 restores the default of one second).  skip_last_copy = 1: the distance kernel's producer
- * never issues the copy of each CTA's last chunk, so the waits on that chunk run out after
- * wait_ns; nothing else is outstanding when they do.  Applies to the split-pipe distance kernel
- * (plan_info cdist_tma = 2; its producer skips the copy) and the Gaussian tensor-core kernel
- * (cdist_tma = 3; its converter warps never publish the chunk), to forwards launched after the
- * call.  0 = normal operation.
+ * have no counterpart).  wait_ns: the bound of every barrier wait of this plan's distance
+ * kernel and tensor-core B V and output kernels (0 restores the default of one second).
+ * skip_last_copy names the kernel that never issues the copy of each CTA's last chunk or tile,
+ * so that the waits on it run out after wait_ns with nothing else outstanding:
+ *   1  the distance kernel: the split-pipe kernel (plan_info cdist_tma = 2; its producer skips
+ *      the copy) or the Gaussian tensor-core kernel (cdist_tma = 3; its converter warps never
+ *      publish the chunk); reported as bit 1;
+ *   2  the tensor-core output kernel (out_tensor_core = 1; its copying thread skips the last
+ *      A^T tile); reported as bit 4;
+ *   3  the tensor-core B V kernel (bv_tensor_core = 1; its copy warp skips the last tile);
+ *      reported as bit 4.
+ * Applies to forwards launched after the call.  0 = normal operation; other values return
+ * LAPL_ERR_INVALID_ARG.
  */
 lapl_status lapl_attn_set_fault_injection(lapl_attn_handle h, unsigned long long wait_ns,
                                           int skip_last_copy);

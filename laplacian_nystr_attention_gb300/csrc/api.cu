@@ -884,7 +884,7 @@ lapl_status lapl_attn_device_errors(lapl_attn_handle h, void* stream, unsigned* 
 
 lapl_status lapl_attn_set_fault_injection(lapl_attn_handle h, unsigned long long wait_ns,
                                           int skip_last_copy) {
-  if (!h || (skip_last_copy != 0 && skip_last_copy != 1)) return LAPL_ERR_INVALID_ARG;
+  if (!h || skip_last_copy < 0 || skip_last_copy > 3) return LAPL_ERR_INVALID_ARG;
   h->cd_wait_ns = wait_ns ? wait_ns : 1000000000ull;
   h->cd_skip_last_copy = skip_last_copy;
   for (int i = 0; i < 2; ++i)

@@ -48,7 +48,6 @@ constexpr unsigned kRawBt = 64 * kTok * 4;               // B^T part of a raw st
 constexpr unsigned kSboA = 128, kLboA = 16 * 128 + 16;   // A: 128 rows
 constexpr unsigned kOpABytes = (kTok / 4) * kLboA;       // 8 K-groups
 constexpr unsigned kSboB = 144;                          // B: padded row-group stride
-constexpr unsigned long long kWaitNs = 1000000000ull;
 
 __host__ __device__ constexpr unsigned align128(unsigned x) { return (x + 127u) & ~127u; }
 __host__ __device__ inline unsigned raw_v_bytes(int d, bool bf16) {
@@ -106,11 +105,13 @@ __device__ __forceinline__ unsigned long long global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-__device__ __forceinline__ bool mbar_wait(unsigned bar, unsigned parity) {
+// Bounded wait: gives up after `bound` ns of %globaltimer.
+__device__ __forceinline__ bool mbar_wait(unsigned bar, unsigned parity,
+                                          unsigned long long bound) {
   if (mbar_test(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (!mbar_test(bar, parity))
-    if (global_ns() - t0 > kWaitNs) return false;
+    if (global_ns() - t0 > bound) return false;
   return true;
 }
 __device__ __forceinline__ void tma_load_2d(unsigned dst, const CUtensorMap* map, int x, int y,
@@ -220,6 +221,8 @@ struct BvTcArgs {
   int m, d, n;
   int tiles_per_split, splits;
   int nraw;             // raw stages (<= kRawMax)
+  unsigned long long wait_ns;   // bound of every barrier wait
+  int skip_last;        // fault injection: the copy warp never copies a CTA's last tile
 };
 
 template <bool kBf16>
@@ -290,10 +293,11 @@ bv_tc_kernel(const BvTcArgs a, const __grid_constant__ CUtensorMap map_bt,
       int issued = 0;
       for (int i = 0; i < ntiles; ++i) {
         const int s = i % kRaw;
-        if (i >= kRaw && !mbar_wait(rempty0 + 8 * s, ((i / kRaw) - 1) & 1)) {
+        if (i >= kRaw && !mbar_wait(rempty0 + 8 * s, ((i / kRaw) - 1) & 1, a.wait_ns)) {
           ok = false;
           break;
         }
+        if (a.skip_last && i == ntiles - 1) break;   // fault injection: never copied
         const int n0 = (t_begin + i) * kTok;
         const unsigned dst = smem_u32(raw + s * raw_bytes);
         mbar_expect_tx(rfull0 + 8 * s, bytes);
@@ -303,7 +307,7 @@ bv_tc_kernel(const BvTcArgs a, const __grid_constant__ CUtensorMap map_bt,
       }
       // Every issued copy lands before the CTA may finish.
       for (int i = max(0, issued - kRaw); i < issued; ++i)
-        mbar_wait(rfull0 + 8 * (i % kRaw), (i / kRaw) & 1);
+        mbar_wait(rfull0 + 8 * (i % kRaw), (i / kRaw) & 1, a.wait_ns);
     }
   } else if (warp < kConvThreads / 32) {
     // ---------------- converters ----------------
@@ -311,8 +315,8 @@ bv_tc_kernel(const BvTcArgs a, const __grid_constant__ CUtensorMap map_bt,
     const int cq = d >> 2;
     for (int i = 0; i < ntiles; ++i) {
       const int rs = i % kRaw, os = i % kOps;
-      bool w = mbar_wait(rfull0 + 8 * rs, (i / kRaw) & 1);
-      if (w && i >= kOps) w = mbar_wait(oempty0 + 8 * os, ((i / kOps) - 1) & 1);
+      bool w = mbar_wait(rfull0 + 8 * rs, (i / kRaw) & 1, a.wait_ns);
+      if (w && i >= kOps) w = mbar_wait(oempty0 + 8 * os, ((i / kOps) - 1) & 1, a.wait_ns);
       // The whole warp takes the same branch (a lane-by-lane exit would strand the others at
       // the warp barrier below).
       if (!__all_sync(0xffffffffu, w)) {
@@ -393,7 +397,7 @@ bv_tc_kernel(const BvTcArgs a, const __grid_constant__ CUtensorMap map_bt,
       const uint32_t id = idesc((unsigned)nb);
       for (int i = 0; i < ntiles; ++i) {
         const int os = i % kOps;
-        if (!mbar_wait(ofull0 + 8 * os, (i / kOps) & 1)) {
+        if (!mbar_wait(ofull0 + 8 * os, (i / kOps) & 1, a.wait_ns)) {
           ok = false;
           break;
         }
@@ -426,7 +430,7 @@ bv_tc_kernel(const BvTcArgs a, const __grid_constant__ CUtensorMap map_bt,
   // ---------------- accumulator -> partial B V ----------------
   // Agree on failures first: a timed-out copy, converter or issuer leaves `done` unreached.
   ok = __syncthreads_and(ok ? 1 : 0) != 0;
-  bool done = ok && (ntiles == 0 || mbar_wait(done_bar, 0));
+  bool done = ok && (ntiles == 0 || mbar_wait(done_bar, 0, a.wait_ns));
   done = __syncthreads_and(done ? 1 : 0) != 0;
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   // [64][d + 4]: rows padded by 16 bytes so that the lanes' row-wise accesses spread over the
@@ -476,7 +480,7 @@ bv_tc_kernel(const BvTcArgs a, const __grid_constant__ CUtensorMap map_bt,
   } else if (!done && threadIdx.x == 0) {
     atomicOr(a.err, kErrBitChain);
     // Wait (bounded) for whatever the tensor core may still be doing before the memory goes.
-    mbar_wait(done_bar, 0);
+    mbar_wait(done_bar, 0, a.wait_ns);
   }
   // Launched as a programmatic dependent of the column-statistics kernel, which it does not
   // read: this grid completes only after that one has, so whatever waits for B V also finds
@@ -566,6 +570,8 @@ cudaError_t launch_bv_tc(const lapl_attn_plan& p, const float* bt, const void* v
   a.m = g.m; a.d = g.d; a.n = g.n;
   a.tiles_per_split = g.bv_tiles_per_split; a.splits = g.bv_splits;
   a.nraw = g.bv_raw_stages;
+  a.wait_ns = p.cd_wait_ns;
+  a.skip_last = p.cd_skip_last_copy == 3 ? 1 : 0;
   const void* f = bf16 ? reinterpret_cast<const void*>(&bv_tc_kernel<true>)
                        : reinterpret_cast<const void*>(&bv_tc_kernel<false>);
   void* args[] = {&a, &p.tmap_bt, &p.tmap_v};

@@ -272,7 +272,7 @@ cudaError_t launch_cdist(const lapl_attn_plan& p, const void* q, const void* k, 
       a.n = g.n;
       a.c_exp = p.neg_log2e_over_lambda;
       a.wait_ns = p.cd_wait_ns;
-      a.skip_last_copy = p.cd_skip_last_copy;
+      a.skip_last_copy = p.cd_skip_last_copy == 1 ? 1 : 0;
       const void* f = cdist_l1::kernel(g.s, g.d, g.cd_groups, bf16);
       if (!f) return cudaErrorInvalidValue;
       void* args[] = {&a, &p.tmap_q, &p.tmap_k};

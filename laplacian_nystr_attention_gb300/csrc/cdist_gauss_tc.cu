@@ -569,7 +569,7 @@ cudaError_t launch_gauss_tc(const lapl_attn_plan& p, const void* q, const void* 
   a.n = g.n; a.m = g.m; a.np = np16(g.m);
   a.c_exp = p.neg_log2e_over_lambda;
   a.wait_ns = p.cd_wait_ns;
-  a.skip_last = p.cd_skip_last_copy;
+  a.skip_last = p.cd_skip_last_copy == 1 ? 1 : 0;
   // Tensor stores of [m x 32] boxes of A^T and B^T, viewed as [BH m rows, N columns]; rows of
   // N fp32 must be a multiple of 16 bytes.  Otherwise plain stores.
   a.tma_store = g.n % 4 == 0 && (long long)g.bh * g.m < (1LL << 31);

@@ -209,8 +209,10 @@ struct lapl_attn_plan {
   mutable const void* tmap_at_pf_ptr;
   mutable const void* tmap_at_st_ptr;
   mutable const void* tmap_bt_st_ptr;
-  // Fault injection for tests (lapl_attn_set_fault_injection): bound of the distance kernel's
-  // barrier waits, and whether its producer skips each CTA's last copy.
+  // Fault injection for tests (lapl_attn_set_fault_injection): bound of the barrier waits of
+  // the distance kernels and the tensor-core chain kernels, and which kernel skips each CTA's
+  // last copy (0 none, 1 the distance kernel, 2 the tensor-core output kernel, 3 the
+  // tensor-core B V kernel).
   unsigned long long cd_wait_ns;
   int cd_skip_last_copy;
   // lapl_attn_forward_host: two half-batch plans (first ceil(B/2), then floor(B/2) batches; null

@@ -48,7 +48,6 @@ constexpr int kOutTcThreads = 32 * 13;
 constexpr unsigned kSboO = 144;                 // A^: padded stride between 8-row core groups
 constexpr unsigned kLboA = 16 * kSboO;          // A^ operand: 128 rows
 constexpr unsigned kSboB = 128;                 // [M_hi; M_lo]: unpadded (written once per head)
-constexpr unsigned long long kWaitNs = 1000000000ull;
 constexpr int kItems = 16 / kConvWarps;         // landmark quads per converter thread (m <= 64)
 
 __host__ __device__ inline int mk8(int m) { return (m + 7) & ~7; }
@@ -104,11 +103,13 @@ __device__ __forceinline__ unsigned long long global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-__device__ __forceinline__ bool mbar_wait(unsigned bar, unsigned parity) {
+// Bounded wait: gives up after `bound` ns of %globaltimer.
+__device__ __forceinline__ bool mbar_wait(unsigned bar, unsigned parity,
+                                          unsigned long long bound) {
   if (mbar_test(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (!mbar_test(bar, parity))
-    if (global_ns() - t0 > kWaitNs) return false;
+    if (global_ns() - t0 > bound) return false;
   return true;
 }
 __device__ __forceinline__ void commit(unsigned bar) {
@@ -175,6 +176,8 @@ struct OutTcArgs {
   long tiles;
   int whiten;
   int ahead;            // A^T tiles prefetched into L2 beyond the one being copied (0: off)
+  unsigned long long wait_ns;   // bound of every barrier wait
+  int skip_last;        // fault injection: thread 0 never copies a CTA's last A^T tile
 };
 
 // Shared memory after the operand stages, the M buffer and the A^T tile, from a 1024-byte
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const unsigned tmem = *slot;
   bool ok = true;
-  int copied = ntiles > 0 ? 1 : 0;     // A^T copies issued (thread 0)
+  int copied = 0;                      // A^T copies issued (thread 0)
 
   if (warp < kConvWarps) {
     // ---------------- converters ----------------
@@ -268,14 +271,19 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
                            (int)(tile / a.tiles_per_head) * m);
       }
     };
-    if (tid == 0 && ntiles > 0) copy_tile(0);
+    // Fault injection: a CTA's last tile is never copied, so the waits on it run out.
+    const bool skip_last = a.skip_last != 0;
+    if (tid == 0 && ntiles > 0 && !(skip_last && ntiles == 1)) {
+      copy_tile(0);
+      copied = 1;
+    }
     for (int j = 2; j <= a.ahead; ++j) prefetch(j);
     for (int i = 0; i < ntiles; ++i) {
       if (a.ahead > 0) prefetch(i + 1 + a.ahead);
       const long tile = t_begin + i;
       const long bh = tile / a.tiles_per_head;
       const int s = i & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(rfull, i & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(rfull, i & 1, a.wait_ns))) {
         ok = false;
         break;
       }
@@ -294,13 +302,13 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(rempty);
       if (warp == 0 && i + 1 < ntiles) {
-        // The next copy overwrites the stage once all four warps hold this tile.
-        const bool freed = lane != 0 || mbar_wait(rempty, i & 1);
+        // The next copy overwrites the stage once every converter warp holds this tile.
+        const bool freed = lane != 0 || mbar_wait(rempty, i & 1, a.wait_ns);
         if (!__all_sync(0xffffffffu, freed)) {
           ok = false;
           break;
         }
-        if (lane == 0) {
+        if (lane == 0 && !(skip_last && i + 1 == ntiles - 1)) {
           copied = i + 2;
           copy_tile(i + 1);
         }
@@ -326,7 +334,7 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
         __syncwarp();
       }
       if (i >= kStagesO &&
-          !__all_sync(0xffffffffu, mbar_wait(oempty0 + 8 * s, ((i >> 1) - 1) & 1))) {
+          !__all_sync(0xffffffffu, mbar_wait(oempty0 + 8 * s, ((i >> 1) - 1) & 1, a.wait_ns))) {
         ok = false;
         break;
       }
@@ -370,7 +378,7 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
           waited = true;
         }
         if (i >= 1 && !__all_sync(0xffffffffu,
-                                  mbar_wait(oempty0 + 8 * ((i - 1) & 1), ((i - 1) >> 1) & 1))) {
+                                  mbar_wait(oempty0 + 8 * ((i - 1) & 1), ((i - 1) >> 1) & 1, a.wait_ns))) {
           ok = false;
           break;
         }
@@ -421,7 +429,7 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
       const long bh = tile / a.tiles_per_head;
       const int n0 = (int)(tile % a.tiles_per_head) * kTileT;
       const int b = i & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(afull0 + 8 * b, (i >> 1) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(afull0 + 8 * b, (i >> 1) & 1, a.wait_ns))) {
         ok = false;
         break;
       }
@@ -504,8 +512,8 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
       const uint32_t id2 = idesc((unsigned)(2 * d)), id1 = idesc((unsigned)d);
       for (int i = 0; i < ntiles; ++i) {
         const int s = i & 1, b = i & 1;
-        if (!mbar_wait(ofull0 + 8 * s, (i >> 1) & 1) ||
-            (i >= 2 && !mbar_wait(aempty0 + 8 * b, ((i >> 1) - 1) & 1))) {
+        if (!mbar_wait(ofull0 + 8 * s, (i >> 1) & 1, a.wait_ns) ||
+            (i >= 2 && !mbar_wait(aempty0 + 8 * b, ((i >> 1) - 1) & 1, a.wait_ns))) {
           ok = false;
           break;
         }
@@ -526,13 +534,13 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
   }
 
   // Every issued copy lands before the CTA may finish (at once unless a wait gave up).
-  if (threadIdx.x == 0 && copied > 0) mbar_wait(rfull, (copied - 1) & 1);
+  if (threadIdx.x == 0 && copied > 0) mbar_wait(rfull, (copied - 1) & 1, a.wait_ns);
   ok = __syncthreads_and(ok ? 1 : 0) != 0;
   if (!ok && threadIdx.x == 0) {
     atomicOr(a.err, kErrBitChain);
-    mbar_wait(done_bar, 0);          // let issued tensor-core work drain (bounded)
+    mbar_wait(done_bar, 0, a.wait_ns);   // let issued tensor-core work drain (bounded)
   }
-  if (ok && threadIdx.x == 0) mbar_wait(done_bar, 0);
+  if (ok && threadIdx.x == 0) mbar_wait(done_bar, 0, a.wait_ns);
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == kMmaWarpO) {
@@ -580,6 +588,8 @@ cudaError_t launch_output_tc(const lapl_attn_plan& p, const float* at, const flo
   a.tiles = g.bh * a.tiles_per_head;
   a.whiten = p.cfg.whiten;
   a.ahead = g.out_ahead;
+  a.wait_ns = p.cd_wait_ns;
+  a.skip_last = p.cd_skip_last_copy == 2 ? 1 : 0;
   if (p.tmap_at_pf_ptr != at) {
     // A^T as [B H m, N] fp32, boxes of one tile: 128 tokens x m landmark rows (the copies and
     // the L2 prefetches).
