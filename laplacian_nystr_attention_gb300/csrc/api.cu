@@ -427,15 +427,36 @@ lapl_status create_plan(const lapl_attn_config* cfg, lapl_attn_plan** out, int f
   w.bv = take(g.cg ? 0 : bh * m * d);
   w.total = off;
 
+  // The column statistics (an HBM-bound read of A^T that only the output kernel needs) run on
+  // a stream of their own beside the tensor-core B V, whose converters leave HBM bandwidth to
+  // spare, when the distance chain is on the launching stream and B V takes more than one
+  // wave of CTAs; otherwise they precede B V on its stream.  Measured both ways: the
+  // high-resolution shape (B V in two waves) 527.7 -> 513.5 us per forward; one-wave shapes
+  // lose 1-6 us (the N = 65536 sweeps, the stage-2/3 shape), the statistics CTAs taking issue
+  // slots from B V's converters for its whole duration.  LAPL_ATTN_STATS_BESIDE=1 / =0 forces
+  // either.
+  {
+    const char* sb = getenv("LAPL_ATTN_STATS_BESIDE");
+    const bool can = g.bv_tc && g.stat_ctas > 0 && !g.ns_exclusive && !g.cg;
+    const bool auto_on = g.bh * g.bv_splits > (long long)p->num_sms;
+    g.stats_beside = can && (sb ? strcmp(sb, "1") == 0 : auto_on);
+  }
+
   // The side stream runs the shorter of the two chains (see the launch sequence).
   e = cudaStreamCreateWithFlags(&p->side_stream, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_pool, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->stat_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_cdist, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_stats, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     set_error(p, e, "create/stream");
     if (p->side_stream) cudaStreamDestroy(p->side_stream);
     if (p->ev_join) cudaEventDestroy(p->ev_join);
     if (p->ev_pool) cudaEventDestroy(p->ev_pool);
+    if (p->stat_stream) cudaStreamDestroy(p->stat_stream);
+    if (p->ev_cdist) cudaEventDestroy(p->ev_cdist);
+    if (p->ev_stats) cudaEventDestroy(p->ev_stats);
     delete p;
     return LAPL_ERR_CUDA;
   }
@@ -563,7 +584,19 @@ static lapl_status run_forward(lapl_attn_handle p, const void* q, const void* k,
     LAPL_TRY(launch_cdist(*p, q, k, v, L, At, Bt, D.d_ql, D.d_lk, D.a, st),
              "forward/cdist");
     LAPL_MARK(kMarkCdistDone, st);
-    LAPL_TRY(launch_bv(*p, Bt, v, bvp, At, mu, rstd, D.mu, D.rstd, st), "forward/bv");
+    if (p->geo.stats_beside) {
+      // B V is launched first, so that its CTAs (one per SM, most of the shared memory) are
+      // placed before the statistics CTAs take the remaining thread slots.
+      LAPL_TRY(cudaEventRecord(p->ev_cdist, st), "forward/distances");
+      LAPL_TRY(launch_bv_tc(*p, Bt, v, bvp, st, false), "forward/bv");
+      LAPL_TRY(cudaStreamWaitEvent(p->stat_stream, p->ev_cdist, 0), "forward/distances-wait");
+      LAPL_TRY(launch_col_stats(*p, At, mu, rstd, D.mu, D.rstd, p->stat_stream),
+               "forward/statistics");
+      LAPL_TRY(cudaEventRecord(p->ev_stats, p->stat_stream), "forward/statistics-done");
+      LAPL_TRY(cudaStreamWaitEvent(st, p->ev_stats, 0), "forward/statistics-wait");
+    } else {
+      LAPL_TRY(launch_bv(*p, Bt, v, bvp, At, mu, rstd, D.mu, D.rstd, st), "forward/bv");
+    }
     LAPL_MARK(kMarkBvDone, st);
   }
   LAPL_TRY(cudaStreamWaitEvent(st, p->ev_join, 0), "forward/join-wait");
@@ -918,6 +951,9 @@ lapl_status lapl_attn_destroy(lapl_attn_handle h) {
   if (h->ev_join) cudaEventDestroy(h->ev_join);
   if (h->ev_pool) cudaEventDestroy(h->ev_pool);
   if (h->side_stream) cudaStreamDestroy(h->side_stream);
+  if (h->ev_cdist) cudaEventDestroy(h->ev_cdist);
+  if (h->ev_stats) cudaEventDestroy(h->ev_stats);
+  if (h->stat_stream) cudaStreamDestroy(h->stat_stream);
   delete h;
   return LAPL_OK;
 }

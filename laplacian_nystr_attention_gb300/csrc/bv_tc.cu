@@ -547,7 +547,7 @@ int bv_tc_occupancy(size_t smem, bool bf16) {
 }
 
 cudaError_t launch_bv_tc(const lapl_attn_plan& p, const float* bt, const void* v, float* bvp,
-                         cudaStream_t st) {
+                         cudaStream_t st, bool pdl) {
   const Geometry& g = p.geo;
   const bool bf16 = p.cfg.in_dtype == LAPL_BF16;
   // B^T viewed as [BH m, N] fp32, boxes of 32 tokens x m rows; V as [BH N, d], boxes of d x 32.
@@ -575,7 +575,8 @@ cudaError_t launch_bv_tc(const lapl_attn_plan& p, const float* bt, const void* v
   const void* f = bf16 ? reinterpret_cast<const void*>(&bv_tc_kernel<true>)
                        : reinterpret_cast<const void*>(&bv_tc_kernel<false>);
   void* args[] = {&a, &p.tmap_bt, &p.tmap_v};
-  // A programmatic dependent of the statistics launch before it (see the kernel's end).
+  // A programmatic dependent of the statistics launch before it when that one precedes it on
+  // the stream (see the kernel's end); a plain launch when the statistics run beside it.
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -585,7 +586,7 @@ cudaError_t launch_bv_tc(const lapl_attn_plan& p, const float* bt, const void* v
   cfg.dynamicSmemBytes = g.bv_smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = p.cfg.whiten ? 1 : 0;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelExC(&cfg, f, args);
 }
 

@@ -537,7 +537,7 @@ cudaError_t launch_bv(const lapl_attn_plan& p, const float* bt, const void* v, f
       const cudaError_t e = launch_col_stats(p, at, mu, rstd, dbg_mu, dbg_rstd, st);
       if (e != cudaSuccess) return e;
     }
-    return launch_bv_tc(p, bt, v, bvp, st);
+    return launch_bv_tc(p, bt, v, bvp, st, g.stat_ctas > 0);
   }
   const long bv_ctas = g.bh * g.bv_splits, stat_ctas = g.stat_ctas;
   const unsigned grid = (unsigned)(bv_ctas + stat_ctas);

@@ -147,6 +147,8 @@ struct Geometry {
   bool bv_tc;              // B V on the tensor cores (bv_tc.cu), after a launch of the
                            // statistics CTAs alone (stat_ctas of stat_threads threads)
   int stat_threads;
+  bool stats_beside;       // the statistics launch runs on a stream of its own beside the
+                           // tensor-core B V (the distance chain on the launching stream)
   int bv_raw_stages;       // tensor-core B V: raw copy stages (as many as fit, <= 12)
   bool out_tc;             // O = A^ M on the tensor cores (out_tc.cu)
   bool out_tma;            // ... with its rows written by TMA tensor stores
@@ -186,6 +188,8 @@ struct lapl_attn_plan {
   float neg_log2e_over_lambda;  // exp(-D/lambda) == exp2(D * this)
   cudaStream_t side_stream;     // runs the shorter of the two chains of a forward
   cudaEvent_t ev_pool, ev_join;   // pooling done; side-stream chain done
+  cudaStream_t stat_stream;     // the column statistics beside the tensor-core B V
+  cudaEvent_t ev_cdist, ev_stats;   // distances done; statistics done
   bool timing;                  // record stage events in forward
   bool timed_once;              // a forward ran with timing on
   cudaEvent_t ev_stage[lapl::kMarks];   // indexed by lapl::Mark
@@ -283,8 +287,9 @@ int bv_tc_raw_stages(int d, bool bf16, size_t smem_limit);
 size_t bv_tc_smem_bytes(int d, bool bf16, int nraw);
 cudaError_t bv_tc_configure(size_t smem);
 int bv_tc_occupancy(size_t smem, bool bf16);
+// pdl: launched as the programmatic dependent of the statistics launch just before it.
 cudaError_t launch_bv_tc(const lapl_attn_plan& p, const float* bt, const void* v, float* bvp,
-                         cudaStream_t st);
+                         cudaStream_t st, bool pdl);
 // O = A^ M on the tensor cores (out_tc.cu); tma_store: O rows written by TMA tensor stores
 // (fp32 O with d = 32 or 64, bf16 O with d = 64: out_tc_tma_store).
 size_t out_tc_smem_bytes(int m, int d, bool tma_store, bool out_bf16);

@@ -99,3 +99,26 @@ def test_bv_choice(monkeypatch):
     assert choice(TINY.replace(head_dim=24)) == 0
     monkeypatch.setenv("LAPL_ATTN_BV", "cuda")
     assert choice(WORKLOADS["hires_bf16"]) == 0
+
+
+@pytest.mark.parametrize("debug", [False, True])
+def test_statistics_beside_bv_same_output(debug, monkeypatch):
+    """The column statistics on a stream of their own beside the tensor-core B V (forced on a
+    shape whose distance chain runs on the launching stream) give the same output and the same
+    statistics bit for bit as the statistics launched before B V, and match the oracle."""
+    import oracle
+    w = WORKLOADS["stage23_bf16"].replace(batch=12)        # 48 heads: the distance chain leads
+    q, k, v = make_inputs(w)
+    runs = {}
+    for mode in ("1", "0"):
+        monkeypatch.setenv("LAPL_ATTN_STATS_BESIDE", mode)
+        info = {}
+        runs[mode] = run_gpu(w, q, k, v, debug=debug, info=info)
+        assert info["bv_tensor_core"] == 1 and info["ns_exclusive"] == 0
+        assert info["device_errors"] == 0
+    (a, ga), (b, gb) = runs["1"], runs["0"]
+    assert np.array_equal(a, b)
+    if debug:
+        assert np.array_equal(ga["mu"], gb["mu"]) and np.array_equal(ga["rstd"], gb["rstd"])
+    ref, _ = oracle.forward(w.config(), q, k, v)
+    assert slice_rel_err(a, ref) < TOL_BF16
