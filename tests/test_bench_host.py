@@ -78,3 +78,19 @@ def test_dominant_kernel_entry():
     assert e["peak"] == 1000.0 and e["bound"] == "latency" and e["share_of_forward"] == 0.5
     assert bench.dominant_kernel_entry(w, {"newton_schulz": 0.05}, {}, {"ns_tensor_core": 0},
                                        0.1) is None
+
+
+def test_distance_traffic_taken_on_the_committed_sources():
+    """Every distance-kernel source the traffic hash covers exists, and each recorded DRAM
+    traffic figure was captured on exactly the sources in the tree (otherwise the bench reports
+    traffic as null and the figure must be re-taken with ncu)."""
+    import os
+    import bench
+    csrc = os.path.join(bench.ROOT, "laplacian_nystr_attention_gb300", "csrc")
+    for f in bench.CDIST_SOURCES:
+        assert os.path.isfile(os.path.join(csrc, f)), f
+    sha = bench.cdist_sources_sha()
+    assert sha == bench.cdist_sources_sha()                 # deterministic
+    for key, (nbytes, taken_on) in bench.CDIST_TRAFFIC.items():
+        assert nbytes > 0, key
+        assert taken_on == sha, key
