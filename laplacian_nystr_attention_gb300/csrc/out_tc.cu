@@ -49,6 +49,10 @@ constexpr unsigned kSboO = 144;                 // A^: padded stride between 8-r
 constexpr unsigned kLboA = 16 * kSboO;          // A^ operand: 128 rows
 constexpr unsigned kSboB = 128;                 // [M_hi; M_lo]: unpadded (written once per head)
 constexpr int kItems = 16 / kConvWarps;         // landmark quads per converter thread (m <= 64)
+// Whitening coefficients (mean, scale, bias) of each converter warp's 4 kItems landmarks.
+constexpr unsigned kCoefFloatsPerWarp = 3 * 4 * kItems;
+constexpr unsigned kCoefBytes = kConvWarps * kCoefFloatsPerWarp * 4;
+constexpr unsigned kBarBytes = 11 * 8;          // 11 mbarriers, then the tensor-memory slot
 
 __host__ __device__ inline int mk8(int m) { return (m + 7) & ~7; }
 __host__ __device__ inline unsigned a_part_bytes(int mk) { return (unsigned)(mk / 4) * kLboA; }
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
     ostage = smem_o + kCoefOff + ((1024u - (at & 1023u)) & 1023u);
     kCoefOff = (unsigned)(ostage - smem_o) + kOstageBytes;
   }
-  unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem_o + kCoefOff + 4 * 48 * 4);
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem_o + kCoefOff + kCoefBytes);
   const unsigned ofull0 = smem_u32(bars), oempty0 = ofull0 + 16, afull0 = oempty0 + 16,
                  aempty0 = afull0 + 16, done_bar = aempty0 + 16, rfull = done_bar + 8,
                  rempty = rfull + 8;
@@ -252,7 +256,7 @@ __global__ void __launch_bounds__(kOutTcThreads, 1)
     // free the stage (the copy of tile i + 1 starts) and convert tile i meanwhile.
     const int tid = threadIdx.x;
     // This warp's whitening coefficients: mean, scale, bias of its 4 kItems landmarks.
-    float* coef = reinterpret_cast<float*>(smem_o + kCoefOff) + warp * 12 * kItems;
+    float* coef = reinterpret_cast<float*>(smem_o + kCoefOff) + warp * kCoefFloatsPerWarp;
     long prev_bh = -1;
     bool waited = false;
     const unsigned tile_bytes = (unsigned)m * kTileT * 4;
@@ -557,7 +561,7 @@ size_t out_tc_smem_bytes(int m, int d, bool tma_store, bool out_bf16) {
   const int mk = mk8(m);
   (void)out_bf16;
   return (size_t)kStagesO * 2 * a_part_bytes(mk) + (size_t)align128(b_bytes(d, mk)) +
-         raw_bytes(m) + (tma_store ? 1024 + (size_t)kOstageBytes : 0) + 4 * 48 * 4 + 11 * 8 + 16;
+         raw_bytes(m) + (tma_store ? 1024 + (size_t)kOstageBytes : 0) + kCoefBytes + kBarBytes + 16;
 }
 
 bool out_tc_tma_store(int d, bool out_bf16) { return out_bf16 ? d == 64 : (d == 32 || d == 64); }
